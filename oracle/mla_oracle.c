@@ -1,0 +1,286 @@
+/* CPU oracle for MLA prefill attention.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the bench's
+ * cpu_baseline leg may load this file's library. It shares no code, header,
+ * table or constant with the CUDA library; it is the plain definition of what
+ * that library computes, written out in fp64 with no blocking, fusion or
+ * reordering, so that it can be checked against the source pages by eye.
+ *
+ * Sources (page title, section):
+ *  - "More throughput from fewer GPUs: profiling and fixing GLM-5.3 prefill
+ *    on NVIDIA B300", section System architecture: multi-head latent
+ *    attention keeps one latent vector per token, shared by all heads; the KV
+ *    cache is FP8. Section KV hand-off and caching: 256-token KV chunks.
+ *  - "GLM-5.3-Optimierungen, Teil 2: PCP, DCP und Hybrid HiSparse auf 16
+ *    H200s", section "Warum nicht TP oder DP?": all 64 heads read one latent
+ *    row; the indexer scores every earlier token and keeps 2,048. Section
+ *    Ausprobieren: sparse MLA runs as MQA, each KV row serving every head.
+ *    Footnote 1: QK runs over 576 dims and PV over 512. Footnote 3: indexer
+ *    keys are 128 FP8 values plus a 4-byte scale.
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *  - Weight-absorbed form: query row q (576 = 512 latent + 64 RoPE dims, RoPE
+ *    already applied) against key K_s = sigma_s * dec(c_s) (576 dims) and value
+ *    V_s = first 512 dims of K_s. The head's W_UV is applied outside.
+ *  - Causal with a cached prefix: new token i of a sequence with prefix P sits
+ *    at position p = P + i and attends to positions 0..p (itself included).
+ *  - FP8 is OCP e4m3fn; one fp32 scale per cached token.
+ *  - Indexer: score(t,s) = sigmaI_s * sum_h w_{t,h} * max(0, q_{t,h} . k_s),
+ *    s <= p; the selected set is the first min(topk, p+1) positions in the
+ *    order (score descending, position ascending).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORA_PAGE 256
+#define ORA_DQK 576
+#define ORA_DV 512
+#define ORA_DIDX 128
+
+static double e4m3_table[256];
+static int table_ready = 0;
+
+/* OCP e4m3fn from its bit fields: sign s (bit 7), exponent e (bits 6..3, bias
+ * 7), mantissa m (bits 2..0). e = 0 is subnormal: m/8 * 2^-6. e = 15, m = 7 is
+ * NaN. Everything else is (1 + m/8) * 2^(e - 7). There is no infinity. */
+static double e4m3_from_fields(unsigned code) {
+    unsigned s = (code >> 7) & 1u, e = (code >> 3) & 15u, m = code & 7u;
+    double mag;
+    if (e == 15u && m == 7u) return NAN;
+    if (e == 0u)
+        mag = ldexp((double)m / 8.0, -6);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+    return s ? -mag : mag;
+}
+
+static void ora_init(void) {
+    if (table_ready) return;
+    for (unsigned c = 0; c < 256; ++c) e4m3_table[c] = e4m3_from_fields(c);
+    table_ready = 1;
+}
+
+double ora_e4m3(uint8_t code) {
+    ora_init();
+    return e4m3_table[code];
+}
+
+/* bfloat16: the IEEE binary32 value whose upper 16 bits are b. */
+double ora_bf16(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+void ora_bf16_to_f64(const uint16_t *b, int64_t n, double *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = ora_bf16(b[i]);
+}
+
+/* Sequence b and in-sequence index i of global new-token t; -1 if out of range. */
+static int locate(int32_t batch, const int32_t *cu, int64_t t, int64_t *i_out) {
+    for (int b = 0; b < batch; ++b)
+        if (t >= cu[b] && t < cu[b + 1]) {
+            *i_out = t - cu[b];
+            return b;
+        }
+    return -1;
+}
+
+/* Physical row (page*256 + slot) of position s of sequence b; -1 if unmapped. */
+static int64_t cache_row(const int32_t *bt, int32_t max_blocks, int32_t num_blocks, int b, int64_t s) {
+    int64_t blk = s / ORA_PAGE;
+    if (blk >= max_blocks) return -1;
+    int32_t page = bt[(int64_t)b * max_blocks + blk];
+    if (page < 0 || page >= num_blocks) return -1;
+    return (int64_t)page * ORA_PAGE + s % ORA_PAGE;
+}
+
+/* Softmax attention of one query row over a list of key positions.
+ * logit_s = sm_scale * sum_d q[d] * K_s[d],   K_s[d] = sigma_s * dec(c_s[d]);
+ * m = max logit; w_s = exp(logit_s - m); out = sum w_s V_s / sum w_s with
+ * V_s = K_s[0..511]; lse = m + ln(sum w_s). Keys with pos < 0 are skipped.
+ * Returns 0, or -1 if a position is unmapped. With no keys: out = 0, lse = -inf. */
+static int attend_row(const double *q, const int64_t *pos, int64_t n, int b,
+                      const int32_t *bt, int32_t max_blocks, int32_t num_blocks,
+                      const uint8_t *kv, const float *kv_scale, double sm_scale,
+                      double *out, double *lse, double *logit) {
+    int64_t valid = 0;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+        if (pos[j] < 0) continue;
+        int64_t r = cache_row(bt, max_blocks, num_blocks, b, pos[j]);
+        if (r < 0) return -1;
+        const uint8_t *c = kv + r * ORA_DQK;
+        double sigma = (double)kv_scale[r];
+        double dot = 0.0;
+        for (int d = 0; d < ORA_DQK; ++d) dot += q[d] * (sigma * e4m3_table[c[d]]);
+        logit[j] = sm_scale * dot;
+        if (logit[j] > m) m = logit[j];
+        ++valid;
+    }
+    for (int d = 0; d < ORA_DV; ++d) out[d] = 0.0;
+    if (valid == 0) {
+        *lse = -INFINITY;
+        return 0;
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        if (pos[j] < 0) continue;
+        int64_t r = cache_row(bt, max_blocks, num_blocks, b, pos[j]);
+        const uint8_t *c = kv + r * ORA_DQK;
+        double sigma = (double)kv_scale[r];
+        double w = exp(logit[j] - m);
+        l += w;
+        for (int d = 0; d < ORA_DV; ++d) out[d] += w * (sigma * e4m3_table[c[d]]);
+    }
+    for (int d = 0; d < ORA_DV; ++d) out[d] /= l;
+    *lse = m + log(l);
+    return 0;
+}
+
+/* Dense causal MLA prefill for n_sel selected new tokens.
+ * q: fp64 [n_sel, H, 576] (the selected tokens' query rows); tokens: global
+ * new-token indices into cu_seqlens_q. out: [n_sel, H, 512]; lse: [n_sel, H].
+ * Returns 0, or a negative count of failed rows. */
+int ora_mla_dense(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *prefix_lens,
+                  const int32_t *block_table, int32_t max_blocks, int32_t num_blocks,
+                  const double *q, const int64_t *tokens, int64_t n_sel, int32_t H,
+                  const uint8_t *kv, const float *kv_scale, double sm_scale,
+                  double *out, double *lse) {
+    ora_init();
+    int64_t fails = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : fails)
+    for (int64_t rh = 0; rh < n_sel * H; ++rh) {
+        int64_t sel = rh / H, h = rh % H, i;
+        int b = locate(batch, cu_seqlens_q, tokens[sel], &i);
+        if (b < 0) {
+            ++fails;
+            continue;
+        }
+        int64_t p = (int64_t)prefix_lens[b] + i;      /* absolute position of the query */
+        int64_t n = p + 1;                            /* keys 0..p */
+        int64_t *pos = (int64_t *)malloc((size_t)n * sizeof(int64_t));
+        double *logit = (double *)malloc((size_t)n * sizeof(double));
+        for (int64_t s = 0; s < n; ++s) pos[s] = s;
+        if (attend_row(q + rh * ORA_DQK, pos, n, b, block_table, max_blocks, num_blocks, kv, kv_scale,
+                       sm_scale, out + rh * ORA_DV, lse + rh, logit) != 0)
+            ++fails;
+        free(pos);
+        free(logit);
+    }
+    return fails ? (int)-fails : 0;
+}
+
+/* Sparse MLA: as dense, but query token sel attends only to the positions
+ * idx[sel*topk .. +topk] (entries < 0 are padding). The causal limit is not
+ * re-applied: the index list is the whole key set. */
+int ora_mla_sparse(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *prefix_lens,
+                   const int32_t *block_table, int32_t max_blocks, int32_t num_blocks,
+                   const double *q, const int64_t *tokens, int64_t n_sel, int32_t H,
+                   const uint8_t *kv, const float *kv_scale, double sm_scale,
+                   const int32_t *idx, int32_t topk, double *out, double *lse) {
+    ora_init();
+    (void)prefix_lens;
+    int64_t fails = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : fails)
+    for (int64_t rh = 0; rh < n_sel * H; ++rh) {
+        int64_t sel = rh / H, i;
+        int b = locate(batch, cu_seqlens_q, tokens[sel], &i);
+        if (b < 0) {
+            ++fails;
+            continue;
+        }
+        int64_t *pos = (int64_t *)malloc((size_t)topk * sizeof(int64_t));
+        double *logit = (double *)malloc((size_t)topk * sizeof(double));
+        for (int64_t j = 0; j < topk; ++j) pos[j] = idx[sel * topk + j];
+        if (attend_row(q + rh * ORA_DQK, pos, topk, b, block_table, max_blocks, num_blocks, kv, kv_scale,
+                       sm_scale, out + rh * ORA_DV, lse + rh, logit) != 0)
+            ++fails;
+        free(pos);
+        free(logit);
+    }
+    return fails ? (int)-fails : 0;
+}
+
+typedef struct {
+    double score;
+    int64_t pos;
+} ora_cand;
+
+/* (score descending, position ascending) */
+static int cand_cmp(const void *a, const void *b) {
+    const ora_cand *x = (const ora_cand *)a, *y = (const ora_cand *)b;
+    if (x->score > y->score) return -1;
+    if (x->score < y->score) return 1;
+    return (x->pos > y->pos) - (x->pos < y->pos);
+}
+
+static int cmp_i32(const void *a, const void *b) {
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+/* Indexer + top-k for n_sel selected new tokens.
+ * qi: e4m3 [n_sel, 64, 128]; w: f32, row sel at w + sel*w_stride (64 values;
+ * stride 0 shares one row); ki: e4m3 [num_blocks, 256, 128]; ki_scale: f32
+ * [num_blocks, 256]. idx_out: [n_sel, topk] selected positions in ascending
+ * order, -1 padded. scores_out (optional, may be NULL): [n_sel, ctx_cap],
+ * score of position s at [sel*ctx_cap + s] for s <= p (others untouched). */
+int ora_indexer_topk(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *prefix_lens,
+                     const int32_t *block_table, int32_t max_blocks, int32_t num_blocks,
+                     const uint8_t *qi, const float *w, int64_t w_stride,
+                     const int64_t *tokens, int64_t n_sel,
+                     const uint8_t *ki, const float *ki_scale, int32_t topk,
+                     int32_t *idx_out, double *scores_out, int64_t ctx_cap) {
+    ora_init();
+    int64_t fails = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : fails)
+    for (int64_t sel = 0; sel < n_sel; ++sel) {
+        int64_t i;
+        int b = locate(batch, cu_seqlens_q, tokens[sel], &i);
+        int32_t *dst = idx_out + sel * topk;
+        for (int32_t j = 0; j < topk; ++j) dst[j] = -1;
+        if (b < 0) {
+            ++fails;
+            continue;
+        }
+        int64_t p = (int64_t)prefix_lens[b] + i;
+        int64_t n = p + 1;
+        ora_cand *c = (ora_cand *)malloc((size_t)n * sizeof(ora_cand));
+        const uint8_t *qrow = qi + sel * 64 * ORA_DIDX;
+        const float *wrow = w + sel * w_stride;
+        int bad = 0;
+        for (int64_t s = 0; s < n; ++s) {
+            int64_t r = cache_row(block_table, max_blocks, num_blocks, b, s);
+            if (r < 0) {
+                bad = 1;
+                break;
+            }
+            const uint8_t *k = ki + r * ORA_DIDX;
+            double e = 0.0;
+            for (int h = 0; h < 64; ++h) {
+                double dot = 0.0;
+                for (int d = 0; d < ORA_DIDX; ++d)
+                    dot += e4m3_table[qrow[h * ORA_DIDX + d]] * e4m3_table[k[d]];
+                e += (double)wrow[h] * (dot > 0.0 ? dot : 0.0);
+            }
+            c[s].score = (double)ki_scale[r] * e;
+            c[s].pos = s;
+            if (scores_out && s < ctx_cap) scores_out[sel * ctx_cap + s] = c[s].score;
+        }
+        if (bad) {
+            ++fails;
+            free(c);
+            continue;
+        }
+        qsort(c, (size_t)n, sizeof(ora_cand), cand_cmp);
+        int64_t keep = n < topk ? n : topk;
+        for (int64_t j = 0; j < keep; ++j) dst[j] = (int32_t)c[j].pos;
+        qsort(dst, (size_t)keep, sizeof(int32_t), cmp_i32);
+        free(c);
+    }
+    return fails ? (int)-fails : 0;
+}
