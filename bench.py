@@ -1,0 +1,405 @@
+#!/usr/bin/env python3
+"""Benchmark of the MLA prefill hot path on one GB300 (or N replicas).
+
+Metric: prefill query tokens per second per layer (one attention call over
+all new tokens of the workload), with attention TFLOP/s and the fraction of
+the measured tensor-core peak. Default workload: dense causal MLA prefill of
+one 32,768-token prompt, 64 heads (the 16-chunk balanced pairing).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun each rank runs its own replica of the workload (no data-path
+collective: the query rows of different prompts are independent); rank 0
+prints one JSON line with the whole-job throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA prefill query tok/s per layer at 32k ctx"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mla_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.remove(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+def host_dense(w):
+    from mla_prefill_attention_gb300 import inputs as I
+    ps = w.seqs()
+    q = I.gen_q_bf16(w.seed, ps.total_q, w.heads)
+    kv, ks = I.gen_latent_cache(w.seed, ps)
+    return ps, q, kv, ks
+
+
+class DenseRun:
+    """One step = one mla_prefill_dense call over every new token."""
+    launches_per_step = 1
+
+    def __init__(self, w, dev):
+        import torch
+        from mla_prefill_attention_gb300 import MLA_OP_DENSE, Seqs, mla_workspace_size
+        from mla_prefill_attention_gb300 import flops as F
+        self.w = w
+        self.ps, q, kv, ks = host_dense(w)
+        self.host = {"q": q, "kv": kv, "ks": ks}
+        self.seqs = Seqs.from_paged(self.ps, device=dev)
+        self.q = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).to(dev)
+        self.kv = torch.from_numpy(kv).to(dev)
+        self.ks = torch.from_numpy(ks).to(dev)
+        T, H = self.ps.total_q, w.heads
+        self.out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(max(16, mla_workspace_size(MLA_OP_DENSE, self.seqs, H)), dtype=torch.uint8, device=dev)
+        self.tokens = T
+        self.flops = F.dense_flops(w.q_lens, w.prefix_lens, H)
+        self.min_bytes = F.dense_min_bytes(T, H, sum(self.ps.seq_len(b) for b in range(self.ps.batch)))
+
+    def step(self):
+        from mla_prefill_attention_gb300 import mla_prefill_dense
+        mla_prefill_dense(self.seqs, self.q, self.kv, self.ks, self.w.sm_scale, out=self.out, lse=self.lse,
+                          workspace=self.ws)
+
+    def e2e(self, steps, warmup):
+        """Same call with inputs in pinned host memory, copies inside the timed region."""
+        import torch
+        from mla_prefill_attention_gb300 import mla_prefill_dense
+        hq = torch.from_numpy(self.host["q"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        hkv = torch.from_numpy(self.host["kv"]).pin_memory()
+        hks = torch.from_numpy(self.host["ks"]).pin_memory()
+        hout = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
+        hlse = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+
+        def one():
+            self.q.copy_(hq, non_blocking=True)
+            self.kv.copy_(hkv, non_blocking=True)
+            self.ks.copy_(hks, non_blocking=True)
+            mla_prefill_dense(self.seqs, self.q, self.kv, self.ks, self.w.sm_scale, out=self.out, lse=self.lse,
+                              workspace=self.ws)
+            hout.copy_(self.out, non_blocking=True)
+            hlse.copy_(self.lse, non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            one()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        h2d = hq.numel() * 2 + hkv.numel() + hks.numel() * 4
+        d2h = hout.numel() * 2 + hlse.numel() * 4
+        return ms, h2d, d2h
+
+    def oracle_rate(self, budget_s: float, seed: int = 0):
+        """Oracle (fp64 CPU) on a bounded sample of query tokens, all heads:
+        returns (sampled tokens, seconds, sampled algorithmic FLOPs)."""
+        from oracle import oracle as O
+        from mla_prefill_attention_gb300 import flops as F
+        ps, h = self.ps, self.host
+        T = ps.total_q
+        rng = np.random.default_rng(seed)
+
+        def flops_of(toks):
+            tot = 0
+            for t in toks:
+                b = int(np.searchsorted(ps.cu_seqlens_q, t, side="right") - 1)
+                pos = int(ps.prefix_lens[b]) + int(t) - int(ps.cu_seqlens_q[b])
+                tot += (pos + 1) * self.w.heads * F.FLOPS_PER_PAIR_HEAD
+            return tot
+
+        probe = np.array([rng.integers(0, T)])
+        t0 = time.perf_counter()
+        O.mla_dense(ps, h["q"][probe], probe, h["kv"], h["ks"], self.w.sm_scale)
+        dt = max(time.perf_counter() - t0, 1e-3)
+        rate = flops_of(probe) / dt
+        n = 1
+        while n < T and flops_of(rng.integers(0, T, n * 2)) / rate < budget_s:
+            n *= 2
+        toks = np.sort(rng.integers(0, T, n))
+        t0 = time.perf_counter()
+        O.mla_dense(ps, h["q"][toks], toks, h["kv"], h["ks"], self.w.sm_scale)
+        dt = time.perf_counter() - t0
+        return len(toks), dt, flops_of(toks)
+
+
+class SparseRun:
+    """One step = mla_indexer_topk + mla_prefill_sparse over every new token."""
+    launches_per_step = 3
+
+    def __init__(self, w, dev):
+        import torch
+        from mla_prefill_attention_gb300 import MLA_OP_INDEXER, Seqs, inputs as I, mla_workspace_size
+        from mla_prefill_attention_gb300 import flops as F
+        self.w = w
+        self.ps = w.seqs()
+        q = I.gen_q_bf16(w.seed, self.ps.total_q, w.heads)
+        kv, ks = I.gen_latent_cache(w.seed, self.ps)
+        qi, wh, ki, kis = I.gen_indexer_inputs(w.seed, self.ps)
+        self.host = dict(q=q, kv=kv, ks=ks, qi=qi, w=wh, ki=ki, kis=kis)
+        self.seqs = Seqs.from_paged(self.ps, device=dev)
+        self.d = {k: torch.from_numpy(v).to(dev) for k, v in self.host.items() if k != "q"}
+        self.d["q"] = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).to(dev)
+        T, H = self.ps.total_q, w.heads
+        self.out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((T, w.topk), dtype=torch.int32, device=dev)
+        self.ws = torch.empty(mla_workspace_size(MLA_OP_INDEXER, self.seqs, 64, w.topk), dtype=torch.uint8,
+                              device=dev)
+        self.tokens = T
+        self.flops = F.sparse_flops(w.q_lens, w.prefix_lens, H, w.topk) + F.indexer_flops(w.q_lens, w.prefix_lens)
+        self.min_bytes = None
+
+    def step(self):
+        from mla_prefill_attention_gb300 import mla_indexer_topk, mla_prefill_sparse
+        d = self.d
+        mla_indexer_topk(self.seqs, d["qi"], d["w"], 0, d["ki"], d["kis"], self.w.topk, idx_out=self.idx,
+                         workspace=self.ws)
+        mla_prefill_sparse(self.seqs, d["q"], d["kv"], d["ks"], self.w.sm_scale, self.idx, out=self.out, lse=self.lse)
+
+    def e2e(self, steps, warmup):
+        return None
+
+    def oracle_rate(self, budget_s, seed=0):
+        from oracle import oracle as O
+        h, ps = self.host, self.ps
+        rng = np.random.default_rng(seed)
+        n = 1
+        t_total, done, fl = 0.0, 0, 0
+        while t_total < budget_s and done < ps.total_q:
+            toks = np.sort(rng.integers(0, ps.total_q, n))
+            t0 = time.perf_counter()
+            idx = O.indexer_topk(ps, h["qi"][toks], h["w"], 0, toks, h["ki"], h["kis"], self.w.topk)
+            O.mla_sparse(ps, h["q"][toks], toks, h["kv"], h["ks"], self.w.sm_scale, idx)
+            t_total += time.perf_counter() - t0
+            done += n
+            n *= 2
+        return done, t_total, done * (self.flops / ps.total_q)
+
+
+RUNS = {"tiny512": DenseRun, "prefix12k": DenseRun, "dense32k": DenseRun, "ragged4": DenseRun,
+        "sparse64k": SparseRun}
+
+
+def time_steps(run, steps, warmup):
+    import torch
+    for _ in range(warmup):
+        run.step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    per = []
+    e0.record()
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run.step()
+        b.record()
+        per.append((a, b))
+    e1.record()
+    torch.cuda.synchronize()
+    total_ms = e0.elapsed_time(e1)
+    per_ms = [a.elapsed_time(b) for a, b in per]
+    return total_ms, per_ms
+
+
+def config_of(w):
+    c = {"workload": w.name, "batch": len(w.q_lens), "q_lens": w.q_lens, "prefix_lens": w.prefix_lens,
+         "heads": w.heads, "d_qk": 576, "d_v": 512, "page": 256, "q_dtype": "bf16",
+         "kv_dtype": "e4m3 + fp32 per-token scale", "sm_scale": "1/sqrt(192)", "parallelism": "replicas",
+         "l2": "inputs larger than L2 (no flush needed)" if w.name in ("dense32k", "ragged4", "sparse64k",
+                                                                       "prefix12k") else "small inputs"}
+    if w.sparse:
+        c.update(topk=w.topk, indexer="64 heads x 128, e4m3")
+    return c
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="dense32k", choices=sorted(RUNS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    from mla_prefill_attention_gb300 import inputs as I
+    w = I.WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+    if args.impl == "reference":
+        # the reference arm is the fp64 CPU oracle, on rank 0 only
+        if rank != 0:
+            return
+        import __graft_entry__
+        from oracle import oracle as O
+        O.build()
+        run = RUNS[args.workload].__new__(RUNS[args.workload])
+        run.w = w
+        if RUNS[args.workload] is DenseRun:
+            run.ps, q, kv, ks = host_dense(w)
+            run.host = {"q": q, "kv": kv, "ks": ks}
+        else:
+            raise SystemExit(json.dumps({"impl": "reference", "unavailable": "reference arm implemented for dense workloads"}))
+        from mla_prefill_attention_gb300 import flops as F
+        total_flops = F.dense_flops(w.q_lens, w.prefix_lens, w.heads)
+        budget = max(2.0, 120.0 / max(1, args.steps + args.warmup))
+        rates = []
+        for i in range(args.warmup + args.steps):
+            n, dt, fl = run.oracle_rate(budget, seed=i)
+            if i >= args.warmup:
+                rates.append(w_tokens := run.ps.total_q / (dt * total_flops / fl))
+        val = statistics.median(rates)
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tok/s", "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * run.ps.total_q / val,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config_of(w),
+                "cpu_baseline": {"value": val, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                                 "sample": f"{n} random query tokens x {w.heads} heads per step, extrapolated by "
+                                           f"algorithmic FLOPs to all {run.ps.total_q} tokens"},
+                "e2e": {"value": val, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    run = RUNS[args.workload](w, dev)
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index if world == 1 else local)
+    clocks.start()
+    total_ms, per_ms = time_steps(run, args.steps, args.warmup)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+
+    ms_per_step = total_ms / args.steps
+    value = world * run.tokens * args.steps / (total_ms / 1000.0)
+    kern_ms = statistics.mean(per_ms)
+    tflops = run.flops / (kern_ms / 1000.0) / 1e12
+    pk, src = peaks()
+    peak = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
+    line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": config_of(w),
+            "attention_tflops": tflops,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "traffic": None,
+                         "peak_source": f"{src} bf16 sustained (f16 and bf16 share the dense tensor rate)",
+                         "kernel": "mla dense (mma.sync f16 path)" if isinstance(run, DenseRun)
+                         else "indexer + top-k + sparse"},
+            "gpu_launches": run.launches_per_step * args.steps}
+    if clk:
+        line["clocks"] = clk
+    if rank == 0 and not args.no_e2e:
+        r = run.e2e(args.steps, args.warmup)
+        if r:
+            ms, h2d, d2h = r
+            line["e2e"] = {"value": world * run.tokens / (ms / 1000.0), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+                           "d2h_bytes_per_step": d2h}
+    if rank == 0 and not args.no_cpu_baseline:
+        n, dt, fl = run.oracle_rate(args.cpu_budget)
+        val = run.tokens / (dt * run.flops / fl)
+        line["cpu_baseline"] = {"value": val, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{n} random query tokens x all heads of the {w.name} workload "
+                                          f"({dt:.1f} s), extrapolated by algorithmic FLOPs"}
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

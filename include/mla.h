@@ -1,0 +1,145 @@
+/*
+ * mla.h - C ABI of the GB300 (sm_103a) MLA prefill attention library.
+ *
+ * What it computes. Causal prefill attention for DeepSeek-style multi-head
+ * latent attention (MLA) in weight-absorbed form, as served for GLM-5.3 on the
+ * pages "More throughput from fewer GPUs: profiling and fixing GLM-5.3
+ * prefill on NVIDIA B300" (section System architecture: one latent vector per
+ * token shared by all heads; FP8 KV cache) and "GLM-5.3-Optimierungen, Teil 2:
+ * PCP, DCP und Hybrid HiSparse auf 16 H200s" (section "Warum nicht TP oder
+ * DP?": 64 heads share the latent row, an indexer scores every earlier token
+ * and keeps 2,048; section Ausprobieren: sparse MLA runs as MQA; footnote 1:
+ * QK over 576 dims, PV over 512; footnote 3: indexer keys are 128 FP8 values
+ * and a 4-byte scale).
+ *
+ * Data layout (all row-major, all device memory unless named *_host):
+ *   query rows     q       bf16  [Tq, H, 576]   dims 0..511 latent, 512..575 RoPE
+ *                                                (RoPE already applied)
+ *   latent cache   kv      e4m3  [num_blocks, 256, 576]   one row per token
+ *   cache scales   kv_scale f32  [num_blocks, 256]        K_s = kv_scale_s * dec(kv_s)
+ *   output         out     bf16  [Tq, H, 512]
+ *   log-sum-exp    lse     f32   [Tq, H]   natural log, optional (NULL = skip)
+ *   indexer q      qi      e4m3  [Tq, 64, 128]
+ *   indexer w      w       f32   row t at w + t*w_token_stride (64 values)
+ *   indexer keys   ki      e4m3  [num_blocks, 256, 128]
+ *   indexer scale  ki_scale f32  [num_blocks, 256]
+ *   top-k indices  idx     int32 [Tq, topk]  positions within the sequence,
+ *                                            ascending, -1 padding at the end
+ * Position s of sequence b lives at page block_table[b*max_blocks_per_seq +
+ * s/256], slot s%256. New token i of sequence b is at position prefix_lens[b]
+ * + i and attends to positions 0..prefix_lens[b]+i (itself included); its
+ * cache row must already be written.
+ *
+ * Ownership. The caller owns every buffer, workspace included. The library
+ * allocates no device or host memory, never synchronises, and enqueues all
+ * work asynchronously on the given stream. Host mirrors (cu_seqlens_q_host,
+ * prefix_lens_host) are read during the call only.
+ *
+ * Errors. Arguments are validated on the host before any launch; a failing
+ * check returns a status and launches nothing. mla_last_error() then returns
+ * a message (thread-local, valid until the thread's next call). Data that only
+ * the device sees (a page id outside [0, num_blocks), a sparse index outside
+ * [-1, position]) never traps: the kernel skips the offending key and ORs a
+ * MLA_DEVERR_* bit into *dev_err (if dev_err is not NULL); the caller reads it
+ * after synchronising. A kernel launch failure returns MLA_ERR_CUDA.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or shape */
+    MLA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. H not in {16,32,64,128}) */
+    MLA_ERR_CUDA = 3,          /* a CUDA call or kernel launch failed */
+    MLA_ERR_WORKSPACE = 4      /* workspace NULL or smaller than mla_workspace_size() */
+} mla_status_t;
+
+/* Bits ORed into *dev_err by the kernels. */
+#define MLA_DEVERR_BAD_PAGE 1   /* block table entry outside [0, num_blocks) */
+#define MLA_DEVERR_BAD_INDEX 2  /* sparse index outside [-1, position of the query] */
+#define MLA_DEVERR_INTERNAL 8   /* a kernel invariant failed (a library bug); the row is -1 filled */
+
+typedef enum {
+    MLA_OP_DENSE = 0,
+    MLA_OP_INDEXER = 1,
+    MLA_OP_SPARSE = 2
+} mla_op_t;
+
+/* Ragged batch of sequences over one paged cache (256-token pages). */
+typedef struct {
+    int32_t batch;                      /* B >= 1 */
+    const int32_t *cu_seqlens_q;        /* device [B+1], cu[0] = 0, non-decreasing */
+    const int32_t *cu_seqlens_q_host;   /* host mirror of cu_seqlens_q */
+    const int32_t *prefix_lens;         /* device [B], cached tokens before the new ones */
+    const int32_t *prefix_lens_host;    /* host mirror of prefix_lens */
+    const int32_t *block_table;         /* device [B, max_blocks_per_seq] page ids */
+    int32_t max_blocks_per_seq;         /* >= ceil((prefix+new)/256) for every sequence */
+    int32_t num_blocks;                 /* pages in the cache */
+} mla_seqs_t;
+
+/* Bytes of workspace the op needs for this batch (0 means none is needed and
+ * workspace may be NULL). Returns 0 on invalid arguments as well; the op call
+ * itself reports those. */
+size_t mla_workspace_size(mla_op_t op, const mla_seqs_t *seqs, int32_t num_heads, int32_t topk);
+
+/* Dense causal MLA prefill, weight-absorbed (MQA over the shared latent row).
+ * For each new token t (position p) and head h:
+ *   logit_s = sm_scale * sum_{d<576} q[t,h,d] * kv_scale_s * dec(kv_s[d]),  s = 0..p
+ *   out[t,h,:] = sum_s softmax(logit)_s * kv_scale_s * dec(kv_s[0:512])
+ *   lse[t,h]   = ln sum_s exp(logit_s)
+ * (More throughput from fewer GPUs, section System architecture; GLM-5.3
+ * Teil 2, footnote 1.) Work is scheduled by pairing query tile i with tile
+ * n-1-i of the same sequence, the load-balanced chunk pairing of GLM-5.3 Teil
+ * 2, section "PCP: teile die Token, nicht die Köpfe", applied across CTAs.
+ * num_heads in {16, 32, 64, 128}. Pointers: q, out 16-byte aligned; kv
+ * 16-byte aligned. workspace: mla_workspace_size(MLA_OP_DENSE, ...) bytes,
+ * 16-byte aligned. */
+mla_status_t mla_prefill_dense(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads,
+                               const uint8_t *kv_e4m3, const float *kv_scale, float sm_scale,
+                               void *out_bf16, float *lse, void *workspace, size_t workspace_bytes,
+                               int32_t *dev_err, cudaStream_t stream);
+
+/* Indexer score and top-k selection (GLM-5.3 Teil 2, section "Warum nicht TP
+ * oder DP?": score every earlier token, keep 2,048; footnote 3: 128 FP8 values
+ * and a 4-byte scale per key). For new token t at position p:
+ *   score(t,s) = ki_scale_s * sum_{h<64} w[t,h] * max(0, sum_{d<128} dec(qi[t,h,d]) * dec(ki_s[d]))
+ * for s = 0..p; idx[t,:] = the min(topk, p+1) positions with the largest
+ * scores, ties going to the lower position, written in ascending position
+ * order and padded with -1. Scores are accumulated in fp32 (exact when q and
+ * k hold small integers). w_token_stride 0 shares one 64-value row among all
+ * tokens. topk in [1, 2048]. qi, ki 16-byte aligned. workspace:
+ * mla_workspace_size(MLA_OP_INDEXER, ...) bytes (fp32 scores of every
+ * visible (token, position) pair plus scheduling data). */
+mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, const float *w,
+                              int64_t w_token_stride, const uint8_t *ki_e4m3, const float *ki_scale,
+                              int32_t topk, int32_t *idx_out, void *workspace, size_t workspace_bytes,
+                              int32_t *dev_err, cudaStream_t stream);
+
+/* Sparse MLA over selected rows, run as MQA: every gathered latent row serves
+ * all heads (GLM-5.3 Teil 2, section Ausprobieren; footnote 1). As
+ * mla_prefill_dense, but token t attends only to the positions idx[t, 0..topk)
+ * (entries -1 are skipped; an index above the token's position or below -1
+ * sets MLA_DEVERR_BAD_INDEX and is skipped). A row whose list holds no valid
+ * index gets out = 0 and lse = -inf. topk in [1, 2048]. */
+mla_status_t mla_prefill_sparse(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads,
+                                const uint8_t *kv_e4m3, const float *kv_scale, float sm_scale,
+                                const int32_t *idx, int32_t topk, void *out_bf16, float *lse,
+                                void *workspace, size_t workspace_bytes, int32_t *dev_err,
+                                cudaStream_t stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char *mla_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

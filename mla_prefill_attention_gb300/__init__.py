@@ -1,0 +1,21 @@
+"""GB300 (sm_103a) MLA prefill attention: dense, indexer top-k and sparse.
+
+The compute path is the CUDA library ``libmla.so`` (C ABI in include/mla.h);
+``binding`` marshals PyTorch tensors into it. Nothing here falls back to a
+CPU or PyTorch implementation.
+"""
+from .binding import (  # noqa: F401
+    MLA_DEVERR_BAD_INDEX,
+    MLA_DEVERR_BAD_PAGE,
+    MLA_OP_DENSE,
+    MLA_OP_INDEXER,
+    MLA_OP_SPARSE,
+    MlaError,
+    Seqs,
+    chunk_bounds,
+    chunked_prefill_sparse,
+    mla_indexer_topk,
+    mla_prefill_dense,
+    mla_prefill_sparse,
+    mla_workspace_size,
+)

@@ -1,0 +1,191 @@
+"""Thin Python binding of ``libmla.so`` (the C ABI declared in include/mla.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library. PyTorch supplies device memory and the current stream. If the
+library is missing or fails to load, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmla.so")
+
+MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_WORKSPACE = range(5)
+MLA_DEVERR_BAD_PAGE, MLA_DEVERR_BAD_INDEX, MLA_DEVERR_INTERNAL = 1, 2, 8
+MLA_OP_DENSE, MLA_OP_INDEXER, MLA_OP_SPARSE = 0, 1, 2
+
+EXPORTS = ("mla_workspace_size", "mla_prefill_dense", "mla_indexer_topk", "mla_prefill_sparse", "mla_last_error")
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"status {status}: {msg}")
+        self.status = status
+
+
+class mla_seqs_t(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("cu_seqlens_q", ctypes.c_void_p),
+        ("cu_seqlens_q_host", ctypes.c_void_p),
+        ("prefix_lens", ctypes.c_void_p),
+        ("prefix_lens_host", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p),
+        ("max_blocks_per_seq", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libmla.so (raises if it is absent: build it with build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise FileNotFoundError(f"{path} not built; run mla_prefill_attention_gb300.build.build()")
+    L = ctypes.CDLL(path)
+    vp, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    L.mla_workspace_size.restype = sz
+    L.mla_workspace_size.argtypes = [ctypes.c_int, ctypes.POINTER(mla_seqs_t), i32, i32]
+    L.mla_prefill_dense.restype = ctypes.c_int
+    L.mla_prefill_dense.argtypes = [ctypes.POINTER(mla_seqs_t), vp, i32, vp, vp, f32, vp, vp, vp, sz, vp, vp]
+    L.mla_indexer_topk.restype = ctypes.c_int
+    L.mla_indexer_topk.argtypes = [ctypes.POINTER(mla_seqs_t), vp, vp, i64, vp, vp, i32, vp, vp, sz, vp, vp]
+    L.mla_prefill_sparse.restype = ctypes.c_int
+    L.mla_prefill_sparse.argtypes = [ctypes.POINTER(mla_seqs_t), vp, i32, vp, vp, f32, vp, i32, vp, vp, vp, sz,
+                                     vp, vp]
+    L.mla_last_error.restype = ctypes.c_char_p
+    L.mla_last_error.argtypes = []
+    _lib = L
+    return L
+
+
+def _check(status: int):
+    if status != MLA_OK:
+        raise MlaError(status, load().mla_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+class Seqs:
+    """Ragged batch over a paged cache: device tensors plus pinned host mirrors."""
+
+    def __init__(self, cu_seqlens_q, prefix_lens, block_table, num_blocks: int, device="cuda"):
+        self.cu_host = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
+        self.prefix_host = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        self.cu = torch.from_numpy(self.cu_host).to(device)
+        self.prefix = torch.from_numpy(self.prefix_host).to(device)
+        self.block_table = torch.from_numpy(bt).to(device)
+        self.num_blocks = int(num_blocks)
+        self.batch = int(self.prefix_host.shape[0])
+        self.total_q = int(self.cu_host[-1])
+        self.max_blocks = int(bt.shape[1])
+
+    @classmethod
+    def from_paged(cls, ps, device="cuda"):
+        return cls(ps.cu_seqlens_q, ps.prefix_lens, ps.block_table, ps.num_blocks, device)
+
+    def c(self) -> mla_seqs_t:
+        return mla_seqs_t(self.batch, self.cu.data_ptr(), self.cu_host.ctypes.data, self.prefix.data_ptr(),
+                          self.prefix_host.ctypes.data, self.block_table.data_ptr(), self.max_blocks,
+                          self.num_blocks)
+
+
+def mla_workspace_size(op: int, seqs: Seqs, num_heads: int = 64, topk: int = 2048) -> int:
+    c = seqs.c()
+    return int(load().mla_workspace_size(op, ctypes.byref(c), num_heads, topk))
+
+
+def _workspace(op, seqs, num_heads, topk, workspace):
+    n = mla_workspace_size(op, seqs, num_heads, topk)
+    if workspace is None and n > 0:
+        workspace = torch.empty(n, dtype=torch.uint8, device=seqs.cu.device)
+    return workspace, (0 if workspace is None else workspace.numel() * workspace.element_size())
+
+
+def mla_prefill_dense(seqs: Seqs, q: torch.Tensor, kv: torch.Tensor, kv_scale: torch.Tensor, sm_scale: float,
+                      out=None, lse=None, want_lse: bool = True, workspace=None, dev_err=None):
+    """Dense causal MLA prefill. q bf16 [Tq,H,576]; kv uint8 [nb,256,576]; kv_scale f32 [nb,256].
+    Returns (out bf16 [Tq,H,512], lse f32 [Tq,H] or None)."""
+    H = q.shape[1]
+    if out is None:
+        out = torch.empty((q.shape[0], H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((q.shape[0], H), dtype=torch.float32, device=q.device)
+    ws, wsb = _workspace(MLA_OP_DENSE, seqs, H, 0, workspace)
+    c = seqs.c()
+    _check(load().mla_prefill_dense(ctypes.byref(c), _ptr(q), H, _ptr(kv), _ptr(kv_scale), float(sm_scale),
+                                    _ptr(out), _ptr(lse), _ptr(ws), wsb, _ptr(dev_err), _stream()))
+    return out, lse
+
+
+def mla_indexer_topk(seqs: Seqs, qi: torch.Tensor, w: torch.Tensor, w_token_stride: int, ki: torch.Tensor,
+                     ki_scale: torch.Tensor, topk: int = 2048, idx_out=None, workspace=None, dev_err=None):
+    """Indexer scores + exact top-k. qi uint8 [Tq,64,128]; w f32; ki uint8 [nb,256,128].
+    Returns idx int32 [Tq, topk] (ascending positions, -1 padded)."""
+    if idx_out is None:
+        idx_out = torch.empty((qi.shape[0], topk), dtype=torch.int32, device=qi.device)
+    ws, wsb = _workspace(MLA_OP_INDEXER, seqs, 64, topk, workspace)
+    c = seqs.c()
+    _check(load().mla_indexer_topk(ctypes.byref(c), _ptr(qi), _ptr(w), int(w_token_stride), _ptr(ki),
+                                   _ptr(ki_scale), int(topk), _ptr(idx_out), _ptr(ws), wsb, _ptr(dev_err),
+                                   _stream()))
+    return idx_out
+
+
+def mla_prefill_sparse(seqs: Seqs, q: torch.Tensor, kv: torch.Tensor, kv_scale: torch.Tensor, sm_scale: float,
+                       idx: torch.Tensor, out=None, lse=None, want_lse: bool = True, workspace=None, dev_err=None):
+    """Sparse MLA over idx [Tq, topk] (-1 skipped). Returns (out, lse)."""
+    H = q.shape[1]
+    if out is None:
+        out = torch.empty((q.shape[0], H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((q.shape[0], H), dtype=torch.float32, device=q.device)
+    ws, wsb = _workspace(MLA_OP_SPARSE, seqs, H, idx.shape[1], workspace)
+    c = seqs.c()
+    _check(load().mla_prefill_sparse(ctypes.byref(c), _ptr(q), H, _ptr(kv), _ptr(kv_scale), float(sm_scale),
+                                     _ptr(idx), int(idx.shape[1]), _ptr(out), _ptr(lse), _ptr(ws), wsb,
+                                     _ptr(dev_err), _stream()))
+    return out, lse
+
+
+def chunk_bounds(total: int, chunk: int):
+    """[start, end) of each prefill chunk: full chunks of `chunk` tokens, the last ragged."""
+    return [(s, min(s + chunk, total)) for s in range(0, total, chunk)]
+
+
+def chunked_prefill_sparse(block_table, num_blocks: int, total: int, chunk: int, q_chunk_fn, kv, kv_scale, qi_chunk_fn,
+                           w, w_token_stride: int, ki, ki_scale, sm_scale: float, topk: int = 2048,
+                           on_chunk=None, dev_err=None):
+    """Chunked prefill of one prompt of `total` tokens (GLM-5.3-Flash page,
+    section on snapshots: prompts are read in fixed-size chunks). Chunk c covers
+    new tokens [c*chunk, min((c+1)*chunk, total)) after a cached prefix of
+    c*chunk tokens; each runs the indexer + top-k and then sparse MLA over the
+    selected rows. q_chunk_fn(start, end) / qi_chunk_fn(start, end) return the
+    chunk's device query tensors. on_chunk(c, start, end, out, lse, idx) sees
+    every chunk's result (the caller keeps what it needs)."""
+    results = []
+    for c, (s, e) in enumerate(chunk_bounds(total, chunk)):
+        seqs = Seqs([0, e - s], [s], block_table, num_blocks, device=kv.device)
+        idx = mla_indexer_topk(seqs, qi_chunk_fn(s, e), w, w_token_stride, ki, ki_scale, topk, dev_err=dev_err)
+        out, lse = mla_prefill_sparse(seqs, q_chunk_fn(s, e), kv, kv_scale, sm_scale, idx, dev_err=dev_err)
+        if on_chunk is not None:
+            on_chunk(c, s, e, out, lse, idx)
+        else:
+            results.append((out, lse, idx))
+    return results

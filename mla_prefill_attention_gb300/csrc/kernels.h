@@ -1,0 +1,57 @@
+// Launch interfaces between the C ABI layer and the kernels (internal).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+struct AttnArgs {
+    const __nv_bfloat16 *q;      // [Tq, H, 576]
+    const uint8_t *kv;           // [num_blocks, 256, 576] e4m3
+    const float *kv_scale;       // [num_blocks, 256]
+    const int32_t *block_table;  // [batch, max_blocks]
+    int32_t max_blocks, num_blocks;
+    const int32_t *cu_seqlens;   // [batch+1]
+    const int32_t *prefix_lens;  // [batch]
+    int32_t batch;
+    __nv_bfloat16 *out;          // [Tq, H, 512]
+    float *lse;                  // [Tq, H] or null
+    int32_t H;
+    float sm_scale_log2;         // sm_scale * log2(e)
+    const int32_t *idx;          // sparse: [Tq, topk]
+    int32_t topk;
+    int32_t *dev_err;
+};
+
+struct IndexerArgs {
+    const uint8_t *qi;           // [Tq, 64, 128] e4m3
+    const float *w;              // row t at w + t * w_stride
+    int64_t w_stride;
+    const uint8_t *ki;           // [num_blocks, 256, 128] e4m3
+    const float *ki_scale;       // [num_blocks, 256]
+    const int32_t *block_table;
+    int32_t max_blocks, num_blocks;
+    const int32_t *cu_seqlens;
+    const int32_t *prefix_lens;
+    int32_t batch;
+    float *scores;               // workspace [Tq, score_stride]
+    int64_t score_stride;
+    int32_t topk;
+    int32_t *idx_out;            // [Tq, topk]
+    int32_t *dev_err;
+};
+
+// Dense work item: x = sequence, y = row tile, z = paired row tile or -1.
+cudaError_t launch_dense_sm80path(const AttnArgs &a, const int4 *work, int n_work, cudaStream_t st);
+cudaError_t launch_sparse_sm80path(const AttnArgs &a, int64_t n_tokens, cudaStream_t st);
+
+// Indexer score work item: x = sequence, y = first new token (in-sequence),
+// z = token count (<= 8), w = key chunk.
+constexpr int kIdxTokensPerCta = 8;
+constexpr int kIdxKeyChunk = 4096;
+cudaError_t launch_indexer_scores(const IndexerArgs &a, const int4 *work, int n_work, cudaStream_t st);
+cudaError_t launch_topk(const IndexerArgs &a, int64_t n_tokens, cudaStream_t st);
+
+}  // namespace mla

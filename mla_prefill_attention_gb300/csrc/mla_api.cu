@@ -1,0 +1,276 @@
+// C ABI of the MLA prefill attention library: argument checks, scheduling,
+// workspace layout and kernel launches. Every entry point is declared and
+// documented in include/mla.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+#include <vector>
+
+#include "../../include/mla.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+mla_status_t fail(mla_status_t s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return s;
+}
+
+mla_status_t cuda_fail(cudaError_t e, const char *where) {
+    return fail(MLA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int kBM = 64;               // query rows per dense tile
+constexpr size_t kWsAlign = 256;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+mla_status_t check_seqs(const mla_seqs_t *s) {
+    if (!s) return fail(MLA_ERR_INVALID_ARG, "seqs is NULL");
+    if (s->batch < 1) return fail(MLA_ERR_INVALID_ARG, "batch must be >= 1 (got %d)", s->batch);
+    if (!s->cu_seqlens_q || !s->cu_seqlens_q_host || !s->prefix_lens || !s->prefix_lens_host || !s->block_table)
+        return fail(MLA_ERR_INVALID_ARG, "cu_seqlens_q, prefix_lens (device and host) and block_table must be set");
+    if (s->max_blocks_per_seq < 1 || s->num_blocks < 1)
+        return fail(MLA_ERR_INVALID_ARG, "max_blocks_per_seq and num_blocks must be >= 1");
+    if (static_cast<int64_t>(s->num_blocks) * 256 > INT32_MAX)
+        return fail(MLA_ERR_UNSUPPORTED, "num_blocks * 256 must fit in int32");
+    if (s->cu_seqlens_q_host[0] != 0) return fail(MLA_ERR_INVALID_ARG, "cu_seqlens_q[0] must be 0");
+    for (int b = 0; b < s->batch; ++b) {
+        const int64_t t = static_cast<int64_t>(s->cu_seqlens_q_host[b + 1]) - s->cu_seqlens_q_host[b];
+        const int64_t p = s->prefix_lens_host[b];
+        if (t < 0) return fail(MLA_ERR_INVALID_ARG, "cu_seqlens_q must be non-decreasing (sequence %d)", b);
+        if (p < 0) return fail(MLA_ERR_INVALID_ARG, "prefix_lens[%d] < 0", b);
+        if (p + t > INT32_MAX - 256) return fail(MLA_ERR_UNSUPPORTED, "sequence %d too long", b);
+        if ((p + t + 255) / 256 > s->max_blocks_per_seq)
+            return fail(MLA_ERR_INVALID_ARG, "sequence %d needs %lld pages > max_blocks_per_seq %d", b,
+                        static_cast<long long>((p + t + 255) / 256), s->max_blocks_per_seq);
+    }
+    return MLA_OK;
+}
+
+bool heads_ok(int32_t h) { return h == 16 || h == 32 || h == 64 || h == 128; }
+
+// Paired row tiles: tile i with tile n-1-i of the same sequence (the V-shaped
+// chunk pairing of the PCP scheme, applied at tile granularity), items sorted
+// by decreasing work so the costliest go first.
+std::vector<int4> dense_schedule(const mla_seqs_t *s, int32_t H) {
+    struct Item {
+        int4 v;
+        int64_t cost;
+    };
+    std::vector<Item> items;
+    for (int b = 0; b < s->batch; ++b) {
+        const int64_t t = s->cu_seqlens_q_host[b + 1] - s->cu_seqlens_q_host[b];
+        const int64_t P = s->prefix_lens_host[b];
+        const int64_t rows = t * H;
+        const int64_t n = (rows + kBM - 1) / kBM;
+        auto tile_keys = [&](int64_t i) {
+            const int64_t last_row = std::min(rows, (i + 1) * kBM) - 1;
+            return P + last_row / H + 1;
+        };
+        for (int64_t i = 0; i < (n + 1) / 2; ++i) {
+            const int64_t j = n - 1 - i;
+            Item it;
+            it.v = make_int4(b, static_cast<int>(i), j != i ? static_cast<int>(j) : -1, 0);
+            it.cost = tile_keys(i) + (j != i ? tile_keys(j) : 0);
+            items.push_back(it);
+        }
+    }
+    std::stable_sort(items.begin(), items.end(), [](const Item &x, const Item &y) { return x.cost > y.cost; });
+    std::vector<int4> out(items.size());
+    for (size_t i = 0; i < items.size(); ++i) out[i] = items[i].v;
+    return out;
+}
+
+int64_t max_context(const mla_seqs_t *s) {
+    int64_t m = 0;
+    for (int b = 0; b < s->batch; ++b)
+        m = std::max<int64_t>(m, s->prefix_lens_host[b] + s->cu_seqlens_q_host[b + 1] - s->cu_seqlens_q_host[b]);
+    return m;
+}
+
+std::vector<int4> indexer_schedule(const mla_seqs_t *s) {
+    std::vector<int4> items;
+    for (int b = 0; b < s->batch; ++b) {
+        const int t = s->cu_seqlens_q_host[b + 1] - s->cu_seqlens_q_host[b];
+        const int P = s->prefix_lens_host[b];
+        for (int i0 = 0; i0 < t; i0 += mla::kIdxTokensPerCta) {
+            const int nt = std::min(mla::kIdxTokensPerCta, t - i0);
+            const int keys = P + i0 + nt;
+            for (int c = 0; c * mla::kIdxKeyChunk < keys; ++c) items.push_back(make_int4(b, i0, nt, c));
+        }
+    }
+    return items;
+}
+
+size_t indexer_score_bytes(const mla_seqs_t *s) {
+    const int64_t tq = s->cu_seqlens_q_host[s->batch];
+    return round_up(static_cast<size_t>(tq) * static_cast<size_t>(max_context(s)) * sizeof(float), kWsAlign);
+}
+
+mla::AttnArgs attn_args(const mla_seqs_t *s, const void *q, int32_t H, const uint8_t *kv, const float *kv_scale,
+                        float sm_scale, void *out, float *lse, int32_t *dev_err) {
+    mla::AttnArgs a{};
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.kv = kv;
+    a.kv_scale = kv_scale;
+    a.block_table = s->block_table;
+    a.max_blocks = s->max_blocks_per_seq;
+    a.num_blocks = s->num_blocks;
+    a.cu_seqlens = s->cu_seqlens_q;
+    a.prefix_lens = s->prefix_lens;
+    a.batch = s->batch;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.lse = lse;
+    a.H = H;
+    a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+    a.dev_err = dev_err;
+    return a;
+}
+
+mla_status_t check_attn_ptrs(const void *q, const uint8_t *kv, const float *kv_scale, const void *out,
+                             const float *lse, float sm_scale) {
+    if (!q || !kv || !kv_scale || !out) return fail(MLA_ERR_INVALID_ARG, "q, kv, kv_scale and out must be set");
+    if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16))
+        return fail(MLA_ERR_INVALID_ARG, "q, kv and out must be 16-byte aligned");
+    if (!aligned(kv_scale, 4) || (lse && !aligned(lse, 4)))
+        return fail(MLA_ERR_INVALID_ARG, "kv_scale and lse must be 4-byte aligned");
+    if (!std::isfinite(sm_scale)) return fail(MLA_ERR_INVALID_ARG, "sm_scale must be finite");
+    return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *mla_last_error(void) { return g_err.c_str(); }
+
+size_t mla_workspace_size(mla_op_t op, const mla_seqs_t *seqs, int32_t num_heads, int32_t topk) {
+    (void)topk;
+    if (check_seqs(seqs) != MLA_OK) return 0;
+    switch (op) {
+        case MLA_OP_DENSE:
+            if (!heads_ok(num_heads)) return 0;
+            return round_up(dense_schedule(seqs, num_heads).size() * sizeof(int4), kWsAlign);
+        case MLA_OP_INDEXER:
+            return indexer_score_bytes(seqs) + round_up(indexer_schedule(seqs).size() * sizeof(int4), kWsAlign);
+        case MLA_OP_SPARSE:
+            return 0;
+    }
+    return 0;
+}
+
+mla_status_t mla_prefill_dense(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads,
+                               const uint8_t *kv_e4m3, const float *kv_scale, float sm_scale, void *out_bf16,
+                               float *lse, void *workspace, size_t workspace_bytes, int32_t *dev_err,
+                               cudaStream_t stream) {
+    g_err.clear();
+    mla_status_t st = check_seqs(seqs);
+    if (st != MLA_OK) return st;
+    if (!heads_ok(num_heads)) return fail(MLA_ERR_UNSUPPORTED, "num_heads must be 16, 32, 64 or 128 (got %d)", num_heads);
+    if ((st = check_attn_ptrs(q_bf16, kv_e4m3, kv_scale, out_bf16, lse, sm_scale)) != MLA_OK) return st;
+    const std::vector<int4> work = dense_schedule(seqs, num_heads);
+    const size_t need = round_up(work.size() * sizeof(int4), kWsAlign);
+    if (work.empty()) return MLA_OK;
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16))
+        return fail(MLA_ERR_WORKSPACE, "dense needs %zu workspace bytes (16-byte aligned), got %zu", need,
+                    workspace ? workspace_bytes : 0);
+    if (static_cast<int64_t>(work.size()) > INT32_MAX)
+        return fail(MLA_ERR_UNSUPPORTED, "too many tiles");
+    cudaError_t e = cudaMemcpyAsync(workspace, work.data(), work.size() * sizeof(int4), cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "schedule upload");
+    const mla::AttnArgs a = attn_args(seqs, q_bf16, num_heads, kv_e4m3, kv_scale, sm_scale, out_bf16, lse, dev_err);
+    e = mla::launch_dense_sm80path(a, static_cast<const int4 *>(workspace), static_cast<int>(work.size()), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "dense launch");
+    return MLA_OK;
+}
+
+mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, const float *w, int64_t w_token_stride,
+                              const uint8_t *ki_e4m3, const float *ki_scale, int32_t topk, int32_t *idx_out,
+                              void *workspace, size_t workspace_bytes, int32_t *dev_err, cudaStream_t stream) {
+    g_err.clear();
+    mla_status_t st = check_seqs(seqs);
+    if (st != MLA_OK) return st;
+    if (!qi_e4m3 || !w || !ki_e4m3 || !ki_scale || !idx_out)
+        return fail(MLA_ERR_INVALID_ARG, "qi, w, ki, ki_scale and idx_out must be set");
+    if (!aligned(qi_e4m3, 16) || !aligned(ki_e4m3, 16))
+        return fail(MLA_ERR_INVALID_ARG, "qi and ki must be 16-byte aligned");
+    if (!aligned(w, 4) || !aligned(ki_scale, 4) || !aligned(idx_out, 4))
+        return fail(MLA_ERR_INVALID_ARG, "w, ki_scale and idx_out must be 4-byte aligned");
+    if (w_token_stride < 0) return fail(MLA_ERR_INVALID_ARG, "w_token_stride must be >= 0");
+    if (topk < 1 || topk > 2048) return fail(MLA_ERR_UNSUPPORTED, "topk must be in [1, 2048] (got %d)", topk);
+    const int64_t tq = seqs->cu_seqlens_q_host[seqs->batch];
+    if (tq == 0) return MLA_OK;
+    const std::vector<int4> work = indexer_schedule(seqs);
+    const size_t sbytes = indexer_score_bytes(seqs);
+    const size_t need = sbytes + round_up(work.size() * sizeof(int4), kWsAlign);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+        return fail(MLA_ERR_WORKSPACE, "indexer needs %zu workspace bytes (256-byte aligned), got %zu", need,
+                    workspace ? workspace_bytes : 0);
+    int4 *dwork = reinterpret_cast<int4 *>(static_cast<char *>(workspace) + sbytes);
+    cudaError_t e = cudaSuccess;
+    if (!work.empty()) {
+        e = cudaMemcpyAsync(dwork, work.data(), work.size() * sizeof(int4), cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "schedule upload");
+    }
+    mla::IndexerArgs a{};
+    a.qi = qi_e4m3;
+    a.w = w;
+    a.w_stride = w_token_stride;
+    a.ki = ki_e4m3;
+    a.ki_scale = ki_scale;
+    a.block_table = seqs->block_table;
+    a.max_blocks = seqs->max_blocks_per_seq;
+    a.num_blocks = seqs->num_blocks;
+    a.cu_seqlens = seqs->cu_seqlens_q;
+    a.prefix_lens = seqs->prefix_lens;
+    a.batch = seqs->batch;
+    a.scores = static_cast<float *>(workspace);
+    a.score_stride = max_context(seqs);
+    a.topk = topk;
+    a.idx_out = idx_out;
+    a.dev_err = dev_err;
+    if ((e = mla::launch_indexer_scores(a, dwork, static_cast<int>(work.size()), stream)) != cudaSuccess)
+        return cuda_fail(e, "indexer score launch");
+    if ((e = mla::launch_topk(a, tq, stream)) != cudaSuccess) return cuda_fail(e, "top-k launch");
+    return MLA_OK;
+}
+
+mla_status_t mla_prefill_sparse(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads,
+                                const uint8_t *kv_e4m3, const float *kv_scale, float sm_scale, const int32_t *idx,
+                                int32_t topk, void *out_bf16, float *lse, void *workspace, size_t workspace_bytes,
+                                int32_t *dev_err, cudaStream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    g_err.clear();
+    mla_status_t st = check_seqs(seqs);
+    if (st != MLA_OK) return st;
+    if (!heads_ok(num_heads)) return fail(MLA_ERR_UNSUPPORTED, "num_heads must be 16, 32, 64 or 128 (got %d)", num_heads);
+    if ((st = check_attn_ptrs(q_bf16, kv_e4m3, kv_scale, out_bf16, lse, sm_scale)) != MLA_OK) return st;
+    if (!idx || !aligned(idx, 4)) return fail(MLA_ERR_INVALID_ARG, "idx must be set and 4-byte aligned");
+    if (topk < 1 || topk > 2048) return fail(MLA_ERR_UNSUPPORTED, "topk must be in [1, 2048] (got %d)", topk);
+    const int64_t tq = seqs->cu_seqlens_q_host[seqs->batch];
+    if (tq == 0) return MLA_OK;
+    if (tq > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "too many query tokens");
+    mla::AttnArgs a = attn_args(seqs, q_bf16, num_heads, kv_e4m3, kv_scale, sm_scale, out_bf16, lse, dev_err);
+    a.idx = idx;
+    a.topk = topk;
+    cudaError_t e = mla::launch_sparse_sm80path(a, tq, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "sparse launch");
+    return MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+"""The C ABI library without a GPU: it builds, exports every declared entry
+point, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from mla_prefill_attention_gb300 import binding as B
+from mla_prefill_attention_gb300 import build as mlabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mlabuild.build()
+    return B.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "mla.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = declared_symbols()
+    assert set(syms) == set(B.EXPORTS)
+    for s in syms:
+        assert hasattr(lib, s), s
+
+
+class HostSeqs:
+    """mla_seqs_t over host arrays only (device pointers are fake but never touched)."""
+
+    def __init__(self, q_lens, prefix, max_blocks=None, num_blocks=None):
+        self.cu = np.zeros(len(q_lens) + 1, np.int32)
+        self.cu[1:] = np.cumsum(q_lens)
+        self.pre = np.asarray(prefix, np.int32)
+        need = max(-(-(p + t) // 256) for p, t in zip(prefix, q_lens))
+        self.mb = max_blocks if max_blocks is not None else max(1, need)
+        self.nb = num_blocks if num_blocks is not None else self.mb * len(q_lens)
+        fake = 0x10000
+        self.c = B.mla_seqs_t(len(q_lens), fake, self.cu.ctypes.data, fake, self.pre.ctypes.data, fake, self.mb,
+                              self.nb)
+
+
+FAKE = ctypes.c_void_p(0x100000)        # 16-byte aligned, never dereferenced on these paths
+FAKE_MIS = ctypes.c_void_p(0x100004)
+
+
+def dense(lib, s, H=64, q=FAKE, out=FAKE, ws=None, wsb=0, scale=0.07):
+    return lib.mla_prefill_dense(ctypes.byref(s.c), q, H, FAKE, FAKE, scale, out, None, ws, wsb, None, None)
+
+
+def test_rejects_bad_arguments(lib):
+    s = HostSeqs([100], [0])
+    assert lib.mla_prefill_dense(None, FAKE, 64, FAKE, FAKE, 0.1, FAKE, None, None, 0, None, None) == B.MLA_ERR_INVALID_ARG
+    assert b"seqs" in lib.mla_last_error()
+    assert dense(lib, s, H=48) == B.MLA_ERR_UNSUPPORTED
+    assert dense(lib, s, q=FAKE_MIS) == B.MLA_ERR_INVALID_ARG
+    assert dense(lib, s, q=None) == B.MLA_ERR_INVALID_ARG
+    assert dense(lib, s, scale=float("nan")) == B.MLA_ERR_INVALID_ARG
+    assert dense(lib, s) == B.MLA_ERR_WORKSPACE                 # no workspace given
+    assert dense(lib, s, ws=FAKE, wsb=16) == B.MLA_ERR_WORKSPACE
+    short = HostSeqs([600], [0], max_blocks=2)                  # needs 3 pages
+    assert dense(lib, short) == B.MLA_ERR_INVALID_ARG
+    assert b"pages" in lib.mla_last_error()
+    bad_cu = HostSeqs([10, 5], [0, 0])
+    bad_cu.cu[2] = 3                                            # decreasing
+    assert dense(lib, bad_cu) == B.MLA_ERR_INVALID_ARG
+    neg = HostSeqs([10], [0])
+    neg.pre[0] = -1
+    assert dense(lib, neg) == B.MLA_ERR_INVALID_ARG
+    for k in (0, 2049):
+        assert lib.mla_prefill_sparse(ctypes.byref(s.c), FAKE, 64, FAKE, FAKE, 0.1, FAKE, k, FAKE, None, None, 0,
+                                      None, None) == B.MLA_ERR_UNSUPPORTED
+        assert lib.mla_indexer_topk(ctypes.byref(s.c), FAKE, FAKE, 0, FAKE, FAKE, k, FAKE, None, 0, None,
+                                    None) == B.MLA_ERR_UNSUPPORTED
+    assert lib.mla_indexer_topk(ctypes.byref(s.c), FAKE, FAKE, -1, FAKE, FAKE, 2048, FAKE, None, 0, None,
+                                None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_indexer_topk(ctypes.byref(s.c), FAKE, FAKE, 0, FAKE, FAKE, 2048, FAKE, None, 0, None,
+                                None) == B.MLA_ERR_WORKSPACE
+    odd = ctypes.c_void_p(0x100002)                             # idx needs 4-byte alignment
+    assert lib.mla_prefill_sparse(ctypes.byref(s.c), FAKE, 64, FAKE, FAKE, 0.1, odd, 2048, FAKE, None, None,
+                                  0, None, None) == B.MLA_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_noop(lib):
+    s = HostSeqs([0, 0], [5, 0])
+    assert dense(lib, s) == B.MLA_OK
+    assert lib.mla_prefill_sparse(ctypes.byref(s.c), FAKE, 64, FAKE, FAKE, 0.1, FAKE, 2048, FAKE, None, None, 0,
+                                  None, None) == B.MLA_OK
+    assert lib.mla_indexer_topk(ctypes.byref(s.c), FAKE, FAKE, 0, FAKE, FAKE, 2048, FAKE, None, 0, None,
+                                None) == B.MLA_OK
+
+
+def test_workspace_sizes(lib):
+    s = HostSeqs([4096], [12288])
+    dense_ws = lib.mla_workspace_size(B.MLA_OP_DENSE, ctypes.byref(s.c), 64, 0)
+    tiles = 4096 * 64 // 64
+    assert dense_ws == -(-((tiles + 1) // 2 * 16) // 256) * 256
+    idx_ws = lib.mla_workspace_size(B.MLA_OP_INDEXER, ctypes.byref(s.c), 64, 2048)
+    assert idx_ws >= 4096 * 16384 * 4
+    assert lib.mla_workspace_size(B.MLA_OP_SPARSE, ctypes.byref(s.c), 64, 2048) == 0
+    assert lib.mla_workspace_size(B.MLA_OP_DENSE, None, 64, 0) == 0
+    assert lib.mla_workspace_size(B.MLA_OP_DENSE, ctypes.byref(s.c), 40, 0) == 0

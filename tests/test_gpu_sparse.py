@@ -1,0 +1,175 @@
+"""Indexer top-k (bit-exact) and sparse MLA (within tolerance) on the GPU
+against the fp64 oracle, plus the chunked long-prompt driver."""
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+from mla_prefill_attention_gb300 import inputs as I
+from tests.parity import Problem, bf16_to_np, check_attention, sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_prefill_attention_gb300 import build
+    build.build()
+
+
+def run_indexer(pb, d, topk):
+    import torch
+    from mla_prefill_attention_gb300 import mla_indexer_topk
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx = mla_indexer_topk(d["seqs"], d["qi"], d["w"], 0, d["ki"], d["kis"], topk, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return idx
+
+
+def run_sparse(pb, d, idx):
+    import torch
+    from mla_prefill_attention_gb300 import mla_prefill_sparse
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = mla_prefill_sparse(d["seqs"], d["q"], d["kv"], d["ks"], pb.sm_scale, idx, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return out, lse
+
+
+def check_idx(pb, idx, toks, topk):
+    ref = O.indexer_topk(pb.ps, pb.qi[toks], pb.w, 0, toks, pb.ki, pb.kis, topk)
+    got = np.sort(idx[toks].cpu().numpy(), axis=1)
+    ref = np.sort(ref, axis=1)
+    bad = np.nonzero(np.any(got != ref, axis=1))[0]
+    assert bad.size == 0, f"{bad.size} rows differ, first token {toks[bad[0]]}"
+
+
+@pytest.mark.parametrize("q_lens,prefix,topk", [
+    ([40], [0], 16),                       # short rows keep everything, long rows select
+    ([300, 7, 129], [0, 2000, 513], 64),   # ragged batch with prefixes
+    ([64], [3000], 2048),                  # all rows longer than topk
+    ([20], [2030], 2048),                  # rows cross t+1 = topk
+])
+def test_indexer_small_exact(q_lens, prefix, topk):
+    pb = Problem(q_lens, prefix, 16, seed=200 + topk, with_indexer=True)
+    d = pb.device()
+    idx = run_indexer(pb, d, topk)
+    check_idx(pb, idx, np.arange(pb.ps.total_q), topk)
+    # positions are ascending, -1 padding only at the end
+    a = idx.cpu().numpy()
+    for r in a:
+        v = r[r >= 0]
+        assert np.all(np.diff(v) > 0) and np.all(r[len(v):] == -1)
+
+
+def test_indexer_ties_go_to_lower_position():
+    """Keys repeat three rows, so whole groups of scores tie at the cut."""
+    import torch
+    pb = Problem([16], [900], 16, seed=31, with_indexer=True)
+    rng = np.random.default_rng(31)
+    base = I.e4m3_bits(rng.integers(-3, 4, (3, 128)).astype(np.float64))
+    pb.ki = base[rng.integers(0, 3, pb.ps.num_blocks * 256)].reshape(pb.ps.num_blocks, 256, 128)
+    d = pb.device()
+    idx = run_indexer(pb, d, 100)
+    check_idx(pb, idx, np.arange(16), 100)
+
+
+@pytest.mark.parametrize("H", [16, 64, 128])
+def test_sparse_small_vs_oracle(H):
+    pb = Problem([50, 30], [700, 100], H, seed=300 + H, with_indexer=True, sm_scale=0.08)
+    d = pb.device()
+    idx = run_indexer(pb, d, 256)
+    out, lse = run_sparse(pb, d, idx)
+    toks = np.arange(pb.ps.total_q)
+    ora, ora_lse = O.mla_sparse(pb.ps, pb.q, toks, pb.kv, pb.ks, pb.sm_scale, idx.cpu().numpy())
+    check_attention(bf16_to_np(out), ora, lse.cpu().numpy(), ora_lse, f"sparse H{H}")
+
+
+def test_sparse_with_all_keys_matches_dense():
+    import torch
+    from mla_prefill_attention_gb300 import mla_prefill_dense
+    pb = Problem([100], [500], 64, seed=41, with_indexer=True)
+    d = pb.device()
+    idx = run_indexer(pb, d, 1024)                     # every row keeps all of its <= 600 keys
+    out_s, lse_s = run_sparse(pb, d, idx)
+    out_d, lse_d = mla_prefill_dense(d["seqs"], d["q"], d["kv"], d["ks"], pb.sm_scale)
+    torch.cuda.synchronize()
+    check_attention(bf16_to_np(out_s), bf16_to_np(out_d).astype(np.float64), lse_s.cpu().numpy(),
+                    lse_d.cpu().numpy().astype(np.float64), "sparse(all) vs dense")
+
+
+def test_sparse_padding_and_bad_index():
+    import torch
+    from mla_prefill_attention_gb300 import MLA_DEVERR_BAD_INDEX, mla_prefill_sparse
+    pb = Problem([4], [300], 64, seed=42)
+    d = pb.device()
+    idx = np.full((4, 64), -1, np.int32)
+    idx[0, :3] = [0, 10, 300]
+    idx[1, :2] = [5, 301]
+    idx[3, 0] = 302                                   # beyond token 3's position 303? no: valid
+    idx[3, 1] = 400                                   # beyond its position: flagged, skipped
+    ti = torch.from_numpy(idx).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = mla_prefill_sparse(d["seqs"], d["q"], d["kv"], d["ks"], pb.sm_scale, ti, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & MLA_DEVERR_BAD_INDEX
+    idx_ok = idx.copy()
+    idx_ok[3, 1] = -1
+    ora, ora_lse = O.mla_sparse(pb.ps, pb.q, np.arange(4), pb.kv, pb.ks, pb.sm_scale, idx_ok)
+    keep = [0, 1, 3]
+    check_attention(bf16_to_np(out[keep]), ora[keep], lse[keep].cpu().numpy(), ora_lse[keep], "padding")
+    assert torch.all(out[2] == 0) and torch.isinf(lse[2]).all()          # no valid index at all
+
+
+def test_sparse64k_sampled():
+    w = I.WORKLOADS["sparse64k"]
+    pb = Problem(w.q_lens, w.prefix_lens, w.heads, w.seed, w.shuffle, w.sm_scale, with_indexer=True)
+    d = pb.device()
+    idx = run_indexer(pb, d, w.topk)
+    toks = sample_tokens(pb.ps.total_q, 16, seed=3, edge=4)
+    check_idx(pb, idx, toks, w.topk)
+    out, lse = run_sparse(pb, d, idx)
+    ora, ora_lse = O.mla_sparse(pb.ps, pb.q[toks], toks, pb.kv, pb.ks, pb.sm_scale, idx[toks].cpu().numpy())
+    check_attention(bf16_to_np(out[toks]), ora, lse[toks].cpu().numpy(), ora_lse, "sparse64k")
+
+
+def test_chunked200k_selected_chunks():
+    """The 200,000-token prompt in 6,144-token chunks: indexer + sparse on
+    chunks 0, 1, 16 and the ragged last one (32), each against the oracle on
+    sampled rows; dense on the last chunk against its own oracle."""
+    import torch
+    from mla_prefill_attention_gb300 import Seqs, chunk_bounds, mla_indexer_topk, mla_prefill_dense, mla_prefill_sparse
+    w = I.WORKLOADS["chunked200k"]
+    ps = w.seqs()
+    kv, ks = I.gen_latent_cache(w.seed, ps)
+    ki, kis = I.gen_indexer_keys(w.seed, ps)
+    wh = I.gen_indexer_w(w.seed)
+    dkv, dks = torch.from_numpy(kv).cuda(), torch.from_numpy(ks).cuda()
+    dki, dkis, dw = torch.from_numpy(ki).cuda(), torch.from_numpy(kis).cuda(), torch.from_numpy(wh).cuda()
+    bounds = chunk_bounds(200000, w.chunk)
+    assert len(bounds) == 33 and bounds[-1] == (196608, 200000)
+    for c in (0, 1, 16, 32):
+        s, e = bounds[c]
+        sub = I.PagedSeqs(np.array([0, e - s], np.int32), np.array([s], np.int32), ps.block_table, ps.num_blocks)
+        seqs = Seqs.from_paged(sub)
+        q = I.gen_q_bf16(w.seed, 200000, w.heads, token_rows=np.arange(s, e))
+        qi = I.gen_indexer_q(w.seed, 200000, token_rows=np.arange(s, e))
+        dq = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).cuda()
+        dqi = torch.from_numpy(qi).cuda()
+        idx = mla_indexer_topk(seqs, dqi, dw, 0, dki, dkis, w.topk)
+        out, lse = mla_prefill_sparse(seqs, dq, dkv, dks, w.sm_scale, idx)
+        torch.cuda.synchronize()
+        toks = sample_tokens(e - s, 6, seed=c, edge=2)
+        ref = O.indexer_topk(sub, qi[toks], wh, 0, toks, ki, kis, w.topk)
+        assert np.array_equal(np.sort(idx[toks].cpu().numpy(), 1), np.sort(ref, 1)), f"chunk {c}"
+        ora, ora_lse = O.mla_sparse(sub, q[toks], toks, kv, ks, w.sm_scale, ref)
+        check_attention(bf16_to_np(out[toks]), ora, lse[toks].cpu().numpy(), ora_lse, f"chunk {c}")
+        if c == 32:
+            outd, lsed = mla_prefill_dense(seqs, dq, dkv, dks, w.sm_scale)
+            torch.cuda.synchronize()
+            td = toks[:4]
+            ora_d, ora_dl = O.mla_dense(sub, q[td], td, kv, ks, w.sm_scale)
+            check_attention(bf16_to_np(outd[td]), ora_d, lsed[td].cpu().numpy(), ora_dl, "last chunk dense")
