@@ -135,6 +135,32 @@ mla_status_t mla_prefill_sparse(const mla_seqs_t *seqs, const void *q_bf16, int3
                                 void *workspace, size_t workspace_bytes, int32_t *dev_err,
                                 cudaStream_t stream);
 
+/* Largest work list mla_prefill_dense_static can hold: 65,536 items of 16
+ * bytes (1 MiB of device memory, reserved on every GPU that loads the library
+ * for the life of the process). One item covers two 64-row query tiles, so
+ * with 64 heads a call can carry about 131,000 new tokens. */
+#define MLA_DENSE_STATIC_MAX_WORK_ITEMS 65536
+
+/* Dense prefill for callers that cannot allocate device memory. This entry
+ * point has no counterpart on the source pages: it exists for code that is
+ * given only its inputs and outputs (a plugin inside a framework that owns
+ * the whole device pool, or a caller that must avoid the implicit device
+ * synchronisation of cudaMalloc). It computes exactly what mla_prefill_dense
+ * computes and takes the same arguments minus the workspace; it calls no
+ * allocator (CUDA's or any library's) and copies nothing from the host.
+ * Its scratch space (the tile work list) is a fixed device array inside the
+ * library. The first call on each device looks that array's address up
+ * (cudaGetSymbolAddress, with the device current); make that first call
+ * before capturing the stream into a graph. All calls share the array: two
+ * calls whose work overlaps on the GPU (different streams, no ordering
+ * between them) race and may return wrong results; calls on one stream are
+ * ordered and safe. Nothing in the array needs to start at zero: each call
+ * writes every entry it reads. A batch needing more than
+ * MLA_DENSE_STATIC_MAX_WORK_ITEMS items returns MLA_ERR_UNSUPPORTED. */
+mla_status_t mla_prefill_dense_static(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads,
+                                      const uint8_t *kv_e4m3, const float *kv_scale, float sm_scale,
+                                      void *out_bf16, float *lse, int32_t *dev_err, cudaStream_t stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char *mla_last_error(void);
 

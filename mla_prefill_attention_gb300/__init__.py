@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     chunked_prefill_sparse,
     mla_indexer_topk,
     mla_prefill_dense,
+    mla_prefill_dense_static,
     mla_prefill_sparse,
     mla_workspace_size,
 )

@@ -19,7 +19,9 @@ MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_WORKSPAC
 MLA_DEVERR_BAD_PAGE, MLA_DEVERR_BAD_INDEX, MLA_DEVERR_INTERNAL = 1, 2, 8
 MLA_OP_DENSE, MLA_OP_INDEXER, MLA_OP_SPARSE = 0, 1, 2
 
-EXPORTS = ("mla_workspace_size", "mla_prefill_dense", "mla_indexer_topk", "mla_prefill_sparse", "mla_last_error")
+EXPORTS = ("mla_workspace_size", "mla_prefill_dense", "mla_indexer_topk", "mla_prefill_sparse", "mla_last_error",
+           "mla_prefill_dense_static")
+DENSE_STATIC_MAX_WORK_ITEMS = 65536
 
 
 class MlaError(RuntimeError):
@@ -62,6 +64,8 @@ def load(path: str = LIB_PATH):
     L.mla_prefill_sparse.restype = ctypes.c_int
     L.mla_prefill_sparse.argtypes = [ctypes.POINTER(mla_seqs_t), vp, i32, vp, vp, f32, vp, i32, vp, vp, vp, sz,
                                      vp, vp]
+    L.mla_prefill_dense_static.restype = ctypes.c_int
+    L.mla_prefill_dense_static.argtypes = [ctypes.POINTER(mla_seqs_t), vp, i32, vp, vp, f32, vp, vp, vp, vp]
     L.mla_last_error.restype = ctypes.c_char_p
     L.mla_last_error.argtypes = []
     _lib = L
@@ -131,6 +135,23 @@ def mla_prefill_dense(seqs: Seqs, q: torch.Tensor, kv: torch.Tensor, kv_scale: t
     c = seqs.c()
     _check(load().mla_prefill_dense(ctypes.byref(c), _ptr(q), H, _ptr(kv), _ptr(kv_scale), float(sm_scale),
                                     _ptr(out), _ptr(lse), _ptr(ws), wsb, _ptr(dev_err), _stream()))
+    return out, lse
+
+
+def mla_prefill_dense_static(seqs: Seqs, q: torch.Tensor, kv: torch.Tensor, kv_scale: torch.Tensor,
+                             sm_scale: float, out=None, lse=None, want_lse: bool = True, dev_err=None):
+    """Dense prefill that allocates nothing inside the library: same result as
+    mla_prefill_dense, for callers that may not allocate device memory (its
+    scratch is a fixed array inside libmla.so; calls on different streams that
+    overlap on the GPU race on it). Returns (out, lse)."""
+    H = q.shape[1]
+    if out is None:
+        out = torch.empty((q.shape[0], H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((q.shape[0], H), dtype=torch.float32, device=q.device)
+    c = seqs.c()
+    _check(load().mla_prefill_dense_static(ctypes.byref(c), _ptr(q), H, _ptr(kv), _ptr(kv_scale), float(sm_scale),
+                                           _ptr(out), _ptr(lse), _ptr(dev_err), _stream()))
     return out, lse
 
 

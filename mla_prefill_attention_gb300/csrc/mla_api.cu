@@ -274,3 +274,20 @@ mla_status_t mla_prefill_sparse(const mla_seqs_t *seqs, const void *q_bf16, int3
 }
 
 }  // extern "C"
+
+// Helpers shared with the allocation-free dense entry point (dense_noalloc.cu).
+namespace mla {
+mla_status_t check_dense_args(const mla_seqs_t *seqs, const void *q, int32_t H, const uint8_t *kv,
+                              const float *kv_scale, const void *out, const float *lse, float sm_scale) {
+    g_err.clear();
+    mla_status_t st = check_seqs(seqs);
+    if (st != MLA_OK) return st;
+    if (!heads_ok(H)) return fail(MLA_ERR_UNSUPPORTED, "num_heads must be 16, 32, 64 or 128 (got %d)", H);
+    return check_attn_ptrs(q, kv, kv_scale, out, lse, sm_scale);
+}
+mla_status_t report(mla_status_t s, const char *msg) { return fail(s, "%s", msg); }
+AttnArgs make_attn_args(const mla_seqs_t *s, const void *q, int32_t H, const uint8_t *kv, const float *kv_scale,
+                        float sm_scale, void *out, float *lse, int32_t *dev_err) {
+    return attn_args(s, q, H, kv, kv_scale, sm_scale, out, lse, dev_err);
+}
+}  // namespace mla
