@@ -65,6 +65,7 @@ typedef enum {
 /* Bits ORed into *dev_err by the kernels. */
 #define MLA_DEVERR_BAD_PAGE 1   /* block table entry outside [0, num_blocks) */
 #define MLA_DEVERR_BAD_INDEX 2  /* sparse index outside [-1, position of the query] */
+#define MLA_DEVERR_TIMEOUT 4    /* a bounded wait inside a kernel gave up; that CTA's rows are not written */
 #define MLA_DEVERR_INTERNAL 8   /* a kernel invariant failed (a library bug); the row is -1 filled */
 
 typedef enum {

@@ -46,6 +46,9 @@ struct IndexerArgs {
 // Dense work item: x = sequence, y = row tile, z = paired row tile or -1.
 cudaError_t launch_dense_sm80path(const AttnArgs &a, const int4 *work, int n_work, cudaStream_t st);
 cudaError_t launch_sparse_sm80path(const AttnArgs &a, int64_t n_tokens, cudaStream_t st);
+// tcgen05/TMEM kernels (64 query rows per CTA; same work items)
+cudaError_t launch_dense_tc(const AttnArgs &a, const int4 *work, int n_work, cudaStream_t st);
+cudaError_t launch_sparse_tc(const AttnArgs &a, int64_t n_tokens, cudaStream_t st);
 
 // Indexer score work item: x = sequence, y = first new token (in-sequence),
 // z = token count (<= 8), w = key chunk.

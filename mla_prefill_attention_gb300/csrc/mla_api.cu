@@ -193,7 +193,7 @@ mla_status_t mla_prefill_dense(const mla_seqs_t *seqs, const void *q_bf16, int32
     cudaError_t e = cudaMemcpyAsync(workspace, work.data(), work.size() * sizeof(int4), cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e, "schedule upload");
     const mla::AttnArgs a = attn_args(seqs, q_bf16, num_heads, kv_e4m3, kv_scale, sm_scale, out_bf16, lse, dev_err);
-    e = mla::launch_dense_sm80path(a, static_cast<const int4 *>(workspace), static_cast<int>(work.size()), stream);
+    e = mla::launch_dense_tc(a, static_cast<const int4 *>(workspace), static_cast<int>(work.size()), stream);
     if (e != cudaSuccess) return cuda_fail(e, "dense launch");
     return MLA_OK;
 }
@@ -268,7 +268,7 @@ mla_status_t mla_prefill_sparse(const mla_seqs_t *seqs, const void *q_bf16, int3
     mla::AttnArgs a = attn_args(seqs, q_bf16, num_heads, kv_e4m3, kv_scale, sm_scale, out_bf16, lse, dev_err);
     a.idx = idx;
     a.topk = topk;
-    cudaError_t e = mla::launch_sparse_sm80path(a, tq, stream);
+    cudaError_t e = mla::launch_sparse_tc(a, tq, stream);
     if (e != cudaSuccess) return cuda_fail(e, "sparse launch");
     return MLA_OK;
 }
