@@ -4,18 +4,22 @@
 // token) and streams the latent rows of the paged e4m3 cache 128 keys at a
 // time. Per key tile:
 //
-//   S   = Q K^T          tcgen05.mma kind::f16, M=64 N=128, K=576, D in TMEM
-//   u   = S*sigma*rowscale + log2(sigma)        (log2 domain, sigma folded in)
+//   S   = Q K'^T         tcgen05.mma kind::f16, M=64 N=128, K=576, D in TMEM
+//   u   = S*sigma'*rowscale + log2(sigma)       (log2 domain, sigma folded in)
 //   P   = 2^(u - m),  l += P / sigma             (m: running reference max)
-//   O  += P V            tcgen05.mma M=64 N=256 (two Dv halves), A=P from TMEM
+//   O  += P V'           tcgen05.mma M=64 N=256 (two Dv halves), A=P from TMEM
 //
-// and at the end out = O / l, lse = ln2 (m + log2 l).
+// and at the end out = 2^8 O / l, lse = ln2 (m + log2 l). K' and V' hold the
+// e4m3 codes times 2^-8: the f16 bit pattern of that product is the code's own
+// bits moved into place (see f16x2_of_e4m3x2), so dequantisation costs three
+// integer operations per code pair and sigma' = 2^8 sigma restores the scale.
 //
 // Why 64 rows: with the 512-wide value head an fp32 O for 128 rows fills all
 // 512 TMEM columns, and a 128 x 576 f16 Q tile alone is 144 KB of shared
 // memory. With 64 rows, O takes two lane-halves x 256 columns and Q 72 KB.
 // M=64 MMAs run at half the M=128 rate on this part (2048 vs 4096 MAC/clk per
-// SM, measured), so this kernel is capped at half the dense tensor peak.
+// SM, measured), so this kernel is capped at half the dense tensor peak per
+// clock.
 //
 // TMEM (M=64 layout: row r lives in lane 32*(r/16) + r%16 + 16*h; h = lane half)
 //   cols   0..255 h=0 : O for value dims   0..255
@@ -28,13 +32,19 @@
 //   K  : 9 slices x [128 keys][64 dims] f16  (144 KB); slices 0..7 double as V
 //        (MN-major B operand of PV), slice 8 holds the RoPE dims
 //
-// Warps: 0-3 softmax/correction (warp w owns TMEM lane quadrant w), 4-7
-// loaders (Q prescale, e4m3 -> f16 conversion of K straight from global
-// memory, per-key scales), 8 MMA issue. The K tile is single-buffered but
-// recycled slice-group by slice-group: slice 8 is refilled as soon as QK has
-// used it, slices 0-3 after the first PV half, slices 4-7 after the second.
-// Every wait is bounded; a wait that runs out sets MLA_DEVERR_TIMEOUT and the
-// CTA abandons its tile.
+// Warps: 0-3 softmax/correction (warp w owns TMEM lane quadrant w and reads S
+// with the 16-lane shapes, so each thread holds two rows x 32 keys), 4-7
+// loaders (one key per thread: the raw e4m3 bytes of the next key tile are
+// fetched into registers while the current one is converted into the
+// swizzled K slices), 8 MMA issue, 9-11 idle. Launched at 168 registers a
+// thread, the softmax and loader warpgroups grow to 200 and 232 while the
+// issuer's warpgroup shrinks to 56 (128 x (200 + 232 + 56) <= 384 x 168).
+// The K tile is single-buffered but recycled
+// slice-group by slice-group: slice 8 is refilled as soon as QK has used it
+// (and the next tile's RoPE part of QK runs while the softmax works), slices
+// 0-3 after the first PV half, slices 4-7 after the second. Every wait is
+// bounded; a wait that runs out sets MLA_DEVERR_TIMEOUT and the CTA abandons
+// its tile.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -49,7 +59,7 @@ using namespace tc;
 constexpr int BM = 64;            // query rows per CTA tile
 constexpr int BN = 128;           // keys per tile
 constexpr int NSLICE = 9;         // 576 / 64
-constexpr int NT = 288;           // 9 warps
+constexpr int NT = 384;           // 12 warps = 3 warpgroups
 constexpr int kQSlice = BM * 128;         // 8192 B
 constexpr int kKSlice = BN * 128;         // 16384 B
 constexpr int kSmemQ = NSLICE * kQSlice;  // 73728
@@ -57,6 +67,9 @@ constexpr int kSmemK = NSLICE * kKSlice;  // 147456
 constexpr int kDynSmem = 1024 + kSmemQ + kSmemK;
 constexpr long long kWaitCycles = 200000000LL;   // ~0.1 s: every wait here covers at most one tile of work
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+constexpr float kCodeScale = 256.0f;       // K', V' hold code * 2^-8
+constexpr uint32_t kRegsSoftmax = 200, kRegsLoader = 232, kRegsIssuer = 56;   // per-thread budgets after the split
+static_assert(128 * (kRegsSoftmax + kRegsLoader + kRegsIssuer) <= NT * 168, "register split exceeds the launch pool");
 
 // TMEM columns
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 384;
@@ -64,21 +77,20 @@ constexpr uint32_t kHalf1 = 16u << 16;     // lane offset of the upper half
 
 enum Bar {
     B_FULL_ROPE, B_FULL_A, B_FULL_B,    // loaders -> issuer: K slices converted (8 | 0-3 | 4-7)
-    B_FREE_ROPE, B_FREE_A, B_FREE_B,    // issuer (MMA commit) -> loaders: slices consumed
-    B_S_FULL,                           // issuer -> softmax: S ready
+    B_FREE_A, B_FREE_B,                 // issuer (MMA commit) -> loaders: V slices consumed by PV
+    B_S_FULL,                           // issuer -> softmax, loaders: QK complete (S ready, slice 8 and Q reusable)
     B_S_FREE,                           // softmax -> issuer: S read out
     B_P_FULL,                           // softmax -> issuer: P written (and O rescaled)
     B_PV_DONE,                          // issuer -> softmax: PV of the tile complete
-    B_Q_FULL,                           // loaders -> issuer: Q tile in smem
+    B_Q_FULL,                           // loaders -> issuer, softmax: Q tile and row data in smem
     B_O_FREE,                           // softmax -> issuer: epilogue finished reading O
     B_FINAL,                            // issuer -> all: every MMA of the CTA complete
-    B_Q_FREE,                           // issuer -> loaders: last QK of a row tile complete (Q reusable)
-    B_META0, B_META1,                   // loaders -> softmax: key metadata (and row data) of tile n, n&1
+    B_META0, B_META1,                   // loaders -> softmax: key metadata of tile n, n&1
     NBAR
 };
 
-struct KeyMeta {
-    float sig, lsig, isig, pad;          // sigma, log2 sigma (-inf = masked), 1/sigma
+struct __align__(16) KeyMeta {
+    float sig, lsig, isig, pad;          // 2^8 sigma, log2 sigma (-inf = masked), 1/sigma
 };
 
 struct Shared {
@@ -193,7 +205,7 @@ __device__ void load_q(const AttnArgs &a, Shared &sh, uint8_t *sq, const RowTile
     }
 }
 
-// Metadata and cache row of key k (0..127) of key tile j.
+// Cache row of key k (0..127) of key tile j (-1: no key) and its scale.
 template <bool kSparse>
 __device__ __forceinline__ int64_t key_row(const AttnArgs &a, const int32_t *bt, const RowTile &rt, int j, int k,
                                            float &sig) {
@@ -214,9 +226,15 @@ __device__ __forceinline__ int64_t key_row(const AttnArgs &a, const int32_t *bt,
     return row;
 }
 
+__device__ __forceinline__ void write_meta(KeyMeta &m, int64_t row, float sig) {
+    m.sig = sig * kCodeScale;
+    m.lsig = row >= 0 ? __log2f(sig) : -INFINITY;
+    m.isig = 1.f / sig;
+}
+
 // Raw e4m3 bytes of slices s0..s0+NS-1 (64 dims each) of one cache row.
 template <int NS>
-__device__ __forceinline__ void fetch_slices(const uint8_t *kv, int64_t row, int s0, uint4 (&raw)[NS * 4]) {
+__device__ __forceinline__ void fetch_slices(const uint8_t *kv, int64_t row, int s0, uint4 *raw) {
 #pragma unroll
     for (int s = 0; s < NS; ++s)
 #pragma unroll
@@ -224,9 +242,18 @@ __device__ __forceinline__ void fetch_slices(const uint8_t *kv, int64_t row, int
             raw[4 * s + i] = row >= 0 ? __ldg(reinterpret_cast<const uint4 *>(kv + row * kDqk + (s0 + s) * 64) + i)
                                       : make_uint4(0, 0, 0, 0);
 }
-// e4m3 -> f16 (exact) into the swizzled K slices, key k.
+
+// Two e4m3 codes (bytes 0 and 2 of t, bytes 1 and 3 zero) -> f16x2 of code * 2^-8,
+// exactly: an e4m3 code's exponent and mantissa fields, moved to bits 7..14,
+// read as an f16 are the code's value times 2^-8 (normal and subnormal alike,
+// since both formats have the same subnormal step relative to their bias);
+// adding the sign bit to itself carries it from bit 14 to bit 15.
+// The two NaN codes (0x7F, 0xFF) come out as +-480 * 2^-8; quantised caches
+// never hold them.
+__device__ __forceinline__ uint32_t f16x2_of_e4m3x2(uint32_t t) { return (t + (t & 0x00800080u)) << 7; }
+
 template <int NS>
-__device__ __forceinline__ void store_slices(uint8_t *sk, int k, int s0, const uint4 (&raw)[NS * 4]) {
+__device__ __forceinline__ void store_slices(uint8_t *sk, int k, int s0, const uint4 *raw) {
 #pragma unroll
     for (int s = 0; s < NS; ++s) {
         uint8_t *dst = sk + (s0 + s) * kKSlice;
@@ -234,15 +261,24 @@ __device__ __forceinline__ void store_slices(uint8_t *sk, int k, int s0, const u
         for (int i = 0; i < 4; ++i) {
             const uint4 r = raw[4 * s + i];
             uint32_t h[8];
-            e4m3x4_to_f16x4(r.x, h[0], h[1]);
-            e4m3x4_to_f16x4(r.y, h[2], h[3]);
-            e4m3x4_to_f16x4(r.z, h[4], h[5]);
-            e4m3x4_to_f16x4(r.w, h[6], h[7]);
+            h[0] = f16x2_of_e4m3x2(__byte_perm(r.x, 0u, 0x4140u));
+            h[1] = f16x2_of_e4m3x2(__byte_perm(r.x, 0u, 0x4342u));
+            h[2] = f16x2_of_e4m3x2(__byte_perm(r.y, 0u, 0x4140u));
+            h[3] = f16x2_of_e4m3x2(__byte_perm(r.y, 0u, 0x4342u));
+            h[4] = f16x2_of_e4m3x2(__byte_perm(r.z, 0u, 0x4140u));
+            h[5] = f16x2_of_e4m3x2(__byte_perm(r.z, 0u, 0x4342u));
+            h[6] = f16x2_of_e4m3x2(__byte_perm(r.w, 0u, 0x4140u));
+            h[7] = f16x2_of_e4m3x2(__byte_perm(r.w, 0u, 0x4342u));
             *reinterpret_cast<uint4 *>(dst + swz(k, 2 * i)) = make_uint4(h[0], h[1], h[2], h[3]);
             *reinterpret_cast<uint4 *>(dst + swz(k, 2 * i + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
         }
     }
 }
+
+// (row tile, key tile) -> next (row tile, key tile) in the CTA's visiting order
+struct Cursor {
+    int r, j, n;        // row tile, key tile, key tiles of row tile r
+};
 
 // ---------------------------------------------------------------------------
 // the kernel
@@ -304,119 +340,143 @@ __global__ void __launch_bounds__(NT, 1) attn_kernel(const AttnArgs a, const int
 
     if (warp >= 4 && warp < 8) {
         // =================== loaders ===================
-        const int lt = tid - 128;              // 0..127 = key index within a tile
-        uint32_t ph_free_rope = 0, ph_free_a = 0, ph_free_b = 0, ph_q_free = 0;
-        int ktile_global = 0;                  // key tiles loaded so far (meta ring index)
-        for (int r = 0; r < n_rt; ++r) {
-            const RowTile rt = make_tile<kSparse>(a, b, tiles[r], sp_tok, sp_h0);
-            if (r > 0) {                       // Q is reusable once the last QK of the previous row tile is done
-                if (!wait(B_Q_FREE, ph_q_free)) break;
-                ph_q_free ^= 1;
+        regs_inc<kRegsLoader>();
+        // Tile t's raw bytes are in registers when iteration t starts; each
+        // group is converted once its slots are free and the same group of
+        // tile t+1 is fetched right after, a whole tile ahead of its use.
+        const int lt = tid - 128;              // key index within a tile
+        RowTile rt = make_tile<kSparse>(a, b, tiles[0], sp_tok, sp_h0);
+        Cursor cur{0, 0, rt.n_ktiles};
+        RowTile rt_next = rt;
+        uint4 r_rope[4], r_a[16], r_b[16];
+        float sig;
+        int64_t row = key_row<kSparse>(a, bt, rt, 0, lt, sig);
+        write_meta(sh.meta[0][lt], row, sig);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_META0]));
+        fetch_slices<1>(a.kv, row, 8, r_rope);
+        fetch_slices<4>(a.kv, row, 0, r_a);
+        fetch_slices<4>(a.kv, row, 4, r_b);
+        load_q<kSparse>(a, sh, sq, rt, b, 0, lt);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_Q_FULL]));
+        for (int t = 0;; ++t) {
+            // ---- slice 8: free once the previous tile's QK is complete (that also frees Q) ----
+            if (t > 0) {
+                if (!wait(B_S_FULL, (t - 1) & 1)) break;
+                if (cur.j == 0) {
+                    load_q<kSparse>(a, sh, sq, rt, b, cur.r & 1, lt);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_Q_FULL]));
+                }
             }
-            load_q<kSparse>(a, sh, sq, rt, b, r & 1, lt);
+            store_slices<1>(sk, lt, 8, r_rope);
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_Q_FULL]));
-            bool ok = true;
-            for (int j = 0; j < rt.n_ktiles && ok; ++j, ++ktile_global) {
-                float sig;
-                const int64_t row = key_row<kSparse>(a, bt, rt, j, lt, sig);
-                const bool first = ktile_global == 0;
-                KeyMeta &m = sh.meta[ktile_global & 3][lt];
-                m.sig = sig;
-                m.lsig = row >= 0 ? __log2f(sig) : -INFINITY;
-                m.isig = 1.f / sig;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[(ktile_global & 1) ? B_META1 : B_META0]));
-                {   // slice 8 (RoPE dims): free once QK of the previous tile has used it
-                    uint4 raw[4];
-                    fetch_slices<1>(a.kv, row, 8, raw);
-                    if (!first && !(ok = wait(B_FREE_ROPE, ph_free_rope))) break;
-                    if (!first) ph_free_rope ^= 1;
-                    store_slices<1>(sk, lt, 8, raw);
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL_ROPE]));
-                }
-#pragma unroll 1
-                for (int g = 0; g < 2; ++g) {   // slices 0-3, then 4-7: free after the matching PV half
-                    uint4 raw[16];
-                    fetch_slices<4>(a.kv, row, 4 * g, raw);
-                    if (!first) {
-                        if (!(ok = wait(g ? B_FREE_B : B_FREE_A, g ? ph_free_b : ph_free_a))) break;
-                        if (g) ph_free_b ^= 1; else ph_free_a ^= 1;
-                    }
-                    store_slices<4>(sk, lt, 4 * g, raw);
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&sh.bar[g ? B_FULL_B : B_FULL_A]));
+            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL_ROPE]));
+            // ---- the next tile: metadata now, raw bytes group by group ----
+            Cursor nxt = cur;
+            bool more = true;
+            if (++nxt.j == nxt.n) {
+                nxt.j = 0;
+                if (++nxt.r < n_rt) {
+                    rt_next = make_tile<kSparse>(a, b, tiles[nxt.r], sp_tok, sp_h0);
+                    nxt.n = rt_next.n_ktiles;
+                } else {
+                    more = false;
                 }
             }
-            if (!ok) break;
+            int64_t row_n = -1;
+            if (more) {
+                row_n = key_row<kSparse>(a, bt, rt_next, nxt.j, lt, sig);
+                write_meta(sh.meta[(t + 1) & 3][lt], row_n, sig);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[((t + 1) & 1) ? B_META1 : B_META0]));
+                fetch_slices<1>(a.kv, row_n, 8, r_rope);
+            }
+            // ---- slices 0-3, then 4-7: free after the matching half of the previous PV ----
+            if (t > 0 && !wait(B_FREE_A, (t - 1) & 1)) break;
+            store_slices<4>(sk, lt, 0, r_a);
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL_A]));
+            if (more) fetch_slices<4>(a.kv, row_n, 0, r_a);
+            if (t > 0 && !wait(B_FREE_B, (t - 1) & 1)) break;
+            store_slices<4>(sk, lt, 4, r_b);
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL_B]));
+            if (!more) break;
+            fetch_slices<4>(a.kv, row_n, 4, r_b);
+            cur = nxt;
+            rt = rt_next;
         }
-    } else if (warp == 8) {
-        // =================== MMA issuer ===================
-        if (lane == 0) {
+    } else if (warp >= 8) {
+        // =================== MMA issuer (warp 8, lane 0) ===================
+        regs_dec<kRegsIssuer>();
+        if (warp == 8 && lane == 0) {
             const uint32_t id_qk = idesc_f16(BM, BN, false, false, false, false);
             const uint32_t id_pv = idesc_f16(BM, 256, false, false, false, true);
-            uint32_t ph_full_rope = 0, ph_full_a = 0, ph_full_b = 0, ph_s_free = 0, ph_p_full = 0, ph_q_full = 0,
-                     ph_o_free = 0;
-            int ktile_global = 0;
-            bool ok = true;
+            // Descriptors of the operand bases; an operand at byte offset x is the base
+            // descriptor plus x/16 (start-address field; shared addresses stay below 2^18).
+            const uint64_t dq0 = sdesc(sq_a, 16, 1024, kSw128);
+            const uint64_t dk0 = sdesc(sk_a, 16, 1024, kSw128);
+            const uint64_t dv0 = sdesc(sk_a, kKSlice, 1024, kSw128);
+            // QK over one 64-dim slice (4 MMAs of K=16)
+            auto qk_slice = [&](int slice, bool first) {
+                const uint64_t da = dq0 + static_cast<uint64_t>((slice * kQSlice) >> 4);
+                const uint64_t db = dk0 + static_cast<uint64_t>((slice * kKSlice) >> 4);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16_ss(tmem + kColS, da + 2 * ks, db + 2 * ks, id_qk, (first && ks == 0) ? 0u : 1u);
+            };
+            int t = 0;
+            bool rope_issued = false, ok = true;
             for (int r = 0; r < n_rt && ok; ++r) {
                 const RowTile rt = make_tile<kSparse>(a, b, tiles[r], sp_tok, sp_h0);
-                ok = wait(B_Q_FULL, ph_q_full);
-                ph_q_full ^= 1;
-                fence_after_sync();
-                for (int j = 0; j < rt.n_ktiles && ok; ++j, ++ktile_global) {
-                    // ---- S = Q K^T, slice order 8, 0-3, 4-7 ----
-                    if (!(ok = wait(B_FULL_ROPE, ph_full_rope))) break;
-                    ph_full_rope ^= 1;
-                    if (ktile_global > 0) {
-                        if (!(ok = wait(B_S_FREE, ph_s_free))) break;
-                        ph_s_free ^= 1;
+                for (int j = 0; j < rt.n_ktiles && ok; ++j, ++t) {
+                    // ---- S = Q K^T: slice 8 (unless already issued), then 0-3, 4-7 ----
+                    if (!rope_issued) {
+                        if (j == 0 && !(ok = wait(B_Q_FULL, r & 1))) break;
+                        if (!(ok = wait(B_FULL_ROPE, t & 1))) break;
+                        if (t > 0 && !(ok = wait(B_S_FREE, (t - 1) & 1))) break;
+                        fence_after_sync();
+                        qk_slice(8, true);
                     }
+                    rope_issued = false;
+                    if (!(ok = wait(B_FULL_A, t & 1))) break;
                     fence_after_sync();
-                    for (int s = 0; s < NSLICE && ok; ++s) {
-                        const int slice = s == 0 ? 8 : s - 1;
-                        if (s == 1) {
-                            if (!(ok = wait(B_FULL_A, ph_full_a))) break;
-                            ph_full_a ^= 1;
-                            fence_after_sync();
-                        }
-                        if (s == 5) {
-                            if (!(ok = wait(B_FULL_B, ph_full_b))) break;
-                            ph_full_b ^= 1;
-                            fence_after_sync();
-                        }
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t da = sdesc(sq_a + slice * kQSlice + ks * 32, 16, 1024, kSw128);
-                            const uint64_t db = sdesc(sk_a + slice * kKSlice + ks * 32, 16, 1024, kSw128);
-                            mma_f16_ss(tmem + kColS, da, db, id_qk, (s > 0 || ks > 0) ? 1u : 0u);
-                        }
-                        if (s == 0) mma_commit(smem_u32(&sh.bar[B_FREE_ROPE]));
-                    }
-                    if (!ok) break;
+#pragma unroll 1
+                    for (int s = 0; s < 4; ++s) qk_slice(s, false);
+                    if (!(ok = wait(B_FULL_B, t & 1))) break;
+                    fence_after_sync();
+#pragma unroll 1
+                    for (int s = 4; s < 8; ++s) qk_slice(s, false);
                     mma_commit(smem_u32(&sh.bar[B_S_FULL]));
-                    if (j + 1 == rt.n_ktiles) mma_commit(smem_u32(&sh.bar[B_Q_FREE]));
+                    // ---- the next tile's RoPE slice while the softmax works on this one ----
+                    if (j + 1 < rt.n_ktiles) {
+                        if (!(ok = wait(B_FULL_ROPE, (t + 1) & 1))) break;
+                        if (!(ok = wait(B_S_FREE, t & 1))) break;
+                        fence_after_sync();
+                        qk_slice(8, true);
+                        rope_issued = true;
+                    }
                     // ---- O += P V ----
                     if (j == 0 && r > 0) {
-                        if (!(ok = wait(B_O_FREE, ph_o_free))) break;
-                        ph_o_free ^= 1;
+                        if (!(ok = wait(B_O_FREE, (r - 1) & 1))) break;
                     }
-                    if (!(ok = wait(B_P_FULL, ph_p_full))) break;
-                    ph_p_full ^= 1;
+                    if (!(ok = wait(B_P_FULL, t & 1))) break;
                     fence_after_sync();
 #pragma unroll 1
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t lane_off = h ? kHalf1 : 0u;
+                        const uint64_t dv = dv0 + static_cast<uint64_t>((4 * h * kKSlice) >> 4);
 #pragma unroll
-                        for (int ks = 0; ks < BN / 16; ++ks) {
-                            const uint64_t dbv = sdesc(sk_a + (4 * h) * kKSlice + ks * 2048, kKSlice, 1024, kSw128);
-                            mma_f16_ts(tmem + lane_off + kColO, tmem + lane_off + kColP + ks * 8, dbv, id_pv,
+                        for (int ks = 0; ks < BN / 16; ++ks)
+                            mma_f16_ts(tmem + lane_off + kColO, tmem + lane_off + kColP + ks * 8, dv + 128 * ks, id_pv,
                                        (j > 0 || ks > 0) ? 1u : 0u);
-                        }
                         mma_commit(smem_u32(&sh.bar[h ? B_FREE_B : B_FREE_A]));
                     }
                     mma_commit(smem_u32(&sh.bar[B_PV_DONE]));
@@ -427,136 +487,155 @@ __global__ void __launch_bounds__(NT, 1) attn_kernel(const AttnArgs a, const int
         __syncwarp();
     } else {
         // =================== softmax / correction (warps 0-3) ===================
+        regs_inc<kRegsSoftmax>();
+        // S is read with the 16-lane shapes: thread t holds rows ra = 16q + t/4
+        // and rb = ra + 8, keys 8i + 2(t%4) + {0,1} for i = 0..15.
         const int q = warp;                        // TMEM lane quadrant
-        const bool lo = lane < 16;                 // lower half: S, P_a, O_a ; upper: P_b, O_b
-        const int row = 16 * q + (lane & 15);
+        const int tq = lane >> 2, tc = lane & 3;
+        const int ra = 16 * q + tq, rb = ra + 8;
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-        uint32_t ph_s_full = 0, ph_pv_done = 0, ph_meta[2] = {0, 0};
-        int ktile_global = 0;
+        int t = 0;
         bool ok = true;
         for (int r = 0; r < n_rt && ok; ++r) {
             const RowTile rt = make_tile<kSparse>(a, b, tiles[r], sp_tok, sp_h0);
-            float m_ref = -INFINITY, l_sum = 0.f;
-            float rs = 0.f;
-            int lim = -1;
-            for (int j = 0; j < rt.n_ktiles && ok; ++j, ++ktile_global) {
-                if (!(ok = wait((ktile_global & 1) ? B_META1 : B_META0, ph_meta[ktile_global & 1]))) break;
-                ph_meta[ktile_global & 1] ^= 1;
-                if (!(ok = wait(B_S_FULL, ph_s_full))) break;
-                ph_s_full ^= 1;
+            float m_a = -INFINITY, m_b = -INFINITY;  // reference maxima (log2 domain)
+            float l_a = 0.f, l_b = 0.f;              // this thread's partial row sums (32 keys per tile)
+            if (!(ok = wait(B_Q_FULL, r & 1))) break;
+            const float rs_a = sh.rowscale[r & 1][ra], rs_b = sh.rowscale[r & 1][rb];
+            const int lim_a = sh.rowlimit[r & 1][ra], lim_b = sh.rowlimit[r & 1][rb];
+            const int lim_min = min(lim_a, lim_b);
+            for (int j = 0; j < rt.n_ktiles && ok; ++j, ++t) {
+                if (!(ok = wait((t & 1) ? B_META1 : B_META0, (t >> 1) & 1))) break;
+                if (!(ok = wait(B_S_FULL, t & 1))) break;
                 fence_after_sync();
-                if (j == 0) {
-                    rs = sh.rowscale[r & 1][row];
-                    lim = sh.rowlimit[r & 1][row];
-                }
-                // S row: lower-half threads keep keys 0..63, upper-half threads take keys 64..127
-                // of the same row from the lower-half lane that holds them
                 uint32_t sv[64];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t t[16];
-                    tmem_ld16(tmem + lane_addr + kColS + 64 + 16 * c, t);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const uint32_t x = __shfl_sync(0xffffffffu, t[i], lane & 15);
-                        if (!lo) sv[16 * c + i] = x;
-                    }
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t t[16];
-                    tmem_ld16(tmem + lane_addr + kColS + 16 * c, t);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (lo) sv[16 * c + i] = t[i];
-                }
+                tmem_ld_16x256b_x8(tmem + lane_addr + kColS, sv);
+                tmem_ld_16x256b_x8(tmem + lane_addr + kColS + 64, sv + 32);
+                tmem_ld_wait();
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_S_FREE]));
-                // ---- logits in the log2 domain, tile max ----
-                const KeyMeta *meta = sh.meta[ktile_global & 3] + (lo ? 0 : 64);
-                const int key0 = (kSparse ? 0 : j * BN) + (lo ? 0 : 64);
-                float mx = -INFINITY;
+                // ---- logits in the log2 domain, tile maxima ----
+                const KeyMeta *meta = sh.meta[t & 3];
+                const int key0 = kSparse ? 0 : j * BN;
+                const bool full = kSparse ? (lim_min >= 0) : (key0 + BN - 1 <= lim_min);
+                float mx_a = -INFINITY, mx_b = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const float4 km = *reinterpret_cast<const float4 *>(&meta[i]);
-                    const bool vis = kSparse ? lim >= 0 : (key0 + i <= lim);
-                    const float u = vis ? fmaf(__uint_as_float(sv[i]) * km.x, rs, km.y) : -INFINITY;
-                    sv[i] = __float_as_uint(u);
-                    mx = fmaxf(mx, u);
+                for (int i = 0; i < 16; ++i) {
+                    const int k0 = 8 * i + 2 * tc;
+                    const float4 m0 = *reinterpret_cast<const float4 *>(&meta[k0]);
+                    const float4 m1 = *reinterpret_cast<const float4 *>(&meta[k0 + 1]);
+                    float u0 = fmaf(__uint_as_float(sv[4 * i + 0]) * m0.x, rs_a, m0.y);
+                    float u1 = fmaf(__uint_as_float(sv[4 * i + 1]) * m1.x, rs_a, m1.y);
+                    float u2 = fmaf(__uint_as_float(sv[4 * i + 2]) * m0.x, rs_b, m0.y);
+                    float u3 = fmaf(__uint_as_float(sv[4 * i + 3]) * m1.x, rs_b, m1.y);
+                    if (!full) {
+                        const bool va0 = kSparse ? lim_a >= 0 : key0 + k0 <= lim_a;
+                        const bool va1 = kSparse ? lim_a >= 0 : key0 + k0 + 1 <= lim_a;
+                        const bool vb0 = kSparse ? lim_b >= 0 : key0 + k0 <= lim_b;
+                        const bool vb1 = kSparse ? lim_b >= 0 : key0 + k0 + 1 <= lim_b;
+                        u0 = va0 ? u0 : -INFINITY;
+                        u1 = va1 ? u1 : -INFINITY;
+                        u2 = vb0 ? u2 : -INFINITY;
+                        u3 = vb1 ? u3 : -INFINITY;
+                    }
+                    sv[4 * i + 0] = __float_as_uint(u0);
+                    sv[4 * i + 1] = __float_as_uint(u1);
+                    sv[4 * i + 2] = __float_as_uint(u2);
+                    sv[4 * i + 3] = __float_as_uint(u3);
+                    mx_a = fmaxf(mx_a, fmaxf(u0, u1));
+                    mx_b = fmaxf(mx_b, fmaxf(u2, u3));
                 }
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                // ---- reference max: moves (and O is rescaled) only when it grows by > 2^8 ----
-                float alpha = 1.f;
-                bool rescale = false;
+                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+                // ---- reference maxima: move (and O is rescaled) only when they grow by > 2^8 ----
+                float al_a = 1.f, al_b = 1.f;
+                bool resc = false;
                 if (j == 0) {
-                    m_ref = mx;
-                } else if (mx > m_ref + kRescaleThreshold) {
-                    alpha = fast_exp2(m_ref - mx);
-                    m_ref = mx;
-                    rescale = true;
+                    m_a = mx_a;
+                    m_b = mx_b;
+                } else {
+                    if (mx_a > m_a + kRescaleThreshold) {
+                        al_a = fast_exp2(m_a - mx_a);
+                        m_a = mx_a;
+                        resc = true;
+                    }
+                    if (mx_b > m_b + kRescaleThreshold) {
+                        al_b = fast_exp2(m_b - mx_b);
+                        m_b = mx_b;
+                        resc = true;
+                    }
                 }
-                const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-                float ls = 0.f;
+                const float mu_a = m_a == -INFINITY ? 0.f : m_a, mu_b = m_b == -INFINITY ? 0.f : m_b;
+                l_a *= al_a;
+                l_b *= al_b;
                 uint32_t pk[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float p0 = fast_exp2(__uint_as_float(sv[2 * i]) - mu);
-                    const float p1 = fast_exp2(__uint_as_float(sv[2 * i + 1]) - mu);
-                    const float4 k0 = *reinterpret_cast<const float4 *>(&meta[2 * i]);
-                    const float4 k1 = *reinterpret_cast<const float4 *>(&meta[2 * i + 1]);
-                    ls = fmaf(p0, k0.z, fmaf(p1, k1.z, ls));
-                    pk[i] = pack_half2(p0, p1);
+                for (int i = 0; i < 16; ++i) {
+                    const int k0 = 8 * i + 2 * tc;
+                    const float i0 = meta[k0].isig, i1 = meta[k0 + 1].isig;
+                    const float p0 = fast_exp2(__uint_as_float(sv[4 * i + 0]) - mu_a);
+                    const float p1 = fast_exp2(__uint_as_float(sv[4 * i + 1]) - mu_a);
+                    const float p2 = fast_exp2(__uint_as_float(sv[4 * i + 2]) - mu_b);
+                    const float p3 = fast_exp2(__uint_as_float(sv[4 * i + 3]) - mu_b);
+                    l_a = fmaf(p0, i0, fmaf(p1, i1, l_a));
+                    l_b = fmaf(p2, i0, fmaf(p3, i1, l_b));
+                    pk[2 * i] = pack_half2(p0, p1);
+                    pk[2 * i + 1] = pack_half2(p2, p3);
                 }
-                ls += __shfl_xor_sync(0xffffffffu, ls, 16);
-                l_sum = fmaf(l_sum, alpha, ls);
                 // ---- the previous PV must be done before O is touched or P overwritten ----
                 if (j > 0) {
-                    if (!(ok = wait(B_PV_DONE, ph_pv_done))) break;
-                    ph_pv_done ^= 1;
+                    if (!(ok = wait(B_PV_DONE, (t - 1) & 1))) break;
                     fence_after_sync();
                 }
-                if (__any_sync(0xffffffffu, rescale)) {
+                if (__any_sync(0xffffffffu, resc)) {
+                    // 32x32b view: lane L holds row 16q + L%16, half L/16; its factor lives in
+                    // thread 4 (L%8) as row a (L%16 < 8) or row b
+                    const int rr = lane & 15;
+                    const float xa = __shfl_sync(0xffffffffu, al_a, 4 * (rr & 7));
+                    const float xb = __shfl_sync(0xffffffffu, al_b, 4 * (rr & 7));
+                    const float al = rr < 8 ? xa : xb;
 #pragma unroll 1
                     for (int c0 = 0; c0 < 256; c0 += 16) {
                         uint32_t o[16];
                         tmem_ld16(tmem + lane_addr + kColO + c0, o);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al);
                         tmem_st16(tmem + lane_addr + kColO + c0, o);
                     }
                 }
-                // ---- P for all 128 keys into this thread's own lane (both halves hold a copy) ----
-                uint32_t full[64];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const uint32_t other = __shfl_xor_sync(0xffffffffu, pk[i], 16);
-                    full[i] = lo ? pk[i] : other;
-                    full[32 + i] = lo ? other : pk[i];
-                }
-#pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 16) {
-                    uint32_t t[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) t[i] = full[c0 + i];
-                    tmem_st16(tmem + lane_addr + kColP + c0, t);
-                }
+                // ---- P into both lane halves (A operand of the two PV halves) ----
+                tmem_st_16x128b_x16(tmem + lane_addr + kColP, pk);
+                tmem_st_16x128b_x16(tmem + lane_addr + kHalf1 + kColP, pk);
                 tmem_st_wait();
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_P_FULL]));
             }
             if (!ok) break;
-            // ---- epilogue: O / l to bf16, lse ----
-            if (!(ok = wait(B_PV_DONE, ph_pv_done))) break;
-            ph_pv_done ^= 1;
+            // ---- epilogue: O 2^8 / l to bf16, lse ----
+            if (!(ok = wait(B_PV_DONE, (t - 1) & 1))) break;
             fence_after_sync();
-            const bool valid = row < rt.nvalid && lim >= 0;
-            const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-            __nv_bfloat16 *dst = a.out + (rt.grow0 + row) * kDv + (lo ? 0 : 256);
+            l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+            l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+            l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+            l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+            if (tc == 0 && a.lse) {
+                if (ra < rt.nvalid && lim_a >= 0)
+                    a.lse[rt.grow0 + ra] = l_a > 0.f ? (m_a + __log2f(l_a)) * kLn2 : -INFINITY;
+                if (rb < rt.nvalid && lim_b >= 0)
+                    a.lse[rt.grow0 + rb] = l_b > 0.f ? (m_b + __log2f(l_b)) * kLn2 : -INFINITY;
+            }
+            const int rr = lane & 15, row = 16 * q + rr;
+            const float ia = l_a > 0.f ? kCodeScale / l_a : 0.f, ib = l_b > 0.f ? kCodeScale / l_b : 0.f;
+            const float xa = __shfl_sync(0xffffffffu, ia, 4 * (rr & 7));
+            const float xb = __shfl_sync(0xffffffffu, ib, 4 * (rr & 7));
+            const float inv = rr < 8 ? xa : xb;
+            const bool valid = row < rt.nvalid && sh.rowlimit[r & 1][row] >= 0;
+            __nv_bfloat16 *dst = a.out + (rt.grow0 + row) * kDv + (lane < 16 ? 0 : 256);
 #pragma unroll 1
             for (int c0 = 0; c0 < 256; c0 += 32) {
                 uint32_t o[32];
@@ -575,8 +654,6 @@ __global__ void __launch_bounds__(NT, 1) attn_kernel(const AttnArgs a, const int
                     }
                 }
             }
-            if (valid && lo && a.lse)
-                a.lse[rt.grow0 + row] = l_sum > 0.f ? (m_ref + __log2f(l_sum)) * kLn2 : -INFINITY;
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_O_FREE]));
