@@ -1,51 +1,57 @@
 // MLA prefill attention on the 5th-generation tensor cores (tcgen05 + TMEM).
 //
 // One CTA owns a tile of 64 query rows (row = (token, head); for 64 heads one
-// token) and streams the latent rows of the paged e4m3 cache 128 keys at a
-// time. Per key tile:
+// token) and streams the latent rows of the paged e4m3 cache 80 keys at a
+// time. Per key tile t:
 //
-//   S   = Q K'^T         tcgen05.mma kind::f16, M=64 N=128, K=576, D in TMEM
-//   u   = S*sigma'*rowscale + log2(sigma)       (log2 domain, sigma folded in)
+//   S   = Q K'^T         tcgen05.mma kind::f16, M=64 N=80, K=576; A = Q in TMEM
+//   u   = S*sigma'*rowscale + log2(sigma)        (log2 domain, sigma folded in)
 //   P   = 2^(u - m),  l += P / sigma             (m: running reference max)
-//   O  += P V'           tcgen05.mma M=64 N=256 (two Dv halves), A=P from TMEM
+//   O  += P V'           M=64 N=128 x 4 chunks of the 512 value dims, A = P in smem
 //
 // and at the end out = 2^8 O / l, lse = ln2 (m + log2 l). K' and V' hold the
 // e4m3 codes times 2^-8: the f16 bit pattern of that product is the code's own
 // bits moved into place (see f16x2_of_e4m3x2), so dequantisation costs three
 // integer operations per code pair and sigma' = 2^8 sigma restores the scale.
 //
-// Why 64 rows: with the 512-wide value head an fp32 O for 128 rows fills all
-// 512 TMEM columns, and a 128 x 576 f16 Q tile alone is 144 KB of shared
-// memory. With 64 rows, O takes two lane-halves x 256 columns and Q 72 KB.
-// M=64 MMAs run at half the M=128 rate on this part (2048 vs 4096 MAC/clk per
-// SM, measured), so this kernel is capped at half the dense tensor peak per
-// clock.
+// Shapes and the memory budget. An fp32 O for 64 rows x 512 dims fills one
+// TMEM lane half (lanes 16..31 of each 32-lane quadrant, 512 columns); Q
+// (64 rows x 576 f16 = 288 columns) and the two score tiles share the other
+// half, so shared memory holds only key slices and P. M=64 MMAs run at half
+// the M=128 rate (2048 MAC/clk per SM) and take at least ~45 clocks each, so
+// N=80 keys is the smallest tile whose QK runs at 90% of that rate while
+// leaving room for the ring of key slices below (measured on this part).
 //
 // TMEM (M=64 layout: row r lives in lane 32*(r/16) + r%16 + 16*h; h = lane half)
-//   cols   0..255 h=0 : O for value dims   0..255
-//   cols   0..255 h=1 : O for value dims 256..511
-//   cols 256..383 h=0 : S (128 keys)
-//   cols 384..447 h=0 / h=1 : P (128 keys as f16 pairs), one copy per half
+//   h=0 cols   0..287 : Q (576 dims as f16 pairs)
+//   h=0 cols 288..367 : S buffer 0,  cols 368..447 : S buffer 1
+//   h=1 cols   0..511 : O
 //
-// Shared memory (1024-B aligned, 128B-swizzled K-major operand layouts)
-//   Q  : 9 slices x [64 rows][64 dims] f16   (72 KB)
-//   K  : 9 slices x [128 keys][64 dims] f16  (144 KB); slices 0..7 double as V
-//        (MN-major B operand of PV), slice 8 holds the RoPE dims
+// Shared memory
+//   18 nope slots x [80 keys][64 dims] f16, 128B-swizzled K-major (10 KB each):
+//      a FIFO ring; key tile t's slice s (dims 64s..64s+63) sits in slot
+//      (8t + s) mod 18, so slices 2c, 2c+1 always share a slot pair and serve as
+//      the N=128 MN-major B operand of PV chunk c
+//   2 RoPE slots (slice 8 of tiles t, t+1)
+//   2 P buffers [64 rows][80 keys] f16, K-major without swizzle (8x16-B core
+//      matrices; 128 B apart along the keys, 1280 B apart along the rows)
 //
-// Warps: 0-3 softmax/correction (warp w owns TMEM lane quadrant w and reads S
-// with the 16-lane shapes, so each thread holds two rows x 32 keys), 4-7
-// loaders (one key per thread: the raw e4m3 bytes of the next key tile are
-// fetched into registers while the current one is converted into the
-// swizzled K slices), 8 MMA issue, 9-11 idle. Launched at 168 registers a
-// thread, the softmax and loader warpgroups grow to 200 and 232 while the
-// issuer's warpgroup shrinks to 56 (128 x (200 + 232 + 56) <= 384 x 168).
-// The K tile is single-buffered but recycled
-// slice-group by slice-group: slice 8 is refilled as soon as QK has used it
-// (and the next tile's RoPE part of QK runs while the softmax works), slices
-// 0-3 after the first PV half, slices 4-7 after the second. Every wait is
-// bounded; a wait that runs out sets MLA_DEVERR_TIMEOUT and the CTA abandons
-// its tile.
+// Warps: 0-3 softmax/correction (warp w owns TMEM quadrant w and reads S with
+// the 16-lane shapes, so each thread holds rows 16w + l/4 and 16w + l/4 + 8 x
+// 20 keys; the same warps prescale Q into TMEM and run the epilogue), 4-6
+// and 8-9 loaders (16 keys each, four lanes per 64-byte slice row; the raw
+// e4m3 bytes of the next tile are fetched into registers while the current
+// one is converted), 7 MMA issue (warp w is
+// scheduled on sub-partition w % 4, so the issuer shares its scheduler with no
+// loader), 10-11 idle.
+//
+// Tensor-core order: QK(t+1) is issued before PV(t), so the softmax of tile t
+// overlaps QK(t+1), and the ring lets the loaders fill tile t+2 while tiles t
+// and t+1 are in use. Every wait is bounded; a wait that runs out sets
+// MLA_DEVERR_TIMEOUT and the CTA abandons its tile.
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -56,47 +62,54 @@ namespace tcattn {
 
 using namespace tc;
 
-constexpr int BM = 64;            // query rows per CTA tile
-constexpr int BN = 128;           // keys per tile
-constexpr int NSLICE = 9;         // 576 / 64
-constexpr int NT = 384;           // 12 warps = 3 warpgroups
-constexpr int kQSlice = BM * 128;         // 8192 B
-constexpr int kKSlice = BN * 128;         // 16384 B
-constexpr int kSmemQ = NSLICE * kQSlice;  // 73728
-constexpr int kSmemK = NSLICE * kKSlice;  // 147456
-constexpr int kDynSmem = 1024 + kSmemQ + kSmemK;
+constexpr int BM = 64;              // query rows per CTA tile
+constexpr int BN = 80;              // keys per tile
+constexpr int NT = 384;             // 12 warps
+constexpr int kLoaders = 5;         // loader warps: 4, 5, 6, 8, 9
+constexpr int kIssuerWarp = 7;      // the only busy warp on its scheduler besides softmax warp 3
+
+// Warp w runs on scheduler w % 4; the issuer's scheduler gets no loader warp.
+__device__ __forceinline__ bool is_loader(int warp) { return warp == 4 || warp == 5 || warp == 6 || warp == 8 || warp == 9; }
+__device__ __forceinline__ int loader_index(int warp) { return warp < 7 ? warp - 4 : warp - 5; }
+constexpr int kSlot = BN * 128;     // one 64-dim slice of a key tile: 10240 B
+constexpr int kNopeSlots = 18;      // ring of nope slices (2.25 tiles)
+constexpr int kPairs = kNopeSlots / 2;
+constexpr int kPBuf = BM * BN * 2;  // 10240 B
+constexpr int kOffRope = kNopeSlots * kSlot;
+constexpr int kOffP = kOffRope + 2 * kSlot;
+constexpr int kDynSmem = 1024 + kOffP + 2 * kPBuf;
 constexpr long long kWaitCycles = 200000000LL;   // ~0.1 s: every wait here covers at most one tile of work
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 constexpr float kCodeScale = 256.0f;       // K', V' hold code * 2^-8
-constexpr uint32_t kRegsSoftmax = 200, kRegsLoader = 232, kRegsIssuer = 56;   // per-thread budgets after the split
-static_assert(128 * (kRegsSoftmax + kRegsLoader + kRegsIssuer) <= NT * 168, "register split exceeds the launch pool");
 
 // TMEM columns
-constexpr uint32_t kColO = 0, kColS = 256, kColP = 384;
+constexpr uint32_t kColQ = 0, kColS = 288, kColO = 0;
 constexpr uint32_t kHalf1 = 16u << 16;     // lane offset of the upper half
 
 enum Bar {
-    B_FULL_ROPE, B_FULL_A, B_FULL_B,    // loaders -> issuer: K slices converted (8 | 0-3 | 4-7)
-    B_FREE_A, B_FREE_B,                 // issuer (MMA commit) -> loaders: V slices consumed by PV
-    B_S_FULL,                           // issuer -> softmax, loaders: QK complete (S ready, slice 8 and Q reusable)
-    B_S_FREE,                           // softmax -> issuer: S read out
-    B_P_FULL,                           // softmax -> issuer: P written (and O rescaled)
-    B_PV_DONE,                          // issuer -> softmax: PV of the tile complete
-    B_Q_FULL,                           // loaders -> issuer, softmax: Q tile and row data in smem
-    B_O_FREE,                           // softmax -> issuer: epilogue finished reading O
-    B_FINAL,                            // issuer -> all: every MMA of the CTA complete
-    B_META0, B_META1,                   // loaders -> softmax: key metadata of tile n, n&1
-    NBAR
+    B_FULL_ROPE = 0,                    // [2]  loaders -> issuer: RoPE slot b converted
+    B_FULL_PAIR = 2,                    // [9]  loaders -> issuer: nope slot pair converted
+    B_FREE_PAIR = 11,                   // [9]  issuer (commit) -> loaders: PV chunk done with the pair
+    B_S_FULL = 20,                      // [2]  issuer (commit) -> softmax, loaders: QK of the tile complete
+    B_S_FREE = 22,                      // [2]  softmax -> issuer: S buffer read out
+    B_P_FULL = 24,                      // [2]  softmax -> issuer: P buffer written (and O rescaled)
+    B_PV_DONE = 26,                     // [2]  issuer (commit) -> softmax: PV of the tile complete
+    B_META = 28,                        // [4]  loaders -> softmax: key metadata of tile t, t&3
+    B_Q_FULL = 32,                      //      softmax -> issuer: Q of the row tile in TMEM
+    B_O_FREE = 33,                      //      softmax -> issuer: epilogue finished reading O
+    B_FINAL = 34,                       //      issuer -> teardown: every MMA complete
+    NBAR = 35
 };
 
+// Per-key data of a key tile, by key pair p (keys 2p, 2p+1): what the
+// softmax thread owning those keys reads in one 16-byte and one 8-byte load.
 struct __align__(16) KeyMeta {
-    float sig, lsig, isig, pad;          // 2^8 sigma, log2 sigma (-inf = masked), 1/sigma
+    float4 sl[BN / 2];                   // 2^8 sigma of both keys, log2 sigma of both (-inf = masked)
+    float2 isig[BN / 2];                 // 1/sigma of both
 };
 
 struct Shared {
-    KeyMeta meta[4][BN];                 // per key tile, ring of 4
-    float rowscale[2][BM];               // sm_scale*log2e / query prescale, per row tile parity
-    int32_t rowlimit[2][BM];             // last visible position (dense); -1 = invalid row
+    KeyMeta meta[4];                     // per key tile, ring of 4
     uint64_t bar[NBAR];
     uint32_t tmem_base;
     int32_t abort;
@@ -106,6 +119,8 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in
     return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// Bounded wait, entered by every lane of the calling warp. A wait that runs
+// out sets MLA_DEVERR_TIMEOUT and the sticky `abort` flag.
 struct Wait {
     Shared *sh;
     int32_t *dev_err;
@@ -152,60 +167,16 @@ __device__ __forceinline__ RowTile make_tile(const AttnArgs &a, int b, int tile,
     return rt;
 }
 
-// ---------------------------------------------------------------------------
-// loaders (warps 4-7): Q tile, per-key metadata, e4m3 -> f16 K slices
-// ---------------------------------------------------------------------------
+// Last key position visible to query row `row` of the tile (-1: invalid row).
 template <bool kSparse>
-__device__ void load_q(const AttnArgs &a, Shared &sh, uint8_t *sq, const RowTile &rt, int b, int rt_par, int lt) {
-    // lt in 0..127: two threads per row (row = lt/2), each 36 of the 72 16-B chunks;
-    // pass 1 finds the row maximum, pass 2 re-reads (cache hits), scales and stores.
-    const int row = lt >> 1, half = lt & 1;
-    const bool ok = row < rt.nvalid;
-    const uint4 *src = reinterpret_cast<const uint4 *>(a.q + (rt.grow0 + (ok ? row : 0)) * kDqk) + half * 36;
-    float mx = 0.f;
-    if (ok) {
-#pragma unroll 6
-        for (int i = 0; i < 36; ++i) {
-            const uint4 v = __ldg(src + i);
-            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 f = __bfloat1622float2(h[j]);
-                mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
-            }
-        }
-    }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    int e = 0;
-    if (mx > 0.f) frexpf(mx, &e);
-    const float scale = mx > 0.f ? ldexpf(1.f, 1 - e) : 1.f;
-#pragma unroll 6
-    for (int i = 0; i < 36; ++i) {
-        const int c = half * 36 + i;           // 16-B chunk of the row (8 dims)
-        const int slice = c >> 3, chunk = c & 7;
-        const uint4 v = ok ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
-        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 f = __bfloat1622float2(h[j]);
-            w[j] = pack_half2(f.x * scale, f.y * scale);
-        }
-        *reinterpret_cast<uint4 *>(sq + slice * kQSlice + swz(row, chunk)) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    if (half == 0) {
-        sh.rowscale[rt_par][row] = a.sm_scale_log2 / scale;
-        if (kSparse) {
-            sh.rowlimit[rt_par][row] = ok ? rt.qpos : -1;
-        } else {
-            const int P = __ldg(a.prefix_lens + b);
-            const int r_lo = static_cast<int>(rt.grow0 - static_cast<int64_t>(__ldg(a.cu_seqlens + b)) * a.H);
-            sh.rowlimit[rt_par][row] = ok ? P + (r_lo + row) / a.H : -1;
-        }
-    }
+__device__ __forceinline__ int row_limit(const AttnArgs &a, const RowTile &rt, int b, int row) {
+    if (row >= rt.nvalid) return -1;
+    if (kSparse) return rt.qpos;
+    const int r_lo = static_cast<int>(rt.grow0 - static_cast<int64_t>(__ldg(a.cu_seqlens + b)) * a.H);
+    return __ldg(a.prefix_lens + b) + (r_lo + row) / a.H;
 }
 
-// Cache row of key k (0..127) of key tile j (-1: no key) and its scale.
+// Cache row of key k of key tile j (-1: no key) and its scale.
 template <bool kSparse>
 __device__ __forceinline__ int64_t key_row(const AttnArgs &a, const int32_t *bt, const RowTile &rt, int j, int k,
                                            float &sig) {
@@ -226,21 +197,11 @@ __device__ __forceinline__ int64_t key_row(const AttnArgs &a, const int32_t *bt,
     return row;
 }
 
-__device__ __forceinline__ void write_meta(KeyMeta &m, int64_t row, float sig) {
-    m.sig = sig * kCodeScale;
-    m.lsig = row >= 0 ? __log2f(sig) : -INFINITY;
-    m.isig = 1.f / sig;
-}
-
-// Raw e4m3 bytes of slices s0..s0+NS-1 (64 dims each) of one cache row.
-template <int NS>
-__device__ __forceinline__ void fetch_slices(const uint8_t *kv, int64_t row, int s0, uint4 *raw) {
-#pragma unroll
-    for (int s = 0; s < NS; ++s)
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            raw[4 * s + i] = row >= 0 ? __ldg(reinterpret_cast<const uint4 *>(kv + row * kDqk + (s0 + s) * 64) + i)
-                                      : make_uint4(0, 0, 0, 0);
+__device__ __forceinline__ void write_meta(KeyMeta &m, int k, int64_t row, float sig) {
+    float *sl = reinterpret_cast<float *>(&m.sl[k >> 1]);
+    sl[k & 1] = sig * kCodeScale;
+    sl[2 + (k & 1)] = row >= 0 ? __log2f(sig) : -INFINITY;
+    reinterpret_cast<float *>(&m.isig[k >> 1])[k & 1] = 1.f / sig;
 }
 
 // Two e4m3 codes (bytes 0 and 2 of t, bytes 1 and 3 zero) -> f16x2 of code * 2^-8,
@@ -252,33 +213,93 @@ __device__ __forceinline__ void fetch_slices(const uint8_t *kv, int64_t row, int
 // never hold them.
 __device__ __forceinline__ uint32_t f16x2_of_e4m3x2(uint32_t t) { return (t + (t & 0x00800080u)) << 7; }
 
-template <int NS>
-__device__ __forceinline__ void store_slices(uint8_t *sk, int k, int s0, const uint4 *raw) {
+// Converts NC 16-byte chunks (16 dims each, starting at chunk c0) of key k
+// into the swizzled f16 slice at dst.
+template <int NC>
+__device__ __forceinline__ void store_chunks(uint8_t *dst, int k, int c0, const uint4 *raw) {
 #pragma unroll
-    for (int s = 0; s < NS; ++s) {
-        uint8_t *dst = sk + (s0 + s) * kKSlice;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 r = raw[4 * s + i];
-            uint32_t h[8];
-            h[0] = f16x2_of_e4m3x2(__byte_perm(r.x, 0u, 0x4140u));
-            h[1] = f16x2_of_e4m3x2(__byte_perm(r.x, 0u, 0x4342u));
-            h[2] = f16x2_of_e4m3x2(__byte_perm(r.y, 0u, 0x4140u));
-            h[3] = f16x2_of_e4m3x2(__byte_perm(r.y, 0u, 0x4342u));
-            h[4] = f16x2_of_e4m3x2(__byte_perm(r.z, 0u, 0x4140u));
-            h[5] = f16x2_of_e4m3x2(__byte_perm(r.z, 0u, 0x4342u));
-            h[6] = f16x2_of_e4m3x2(__byte_perm(r.w, 0u, 0x4140u));
-            h[7] = f16x2_of_e4m3x2(__byte_perm(r.w, 0u, 0x4342u));
-            *reinterpret_cast<uint4 *>(dst + swz(k, 2 * i)) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4 *>(dst + swz(k, 2 * i + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
-        }
+    for (int c = 0; c < NC; ++c) {
+        const int i = c0 + c;
+        const uint4 r = raw[c];
+        uint32_t h[8];
+        h[0] = f16x2_of_e4m3x2(__byte_perm(r.x, 0u, 0x4140u));
+        h[1] = f16x2_of_e4m3x2(__byte_perm(r.x, 0u, 0x4342u));
+        h[2] = f16x2_of_e4m3x2(__byte_perm(r.y, 0u, 0x4140u));
+        h[3] = f16x2_of_e4m3x2(__byte_perm(r.y, 0u, 0x4342u));
+        h[4] = f16x2_of_e4m3x2(__byte_perm(r.z, 0u, 0x4140u));
+        h[5] = f16x2_of_e4m3x2(__byte_perm(r.z, 0u, 0x4342u));
+        h[6] = f16x2_of_e4m3x2(__byte_perm(r.w, 0u, 0x4140u));
+        h[7] = f16x2_of_e4m3x2(__byte_perm(r.w, 0u, 0x4342u));
+        *reinterpret_cast<uint4 *>(dst + swz(k, 2 * i)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(dst + swz(k, 2 * i + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
     }
 }
-
-// (row tile, key tile) -> next (row tile, key tile) in the CTA's visiting order
-struct Cursor {
-    int r, j, n;        // row tile, key tile, key tiles of row tile r
+// The CTA's key tiles in visiting order: global index t -> (row tile, key tile).
+struct Walk {
+    int n0, total;      // key tiles of row tile 0, of both
+    __device__ int r(int t) const { return t < n0 ? 0 : 1; }
+    __device__ int j(int t) const { return t < n0 ? t : t - n0; }
 };
+
+// ---------------------------------------------------------------------------
+// softmax-warp pieces
+// ---------------------------------------------------------------------------
+// Q rows ra, rb of the tile -> f16 (times a power-of-two row scale) in TMEM
+// columns 0..287 of lane half 0 (16x256b layout: column group i holds dims
+// 16i + 4tc .. +3 of this thread's rows); returns sm_scale*log2e / scale.
+__device__ __forceinline__ void load_q_tmem(const AttnArgs &a, const RowTile &rt, uint32_t tq_addr, int ra, int rb,
+                                            int tc, float &rs_a, float &rs_b) {
+    const bool oka = ra < rt.nvalid, okb = rb < rt.nvalid;
+    const __nv_bfloat16 *qa = a.q + (rt.grow0 + (oka ? ra : 0)) * kDqk + 4 * tc;
+    const __nv_bfloat16 *qb = a.q + (rt.grow0 + (okb ? rb : 0)) * kDqk + 4 * tc;
+    float mxa = 0.f, mxb = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < 36; ++i) {
+        const uint2 va = oka ? __ldg(reinterpret_cast<const uint2 *>(qa + 16 * i)) : make_uint2(0, 0);
+        const uint2 vb = okb ? __ldg(reinterpret_cast<const uint2 *>(qb + 16 * i)) : make_uint2(0, 0);
+        const __nv_bfloat162 *ha = reinterpret_cast<const __nv_bfloat162 *>(&va);
+        const __nv_bfloat162 *hb = reinterpret_cast<const __nv_bfloat162 *>(&vb);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float2 fa = __bfloat1622float2(ha[e]), fb = __bfloat1622float2(hb[e]);
+            mxa = fmaxf(mxa, fmaxf(fabsf(fa.x), fabsf(fa.y)));
+            mxb = fmaxf(mxb, fmaxf(fabsf(fb.x), fabsf(fb.y)));
+        }
+    }
+    mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
+    mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
+    mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
+    mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
+    int ea = 0, eb = 0;
+    if (mxa > 0.f) frexpf(mxa, &ea);
+    if (mxb > 0.f) frexpf(mxb, &eb);
+    const float sa = mxa > 0.f ? ldexpf(1.f, 1 - ea) : 1.f, sb = mxb > 0.f ? ldexpf(1.f, 1 - eb) : 1.f;
+    rs_a = a.sm_scale_log2 / sa;
+    rs_b = a.sm_scale_log2 / sb;
+#pragma unroll 1
+    for (int g0 = 0; g0 < 36; g0 += 8) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int g = g0 + i;
+            uint2 va = make_uint2(0, 0), vb = make_uint2(0, 0);
+            if (g < 36) {
+                if (oka) va = __ldg(reinterpret_cast<const uint2 *>(qa + 16 * g));
+                if (okb) vb = __ldg(reinterpret_cast<const uint2 *>(qb + 16 * g));
+            }
+            const __nv_bfloat162 *ha = reinterpret_cast<const __nv_bfloat162 *>(&va);
+            const __nv_bfloat162 *hb = reinterpret_cast<const __nv_bfloat162 *>(&vb);
+            const float2 a0 = __bfloat1622float2(ha[0]), a1 = __bfloat1622float2(ha[1]);
+            const float2 b0 = __bfloat1622float2(hb[0]), b1 = __bfloat1622float2(hb[1]);
+            w[4 * i + 0] = pack_half2(a0.x * sa, a0.y * sa);
+            w[4 * i + 1] = pack_half2(a1.x * sa, a1.y * sa);
+            w[4 * i + 2] = pack_half2(b0.x * sb, b0.y * sb);
+            w[4 * i + 3] = pack_half2(b1.x * sb, b1.y * sb);
+        }
+        if (g0 + 8 <= 36) tmem_st_16x256b_x8(tq_addr + 8 * g0, w);
+        else tmem_st_16x256b_x4(tq_addr + 8 * g0, w);
+    }
+}
 
 // ---------------------------------------------------------------------------
 // the kernel
@@ -289,9 +310,8 @@ __global__ void __launch_bounds__(NT, 1) attn_kernel(const AttnArgs a, const int
     __shared__ Shared sh;
     const uint32_t raw = smem_u32(dsm);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-    uint8_t *sq = dsm + pad;
-    uint8_t *sk = sq + kSmemQ;
-    const uint32_t sq_a = raw + pad, sk_a = sq_a + kSmemQ;
+    uint8_t *sbase = dsm + pad;
+    const uint32_t sbase_a = raw + pad;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ----- the row tiles of this CTA -----
@@ -316,19 +336,23 @@ __global__ void __launch_bounds__(NT, 1) attn_kernel(const AttnArgs a, const int
     }
     const int n_rt = tiles[1] >= 0 ? 2 : 1;
     const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.max_blocks;
+    Walk walk;
+    walk.n0 = make_tile<kSparse>(a, b, tiles[0], sp_tok, sp_h0).n_ktiles;
+    walk.total = walk.n0 + (n_rt > 1 ? make_tile<kSparse>(a, b, tiles[1], sp_tok, sp_h0).n_ktiles : 0);
 
     if (tid == 0) {
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
-            if (i == B_FULL_ROPE || i == B_FULL_A || i == B_FULL_B || i == B_Q_FULL || i == B_META0 || i == B_META1)
-                cnt = 4;                                                                          // 4 loader warps
-            if (i == B_S_FREE || i == B_P_FULL || i == B_O_FREE) cnt = 4;                      // 4 softmax warps
+            if (i < B_FREE_PAIR || (i >= B_META && i < B_META + 4)) cnt = kLoaders;     // FULL_ROPE, FULL_PAIR, META
+            if ((i >= B_S_FREE && i < B_S_FREE + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) || i == B_Q_FULL ||
+                i == B_O_FREE)
+                cnt = 4;                                                                  // softmax warps
             mbar_init(smem_u32(&sh.bar[i]), cnt);
         }
         sh.abort = 0;
         mbar_fence_init();
     }
-    if (warp == 8) {
+    if (warp == kIssuerWarp) {
         tmem_alloc(smem_u32(&sh.tmem_base), 512);
         tmem_relinquish();
     }
@@ -338,214 +362,246 @@ __global__ void __launch_bounds__(NT, 1) attn_kernel(const AttnArgs a, const int
     const uint32_t tmem = sh.tmem_base;
     const Wait wait{&sh, a.dev_err};
 
-    if (warp >= 4 && warp < 8) {
+    if (is_loader(warp)) {
         // =================== loaders ===================
-        regs_inc<kRegsLoader>();
+        // Loader warp w covers keys 16w..16w+15 of a tile as two groups of 8;
+        // lane l holds 16-byte chunk l%4 of one 64-dim slice row of key
+        // 16w + 8g + l/4, so every warp-wide load reads 8 rows x 64 contiguous
+        // bytes and every swizzled 16-byte store of 8 rows is conflict-free.
         // Tile t's raw bytes are in registers when iteration t starts; each
-        // group is converted once its slots are free and the same group of
-        // tile t+1 is fetched right after, a whole tile ahead of its use.
-        const int lt = tid - 128;              // key index within a tile
+        // part is converted once its slot is free and the same part of tile t+1
+        // is fetched right after.
+        const int kq = 16 * loader_index(warp) + (lane >> 2), jc = lane & 3;   // key of group 0, chunk
         RowTile rt = make_tile<kSparse>(a, b, tiles[0], sp_tok, sp_h0);
-        Cursor cur{0, 0, rt.n_ktiles};
-        RowTile rt_next = rt;
-        uint4 r_rope[4], r_a[16], r_b[16];
-        float sig;
-        int64_t row = key_row<kSparse>(a, bt, rt, 0, lt, sig);
-        write_meta(sh.meta[0][lt], row, sig);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_META0]));
-        fetch_slices<1>(a.kv, row, 8, r_rope);
-        fetch_slices<4>(a.kv, row, 0, r_a);
-        fetch_slices<4>(a.kv, row, 4, r_b);
-        load_q<kSparse>(a, sh, sq, rt, b, 0, lt);
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_Q_FULL]));
-        for (int t = 0;; ++t) {
-            // ---- slice 8: free once the previous tile's QK is complete (that also frees Q) ----
-            if (t > 0) {
-                if (!wait(B_S_FULL, (t - 1) & 1)) break;
-                if (cur.j == 0) {
-                    load_q<kSparse>(a, sh, sq, rt, b, cur.r & 1, lt);
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_Q_FULL]));
-                }
-            }
-            store_slices<1>(sk, lt, 8, r_rope);
+        uint4 r_rope[2], r_s[4][4];            // [group], [pair][2 * half + group]
+        float sig_cur[2];
+        int64_t row_cur[2];
+        auto fetch = [&](const int64_t (&row)[2], int slice, uint4 *dst, int stride) {
+#pragma unroll
+            for (int g = 0; g < 2; ++g)
+                dst[stride * g] = row[g] >= 0
+                                      ? __ldg(reinterpret_cast<const uint4 *>(a.kv + row[g] * kDqk + slice * 64) + jc)
+                                      : make_uint4(0, 0, 0, 0);
+        };
+#pragma unroll
+        for (int g = 0; g < 2; ++g) row_cur[g] = key_row<kSparse>(a, bt, rt, 0, kq + 8 * g, sig_cur[g]);
+        fetch(row_cur, 8, r_rope, 1);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            fetch(row_cur, 2 * c, &r_s[c][0], 1);
+            fetch(row_cur, 2 * c + 1, &r_s[c][2], 1);
+        }
+        bool ok = true;
+        for (int t = 0; t < walk.total && ok; ++t) {
+            const int rb = t & 1;
+            // ---- RoPE slot rb: free once QK of tile t-2 is complete ----
+            if (t >= 2 && !(ok = wait(B_S_FULL + rb, ((t >> 1) - 1) & 1))) break;
+#pragma unroll
+            for (int g = 0; g < 2; ++g) store_chunks<1>(sbase + kOffRope + rb * kSlot, kq + 8 * g, jc, &r_rope[g]);
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL_ROPE]));
-            // ---- the next tile: metadata now, raw bytes group by group ----
-            Cursor nxt = cur;
-            bool more = true;
-            if (++nxt.j == nxt.n) {
-                nxt.j = 0;
-                if (++nxt.r < n_rt) {
-                    rt_next = make_tile<kSparse>(a, b, tiles[nxt.r], sp_tok, sp_h0);
-                    nxt.n = rt_next.n_ktiles;
-                } else {
-                    more = false;
-                }
-            }
-            int64_t row_n = -1;
+            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL_ROPE + rb]));
+            // ---- the next tile's cache rows and RoPE bytes ----
+            const bool more = t + 1 < walk.total;
+            int64_t row_n[2] = {-1, -1};
+            float sig_n[2] = {1.f, 1.f};
             if (more) {
-                row_n = key_row<kSparse>(a, bt, rt_next, nxt.j, lt, sig);
-                write_meta(sh.meta[(t + 1) & 3][lt], row_n, sig);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[((t + 1) & 1) ? B_META1 : B_META0]));
-                fetch_slices<1>(a.kv, row_n, 8, r_rope);
+                const int tn = t + 1;
+                if (walk.r(tn) != walk.r(t)) rt = make_tile<kSparse>(a, b, tiles[walk.r(tn)], sp_tok, sp_h0);
+#pragma unroll
+                for (int g = 0; g < 2; ++g) row_n[g] = key_row<kSparse>(a, bt, rt, walk.j(tn), kq + 8 * g, sig_n[g]);
+                fetch(row_n, 8, r_rope, 1);
             }
-            // ---- slices 0-3, then 4-7: free after the matching half of the previous PV ----
-            if (t > 0 && !wait(B_FREE_A, (t - 1) & 1)) break;
-            store_slices<4>(sk, lt, 0, r_a);
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL_A]));
-            if (more) fetch_slices<4>(a.kv, row_n, 0, r_a);
-            if (t > 0 && !wait(B_FREE_B, (t - 1) & 1)) break;
-            store_slices<4>(sk, lt, 4, r_b);
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL_B]));
-            if (!more) break;
-            fetch_slices<4>(a.kv, row_n, 4, r_b);
-            cur = nxt;
-            rt = rt_next;
-        }
-    } else if (warp >= 8) {
-        // =================== MMA issuer (warp 8, lane 0) ===================
-        regs_dec<kRegsIssuer>();
-        if (warp == 8 && lane == 0) {
-            const uint32_t id_qk = idesc_f16(BM, BN, false, false, false, false);
-            const uint32_t id_pv = idesc_f16(BM, 256, false, false, false, true);
-            // Descriptors of the operand bases; an operand at byte offset x is the base
-            // descriptor plus x/16 (start-address field; shared addresses stay below 2^18).
-            const uint64_t dq0 = sdesc(sq_a, 16, 1024, kSw128);
-            const uint64_t dk0 = sdesc(sk_a, 16, 1024, kSw128);
-            const uint64_t dv0 = sdesc(sk_a, kKSlice, 1024, kSw128);
-            // QK over one 64-dim slice (4 MMAs of K=16)
-            auto qk_slice = [&](int slice, bool first) {
-                const uint64_t da = dq0 + static_cast<uint64_t>((slice * kQSlice) >> 4);
-                const uint64_t db = dk0 + static_cast<uint64_t>((slice * kKSlice) >> 4);
+            // ---- nope pairs; pair c of tile t uses slot pair (4t + c) mod 9 ----
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_f16_ss(tmem + kColS, da + 2 * ks, db + 2 * ks, id_qk, (first && ks == 0) ? 0u : 1u);
-            };
-            int t = 0;
-            bool rope_issued = false, ok = true;
-            for (int r = 0; r < n_rt && ok; ++r) {
-                const RowTile rt = make_tile<kSparse>(a, b, tiles[r], sp_tok, sp_h0);
-                for (int j = 0; j < rt.n_ktiles && ok; ++j, ++t) {
-                    // ---- S = Q K^T: slice 8 (unless already issued), then 0-3, 4-7 ----
-                    if (!rope_issued) {
-                        if (j == 0 && !(ok = wait(B_Q_FULL, r & 1))) break;
-                        if (!(ok = wait(B_FULL_ROPE, t & 1))) break;
-                        if (t > 0 && !(ok = wait(B_S_FREE, (t - 1) & 1))) break;
-                        fence_after_sync();
-                        qk_slice(8, true);
+            for (int c = 0; c < 4; ++c) {
+                const int qn = 4 * t + c, p = qn % kPairs;
+                if (qn >= kPairs && !(ok = wait(B_FREE_PAIR + p, ((qn / kPairs) - 1) & 1))) break;
+                if (c == 0) {   // the tile's metadata (its ring slot was last read by the softmax of tile t-4)
+                    if (jc == 0) {
+                        write_meta(sh.meta[t & 3], kq, row_cur[0], sig_cur[0]);
+                        write_meta(sh.meta[t & 3], kq + 8, row_cur[1], sig_cur[1]);
                     }
-                    rope_issued = false;
-                    if (!(ok = wait(B_FULL_A, t & 1))) break;
-                    fence_after_sync();
-#pragma unroll 1
-                    for (int s = 0; s < 4; ++s) qk_slice(s, false);
-                    if (!(ok = wait(B_FULL_B, t & 1))) break;
-                    fence_after_sync();
-#pragma unroll 1
-                    for (int s = 4; s < 8; ++s) qk_slice(s, false);
-                    mma_commit(smem_u32(&sh.bar[B_S_FULL]));
-                    // ---- the next tile's RoPE slice while the softmax works on this one ----
-                    if (j + 1 < rt.n_ktiles) {
-                        if (!(ok = wait(B_FULL_ROPE, (t + 1) & 1))) break;
-                        if (!(ok = wait(B_S_FREE, t & 1))) break;
-                        fence_after_sync();
-                        qk_slice(8, true);
-                        rope_issued = true;
-                    }
-                    // ---- O += P V ----
-                    if (j == 0 && r > 0) {
-                        if (!(ok = wait(B_O_FREE, (r - 1) & 1))) break;
-                    }
-                    if (!(ok = wait(B_P_FULL, t & 1))) break;
-                    fence_after_sync();
-#pragma unroll 1
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t lane_off = h ? kHalf1 : 0u;
-                        const uint64_t dv = dv0 + static_cast<uint64_t>((4 * h * kKSlice) >> 4);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_META + (t & 3)]));
+                }
 #pragma unroll
-                        for (int ks = 0; ks < BN / 16; ++ks)
-                            mma_f16_ts(tmem + lane_off + kColO, tmem + lane_off + kColP + ks * 8, dv + 128 * ks, id_pv,
-                                       (j > 0 || ks > 0) ? 1u : 0u);
-                        mma_commit(smem_u32(&sh.bar[h ? B_FREE_B : B_FREE_A]));
-                    }
-                    mma_commit(smem_u32(&sh.bar[B_PV_DONE]));
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int g = 0; g < 2; ++g)
+                        store_chunks<1>(sbase + (2 * p + h) * kSlot, kq + 8 * g, jc, &r_s[c][2 * h + g]);
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL_PAIR + p]));
+                if (more) {
+                    fetch(row_n, 2 * c, &r_s[c][0], 1);
+                    fetch(row_n, 2 * c + 1, &r_s[c][2], 1);
                 }
             }
-            mma_commit(smem_u32(&sh.bar[B_FINAL]));
+            row_cur[0] = row_n[0];
+            row_cur[1] = row_n[1];
+            sig_cur[0] = sig_n[0];
+            sig_cur[1] = sig_n[1];
         }
-        __syncwarp();
-    } else {
+    } else if (warp >= 4) {
+        // =================== MMA issuer (warp 7); warps 10, 11 idle ===================
+        // The whole warp runs the issue loop in lockstep (waits, operand
+        // addresses) and lane 0 alone issues each MMA and commit.
+        if (warp == kIssuerWarp) {
+            const uint32_t lead = lane == 0 ? 1u : 0u;
+            const uint32_t id_qk = idesc_f16(BM, BN, false, false, false, false);
+            const uint32_t id_pv = idesc_f16(BM, 128, false, false, false, true);
+            // descriptors of the bases; an operand at byte offset x is the base plus x/16
+            const uint64_t dk0 = sdesc(sbase_a, 16, 1024, kSw128);           // K-major key slices
+            const uint64_t dv0 = sdesc(sbase_a, kSlot, 1024, kSw128);        // MN-major slot pairs (V)
+            const uint64_t dp0 = sdesc(sbase_a + kOffP, 128, 1280, kSwNone); // P buffers
+            bool ok = true;
+            // QK(t): S buffer t&1 = Q K^T over slice 8 (RoPE), then pairs 0..3
+            auto qk = [&](int t) -> bool {
+                const int sb = t & 1;
+                if (!wait(B_FULL_ROPE + sb, (t >> 1) & 1)) return false;
+                if (t >= 2 && !wait(B_S_FREE + sb, ((t >> 1) - 1) & 1)) return false;
+                fence_after_sync();
+                const uint32_t d = tmem + kColS + BN * sb;
+                {
+                    const uint64_t db = dk0 + static_cast<uint64_t>((kOffRope + sb * kSlot) >> 4);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16_ts_w(d, tmem + kColQ + 32 * 8 + 8 * ks, db + 2 * ks, id_qk, ks > 0 ? 1u : 0u, lead);
+                }
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    const int qn = 4 * t + c, p = qn % kPairs;
+                    if (!wait(B_FULL_PAIR + p, (qn / kPairs) & 1)) return false;
+                    fence_after_sync();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int s = 2 * c + h;
+                        const uint64_t db = dk0 + static_cast<uint64_t>(((2 * p + h) * kSlot) >> 4);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_f16_ts_w(d, tmem + kColQ + 32 * s + 8 * ks, db + 2 * ks, id_qk, 1u, lead);
+                    }
+                }
+                mma_commit_w(smem_u32(&sh.bar[B_S_FULL + sb]), lead);
+                return true;
+            };
+            // PV(t): O += P(t) V(t), four 128-dim chunks, each releasing its slot pair
+            auto pv = [&](int t) -> bool {
+                const int pb = t & 1, j = walk.j(t), r = walk.r(t);
+                if (j == 0 && r > 0 && !wait(B_O_FREE, (r - 1) & 1)) return false;
+                if (!wait(B_P_FULL + pb, (t >> 1) & 1)) return false;
+                fence_after_sync();
+                const uint64_t da = dp0 + static_cast<uint64_t>((pb * kPBuf) >> 4);
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    const int p = (4 * t + c) % kPairs;
+                    const uint64_t dv = dv0 + static_cast<uint64_t>((2 * p * kSlot) >> 4);
+                    const uint32_t d = tmem + kHalf1 + kColO + 128u * c;
+#pragma unroll
+                    for (int ks = 0; ks < BN / 16; ++ks)
+                        mma_f16_ss_w(d, da + 16 * ks, dv + 128 * ks, id_pv, (j > 0 || ks > 0) ? 1u : 0u, lead);
+                    mma_commit_w(smem_u32(&sh.bar[B_FREE_PAIR + p]), lead);
+                }
+                mma_commit_w(smem_u32(&sh.bar[B_PV_DONE + pb]), lead);
+                return true;
+            };
+            if (walk.total > 0) ok = wait(B_Q_FULL, 0) && qk(0);
+            for (int t = 0; t < walk.total && ok; ++t) {
+                const bool more = t + 1 < walk.total;
+                const bool new_rt = more && walk.r(t + 1) != walk.r(t);
+                if (more && !new_rt && !(ok = qk(t + 1))) break;
+                if (!(ok = pv(t))) break;
+                if (new_rt) {
+                    if (!(ok = wait(B_Q_FULL, walk.r(t + 1) & 1))) break;
+                    if (!(ok = qk(t + 1))) break;
+                }
+            }
+            mma_commit_w(smem_u32(&sh.bar[B_FINAL]), lead);
+        }
+    } else if (warp < 4) {
         // =================== softmax / correction (warps 0-3) ===================
-        regs_inc<kRegsSoftmax>();
-        // S is read with the 16-lane shapes: thread t holds rows ra = 16q + t/4
-        // and rb = ra + 8, keys 8i + 2(t%4) + {0,1} for i = 0..15.
         const int q = warp;                        // TMEM lane quadrant
         const int tq = lane >> 2, tc = lane & 3;
         const int ra = 16 * q + tq, rb = ra + 8;
-        const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-        int t = 0;
+        const uint32_t lane_lo = static_cast<uint32_t>(32 * q) << 16;
+        const uint32_t lane_hi = lane_lo + kHalf1;
+        uint8_t *pbuf = sbase + kOffP;
+        // P word (row, keys 8i + 2tc, +1) lives at (row/8)*1280 + i*128 + (row%8)*16 + 4tc
+        const uint32_t poff_a = static_cast<uint32_t>((ra >> 3) * 1280 + (ra & 7) * 16 + 4 * tc);
+        const uint32_t poff_b = static_cast<uint32_t>((rb >> 3) * 1280 + (rb & 7) * 16 + 4 * tc);
         bool ok = true;
+        RowTile rt = make_tile<kSparse>(a, b, tiles[0], sp_tok, sp_h0);
+        float rs_a, rs_b;
+        load_q_tmem(a, rt, tmem + lane_lo + kColQ, ra, rb, tc, rs_a, rs_b);
+        tmem_st_wait();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_Q_FULL]));
+        int t = 0;
         for (int r = 0; r < n_rt && ok; ++r) {
-            const RowTile rt = make_tile<kSparse>(a, b, tiles[r], sp_tok, sp_h0);
             float m_a = -INFINITY, m_b = -INFINITY;  // reference maxima (log2 domain)
-            float l_a = 0.f, l_b = 0.f;              // this thread's partial row sums (32 keys per tile)
-            if (!(ok = wait(B_Q_FULL, r & 1))) break;
-            const float rs_a = sh.rowscale[r & 1][ra], rs_b = sh.rowscale[r & 1][rb];
-            const int lim_a = sh.rowlimit[r & 1][ra], lim_b = sh.rowlimit[r & 1][rb];
+            float l_a = 0.f, l_b = 0.f;              // this thread's partial row sums (20 keys per tile)
+            const int lim_a = row_limit<kSparse>(a, rt, b, ra), lim_b = row_limit<kSparse>(a, rt, b, rb);
             const int lim_min = min(lim_a, lim_b);
             for (int j = 0; j < rt.n_ktiles && ok; ++j, ++t) {
-                if (!(ok = wait((t & 1) ? B_META1 : B_META0, (t >> 1) & 1))) break;
-                if (!(ok = wait(B_S_FULL, t & 1))) break;
+                const int sb = t & 1;
+                if (!(ok = wait(B_META + (t & 3), (t >> 2) & 1))) break;
+                if (!(ok = wait(B_S_FULL + sb, (t >> 1) & 1))) break;
                 fence_after_sync();
-                uint32_t sv[64];
-                tmem_ld_16x256b_x8(tmem + lane_addr + kColS, sv);
-                tmem_ld_16x256b_x8(tmem + lane_addr + kColS + 64, sv + 32);
+                uint32_t sv[40];
+                tmem_ld_16x256b_x8(tmem + lane_lo + kColS + BN * sb, sv);
+                tmem_ld_16x256b_x2(tmem + lane_lo + kColS + BN * sb + 64, sv + 32);
                 tmem_ld_wait();
                 fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_S_FREE]));
-                // ---- logits in the log2 domain, tile maxima ----
-                const KeyMeta *meta = sh.meta[t & 3];
+                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_S_FREE + sb]));
+                // ---- logits u in the log2 domain and tile maxima; for j > 0 also P against
+                // the current reference maxima (kept unless the tile raises one by > 2^8) ----
+                const KeyMeta &meta = sh.meta[t & 3];
                 const int key0 = kSparse ? 0 : j * BN;
                 const bool full = kSparse ? (lim_min >= 0) : (key0 + BN - 1 <= lim_min);
-                float mx_a = -INFINITY, mx_b = -INFINITY;
+                const float mu_a0 = m_a == -INFINITY ? 0.f : m_a, mu_b0 = m_b == -INFINITY ? 0.f : m_b;
+                float mx_a = -INFINITY, mx_b = -INFINITY, lt_a = 0.f, lt_b = 0.f;
+                uint32_t pk[20];
+                auto logits = [&](auto with_p) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int k0 = 8 * i + 2 * tc;
-                    const float4 m0 = *reinterpret_cast<const float4 *>(&meta[k0]);
-                    const float4 m1 = *reinterpret_cast<const float4 *>(&meta[k0 + 1]);
-                    float u0 = fmaf(__uint_as_float(sv[4 * i + 0]) * m0.x, rs_a, m0.y);
-                    float u1 = fmaf(__uint_as_float(sv[4 * i + 1]) * m1.x, rs_a, m1.y);
-                    float u2 = fmaf(__uint_as_float(sv[4 * i + 2]) * m0.x, rs_b, m0.y);
-                    float u3 = fmaf(__uint_as_float(sv[4 * i + 3]) * m1.x, rs_b, m1.y);
-                    if (!full) {
-                        const bool va0 = kSparse ? lim_a >= 0 : key0 + k0 <= lim_a;
-                        const bool va1 = kSparse ? lim_a >= 0 : key0 + k0 + 1 <= lim_a;
-                        const bool vb0 = kSparse ? lim_b >= 0 : key0 + k0 <= lim_b;
-                        const bool vb1 = kSparse ? lim_b >= 0 : key0 + k0 + 1 <= lim_b;
-                        u0 = va0 ? u0 : -INFINITY;
-                        u1 = va1 ? u1 : -INFINITY;
-                        u2 = vb0 ? u2 : -INFINITY;
-                        u3 = vb1 ? u3 : -INFINITY;
+                    for (int i = 0; i < BN / 8; ++i) {
+                        const int k0 = 8 * i + 2 * tc;
+                        const float4 m = meta.sl[4 * i + tc];     // keys k0, k0+1
+                        float u0 = fmaf(__uint_as_float(sv[4 * i + 0]) * m.x, rs_a, m.z);
+                        float u1 = fmaf(__uint_as_float(sv[4 * i + 1]) * m.y, rs_a, m.w);
+                        float u2 = fmaf(__uint_as_float(sv[4 * i + 2]) * m.x, rs_b, m.z);
+                        float u3 = fmaf(__uint_as_float(sv[4 * i + 3]) * m.y, rs_b, m.w);
+                        if (!full) {
+                            const bool va0 = kSparse ? lim_a >= 0 : key0 + k0 <= lim_a;
+                            const bool va1 = kSparse ? lim_a >= 0 : key0 + k0 + 1 <= lim_a;
+                            const bool vb0 = kSparse ? lim_b >= 0 : key0 + k0 <= lim_b;
+                            const bool vb1 = kSparse ? lim_b >= 0 : key0 + k0 + 1 <= lim_b;
+                            u0 = va0 ? u0 : -INFINITY;
+                            u1 = va1 ? u1 : -INFINITY;
+                            u2 = vb0 ? u2 : -INFINITY;
+                            u3 = vb1 ? u3 : -INFINITY;
+                        }
+                        sv[4 * i + 0] = __float_as_uint(u0);
+                        sv[4 * i + 1] = __float_as_uint(u1);
+                        sv[4 * i + 2] = __float_as_uint(u2);
+                        sv[4 * i + 3] = __float_as_uint(u3);
+                        mx_a = fmaxf(mx_a, fmaxf(u0, u1));
+                        mx_b = fmaxf(mx_b, fmaxf(u2, u3));
+                        if (decltype(with_p)::value) {
+                            const float2 is = meta.isig[4 * i + tc];
+                            const float p0 = fast_exp2(u0 - mu_a0), p1 = fast_exp2(u1 - mu_a0);
+                            const float p2 = fast_exp2(u2 - mu_b0), p3 = fast_exp2(u3 - mu_b0);
+                            lt_a = fmaf(p0, is.x, fmaf(p1, is.y, lt_a));
+                            lt_b = fmaf(p2, is.x, fmaf(p3, is.y, lt_b));
+                            pk[2 * i] = pack_half2(p0, p1);
+                            pk[2 * i + 1] = pack_half2(p2, p3);
+                        }
                     }
-                    sv[4 * i + 0] = __float_as_uint(u0);
-                    sv[4 * i + 1] = __float_as_uint(u1);
-                    sv[4 * i + 2] = __float_as_uint(u2);
-                    sv[4 * i + 3] = __float_as_uint(u3);
-                    mx_a = fmaxf(mx_a, fmaxf(u0, u1));
-                    mx_b = fmaxf(mx_b, fmaxf(u2, u3));
-                }
+                };
+                if (j > 0) logits(std::true_type{});
+                else logits(std::false_type{});
                 mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
                 mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
                 mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
@@ -568,101 +624,113 @@ __global__ void __launch_bounds__(NT, 1) attn_kernel(const AttnArgs a, const int
                         resc = true;
                     }
                 }
-                const float mu_a = m_a == -INFINITY ? 0.f : m_a, mu_b = m_b == -INFINITY ? 0.f : m_b;
-                l_a *= al_a;
-                l_b *= al_b;
-                uint32_t pk[32];
+                const bool any_resc = __any_sync(0xffffffffu, resc);
+                if (j == 0 || any_resc) {
+                    // P (again) against the reference maxima now in force
+                    const float mu_a = m_a == -INFINITY ? 0.f : m_a, mu_b = m_b == -INFINITY ? 0.f : m_b;
+                    lt_a = 0.f;
+                    lt_b = 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int k0 = 8 * i + 2 * tc;
-                    const float i0 = meta[k0].isig, i1 = meta[k0 + 1].isig;
-                    const float p0 = fast_exp2(__uint_as_float(sv[4 * i + 0]) - mu_a);
-                    const float p1 = fast_exp2(__uint_as_float(sv[4 * i + 1]) - mu_a);
-                    const float p2 = fast_exp2(__uint_as_float(sv[4 * i + 2]) - mu_b);
-                    const float p3 = fast_exp2(__uint_as_float(sv[4 * i + 3]) - mu_b);
-                    l_a = fmaf(p0, i0, fmaf(p1, i1, l_a));
-                    l_b = fmaf(p2, i0, fmaf(p3, i1, l_b));
-                    pk[2 * i] = pack_half2(p0, p1);
-                    pk[2 * i + 1] = pack_half2(p2, p3);
-                }
-                // ---- the previous PV must be done before O is touched or P overwritten ----
-                if (j > 0) {
-                    if (!(ok = wait(B_PV_DONE, (t - 1) & 1))) break;
-                    fence_after_sync();
-                }
-                if (__any_sync(0xffffffffu, resc)) {
-                    // 32x32b view: lane L holds row 16q + L%16, half L/16; its factor lives in
-                    // thread 4 (L%8) as row a (L%16 < 8) or row b
-                    const int rr = lane & 15;
-                    const float xa = __shfl_sync(0xffffffffu, al_a, 4 * (rr & 7));
-                    const float xb = __shfl_sync(0xffffffffu, al_b, 4 * (rr & 7));
-                    const float al = rr < 8 ? xa : xb;
-#pragma unroll 1
-                    for (int c0 = 0; c0 < 256; c0 += 16) {
-                        uint32_t o[16];
-                        tmem_ld16(tmem + lane_addr + kColO + c0, o);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al);
-                        tmem_st16(tmem + lane_addr + kColO + c0, o);
+                    for (int i = 0; i < BN / 8; ++i) {
+                        const float2 is = meta.isig[4 * i + tc];
+                        const float p0 = fast_exp2(__uint_as_float(sv[4 * i + 0]) - mu_a);
+                        const float p1 = fast_exp2(__uint_as_float(sv[4 * i + 1]) - mu_a);
+                        const float p2 = fast_exp2(__uint_as_float(sv[4 * i + 2]) - mu_b);
+                        const float p3 = fast_exp2(__uint_as_float(sv[4 * i + 3]) - mu_b);
+                        lt_a = fmaf(p0, is.x, fmaf(p1, is.y, lt_a));
+                        lt_b = fmaf(p2, is.x, fmaf(p3, is.y, lt_b));
+                        pk[2 * i] = pack_half2(p0, p1);
+                        pk[2 * i + 1] = pack_half2(p2, p3);
                     }
                 }
-                // ---- P into both lane halves (A operand of the two PV halves) ----
-                tmem_st_16x128b_x16(tmem + lane_addr + kColP, pk);
-                tmem_st_16x128b_x16(tmem + lane_addr + kHalf1 + kColP, pk);
+                l_a = fmaf(l_a, al_a, lt_a);
+                l_b = fmaf(l_b, al_b, lt_b);
+                // ---- O rescale (rare): PV(t-1) must be complete, PV(t) is not yet issued ----
+                if (any_resc) {
+                    if (!(ok = wait(B_PV_DONE + ((t - 1) & 1), ((t - 1) >> 1) & 1))) break;
+                    fence_after_sync();
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 512; c0 += 64) {
+                        uint32_t o[32];
+                        tmem_ld_16x256b_x8(tmem + lane_hi + kColO + c0, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            o[4 * i + 0] = __float_as_uint(__uint_as_float(o[4 * i + 0]) * al_a);
+                            o[4 * i + 1] = __float_as_uint(__uint_as_float(o[4 * i + 1]) * al_a);
+                            o[4 * i + 2] = __float_as_uint(__uint_as_float(o[4 * i + 2]) * al_b);
+                            o[4 * i + 3] = __float_as_uint(__uint_as_float(o[4 * i + 3]) * al_b);
+                        }
+                        tmem_st_16x256b_x8(tmem + lane_hi + kColO + c0, o);
+                    }
+                    tmem_st_wait();
+                }
+                // ---- P into smem buffer t&1 (its last reader, PV(t-2), must be complete) ----
+                if (t >= 2 && !(ok = wait(B_PV_DONE + sb, ((t >> 1) - 1) & 1))) break;
+                uint8_t *pw = pbuf + sb * kPBuf;
+#pragma unroll
+                for (int i = 0; i < BN / 8; ++i) {
+                    *reinterpret_cast<uint32_t *>(pw + poff_a + 128 * i) = pk[2 * i];
+                    *reinterpret_cast<uint32_t *>(pw + poff_b + 128 * i) = pk[2 * i + 1];
+                }
+                fence_proxy_async();
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_P_FULL + sb]));
+            }
+            if (!ok) break;
+            // ---- the next row tile's Q (QK of this row tile is complete: its last S was read) ----
+            const RowTile rt_done = rt;
+            float rs_na = 0.f, rs_nb = 0.f;
+            if (r + 1 < n_rt) {
+                rt = make_tile<kSparse>(a, b, tiles[r + 1], sp_tok, sp_h0);
+                load_q_tmem(a, rt, tmem + lane_lo + kColQ, ra, rb, tc, rs_na, rs_nb);
                 tmem_st_wait();
                 fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_P_FULL]));
+                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_Q_FULL]));
             }
-            if (!ok) break;
             // ---- epilogue: O 2^8 / l to bf16, lse ----
-            if (!(ok = wait(B_PV_DONE, (t - 1) & 1))) break;
+            if (!(ok = wait(B_PV_DONE + ((t - 1) & 1), ((t - 1) >> 1) & 1))) break;
             fence_after_sync();
             l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
             l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
             l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
             l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+            const bool va = lim_a >= 0, vb = lim_b >= 0;
             if (tc == 0 && a.lse) {
-                if (ra < rt.nvalid && lim_a >= 0)
-                    a.lse[rt.grow0 + ra] = l_a > 0.f ? (m_a + __log2f(l_a)) * kLn2 : -INFINITY;
-                if (rb < rt.nvalid && lim_b >= 0)
-                    a.lse[rt.grow0 + rb] = l_b > 0.f ? (m_b + __log2f(l_b)) * kLn2 : -INFINITY;
+                if (va) a.lse[rt_done.grow0 + ra] = l_a > 0.f ? (m_a + __log2f(l_a)) * kLn2 : -INFINITY;
+                if (vb) a.lse[rt_done.grow0 + rb] = l_b > 0.f ? (m_b + __log2f(l_b)) * kLn2 : -INFINITY;
             }
-            const int rr = lane & 15, row = 16 * q + rr;
             const float ia = l_a > 0.f ? kCodeScale / l_a : 0.f, ib = l_b > 0.f ? kCodeScale / l_b : 0.f;
-            const float xa = __shfl_sync(0xffffffffu, ia, 4 * (rr & 7));
-            const float xb = __shfl_sync(0xffffffffu, ib, 4 * (rr & 7));
-            const float inv = rr < 8 ? xa : xb;
-            const bool valid = row < rt.nvalid && sh.rowlimit[r & 1][row] >= 0;
-            __nv_bfloat16 *dst = a.out + (rt.grow0 + row) * kDv + (lane < 16 ? 0 : 256);
+            __nv_bfloat16 *da = a.out + (rt_done.grow0 + ra) * kDv + 2 * tc;
+            __nv_bfloat16 *db = a.out + (rt_done.grow0 + rb) * kDv + 2 * tc;
 #pragma unroll 1
-            for (int c0 = 0; c0 < 256; c0 += 32) {
+            for (int c0 = 0; c0 < 512; c0 += 64) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_addr + kColO + c0, o);
+                tmem_ld_16x256b_x8(tmem + lane_hi + kColO + c0, o);
                 tmem_ld_wait();
-                if (valid) {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint4 w;
-                        w.x = pack_bf162(__uint_as_float(o[8 * i + 0]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
-                        w.y = pack_bf162(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv);
-                        w.z = pack_bf162(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv);
-                        w.w = pack_bf162(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv);
-                        d4[i] = w;
-                    }
+                for (int i = 0; i < 8; ++i) {
+                    if (va)
+                        *reinterpret_cast<uint32_t *>(da + c0 + 8 * i) =
+                            pack_bf162(__uint_as_float(o[4 * i + 0]) * ia, __uint_as_float(o[4 * i + 1]) * ia);
+                    if (vb)
+                        *reinterpret_cast<uint32_t *>(db + c0 + 8 * i) =
+                            pack_bf162(__uint_as_float(o[4 * i + 2]) * ib, __uint_as_float(o[4 * i + 3]) * ib);
                 }
             }
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_O_FREE]));
+            rs_a = rs_na;
+            rs_b = rs_nb;
         }
     }
 
     // ----- teardown: every MMA complete before TMEM is released -----
     __syncthreads();
-    if (warp == 8) {
+    if (warp == kIssuerWarp) {
         if (!mbar_wait_cycles(smem_u32(&sh.bar[B_FINAL]), 0, kWaitCycles)) set_dev_err(a.dev_err, MLA_DEVERR_TIMEOUT);
         fence_after_sync();
         tmem_dealloc(tmem, 512);
