@@ -378,8 +378,9 @@ def main():
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak, "traffic": None,
                          "peak_source": f"{src} bf16 sustained (f16 and bf16 share the dense tensor rate)",
-                         "kernel": "mla dense (mma.sync f16 path)" if isinstance(run, DenseRun)
-                         else "indexer + top-k + sparse"},
+                         "kernel": "attn_kernel<dense>: tcgen05 f16, Q in TMEM, 64 rows x 80 keys"
+                         if isinstance(run, DenseRun) else
+                         "indexer (mma.sync e4m3) + top-k + attn_kernel<sparse> (tcgen05 f16)"},
             "gpu_launches": run.launches_per_step * args.steps}
     if clk:
         line["clocks"] = clk

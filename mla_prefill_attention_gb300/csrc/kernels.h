@@ -43,10 +43,8 @@ struct IndexerArgs {
     int32_t *dev_err;
 };
 
-// Dense work item: x = sequence, y = row tile, z = paired row tile or -1.
-cudaError_t launch_dense_sm80path(const AttnArgs &a, const int4 *work, int n_work, cudaStream_t st);
-cudaError_t launch_sparse_sm80path(const AttnArgs &a, int64_t n_tokens, cudaStream_t st);
-// tcgen05/TMEM kernels (64 query rows per CTA; same work items)
+// tcgen05/TMEM attention (64 query rows per CTA). Dense work item: x = sequence,
+// y = row tile, z = paired row tile or -1. Sparse: one CTA per (token, 64 heads).
 cudaError_t launch_dense_tc(const AttnArgs &a, const int4 *work, int n_work, cudaStream_t st);
 cudaError_t launch_sparse_tc(const AttnArgs &a, int64_t n_tokens, cudaStream_t st);
 
