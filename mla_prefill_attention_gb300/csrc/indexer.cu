@@ -1,4 +1,5 @@
-// Indexer score and exact top-k selection (sm_103a).
+// Exact top-k selection over the indexer's scores (sm_103a); the scores come
+// from indexer_tc.cu.
 //
 // score(t,s) = sigmaI_s * sum_h w[t,h] * max(0, q_{t,h} . k_s), s <= position(t)
 // (GLM-5.3 Teil 2, section "Warum nicht TP oder DP?": the indexer scores every
@@ -17,14 +18,6 @@
 namespace mla {
 namespace idx {
 
-constexpr int NT = 256;             // 8 warps = 8 query tokens per CTA
-constexpr int KT = 128;             // keys per smem tile
-constexpr int kRow = kDidx;         // 128 B per e4m3 key row
-
-__device__ __forceinline__ uint32_t sw128(uint32_t base, int row, int chunk) {
-    return base + row * 128 + ((chunk ^ (row & 7)) << 4);
-}
-
 __device__ __forceinline__ int find_seq(const int32_t *cu, int batch, int64_t t) {
     int lo = 0, hi = batch - 1;
     while (lo < hi) {
@@ -32,111 +25,6 @@ __device__ __forceinline__ int find_seq(const int32_t *cu, int batch, int64_t t)
         if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
     }
     return lo;
-}
-
-__global__ void __launch_bounds__(NT, 1) score_kernel(const IndexerArgs a, const int4 *__restrict__ work) {
-    __shared__ __align__(128) uint8_t sk[2][KT * kRow];
-    __shared__ int64_t srow[2][KT];
-    __shared__ float ssig[2][KT];
-
-    const int4 it = work[blockIdx.x];
-    const int b = it.x, i0 = it.y, ntok = it.z;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-    const int q0 = __ldg(a.cu_seqlens + b), P = __ldg(a.prefix_lens + b);
-    const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.max_blocks;
-    const int k_lo = it.w * kIdxKeyChunk;
-    const int k_hi = min(k_lo + kIdxKeyChunk, P + i0 + ntok);       // exclusive
-    const bool tok_ok = warp < ntok;
-    const int64_t tg = static_cast<int64_t>(q0) + i0 + warp;        // global token of this warp
-    const int limit = P + i0 + warp;                                // last visible position
-
-    // this token's 64 heads x 128 dims as m16n8k32 B fragments (n = head, k = dim)
-    uint32_t bq[8][4][2];
-    float wv[8][2];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-        const int head = 8 * nt + g;
-        const uint8_t *qrow = a.qi + (tg * kHidx + head) * kDidx + 4 * t4;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            bq[nt][ks][0] = tok_ok ? __ldg(reinterpret_cast<const uint32_t *>(qrow + 32 * ks)) : 0u;
-            bq[nt][ks][1] = tok_ok ? __ldg(reinterpret_cast<const uint32_t *>(qrow + 32 * ks + 16)) : 0u;
-        }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) wv[nt][j] = tok_ok ? __ldg(a.w + tg * a.w_stride + 8 * nt + 2 * t4 + j) : 0.f;
-    }
-
-    const int n_tiles = (k_hi - k_lo + KT - 1) / KT;
-    auto meta = [&](int buf, int tile) {
-        const int k = threadIdx.x;
-        if (k < KT) {
-            const int pos = k_lo + tile * KT + k;
-            const int64_t row = pos < k_hi ? cache_row(bt, a.max_blocks, a.num_blocks, pos, a.dev_err) : -1;
-            srow[buf][k] = row;
-            ssig[buf][k] = row >= 0 ? __ldg(a.ki_scale + row) : 0.f;
-        }
-    };
-    auto issue = [&](int buf) {
-        const uint32_t base = smem_u32(sk[buf]);
-#pragma unroll
-        for (int i = 0; i < (KT * kRow / 16) / NT; ++i) {
-            const int c = threadIdx.x + NT * i;
-            const int key = c >> 3, part = c & 7;
-            const int64_t row = srow[buf][key];
-            cp_async16(sw128(base, key, part), a.ki + (row >= 0 ? row : 0) * kRow + part * 16, row >= 0 ? 16 : 0);
-        }
-        cp_async_commit();
-    };
-
-    if (n_tiles > 0) {
-        meta(0, 0);
-        __syncthreads();
-        issue(0);
-    }
-    for (int j = 0; j < n_tiles; ++j) {
-        const int buf = j & 1;
-        cp_async_wait<0>();
-        __syncthreads();
-        if (j + 1 < n_tiles) meta(buf ^ 1, j + 1);
-        __syncthreads();
-        if (j + 1 < n_tiles) issue(buf ^ 1);
-
-        const uint32_t base = smem_u32(sk[buf]);
-        const int tile0 = k_lo + j * KT;
-#pragma unroll 1
-        for (int st = 0; st < KT / 16; ++st) {
-            if (!tok_ok || tile0 + 16 * st > limit) break;
-            uint32_t af[4][4];
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                ldsm_x4(sw128(base, 16 * st + (lane & 7) + (((lane >> 3) & 1) << 3), 2 * ks + (lane >> 4)),
-                        af[ks][0], af[ks][1], af[ks][2], af[ks][3]);
-            float e0 = 0.f, e1 = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_e4m3_16832(c, af[ks][0], af[ks][1], af[ks][2], af[ks][3], bq[nt][ks][0], bq[nt][ks][1]);
-                e0 = fmaf(wv[nt][0], fmaxf(c[0], 0.f), e0);
-                e0 = fmaf(wv[nt][1], fmaxf(c[1], 0.f), e0);
-                e1 = fmaf(wv[nt][0], fmaxf(c[2], 0.f), e1);
-                e1 = fmaf(wv[nt][1], fmaxf(c[3], 0.f), e1);
-            }
-            e0 += __shfl_xor_sync(0xffffffffu, e0, 1);
-            e1 += __shfl_xor_sync(0xffffffffu, e1, 1);
-            e0 += __shfl_xor_sync(0xffffffffu, e0, 2);
-            e1 += __shfl_xor_sync(0xffffffffu, e1, 2);
-            if (t4 < 2) {
-                const int kk = 16 * st + g + 8 * t4;
-                const int pos = tile0 + kk;
-                if (pos <= limit && pos < k_hi) {
-                    const float v = t4 == 0 ? e0 : e1;
-                    a.scores[tg * a.score_stride + pos] = srow[buf][kk] >= 0 ? ssig[buf][kk] * v : -INFINITY;
-                }
-            }
-        }
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -300,11 +188,6 @@ __global__ void __launch_bounds__(TK_NT, 1) topk_kernel(const IndexerArgs a) {
 }
 
 }  // namespace idx
-
-cudaError_t launch_indexer_scores(const IndexerArgs &a, const int4 *work, int n_work, cudaStream_t st) {
-    if (n_work > 0) idx::score_kernel<<<n_work, idx::NT, 0, st>>>(a, work);
-    return cudaGetLastError();
-}
 
 cudaError_t launch_topk(const IndexerArgs &a, int64_t n_tokens, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(idx::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, idx::TK_SMEM);

@@ -1,0 +1,229 @@
+// Indexer scores on the 5th-generation tensor cores (tcgen05 kind::f8f6f4).
+//
+// score(t,s) = sigmaI_s * sum_h w[t,h] * max(0, q_{t,h} . k_s),   s <= position(t)
+// (GLM-5.3 Teil 2, section "Warum nicht TP oder DP?": the indexer scores every
+// earlier token to pick 2,048; footnote 3: an indexer key is 128 FP8 values
+// plus a 4-byte scale.)
+//
+// One CTA scores 4 query tokens (x 64 heads) against a chunk of keys, 128 keys
+// at a time:
+//
+//   D[key][64 j + h] = k_key . q_{t_j,h}    tcgen05.mma e4m3 x e4m3 -> f32,
+//                                           M = 128 keys, N = 256 = 4 tokens x 64
+//                                           heads, K = 128 (4 steps of 32)
+//
+// so TMEM lane = key and each epilogue thread owns one key: the head sum
+// sum_h w[t,h] max(0, D) is a per-thread loop over its own columns, with no
+// cross-thread reduction. The products of the codes are exact in f32 and the
+// sums are exact while they stay below 2^24 in units of the smallest product,
+// which the integer-valued keys and queries of the indexer guarantee.
+//
+// Keys arrive by TMA: a 128-key tile starts at a multiple of 128 and so lies in
+// one 256-token page, i.e. 128 contiguous rows of the paged key cache, copied
+// with the 128-byte swizzle the MMA's K-major operand layout expects. The 4
+// tokens' queries (256 rows) are one more TMA copy.
+//
+// Warps: 0-7 epilogue (warp w reads TMEM lane quadrant w%4 = keys 32(w%4)..+31
+// and tokens 2(w/4), 2(w/4)+1), 8 TMA producer, 9 MMA issue + TMEM owner. Key
+// tiles go through a 6-stage ring; the accumulator is double-buffered in TMEM
+// (2 x 256 columns) so the MMA of tile i+1 overlaps the epilogue of tile i.
+// Every wait is bounded and reports MLA_DEVERR_TIMEOUT.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace mla {
+namespace idxtc {
+
+using namespace tc;
+
+constexpr int TOK = kIdxTokensPerCta;   // 4 query tokens per CTA
+constexpr int KT = 128;                 // keys per tile
+constexpr int STAGES = 6;
+constexpr int NT = 320;                 // 10 warps
+constexpr int kProducerWarp = 8, kIssuerWarp = 9;
+constexpr int kQBytes = TOK * kHidx * kDidx;       // 32 KB
+constexpr int kTileBytes = KT * kDidx;             // 16 KB
+constexpr int kDynSmem = 1024 + kQBytes + STAGES * kTileBytes;
+constexpr long long kWaitCycles = 200000000LL;
+static_assert(kIdxKeyChunk % KT == 0 && kPage % KT == 0, "key tiles must not straddle pages or chunks");
+
+enum Bar {
+    B_Q_FULL = 0,
+    B_K_FULL = 1,                       // [STAGES]  TMA -> issuer
+    B_K_EMPTY = B_K_FULL + STAGES,      // [STAGES]  issuer (commit) -> producer
+    B_D_FULL = B_K_EMPTY + STAGES,      // [2]       issuer (commit) -> epilogue
+    B_D_EMPTY = B_D_FULL + 2,           // [2]       epilogue (8 warps) -> issuer
+    B_FINAL = B_D_EMPTY + 2,
+    NBAR
+};
+
+struct Shared {
+    float w[TOK][kHidx];
+    uint64_t bar[NBAR];
+    uint32_t tmem_base;
+};
+
+__device__ __forceinline__ bool wait_bar(Shared &sh, int32_t *dev_err, int b, uint32_t parity) {
+    if (mbar_wait_cycles(smem_u32(&sh.bar[b]), parity, kWaitCycles)) return true;
+    set_dev_err(dev_err, MLA_DEVERR_TIMEOUT);
+    return false;
+}
+
+__global__ void __launch_bounds__(NT, 1)
+    score_kernel(const IndexerArgs a, const int4 *__restrict__ work, const __grid_constant__ CUtensorMap tmap_k,
+                 const __grid_constant__ CUtensorMap tmap_q) {
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    __shared__ Shared sh;
+    const uint32_t raw = smem_u32(dsm);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    const uint32_t sq = raw + pad, sk = sq + kQBytes;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const int4 it = work[blockIdx.x];
+    const int b = it.x, i0 = it.y, ntok = it.z;
+    const int q0 = __ldg(a.cu_seqlens + b), P = __ldg(a.prefix_lens + b);
+    const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.max_blocks;
+    const int k_lo = it.w * kIdxKeyChunk;
+    const int k_hi = min(k_lo + kIdxKeyChunk, P + i0 + ntok);       // exclusive
+    const int n_tiles = (k_hi - k_lo + KT - 1) / KT;
+
+    if (tid == 0) {
+        for (int i = 0; i < NBAR; ++i) mbar_init(smem_u32(&sh.bar[i]), (i == B_D_EMPTY || i == B_D_EMPTY + 1) ? 8 : 1);
+        mbar_fence_init();
+    }
+    for (int i = tid; i < TOK * kHidx; i += NT) {
+        const int j = i / kHidx;
+        sh.w[j][i % kHidx] = j < ntok ? __ldg(a.w + static_cast<int64_t>(q0 + i0 + j) * a.w_stride + i % kHidx) : 0.f;
+    }
+    if (warp == kIssuerWarp) {
+        tmem_alloc(smem_u32(&sh.tmem_base), 512);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = sh.tmem_base;
+
+    if (warp == kProducerWarp) {
+        // =================== TMA producer ===================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_q);
+            mbar_expect_tx(smem_u32(&sh.bar[B_Q_FULL]), kQBytes);
+            tma_load_2d(sq, &tmap_q, 0, (q0 + i0) * kHidx, smem_u32(&sh.bar[B_Q_FULL]));
+            for (int i = 0; i < n_tiles; ++i) {
+                const int s = i % STAGES;
+                if (i >= STAGES && !wait_bar(sh, a.dev_err, B_K_EMPTY + s, ((i / STAGES) - 1) & 1)) break;
+                const int pos0 = k_lo + i * KT;
+                const int page = pos0 / kPage;
+                int blk = page < a.max_blocks ? __ldg(bt + page) : -1;
+                if (blk < 0 || blk >= a.num_blocks) {   // reported; the epilogue masks these keys
+                    set_dev_err(a.dev_err, MLA_DEVERR_BAD_PAGE);
+                    blk = 0;
+                }
+                mbar_expect_tx(smem_u32(&sh.bar[B_K_FULL + s]), kTileBytes);
+                tma_load_2d(sk + s * kTileBytes, &tmap_k, 0, blk * kPage + pos0 % kPage, smem_u32(&sh.bar[B_K_FULL + s]));
+            }
+        }
+        __syncwarp();
+    } else if (warp == kIssuerWarp) {
+        // =================== MMA issuer ===================
+        if (lane == 0) {
+            const uint32_t id = idesc_e4m3(KT, TOK * kHidx, false, false);
+            const uint64_t dq = sdesc(sq, 16, 1024, kSw128);
+            const uint64_t dk0 = sdesc(sk, 16, 1024, kSw128);
+            bool ok = wait_bar(sh, a.dev_err, B_Q_FULL, 0);
+            for (int i = 0; i < n_tiles && ok; ++i) {
+                const int s = i % STAGES, db = i & 1;
+                if (!(ok = wait_bar(sh, a.dev_err, B_K_FULL + s, (i / STAGES) & 1))) break;
+                if (i >= 2 && !(ok = wait_bar(sh, a.dev_err, B_D_EMPTY + db, ((i >> 1) - 1) & 1))) break;
+                fence_after_sync();
+                const uint64_t dk = dk0 + static_cast<uint64_t>((s * kTileBytes) >> 4);
+#pragma unroll
+                for (int ks = 0; ks < kDidx / 32; ++ks)
+                    mma_e4m3_ss(tmem + 256u * db, dk + 2 * ks, dq + 2 * ks, id, ks > 0 ? 1u : 0u);
+                mma_commit(smem_u32(&sh.bar[B_K_EMPTY + s]));
+                mma_commit(smem_u32(&sh.bar[B_D_FULL + db]));
+            }
+            mma_commit(smem_u32(&sh.bar[B_FINAL]));
+        }
+        __syncwarp();
+    } else {
+        // =================== epilogue (warps 0-7) ===================
+        const int quad = warp & 3, tp = warp >> 2;                    // keys 32 quad.., tokens 2tp, 2tp+1
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * quad) << 16;
+        const int kk = 32 * quad + lane;                              // key within the tile
+        for (int i = 0; i < n_tiles; ++i) {
+            const int db = i & 1;
+            // this key's cache row and scale (issued before the wait)
+            const int pos = k_lo + i * KT + kk;
+            int64_t row = -1;
+            if (pos < k_hi) {
+                const int page = pos / kPage;
+                const int blk = page < a.max_blocks ? __ldg(bt + page) : -1;
+                if (blk >= 0 && blk < a.num_blocks) row = static_cast<int64_t>(blk) * kPage + pos % kPage;
+            }
+            const float sig = row >= 0 ? __ldg(a.ki_scale + row) : 0.f;
+            if (!wait_bar(sh, a.dev_err, B_D_FULL + db, (i >> 1) & 1)) break;
+            fence_after_sync();
+            float sc[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int j = 2 * tp + u;
+                uint32_t d0[32], d1[32];
+                tmem_ld32(tmem + lane_addr + 256u * db + 64u * j, d0);
+                tmem_ld32(tmem + lane_addr + 256u * db + 64u * j + 32, d1);
+                tmem_ld_wait();
+                const float4 *wj = reinterpret_cast<const float4 *>(sh.w[j]);
+                float e0 = 0.f, e1 = 0.f;
+#pragma unroll
+                for (int h4 = 0; h4 < 8; ++h4) {
+                    const float4 wa = wj[h4], wb = wj[8 + h4];
+                    e0 = fmaf(wa.x, fmaxf(__uint_as_float(d0[4 * h4 + 0]), 0.f), e0);
+                    e1 = fmaf(wa.y, fmaxf(__uint_as_float(d0[4 * h4 + 1]), 0.f), e1);
+                    e0 = fmaf(wa.z, fmaxf(__uint_as_float(d0[4 * h4 + 2]), 0.f), e0);
+                    e1 = fmaf(wa.w, fmaxf(__uint_as_float(d0[4 * h4 + 3]), 0.f), e1);
+                    e0 = fmaf(wb.x, fmaxf(__uint_as_float(d1[4 * h4 + 0]), 0.f), e0);
+                    e1 = fmaf(wb.y, fmaxf(__uint_as_float(d1[4 * h4 + 1]), 0.f), e1);
+                    e0 = fmaf(wb.z, fmaxf(__uint_as_float(d1[4 * h4 + 2]), 0.f), e0);
+                    e1 = fmaf(wb.w, fmaxf(__uint_as_float(d1[4 * h4 + 3]), 0.f), e1);
+                }
+                sc[u] = e0 + e1;
+            }
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_D_EMPTY + db]));
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int j = 2 * tp + u;
+                if (j < ntok && pos < k_hi && pos <= P + i0 + j)
+                    a.scores[static_cast<int64_t>(q0 + i0 + j) * a.score_stride + pos] = row >= 0 ? sig * sc[u] : -INFINITY;
+            }
+        }
+    }
+
+    // ----- teardown -----
+    __syncthreads();
+    if (warp == kIssuerWarp) {
+        if (!mbar_wait_cycles(smem_u32(&sh.bar[B_FINAL]), 0, kWaitCycles)) set_dev_err(a.dev_err, MLA_DEVERR_TIMEOUT);
+        fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace idxtc
+
+cudaError_t launch_indexer_scores_tc(const IndexerArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_k,
+                                     const CUtensorMap &tmap_q, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(idxtc::score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         idxtc::kDynSmem);
+    if (e != cudaSuccess) return e;
+    if (n_work > 0) idxtc::score_kernel<<<n_work, idxtc::NT, idxtc::kDynSmem, st>>>(a, work, tmap_k, tmap_q);
+    return cudaGetLastError();
+}
+
+}  // namespace mla

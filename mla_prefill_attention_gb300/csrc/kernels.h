@@ -1,6 +1,7 @@
 // Launch interfaces between the C ABI layer and the kernels (internal).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -49,10 +50,13 @@ cudaError_t launch_dense_tc(const AttnArgs &a, const int4 *work, int n_work, cud
 cudaError_t launch_sparse_tc(const AttnArgs &a, int64_t n_tokens, cudaStream_t st);
 
 // Indexer score work item: x = sequence, y = first new token (in-sequence),
-// z = token count (<= 8), w = key chunk.
-constexpr int kIdxTokensPerCta = 8;
-constexpr int kIdxKeyChunk = 4096;
-cudaError_t launch_indexer_scores(const IndexerArgs &a, const int4 *work, int n_work, cudaStream_t st);
+// z = token count (<= 4), w = key chunk. tmap_k: the key cache as
+// [num_blocks * 256 rows][128 B]; tmap_q: the queries as [Tq * 64 rows][128 B];
+// both with 128-byte boxes rows wide, 128-byte swizzle (128- and 256-row boxes).
+constexpr int kIdxTokensPerCta = 4;
+constexpr int kIdxKeyChunk = 8192;
+cudaError_t launch_indexer_scores_tc(const IndexerArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_k,
+                                     const CUtensorMap &tmap_q, cudaStream_t st);
 cudaError_t launch_topk(const IndexerArgs &a, int64_t n_tokens, cudaStream_t st);
 
 }  // namespace mla

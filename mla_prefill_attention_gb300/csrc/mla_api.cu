@@ -1,6 +1,7 @@
 // C ABI of the MLA prefill attention library: argument checks, scheduling,
 // workspace layout and kernel launches. Every entry point is declared and
 // documented in include/mla.h.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -121,6 +122,32 @@ size_t indexer_score_bytes(const mla_seqs_t *s) {
     return round_up(static_cast<size_t>(tq) * static_cast<size_t>(max_context(s)) * sizeof(float), kWsAlign);
 }
 
+// 2-D tensor map over a row-major u8 matrix [rows][128] for TMA copies of
+// box_rows x 128-byte boxes with the 128-byte swizzle. The encoder is fetched
+// from the driver once; no link against the driver library is needed.
+bool encode_rows128(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+    using Encode = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static Encode encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return false;
+        encode = reinterpret_cast<Encode>(fn);
+    }
+    const cuuint64_t dims[2] = {128, rows};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 mla::AttnArgs attn_args(const mla_seqs_t *s, const void *q, int32_t H, const uint8_t *kv, const float *kv_scale,
                         float sm_scale, void *out, float *lse, int32_t *dev_err) {
     mla::AttnArgs a{};
@@ -214,6 +241,7 @@ mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, co
     if (topk < 1 || topk > 2048) return fail(MLA_ERR_UNSUPPORTED, "topk must be in [1, 2048] (got %d)", topk);
     const int64_t tq = seqs->cu_seqlens_q_host[seqs->batch];
     if (tq == 0) return MLA_OK;
+    if (tq * 64 > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "too many query tokens for the indexer (Tq * 64 > 2^31 - 1)");
     const std::vector<int4> work = indexer_schedule(seqs);
     const size_t sbytes = indexer_score_bytes(seqs);
     const size_t need = sbytes + round_up(work.size() * sizeof(int4), kWsAlign);
@@ -243,7 +271,12 @@ mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, co
     a.topk = topk;
     a.idx_out = idx_out;
     a.dev_err = dev_err;
-    if ((e = mla::launch_indexer_scores(a, dwork, static_cast<int>(work.size()), stream)) != cudaSuccess)
+    CUtensorMap tmap_k, tmap_q;
+    if (!encode_rows128(&tmap_k, ki_e4m3, static_cast<uint64_t>(seqs->num_blocks) * 256, 128) ||
+        !encode_rows128(&tmap_q, qi_e4m3, static_cast<uint64_t>(tq) * 64, 256))
+        return fail(MLA_ERR_CUDA, "tensor map encoding for the indexer failed");
+    if ((e = mla::launch_indexer_scores_tc(a, dwork, static_cast<int>(work.size()), tmap_k, tmap_q, stream)) !=
+        cudaSuccess)
         return cuda_fail(e, "indexer score launch");
     if ((e = mla::launch_topk(a, tq, stream)) != cudaSuccess) return cuda_fail(e, "top-k launch");
     return MLA_OK;
