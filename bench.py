@@ -252,8 +252,118 @@ class SparseRun:
         return done, t_total, done * (self.flops / ps.total_q)
 
 
+class ChunkedRun:
+    """One step = the whole chunked prefill of a long prompt: for every chunk,
+    mla_indexer_topk + mla_prefill_sparse after the cached prefix of the earlier
+    chunks. Every chunk's queries are resident in HBM before timing. Also times
+    the dense path on the final chunk (reported beside the step)."""
+
+    def __init__(self, w, dev):
+        import torch
+        from mla_prefill_attention_gb300 import MLA_OP_DENSE, MLA_OP_INDEXER, Seqs, chunk_bounds, inputs as I
+        from mla_prefill_attention_gb300 import mla_workspace_size
+        from mla_prefill_attention_gb300 import flops as F
+        self.w, self.dev = w, dev
+        self.ps = w.seqs()
+        N = w.q_lens[0]
+        kv, ks = I.gen_latent_cache(w.seed, self.ps)
+        ki, kis = I.gen_indexer_keys(w.seed, self.ps)
+        wh = I.gen_indexer_w(w.seed)
+        self.host = dict(kv=kv, ks=ks, ki=ki, kis=kis, w=wh)
+        self.d = {k: torch.from_numpy(v).to(dev) for k, v in self.host.items()}
+        self.bounds = chunk_bounds(N, w.chunk)
+        self.chunks = []
+        max_c = max(e - s for s, e in self.bounds)
+        ws = 0
+        for s, e in self.bounds:
+            sub = I.PagedSeqs(np.array([0, e - s], np.int32), np.array([s], np.int32), self.ps.block_table,
+                              self.ps.num_blocks)
+            seqs = Seqs.from_paged(sub, device=dev)
+            q = I.gen_q_bf16(w.seed, N, w.heads, token_rows=np.arange(s, e))
+            qi = I.gen_indexer_q(w.seed, N, token_rows=np.arange(s, e))
+            self.chunks.append(dict(seqs=seqs, sub=sub, q=torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).to(dev),
+                                    qi=torch.from_numpy(qi).to(dev)))
+            ws = max(ws, mla_workspace_size(MLA_OP_INDEXER, seqs, 64, w.topk))
+        last = self.chunks[-1]["seqs"]
+        ws = max(ws, mla_workspace_size(MLA_OP_DENSE, last, w.heads))
+        H = w.heads
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+        self.out = torch.empty((max_c, H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((max_c, H), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((max_c, w.topk), dtype=torch.int32, device=dev)
+        self.tokens = N
+        self.flops = F.sparse_flops(w.q_lens, w.prefix_lens, H, w.topk) + F.indexer_flops(w.q_lens, w.prefix_lens)
+        self.launches_per_step = 3 * len(self.bounds)
+        self.chunk_ms = [0.0] * len(self.bounds)
+        self.ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in self.bounds]
+        self.min_bytes = None
+
+    def _chunk(self, c):
+        from mla_prefill_attention_gb300 import mla_indexer_topk, mla_prefill_sparse
+        ch, d, n = self.chunks[c], self.d, self.bounds[c][1] - self.bounds[c][0]
+        mla_indexer_topk(ch["seqs"], ch["qi"], d["w"], 0, d["ki"], d["kis"], self.w.topk, idx_out=self.idx[:n],
+                         workspace=self.ws)
+        mla_prefill_sparse(ch["seqs"], ch["q"], d["kv"], d["ks"], self.w.sm_scale, self.idx[:n], out=self.out[:n],
+                           lse=self.lse[:n])
+
+    def step(self):
+        for c in range(len(self.bounds)):
+            self.ev[c][0].record()
+            self._chunk(c)
+            self.ev[c][1].record()
+
+    def collect_chunk_ms(self):
+        self.chunk_ms = [a.elapsed_time(b) for a, b in self.ev]
+
+    def dense_last_chunk_ms(self, reps=3):
+        """The dense path on the final chunk (same inputs), median of reps calls."""
+        import torch
+        from mla_prefill_attention_gb300 import mla_prefill_dense
+        ch, d = self.chunks[-1], self.d
+        n = self.bounds[-1][1] - self.bounds[-1][0]
+        call = lambda: mla_prefill_dense(ch["seqs"], ch["q"], d["kv"], d["ks"], self.w.sm_scale, out=self.out[:n],
+                                         lse=self.lse[:n], workspace=self.ws)
+        call()
+        times = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    def e2e(self, steps, warmup):
+        return None
+
+    def oracle_rate(self, budget_s, seed=0):
+        """Oracle on random query tokens of random chunks (indexer + sparse),
+        extrapolated by algorithmic FLOPs."""
+        from oracle import oracle as O
+        from mla_prefill_attention_gb300 import inputs as I, flops as F
+        h, w = self.host, self.w
+        rng = np.random.default_rng(seed)
+        t_total, done, fl = 0.0, 0, 0
+        while t_total < budget_s and done < 64:
+            c = int(rng.integers(0, len(self.bounds)))
+            s, e = self.bounds[c]
+            t = int(rng.integers(0, e - s))
+            sub = self.chunks[c]["sub"]
+            q = I.gen_q_bf16(w.seed, w.q_lens[0], w.heads, token_rows=np.array([s + t]))
+            qi = I.gen_indexer_q(w.seed, w.q_lens[0], token_rows=np.array([s + t]))
+            t0 = time.perf_counter()
+            idx = O.indexer_topk(sub, qi, h["w"], 0, np.array([t]), h["ki"], h["kis"], w.topk)
+            O.mla_sparse(sub, q, np.array([t]), h["kv"], h["ks"], w.sm_scale, idx)
+            t_total += time.perf_counter() - t0
+            done += 1
+            ctx = s + t + 1
+            fl += min(ctx, w.topk) * w.heads * F.FLOPS_PER_PAIR_HEAD + ctx * F.H_IDX * F.D_IDX * 2
+        return done, t_total, fl
+
+
 RUNS = {"tiny512": DenseRun, "prefix12k": DenseRun, "dense32k": DenseRun, "ragged4": DenseRun,
-        "sparse64k": SparseRun}
+        "sparse64k": SparseRun, "chunked200k": ChunkedRun}
 
 
 def time_steps(run, steps, warmup):
@@ -282,9 +392,11 @@ def config_of(w):
          "heads": w.heads, "d_qk": 576, "d_v": 512, "page": 256, "q_dtype": "bf16",
          "kv_dtype": "e4m3 + fp32 per-token scale", "sm_scale": "1/sqrt(192)", "parallelism": "replicas",
          "l2": "inputs larger than L2 (no flush needed)" if w.name in ("dense32k", "ragged4", "sparse64k",
-                                                                       "prefix12k") else "small inputs"}
+                                                                       "prefix12k", "chunked200k") else "small inputs"}
     if w.sparse:
         c.update(topk=w.topk, indexer="64 heads x 128, e4m3")
+    if w.chunk:
+        c.update(chunk=w.chunk)
     return c
 
 
@@ -380,10 +492,16 @@ def main():
                          "peak_source": f"{src} bf16 sustained (f16 and bf16 share the dense tensor rate)",
                          "kernel": "attn_kernel<dense>: tcgen05 f16, Q in TMEM, 64 rows x 80 keys"
                          if isinstance(run, DenseRun) else
-                         "indexer (mma.sync e4m3) + top-k + attn_kernel<sparse> (tcgen05 f16)"},
+                         "indexer (tcgen05 e4m3) + top-k + attn_kernel<sparse> (tcgen05 f16)"},
             "gpu_launches": run.launches_per_step * args.steps}
     if clk:
         line["clocks"] = clk
+    if isinstance(run, ChunkedRun):
+        run.collect_chunk_ms()
+        line["chunks"] = {"count": len(run.bounds), "chunk_tokens": run.w.chunk,
+                          "ms_per_chunk_last_step": [round(x, 3) for x in run.chunk_ms],
+                          "dense_last_chunk_ms": run.dense_last_chunk_ms(),
+                          "sparse_last_chunk_ms": round(run.chunk_ms[-1], 3)}
     if rank == 0 and not args.no_e2e:
         r = run.e2e(args.steps, args.warmup)
         if r:
