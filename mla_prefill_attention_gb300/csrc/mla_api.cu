@@ -117,9 +117,12 @@ std::vector<int4> indexer_schedule(const mla_seqs_t *s) {
     return items;
 }
 
+// fp32 score row per query token; rows start 16-byte aligned (the top-k reads them 4 at a time)
+int64_t score_stride(const mla_seqs_t *s) { return (max_context(s) + 3) / 4 * 4; }
+
 size_t indexer_score_bytes(const mla_seqs_t *s) {
     const int64_t tq = s->cu_seqlens_q_host[s->batch];
-    return round_up(static_cast<size_t>(tq) * static_cast<size_t>(max_context(s)) * sizeof(float), kWsAlign);
+    return round_up(static_cast<size_t>(tq) * static_cast<size_t>(score_stride(s)) * sizeof(float), kWsAlign);
 }
 
 // 2-D tensor map over a row-major u8 matrix [rows][128] for TMA copies of
@@ -267,7 +270,7 @@ mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, co
     a.prefix_lens = seqs->prefix_lens;
     a.batch = seqs->batch;
     a.scores = static_cast<float *>(workspace);
-    a.score_stride = max_context(seqs);
+    a.score_stride = score_stride(seqs);
     a.topk = topk;
     a.idx_out = idx_out;
     a.dev_err = dev_err;
