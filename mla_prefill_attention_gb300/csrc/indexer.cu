@@ -30,10 +30,14 @@ __device__ __forceinline__ int find_seq(const int32_t *cu, int batch, int64_t t)
 // ---------------------------------------------------------------------------
 // exact top-k over one score row per token
 // ---------------------------------------------------------------------------
-constexpr int TK_NT = 1024;
-constexpr int TK_CAP = 6144;
-constexpr int TK_SEL = 2048;            // selected positions (max topk), sorted before the write
+constexpr int TK_NT = 512;              // two CTAs per SM hide each other's barriers
+constexpr int TK_NW = TK_NT / 32;
+constexpr int TK_U = 4;                 // float4 loads in flight per thread and pass step
+constexpr int TK_STEP = 4 * TK_U * TK_NT;   // scores per step of a global pass
+constexpr int TK_CAP = 8192;            // keys sharing the k-th key's prefix kept in shared memory
+constexpr int TK_SEL = 2048;            // selected positions (max topk)
 constexpr int TK_SMEM = TK_CAP * 8 + 4096 * 4 + TK_SEL * 4;
+static_assert(TK_STEP < 65536 && TK_CAP < 65536, "per-step counts are packed in 16 bits");
 
 __device__ __forceinline__ uint32_t ord_f32(float x) {
     if (x != x) return 0u;          // NaN ranks below everything
@@ -49,45 +53,14 @@ __device__ __forceinline__ bool prefix_match(uint64_t k, uint64_t prefix, int bi
 }
 
 struct TkState {
-    uint64_t prefix;
-    int bits;
-    uint32_t krem, cnt, ncand;
-    uint32_t wtot[32];
-    uint32_t base;
+    uint64_t prefix;    // digits fixed so far (high bits of the k-th key)
+    int bits;           // how many
+    uint32_t krem;      // rank of the k-th key among the keys with that prefix (1-based)
+    uint32_t cnt;       // how many keys share the prefix
 };
 
-// Pick the digit holding the krem-th largest key; warp 0 only.
-__device__ void pick_digit(const uint32_t *hist, int width, int shift, TkState &st) {
-    const int lane = threadIdx.x & 31;
-    const int nb = 1 << width, per = nb / 32;
-    uint32_t sum = 0;
-    for (int d = lane * per; d < lane * per + per; ++d) sum += hist[d];
-    // above = sum over lanes with higher bins
-    uint32_t incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_down_sync(0xffffffffu, incl, o);
-        if (lane + o < 32) incl += v;
-    }
-    const uint32_t above = incl - sum;
-    const uint32_t krem = st.krem;
-    if (above < krem && krem <= above + sum) {
-        uint32_t acc = above;
-        for (int d = lane * per + per - 1; d >= lane * per; --d) {
-            if (acc + hist[d] >= krem) {
-                st.prefix |= static_cast<uint64_t>(d) << shift;
-                st.bits += width;
-                st.krem = krem - acc;
-                st.cnt = hist[d];
-                break;
-            }
-            acc += hist[d];
-        }
-    }
-}
-
-// Exclusive block-wide prefix sum of v (every thread of the block calls it);
-// also returns the block total. wsum: 32 words of shared scratch.
+// Exclusive block-wide prefix sum of v in thread order; also the block total.
+// wsum: TK_NW + 1 words of shared scratch. Every thread of the block calls it.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *wsum, uint32_t &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t incl = v;
@@ -99,21 +72,64 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *wsum, 
     if (lane == 31) wsum[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        const uint32_t w = wsum[lane];
+        const uint32_t w = lane < TK_NW ? wsum[lane] : 0u;
         uint32_t wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t u = __shfl_up_sync(0xffffffffu, wi, o);
             if (lane >= o) wi += u;
         }
-        wsum[lane] = wi - w;                 // exclusive prefix of the warp totals
-        if (lane == 31) wsum[32] = wi;       // block total
+        if (lane < TK_NW) wsum[lane] = wi - w;
+        if (lane == 31) wsum[TK_NW] = wi;
     }
     __syncthreads();
     const uint32_t r = wsum[warp] + incl - v;
-    total = wsum[32];
+    total = wsum[TK_NW];
     __syncthreads();                         // wsum is reused by the next call
     return r;
+}
+
+// The same over TK_U values per thread, ordered (u, thread): r[u] counts the
+// values of every earlier u and of the lower threads at the same u.
+// wsum: TK_U * TK_NW + 1 words.
+__device__ __forceinline__ void block_excl_scan_u(const uint32_t (&v)[TK_U], uint32_t (&r)[TK_U], uint32_t *wsum,
+                                                  uint32_t &total) {
+    static_assert(TK_U * TK_NW == 64, "warp 0 scans two words per lane");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl[TK_U];
+#pragma unroll
+    for (int u = 0; u < TK_U; ++u) {
+        incl[u] = v[u];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(0xffffffffu, incl[u], o);
+            if (lane >= o) incl[u] += x;
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int u = 0; u < TK_U; ++u) wsum[u * TK_NW + warp] = incl[u];
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t w0 = wsum[lane], w1 = wsum[lane + 32];
+        uint32_t a = w0, b = w1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t xa = __shfl_up_sync(0xffffffffu, a, o);
+            const uint32_t xb = __shfl_up_sync(0xffffffffu, b, o);
+            if (lane >= o) { a += xa; b += xb; }
+        }
+        const uint32_t ta = __shfl_sync(0xffffffffu, a, 31);
+        wsum[lane] = a - w0;
+        wsum[lane + 32] = ta + b - w1;
+        if (lane == 31) wsum[64] = ta + b;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < TK_U; ++u) r[u] = wsum[u * TK_NW + warp] + incl[u] - v[u];
+    total = wsum[64];
+    __syncthreads();
 }
 
 // Histogram of one digit over the keys that match the current prefix; lanes
@@ -125,33 +141,84 @@ __device__ __forceinline__ void hist_add(uint32_t *hist, bool act, uint32_t bin)
     if (act && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
 }
 
+// Pick the digit (one of 2^width bins, PER bins per thread) that holds the
+// krem-th largest key and narrow the state to it. Every thread calls it; bins
+// are taken in descending order so a block scan gives the keys above each.
+template <int PER>    // 4096 bins: PER = 8, all threads in range; 256 bins: PER = 1
+__device__ __forceinline__ void pick_digit(const uint32_t *hist, int width, int shift, TkState &st, uint32_t *wsum) {
+    const int nb = 1 << width;
+    const int tid = threadIdx.x;
+    const int lo = nb - PER * (tid + 1);            // this thread's lowest bin
+    uint32_t h[PER];
+    uint32_t sum = 0;
+    if constexpr (PER % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < PER; i += 4) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(hist + lo + i);
+            h[i] = w.x; h[i + 1] = w.y; h[i + 2] = w.z; h[i + 3] = w.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) h[i] = lo >= 0 ? hist[lo + i] : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) sum += h[i];
+    uint32_t tot;
+    const uint32_t above = block_excl_scan(sum, wsum, tot);
+    const uint32_t krem = st.krem;
+    if (above < krem && krem <= above + sum) {      // exactly one thread
+        uint32_t acc = above;
+#pragma unroll
+        for (int i = PER - 1; i >= 0; --i) {
+            if (acc < krem && krem <= acc + h[i]) {
+                st.prefix |= static_cast<uint64_t>(lo + i) << shift;
+                st.bits += width;
+                st.krem = krem - acc;
+                st.cnt = h[i];
+            }
+            acc += h[i];
+        }
+    }
+    __syncthreads();
+}
+
+__device__ __noinline__ void pick(const uint32_t *hist, int width, int shift, TkState &st, uint32_t *wsum) {
+    if (width == 12) pick_digit<4096 / TK_NT>(hist, width, shift, st, wsum);
+    else pick_digit<1>(hist, width, shift, st, wsum);
+}
+
+__device__ __forceinline__ void topk_fail(const IndexerArgs &a, int32_t *out) {
+    if (threadIdx.x == 0) set_dev_err(a.dev_err, MLA_DEVERR_INTERNAL);
+    for (int j = threadIdx.x; j < a.topk; j += TK_NT) out[j] = -1;
+}
+
 // Per token: the exact top-k under the total order of key64 (score desc, then
 // lower position first). Phase A: digit histograms over the global row until
 // the keys sharing the k-th key's prefix fit in shared memory. Phase B, one
-// more pass: keys above that prefix are winners and go straight to the output;
-// keys with the prefix are gathered into shared memory. Phase C resolves the
-// remaining digits there and phase D adds the candidates at or above the k-th
-// key. Both runs are gathered in position order in shared memory and merged,
-// so the row is written in ascending position order.
-__global__ void __launch_bounds__(TK_NT, 1) topk_kernel(const IndexerArgs a) {
+// more pass: keys above that prefix are winners and their positions are kept
+// in order; keys with the prefix are gathered, in order, into shared memory.
+// Phase C resolves the remaining digits there and phase D appends the
+// candidates at or above the k-th key. The two ascending runs are merged, so
+// the row is written in ascending position order.
+__global__ void __launch_bounds__(TK_NT, 2) topk_kernel(const IndexerArgs a) {
     extern __shared__ __align__(16) uint8_t tk_raw[];
     uint64_t *cand = reinterpret_cast<uint64_t *>(tk_raw);
     uint32_t *hist = reinterpret_cast<uint32_t *>(tk_raw + TK_CAP * 8);
     int32_t *sel = reinterpret_cast<int32_t *>(tk_raw + TK_CAP * 8 + 4096 * 4);
     __shared__ TkState st;
-    __shared__ uint32_t wsum[33];
+    __shared__ uint32_t wsum[TK_U * TK_NW + 1];
 
     const int64_t t = blockIdx.x;
     const int b = find_seq(a.cu_seqlens, a.batch, t);
-    const int64_t n = static_cast<int64_t>(__ldg(a.prefix_lens + b)) + (t - __ldg(a.cu_seqlens + b)) + 1;
+    const int n = __ldg(a.prefix_lens + b) + static_cast<int>(t - __ldg(a.cu_seqlens + b)) + 1;
     int32_t *out = a.idx_out + t * a.topk;
     const int tid = threadIdx.x;
     if (n <= a.topk) {
         for (int j = tid; j < a.topk; j += TK_NT) out[j] = j < n ? j : -1;
         return;
     }
-    const float *row = a.scores + t * a.score_stride;
-    const float4 *row4 = reinterpret_cast<const float4 *>(row);
+    const float4 *row4 = reinterpret_cast<const float4 *>(a.scores + t * a.score_stride);
+    const int n4 = (n + 3) >> 2;           // the row stride is a multiple of 4 floats
     const int widths[6] = {12, 12, 8, 12, 12, 8};
     if (tid == 0) {
         st.prefix = 0;
@@ -162,77 +229,94 @@ __global__ void __launch_bounds__(TK_NT, 1) topk_kernel(const IndexerArgs a) {
     __syncthreads();
     int di = 0;
     // ---- phase A: digit passes over the global row while the prefix holds too many keys ----
-    while (di < 6 && st.bits < 64 && st.cnt > TK_CAP) {
+    while (di < 6 && st.cnt > TK_CAP) {
         const int width = widths[di++], shift = 64 - st.bits - width;
         const uint64_t prefix = st.prefix;
         const int bits = st.bits;
         for (int d = tid; d < (1 << width); d += TK_NT) hist[d] = 0;
         __syncthreads();
-        for (int64_t s4 = tid; 4 * s4 < n; s4 += TK_NT) {
-            const float4 v = row4[s4];
-            const float f[4] = {v.x, v.y, v.z, v.w};
+        for (int q0 = 0; q0 < n4; q0 += TK_U * TK_NT) {
+            float4 v[TK_U];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int64_t s = 4 * s4 + e;
-                const uint64_t k = key64(f[e], static_cast<int>(s));
-                hist_add(hist, s < n && prefix_match(k, prefix, bits),
-                         static_cast<uint32_t>((k >> shift) & ((1u << width) - 1)));
+            for (int u = 0; u < TK_U; ++u) {
+                const int q = q0 + u * TK_NT + tid;
+                v[u] = q < n4 ? row4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < TK_U; ++u) {
+                const int s0 = 4 * (q0 + u * TK_NT + tid);
+                const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint64_t k = key64(f[e], s0 + e);
+                    hist_add(hist, s0 + e < n && prefix_match(k, prefix, bits),
+                             static_cast<uint32_t>((k >> shift) & ((1u << width) - 1)));
+                }
             }
         }
         __syncthreads();
-        if (tid < 32) pick_digit(hist, width, shift, st);
-        __syncthreads();
+        pick(hist, width, shift, st, wsum);
     }
     const uint64_t prefix = st.prefix;
     const int bits = st.bits;
     const uint32_t need = st.krem;                       // still to pick among the prefix's keys
     const uint32_t n_win = static_cast<uint32_t>(a.topk) - need;
-    // ---- phase B: winners above the prefix to the output, the prefix's keys to smem ----
+    // ---- phase B: positions above the prefix in order, the prefix's keys to smem ----
+    uint32_t nc;
     {
         uint32_t wbase = 0, cbase = 0;
-        for (int64_t c0 = 0; c0 < n; c0 += 4 * TK_NT) {
-            const int64_t s0 = c0 + 4 * tid;
-            uint64_t k[4];
-            uint32_t win = 0, cnd = 0;
-            if (s0 < n) {
-                const float4 v = row4[s0 >> 2];
-                const float f[4] = {v.x, v.y, v.z, v.w};
+        for (int q0 = 0; q0 < n4; q0 += TK_U * TK_NT) {
+            float4 v[TK_U];
+#pragma unroll
+            for (int u = 0; u < TK_U; ++u) {
+                const int q = q0 + u * TK_NT + tid;
+                v[u] = q < n4 ? row4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            uint32_t win[TK_U], cnd[TK_U], cnt[TK_U], off[TK_U];
+#pragma unroll
+            for (int u = 0; u < TK_U; ++u) {
+                const int s0 = 4 * (q0 + u * TK_NT + tid);
+                const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                win[u] = 0;
+                cnd[u] = 0;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    k[e] = key64(f[e], static_cast<int>(s0 + e));
+                    const uint64_t k = key64(f[e], s0 + e);
                     if (s0 + e < n) {
-                        if (bits > 0 && (k[e] >> (64 - bits)) > (prefix >> (64 - bits))) win |= 1u << e;
-                        else if (prefix_match(k[e], prefix, bits)) cnd |= 1u << e;
+                        if (bits > 0 && (k >> (64 - bits)) > (prefix >> (64 - bits))) win[u] |= 1u << e;
+                        else if (prefix_match(k, prefix, bits)) cnd[u] |= 1u << e;
                     }
                 }
+                cnt[u] = (static_cast<uint32_t>(__popc(cnd[u])) << 16) | static_cast<uint32_t>(__popc(win[u]));
             }
             uint32_t tot;
-            const uint32_t off = block_excl_scan((static_cast<uint32_t>(__popc(cnd)) << 16) | __popc(win), wsum, tot);
-            uint32_t wo = wbase + (off & 0xFFFFu), co = cbase + (off >> 16);
+            block_excl_scan_u(cnt, off, wsum, tot);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (win >> e & 1u) {
-                    if (wo < n_win) sel[wo] = static_cast<int32_t>(s0 + e);
-                    ++wo;
-                } else if (cnd >> e & 1u) {
-                    if (co < TK_CAP) cand[co] = k[e];
-                    ++co;
+            for (int u = 0; u < TK_U; ++u) {
+                const int s0 = 4 * (q0 + u * TK_NT + tid);
+                const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                uint32_t wo = wbase + (off[u] & 0xFFFFu), co = cbase + (off[u] >> 16);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (win[u] >> e & 1u) {
+                        if (wo < n_win) sel[wo] = s0 + e;
+                        ++wo;
+                    } else if (cnd[u] >> e & 1u) {
+                        if (co < TK_CAP) cand[co] = key64(f[e], s0 + e);
+                        ++co;
+                    }
                 }
             }
             wbase += tot & 0xFFFFu;
             cbase += tot >> 16;
         }
-        if (tid == 0) st.ncand = cbase;
-        __syncthreads();
         if (wbase != n_win || cbase > TK_CAP) {   // the histograms guarantee both; report instead of guessing
-            if (tid == 0) set_dev_err(a.dev_err, MLA_DEVERR_INTERNAL);
-            for (int j = tid; j < a.topk; j += TK_NT) out[j] = -1;
+            topk_fail(a, out);
             return;
         }
+        nc = cbase;
     }
     // ---- phase C: remaining digits among the candidates, in shared memory ----
-    const uint32_t nc = st.ncand;
-    if (tid == 0) st.krem = need;
     __syncthreads();
     while (di < 6 && st.bits < 64) {
         const int width = widths[di++], shift = 64 - st.bits - width;
@@ -245,29 +329,35 @@ __global__ void __launch_bounds__(TK_NT, 1) topk_kernel(const IndexerArgs a) {
             hist_add(hist, prefix_match(k, pf, bb), static_cast<uint32_t>((k >> shift) & ((1u << width) - 1)));
         }
         __syncthreads();
-        if (tid < 32) pick_digit(hist, width, shift, st);
-        __syncthreads();
+        pick(hist, width, shift, st, wsum);
     }
     if (st.bits != 64) {
-        if (tid == 0) set_dev_err(a.dev_err, MLA_DEVERR_INTERNAL);
-        for (int j = tid; j < a.topk; j += TK_NT) out[j] = -1;
+        topk_fail(a, out);
         return;
     }
-    // ---- phase D: candidates at or above the k-th key, after the winners ----
+    // ---- phase D: candidates at or above the k-th key, in order, after the winners ----
     const uint64_t kth = st.prefix;
     uint32_t base = n_win;
-    for (uint32_t c0 = 0; c0 < nc; c0 += TK_NT) {
-        const uint32_t i = c0 + tid;
-        const bool f = i < nc && cand[i] >= kth;
+    for (uint32_t c0 = 0; c0 < nc; c0 += 4 * TK_NT) {
+        const uint32_t i0 = c0 + 4 * tid;
+        uint32_t f = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (i0 + j < nc && cand[i0 + j] >= kth) f |= 1u << j;
         uint32_t tot;
-        const uint32_t off = block_excl_scan(f ? 1u : 0u, wsum, tot);
-        if (f && base + off < static_cast<uint32_t>(a.topk))
-            sel[base + off] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(cand[i] & 0xFFFFFFFFu));
+        uint32_t o = base + block_excl_scan(static_cast<uint32_t>(__popc(f)), wsum, tot);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (f >> j & 1u) {
+                if (o < static_cast<uint32_t>(a.topk))
+                    sel[o] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(cand[i0 + j] & 0xFFFFFFFFu));
+                ++o;
+            }
+        }
         base += tot;
     }
     if (base != static_cast<uint32_t>(a.topk)) {  // exactly `need` distinct keys sit at or above the k-th
-        if (tid == 0) set_dev_err(a.dev_err, MLA_DEVERR_INTERNAL);
-        for (int j = tid; j < a.topk; j += TK_NT) out[j] = -1;
+        topk_fail(a, out);
         return;
     }
     // ---- ascending positions: merge the two ascending runs (winners, then candidates);
