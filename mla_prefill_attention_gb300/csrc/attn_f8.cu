@@ -1,0 +1,681 @@
+// Dense MLA prefill attention with e4m3 tensor-core operands (tcgen05 kind::f8f6f4).
+//
+// The cache holds e4m3 codes, so the key/value operand needs no conversion: a
+// 96-key tile is copied by TMA straight from its pages into 128-byte-swizzled
+// shared memory, and both MMAs read the codes as they are. The other operand of
+// each product is split into two e4m3 terms whose sum carries bf16 precision:
+//
+//   Q/s_Q = Qh + Ql   (s_Q a power of two per row; for bf16 input the split is
+//                      exact while |Q/s_Q| >= 2^-2, and the largest element sits
+//                      in [128, 256))
+//   P     = Ph + Pl   (P rounded to f16 first; 8 significant bits in total)
+//
+//   S   = Qh K^T + Ql K^T          M=64 N=96, K=576 (A = Qh, Ql in TMEM)
+//   u   = S s_Q sigma sm_scale log2(e) + log2(sigma)
+//   P   = 2^(u - m + 6),  l += P / sigma     (m: reference max, log2 domain)
+//   O  += Ph V + Pl V              M=64 N=256 x 2 chunks of the 512 value dims
+//
+// and out = O / l, lse = ln2 (m - 6 + log2 l). The offset 6 keeps the largest
+// weights of a row in the normal e4m3 range (a P of 1 would leave most of the
+// row's mass in subnormals); the reference max moves when a tile raises a row's
+// max by more than 2 (log2 units), so P never exceeds 2^8 < 448.
+//
+// Each M=64 e4m3 MMA runs at 4096 MAC/clk per SM, twice the f16 rate, so the two
+// terms cost what one f16 product would; what goes away is the conversion pass
+// (no warp writes key data to shared memory) and half of the operand bytes.
+//
+// TMEM (M=64 layout: row r in lane 32*(r/16) + r%16 + 16*h, h = lane half)
+//   h=0 cols   0..143 : Qh (576 codes, four per column)
+//   h=0 cols 144..287 : Ql
+//   h=0 cols 288..383 : S buffer 0,  cols 384..479 : S buffer 1
+//   h=1 cols   0..511 : O
+//
+// Shared memory
+//   3 stages x 5 slices x [96 keys][128 B], 128-byte swizzle (TMA box 128 B x 32
+//     keys; a page holds 8 boxes, so no box straddles a page). Slices 0-3 are
+//     the value dims (K-major for QK, MN-major for PV); slice 4 is the RoPE part
+//     (dims 512..575, the box's upper 64 bytes zero-filled by TMA)
+//   P: 2 buffers x {Ph, Pl} x [64 rows][96 keys], K-major without swizzle
+//     (16-byte x 8-row core matrices; 128 B apart along the keys, 768 B apart
+//     along the rows)
+//
+// Warps: 0-3 softmax (as in the f16 kernel: warp w owns TMEM quadrant w, thread
+// (tq, tc) rows 16w + tq and 16w + tq + 8 x 24 keys; they also split Q into
+// TMEM and run the epilogue), 4 TMA producer and key metadata, 5 MMA issue.
+// Keys past a row tile's causal limit are zeroed in shared memory (they may be
+// unwritten cache rows; a NaN code there would survive a zero weight).
+// Every wait is bounded; one that runs out sets MLA_DEVERR_TIMEOUT.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace mla {
+namespace f8attn {
+
+using namespace tc;
+
+constexpr int BM = 64;                          // query rows per tile
+constexpr int BN = 96;                          // keys per tile
+constexpr int NT = 192;                         // 6 warps
+constexpr int kProducerWarp = 4, kIssuerWarp = 5;
+constexpr int kBox = 32;                        // keys per TMA box
+constexpr int kBoxes = BN / kBox;
+constexpr int kSlices = 5;
+constexpr int kSliceBytes = BN * 128;           // 12288
+constexpr int kBoxBytes = kBox * 128;           // 4096
+constexpr int kStageBytes = kSlices * kSliceBytes;
+constexpr int kStages = 3;
+constexpr int kPBytes = BM * BN;                // one e4m3 term of P: 6144
+constexpr int kOffP = kStages * kStageBytes;
+constexpr int kDynSmem = 1024 + kOffP + 4 * kPBytes;
+constexpr long long kWaitCycles = 200000000LL;
+constexpr float kRescaleThreshold = 2.0f;
+constexpr float kPOffset = 6.0f;
+static_assert(kPage % kBox == 0, "a TMA box must not straddle a page");
+
+constexpr uint32_t kColQh = 0, kColQl = 144, kColS = 288;
+constexpr uint32_t kHalf1 = 16u << 16;
+
+enum Bar {
+    B_FULL = 0,          // [3] producer (+TMA bytes) -> issuer: stage loaded
+    B_EMPTY = 3,         // [3] issuer (commit) -> producer: PV done with the stage
+    B_META = 6,          // [4] producer -> softmax: key metadata of tile t, ring t&3
+    B_S_FULL = 10,       // [2] issuer (commit) -> softmax
+    B_S_FREE = 12,       // [2] softmax -> issuer
+    B_P_FULL = 14,       // [2] softmax -> issuer (P written, O rescaled)
+    B_PV_DONE = 16,      // [2] issuer (commit) -> softmax
+    B_Q_FULL = 18,       //     softmax -> issuer
+    B_O_FREE = 19,       //     softmax -> issuer: epilogue done with O
+    B_FINAL = 20,        //     issuer -> teardown
+    B_FIX = 21,          //     producer's own: a box whose tail it zeroes
+    NBAR = 22
+};
+
+struct __align__(16) KeyMeta {
+    float4 sl[BN / 2];    // sigma of keys 2p, 2p+1; log2 sigma of both (-inf: masked)
+    float2 isig[BN / 2];  // 1/sigma of both
+};
+
+struct Shared {
+    KeyMeta meta[4];
+    uint64_t bar[NBAR];
+    uint32_t tmem_base;
+};
+
+struct Wait {
+    Shared *sh;
+    int32_t *dev_err;
+    __device__ bool operator()(int b, uint32_t parity) const {
+        if (mbar_wait_cycles(smem_u32(&sh->bar[b]), parity, kWaitCycles)) return true;
+        set_dev_err(dev_err, MLA_DEVERR_TIMEOUT);
+        return false;
+    }
+};
+
+struct RowTile {
+    int64_t grow0;      // first global query row (token*H + head)
+    int nvalid;         // valid rows
+    int n_ktiles;       // key tiles to visit
+    int key_last;       // last key position visible to any row
+};
+
+__device__ __forceinline__ RowTile make_tile(const AttnArgs &a, int b, int tile) {
+    RowTile rt;
+    const int q0 = __ldg(a.cu_seqlens + b), qn = __ldg(a.cu_seqlens + b + 1) - q0;
+    const int P = __ldg(a.prefix_lens + b);
+    const int rows = qn * a.H, r_lo = tile * BM;
+    rt.grow0 = static_cast<int64_t>(q0) * a.H + r_lo;
+    rt.nvalid = min(BM, rows - r_lo);
+    rt.key_last = P + (r_lo + rt.nvalid - 1) / a.H;
+    rt.n_ktiles = rt.key_last / BN + 1;
+    return rt;
+}
+
+__device__ __forceinline__ int row_limit(const AttnArgs &a, const RowTile &rt, int b, int row) {
+    if (row >= rt.nvalid) return -1;
+    const int r_lo = static_cast<int>(rt.grow0 - static_cast<int64_t>(__ldg(a.cu_seqlens + b)) * a.H);
+    return __ldg(a.prefix_lens + b) + (r_lo + row) / a.H;
+}
+
+struct Walk {
+    int n0, total;
+    __device__ int r(int t) const { return t < n0 ? 0 : 1; }
+    __device__ int j(int t) const { return t < n0 ? t : t - n0; }
+};
+
+// ---------------------------------------------------------------------------
+// e4m3 conversions
+// ---------------------------------------------------------------------------
+// Two floats -> e4m3 codes (lo in byte 0), round to nearest even, saturating.
+__device__ __forceinline__ uint32_t e4m3x2_of(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ uint32_t e4m3x2_of_f16x2(uint32_t h) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+    return r;
+}
+__device__ __forceinline__ uint32_t f16x2_of_e4m3x2(uint32_t c) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(c)));
+    return r;
+}
+__device__ __forceinline__ uint32_t hsub2_bits(uint32_t x, uint32_t y) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
+    return r;
+}
+__device__ __forceinline__ float2 float2_of_f16x2(uint32_t h) {
+    __half2 v;
+    *reinterpret_cast<uint32_t *>(&v) = h;
+    return __half22float2(v);
+}
+// (p0, p1) -> (head codes) | (tail codes) << 16: head = e4m3 of the f16 values,
+// tail = e4m3 of what the head leaves (exact in f16).
+__device__ __forceinline__ uint32_t split_p2(float p0, float p1) {
+    const uint32_t h = pack_half2(p0, p1);
+    const uint32_t hd = e4m3x2_of_f16x2(h);
+    const uint32_t tl = e4m3x2_of_f16x2(hsub2_bits(h, f16x2_of_e4m3x2(hd)));
+    return hd | (tl << 16);
+}
+
+// Q rows ra, rb of the tile -> Qh, Ql in TMEM (lane half 0; 16x256b layout:
+// column group g holds dims 32g + 8tc .. +7 of this thread's rows). Returns the
+// logit scale s_Q * sm_scale * log2(e) per row.
+__device__ __forceinline__ void load_q_split(const AttnArgs &a, const RowTile &rt, uint32_t tq_addr, int ra, int rb,
+                                             int tc, float &rs_a, float &rs_b) {
+    const bool oka = ra < rt.nvalid, okb = rb < rt.nvalid;
+    const uint4 *qa = reinterpret_cast<const uint4 *>(a.q + (rt.grow0 + (oka ? ra : 0)) * kDqk + 8 * tc);
+    const uint4 *qb = reinterpret_cast<const uint4 *>(a.q + (rt.grow0 + (okb ? rb : 0)) * kDqk + 8 * tc);
+    float mxa = 0.f, mxb = 0.f;
+#pragma unroll 6
+    for (int g = 0; g < 18; ++g) {
+        const uint4 va = oka ? __ldg(qa + 4 * g) : make_uint4(0, 0, 0, 0);
+        const uint4 vb = okb ? __ldg(qb + 4 * g) : make_uint4(0, 0, 0, 0);
+        const __nv_bfloat162 *ha = reinterpret_cast<const __nv_bfloat162 *>(&va);
+        const __nv_bfloat162 *hb = reinterpret_cast<const __nv_bfloat162 *>(&vb);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 fa = __bfloat1622float2(ha[e]), fb = __bfloat1622float2(hb[e]);
+            mxa = fmaxf(mxa, fmaxf(fabsf(fa.x), fabsf(fa.y)));
+            mxb = fmaxf(mxb, fmaxf(fabsf(fb.x), fabsf(fb.y)));
+        }
+    }
+    mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
+    mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
+    mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
+    mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
+    // s_Q = 2^(e - 8) for max = f 2^e, f in [0.5, 1): the largest |Q/s_Q| is in [128, 256)
+    int ea = 0, eb = 0;
+    if (mxa > 0.f) frexpf(mxa, &ea);
+    if (mxb > 0.f) frexpf(mxb, &eb);
+    const float ia = mxa > 0.f ? ldexpf(1.f, 8 - ea) : 1.f, ib = mxb > 0.f ? ldexpf(1.f, 8 - eb) : 1.f;
+    rs_a = a.sm_scale_log2 / ia;
+    rs_b = a.sm_scale_log2 / ib;
+    // a row's 8 dims of one group -> (head word pair, tail word pair)
+    auto split8 = [](const uint4 &v, float inv, uint32_t (&hd)[2], uint32_t (&tl)[2]) {
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            const float2 f0 = __bfloat1622float2(h[2 * w]), f1 = __bfloat1622float2(h[2 * w + 1]);
+            const float x0 = f0.x * inv, x1 = f0.y * inv, x2 = f1.x * inv, x3 = f1.y * inv;
+            const uint32_t h01 = e4m3x2_of(x0, x1), h23 = e4m3x2_of(x2, x3);
+            const float2 g01 = float2_of_f16x2(f16x2_of_e4m3x2(h01)), g23 = float2_of_f16x2(f16x2_of_e4m3x2(h23));
+            hd[w] = h01 | (h23 << 16);
+            tl[w] = e4m3x2_of(x0 - g01.x, x1 - g01.y) | (e4m3x2_of(x2 - g23.x, x3 - g23.y) << 16);
+        }
+    };
+#pragma unroll 1
+    for (int g0 = 0; g0 < 18; g0 += 8) {
+        uint32_t wh[32], wl[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int g = g0 + i;
+            uint4 va = make_uint4(0, 0, 0, 0), vb = make_uint4(0, 0, 0, 0);
+            if (g < 18) {
+                if (oka) va = __ldg(qa + 4 * g);
+                if (okb) vb = __ldg(qb + 4 * g);
+            }
+            uint32_t ha[2], la[2], hb[2], lb[2];
+            split8(va, ia, ha, la);
+            split8(vb, ib, hb, lb);
+            wh[4 * i + 0] = ha[0];
+            wh[4 * i + 1] = ha[1];
+            wh[4 * i + 2] = hb[0];
+            wh[4 * i + 3] = hb[1];
+            wl[4 * i + 0] = la[0];
+            wl[4 * i + 1] = la[1];
+            wl[4 * i + 2] = lb[0];
+            wl[4 * i + 3] = lb[1];
+        }
+        if (g0 + 8 <= 18) {
+            tmem_st_16x256b_x8(tq_addr + kColQh + 8 * g0, wh);
+            tmem_st_16x256b_x8(tq_addr + kColQl + 8 * g0, wl);
+        } else {
+            tmem_st_16x256b_x2(tq_addr + kColQh + 8 * g0, wh);
+            tmem_st_16x256b_x2(tq_addr + kColQl + 8 * g0, wl);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(NT, 1)
+    attn_f8_kernel(const AttnArgs a, const int4 *__restrict__ work, const __grid_constant__ CUtensorMap tmap_kv) {
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    __shared__ Shared sh;
+    const uint32_t raw = smem_u32(dsm);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint8_t *sbase = dsm + pad;
+    const uint32_t sbase_a = raw + pad;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const int4 it = work[blockIdx.x];
+    const int b = it.x;
+    const int tiles[2] = {it.y, it.z};
+    const int n_rt = tiles[1] >= 0 ? 2 : 1;
+    const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.max_blocks;
+    Walk walk;
+    walk.n0 = make_tile(a, b, tiles[0]).n_ktiles;
+    walk.total = walk.n0 + (n_rt > 1 ? make_tile(a, b, tiles[1]).n_ktiles : 0);
+
+    if (tid == 0) {
+        for (int i = 0; i < NBAR; ++i) {
+            uint32_t cnt = 1;
+            if ((i >= B_S_FREE && i < B_S_FREE + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) || i == B_Q_FULL ||
+                i == B_O_FREE)
+                cnt = 4;
+            mbar_init(smem_u32(&sh.bar[i]), cnt);
+        }
+        mbar_fence_init();
+    }
+    if (warp == kIssuerWarp) {
+        tmem_alloc(smem_u32(&sh.tmem_base), 512);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = sh.tmem_base;
+    const Wait wait{&sh, a.dev_err};
+
+    if (warp == kProducerWarp) {
+        // =================== TMA producer + key metadata ===================
+        if (lane == 0) tma_prefetch_desc(&tmap_kv);
+        RowTile rt = make_tile(a, b, tiles[0]);
+        uint32_t fix_phase = 0;
+        bool ok = true;
+        for (int t = 0; t < walk.total && ok; ++t) {
+            const int st = t % kStages;
+            if (t >= kStages && !(ok = wait(B_EMPTY + st, ((t / kStages) - 1) & 1))) break;
+            if (t > 0 && walk.r(t) != walk.r(t - 1)) rt = make_tile(a, b, tiles[1]);
+            const int key0 = walk.j(t) * BN;
+            // metadata (its ring slot was last read by the softmax of tile t-4, which
+            // finished before PV(t-3), the stage release just waited for)
+            KeyMeta &mt = sh.meta[t & 3];
+#pragma unroll
+            for (int i = 0; i < BN / 32; ++i) {
+                const int k = lane + 32 * i, pos = key0 + k;
+                int64_t row = -1;
+                if (pos <= rt.key_last) row = cache_row(bt, a.max_blocks, a.num_blocks, pos, a.dev_err);
+                const float sig = row >= 0 ? __ldg(a.kv_scale + row) : 1.f;
+                float *sl = reinterpret_cast<float *>(&mt.sl[k >> 1]);
+                sl[k & 1] = sig;
+                sl[2 + (k & 1)] = row >= 0 ? __log2f(sig) : -INFINITY;
+                reinterpret_cast<float *>(&mt.isig[k >> 1])[k & 1] = 1.f / sig;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_META + (t & 3)]));
+            // boxes: whole ones by TMA; one straddling the causal limit by TMA, then its
+            // tail zeroed; ones past the limit (or on a bad page) zeroed
+            const uint32_t sdst = sbase_a + st * kStageBytes;
+            int nval[kBoxes];
+            int64_t brow[kBoxes];
+            uint32_t full_bytes = 0;
+#pragma unroll
+            for (int g = 0; g < kBoxes; ++g) {
+                const int p0 = key0 + kBox * g;
+                nval[g] = max(0, min(kBox, rt.key_last - p0 + 1));
+                brow[g] = nval[g] > 0 ? cache_row(bt, a.max_blocks, a.num_blocks, p0, a.dev_err) : -1;
+                if (brow[g] < 0) nval[g] = 0;
+                if (nval[g] == kBox) full_bytes += kSlices * kBoxBytes;
+            }
+            if (lane == 0) {
+                mbar_add_tx(smem_u32(&sh.bar[B_FULL + st]), full_bytes);
+#pragma unroll
+                for (int g = 0; g < kBoxes; ++g) {
+                    if (nval[g] != kBox) continue;
+#pragma unroll
+                    for (int s = 0; s < kSlices; ++s)
+                        tma_load_2d(sdst + s * kSliceBytes + g * kBoxBytes, &tmap_kv, 128 * s,
+                                    static_cast<int>(brow[g]), smem_u32(&sh.bar[B_FULL + st]));
+                }
+            }
+            bool zeroed = false;
+#pragma unroll 1
+            for (int g = 0; g < kBoxes; ++g) {
+                if (nval[g] == kBox) continue;
+                if (nval[g] > 0) {
+                    if (lane == 0) {
+                        mbar_expect_tx(smem_u32(&sh.bar[B_FIX]), kSlices * kBoxBytes);
+                        for (int s = 0; s < kSlices; ++s)
+                            tma_load_2d(sdst + s * kSliceBytes + g * kBoxBytes, &tmap_kv, 128 * s,
+                                        static_cast<int>(brow[g]), smem_u32(&sh.bar[B_FIX]));
+                    }
+                    if (!(ok = wait(B_FIX, fix_phase))) break;
+                    fix_phase ^= 1;
+                }
+                // rows nval..31 of the box, every slice (a row is 128 contiguous bytes)
+                for (int s = 0; s < kSlices; ++s) {
+                    uint8_t *box = sbase + st * kStageBytes + s * kSliceBytes + g * kBoxBytes;
+                    for (int o = nval[g] * 128 + 16 * lane; o < kBoxBytes; o += 512)
+                        *reinterpret_cast<uint4 *>(box + o) = make_uint4(0, 0, 0, 0);
+                }
+                zeroed = true;
+            }
+            if (!ok) break;
+            if (zeroed) fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL + st]));
+        }
+    } else if (warp == kIssuerWarp) {
+        // =================== MMA issuer ===================
+        const uint32_t lead = lane == 0 ? 1u : 0u;
+        const uint32_t id_qk = idesc_e4m3(BM, BN, false, false);
+        const uint32_t id_pv = idesc_e4m3(BM, 256, false, true);
+        const uint64_t dk0 = sdesc(sbase_a, 16, 1024, kSw128);              // K-major key slices
+        const uint64_t dv0 = sdesc(sbase_a, kSliceBytes, 1024, kSw128);     // MN-major value chunks
+        const uint64_t dp0 = sdesc(sbase_a + kOffP, 128, 768, kSwNone);     // P terms
+        bool ok = true;
+        auto qk = [&](int t) -> bool {
+            const int sb = t & 1, st = t % kStages;
+            if (!wait(B_FULL + st, (t / kStages) & 1)) return false;
+            if (t >= 2 && !wait(B_S_FREE + sb, ((t >> 1) - 1) & 1)) return false;
+            fence_after_sync();
+            const uint32_t d = tmem + kColS + BN * sb;
+#pragma unroll 1
+            for (int s = 0; s < kSlices; ++s) {
+                const uint64_t db = dk0 + static_cast<uint64_t>((st * kStageBytes + s * kSliceBytes) >> 4);
+                const int nks = s < 4 ? 4 : 2;   // the RoPE slice holds 64 dims
+#pragma unroll 4
+                for (int ks = 0; ks < nks; ++ks) {
+                    const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
+                    mma_e4m3_ts_w(d, tmem + kColQh + 32 * s + 8 * ks, db + 2 * ks, id_qk, acc, lead);
+                    mma_e4m3_ts_w(d, tmem + kColQl + 32 * s + 8 * ks, db + 2 * ks, id_qk, 1u, lead);
+                }
+            }
+            mma_commit_w(smem_u32(&sh.bar[B_S_FULL + sb]), lead);
+            return true;
+        };
+        auto pv = [&](int t) -> bool {
+            const int pb = t & 1, st = t % kStages, j = walk.j(t), r = walk.r(t);
+            if (j == 0 && r > 0 && !wait(B_O_FREE, (r - 1) & 1)) return false;
+            if (!wait(B_P_FULL + pb, (t >> 1) & 1)) return false;
+            fence_after_sync();
+            const uint64_t dph = dp0 + static_cast<uint64_t>(((2 * pb) * kPBytes) >> 4);
+            const uint64_t dpl = dp0 + static_cast<uint64_t>(((2 * pb + 1) * kPBytes) >> 4);
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+                const uint64_t dv = dv0 + static_cast<uint64_t>((st * kStageBytes + 2 * c * kSliceBytes) >> 4);
+                const uint32_t d = tmem + kHalf1 + 256u * c;
+#pragma unroll
+                for (int ks = 0; ks < BN / 32; ++ks) {
+                    mma_e4m3_ss_w(d, dph + 16 * ks, dv + 256 * ks, id_pv, (j > 0 || ks > 0) ? 1u : 0u, lead);
+                    mma_e4m3_ss_w(d, dpl + 16 * ks, dv + 256 * ks, id_pv, 1u, lead);
+                }
+            }
+            mma_commit_w(smem_u32(&sh.bar[B_EMPTY + st]), lead);
+            mma_commit_w(smem_u32(&sh.bar[B_PV_DONE + pb]), lead);
+            return true;
+        };
+        if (walk.total > 0) ok = wait(B_Q_FULL, 0) && qk(0);
+        for (int t = 0; t < walk.total && ok; ++t) {
+            const bool more = t + 1 < walk.total;
+            const bool new_rt = more && walk.r(t + 1) != walk.r(t);
+            if (more && !new_rt && !(ok = qk(t + 1))) break;
+            if (!(ok = pv(t))) break;
+            if (new_rt) {
+                if (!(ok = wait(B_Q_FULL, walk.r(t + 1) & 1))) break;
+                if (!(ok = qk(t + 1))) break;
+            }
+        }
+        mma_commit_w(smem_u32(&sh.bar[B_FINAL]), lead);
+    } else {
+        // =================== softmax / correction (warps 0-3) ===================
+        const int q = warp;
+        const int tq = lane >> 2, tc = lane & 3;
+        const int ra = 16 * q + tq, rb = ra + 8;
+        const uint32_t lane_lo = static_cast<uint32_t>(32 * q) << 16;
+        const uint32_t lane_hi = lane_lo + kHalf1;
+        // P word (own row, keys 8i + 4(tc/2) .. +3) at (row/8)*768 + (i/2)*128 + (row%8)*16 + 8(i&1) + 4(tc/2)
+        const bool even = (tc & 1) == 0;
+        const int prow = even ? ra : rb;
+        const uint32_t poff = static_cast<uint32_t>((prow >> 3) * 768 + (prow & 7) * 16 + 4 * (tc >> 1));
+        uint8_t *pbase = sbase + kOffP;
+        bool ok = true;
+        RowTile rt = make_tile(a, b, tiles[0]);
+        float rs_a, rs_b;
+        load_q_split(a, rt, tmem + lane_lo, ra, rb, tc, rs_a, rs_b);
+        tmem_st_wait();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_Q_FULL]));
+        int t = 0;
+        for (int r = 0; r < n_rt && ok; ++r) {
+            float m_a = -INFINITY, m_b = -INFINITY;
+            float l_a = 0.f, l_b = 0.f;
+            const int lim_a = row_limit(a, rt, b, ra), lim_b = row_limit(a, rt, b, rb);
+            const int lim_min = min(lim_a, lim_b);
+            for (int j = 0; j < rt.n_ktiles && ok; ++j, ++t) {
+                const int sb = t & 1;
+                if (!(ok = wait(B_META + (t & 3), (t >> 2) & 1))) break;
+                if (!(ok = wait(B_S_FULL + sb, (t >> 1) & 1))) break;
+                fence_after_sync();
+                uint32_t sv[48];
+                tmem_ld_16x256b_x8(tmem + lane_lo + kColS + BN * sb, sv);
+                tmem_ld_16x256b_x4(tmem + lane_lo + kColS + BN * sb + 64, sv + 32);
+                tmem_ld_wait();
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_S_FREE + sb]));
+                const KeyMeta &meta = sh.meta[t & 3];
+                const int key0 = j * BN;
+                const bool full = key0 + BN - 1 <= lim_min;
+                const float mu_a0 = m_a == -INFINITY ? 0.f : m_a - kPOffset;
+                const float mu_b0 = m_b == -INFINITY ? 0.f : m_b - kPOffset;
+                float mx_a = -INFINITY, mx_b = -INFINITY, lt_a = 0.f, lt_b = 0.f;
+                uint32_t pa[BN / 8], pb[BN / 8];   // per 8-key group: this thread's pair of row a / row b, head | tail << 16
+                auto logits = [&](auto with_p) {
+#pragma unroll
+                    for (int i = 0; i < BN / 8; ++i) {
+                        const int k0 = 8 * i + 2 * tc;
+                        const float4 m = meta.sl[4 * i + tc];
+                        float u0 = fmaf(__uint_as_float(sv[4 * i + 0]) * m.x, rs_a, m.z);
+                        float u1 = fmaf(__uint_as_float(sv[4 * i + 1]) * m.y, rs_a, m.w);
+                        float u2 = fmaf(__uint_as_float(sv[4 * i + 2]) * m.x, rs_b, m.z);
+                        float u3 = fmaf(__uint_as_float(sv[4 * i + 3]) * m.y, rs_b, m.w);
+                        if (!full) {
+                            u0 = key0 + k0 <= lim_a ? u0 : -INFINITY;
+                            u1 = key0 + k0 + 1 <= lim_a ? u1 : -INFINITY;
+                            u2 = key0 + k0 <= lim_b ? u2 : -INFINITY;
+                            u3 = key0 + k0 + 1 <= lim_b ? u3 : -INFINITY;
+                        }
+                        sv[4 * i + 0] = __float_as_uint(u0);
+                        sv[4 * i + 1] = __float_as_uint(u1);
+                        sv[4 * i + 2] = __float_as_uint(u2);
+                        sv[4 * i + 3] = __float_as_uint(u3);
+                        mx_a = fmaxf(mx_a, fmaxf(u0, u1));
+                        mx_b = fmaxf(mx_b, fmaxf(u2, u3));
+                        if (decltype(with_p)::value) {
+                            const float2 is = meta.isig[4 * i + tc];
+                            const float p0 = fast_exp2(u0 - mu_a0), p1 = fast_exp2(u1 - mu_a0);
+                            const float p2 = fast_exp2(u2 - mu_b0), p3 = fast_exp2(u3 - mu_b0);
+                            lt_a = fmaf(p0, is.x, fmaf(p1, is.y, lt_a));
+                            lt_b = fmaf(p2, is.x, fmaf(p3, is.y, lt_b));
+                            pa[i] = split_p2(p0, p1);
+                            pb[i] = split_p2(p2, p3);
+                        }
+                    }
+                };
+                if (j > 0) logits(std::true_type{});
+                else logits(std::false_type{});
+                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+                float al_a = 1.f, al_b = 1.f;
+                bool resc = false;
+                if (j == 0) {
+                    m_a = mx_a;
+                    m_b = mx_b;
+                } else {
+                    if (mx_a > m_a + kRescaleThreshold) {
+                        al_a = fast_exp2(m_a - mx_a);
+                        m_a = mx_a;
+                        resc = true;
+                    }
+                    if (mx_b > m_b + kRescaleThreshold) {
+                        al_b = fast_exp2(m_b - mx_b);
+                        m_b = mx_b;
+                        resc = true;
+                    }
+                }
+                const bool any_resc = __any_sync(0xffffffffu, resc);
+                if (j == 0 || any_resc) {
+                    const float mu_a = m_a == -INFINITY ? 0.f : m_a - kPOffset;
+                    const float mu_b = m_b == -INFINITY ? 0.f : m_b - kPOffset;
+                    lt_a = 0.f;
+                    lt_b = 0.f;
+#pragma unroll
+                    for (int i = 0; i < BN / 8; ++i) {
+                        const float2 is = meta.isig[4 * i + tc];
+                        const float p0 = fast_exp2(__uint_as_float(sv[4 * i + 0]) - mu_a);
+                        const float p1 = fast_exp2(__uint_as_float(sv[4 * i + 1]) - mu_a);
+                        const float p2 = fast_exp2(__uint_as_float(sv[4 * i + 2]) - mu_b);
+                        const float p3 = fast_exp2(__uint_as_float(sv[4 * i + 3]) - mu_b);
+                        lt_a = fmaf(p0, is.x, fmaf(p1, is.y, lt_a));
+                        lt_b = fmaf(p2, is.x, fmaf(p3, is.y, lt_b));
+                        pa[i] = split_p2(p0, p1);
+                        pb[i] = split_p2(p2, p3);
+                    }
+                }
+                l_a = fmaf(l_a, al_a, lt_a);
+                l_b = fmaf(l_b, al_b, lt_b);
+                if (any_resc) {
+                    if (!(ok = wait(B_PV_DONE + ((t - 1) & 1), ((t - 1) >> 1) & 1))) break;
+                    fence_after_sync();
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 512; c0 += 64) {
+                        uint32_t o[32];
+                        tmem_ld_16x256b_x8(tmem + lane_hi + c0, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            o[4 * i + 0] = __float_as_uint(__uint_as_float(o[4 * i + 0]) * al_a);
+                            o[4 * i + 1] = __float_as_uint(__uint_as_float(o[4 * i + 1]) * al_a);
+                            o[4 * i + 2] = __float_as_uint(__uint_as_float(o[4 * i + 2]) * al_b);
+                            o[4 * i + 3] = __float_as_uint(__uint_as_float(o[4 * i + 3]) * al_b);
+                        }
+                        tmem_st_16x256b_x8(tmem + lane_hi + c0, o);
+                    }
+                    tmem_st_wait();
+                }
+                // ---- P terms into buffer t&1 (last read by PV(t-2)) ----
+                if (t >= 2 && !(ok = wait(B_PV_DONE + sb, ((t >> 1) - 1) & 1))) break;
+                uint8_t *ph = pbase + (2 * sb) * kPBytes, *pl = ph + kPBytes;
+#pragma unroll
+                for (int i = 0; i < BN / 8; ++i) {
+                    // the even lane of a pair writes row a's word, the odd lane row b's
+                    const uint32_t own = even ? pa[i] : pb[i];
+                    const uint32_t oth = __shfl_xor_sync(0xffffffffu, even ? pb[i] : pa[i], 1);
+                    const uint32_t lo2 = even ? own : oth, hi2 = even ? oth : own;   // lower keys first
+                    const uint32_t hw = (lo2 & 0xFFFFu) | (hi2 << 16);
+                    const uint32_t lw = (lo2 >> 16) | (hi2 & 0xFFFF0000u);
+                    const uint32_t off = poff + (i >> 1) * 128 + 8 * (i & 1);
+                    *reinterpret_cast<uint32_t *>(ph + off) = hw;
+                    *reinterpret_cast<uint32_t *>(pl + off) = lw;
+                }
+                fence_proxy_async();
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_P_FULL + sb]));
+            }
+            if (!ok) break;
+            const RowTile rt_done = rt;
+            float rs_na = 0.f, rs_nb = 0.f;
+            if (r + 1 < n_rt) {
+                rt = make_tile(a, b, tiles[r + 1]);
+                load_q_split(a, rt, tmem + lane_lo, ra, rb, tc, rs_na, rs_nb);
+                tmem_st_wait();
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_Q_FULL]));
+            }
+            // ---- epilogue: O / l to bf16, lse ----
+            if (!(ok = wait(B_PV_DONE + ((t - 1) & 1), ((t - 1) >> 1) & 1))) break;
+            fence_after_sync();
+            l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+            l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+            l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+            l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+            const bool va = lim_a >= 0, vb = lim_b >= 0;
+            if (tc == 0 && a.lse) {
+                if (va) a.lse[rt_done.grow0 + ra] = l_a > 0.f ? (m_a - kPOffset + __log2f(l_a)) * kLn2 : -INFINITY;
+                if (vb) a.lse[rt_done.grow0 + rb] = l_b > 0.f ? (m_b - kPOffset + __log2f(l_b)) * kLn2 : -INFINITY;
+            }
+            const float ia = l_a > 0.f ? 1.f / l_a : 0.f, ib = l_b > 0.f ? 1.f / l_b : 0.f;
+            __nv_bfloat16 *da = a.out + (rt_done.grow0 + ra) * kDv + 2 * tc;
+            __nv_bfloat16 *db = a.out + (rt_done.grow0 + rb) * kDv + 2 * tc;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 512; c0 += 64) {
+                uint32_t o[32];
+                tmem_ld_16x256b_x8(tmem + lane_hi + c0, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (va)
+                        *reinterpret_cast<uint32_t *>(da + c0 + 8 * i) =
+                            pack_bf162(__uint_as_float(o[4 * i + 0]) * ia, __uint_as_float(o[4 * i + 1]) * ia);
+                    if (vb)
+                        *reinterpret_cast<uint32_t *>(db + c0 + 8 * i) =
+                            pack_bf162(__uint_as_float(o[4 * i + 2]) * ib, __uint_as_float(o[4 * i + 3]) * ib);
+                }
+            }
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_O_FREE]));
+            rs_a = rs_na;
+            rs_b = rs_nb;
+        }
+    }
+
+    // ----- teardown: every MMA complete before TMEM is released -----
+    __syncthreads();
+    if (warp == kIssuerWarp) {
+        if (!mbar_wait_cycles(smem_u32(&sh.bar[B_FINAL]), 0, kWaitCycles)) set_dev_err(a.dev_err, MLA_DEVERR_TIMEOUT);
+        fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace f8attn
+
+cudaError_t launch_dense_f8(const AttnArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_kv,
+                            cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(f8attn::attn_f8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         f8attn::kDynSmem);
+    if (e != cudaSuccess) return e;
+    if (n_work > 0) f8attn::attn_f8_kernel<<<n_work, f8attn::NT, f8attn::kDynSmem, st>>>(a, work, tmap_kv);
+    return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -124,7 +124,10 @@ extern "C" mla_status_t mla_prefill_dense_static(const mla_seqs_t *seqs, const v
     if ((e = cudaGetLastError()) != cudaSuccess) return mla::report(MLA_ERR_CUDA, cudaGetErrorString(e));
     const mla::AttnArgs a =
         mla::make_attn_args(seqs, q_bf16, num_heads, kv_e4m3, kv_scale, sm_scale, out_bf16, lse, dev_err);
-    e = mla::launch_dense_tc(a, work, static_cast<int>(items), stream);
+    CUtensorMap tmap_kv;
+    if (!mla::encode_kv_tmap(&tmap_kv, kv_e4m3, seqs->num_blocks))
+        return mla::report(MLA_ERR_CUDA, "tensor map encoding for the latent cache failed");
+    e = mla::launch_dense_f8(a, work, static_cast<int>(items), tmap_kv, stream);
     if (e != cudaSuccess) return mla::report(MLA_ERR_CUDA, cudaGetErrorString(e));
     return MLA_OK;
 }

@@ -23,10 +23,12 @@
 // with the 128-byte swizzle the MMA's K-major operand layout expects. The 4
 // tokens' queries (256 rows) are one more TMA copy.
 //
-// Warps: 0-7 epilogue (warp w reads TMEM lane quadrant w%4 = keys 32(w%4)..+31
-// and tokens 2(w/4), 2(w/4)+1), 8 TMA producer, 9 MMA issue + TMEM owner. Key
-// tiles go through a 6-stage ring; the accumulator is double-buffered in TMEM
-// (2 x 256 columns) so the MMA of tile i+1 overlaps the epilogue of tile i.
+// Warps: 0-15 epilogue (warp w reads TMEM lane quadrant w%4 = keys 32(w%4)..+31
+// of token w/4), 16 TMA producer, 17 MMA issue + TMEM owner. Key tiles go
+// through a 6-stage ring; the accumulator is double-buffered in TMEM (2 x 256
+// columns) so the MMA of tile i+1 overlaps the epilogue of tile i. The head
+// sum runs on paired f32 FMAs (fma.rn.f32x2: two IEEE fmas, so the same
+// result as scalar ones) with four independent accumulator pairs.
 // Every wait is bounded and reports MLA_DEVERR_TIMEOUT.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -43,8 +45,9 @@ using namespace tc;
 constexpr int TOK = kIdxTokensPerCta;   // 4 query tokens per CTA
 constexpr int KT = 128;                 // keys per tile
 constexpr int STAGES = 6;
-constexpr int NT = 320;                 // 10 warps
-constexpr int kProducerWarp = 8, kIssuerWarp = 9;
+constexpr int kEpiWarps = 16;           // 4 tokens x 4 TMEM lane quadrants
+constexpr int NT = 32 * (kEpiWarps + 2);
+constexpr int kProducerWarp = kEpiWarps, kIssuerWarp = kEpiWarps + 1;
 constexpr int kQBytes = TOK * kHidx * kDidx;       // 32 KB
 constexpr int kTileBytes = KT * kDidx;             // 16 KB
 constexpr int kDynSmem = 1024 + kQBytes + STAGES * kTileBytes;
@@ -56,7 +59,7 @@ enum Bar {
     B_K_FULL = 1,                       // [STAGES]  TMA -> issuer
     B_K_EMPTY = B_K_FULL + STAGES,      // [STAGES]  issuer (commit) -> producer
     B_D_FULL = B_K_EMPTY + STAGES,      // [2]       issuer (commit) -> epilogue
-    B_D_EMPTY = B_D_FULL + 2,           // [2]       epilogue (8 warps) -> issuer
+    B_D_EMPTY = B_D_FULL + 2,           // [2]       epilogue (16 warps) -> issuer
     B_FINAL = B_D_EMPTY + 2,
     NBAR
 };
@@ -66,6 +69,22 @@ struct Shared {
     uint64_t bar[NBAR];
     uint32_t tmem_base;
 };
+
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float sum2(uint64_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo + hi;
+}
+// acc += a * b, elementwise on two packed floats
+__device__ __forceinline__ void ffma2(uint64_t &acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ float relu_bits(uint32_t x) { return fmaxf(__uint_as_float(x), 0.f); }
 
 __device__ __forceinline__ bool wait_bar(Shared &sh, int32_t *dev_err, int b, uint32_t parity) {
     if (mbar_wait_cycles(smem_u32(&sh.bar[b]), parity, kWaitCycles)) return true;
@@ -92,7 +111,7 @@ __global__ void __launch_bounds__(NT, 1)
     const int n_tiles = (k_hi - k_lo + KT - 1) / KT;
 
     if (tid == 0) {
-        for (int i = 0; i < NBAR; ++i) mbar_init(smem_u32(&sh.bar[i]), (i == B_D_EMPTY || i == B_D_EMPTY + 1) ? 8 : 1);
+        for (int i = 0; i < NBAR; ++i) mbar_init(smem_u32(&sh.bar[i]), (i == B_D_EMPTY || i == B_D_EMPTY + 1) ? kEpiWarps : 1);
         mbar_fence_init();
     }
     for (int i = tid; i < TOK * kHidx; i += NT) {
@@ -153,56 +172,63 @@ __global__ void __launch_bounds__(NT, 1)
         }
         __syncwarp();
     } else {
-        // =================== epilogue (warps 0-7) ===================
-        const int quad = warp & 3, tp = warp >> 2;                    // keys 32 quad.., tokens 2tp, 2tp+1
+        // =================== epilogue (warps 0-15) ===================
+        const int quad = warp & 3, j = warp >> 2;                     // keys 32 quad.., token j
         const uint32_t lane_addr = static_cast<uint32_t>(32 * quad) << 16;
         const int kk = 32 * quad + lane;                              // key within the tile
+        const float4 *wj = reinterpret_cast<const float4 *>(sh.w[j]);
+        float *out_row = a.scores + static_cast<int64_t>(q0 + i0 + j) * a.score_stride;
+        const int pos_hi = min(k_hi, P + i0 + j + 1);                 // causal bound of token j (exclusive)
+        // The key scales go through a register pipeline: the page of tile i+3 and
+        // the scale of tile i+2 are fetched while tile i is reduced, so the two
+        // dependent global loads never sit on a tile's critical path. A tile lies
+        // in one page; blk < 0 marks a bad page or a tile past the chunk.
+        auto page_blk = [&](int i) -> int {
+            if (i >= n_tiles) return -1;
+            const int page = (k_lo + i * KT) / kPage;
+            const int blk = page < a.max_blocks ? __ldg(bt + page) : -1;
+            return blk;
+        };
+        auto key_ok = [&](int blk) { return blk >= 0 && blk < a.num_blocks; };
+        auto key_sig = [&](int i, int blk) -> float {
+            const int pos = k_lo + i * KT + kk;
+            if (!key_ok(blk) || pos >= k_hi) return 0.f;
+            return __ldg(a.ki_scale + static_cast<int64_t>(blk) * kPage + pos % kPage);
+        };
+        int blk0 = page_blk(0), blk1 = page_blk(1), blk2 = page_blk(2);
+        float sig0 = key_sig(0, blk0), sig1 = key_sig(1, blk1);
+        int blk3 = page_blk(3);
         for (int i = 0; i < n_tiles; ++i) {
             const int db = i & 1;
-            // this key's cache row and scale (issued before the wait)
             const int pos = k_lo + i * KT + kk;
-            int64_t row = -1;
-            if (pos < k_hi) {
-                const int page = pos / kPage;
-                const int blk = page < a.max_blocks ? __ldg(bt + page) : -1;
-                if (blk >= 0 && blk < a.num_blocks) row = static_cast<int64_t>(blk) * kPage + pos % kPage;
-            }
-            const float sig = row >= 0 ? __ldg(a.ki_scale + row) : 0.f;
+            const float sig = sig0;
+            const bool ok_key = key_ok(blk0);
+            sig0 = sig1;
+            sig1 = key_sig(i + 2, blk2);
+            blk0 = blk1;
+            blk1 = blk2;
+            blk2 = blk3;
+            blk3 = page_blk(i + 4);
             if (!wait_bar(sh, a.dev_err, B_D_FULL + db, (i >> 1) & 1)) break;
             fence_after_sync();
-            float sc[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int j = 2 * tp + u;
-                uint32_t d0[32], d1[32];
-                tmem_ld32(tmem + lane_addr + 256u * db + 64u * j, d0);
-                tmem_ld32(tmem + lane_addr + 256u * db + 64u * j + 32, d1);
-                tmem_ld_wait();
-                const float4 *wj = reinterpret_cast<const float4 *>(sh.w[j]);
-                float e0 = 0.f, e1 = 0.f;
-#pragma unroll
-                for (int h4 = 0; h4 < 8; ++h4) {
-                    const float4 wa = wj[h4], wb = wj[8 + h4];
-                    e0 = fmaf(wa.x, fmaxf(__uint_as_float(d0[4 * h4 + 0]), 0.f), e0);
-                    e1 = fmaf(wa.y, fmaxf(__uint_as_float(d0[4 * h4 + 1]), 0.f), e1);
-                    e0 = fmaf(wa.z, fmaxf(__uint_as_float(d0[4 * h4 + 2]), 0.f), e0);
-                    e1 = fmaf(wa.w, fmaxf(__uint_as_float(d0[4 * h4 + 3]), 0.f), e1);
-                    e0 = fmaf(wb.x, fmaxf(__uint_as_float(d1[4 * h4 + 0]), 0.f), e0);
-                    e1 = fmaf(wb.y, fmaxf(__uint_as_float(d1[4 * h4 + 1]), 0.f), e1);
-                    e0 = fmaf(wb.z, fmaxf(__uint_as_float(d1[4 * h4 + 2]), 0.f), e0);
-                    e1 = fmaf(wb.w, fmaxf(__uint_as_float(d1[4 * h4 + 3]), 0.f), e1);
-                }
-                sc[u] = e0 + e1;
-            }
+            uint32_t d0[32], d1[32];
+            tmem_ld32(tmem + lane_addr + 256u * db + 64u * j, d0);
+            tmem_ld32(tmem + lane_addr + 256u * db + 64u * j + 32, d1);
+            tmem_ld_wait();
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_D_EMPTY + db]));
+            uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int j = 2 * tp + u;
-                if (j < ntok && pos < k_hi && pos <= P + i0 + j)
-                    a.scores[static_cast<int64_t>(q0 + i0 + j) * a.score_stride + pos] = row >= 0 ? sig * sc[u] : -INFINITY;
+            for (int h4 = 0; h4 < 8; ++h4) {
+                const float4 wa = wj[h4], wb = wj[8 + h4];
+                ffma2(acc[0], pack2(wa.x, wa.y), pack2(relu_bits(d0[4 * h4 + 0]), relu_bits(d0[4 * h4 + 1])));
+                ffma2(acc[1], pack2(wa.z, wa.w), pack2(relu_bits(d0[4 * h4 + 2]), relu_bits(d0[4 * h4 + 3])));
+                ffma2(acc[2], pack2(wb.x, wb.y), pack2(relu_bits(d1[4 * h4 + 0]), relu_bits(d1[4 * h4 + 1])));
+                ffma2(acc[3], pack2(wb.z, wb.w), pack2(relu_bits(d1[4 * h4 + 2]), relu_bits(d1[4 * h4 + 3])));
             }
+            const float sc = (sum2(acc[0]) + sum2(acc[1])) + (sum2(acc[2]) + sum2(acc[3]));
+            if (j < ntok && pos < pos_hi) out_row[pos] = ok_key ? sig * sc : -INFINITY;
         }
     }
 

@@ -49,6 +49,12 @@ struct IndexerArgs {
 cudaError_t launch_dense_tc(const AttnArgs &a, const int4 *work, int n_work, cudaStream_t st);
 cudaError_t launch_sparse_tc(const AttnArgs &a, int64_t n_tokens, cudaStream_t st);
 
+// Dense attention on e4m3 operands (kind::f8f6f4): same work items as
+// launch_dense_tc. tmap_kv: the latent cache as [num_blocks * 256 rows][576 B],
+// 128 x 32 boxes, 128-byte swizzle (encode_kv_tmap).
+cudaError_t launch_dense_f8(const AttnArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_kv, cudaStream_t st);
+bool encode_kv_tmap(CUtensorMap *map, const uint8_t *kv, int32_t num_blocks);
+
 // Indexer score work item: x = sequence, y = first new token (in-sequence),
 // z = token count (<= 4), w = key chunk. tmap_k: the key cache as
 // [num_blocks * 256 rows][128 B]; tmap_q: the queries as [Tq * 64 rows][128 B];

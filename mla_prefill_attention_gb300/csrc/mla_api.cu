@@ -125,10 +125,11 @@ size_t indexer_score_bytes(const mla_seqs_t *s) {
     return round_up(static_cast<size_t>(tq) * static_cast<size_t>(score_stride(s)) * sizeof(float), kWsAlign);
 }
 
-// 2-D tensor map over a row-major u8 matrix [rows][128] for TMA copies of
-// box_rows x 128-byte boxes with the 128-byte swizzle. The encoder is fetched
-// from the driver once; no link against the driver library is needed.
-bool encode_rows128(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+// 2-D tensor map over a row-major u8 matrix [rows][width] for TMA copies of
+// box_rows x 128-byte boxes with the 128-byte swizzle (bytes past the row end
+// read as zero). The encoder is fetched from the driver once; no link against
+// the driver library is needed.
+bool encode_u8_rows(CUtensorMap *map, const void *base, uint64_t width, uint64_t rows, uint32_t box_rows) {
     using Encode = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -142,13 +143,16 @@ bool encode_rows128(CUtensorMap *map, const void *base, uint64_t rows, uint32_t 
             return false;
         encode = reinterpret_cast<Encode>(fn);
     }
-    const cuuint64_t dims[2] = {128, rows};
-    const cuuint64_t strides[1] = {128};
+    const cuuint64_t dims[2] = {width, rows};
+    const cuuint64_t strides[1] = {width};
     const cuuint32_t box[2] = {128, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool encode_rows128(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+    return encode_u8_rows(map, base, 128, rows, box_rows);
 }
 
 mla::AttnArgs attn_args(const mla_seqs_t *s, const void *q, int32_t H, const uint8_t *kv, const float *kv_scale,
@@ -223,7 +227,10 @@ mla_status_t mla_prefill_dense(const mla_seqs_t *seqs, const void *q_bf16, int32
     cudaError_t e = cudaMemcpyAsync(workspace, work.data(), work.size() * sizeof(int4), cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e, "schedule upload");
     const mla::AttnArgs a = attn_args(seqs, q_bf16, num_heads, kv_e4m3, kv_scale, sm_scale, out_bf16, lse, dev_err);
-    e = mla::launch_dense_tc(a, static_cast<const int4 *>(workspace), static_cast<int>(work.size()), stream);
+    CUtensorMap tmap_kv;
+    if (!mla::encode_kv_tmap(&tmap_kv, kv_e4m3, seqs->num_blocks))
+        return fail(MLA_ERR_CUDA, "tensor map encoding for the latent cache failed");
+    e = mla::launch_dense_f8(a, static_cast<const int4 *>(workspace), static_cast<int>(work.size()), tmap_kv, stream);
     if (e != cudaSuccess) return cuda_fail(e, "dense launch");
     return MLA_OK;
 }
@@ -313,6 +320,10 @@ mla_status_t mla_prefill_sparse(const mla_seqs_t *seqs, const void *q_bf16, int3
 
 // Helpers shared with the allocation-free dense entry point (dense_noalloc.cu).
 namespace mla {
+bool encode_kv_tmap(CUtensorMap *map, const uint8_t *kv, int32_t num_blocks) {
+    // rows of 576 e4m3 codes (512 latent + 64 RoPE); 32-row boxes never straddle a 256-row page
+    return num_blocks > 0 && encode_u8_rows(map, kv, 576, static_cast<uint64_t>(num_blocks) * 256, 32);
+}
 mla_status_t check_dense_args(const mla_seqs_t *seqs, const void *q, int32_t H, const uint8_t *kv,
                               const float *kv_scale, const void *out, const float *lse, float sm_scale) {
     g_err.clear();

@@ -5,7 +5,7 @@ import pytest
 
 from oracle import oracle as O
 from mla_prefill_attention_gb300 import inputs as I
-from tests.parity import Problem, bf16_to_np, check_attention, sample_tokens
+from tests.parity import TOL_MAX, TOL_MEAN, Problem, bf16_to_np, check_attention, rel_errors, sample_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -97,8 +97,15 @@ def test_sparse_with_all_keys_matches_dense():
     out_s, lse_s = run_sparse(pb, d, idx)
     out_d, lse_d = mla_prefill_dense(d["seqs"], d["q"], d["kv"], d["ks"], pb.sm_scale)
     torch.cuda.synchronize()
-    check_attention(bf16_to_np(out_s), bf16_to_np(out_d).astype(np.float64), lse_s.cpu().numpy(),
-                    lse_d.cpu().numpy().astype(np.float64), "sparse(all) vs dense")
+    # both against the dense oracle: with every key selected the sparse path is the dense one
+    toks = np.arange(pb.ps.total_q)
+    ora, ora_lse = O.mla_dense(pb.ps, pb.q, toks, pb.kv, pb.ks, pb.sm_scale)
+    check_attention(bf16_to_np(out_s), ora, lse_s.cpu().numpy(), ora_lse, "sparse(all) vs dense oracle")
+    check_attention(bf16_to_np(out_d), ora, lse_d.cpu().numpy(), ora_lse, "dense vs dense oracle")
+    # and against each other: two bf16 results, each rounded on its own, may sit up to
+    # two half-ulps apart, so the bound is twice the oracle bound
+    mx, mean, _ = rel_errors(bf16_to_np(out_s), bf16_to_np(out_d))
+    assert mx <= 2 * TOL_MAX and mean <= 2 * TOL_MEAN, f"sparse(all) vs dense: max {mx:.3e} mean {mean:.3e}"
 
 
 def test_sparse_padding_and_bad_index():
