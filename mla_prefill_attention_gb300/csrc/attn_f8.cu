@@ -310,45 +310,42 @@ __global__ void __launch_bounds__(NT, 1)
 
     if (warp == kProducerWarp) {
         // =================== TMA producer + key metadata ===================
+        // The global loads of tile t (block-table entries, then key scales) are
+        // issued before the wait for its stage, so their latency hides behind it;
+        // once the stage is free the boxes go to TMA at once.
         if (lane == 0) tma_prefetch_desc(&tmap_kv);
         RowTile rt = make_tile(a, b, tiles[0]);
         uint32_t fix_phase = 0;
         bool ok = true;
         for (int t = 0; t < walk.total && ok; ++t) {
             const int st = t % kStages;
-            if (t >= kStages && !(ok = wait(B_EMPTY + st, ((t / kStages) - 1) & 1))) break;
             if (t > 0 && walk.r(t) != walk.r(t - 1)) rt = make_tile(a, b, tiles[1]);
             const int key0 = walk.j(t) * BN;
-            // metadata (its ring slot was last read by the softmax of tile t-4, which
-            // finished before PV(t-3), the stage release just waited for)
-            KeyMeta &mt = sh.meta[t & 3];
+            // this lane's keys lane + 32i: cache rows, then scales
+            int64_t krow[kBoxes];
+            float ksig[kBoxes];
 #pragma unroll
-            for (int i = 0; i < BN / 32; ++i) {
-                const int k = lane + 32 * i, pos = key0 + k;
-                int64_t row = -1;
-                if (pos <= rt.key_last) row = cache_row(bt, a.max_blocks, a.num_blocks, pos, a.dev_err);
-                const float sig = row >= 0 ? __ldg(a.kv_scale + row) : 1.f;
-                float *sl = reinterpret_cast<float *>(&mt.sl[k >> 1]);
-                sl[k & 1] = sig;
-                sl[2 + (k & 1)] = row >= 0 ? __log2f(sig) : -INFINITY;
-                reinterpret_cast<float *>(&mt.isig[k >> 1])[k & 1] = 1.f / sig;
+            for (int i = 0; i < kBoxes; ++i) {
+                const int pos = key0 + lane + kBox * i;
+                krow[i] = pos <= rt.key_last ? cache_row(bt, a.max_blocks, a.num_blocks, pos, a.dev_err) : -1;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_META + (t & 3)]));
+#pragma unroll
+            for (int i = 0; i < kBoxes; ++i) ksig[i] = krow[i] >= 0 ? __ldg(a.kv_scale + krow[i]) : 1.f;
             // boxes: whole ones by TMA; one straddling the causal limit by TMA, then its
-            // tail zeroed; ones past the limit (or on a bad page) zeroed
-            const uint32_t sdst = sbase_a + st * kStageBytes;
+            // tail zeroed; ones past the limit (or on a bad page) zeroed. Box g starts
+            // at lane 0's key g.
             int nval[kBoxes];
             int64_t brow[kBoxes];
             uint32_t full_bytes = 0;
 #pragma unroll
             for (int g = 0; g < kBoxes; ++g) {
-                const int p0 = key0 + kBox * g;
-                nval[g] = max(0, min(kBox, rt.key_last - p0 + 1));
-                brow[g] = nval[g] > 0 ? cache_row(bt, a.max_blocks, a.num_blocks, p0, a.dev_err) : -1;
+                nval[g] = max(0, min(kBox, rt.key_last - (key0 + kBox * g) + 1));
+                brow[g] = __shfl_sync(0xffffffffu, krow[g], 0);
                 if (brow[g] < 0) nval[g] = 0;
                 if (nval[g] == kBox) full_bytes += kSlices * kBoxBytes;
             }
+            if (t >= kStages && !(ok = wait(B_EMPTY + st, ((t / kStages) - 1) & 1))) break;
+            const uint32_t sdst = sbase_a + st * kStageBytes;
             if (lane == 0) {
                 mbar_add_tx(smem_u32(&sh.bar[B_FULL + st]), full_bytes);
 #pragma unroll
@@ -360,6 +357,19 @@ __global__ void __launch_bounds__(NT, 1)
                                     static_cast<int>(brow[g]), smem_u32(&sh.bar[B_FULL + st]));
                 }
             }
+            // metadata (its ring slot was last read by the softmax of tile t-4, which
+            // finished before PV(t-3), the stage release just waited for)
+            KeyMeta &mt = sh.meta[t & 3];
+#pragma unroll
+            for (int i = 0; i < kBoxes; ++i) {
+                const int k = lane + kBox * i;
+                float *sl = reinterpret_cast<float *>(&mt.sl[k >> 1]);
+                sl[k & 1] = ksig[i];
+                sl[2 + (k & 1)] = krow[i] >= 0 ? __log2f(ksig[i]) : -INFINITY;
+                reinterpret_cast<float *>(&mt.isig[k >> 1])[k & 1] = 1.f / ksig[i];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_META + (t & 3)]));
             bool zeroed = false;
 #pragma unroll 1
             for (int g = 0; g < kBoxes; ++g) {
@@ -388,67 +398,73 @@ __global__ void __launch_bounds__(NT, 1)
             if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL + st]));
         }
     } else if (warp == kIssuerWarp) {
-        // =================== MMA issuer ===================
-        const uint32_t lead = lane == 0 ? 1u : 0u;
-        const uint32_t id_qk = idesc_e4m3(BM, BN, false, false);
-        const uint32_t id_pv = idesc_e4m3(BM, 256, false, true);
-        const uint64_t dk0 = sdesc(sbase_a, 16, 1024, kSw128);              // K-major key slices
-        const uint64_t dv0 = sdesc(sbase_a, kSliceBytes, 1024, kSw128);     // MN-major value chunks
-        const uint64_t dp0 = sdesc(sbase_a + kOffP, 128, 768, kSwNone);     // P terms
-        bool ok = true;
-        auto qk = [&](int t) -> bool {
-            const int sb = t & 1, st = t % kStages;
-            if (!wait(B_FULL + st, (t / kStages) & 1)) return false;
-            if (t >= 2 && !wait(B_S_FREE + sb, ((t >> 1) - 1) & 1)) return false;
-            fence_after_sync();
-            const uint32_t d = tmem + kColS + BN * sb;
+        // =================== MMA issuer (lane 0; the other lanes wait at the end) ===================
+        // One thread issues: the same instruction stream issued warp-wide with a
+        // leader predicate runs ~1.5x slower (measured), as the issue itself
+        // becomes the bottleneck of M=64 MMAs.
+        if (lane == 0) {
+            const uint32_t lead = 1u;
+            const uint32_t id_qk = idesc_e4m3(BM, BN, false, false);
+            const uint32_t id_pv = idesc_e4m3(BM, 256, false, true);
+            const uint64_t dk0 = sdesc(sbase_a, 16, 1024, kSw128);              // K-major key slices
+            const uint64_t dv0 = sdesc(sbase_a, kSliceBytes, 1024, kSw128);     // MN-major value chunks
+            const uint64_t dp0 = sdesc(sbase_a + kOffP, 128, 768, kSwNone);     // P terms
+            bool ok = true;
+            auto qk = [&](int t) -> bool {
+                const int sb = t & 1, st = t % kStages;
+                if (!wait(B_FULL + st, (t / kStages) & 1)) return false;
+                if (t >= 2 && !wait(B_S_FREE + sb, ((t >> 1) - 1) & 1)) return false;
+                fence_after_sync();
+                const uint32_t d = tmem + kColS + BN * sb;
 #pragma unroll 1
-            for (int s = 0; s < kSlices; ++s) {
-                const uint64_t db = dk0 + static_cast<uint64_t>((st * kStageBytes + s * kSliceBytes) >> 4);
-                const int nks = s < 4 ? 4 : 2;   // the RoPE slice holds 64 dims
+                for (int s = 0; s < kSlices; ++s) {
+                    const uint64_t db = dk0 + static_cast<uint64_t>((st * kStageBytes + s * kSliceBytes) >> 4);
+                    const int nks = s < 4 ? 4 : 2;   // the RoPE slice holds 64 dims
 #pragma unroll 4
-                for (int ks = 0; ks < nks; ++ks) {
-                    const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
-                    mma_e4m3_ts_w(d, tmem + kColQh + 32 * s + 8 * ks, db + 2 * ks, id_qk, acc, lead);
-                    mma_e4m3_ts_w(d, tmem + kColQl + 32 * s + 8 * ks, db + 2 * ks, id_qk, 1u, lead);
+                    for (int ks = 0; ks < nks; ++ks) {
+                        const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
+                        mma_e4m3_ts_w(d, tmem + kColQh + 32 * s + 8 * ks, db + 2 * ks, id_qk, acc, lead);
+                        mma_e4m3_ts_w(d, tmem + kColQl + 32 * s + 8 * ks, db + 2 * ks, id_qk, 1u, lead);
+                    }
                 }
-            }
-            mma_commit_w(smem_u32(&sh.bar[B_S_FULL + sb]), lead);
-            return true;
-        };
-        auto pv = [&](int t) -> bool {
-            const int pb = t & 1, st = t % kStages, j = walk.j(t), r = walk.r(t);
-            if (j == 0 && r > 0 && !wait(B_O_FREE, (r - 1) & 1)) return false;
-            if (!wait(B_P_FULL + pb, (t >> 1) & 1)) return false;
-            fence_after_sync();
-            const uint64_t dph = dp0 + static_cast<uint64_t>(((2 * pb) * kPBytes) >> 4);
-            const uint64_t dpl = dp0 + static_cast<uint64_t>(((2 * pb + 1) * kPBytes) >> 4);
+                mma_commit_w(smem_u32(&sh.bar[B_S_FULL + sb]), lead);
+                return true;
+            };
+            auto pv = [&](int t) -> bool {
+                const int pb = t & 1, st = t % kStages, j = walk.j(t), r = walk.r(t);
+                if (j == 0 && r > 0 && !wait(B_O_FREE, (r - 1) & 1)) return false;
+                if (!wait(B_P_FULL + pb, (t >> 1) & 1)) return false;
+                fence_after_sync();
+                const uint64_t dph = dp0 + static_cast<uint64_t>(((2 * pb) * kPBytes) >> 4);
+                const uint64_t dpl = dp0 + static_cast<uint64_t>(((2 * pb + 1) * kPBytes) >> 4);
 #pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-                const uint64_t dv = dv0 + static_cast<uint64_t>((st * kStageBytes + 2 * c * kSliceBytes) >> 4);
-                const uint32_t d = tmem + kHalf1 + 256u * c;
+                for (int c = 0; c < 2; ++c) {
+                    const uint64_t dv = dv0 + static_cast<uint64_t>((st * kStageBytes + 2 * c * kSliceBytes) >> 4);
+                    const uint32_t d = tmem + kHalf1 + 256u * c;
 #pragma unroll
-                for (int ks = 0; ks < BN / 32; ++ks) {
-                    mma_e4m3_ss_w(d, dph + 16 * ks, dv + 256 * ks, id_pv, (j > 0 || ks > 0) ? 1u : 0u, lead);
-                    mma_e4m3_ss_w(d, dpl + 16 * ks, dv + 256 * ks, id_pv, 1u, lead);
+                    for (int ks = 0; ks < BN / 32; ++ks) {
+                        mma_e4m3_ss_w(d, dph + 16 * ks, dv + 256 * ks, id_pv, (j > 0 || ks > 0) ? 1u : 0u, lead);
+                        mma_e4m3_ss_w(d, dpl + 16 * ks, dv + 256 * ks, id_pv, 1u, lead);
+                    }
+                }
+                mma_commit_w(smem_u32(&sh.bar[B_EMPTY + st]), lead);
+                mma_commit_w(smem_u32(&sh.bar[B_PV_DONE + pb]), lead);
+                return true;
+            };
+            if (walk.total > 0) ok = wait(B_Q_FULL, 0) && qk(0);
+            for (int t = 0; t < walk.total && ok; ++t) {
+                const bool more = t + 1 < walk.total;
+                const bool new_rt = more && walk.r(t + 1) != walk.r(t);
+                if (more && !new_rt && !(ok = qk(t + 1))) break;
+                if (!(ok = pv(t))) break;
+                if (new_rt) {
+                    if (!(ok = wait(B_Q_FULL, walk.r(t + 1) & 1))) break;
+                    if (!(ok = qk(t + 1))) break;
                 }
             }
-            mma_commit_w(smem_u32(&sh.bar[B_EMPTY + st]), lead);
-            mma_commit_w(smem_u32(&sh.bar[B_PV_DONE + pb]), lead);
-            return true;
-        };
-        if (walk.total > 0) ok = wait(B_Q_FULL, 0) && qk(0);
-        for (int t = 0; t < walk.total && ok; ++t) {
-            const bool more = t + 1 < walk.total;
-            const bool new_rt = more && walk.r(t + 1) != walk.r(t);
-            if (more && !new_rt && !(ok = qk(t + 1))) break;
-            if (!(ok = pv(t))) break;
-            if (new_rt) {
-                if (!(ok = wait(B_Q_FULL, walk.r(t + 1) & 1))) break;
-                if (!(ok = qk(t + 1))) break;
-            }
+            mma_commit_w(smem_u32(&sh.bar[B_FINAL]), lead);
         }
-        mma_commit_w(smem_u32(&sh.bar[B_FINAL]), lead);
+        __syncwarp();
     } else {
         // =================== softmax / correction (warps 0-3) ===================
         const int q = warp;
