@@ -444,11 +444,11 @@ __global__ void __launch_bounds__(NT, 1) attn_kernel(const AttnArgs a, const int
             sig_cur[1] = sig_n[1];
         }
     } else if (warp >= 4) {
-        // =================== MMA issuer (warp 7); warps 10, 11 idle ===================
-        // The whole warp runs the issue loop in lockstep (waits, operand
-        // addresses) and lane 0 alone issues each MMA and commit.
-        if (warp == kIssuerWarp) {
-            const uint32_t lead = lane == 0 ? 1u : 0u;
+        // =================== MMA issuer (warp 7, lane 0); warps 10, 11 idle ===================
+        // One thread runs the issue loop: issued warp-wide with a leader
+        // predicate, the short M=64 MMAs become issue-bound (measured).
+        if (warp == kIssuerWarp && lane == 0) {
+            const uint32_t lead = 1u;
             const uint32_t id_qk = idesc_f16(BM, BN, false, false, false, false);
             const uint32_t id_pv = idesc_f16(BM, 128, false, false, false, true);
             // descriptors of the bases; an operand at byte offset x is the base plus x/16
@@ -519,6 +519,7 @@ __global__ void __launch_bounds__(NT, 1) attn_kernel(const AttnArgs a, const int
             }
             mma_commit_w(smem_u32(&sh.bar[B_FINAL]), lead);
         }
+        __syncwarp();
     } else if (warp < 4) {
         // =================== softmax / correction (warps 0-3) ===================
         const int q = warp;                        // TMEM lane quadrant
