@@ -190,7 +190,7 @@ __device__ __forceinline__ uint32_t split_p2(float p0, float p1) {
 // Q rows ra, rb of the tile -> Qh, Ql in TMEM (lane half 0; 16x256b layout:
 // column group g holds dims 32g + 8tc .. +7 of this thread's rows). Returns the
 // logit scale s_Q * sm_scale * log2(e) per row.
-__device__ __forceinline__ void load_q_split(const AttnArgs &a, const RowTile &rt, uint32_t tq_addr, int ra, int rb,
+__device__ __noinline__ void load_q_split(const AttnArgs &a, const RowTile &rt, uint32_t tq_addr, int ra, int rb,
                                              int tc, float &rs_a, float &rs_b) {
     const bool oka = ra < rt.nvalid, okb = rb < rt.nvalid;
     const uint4 *qa = reinterpret_cast<const uint4 *>(a.q + (rt.grow0 + (oka ? ra : 0)) * kDqk + 8 * tc);
@@ -510,7 +510,8 @@ __global__ void __launch_bounds__(NT, 1)
                 const float mu_b0 = m_b == -INFINITY ? 0.f : m_b - kPOffset;
                 float mx_a = -INFINITY, mx_b = -INFINITY, lt_a = 0.f, lt_b = 0.f;
                 uint32_t pa[BN / 8], pb[BN / 8];   // per 8-key group: this thread's pair of row a / row b, head | tail << 16
-                auto logits = [&](auto with_p) {
+                {   // logits, tile maxima and (against the reference max in force) P; for
+                    // j == 0 that P is recomputed below once the max is known
 #pragma unroll
                     for (int i = 0; i < BN / 8; ++i) {
                         const int k0 = 8 * i + 2 * tc;
@@ -531,7 +532,7 @@ __global__ void __launch_bounds__(NT, 1)
                         sv[4 * i + 3] = __float_as_uint(u3);
                         mx_a = fmaxf(mx_a, fmaxf(u0, u1));
                         mx_b = fmaxf(mx_b, fmaxf(u2, u3));
-                        if (decltype(with_p)::value) {
+                        {
                             const float2 is = meta.isig[4 * i + tc];
                             const float p0 = fast_exp2(u0 - mu_a0), p1 = fast_exp2(u1 - mu_a0);
                             const float p2 = fast_exp2(u2 - mu_b0), p3 = fast_exp2(u3 - mu_b0);
@@ -541,9 +542,7 @@ __global__ void __launch_bounds__(NT, 1)
                             pb[i] = split_p2(p2, p3);
                         }
                     }
-                };
-                if (j > 0) logits(std::true_type{});
-                else logits(std::false_type{});
+                }
                 mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
                 mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
                 mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
