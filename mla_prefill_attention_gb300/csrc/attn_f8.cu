@@ -62,8 +62,17 @@ using namespace tc;
 
 constexpr int BM = 64;                          // query rows per tile
 constexpr int BN = 96;                          // keys per tile
-constexpr int NT = 192;                         // 6 warps
+// dense: 6 warps (4 softmax, TMA producer, issuer); sparse: 9 (4 softmax, issuer and
+// two pairs of gather warps: a warp keeps only so many row copies in flight)
+template <bool kSparse>
+constexpr int kThreads = kSparse ? 288 : 192;
 constexpr int kProducerWarp = 4, kIssuerWarp = 5;
+// Gather warps 4, 6 (pair 0: even tiles) and 7, 8 (pair 1: odd tiles); each warp of
+// a pair copies half of the tile's rows. A pair waits for a stage at most one
+// phase ahead of its completed one (its previous tile waited for the phase before),
+// which keeps the parity waits exact.
+__device__ __forceinline__ int gather_pair(int warp) { return warp == 4 || warp == 6 ? 0 : 1; }
+__device__ __forceinline__ int gather_half(int warp) { return warp == 4 || warp == 7 ? 0 : 1; }
 constexpr int kBox = 32;                        // keys per TMA box
 constexpr int kBoxes = BN / kBox;
 constexpr int kSlices = 5;
@@ -122,26 +131,62 @@ struct RowTile {
     int64_t grow0;      // first global query row (token*H + head)
     int nvalid;         // valid rows
     int n_ktiles;       // key tiles to visit
-    int key_last;       // last key position visible to any row
+    int key_last;       // dense: last key position visible to any row; sparse: the token's position
+    int b;              // sequence
+    int64_t tok;        // sparse: the token
 };
 
-__device__ __forceinline__ RowTile make_tile(const AttnArgs &a, int b, int tile) {
+__device__ __forceinline__ int find_seq(const int32_t *cu, int batch, int64_t t) {
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Dense: row tile `tile` of sequence b. Sparse: heads h0.. of token tok, whose
+// top-k indices give its keys.
+template <bool kSparse>
+__device__ __forceinline__ RowTile make_tile(const AttnArgs &a, int b, int tile, int64_t tok, int h0) {
     RowTile rt;
-    const int q0 = __ldg(a.cu_seqlens + b), qn = __ldg(a.cu_seqlens + b + 1) - q0;
-    const int P = __ldg(a.prefix_lens + b);
-    const int rows = qn * a.H, r_lo = tile * BM;
-    rt.grow0 = static_cast<int64_t>(q0) * a.H + r_lo;
-    rt.nvalid = min(BM, rows - r_lo);
-    rt.key_last = P + (r_lo + rt.nvalid - 1) / a.H;
-    rt.n_ktiles = rt.key_last / BN + 1;
+    if (kSparse) {
+        rt.b = find_seq(a.cu_seqlens, a.batch, tok);
+        rt.tok = tok;
+        rt.grow0 = tok * a.H + h0;
+        rt.nvalid = min(BM, a.H - h0);
+        rt.key_last = __ldg(a.prefix_lens + rt.b) + static_cast<int>(tok - __ldg(a.cu_seqlens + rt.b));
+        rt.n_ktiles = (a.topk + BN - 1) / BN;
+    } else {
+        const int q0 = __ldg(a.cu_seqlens + b), qn = __ldg(a.cu_seqlens + b + 1) - q0;
+        const int P = __ldg(a.prefix_lens + b);
+        const int rows = qn * a.H, r_lo = tile * BM;
+        rt.b = b;
+        rt.tok = -1;
+        rt.grow0 = static_cast<int64_t>(q0) * a.H + r_lo;
+        rt.nvalid = min(BM, rows - r_lo);
+        rt.key_last = P + (r_lo + rt.nvalid - 1) / a.H;
+        rt.n_ktiles = rt.key_last / BN + 1;
+    }
     return rt;
 }
 
-__device__ __forceinline__ int row_limit(const AttnArgs &a, const RowTile &rt, int b, int row) {
+// Last key position row `row` may see (dense), the token's position (sparse); -1: no row.
+template <bool kSparse>
+__device__ __forceinline__ int row_limit(const AttnArgs &a, const RowTile &rt, int row) {
     if (row >= rt.nvalid) return -1;
-    const int r_lo = static_cast<int>(rt.grow0 - static_cast<int64_t>(__ldg(a.cu_seqlens + b)) * a.H);
-    return __ldg(a.prefix_lens + b) + (r_lo + row) / a.H;
+    if (kSparse) return rt.key_last;
+    const int r_lo = static_cast<int>(rt.grow0 - static_cast<int64_t>(__ldg(a.cu_seqlens + rt.b)) * a.H);
+    return __ldg(a.prefix_lens + rt.b) + (r_lo + row) / a.H;
 }
+
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in a [rows][128 B] SW128 slice
+    return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 struct Walk {
     int n0, total;
@@ -269,7 +314,8 @@ __device__ __noinline__ void load_q_split(const AttnArgs &a, const RowTile &rt, 
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(NT, 1)
+template <bool kSparse>
+__global__ void __launch_bounds__(kThreads<kSparse>, 1)
     attn_f8_kernel(const AttnArgs a, const int4 *__restrict__ work, const __grid_constant__ CUtensorMap tmap_kv) {
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ Shared sh;
@@ -279,14 +325,28 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t sbase_a = raw + pad;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    const int4 it = work[blockIdx.x];
-    const int b = it.x;
-    const int tiles[2] = {it.y, it.z};
-    const int n_rt = tiles[1] >= 0 ? 2 : 1;
-    const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.max_blocks;
+    // the CTA's two row tiles: dense, a work item (sequence, tile, tile or -1);
+    // sparse, tokens 2x and 2x+1 (if any) for heads 64y..
+    int b = 0, tiles[2] = {-1, -1}, h0 = 0;
+    int64_t toks[2] = {-1, -1};
+    int n_rt;
+    if (kSparse) {
+        const int64_t tq = __ldg(a.cu_seqlens + a.batch);
+        toks[0] = 2 * static_cast<int64_t>(blockIdx.x);
+        toks[1] = toks[0] + 1 < tq ? toks[0] + 1 : -1;
+        h0 = blockIdx.y * BM;
+        n_rt = toks[1] >= 0 ? 2 : 1;
+    } else {
+        const int4 it = work[blockIdx.x];
+        b = it.x;
+        tiles[0] = it.y;
+        tiles[1] = it.z;
+        n_rt = tiles[1] >= 0 ? 2 : 1;
+    }
+    auto tile_of = [&](int r) { return make_tile<kSparse>(a, b, tiles[r], toks[r], h0); };
     Walk walk;
-    walk.n0 = make_tile(a, b, tiles[0]).n_ktiles;
-    walk.total = walk.n0 + (n_rt > 1 ? make_tile(a, b, tiles[1]).n_ktiles : 0);
+    walk.n0 = tile_of(0).n_ktiles;
+    walk.total = walk.n0 + (n_rt > 1 ? tile_of(1).n_ktiles : 0);
 
     if (tid == 0) {
         for (int i = 0; i < NBAR; ++i) {
@@ -294,6 +354,7 @@ __global__ void __launch_bounds__(NT, 1)
             if ((i >= B_S_FREE && i < B_S_FREE + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) || i == B_Q_FULL ||
                 i == B_O_FREE)
                 cnt = 4;
+            if (kSparse && i >= B_FULL && i < B_FULL + kStages) cnt = 2;       // both warps of a gather pair
             mbar_init(smem_u32(&sh.bar[i]), cnt);
         }
         mbar_fence_init();
@@ -308,18 +369,19 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t tmem = sh.tmem_base;
     const Wait wait{&sh, a.dev_err};
 
-    if (warp == kProducerWarp) {
+    if (!kSparse && warp == kProducerWarp) {
         // =================== TMA producer + key metadata ===================
         // The global loads of tile t (block-table entries, then key scales) are
         // issued before the wait for its stage, so their latency hides behind it;
         // once the stage is free the boxes go to TMA at once.
         if (lane == 0) tma_prefetch_desc(&tmap_kv);
-        RowTile rt = make_tile(a, b, tiles[0]);
+        RowTile rt = tile_of(0);
+        const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.max_blocks;
         uint32_t fix_phase = 0;
         bool ok = true;
         for (int t = 0; t < walk.total && ok; ++t) {
             const int st = t % kStages;
-            if (t > 0 && walk.r(t) != walk.r(t - 1)) rt = make_tile(a, b, tiles[1]);
+            if (t > 0 && walk.r(t) != walk.r(t - 1)) rt = tile_of(1);
             const int key0 = walk.j(t) * BN;
             // this lane's keys lane + 32i: cache rows, then scales
             int64_t krow[kBoxes];
@@ -394,6 +456,67 @@ __global__ void __launch_bounds__(NT, 1)
             }
             if (!ok) break;
             if (zeroed) fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL + st]));
+        }
+    } else if (kSparse && warp >= 4 && warp != kIssuerWarp) {
+        // =================== row gathers (sparse): pair p takes tiles p, p+2, ... ===================
+        // Key k's 576 bytes go by 16-byte cp.async into the swizzled slices, eight
+        // lanes per row (one 128-byte slice row per instruction and row), four rows
+        // per warp instruction; a key that is padding (-1) or invalid is zeroed.
+        const int gk = lane >> 3, gc = lane & 7;
+        const int half = gather_half(warp);
+        bool ok = true;
+        for (int t = gather_pair(warp); t < walk.total && ok; t += 2) {
+            const int st = t % kStages;
+            const RowTile rt = tile_of(walk.r(t));
+            const int32_t *bt = a.block_table + static_cast<int64_t>(rt.b) * a.max_blocks;
+            const int key0 = walk.j(t) * BN;
+            int64_t krow[kBoxes];
+            float ksig[kBoxes];
+#pragma unroll
+            for (int i = 0; i < kBoxes; ++i) {
+                const int kk = key0 + lane + 32 * i;
+                int pos = kk < a.topk ? __ldg(a.idx + rt.tok * a.topk + kk) : -1;
+                if (pos < -1 || pos > rt.key_last) {
+                    set_dev_err(a.dev_err, MLA_DEVERR_BAD_INDEX);
+                    pos = -1;
+                }
+                krow[i] = pos >= 0 ? cache_row(bt, a.max_blocks, a.num_blocks, pos, a.dev_err) : -1;
+            }
+#pragma unroll
+            for (int i = 0; i < kBoxes; ++i) ksig[i] = krow[i] >= 0 ? __ldg(a.kv_scale + krow[i]) : 1.f;
+            if (t >= kStages && !(ok = wait(B_EMPTY + st, ((t / kStages) - 1) & 1))) break;
+            if (half == 0) {
+                KeyMeta &mt = sh.meta[t & 3];
+#pragma unroll
+                for (int i = 0; i < kBoxes; ++i) {
+                    const int k = lane + 32 * i;
+                    float *sl = reinterpret_cast<float *>(&mt.sl[k >> 1]);
+                    sl[k & 1] = ksig[i];
+                    sl[2 + (k & 1)] = krow[i] >= 0 ? __log2f(ksig[i]) : -INFINITY;
+                    reinterpret_cast<float *>(&mt.isig[k >> 1])[k & 1] = 1.f / ksig[i];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_META + (t & 3)]));
+            }
+            const uint32_t sst = sbase_a + st * kStageBytes;
+#pragma unroll 4
+            for (int g = half * (BN / 8); g < (half + 1) * (BN / 8); ++g) {
+                const int k = 4 * g + gk, kb = (4 * g) >> 5;     // kb: the same for the four rows
+                const int64_t r0 = kb == 0 ? krow[0] : (kb == 1 ? krow[1] : krow[2]);
+                const int64_t row = __shfl_sync(0xffffffffu, r0, k & 31);
+                const uint8_t *src = a.kv + (row >= 0 ? row : 0) * kDqk + 16 * gc;
+#pragma unroll
+                for (int s = 0; s < kSlices; ++s) {
+                    if (s == kSlices - 1 && gc >= 4) break;      // the RoPE slice holds 64 bytes
+                    const uint32_t off = s * kSliceBytes + swz(k, gc);
+                    if (row >= 0) cp_async16(sst + off, src + 128 * s);
+                    else *reinterpret_cast<uint4 *>(sbase + st * kStageBytes + off) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            cp_async_wait_all();
+            fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL + st]));
         }
@@ -478,7 +601,7 @@ __global__ void __launch_bounds__(NT, 1)
         const uint32_t poff = static_cast<uint32_t>((prow >> 3) * 768 + (prow & 7) * 16 + 4 * (tc >> 1));
         uint8_t *pbase = sbase + kOffP;
         bool ok = true;
-        RowTile rt = make_tile(a, b, tiles[0]);
+        RowTile rt = tile_of(0);
         float rs_a, rs_b;
         load_q_split(a, rt, tmem + lane_lo, ra, rb, tc, rs_a, rs_b);
         tmem_st_wait();
@@ -489,7 +612,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int r = 0; r < n_rt && ok; ++r) {
             float m_a = -INFINITY, m_b = -INFINITY;
             float l_a = 0.f, l_b = 0.f;
-            const int lim_a = row_limit(a, rt, b, ra), lim_b = row_limit(a, rt, b, rb);
+            const int lim_a = row_limit<kSparse>(a, rt, ra), lim_b = row_limit<kSparse>(a, rt, rb);
             const int lim_min = min(lim_a, lim_b);
             for (int j = 0; j < rt.n_ktiles && ok; ++j, ++t) {
                 const int sb = t & 1;
@@ -505,7 +628,7 @@ __global__ void __launch_bounds__(NT, 1)
                 if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_S_FREE + sb]));
                 const KeyMeta &meta = sh.meta[t & 3];
                 const int key0 = j * BN;
-                const bool full = key0 + BN - 1 <= lim_min;
+                const bool full = kSparse ? lim_min >= 0 : key0 + BN - 1 <= lim_min;
                 const float mu_a0 = m_a == -INFINITY ? 0.f : m_a - kPOffset;
                 const float mu_b0 = m_b == -INFINITY ? 0.f : m_b - kPOffset;
                 float mx_a = -INFINITY, mx_b = -INFINITY, lt_a = 0.f, lt_b = 0.f;
@@ -521,10 +644,14 @@ __global__ void __launch_bounds__(NT, 1)
                         float u2 = fmaf(__uint_as_float(sv[4 * i + 2]) * m.x, rs_b, m.z);
                         float u3 = fmaf(__uint_as_float(sv[4 * i + 3]) * m.y, rs_b, m.w);
                         if (!full) {
-                            u0 = key0 + k0 <= lim_a ? u0 : -INFINITY;
-                            u1 = key0 + k0 + 1 <= lim_a ? u1 : -INFINITY;
-                            u2 = key0 + k0 <= lim_b ? u2 : -INFINITY;
-                            u3 = key0 + k0 + 1 <= lim_b ? u3 : -INFINITY;
+                            const bool va0 = kSparse ? lim_a >= 0 : key0 + k0 <= lim_a;
+                            const bool va1 = kSparse ? lim_a >= 0 : key0 + k0 + 1 <= lim_a;
+                            const bool vb0 = kSparse ? lim_b >= 0 : key0 + k0 <= lim_b;
+                            const bool vb1 = kSparse ? lim_b >= 0 : key0 + k0 + 1 <= lim_b;
+                            u0 = va0 ? u0 : -INFINITY;
+                            u1 = va1 ? u1 : -INFINITY;
+                            u2 = vb0 ? u2 : -INFINITY;
+                            u3 = vb1 ? u3 : -INFINITY;
                         }
                         sv[4 * i + 0] = __float_as_uint(u0);
                         sv[4 * i + 1] = __float_as_uint(u1);
@@ -628,7 +755,7 @@ __global__ void __launch_bounds__(NT, 1)
             const RowTile rt_done = rt;
             float rs_na = 0.f, rs_nb = 0.f;
             if (r + 1 < n_rt) {
-                rt = make_tile(a, b, tiles[r + 1]);
+                rt = tile_of(r + 1);
                 load_q_split(a, rt, tmem + lane_lo, ra, rb, tc, rs_na, rs_nb);
                 tmem_st_wait();
                 fence_before_sync();
@@ -686,10 +813,22 @@ __global__ void __launch_bounds__(NT, 1)
 
 cudaError_t launch_dense_f8(const AttnArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_kv,
                             cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(f8attn::attn_f8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(f8attn::attn_f8_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          f8attn::kDynSmem);
     if (e != cudaSuccess) return e;
-    if (n_work > 0) f8attn::attn_f8_kernel<<<n_work, f8attn::NT, f8attn::kDynSmem, st>>>(a, work, tmap_kv);
+    if (n_work > 0)
+        f8attn::attn_f8_kernel<false><<<n_work, f8attn::kThreads<false>, f8attn::kDynSmem, st>>>(a, work, tmap_kv);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_f8(const AttnArgs &a, int64_t n_tokens, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(f8attn::attn_f8_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         f8attn::kDynSmem);
+    if (e != cudaSuccess) return e;
+    const CUtensorMap unused{};   // the gather path reads rows with cp.async
+    const dim3 grid(static_cast<unsigned>((n_tokens + 1) / 2), (a.H + f8attn::BM - 1) / f8attn::BM);
+    if (n_tokens > 0)
+        f8attn::attn_f8_kernel<true><<<grid, f8attn::kThreads<true>, f8attn::kDynSmem, st>>>(a, nullptr, unused);
     return cudaGetLastError();
 }
 

@@ -54,6 +54,9 @@ cudaError_t launch_sparse_tc(const AttnArgs &a, int64_t n_tokens, cudaStream_t s
 // 128 x 32 boxes, 128-byte swizzle (encode_kv_tmap).
 cudaError_t launch_dense_f8(const AttnArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_kv, cudaStream_t st);
 bool encode_kv_tmap(CUtensorMap *map, const uint8_t *kv, int32_t num_blocks);
+// Sparse attention on e4m3 operands: rows gathered by index (cp.async), two
+// tokens x 64 heads per CTA.
+cudaError_t launch_sparse_f8(const AttnArgs &a, int64_t n_tokens, cudaStream_t st);
 
 // Indexer score work item: x = sequence, y = first new token (in-sequence),
 // z = token count (<= 4), w = key chunk. tmap_k: the key cache as

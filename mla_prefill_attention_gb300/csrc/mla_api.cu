@@ -311,7 +311,7 @@ mla_status_t mla_prefill_sparse(const mla_seqs_t *seqs, const void *q_bf16, int3
     mla::AttnArgs a = attn_args(seqs, q_bf16, num_heads, kv_e4m3, kv_scale, sm_scale, out_bf16, lse, dev_err);
     a.idx = idx;
     a.topk = topk;
-    cudaError_t e = mla::launch_sparse_tc(a, tq, stream);
+    cudaError_t e = mla::launch_sparse_f8(a, tq, stream);
     if (e != cudaSuccess) return cuda_fail(e, "sparse launch");
     return MLA_OK;
 }
