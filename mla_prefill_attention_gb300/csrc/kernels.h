@@ -44,14 +44,9 @@ struct IndexerArgs {
     int32_t *dev_err;
 };
 
-// tcgen05/TMEM attention (64 query rows per CTA). Dense work item: x = sequence,
-// y = row tile, z = paired row tile or -1. Sparse: one CTA per (token, 64 heads).
-cudaError_t launch_dense_tc(const AttnArgs &a, const int4 *work, int n_work, cudaStream_t st);
-cudaError_t launch_sparse_tc(const AttnArgs &a, int64_t n_tokens, cudaStream_t st);
-
-// Dense attention on e4m3 operands (kind::f8f6f4): same work items as
-// launch_dense_tc. tmap_kv: the latent cache as [num_blocks * 256 rows][576 B],
-// 128 x 32 boxes, 128-byte swizzle (encode_kv_tmap).
+// Dense attention on e4m3 operands (kind::f8f6f4). Work item: x = sequence,
+// y = 64-row tile, z = paired row tile or -1. tmap_kv: the latent cache as
+// [num_blocks * 256 rows][576 B], 128 x 32 boxes, 128-byte swizzle (encode_kv_tmap).
 cudaError_t launch_dense_f8(const AttnArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_kv, cudaStream_t st);
 bool encode_kv_tmap(CUtensorMap *map, const uint8_t *kv, int32_t num_blocks);
 // Sparse attention on e4m3 operands: rows gathered by index (cp.async), two
