@@ -116,7 +116,8 @@ mla_status_t mla_prefill_dense(const mla_seqs_t *seqs, const void *q_bf16, int32
  * scores, ties going to the lower position, written in ascending position
  * order and padded with -1. Scores are accumulated in fp32 (exact when q and
  * k hold small integers). w_token_stride 0 shares one 64-value row among all
- * tokens. topk in [1, 2048]. qi, ki 16-byte aligned. workspace:
+ * tokens; otherwise it is a multiple of 4. topk in [1, 2048]. qi, ki, w
+ * 16-byte aligned. workspace:
  * mla_workspace_size(MLA_OP_INDEXER, ...) bytes (fp32 scores of every
  * visible (token, position) pair plus scheduling data). */
 mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, const float *w,

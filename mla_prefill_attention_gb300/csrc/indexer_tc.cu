@@ -65,7 +65,6 @@ enum Bar {
 };
 
 struct Shared {
-    float w[TOK][kHidx];
     uint64_t bar[NBAR];
     uint32_t tmem_base;
 };
@@ -113,10 +112,6 @@ __global__ void __launch_bounds__(NT, 1)
     if (tid == 0) {
         for (int i = 0; i < NBAR; ++i) mbar_init(smem_u32(&sh.bar[i]), (i == B_D_EMPTY || i == B_D_EMPTY + 1) ? kEpiWarps : 1);
         mbar_fence_init();
-    }
-    for (int i = tid; i < TOK * kHidx; i += NT) {
-        const int j = i / kHidx;
-        sh.w[j][i % kHidx] = j < ntok ? __ldg(a.w + static_cast<int64_t>(q0 + i0 + j) * a.w_stride + i % kHidx) : 0.f;
     }
     if (warp == kIssuerWarp) {
         tmem_alloc(smem_u32(&sh.tmem_base), 512);
@@ -176,7 +171,10 @@ __global__ void __launch_bounds__(NT, 1)
         const int quad = warp & 3, j = warp >> 2;                     // keys 32 quad.., token j
         const uint32_t lane_addr = static_cast<uint32_t>(32 * quad) << 16;
         const int kk = 32 * quad + lane;                              // key within the tile
-        const float4 *wj = reinterpret_cast<const float4 *>(sh.w[j]);
+        // head weights by read-only global loads: the L1 path costs the tensor core's
+        // shared-memory operand reads nothing, which broadcast shared loads did (measured)
+        const float4 *wg = reinterpret_cast<const float4 *>(a.w + static_cast<int64_t>(q0 + i0 + min(j, ntok - 1)) *
+                                                            a.w_stride);
         float *out_row = a.scores + static_cast<int64_t>(q0 + i0 + j) * a.score_stride;
         const int pos_hi = min(k_hi, P + i0 + j + 1);                 // causal bound of token j (exclusive)
         // The key scales go through a register pipeline: the page of tile i+3 and
@@ -221,7 +219,7 @@ __global__ void __launch_bounds__(NT, 1)
             uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
             for (int h4 = 0; h4 < 8; ++h4) {
-                const float4 wa = wj[h4], wb = wj[8 + h4];
+                const float4 wa = __ldg(wg + h4), wb = __ldg(wg + 8 + h4);
                 ffma2(acc[0], pack2(wa.x, wa.y), pack2(relu_bits(d0[4 * h4 + 0]), relu_bits(d0[4 * h4 + 1])));
                 ffma2(acc[1], pack2(wa.z, wa.w), pack2(relu_bits(d0[4 * h4 + 2]), relu_bits(d0[4 * h4 + 3])));
                 ffma2(acc[2], pack2(wb.x, wb.y), pack2(relu_bits(d1[4 * h4 + 0]), relu_bits(d1[4 * h4 + 1])));

@@ -245,9 +245,11 @@ mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, co
         return fail(MLA_ERR_INVALID_ARG, "qi, w, ki, ki_scale and idx_out must be set");
     if (!aligned(qi_e4m3, 16) || !aligned(ki_e4m3, 16))
         return fail(MLA_ERR_INVALID_ARG, "qi and ki must be 16-byte aligned");
-    if (!aligned(w, 4) || !aligned(ki_scale, 4) || !aligned(idx_out, 4))
-        return fail(MLA_ERR_INVALID_ARG, "w, ki_scale and idx_out must be 4-byte aligned");
-    if (w_token_stride < 0) return fail(MLA_ERR_INVALID_ARG, "w_token_stride must be >= 0");
+    if (!aligned(w, 16)) return fail(MLA_ERR_INVALID_ARG, "w must be 16-byte aligned");
+    if (!aligned(ki_scale, 4) || !aligned(idx_out, 4))
+        return fail(MLA_ERR_INVALID_ARG, "ki_scale and idx_out must be 4-byte aligned");
+    if (w_token_stride < 0 || w_token_stride % 4 != 0)
+        return fail(MLA_ERR_INVALID_ARG, "w_token_stride must be a non-negative multiple of 4");
     if (topk < 1 || topk > 2048) return fail(MLA_ERR_UNSUPPORTED, "topk must be in [1, 2048] (got %d)", topk);
     const int64_t tq = seqs->cu_seqlens_q_host[seqs->batch];
     if (tq == 0) return MLA_OK;

@@ -81,6 +81,11 @@ def test_rejects_bad_arguments(lib):
                                     None) == B.MLA_ERR_UNSUPPORTED
     assert lib.mla_indexer_topk(ctypes.byref(s.c), FAKE, FAKE, -1, FAKE, FAKE, 2048, FAKE, None, 0, None,
                                 None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_indexer_topk(ctypes.byref(s.c), FAKE, FAKE, 6, FAKE, FAKE, 2048, FAKE, None, 0, None,
+                                None) == B.MLA_ERR_INVALID_ARG          # token stride not a multiple of 4
+    w4 = ctypes.c_void_p(0x100004)                              # w needs 16-byte alignment (float4 loads)
+    assert lib.mla_indexer_topk(ctypes.byref(s.c), FAKE, w4, 0, FAKE, FAKE, 2048, FAKE, None, 0, None,
+                                None) == B.MLA_ERR_INVALID_ARG
     assert lib.mla_indexer_topk(ctypes.byref(s.c), FAKE, FAKE, 0, FAKE, FAKE, 2048, FAKE, None, 0, None,
                                 None) == B.MLA_ERR_WORKSPACE
     odd = ctypes.c_void_p(0x100002)                             # idx needs 4-byte alignment

@@ -65,6 +65,24 @@ def test_indexer_small_exact(q_lens, prefix, topk):
         assert np.all(np.diff(v) > 0) and np.all(r[len(v):] == -1)
 
 
+def test_indexer_per_token_weights():
+    """One weight row per token (token stride 64) instead of a shared row."""
+    import torch
+    pb = Problem([40, 24], [600, 200], 16, seed=33, with_indexer=True)
+    rng = np.random.default_rng(33)
+    wt = (2.0 ** -rng.integers(0, 5, (pb.ps.total_q, 64))).astype(np.float32)   # exact like the shared row
+    d = pb.device()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    from mla_prefill_attention_gb300 import mla_indexer_topk
+    idx = mla_indexer_topk(d["seqs"], d["qi"], torch.from_numpy(wt).cuda(), 64, d["ki"], d["kis"], 300, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    toks = np.arange(pb.ps.total_q)
+    ref = O.indexer_topk(pb.ps, pb.qi, wt, 64, toks, pb.ki, pb.kis, 300)
+    got = np.sort(idx.cpu().numpy(), axis=1)
+    assert np.array_equal(np.sort(ref, axis=1), got)
+
+
 def test_indexer_ties_go_to_lower_position():
     """Keys repeat three rows, so whole groups of scores tie at the cut."""
     import torch
