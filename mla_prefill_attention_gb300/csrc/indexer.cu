@@ -192,32 +192,16 @@ __device__ __forceinline__ void topk_fail(const IndexerArgs &a, int32_t *out) {
     for (int j = threadIdx.x; j < a.topk; j += TK_NT) out[j] = -1;
 }
 
-// Per token: the exact top-k under the total order of key64 (score desc, then
-// lower position first). Phase A: digit histograms over the global row until
-// the keys sharing the k-th key's prefix fit in shared memory. Phase B, one
-// more pass: keys above that prefix are winners and their positions are kept
-// in order; keys with the prefix are gathered, in order, into shared memory.
-// Phase C resolves the remaining digits there and phase D appends the
-// candidates at or above the k-th key. The two ascending runs are merged, so
-// the row is written in ascending position order.
-__global__ void __launch_bounds__(TK_NT, 2) topk_kernel(const IndexerArgs a) {
-    extern __shared__ __align__(16) uint8_t tk_raw[];
-    uint64_t *cand = reinterpret_cast<uint64_t *>(tk_raw);
-    uint32_t *hist = reinterpret_cast<uint32_t *>(tk_raw + TK_CAP * 8);
-    int32_t *sel = reinterpret_cast<int32_t *>(tk_raw + TK_CAP * 8 + 4096 * 4);
-    __shared__ TkState st;
-    __shared__ uint32_t wsum[TK_U * TK_NW + 1];
-
-    const int64_t t = blockIdx.x;
-    const int b = find_seq(a.cu_seqlens, a.batch, t);
-    const int n = __ldg(a.prefix_lens + b) + static_cast<int>(t - __ldg(a.cu_seqlens + b)) + 1;
-    int32_t *out = a.idx_out + t * a.topk;
+// Exact radix path (any input; the fallback of the sampled path). Phase A:
+// digit histograms over the global row until the keys sharing the k-th key's
+// prefix fit in shared memory. Phase B, one more pass: keys above that prefix
+// are winners and their positions are kept in order; keys with the prefix are
+// gathered, in order, into shared memory. Phase C resolves the remaining digits
+// there and phase D appends the candidates at or above the k-th key. The two
+// ascending runs are merged, so the row is written in ascending position order.
+__device__ __noinline__ void topk_radix(const IndexerArgs &a, const float4 *row4, int n, int32_t *out, uint64_t *cand,
+                                        uint32_t *hist, int32_t *sel, TkState &st, uint32_t *wsum) {
     const int tid = threadIdx.x;
-    if (n <= a.topk) {
-        for (int j = tid; j < a.topk; j += TK_NT) out[j] = j < n ? j : -1;
-        return;
-    }
-    const float4 *row4 = reinterpret_cast<const float4 *>(a.scores + t * a.score_stride);
     const int n4 = (n + 3) >> 2;           // the row stride is a multiple of 4 floats
     const int widths[6] = {12, 12, 8, 12, 12, 8};
     if (tid == 0) {
@@ -375,6 +359,263 @@ __global__ void __launch_bounds__(TK_NT, 2) topk_kernel(const IndexerArgs a) {
             if (other[mid] < x) lo = mid + 1; else hi = mid;
         }
         out[(in_a ? i : i - na) + lo] = x;
+    }
+}
+
+// Block-wide bitonic sort of v[0..P) in shared memory (P a power of two).
+template <typename T, bool kDescending>
+__device__ __forceinline__ void bitonic_sort(T *v, int P) {
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < P / 2; i += TK_NT) {
+                const int lo = 2 * i - (i & (stride - 1)), hi = lo + stride;
+                const bool asc = ((lo & size) == 0) != kDescending;
+                const T x = v[lo], y = v[hi];
+                if (asc ? x > y : x < y) {
+                    v[lo] = y;
+                    v[hi] = x;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+__device__ __forceinline__ int pow2_at_least(int x) {
+    int p = 2;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+constexpr int TK_SAMPLE = 1024;
+constexpr int TK_PU = 4;    // float4 loads in flight per lane in the sampled passes
+
+__device__ __forceinline__ int bit_width(uint32_t x) { return x ? 32 - __clz(x) : 0; }
+
+// Sampled path: the k-th largest score is bracketed from an evenly spaced sample
+// of 1,024 scores (ranks expected +- 4 standard deviations + 2); two passes over
+// the row follow, each warp over its own contiguous segment with no atomics and
+// no block barrier: one counts the keys above the bracket (winners) and inside
+// it (candidates), the other stores them in position order. The candidates'
+// keys are re-based to the bracket (score bits - low end, then the position's
+// significant bits), and the radix digits run over those few bits in shared
+// memory; candidates at or above the k-th key follow the winners, and the two
+// ascending runs are merged. Returns false, having written nothing, when the
+// bracket misses (too few or too many keys inside it); the caller then takes
+// the radix path. The order is key64's, so ties resolve the same way.
+__device__ __noinline__ bool topk_sampled(const IndexerArgs &a, const float *row, const float4 *row4, int n,
+                                          int32_t *out, uint64_t *cand, uint32_t *hist, int32_t *sel,
+                                          uint32_t (*wcnt)[2], uint32_t *info, TkState &st, uint32_t *wsum) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int k = a.topk;
+    uint32_t *samp = hist;
+    for (int i = tid; i < TK_SAMPLE; i += TK_NT)
+        samp[i] = ord_f32(row[static_cast<int>((static_cast<int64_t>(i) * n) / TK_SAMPLE)]);
+    __syncthreads();
+    bitonic_sort<uint32_t, true>(samp, TK_SAMPLE);
+    const float e = static_cast<float>(k) * TK_SAMPLE / static_cast<float>(n);
+    const float mg = 4.f * sqrtf(e) + 2.f;
+    const int rh = static_cast<int>(floorf(e - mg)), rl = static_cast<int>(ceilf(e + mg));
+    const uint32_t t_hi = rh >= 0 ? samp[rh] : 0xFFFFFFFFu;   // winners: ord > t_hi
+    const uint32_t t_lo = rl < TK_SAMPLE ? samp[rl] : 0u;      // candidates: t_lo <= ord <= t_hi
+    __syncthreads();                                          // samp is reused as the histogram
+    const int n4 = (n + 3) >> 2;
+    const int seg4 = (n4 + TK_NW - 1) / TK_NW;
+    const int q_lo = warp * seg4, q_hi = min(n4, q_lo + seg4);
+    // ---- pass 1: counts per warp segment ----
+    uint32_t cw = 0, cc = 0;
+    for (int q0 = q_lo; q0 < q_hi; q0 += 32 * TK_PU) {
+        float4 v[TK_PU];
+#pragma unroll
+        for (int u = 0; u < TK_PU; ++u) {
+            const int q = q0 + 32 * u + lane;
+            v[u] = q < q_hi ? row4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < TK_PU; ++u) {
+            const int q = q0 + 32 * u + lane;
+            const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4) {
+                const uint32_t o = ord_f32(f[e4]);
+                const bool in = q < q_hi && 4 * q + e4 < n;
+                cw += (in && o > t_hi) ? 1u : 0u;
+                cc += (in && o >= t_lo && o <= t_hi) ? 1u : 0u;
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        cw += __shfl_xor_sync(0xffffffffu, cw, o);
+        cc += __shfl_xor_sync(0xffffffffu, cc, o);
+    }
+    if (lane == 0) {
+        wcnt[warp][0] = cw;
+        wcnt[warp][1] = cc;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t tw = 0, tc = 0;
+        for (int w = 0; w < TK_NW; ++w) {
+            const uint32_t x = wcnt[w][0], y = wcnt[w][1];
+            wcnt[w][0] = tw;
+            wcnt[w][1] = tc;
+            tw += x;
+            tc += y;
+        }
+        info[0] = tw;
+        info[1] = tc;
+        info[2] = (tw <= static_cast<uint32_t>(k) && static_cast<uint32_t>(k) <= tw + tc && tc <= TK_CAP) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!info[2]) return false;
+    const uint32_t n_win = info[0], nc = info[1];
+    // candidate key: (ord - t_lo) above the position's pb significant bits (complemented),
+    // shifted to the top of 64 bits so the standard digit sequence applies
+    const int pb = bit_width(static_cast<uint32_t>(n - 1));
+    const int kb = bit_width(t_hi - t_lo) + pb;               // <= 32 + 31
+    const uint32_t pmask = pb >= 32 ? 0xFFFFFFFFu : ((1u << pb) - 1u);
+    // ---- pass 2: winners' positions and candidates' keys, in position order ----
+    uint32_t wo = wcnt[warp][0], co = wcnt[warp][1];
+    for (int q0 = q_lo; q0 < q_hi; q0 += 32 * TK_PU) {
+        float4 v[TK_PU];
+#pragma unroll
+        for (int u = 0; u < TK_PU; ++u) {
+            const int q = q0 + 32 * u + lane;
+            v[u] = q < q_hi ? row4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < TK_PU; ++u) {
+            const int q = q0 + 32 * u + lane;
+            const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            uint32_t wm = 0, cm = 0, o[4];
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4) {
+                o[e4] = ord_f32(f[e4]);
+                if (q < q_hi && 4 * q + e4 < n) {
+                    if (o[e4] > t_hi) wm |= 1u << e4;
+                    else if (o[e4] >= t_lo) cm |= 1u << e4;
+                }
+            }
+            const uint32_t x = (static_cast<uint32_t>(__popc(cm)) << 16) | static_cast<uint32_t>(__popc(wm));
+            uint32_t incl = x;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += y;
+            }
+            const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31), ex = incl - x;
+            uint32_t pw = wo + (ex & 0xFFFFu), pc = co + (ex >> 16);
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4) {
+                const uint32_t s4 = static_cast<uint32_t>(4 * q + e4);
+                if (wm >> e4 & 1u) {
+                    sel[pw++] = static_cast<int32_t>(s4);
+                } else if (cm >> e4 & 1u) {
+                    const uint64_t key = (static_cast<uint64_t>(o[e4] - t_lo) << pb) | ((~s4) & pmask);
+                    cand[pc++] = key << (64 - kb);
+                }
+            }
+            wo += tot & 0xFFFFu;
+            co += tot >> 16;
+        }
+    }
+    // ---- the k-th key among the candidates (digits over the kb significant bits) ----
+    const uint32_t need = static_cast<uint32_t>(k) - n_win;
+    if (tid == 0) {
+        st.prefix = 0;
+        st.bits = 0;
+        st.krem = need;
+    }
+    __syncthreads();
+    if (need > 0) {
+        const int widths[6] = {12, 12, 8, 12, 12, 8};
+        int di = 0;
+        while (di < 6 && st.bits < kb) {
+            const int width = widths[di++], shift = 64 - st.bits - width;
+            const uint64_t pf = st.prefix;
+            const int bb = st.bits;
+            for (int d = tid; d < (1 << width); d += TK_NT) hist[d] = 0;
+            __syncthreads();
+            for (uint32_t i = tid; i < nc; i += TK_NT) {
+                const uint64_t key = cand[i];
+                hist_add(hist, prefix_match(key, pf, bb), static_cast<uint32_t>((key >> shift) & ((1u << width) - 1)));
+            }
+            __syncthreads();
+            pick(hist, width, shift, st, wsum);
+        }
+        if (st.bits < kb) {   // 64 bits cover any kb; unreachable
+            topk_fail(a, out);
+            return true;
+        }
+        // ---- candidates at or above the k-th key, in order, after the winners ----
+        const uint64_t kth = st.prefix;
+        uint32_t base = n_win;
+        for (uint32_t c0 = 0; c0 < nc; c0 += 4 * TK_NT) {
+            const uint32_t i0 = c0 + 4 * tid;
+            uint32_t f = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (i0 + j < nc && cand[i0 + j] >= kth) f |= 1u << j;
+            uint32_t tot;
+            uint32_t o = base + block_excl_scan(static_cast<uint32_t>(__popc(f)), wsum, tot);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (f >> j & 1u) {
+                    if (o < static_cast<uint32_t>(k)) {
+                        const uint32_t lowbits = static_cast<uint32_t>(cand[i0 + j] >> (64 - kb)) & pmask;
+                        sel[o] = static_cast<int32_t>((~lowbits) & pmask);
+                    }
+                    ++o;
+                }
+            }
+            base += tot;
+        }
+        if (base != static_cast<uint32_t>(k)) {
+            topk_fail(a, out);
+            return true;
+        }
+    }
+    // ---- merge the two ascending runs (winners, chosen candidates) ----
+    __syncthreads();
+    const int na = static_cast<int>(n_win), nb = k - na;
+    for (int i = tid; i < k; i += TK_NT) {
+        const bool in_a = i < na;
+        const int x = sel[i];
+        const int *other = in_a ? sel + na : sel;
+        int lo = 0, hi = in_a ? nb : na;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (other[mid] < x) lo = mid + 1; else hi = mid;
+        }
+        out[(in_a ? i : i - na) + lo] = x;
+    }
+    return true;
+}
+
+__global__ void __launch_bounds__(TK_NT, 2) topk_kernel(const IndexerArgs a) {
+    extern __shared__ __align__(16) uint8_t tk_raw[];
+    uint64_t *cand = reinterpret_cast<uint64_t *>(tk_raw);
+    uint32_t *hist = reinterpret_cast<uint32_t *>(tk_raw + TK_CAP * 8);   // also the sample
+    int32_t *sel = reinterpret_cast<int32_t *>(tk_raw + TK_CAP * 8 + 4096 * 4);
+    __shared__ TkState st;
+    __shared__ uint32_t wsum[TK_U * TK_NW + 1];
+    __shared__ uint32_t wcnt[TK_NW][2];
+    __shared__ uint32_t info[4];
+
+    const int64_t t = blockIdx.x;
+    const int b = find_seq(a.cu_seqlens, a.batch, t);
+    const int n = __ldg(a.prefix_lens + b) + static_cast<int>(t - __ldg(a.cu_seqlens + b)) + 1;
+    int32_t *out = a.idx_out + t * a.topk;
+    if (n <= a.topk) {
+        for (int j = threadIdx.x; j < a.topk; j += TK_NT) out[j] = j < n ? j : -1;
+        return;
+    }
+    const float *row = a.scores + t * a.score_stride;
+    const float4 *row4 = reinterpret_cast<const float4 *>(row);
+    if (!topk_sampled(a, row, row4, n, out, cand, hist, sel, wcnt, info, st, wsum)) {
+        __syncthreads();
+        topk_radix(a, row4, n, out, cand, hist, sel, st, wsum);
     }
 }
 
