@@ -56,6 +56,23 @@ def test_small_full(q_lens, prefix, H):
     check_rows(pb, out, lse, np.arange(pb.ps.total_q), f"{q_lens}/{prefix}/H{H}")
 
 
+def test_unwritten_cache_slots_are_ignored():
+    """Slots of a sequence's last page past its last token, and whole pages no
+    sequence owns, hold NaN codes (0x7F) and huge scales: nothing may leak into
+    the output (a NaN multiplied by a zero weight stays NaN)."""
+    import torch
+    pb = Problem([37, 5], [150, 700], 64, seed=77, shuffle=True, sm_scale=0.09, extra_blocks=2)
+    used = np.zeros(pb.kv.shape[:2], dtype=bool)
+    for bq in range(pb.ps.batch):
+        sp = np.arange(pb.ps.seq_len(bq))
+        used[pb.ps.block_table[bq, sp // 256], sp % 256] = True
+    pb.kv[~used] = 0x7F
+    pb.ks[~used] = 1e30
+    out, lse = run_dense(pb)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    check_rows(pb, out, lse, np.arange(pb.ps.total_q), "NaN-filled unwritten slots")
+
+
 def test_prefix12k_sampled():
     w = I.WORKLOADS["prefix12k"]
     pb = Problem(w.q_lens, w.prefix_lens, w.heads, w.seed, w.shuffle, w.sm_scale)
