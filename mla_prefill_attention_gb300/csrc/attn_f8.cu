@@ -223,13 +223,45 @@ __device__ __forceinline__ float2 float2_of_f16x2(uint32_t h) {
     *reinterpret_cast<uint32_t *>(&v) = h;
     return __half22float2(v);
 }
-// (p0, p1) -> (head codes) | (tail codes) << 16: head = e4m3 of the f16 values,
-// tail = e4m3 of what the head leaves (exact in f16).
+// (p0, p1) -> (head codes) | (tail codes) << 16: head = e4m3 of the f16 values
+// (rounded to nearest, so the remainder is at most half a head ulp), tail =
+// e4m3 of what the head leaves (exact in f16).
 __device__ __forceinline__ uint32_t split_p2(float p0, float p1) {
     const uint32_t h = pack_half2(p0, p1);
     const uint32_t hd = e4m3x2_of_f16x2(h);
     const uint32_t tl = e4m3x2_of_f16x2(hsub2_bits(h, f16x2_of_e4m3x2(hd)));
     return hd | (tl << 16);
+}
+// paired f32 arithmetic (two IEEE operations per instruction)
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 upk2(uint64_t v) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+    return f;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
 // Q rows ra, rb of the tile -> Qh, Ql in TMEM (lane half 0; 16x256b layout:
@@ -631,7 +663,10 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                 const bool full = kSparse ? lim_min >= 0 : key0 + BN - 1 <= lim_min;
                 const float mu_a0 = m_a == -INFINITY ? 0.f : m_a - kPOffset;
                 const float mu_b0 = m_b == -INFINITY ? 0.f : m_b - kPOffset;
-                float mx_a = -INFINITY, mx_b = -INFINITY, lt_a = 0.f, lt_b = 0.f;
+                float mx_a = -INFINITY, mx_b = -INFINITY;
+                uint64_t lt2a = 0, lt2b = 0;    // per-thread partial sums of P / sigma, two keys per word
+                const uint64_t rs2a = pk2(rs_a, rs_a), rs2b = pk2(rs_b, rs_b);
+                const uint64_t mu2a0 = pk2(mu_a0, mu_a0), mu2b0 = pk2(mu_b0, mu_b0);
                 uint32_t pa[BN / 8], pb[BN / 8];   // per 8-key group: this thread's pair of row a / row b, head | tail << 16
                 {   // logits, tile maxima and (against the reference max in force) P; for
                     // j == 0 that P is recomputed below once the max is known
@@ -639,10 +674,10 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                     for (int i = 0; i < BN / 8; ++i) {
                         const int k0 = 8 * i + 2 * tc;
                         const float4 m = meta.sl[4 * i + tc];
-                        float u0 = fmaf(__uint_as_float(sv[4 * i + 0]) * m.x, rs_a, m.z);
-                        float u1 = fmaf(__uint_as_float(sv[4 * i + 1]) * m.y, rs_a, m.w);
-                        float u2 = fmaf(__uint_as_float(sv[4 * i + 2]) * m.x, rs_b, m.z);
-                        float u3 = fmaf(__uint_as_float(sv[4 * i + 3]) * m.y, rs_b, m.w);
+                        const uint64_t sg = pk2(m.x, m.y), l2 = pk2(m.z, m.w);
+                        const float2 ua = upk2(fma2(mul2(pk2(__uint_as_float(sv[4 * i + 0]), __uint_as_float(sv[4 * i + 1])), sg), rs2a, l2));
+                        const float2 ub = upk2(fma2(mul2(pk2(__uint_as_float(sv[4 * i + 2]), __uint_as_float(sv[4 * i + 3])), sg), rs2b, l2));
+                        float u0 = ua.x, u1 = ua.y, u2 = ub.x, u3 = ub.y;
                         if (!full) {
                             const bool va0 = kSparse ? lim_a >= 0 : key0 + k0 <= lim_a;
                             const bool va1 = kSparse ? lim_a >= 0 : key0 + k0 + 1 <= lim_a;
@@ -657,14 +692,16 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                         sv[4 * i + 1] = __float_as_uint(u1);
                         sv[4 * i + 2] = __float_as_uint(u2);
                         sv[4 * i + 3] = __float_as_uint(u3);
-                        mx_a = fmaxf(mx_a, fmaxf(u0, u1));
-                        mx_b = fmaxf(mx_b, fmaxf(u2, u3));
+                        mx_a = max3(mx_a, u0, u1);
+                        mx_b = max3(mx_b, u2, u3);
                         {
                             const float2 is = meta.isig[4 * i + tc];
-                            const float p0 = fast_exp2(u0 - mu_a0), p1 = fast_exp2(u1 - mu_a0);
-                            const float p2 = fast_exp2(u2 - mu_b0), p3 = fast_exp2(u3 - mu_b0);
-                            lt_a = fmaf(p0, is.x, fmaf(p1, is.y, lt_a));
-                            lt_b = fmaf(p2, is.x, fmaf(p3, is.y, lt_b));
+                            const uint64_t isg = pk2(is.x, is.y);
+                            const float2 da = upk2(sub2(pk2(u0, u1), mu2a0)), db = upk2(sub2(pk2(u2, u3), mu2b0));
+                            const float p0 = fast_exp2(da.x), p1 = fast_exp2(da.y);
+                            const float p2 = fast_exp2(db.x), p3 = fast_exp2(db.y);
+                            lt2a = fma2(pk2(p0, p1), isg, lt2a);
+                            lt2b = fma2(pk2(p2, p3), isg, lt2b);
                             pa[i] = split_p2(p0, p1);
                             pb[i] = split_p2(p2, p3);
                         }
@@ -695,23 +732,28 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                 if (j == 0 || any_resc) {
                     const float mu_a = m_a == -INFINITY ? 0.f : m_a - kPOffset;
                     const float mu_b = m_b == -INFINITY ? 0.f : m_b - kPOffset;
-                    lt_a = 0.f;
-                    lt_b = 0.f;
+                    lt2a = 0;
+                    lt2b = 0;
+                    const uint64_t mu2a = pk2(mu_a, mu_a), mu2b = pk2(mu_b, mu_b);
 #pragma unroll
                     for (int i = 0; i < BN / 8; ++i) {
                         const float2 is = meta.isig[4 * i + tc];
-                        const float p0 = fast_exp2(__uint_as_float(sv[4 * i + 0]) - mu_a);
-                        const float p1 = fast_exp2(__uint_as_float(sv[4 * i + 1]) - mu_a);
-                        const float p2 = fast_exp2(__uint_as_float(sv[4 * i + 2]) - mu_b);
-                        const float p3 = fast_exp2(__uint_as_float(sv[4 * i + 3]) - mu_b);
-                        lt_a = fmaf(p0, is.x, fmaf(p1, is.y, lt_a));
-                        lt_b = fmaf(p2, is.x, fmaf(p3, is.y, lt_b));
+                        const uint64_t isg = pk2(is.x, is.y);
+                        const float2 da = upk2(sub2(pk2(__uint_as_float(sv[4 * i + 0]), __uint_as_float(sv[4 * i + 1])), mu2a));
+                        const float2 db = upk2(sub2(pk2(__uint_as_float(sv[4 * i + 2]), __uint_as_float(sv[4 * i + 3])), mu2b));
+                        const float p0 = fast_exp2(da.x), p1 = fast_exp2(da.y);
+                        const float p2 = fast_exp2(db.x), p3 = fast_exp2(db.y);
+                        lt2a = fma2(pk2(p0, p1), isg, lt2a);
+                        lt2b = fma2(pk2(p2, p3), isg, lt2b);
                         pa[i] = split_p2(p0, p1);
                         pb[i] = split_p2(p2, p3);
                     }
                 }
-                l_a = fmaf(l_a, al_a, lt_a);
-                l_b = fmaf(l_b, al_b, lt_b);
+                {
+                    const float2 sa = upk2(lt2a), sb = upk2(lt2b);
+                    l_a = fmaf(l_a, al_a, sa.x + sa.y);
+                    l_b = fmaf(l_b, al_b, sb.x + sb.y);
+                }
                 if (any_resc) {
                     if (!(ok = wait(B_PV_DONE + ((t - 1) & 1), ((t - 1) >> 1) & 1))) break;
                     fence_after_sync();
