@@ -62,12 +62,17 @@ using namespace tc;
 
 constexpr int BM = 64;                          // query rows per tile
 constexpr int BN = 96;                          // keys per tile
-// dense: 6 warps (4 softmax, TMA producer, issuer); sparse: 9 (4 softmax, issuer and
-// two pairs of gather warps: a warp keeps only so many row copies in flight)
-template <bool kSparse>
-constexpr int kThreads = kSparse ? 288 : 192;
-constexpr int kProducerWarp = 4, kIssuerWarp = 5;
-// Gather warps 4, 6 (pair 0: even tiles) and 7, 8 (pair 1: odd tiles); each warp of
+// Warps. dense: 10 = 8 softmax (two per TMEM lane quadrant, 48 of a tile's 96 keys
+// each: the softmax of tile t then ends before QK(t+1) does), TMA producer (8),
+// issuer (9). sparse: 9 = 4 softmax (96 keys each; with eight, the register cap of
+// 13 warps costs more than the shorter softmax gains), issuer (5) and two pairs of
+// gather warps (4, 6 and 7, 8: a warp keeps only so many row copies in flight).
+template <bool kSparse> constexpr int kSmWarps = kSparse ? 4 : 8;
+template <bool kSparse> constexpr int kSmKeys = BN * 4 / kSmWarps<kSparse>;   // keys per softmax warp
+template <bool kSparse> constexpr int kThreads = kSparse ? 288 : 320;
+template <bool kSparse> constexpr int kIssuerWarp = kSparse ? 5 : 9;
+constexpr int kProducerWarp = 8;   // dense
+// Gather pair 0 (warps 4, 6) takes even tiles, pair 1 (7, 8) odd ones; each warp of
 // a pair copies half of the tile's rows. A pair waits for a stage at most one
 // phase ahead of its completed one (its previous tile waited for the phase before),
 // which keeps the parity waits exact.
@@ -103,7 +108,8 @@ enum Bar {
     B_O_FREE = 19,       //     softmax -> issuer: epilogue done with O
     B_FINAL = 20,        //     issuer -> teardown
     B_FIX = 21,          //     producer's own: a box whose tail it zeroes
-    NBAR = 22
+    B_XCH = 22,          // [4] the two softmax warps of a quadrant: tile maxima, then row sums
+    NBAR = 26
 };
 
 struct __align__(16) KeyMeta {
@@ -113,6 +119,8 @@ struct __align__(16) KeyMeta {
 
 struct Shared {
     KeyMeta meta[4];
+    float xmax[2][4][2][16];   // [tile parity][quadrant][key half][row]: tile maxima
+    float xsum[4][2][16];      // [quadrant][key half][row]: row sums at the epilogue
     uint64_t bar[NBAR];
     uint32_t tmem_base;
 };
@@ -268,7 +276,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // column group g holds dims 32g + 8tc .. +7 of this thread's rows). Returns the
 // logit scale s_Q * sm_scale * log2(e) per row.
 __device__ __noinline__ void load_q_split(const AttnArgs &a, const RowTile &rt, uint32_t tq_addr, int ra, int rb,
-                                             int tc, float &rs_a, float &rs_b) {
+                                             int tc, int g_first, int g_count, float &rs_a, float &rs_b) {
     const bool oka = ra < rt.nvalid, okb = rb < rt.nvalid;
     const uint4 *qa = reinterpret_cast<const uint4 *>(a.q + (rt.grow0 + (oka ? ra : 0)) * kDqk + 8 * tc);
     const uint4 *qb = reinterpret_cast<const uint4 *>(a.q + (rt.grow0 + (okb ? rb : 0)) * kDqk + 8 * tc);
@@ -310,14 +318,15 @@ __device__ __noinline__ void load_q_split(const AttnArgs &a, const RowTile &rt, 
             tl[w] = e4m3x2_of(x0 - g01.x, x1 - g01.y) | (e4m3x2_of(x2 - g23.x, x3 - g23.y) << 16);
         }
     };
+    // this warp's column groups g_first .. g_first + g_count - 1 (all 18, or one half)
 #pragma unroll 1
-    for (int g0 = 0; g0 < 18; g0 += 8) {
+    for (int g0 = g_first; g0 < g_first + g_count; g0 += 8) {
         uint32_t wh[32], wl[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int g = g0 + i;
             uint4 va = make_uint4(0, 0, 0, 0), vb = make_uint4(0, 0, 0, 0);
-            if (g < 18) {
+            if (g < g_first + g_count) {
                 if (oka) va = __ldg(qa + 4 * g);
                 if (okb) vb = __ldg(qb + 4 * g);
             }
@@ -333,12 +342,16 @@ __device__ __noinline__ void load_q_split(const AttnArgs &a, const RowTile &rt, 
             wl[4 * i + 2] = lb[0];
             wl[4 * i + 3] = lb[1];
         }
-        if (g0 + 8 <= 18) {
+        const int left = g_first + g_count - g0;        // 8 or more, 2 (all 18) or 1 (a half)
+        if (left >= 8) {
             tmem_st_16x256b_x8(tq_addr + kColQh + 8 * g0, wh);
             tmem_st_16x256b_x8(tq_addr + kColQl + 8 * g0, wl);
-        } else {
+        } else if (left == 2) {
             tmem_st_16x256b_x2(tq_addr + kColQh + 8 * g0, wh);
             tmem_st_16x256b_x2(tq_addr + kColQl + 8 * g0, wl);
+        } else {
+            tmem_st_16x256b_x1(tq_addr + kColQh + 8 * g0, wh);
+            tmem_st_16x256b_x1(tq_addr + kColQl + 8 * g0, wl);
         }
     }
 }
@@ -385,13 +398,14 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
             uint32_t cnt = 1;
             if ((i >= B_S_FREE && i < B_S_FREE + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) || i == B_Q_FULL ||
                 i == B_O_FREE)
-                cnt = 4;
+                cnt = kSmWarps<kSparse>;
             if (kSparse && i >= B_FULL && i < B_FULL + kStages) cnt = 2;       // both warps of a gather pair
+            if (i >= B_XCH && i < B_XCH + 4) cnt = 2;                          // the quadrant's two softmax warps
             mbar_init(smem_u32(&sh.bar[i]), cnt);
         }
         mbar_fence_init();
     }
-    if (warp == kIssuerWarp) {
+    if (warp == kIssuerWarp<kSparse>) {
         tmem_alloc(smem_u32(&sh.tmem_base), 512);
         tmem_relinquish();
     }
@@ -491,7 +505,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL + st]));
         }
-    } else if (kSparse && warp >= 4 && warp != kIssuerWarp) {
+    } else if (kSparse && warp >= kSmWarps<kSparse> && warp != kIssuerWarp<kSparse>) {
         // =================== row gathers (sparse): pair p takes tiles p, p+2, ... ===================
         // Key k's 576 bytes go by 16-byte cp.async into the swizzled slices, eight
         // lanes per row (one 128-byte slice row per instruction and row), four rows
@@ -552,7 +566,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL + st]));
         }
-    } else if (warp == kIssuerWarp) {
+    } else if (warp == kIssuerWarp<kSparse>) {
         // =================== MMA issuer (lane 0; the other lanes wait at the end) ===================
         // One thread issues: the same instruction stream issued warp-wide with a
         // leader predicate runs ~1.5x slower (measured), as the issue itself
@@ -621,8 +635,22 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
         }
         __syncwarp();
     } else {
-        // =================== softmax / correction (warps 0-3) ===================
-        const int q = warp;
+        // =================== softmax / correction ===================
+        // warp w: TMEM quadrant w % 4, keys kSmKeys * (w / 4) .. of each tile; with two
+        // warps per quadrant they trade tile maxima (and, at the end, row sums) in smem
+        constexpr int kKeys = kSmKeys<kSparse>;
+        constexpr bool kPair = kSmWarps<kSparse> == 8;
+        constexpr int kGroups = 18 * kKeys / BN;         // Q column groups per warp
+        constexpr int kOCols = 512 * kKeys / BN;         // O columns per warp
+        const int q = warp & 3, kh = warp >> 2;
+        uint32_t xph = 0;
+        auto xch = [&]() -> bool {      // both warps of the quadrant arrive, then wait
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_XCH + q]));
+            const bool w = wait(B_XCH + q, xph);
+            xph ^= 1;
+            return w;
+        };
         const int tq = lane >> 2, tc = lane & 3;
         const int ra = 16 * q + tq, rb = ra + 8;
         const uint32_t lane_lo = static_cast<uint32_t>(32 * q) << 16;
@@ -635,7 +663,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
         bool ok = true;
         RowTile rt = tile_of(0);
         float rs_a, rs_b;
-        load_q_split(a, rt, tmem + lane_lo, ra, rb, tc, rs_a, rs_b);
+        load_q_split(a, rt, tmem + lane_lo, ra, rb, tc, kGroups * kh, kGroups, rs_a, rs_b);
         tmem_st_wait();
         fence_before_sync();
         __syncwarp();
@@ -651,29 +679,34 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                 if (!(ok = wait(B_META + (t & 3), (t >> 2) & 1))) break;
                 if (!(ok = wait(B_S_FULL + sb, (t >> 1) & 1))) break;
                 fence_after_sync();
-                uint32_t sv[48];
-                tmem_ld_16x256b_x8(tmem + lane_lo + kColS + BN * sb, sv);
-                tmem_ld_16x256b_x4(tmem + lane_lo + kColS + BN * sb + 64, sv + 32);
+                uint32_t sv[kKeys / 2];
+                if constexpr (kKeys == 48) {
+                    tmem_ld_16x256b_x4(tmem + lane_lo + kColS + BN * sb + kKeys * kh, sv);
+                    tmem_ld_16x256b_x2(tmem + lane_lo + kColS + BN * sb + kKeys * kh + 32, sv + 16);
+                } else {
+                    tmem_ld_16x256b_x8(tmem + lane_lo + kColS + BN * sb, sv);
+                    tmem_ld_16x256b_x4(tmem + lane_lo + kColS + BN * sb + 64, sv + 32);
+                }
                 tmem_ld_wait();
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_S_FREE + sb]));
                 const KeyMeta &meta = sh.meta[t & 3];
-                const int key0 = j * BN;
-                const bool full = kSparse ? lim_min >= 0 : key0 + BN - 1 <= lim_min;
+                const int key0 = j * BN + kKeys * kh;     // this warp's first key
+                const bool full = kSparse ? lim_min >= 0 : key0 + kKeys - 1 <= lim_min;
                 const float mu_a0 = m_a == -INFINITY ? 0.f : m_a - kPOffset;
                 const float mu_b0 = m_b == -INFINITY ? 0.f : m_b - kPOffset;
                 float mx_a = -INFINITY, mx_b = -INFINITY;
                 uint64_t lt2a = 0, lt2b = 0;    // per-thread partial sums of P / sigma, two keys per word
                 const uint64_t rs2a = pk2(rs_a, rs_a), rs2b = pk2(rs_b, rs_b);
                 const uint64_t mu2a0 = pk2(mu_a0, mu_a0), mu2b0 = pk2(mu_b0, mu_b0);
-                uint32_t pa[BN / 8], pb[BN / 8];   // per 8-key group: this thread's pair of row a / row b, head | tail << 16
+                uint32_t pa[kKeys / 8], pb[kKeys / 8];   // per 8-key group: this thread's pair of row a / row b, head | tail << 16
                 {   // logits, tile maxima and (against the reference max in force) P; for
                     // j == 0 that P is recomputed below once the max is known
 #pragma unroll
-                    for (int i = 0; i < BN / 8; ++i) {
+                    for (int i = 0; i < kKeys / 8; ++i) {
                         const int k0 = 8 * i + 2 * tc;
-                        const float4 m = meta.sl[4 * i + tc];
+                        const float4 m = meta.sl[kKeys / 2 * kh + 4 * i + tc];
                         const uint64_t sg = pk2(m.x, m.y), l2 = pk2(m.z, m.w);
                         const float2 ua = upk2(fma2(mul2(pk2(__uint_as_float(sv[4 * i + 0]), __uint_as_float(sv[4 * i + 1])), sg), rs2a, l2));
                         const float2 ub = upk2(fma2(mul2(pk2(__uint_as_float(sv[4 * i + 2]), __uint_as_float(sv[4 * i + 3])), sg), rs2b, l2));
@@ -695,7 +728,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                         mx_a = max3(mx_a, u0, u1);
                         mx_b = max3(mx_b, u2, u3);
                         {
-                            const float2 is = meta.isig[4 * i + tc];
+                            const float2 is = meta.isig[kKeys / 2 * kh + 4 * i + tc];
                             const uint64_t isg = pk2(is.x, is.y);
                             const float2 da = upk2(sub2(pk2(u0, u1), mu2a0)), db = upk2(sub2(pk2(u2, u3), mu2b0));
                             const float p0 = fast_exp2(da.x), p1 = fast_exp2(da.y);
@@ -711,6 +744,16 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                 mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
                 mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
                 mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+                if constexpr (kPair) {   // the other key half's maxima of the same rows
+                    float (*xm)[16] = sh.xmax[t & 1][q];
+                    if (tc == 0) {
+                        xm[kh][tq] = mx_a;
+                        xm[kh][8 + tq] = mx_b;
+                    }
+                    if (!(ok = xch())) break;
+                    mx_a = fmaxf(mx_a, xm[kh ^ 1][tq]);
+                    mx_b = fmaxf(mx_b, xm[kh ^ 1][8 + tq]);
+                }
                 float al_a = 1.f, al_b = 1.f;
                 bool resc = false;
                 if (j == 0) {
@@ -736,8 +779,8 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                     lt2b = 0;
                     const uint64_t mu2a = pk2(mu_a, mu_a), mu2b = pk2(mu_b, mu_b);
 #pragma unroll
-                    for (int i = 0; i < BN / 8; ++i) {
-                        const float2 is = meta.isig[4 * i + tc];
+                    for (int i = 0; i < kKeys / 8; ++i) {
+                        const float2 is = meta.isig[kKeys / 2 * kh + 4 * i + tc];
                         const uint64_t isg = pk2(is.x, is.y);
                         const float2 da = upk2(sub2(pk2(__uint_as_float(sv[4 * i + 0]), __uint_as_float(sv[4 * i + 1])), mu2a));
                         const float2 db = upk2(sub2(pk2(__uint_as_float(sv[4 * i + 2]), __uint_as_float(sv[4 * i + 3])), mu2b));
@@ -758,7 +801,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                     if (!(ok = wait(B_PV_DONE + ((t - 1) & 1), ((t - 1) >> 1) & 1))) break;
                     fence_after_sync();
 #pragma unroll 1
-                    for (int c0 = 0; c0 < 512; c0 += 64) {
+                    for (int c0 = kOCols * kh; c0 < kOCols * kh + kOCols; c0 += 64) {   // this warp's O columns
                         uint32_t o[32];
                         tmem_ld_16x256b_x8(tmem + lane_hi + c0, o);
                         tmem_ld_wait();
@@ -777,14 +820,15 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                 if (t >= 2 && !(ok = wait(B_PV_DONE + sb, ((t >> 1) - 1) & 1))) break;
                 uint8_t *ph = pbase + (2 * sb) * kPBytes, *pl = ph + kPBytes;
 #pragma unroll
-                for (int i = 0; i < BN / 8; ++i) {
+                for (int i = 0; i < kKeys / 8; ++i) {
                     // the even lane of a pair writes row a's word, the odd lane row b's
                     const uint32_t own = even ? pa[i] : pb[i];
                     const uint32_t oth = __shfl_xor_sync(0xffffffffu, even ? pb[i] : pa[i], 1);
                     const uint32_t lo2 = even ? own : oth, hi2 = even ? oth : own;   // lower keys first
                     const uint32_t hw = (lo2 & 0xFFFFu) | (hi2 << 16);
                     const uint32_t lw = (lo2 >> 16) | (hi2 & 0xFFFF0000u);
-                    const uint32_t off = poff + (i >> 1) * 128 + 8 * (i & 1);
+                    const int ig = kKeys / 8 * kh + i;           // 8-key group within the tile
+                    const uint32_t off = poff + (ig >> 1) * 128 + 8 * (ig & 1);
                     *reinterpret_cast<uint32_t *>(ph + off) = hw;
                     *reinterpret_cast<uint32_t *>(pl + off) = lw;
                 }
@@ -798,7 +842,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
             float rs_na = 0.f, rs_nb = 0.f;
             if (r + 1 < n_rt) {
                 rt = tile_of(r + 1);
-                load_q_split(a, rt, tmem + lane_lo, ra, rb, tc, rs_na, rs_nb);
+                load_q_split(a, rt, tmem + lane_lo, ra, rb, tc, kGroups * kh, kGroups, rs_na, rs_nb);
                 tmem_st_wait();
                 fence_before_sync();
                 __syncwarp();
@@ -811,8 +855,18 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
             l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
             l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
             l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+            if constexpr (kPair) {   // plus the other key half's sums
+                if (tc == 0) {
+                    sh.xsum[q][kh][tq] = l_a;
+                    sh.xsum[q][kh][8 + tq] = l_b;
+                }
+                if (!(ok = xch())) break;
+                l_a += sh.xsum[q][kh ^ 1][tq];
+                l_b += sh.xsum[q][kh ^ 1][8 + tq];
+                if (!(ok = xch())) break;      // both read before the next row tile writes again
+            }
             const bool va = lim_a >= 0, vb = lim_b >= 0;
-            if (tc == 0 && a.lse) {
+            if (tc == 0 && kh == 0 && a.lse) {
                 if (va) a.lse[rt_done.grow0 + ra] = l_a > 0.f ? (m_a - kPOffset + __log2f(l_a)) * kLn2 : -INFINITY;
                 if (vb) a.lse[rt_done.grow0 + rb] = l_b > 0.f ? (m_b - kPOffset + __log2f(l_b)) * kLn2 : -INFINITY;
             }
@@ -820,7 +874,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
             __nv_bfloat16 *da = a.out + (rt_done.grow0 + ra) * kDv + 2 * tc;
             __nv_bfloat16 *db = a.out + (rt_done.grow0 + rb) * kDv + 2 * tc;
 #pragma unroll 1
-            for (int c0 = 0; c0 < 512; c0 += 64) {
+            for (int c0 = kOCols * kh; c0 < kOCols * kh + kOCols; c0 += 64) {     // this warp's O columns
                 uint32_t o[32];
                 tmem_ld_16x256b_x8(tmem + lane_hi + c0, o);
                 tmem_ld_wait();
@@ -844,7 +898,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
 
     // ----- teardown: every MMA complete before TMEM is released -----
     __syncthreads();
-    if (warp == kIssuerWarp) {
+    if (warp == kIssuerWarp<kSparse>) {
         if (!mbar_wait_cycles(smem_u32(&sh.bar[B_FINAL]), 0, kWaitCycles)) set_dev_err(a.dev_err, MLA_DEVERR_TIMEOUT);
         fence_after_sync();
         tmem_dealloc(tmem, 512);

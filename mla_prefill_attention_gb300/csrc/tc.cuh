@@ -192,7 +192,11 @@ __device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t *r) 
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
-// Stores with the .16x256b layout (the inverse of the loads above): 64, 32 and 16 columns.
+// Stores with the .16x256b layout (the inverse of the loads above): 8 to 64 columns.
+__device__ __forceinline__ void tmem_st_16x256b_x1(uint32_t taddr, const uint32_t *r) {
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3]));
+}
 __device__ __forceinline__ void tmem_st_16x256b_x2(uint32_t taddr, const uint32_t *r) {
     asm volatile("tcgen05.st.sync.aligned.16x256b.x2.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr), "r"(r[0]),
                  "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
