@@ -61,14 +61,22 @@ namespace f8attn {
 using namespace tc;
 
 constexpr int BM = 64;                          // query rows per tile
-constexpr int BN = 96;                          // keys per tile
+// Key tiles: dense 128 keys (a QK MMA of N=128 runs at its nominal rate under a full
+// SM; N=96 loses ~40%), sparse 96. Dense keeps two stages, each released in three
+// parts (RoPE after QK, value dims 0-255 and 256-511 after the two PV chunks), and one
+// S buffer; sparse keeps three whole stages and two S buffers.
+template <bool S> constexpr int kBN = S ? 96 : 128;
+template <bool S> constexpr int kStages = S ? 3 : 2;
+template <bool S> constexpr int kParts = S ? 1 : 3;
+template <bool S> constexpr int kSBufs = S ? 2 : 1;
+constexpr int kBNMax = 128;
 // Warps. dense: 10 = 8 softmax (two per TMEM lane quadrant, 48 of a tile's 96 keys
 // each: the softmax of tile t then ends before QK(t+1) does), TMA producer (8),
 // issuer (9). sparse: 9 = 4 softmax (96 keys each; with eight, the register cap of
 // 13 warps costs more than the shorter softmax gains), issuer (5) and two pairs of
 // gather warps (4, 6 and 7, 8: a warp keeps only so many row copies in flight).
 template <bool kSparse> constexpr int kSmWarps = kSparse ? 4 : 8;
-template <bool kSparse> constexpr int kSmKeys = BN * 4 / kSmWarps<kSparse>;   // keys per softmax warp
+template <bool kSparse> constexpr int kSmKeys = kBN<kSparse> * 4 / kSmWarps<kSparse>;   // keys per softmax warp
 template <bool kSparse> constexpr int kThreads = kSparse ? 288 : 320;
 template <bool kSparse> constexpr int kIssuerWarp = kSparse ? 5 : 9;
 constexpr int kProducerWarp = 8;   // dense
@@ -78,43 +86,41 @@ constexpr int kProducerWarp = 8;   // dense
 // which keeps the parity waits exact.
 __device__ __forceinline__ int gather_pair(int warp) { return warp == 4 || warp == 6 ? 0 : 1; }
 __device__ __forceinline__ int gather_half(int warp) { return warp == 4 || warp == 7 ? 0 : 1; }
-constexpr int kBox = 32;                        // keys per TMA box
-constexpr int kBoxes = BN / kBox;
 constexpr int kSlices = 5;
-constexpr int kSliceBytes = BN * 128;           // 12288
-constexpr int kBoxBytes = kBox * 128;           // 4096
-constexpr int kStageBytes = kSlices * kSliceBytes;
-constexpr int kStages = 3;
-constexpr int kPBytes = BM * BN;                // one e4m3 term of P: 6144
-constexpr int kOffP = kStages * kStageBytes;
-constexpr int kDynSmem = 1024 + kOffP + 4 * kPBytes;
+template <bool S> constexpr int kSliceBytes = kBN<S> * 128;
+template <bool S> constexpr int kStageBytes = kSlices * kSliceBytes<S>;
+template <bool S> constexpr int kPBytes = BM * kBN<S>;          // one e4m3 term of P
+template <bool S> constexpr int kPSbo = kBN<S> / 16 * 128;      // P: 8-row band stride
+template <bool S> constexpr int kOffP = kStages<S> * kStageBytes<S>;
+template <bool S> constexpr int kDynSmem = 1024 + kOffP<S> + 4 * kPBytes<S>;
+constexpr int kGroupRows = 32;                  // sparse metadata: keys per lane round
 constexpr long long kWaitCycles = 200000000LL;
 constexpr float kRescaleThreshold = 2.0f;
 constexpr float kPOffset = 6.0f;
-static_assert(kPage % kBox == 0, "a TMA box must not straddle a page");
+static_assert(kPage % kBN<false> == 0, "a dense key tile must not straddle a page");
 
 constexpr uint32_t kColQh = 0, kColQl = 144, kColS = 288;
 constexpr uint32_t kHalf1 = 16u << 16;
 
 enum Bar {
-    B_FULL = 0,          // [3] producer (+TMA bytes) -> issuer: stage loaded
-    B_EMPTY = 3,         // [3] issuer (commit) -> producer: PV done with the stage
-    B_META = 6,          // [4] producer -> softmax: key metadata of tile t, ring t&3
-    B_S_FULL = 10,       // [2] issuer (commit) -> softmax
-    B_S_FREE = 12,       // [2] softmax -> issuer
-    B_P_FULL = 14,       // [2] softmax -> issuer (P written, O rescaled)
-    B_PV_DONE = 16,      // [2] issuer (commit) -> softmax
-    B_Q_FULL = 18,       //     softmax -> issuer
-    B_O_FREE = 19,       //     softmax -> issuer: epilogue done with O
-    B_FINAL = 20,        //     issuer -> teardown
-    B_FIX = 21,          //     producer's own: a box whose tail it zeroes
-    B_XCH = 22,          // [4] the two softmax warps of a quadrant: tile maxima, then row sums
-    NBAR = 26
+    B_FULL = 0,          // [part * stages + stage] producer (+TMA bytes) -> issuer: loaded
+    B_EMPTY = 9,         // [part * stages + stage] issuer (commit) -> producer: done with it
+    B_META = 18,         // [4] producer -> softmax: key metadata of tile t, ring t&3
+    B_S_FULL = 22,       // [2] issuer (commit) -> softmax
+    B_S_FREE = 24,       // [2] softmax -> issuer
+    B_P_FULL = 26,       // [2] softmax -> issuer (P written, O rescaled)
+    B_PV_DONE = 28,      // [2] issuer (commit) -> softmax
+    B_Q_FULL = 30,       //     softmax -> issuer
+    B_O_FREE = 31,       //     softmax -> issuer: epilogue done with O
+    B_FINAL = 32,        //     issuer -> teardown
+    B_FIX = 33,          //     producer's own: a tile whose tail it zeroes
+    B_XCH = 34,          // [4] the two softmax warps of a quadrant: tile maxima, then row sums
+    NBAR = 38
 };
 
 struct __align__(16) KeyMeta {
-    float4 sl[BN / 2];    // sigma of keys 2p, 2p+1; log2 sigma of both (-inf: masked)
-    float2 isig[BN / 2];  // 1/sigma of both
+    float4 sl[kBNMax / 2];    // sigma of keys 2p, 2p+1; log2 sigma of both (-inf: masked)
+    float2 isig[kBNMax / 2];  // 1/sigma of both
 };
 
 struct Shared {
@@ -164,7 +170,7 @@ __device__ __forceinline__ RowTile make_tile(const AttnArgs &a, int b, int tile,
         rt.grow0 = tok * a.H + h0;
         rt.nvalid = min(BM, a.H - h0);
         rt.key_last = __ldg(a.prefix_lens + rt.b) + static_cast<int>(tok - __ldg(a.cu_seqlens + rt.b));
-        rt.n_ktiles = (a.topk + BN - 1) / BN;
+        rt.n_ktiles = (a.topk + kBN<true> - 1) / kBN<true>;
     } else {
         const int q0 = __ldg(a.cu_seqlens + b), qn = __ldg(a.cu_seqlens + b + 1) - q0;
         const int P = __ldg(a.prefix_lens + b);
@@ -174,7 +180,7 @@ __device__ __forceinline__ RowTile make_tile(const AttnArgs &a, int b, int tile,
         rt.grow0 = static_cast<int64_t>(q0) * a.H + r_lo;
         rt.nvalid = min(BM, rows - r_lo);
         rt.key_last = P + (r_lo + rt.nvalid - 1) / a.H;
-        rt.n_ktiles = rt.key_last / BN + 1;
+        rt.n_ktiles = rt.key_last / kBN<false> + 1;
     }
     return rt;
 }
@@ -399,7 +405,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
             if ((i >= B_S_FREE && i < B_S_FREE + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) || i == B_Q_FULL ||
                 i == B_O_FREE)
                 cnt = kSmWarps<kSparse>;
-            if (kSparse && i >= B_FULL && i < B_FULL + kStages) cnt = 2;       // both warps of a gather pair
+            if (kSparse && i >= B_FULL && i < B_FULL + kStages<true>) cnt = 2;   // both warps of a gather pair
             if (i >= B_XCH && i < B_XCH + 4) cnt = 2;                          // the quadrant's two softmax warps
             mbar_init(smem_u32(&sh.bar[i]), cnt);
         }
@@ -417,104 +423,112 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
 
     if (!kSparse && warp == kProducerWarp) {
         // =================== TMA producer + key metadata ===================
-        // The global loads of tile t (block-table entries, then key scales) are
-        // issued before the wait for its stage, so their latency hides behind it;
-        // once the stage is free the boxes go to TMA at once.
+        // Tile t: one 128-row box per slice (a tile lies in one page). Its parts go
+        // as they are released: the RoPE slice once QK(t-2) is done with it, value
+        // slices 0-1 and 2-3 once the two PV chunks of tile t-2 are. The block-table
+        // and scale loads are issued before the first wait. A tile that reaches past
+        // the causal limit is loaded whole, then its tail rows are zeroed (an
+        // unwritten cache row could hold a NaN code, which a zero weight would not
+        // cancel), and all three parts are released together.
+        constexpr int BN = kBN<false>, ST = kStages<false>;
         if (lane == 0) tma_prefetch_desc(&tmap_kv);
         RowTile rt = tile_of(0);
         const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.max_blocks;
         uint32_t fix_phase = 0;
         bool ok = true;
+        auto wait_empty = [&](int part, int t) -> bool {
+            return t < ST || wait(B_EMPTY + part * ST + t % ST, ((t / ST) - 1) & 1);
+        };
         for (int t = 0; t < walk.total && ok; ++t) {
-            const int st = t % kStages;
+            const int st = t % ST;
             if (t > 0 && walk.r(t) != walk.r(t - 1)) rt = tile_of(1);
             const int key0 = walk.j(t) * BN;
-            // this lane's keys lane + 32i: cache rows, then scales
-            int64_t krow[kBoxes];
-            float ksig[kBoxes];
+            int64_t krow[BN / 32];
+            float ksig[BN / 32];
 #pragma unroll
-            for (int i = 0; i < kBoxes; ++i) {
-                const int pos = key0 + lane + kBox * i;
+            for (int i = 0; i < BN / 32; ++i) {
+                const int pos = key0 + lane + 32 * i;
                 krow[i] = pos <= rt.key_last ? cache_row(bt, a.max_blocks, a.num_blocks, pos, a.dev_err) : -1;
             }
 #pragma unroll
-            for (int i = 0; i < kBoxes; ++i) ksig[i] = krow[i] >= 0 ? __ldg(a.kv_scale + krow[i]) : 1.f;
-            // boxes: whole ones by TMA; one straddling the causal limit by TMA, then its
-            // tail zeroed; ones past the limit (or on a bad page) zeroed. Box g starts
-            // at lane 0's key g.
-            int nval[kBoxes];
-            int64_t brow[kBoxes];
-            uint32_t full_bytes = 0;
+            for (int i = 0; i < BN / 32; ++i) ksig[i] = krow[i] >= 0 ? __ldg(a.kv_scale + krow[i]) : 1.f;
+            const int64_t brow = __shfl_sync(0xffffffffu, krow[0], 0);       // the tile's first key
+            const int nval = brow < 0 ? 0 : max(0, min(BN, rt.key_last - key0 + 1));
+            const uint32_t sdst = sbase_a + st * kStageBytes<false>;
+            auto load = [&](int s, int part) {
+                tma_load_2d(sdst + s * kSliceBytes<false>, &tmap_kv, 128 * s, static_cast<int>(brow),
+                            smem_u32(&sh.bar[B_FULL + part * ST + st]));
+            };
+            auto meta = [&]() {
+                // its ring slot was last read by the softmax of tile t-4, long before
+                KeyMeta &mt = sh.meta[t & 3];
 #pragma unroll
-            for (int g = 0; g < kBoxes; ++g) {
-                nval[g] = max(0, min(kBox, rt.key_last - (key0 + kBox * g) + 1));
-                brow[g] = __shfl_sync(0xffffffffu, krow[g], 0);
-                if (brow[g] < 0) nval[g] = 0;
-                if (nval[g] == kBox) full_bytes += kSlices * kBoxBytes;
-            }
-            if (t >= kStages && !(ok = wait(B_EMPTY + st, ((t / kStages) - 1) & 1))) break;
-            const uint32_t sdst = sbase_a + st * kStageBytes;
-            if (lane == 0) {
-                mbar_add_tx(smem_u32(&sh.bar[B_FULL + st]), full_bytes);
-#pragma unroll
-                for (int g = 0; g < kBoxes; ++g) {
-                    if (nval[g] != kBox) continue;
-#pragma unroll
-                    for (int s = 0; s < kSlices; ++s)
-                        tma_load_2d(sdst + s * kSliceBytes + g * kBoxBytes, &tmap_kv, 128 * s,
-                                    static_cast<int>(brow[g]), smem_u32(&sh.bar[B_FULL + st]));
+                for (int i = 0; i < BN / 32; ++i) {
+                    const int k = lane + 32 * i;
+                    float *sl = reinterpret_cast<float *>(&mt.sl[k >> 1]);
+                    sl[k & 1] = ksig[i];
+                    sl[2 + (k & 1)] = krow[i] >= 0 ? __log2f(ksig[i]) : -INFINITY;
+                    reinterpret_cast<float *>(&mt.isig[k >> 1])[k & 1] = 1.f / ksig[i];
                 }
-            }
-            // metadata (its ring slot was last read by the softmax of tile t-4, which
-            // finished before PV(t-3), the stage release just waited for)
-            KeyMeta &mt = sh.meta[t & 3];
-#pragma unroll
-            for (int i = 0; i < kBoxes; ++i) {
-                const int k = lane + kBox * i;
-                float *sl = reinterpret_cast<float *>(&mt.sl[k >> 1]);
-                sl[k & 1] = ksig[i];
-                sl[2 + (k & 1)] = krow[i] >= 0 ? __log2f(ksig[i]) : -INFINITY;
-                reinterpret_cast<float *>(&mt.isig[k >> 1])[k & 1] = 1.f / ksig[i];
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_META + (t & 3)]));
-            bool zeroed = false;
-#pragma unroll 1
-            for (int g = 0; g < kBoxes; ++g) {
-                if (nval[g] == kBox) continue;
-                if (nval[g] > 0) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_META + (t & 3)]));
+            };
+            if (nval == BN) {
+                if (!(ok = wait_empty(0, t))) break;
+                if (lane == 0) {
+                    mbar_expect_tx(smem_u32(&sh.bar[B_FULL + 0 * ST + st]), kSliceBytes<false>);
+                    load(4, 0);
+                }
+                meta();
+                if (!(ok = wait_empty(1, t))) break;
+                if (lane == 0) {
+                    mbar_expect_tx(smem_u32(&sh.bar[B_FULL + 1 * ST + st]), 2 * kSliceBytes<false>);
+                    load(0, 1);
+                    load(1, 1);
+                }
+                if (!(ok = wait_empty(2, t))) break;
+                if (lane == 0) {
+                    mbar_expect_tx(smem_u32(&sh.bar[B_FULL + 2 * ST + st]), 2 * kSliceBytes<false>);
+                    load(2, 2);
+                    load(3, 2);
+                }
+            } else {
+                if (!(ok = wait_empty(0, t) && wait_empty(1, t) && wait_empty(2, t))) break;
+                meta();
+                if (nval > 0) {
                     if (lane == 0) {
-                        mbar_expect_tx(smem_u32(&sh.bar[B_FIX]), kSlices * kBoxBytes);
+                        mbar_expect_tx(smem_u32(&sh.bar[B_FIX]), kSlices * kSliceBytes<false>);
                         for (int s = 0; s < kSlices; ++s)
-                            tma_load_2d(sdst + s * kSliceBytes + g * kBoxBytes, &tmap_kv, 128 * s,
-                                        static_cast<int>(brow[g]), smem_u32(&sh.bar[B_FIX]));
+                            tma_load_2d(sdst + s * kSliceBytes<false>, &tmap_kv, 128 * s, static_cast<int>(brow),
+                                        smem_u32(&sh.bar[B_FIX]));
                     }
                     if (!(ok = wait(B_FIX, fix_phase))) break;
                     fix_phase ^= 1;
                 }
-                // rows nval..31 of the box, every slice (a row is 128 contiguous bytes)
+                // rows nval..BN-1 of every slice (a row is 128 contiguous bytes)
                 for (int s = 0; s < kSlices; ++s) {
-                    uint8_t *box = sbase + st * kStageBytes + s * kSliceBytes + g * kBoxBytes;
-                    for (int o = nval[g] * 128 + 16 * lane; o < kBoxBytes; o += 512)
-                        *reinterpret_cast<uint4 *>(box + o) = make_uint4(0, 0, 0, 0);
+                    uint8_t *sl = sbase + st * kStageBytes<false> + s * kSliceBytes<false>;
+                    for (int o = nval * 128 + 16 * lane; o < kSliceBytes<false>; o += 512)
+                        *reinterpret_cast<uint4 *>(sl + o) = make_uint4(0, 0, 0, 0);
                 }
-                zeroed = true;
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0)
+                    for (int part = 0; part < 3; ++part) mbar_arrive(smem_u32(&sh.bar[B_FULL + part * ST + st]));
             }
-            if (!ok) break;
-            if (zeroed) fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL + st]));
         }
     } else if (kSparse && warp >= kSmWarps<kSparse> && warp != kIssuerWarp<kSparse>) {
         // =================== row gathers (sparse): pair p takes tiles p, p+2, ... ===================
         // Key k's 576 bytes go by 16-byte cp.async into the swizzled slices, eight
         // lanes per row (one 128-byte slice row per instruction and row), four rows
         // per warp instruction; a key that is padding (-1) or invalid is zeroed.
+        constexpr int BN = kBN<true>, ST = kStages<true>, kBoxes = BN / kGroupRows;
+        constexpr int kSliceB = kSliceBytes<true>, kStageB = kStageBytes<true>;
         const int gk = lane >> 3, gc = lane & 7;
         const int half = gather_half(warp);
         bool ok = true;
         for (int t = gather_pair(warp); t < walk.total && ok; t += 2) {
-            const int st = t % kStages;
+            const int st = t % ST;
             const RowTile rt = tile_of(walk.r(t));
             const int32_t *bt = a.block_table + static_cast<int64_t>(rt.b) * a.max_blocks;
             const int key0 = walk.j(t) * BN;
@@ -532,7 +546,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
             }
 #pragma unroll
             for (int i = 0; i < kBoxes; ++i) ksig[i] = krow[i] >= 0 ? __ldg(a.kv_scale + krow[i]) : 1.f;
-            if (t >= kStages && !(ok = wait(B_EMPTY + st, ((t / kStages) - 1) & 1))) break;
+            if (t >= ST && !(ok = wait(B_EMPTY + st, ((t / ST) - 1) & 1))) break;
             if (half == 0) {
                 KeyMeta &mt = sh.meta[t & 3];
 #pragma unroll
@@ -546,7 +560,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_META + (t & 3)]));
             }
-            const uint32_t sst = sbase_a + st * kStageBytes;
+            const uint32_t sst = sbase_a + st * kStageB;
 #pragma unroll 4
             for (int g = half * (BN / 8); g < (half + 1) * (BN / 8); ++g) {
                 const int k = 4 * g + gk, kb = (4 * g) >> 5;     // kb: the same for the four rows
@@ -556,9 +570,9 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
 #pragma unroll
                 for (int s = 0; s < kSlices; ++s) {
                     if (s == kSlices - 1 && gc >= 4) break;      // the RoPE slice holds 64 bytes
-                    const uint32_t off = s * kSliceBytes + swz(k, gc);
+                    const uint32_t off = s * kSliceB + swz(k, gc);
                     if (row >= 0) cp_async16(sst + off, src + 128 * s);
-                    else *reinterpret_cast<uint4 *>(sbase + st * kStageBytes + off) = make_uint4(0, 0, 0, 0);
+                    else *reinterpret_cast<uint4 *>(sbase + st * kStageB + off) = make_uint4(0, 0, 0, 0);
                 }
             }
             cp_async_wait_all();
@@ -573,50 +587,67 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
         // becomes the bottleneck of M=64 MMAs.
         if (lane == 0) {
             const uint32_t lead = 1u;
+            constexpr int BN = kBN<kSparse>, ST = kStages<kSparse>, SB = kSBufs<kSparse>;
             const uint32_t id_qk = idesc_e4m3(BM, BN, false, false);
             const uint32_t id_pv = idesc_e4m3(BM, 256, false, true);
             const uint64_t dk0 = sdesc(sbase_a, 16, 1024, kSw128);              // K-major key slices
-            const uint64_t dv0 = sdesc(sbase_a, kSliceBytes, 1024, kSw128);     // MN-major value chunks
-            const uint64_t dp0 = sdesc(sbase_a + kOffP, 128, 768, kSwNone);     // P terms
+            const uint64_t dv0 = sdesc(sbase_a, kSliceBytes<kSparse>, 1024, kSw128);   // MN-major value chunks
+            const uint64_t dp0 = sdesc(sbase_a + kOffP<kSparse>, 128, kPSbo<kSparse>, kSwNone);   // P terms
             bool ok = true;
+            // QK(t): the RoPE slice first (dense: released right after), then value slices
+            // 0-3; dense waits for each part as it lands
             auto qk = [&](int t) -> bool {
-                const int sb = t & 1, st = t % kStages;
-                if (!wait(B_FULL + st, (t / kStages) & 1)) return false;
-                if (t >= 2 && !wait(B_S_FREE + sb, ((t >> 1) - 1) & 1)) return false;
-                fence_after_sync();
+                const int sb = t % SB, st = t % ST, ph = (t / ST) & 1;
+                if (t >= SB && !wait(B_S_FREE + sb, ((t / SB) - 1) & 1)) return false;
                 const uint32_t d = tmem + kColS + BN * sb;
-#pragma unroll 1
-                for (int s = 0; s < kSlices; ++s) {
-                    const uint64_t db = dk0 + static_cast<uint64_t>((st * kStageBytes + s * kSliceBytes) >> 4);
+                auto slice = [&](int s, uint32_t acc0) {
+                    const uint64_t db = dk0 + static_cast<uint64_t>((st * kStageBytes<kSparse> + s * kSliceBytes<kSparse>) >> 4);
                     const int nks = s < 4 ? 4 : 2;   // the RoPE slice holds 64 dims
 #pragma unroll 4
                     for (int ks = 0; ks < nks; ++ks) {
-                        const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
-                        mma_e4m3_ts_w(d, tmem + kColQh + 32 * s + 8 * ks, db + 2 * ks, id_qk, acc, lead);
+                        mma_e4m3_ts_w(d, tmem + kColQh + 32 * s + 8 * ks, db + 2 * ks, id_qk, (acc0 || ks > 0) ? 1u : 0u, lead);
                         mma_e4m3_ts_w(d, tmem + kColQl + 32 * s + 8 * ks, db + 2 * ks, id_qk, 1u, lead);
                     }
+                };
+                if (!wait(B_FULL + 0 * ST + st, ph)) return false;
+                fence_after_sync();
+                slice(4, 0u);
+                if (kParts<kSparse> == 3) {
+                    mma_commit_w(smem_u32(&sh.bar[B_EMPTY + 0 * ST + st]), lead);   // RoPE slice free
+                    if (!wait(B_FULL + 1 * ST + st, ph)) return false;
+                    fence_after_sync();
                 }
+                slice(0, 1u);
+                slice(1, 1u);
+                if (kParts<kSparse> == 3) {
+                    if (!wait(B_FULL + 2 * ST + st, ph)) return false;
+                    fence_after_sync();
+                }
+                slice(2, 1u);
+                slice(3, 1u);
                 mma_commit_w(smem_u32(&sh.bar[B_S_FULL + sb]), lead);
                 return true;
             };
             auto pv = [&](int t) -> bool {
-                const int pb = t & 1, st = t % kStages, j = walk.j(t), r = walk.r(t);
+                const int pb = t & 1, st = t % ST, j = walk.j(t), r = walk.r(t);
                 if (j == 0 && r > 0 && !wait(B_O_FREE, (r - 1) & 1)) return false;
                 if (!wait(B_P_FULL + pb, (t >> 1) & 1)) return false;
                 fence_after_sync();
-                const uint64_t dph = dp0 + static_cast<uint64_t>(((2 * pb) * kPBytes) >> 4);
-                const uint64_t dpl = dp0 + static_cast<uint64_t>(((2 * pb + 1) * kPBytes) >> 4);
+                const uint64_t dph = dp0 + static_cast<uint64_t>(((2 * pb) * kPBytes<kSparse>) >> 4);
+                const uint64_t dpl = dp0 + static_cast<uint64_t>(((2 * pb + 1) * kPBytes<kSparse>) >> 4);
 #pragma unroll 1
                 for (int c = 0; c < 2; ++c) {
-                    const uint64_t dv = dv0 + static_cast<uint64_t>((st * kStageBytes + 2 * c * kSliceBytes) >> 4);
+                    const uint64_t dv = dv0 + static_cast<uint64_t>((st * kStageBytes<kSparse> + 2 * c * kSliceBytes<kSparse>) >> 4);
                     const uint32_t d = tmem + kHalf1 + 256u * c;
 #pragma unroll
                     for (int ks = 0; ks < BN / 32; ++ks) {
                         mma_e4m3_ss_w(d, dph + 16 * ks, dv + 256 * ks, id_pv, (j > 0 || ks > 0) ? 1u : 0u, lead);
                         mma_e4m3_ss_w(d, dpl + 16 * ks, dv + 256 * ks, id_pv, 1u, lead);
                     }
+                    if (kParts<kSparse> == 3)   // value slices 2c, 2c+1 free
+                        mma_commit_w(smem_u32(&sh.bar[B_EMPTY + (1 + c) * ST + st]), lead);
                 }
-                mma_commit_w(smem_u32(&sh.bar[B_EMPTY + st]), lead);
+                if (kParts<kSparse> == 1) mma_commit_w(smem_u32(&sh.bar[B_EMPTY + st]), lead);
                 mma_commit_w(smem_u32(&sh.bar[B_PV_DONE + pb]), lead);
                 return true;
             };
@@ -640,6 +671,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
         // warps per quadrant they trade tile maxima (and, at the end, row sums) in smem
         constexpr int kKeys = kSmKeys<kSparse>;
         constexpr bool kPair = kSmWarps<kSparse> == 8;
+        constexpr int BN = kBN<kSparse>, SB = kSBufs<kSparse>;
         constexpr int kGroups = 18 * kKeys / BN;         // Q column groups per warp
         constexpr int kOCols = 512 * kKeys / BN;         // O columns per warp
         const int q = warp & 3, kh = warp >> 2;
@@ -655,11 +687,11 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
         const int ra = 16 * q + tq, rb = ra + 8;
         const uint32_t lane_lo = static_cast<uint32_t>(32 * q) << 16;
         const uint32_t lane_hi = lane_lo + kHalf1;
-        // P word (own row, keys 8i + 4(tc/2) .. +3) at (row/8)*768 + (i/2)*128 + (row%8)*16 + 8(i&1) + 4(tc/2)
+        // P word (own row, keys 8i + 4(tc/2) .. +3) at (row/8)*SBO + (i/2)*128 + (row%8)*16 + 8(i&1) + 4(tc/2)
         const bool even = (tc & 1) == 0;
         const int prow = even ? ra : rb;
-        const uint32_t poff = static_cast<uint32_t>((prow >> 3) * 768 + (prow & 7) * 16 + 4 * (tc >> 1));
-        uint8_t *pbase = sbase + kOffP;
+        const uint32_t poff = static_cast<uint32_t>((prow >> 3) * kPSbo<kSparse> + (prow & 7) * 16 + 4 * (tc >> 1));
+        uint8_t *pbase = sbase + kOffP<kSparse>;
         bool ok = true;
         RowTile rt = tile_of(0);
         float rs_a, rs_b;
@@ -675,14 +707,13 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
             const int lim_a = row_limit<kSparse>(a, rt, ra), lim_b = row_limit<kSparse>(a, rt, rb);
             const int lim_min = min(lim_a, lim_b);
             for (int j = 0; j < rt.n_ktiles && ok; ++j, ++t) {
-                const int sb = t & 1;
+                const int sb = t % SB, pbf = t & 1;     // S buffer, P buffer
                 if (!(ok = wait(B_META + (t & 3), (t >> 2) & 1))) break;
-                if (!(ok = wait(B_S_FULL + sb, (t >> 1) & 1))) break;
+                if (!(ok = wait(B_S_FULL + sb, (t / SB) & 1))) break;
                 fence_after_sync();
                 uint32_t sv[kKeys / 2];
-                if constexpr (kKeys == 48) {
-                    tmem_ld_16x256b_x4(tmem + lane_lo + kColS + BN * sb + kKeys * kh, sv);
-                    tmem_ld_16x256b_x2(tmem + lane_lo + kColS + BN * sb + kKeys * kh + 32, sv + 16);
+                if constexpr (kKeys == 64) {
+                    tmem_ld_16x256b_x8(tmem + lane_lo + kColS + BN * sb + kKeys * kh, sv);
                 } else {
                     tmem_ld_16x256b_x8(tmem + lane_lo + kColS + BN * sb, sv);
                     tmem_ld_16x256b_x4(tmem + lane_lo + kColS + BN * sb + 64, sv + 32);
@@ -817,8 +848,8 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                     tmem_st_wait();
                 }
                 // ---- P terms into buffer t&1 (last read by PV(t-2)) ----
-                if (t >= 2 && !(ok = wait(B_PV_DONE + sb, ((t >> 1) - 1) & 1))) break;
-                uint8_t *ph = pbase + (2 * sb) * kPBytes, *pl = ph + kPBytes;
+                if (t >= 2 && !(ok = wait(B_PV_DONE + pbf, ((t >> 1) - 1) & 1))) break;
+                uint8_t *ph = pbase + (2 * pbf) * kPBytes<kSparse>, *pl = ph + kPBytes<kSparse>;
 #pragma unroll
                 for (int i = 0; i < kKeys / 8; ++i) {
                     // the even lane of a pair writes row a's word, the odd lane row b's
@@ -835,7 +866,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                 fence_proxy_async();
                 fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_P_FULL + sb]));
+                if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_P_FULL + pbf]));
             }
             if (!ok) break;
             const RowTile rt_done = rt;
@@ -910,21 +941,21 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
 cudaError_t launch_dense_f8(const AttnArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_kv,
                             cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(f8attn::attn_f8_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         f8attn::kDynSmem);
+                                         f8attn::kDynSmem<false>);
     if (e != cudaSuccess) return e;
     if (n_work > 0)
-        f8attn::attn_f8_kernel<false><<<n_work, f8attn::kThreads<false>, f8attn::kDynSmem, st>>>(a, work, tmap_kv);
+        f8attn::attn_f8_kernel<false><<<n_work, f8attn::kThreads<false>, f8attn::kDynSmem<false>, st>>>(a, work, tmap_kv);
     return cudaGetLastError();
 }
 
 cudaError_t launch_sparse_f8(const AttnArgs &a, int64_t n_tokens, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(f8attn::attn_f8_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         f8attn::kDynSmem);
+                                         f8attn::kDynSmem<true>);
     if (e != cudaSuccess) return e;
     const CUtensorMap unused{};   // the gather path reads rows with cp.async
     const dim3 grid(static_cast<unsigned>((n_tokens + 1) / 2), (a.H + f8attn::BM - 1) / f8attn::BM);
     if (n_tokens > 0)
-        f8attn::attn_f8_kernel<true><<<grid, f8attn::kThreads<true>, f8attn::kDynSmem, st>>>(a, nullptr, unused);
+        f8attn::attn_f8_kernel<true><<<grid, f8attn::kThreads<true>, f8attn::kDynSmem<true>, st>>>(a, nullptr, unused);
     return cudaGetLastError();
 }
 

@@ -46,7 +46,7 @@ struct IndexerArgs {
 
 // Dense attention on e4m3 operands (kind::f8f6f4). Work item: x = sequence,
 // y = 64-row tile, z = paired row tile or -1. tmap_kv: the latent cache as
-// [num_blocks * 256 rows][576 B], 128 x 32 boxes, 128-byte swizzle (encode_kv_tmap).
+// [num_blocks * 256 rows][576 B], 128 x 128 boxes, 128-byte swizzle (encode_kv_tmap).
 cudaError_t launch_dense_f8(const AttnArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_kv, cudaStream_t st);
 bool encode_kv_tmap(CUtensorMap *map, const uint8_t *kv, int32_t num_blocks);
 // Sparse attention on e4m3 operands: rows gathered by index (cp.async), two

@@ -323,8 +323,9 @@ mla_status_t mla_prefill_sparse(const mla_seqs_t *seqs, const void *q_bf16, int3
 // Helpers shared with the allocation-free dense entry point (dense_noalloc.cu).
 namespace mla {
 bool encode_kv_tmap(CUtensorMap *map, const uint8_t *kv, int32_t num_blocks) {
-    // rows of 576 e4m3 codes (512 latent + 64 RoPE); 32-row boxes never straddle a 256-row page
-    return num_blocks > 0 && encode_u8_rows(map, kv, 576, static_cast<uint64_t>(num_blocks) * 256, 32);
+    // rows of 576 e4m3 codes (512 latent + 64 RoPE); 128-row boxes (a dense key tile)
+    // start at multiples of 128 and never straddle a 256-row page
+    return num_blocks > 0 && encode_u8_rows(map, kv, 576, static_cast<uint64_t>(num_blocks) * 256, 128);
 }
 mla_status_t check_dense_args(const mla_seqs_t *seqs, const void *q, int32_t H, const uint8_t *kv,
                               const float *kv_scale, const void *out, const float *lse, float sm_scale) {
