@@ -509,7 +509,7 @@ def main():
                 "peak_source": f"{src} bf16 sustained; the kernel runs each algorithmic FLOP as two e4m3 tensor "
                                f"FLOPs at twice the bf16 rate, so this equals the e4m3 roof",
                 "kernel": "attn_f8_kernel: tcgen05 kind::f8f6f4, e4m3 cache tiles by TMA, two-term e4m3 Q and P, "
-                          "64 rows x 96 keys"}
+                          "64 rows x 128 keys"}
     elif getattr(run, "split_ms", None):
         idx_ms, att_ms = statistics.mean(run.split_ms[0]), statistics.mean(run.split_ms[1])
         idx_tf = run.indexer_flops / (idx_ms / 1000.0) / 1e12
