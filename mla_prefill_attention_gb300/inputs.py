@@ -47,7 +47,7 @@ D_IDX = 128         # indexer head dim
 H_IDX = 64          # indexer heads
 
 # tensor ids of the counter-based streams
-T_Q, T_KV, T_QIDX, T_KIDX, T_WIDX, T_PERM, T_MISC = 1, 2, 3, 4, 5, 6, 7
+T_Q, T_KV, T_QIDX, T_KIDX, T_WIDX, T_PERM, T_MISC, T_NEWKV, T_NEWKIDX, T_GAIN = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "inputs_gen.c")
@@ -262,6 +262,16 @@ def gen_indexer_inputs(seed: int, seqs: PagedSeqs, token_rows=None):
     q = gen_indexer_q(seed, seqs.total_q, token_rows)
     k, ks = gen_indexer_keys(seed, seqs)
     return q, gen_indexer_w(seed), k, ks
+
+
+def gen_new_rows_bf16(seed: int, total_q: int, dim: int, tensor: int = T_NEWKV) -> np.ndarray:
+    """bf16 bits [total_q, dim] of the new tokens' unquantised cache rows (the
+    latent row with dim 576 under T_NEWKV, the indexer key with dim 128 under
+    T_NEWKIDX): N(0,1) draws times a per-token gain 2^g, g uniform in [-4, 4),
+    so that the per-token scales spread over eight octaves. Row stream = token."""
+    toks = np.arange(total_q, dtype=np.int64)
+    gain = np.exp2(uniform_rows(seed, T_GAIN * 16 + tensor, toks, 1)[:, 0] * 8.0 - 4.0)
+    return bf16_bits(normal_rows(seed, tensor, toks, dim) * gain[:, None])
 
 
 # ----------------------------------------------------------------------------

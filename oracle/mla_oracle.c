@@ -28,6 +28,9 @@
  *  - Indexer: score(t,s) = sigmaI_s * sum_h w_{t,h} * max(0, q_{t,h} . k_s),
  *    s <= p; the selected set is the first min(topk, p+1) positions in the
  *    order (score descending, position ascending).
+ *  - Cache write (the step before attention): per token and row, scale =
+ *    absmax / 448 (1 for a zero row), codes = nearest e4m3 of x / scale, ties
+ *    to even, clamped at 448; both divisions in IEEE binary32.
  */
 #include <math.h>
 #include <stdint.h>
@@ -281,6 +284,80 @@ int ora_indexer_topk(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *
         for (int64_t j = 0; j < keep; ++j) dst[j] = (int32_t)c[j].pos;
         qsort(dst, (size_t)keep, sizeof(int32_t), cmp_i32);
         free(c);
+    }
+    return fails ? (int)-fails : 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Cache write of the new tokens (the step before attention).
+ *
+ * Sources: "More throughput from fewer GPUs", section System architecture
+ * (the KV cache is FP8, one latent row per token) and section KV hand-off and
+ * caching (256-token chunks); GLM-5.3 Teil 2, footnote 3 (indexer keys: 128
+ * FP8 values plus a 4-byte scale). The pages name the format but not the
+ * quantiser. Readings: one fp32 scale per token and row, equal to the row's
+ * absolute maximum divided by 448 (the largest e4m3 value), 1 for an all-zero
+ * row; each code is the e4m3 value nearest to x / scale, ties to the even
+ * code, magnitudes above 448 clamped to 448. Both divisions are IEEE binary32
+ * operations (the precision the quantised code is decided in); the rounding
+ * to e4m3 is then exact.
+ * ------------------------------------------------------------------------ */
+
+/* The e4m3 code nearest to v: by definition, the finite code whose value is
+ * closest to |v| (codes 0..126 hold increasing magnitudes 0..448; 127 is
+ * NaN), the even code on a tie, 448 above the range; the sign bit is v's. */
+uint8_t ora_e4m3_nearest(float v) {
+    ora_init();
+    double a = fabs((double)v);
+    unsigned lo = 0, hi = 126;
+    if (a >= e4m3_table[126]) return (uint8_t)((signbit(v) ? 0x80u : 0u) | 126u);
+    /* largest code lo with table[lo] <= a (table[0] = 0 <= a < table[126]) */
+    while (hi - lo > 1) {
+        unsigned mid = (lo + hi) / 2;
+        if (e4m3_table[mid] <= a) lo = mid; else hi = mid;
+    }
+    double dlo = a - e4m3_table[lo], dhi = e4m3_table[lo + 1] - a;
+    unsigned c = dlo < dhi ? lo : dhi < dlo ? lo + 1 : ((lo & 1u) ? lo + 1 : lo);
+    return (uint8_t)((signbit(v) ? 0x80u : 0u) | c);
+}
+
+/* One row of n bf16 values -> n e4m3 codes and its scale (see above). */
+void ora_quantize_row(const uint16_t *x, int64_t n, uint8_t *codes, float *scale_out) {
+    double amax = 0.0;
+    for (int64_t d = 0; d < n; ++d) {
+        double a = fabs(ora_bf16(x[d]));
+        if (a > amax) amax = a;
+    }
+    /* amax is a bf16 value, so (float)amax is exact */
+    float scale = amax > 0.0 ? (float)amax / 448.0f : 1.0f;
+    for (int64_t d = 0; d < n; ++d) {
+        float v = (float)ora_bf16(x[d]) / scale;
+        codes[d] = ora_e4m3_nearest(v);
+    }
+    *scale_out = scale;
+}
+
+/* New token t (global index into the batch's new tokens) of sequence b sits
+ * at position prefix_lens[b] + (t - cu_seqlens_q[b]); its latent row
+ * (576 bf16) and indexer key (128 bf16, optional) are quantised and stored at
+ * that position's page and slot. Returns 0, or -(number of tokens whose
+ * position has no valid page); those tokens write nothing. */
+int ora_kv_append(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *prefix_lens,
+                  const int32_t *block_table, int32_t max_blocks, int32_t num_blocks,
+                  const uint16_t *latent, const uint16_t *kidx,
+                  uint8_t *kv, float *kv_scale, uint8_t *ki, float *ki_scale) {
+    int64_t n_tok = cu_seqlens_q[batch];
+    int64_t fails = 0;
+    for (int64_t t = 0; t < n_tok; ++t) {
+        int64_t i;
+        int b = locate(batch, cu_seqlens_q, t, &i);
+        int64_t r = b < 0 ? -1 : cache_row(block_table, max_blocks, num_blocks, b, prefix_lens[b] + i);
+        if (r < 0) {
+            ++fails;
+            continue;
+        }
+        ora_quantize_row(latent + t * ORA_DQK, ORA_DQK, kv + r * ORA_DQK, kv_scale + r);
+        if (kidx) ora_quantize_row(kidx + t * ORA_DIDX, ORA_DIDX, ki + r * ORA_DIDX, ki_scale + r);
     }
     return fails ? (int)-fails : 0;
 }

@@ -45,6 +45,12 @@ def lib():
         L.ora_mla_sparse.argtypes = seq + [vp, vp, i64, i32, vp, vp, dbl, vp, i32, vp, vp]
         L.ora_indexer_topk.restype = ctypes.c_int
         L.ora_indexer_topk.argtypes = seq + [vp, vp, i64, vp, i64, vp, vp, i32, vp, vp, i64]
+        L.ora_e4m3_nearest.restype = ctypes.c_uint8
+        L.ora_e4m3_nearest.argtypes = [ctypes.c_float]
+        L.ora_quantize_row.restype = None
+        L.ora_quantize_row.argtypes = [vp, i64, vp, vp]
+        L.ora_kv_append.restype = ctypes.c_int
+        L.ora_kv_append.argtypes = seq + [vp, vp, vp, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -138,3 +144,41 @@ def indexer_topk(seqs, qi, w, w_stride, tokens, ki, ki_scale, topk, want_scores=
     if rc != 0:
         raise ValueError(f"oracle indexer: {-rc} rows failed")
     return (idx, sc) if want_scores else idx
+
+
+def e4m3_nearest(v) -> np.ndarray:
+    """Nearest e4m3 codes (ties to even, clamped at 448) of float32 values."""
+    x = np.ascontiguousarray(v, dtype=np.float32)
+    f = lib().ora_e4m3_nearest
+    return np.array([f(float(a)) for a in x.ravel()], dtype=np.uint8).reshape(x.shape)
+
+
+def quantize_row(x_bf16):
+    """Per-row absmax/448 quantisation of bf16 bits [n] -> (codes u8 [n], scale f32)."""
+    x = _c(x_bf16, np.uint16)
+    codes = np.empty(x.shape, dtype=np.uint8)
+    sc = ctypes.c_float()
+    lib().ora_quantize_row(_p(x), x.size, _p(codes), ctypes.byref(sc))
+    return codes, np.float32(sc.value)
+
+
+def kv_append(seqs, latent, kidx, kv, kv_scale, ki=None, ki_scale=None):
+    """Write the new tokens' quantised rows into copies of the caches.
+    latent: bf16 bits [Tq, 576]; kidx: bf16 bits [Tq, 128] or None.
+    Returns (kv, kv_scale, ki, ki_scale) (the last two None without kidx)."""
+    lat = _c(latent, np.uint16)
+    if lat.ndim != 2 or lat.shape[1] != 576 or lat.shape[0] != int(seqs.cu_seqlens_q[-1]):
+        raise ValueError("latent must be [Tq, 576]")
+    kvc, kvs = np.array(kv, dtype=np.uint8, order="C"), np.array(kv_scale, dtype=np.float32, order="C")
+    kic = kis = kx = None
+    if kidx is not None:
+        kx = _c(kidx, np.uint16)
+        if kx.shape != (lat.shape[0], 128):
+            raise ValueError("kidx must be [Tq, 128]")
+        kic, kis = np.array(ki, dtype=np.uint8, order="C"), np.array(ki_scale, dtype=np.float32, order="C")
+    keep, sa = _seq_args(seqs)
+    rc = lib().ora_kv_append(*sa, _p(lat), _p(kx) if kx is not None else None, _p(kvc), _p(kvs),
+                             _p(kic) if kic is not None else None, _p(kis) if kis is not None else None)
+    if rc != 0:
+        raise ValueError(f"oracle kv append: {-rc} tokens have no valid page")
+    return kvc, kvs, kic, kis
