@@ -29,9 +29,11 @@
  *    s <= p; the selected set is the first min(topk, p+1) positions in the
  *    order (score descending, position ascending).
  *  - Cache write (the step before attention): per token and row, scale =
- *    absmax / 448 (1 for a zero row), codes = nearest e4m3 of x / scale, ties
- *    to even, clamped at 448; both divisions in IEEE binary32.
+ *    absmax / 448 (1 for a zero row, at least 2^-126 otherwise), codes =
+ *    nearest e4m3 of x times the reciprocal of the scale, ties to even,
+ *    clamped at 448; every step in IEEE binary32.
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -297,10 +299,12 @@ int ora_indexer_topk(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *
  * FP8 values plus a 4-byte scale). The pages name the format but not the
  * quantiser. Readings: one fp32 scale per token and row, equal to the row's
  * absolute maximum divided by 448 (the largest e4m3 value), 1 for an all-zero
- * row; each code is the e4m3 value nearest to x / scale, ties to the even
- * code, magnitudes above 448 clamped to 448. Both divisions are IEEE binary32
- * operations (the precision the quantised code is decided in); the rounding
- * to e4m3 is then exact.
+ * row, and never below 2^-126 (the smallest normal binary32 value, so that its
+ * reciprocal is finite); each element is multiplied by the reciprocal of the
+ * scale and the code is the e4m3 value nearest to that product, ties to the
+ * even code, magnitudes above 448 clamped to 448. The division, reciprocal
+ * and product are IEEE binary32 operations (the precision the quantised code
+ * is decided in); the rounding to e4m3 is then exact.
  * ------------------------------------------------------------------------ */
 
 /* The e4m3 code nearest to v: by definition, the finite code whose value is
@@ -330,8 +334,10 @@ void ora_quantize_row(const uint16_t *x, int64_t n, uint8_t *codes, float *scale
     }
     /* amax is a bf16 value, so (float)amax is exact */
     float scale = amax > 0.0 ? (float)amax / 448.0f : 1.0f;
+    if (scale < FLT_MIN) scale = FLT_MIN;
+    float inv = 1.0f / scale;
     for (int64_t d = 0; d < n; ++d) {
-        float v = (float)ora_bf16(x[d]) / scale;
+        float v = (float)ora_bf16(x[d]) * inv;
         codes[d] = ora_e4m3_nearest(v);
     }
     *scale_out = scale;
