@@ -28,6 +28,8 @@
  *  - Indexer: score(t,s) = sigmaI_s * sum_h w_{t,h} * max(0, q_{t,h} . k_s),
  *    s <= p; the selected set is the first min(topk, p+1) positions in the
  *    order (score descending, position ascending).
+ *  - Merge of partial results (DCP section of GLM-5.3 Teil 2): out and lse of
+ *    attention over a union of disjoint key sets from each set's out and lse.
  *  - Cache write (the step before attention): per token and row, scale =
  *    absmax / 448 (1 for a zero row, at least 2^-126 otherwise), codes =
  *    nearest e4m3 of x times the reciprocal of the scale, ties to even,
@@ -366,4 +368,39 @@ int ora_kv_append(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *pre
         if (kidx) ora_quantize_row(kidx + t * ORA_DIDX, ORA_DIDX, ki + r * ORA_DIDX, ki_scale + r);
     }
     return fails ? (int)-fails : 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Merge of partial attention results over disjoint key sets.
+ *
+ * Source: GLM-5.3 Teil 2, section "DCP: Sharding auch des KV-Caches": when
+ * the cache is split by token across GPUs, each runs attention over its own
+ * shard and the partial results are combined through their log-sum-exp.
+ * Written out: for parts i with outputs o_i (softmax-weighted means over their
+ * keys) and lse_i = ln(sum of exp(logit) over their keys),
+ *   lse = ln sum_i exp(lse_i),   out = sum_i exp(lse_i - lse) * o_i,
+ * which is attention over the union of the key sets. A part with lse_i = -inf
+ * (no keys) contributes nothing; with every part empty, out = 0, lse = -inf.
+ * ------------------------------------------------------------------------ */
+void ora_merge(int32_t n_parts, const double *outs, const double *lses, int64_t rows, int64_t dv,
+               double *out, double *lse) {
+    for (int64_t r = 0; r < rows; ++r) {
+        double m = -INFINITY;
+        for (int i = 0; i < n_parts; ++i)
+            if (lses[(int64_t)i * rows + r] > m) m = lses[(int64_t)i * rows + r];
+        double *o = out + r * dv;
+        for (int64_t d = 0; d < dv; ++d) o[d] = 0.0;
+        if (m == -INFINITY) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double total = 0.0;
+        for (int i = 0; i < n_parts; ++i) total += exp(lses[(int64_t)i * rows + r] - m);
+        for (int i = 0; i < n_parts; ++i) {
+            double wgt = exp(lses[(int64_t)i * rows + r] - m) / total;
+            const double *oi = outs + ((int64_t)i * rows + r) * dv;
+            for (int64_t d = 0; d < dv; ++d) o[d] += wgt * oi[d];
+        }
+        lse[r] = m + log(total);
+    }
 }

@@ -51,6 +51,8 @@ def lib():
         L.ora_quantize_row.argtypes = [vp, i64, vp, vp]
         L.ora_kv_append.restype = ctypes.c_int
         L.ora_kv_append.argtypes = seq + [vp, vp, vp, vp, vp, vp]
+        L.ora_merge.restype = None
+        L.ora_merge.argtypes = [i32, vp, vp, i64, i64, vp, vp]
         _lib = L
     return _lib
 
@@ -182,3 +184,19 @@ def kv_append(seqs, latent, kidx, kv, kv_scale, ki=None, ki_scale=None):
     if rc != 0:
         raise ValueError(f"oracle kv append: {-rc} tokens have no valid page")
     return kvc, kvs, kic, kis
+
+
+def merge(outs, lses):
+    """Merge partial results over disjoint key sets: outs [n, rows, dv] (fp64, or
+    bf16 bits as uint16), lses [n, rows] (natural log, -inf = empty part).
+    Returns (out [rows, dv], lse [rows]) in fp64."""
+    o = np.asarray(outs)
+    od = bf16_to_f64(o) if o.dtype == np.uint16 else _c(o, np.float64)
+    ls = _c(lses, np.float64)
+    n, rows, dv = od.shape
+    if ls.shape != (n, rows):
+        raise ValueError("lses must be [n_parts, rows]")
+    out = np.empty((rows, dv), dtype=np.float64)
+    lse = np.empty(rows, dtype=np.float64)
+    lib().ora_merge(n, _p(od), _p(ls), rows, dv, _p(out), _p(lse))
+    return out, lse
