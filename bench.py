@@ -405,6 +405,98 @@ def time_steps(run, steps, warmup):
     return total_ms, per_ms
 
 
+KV_APPEND_BYTES_PER_TOKEN = 2 * 576 + 2 * 128 + 576 + 4 + 128 + 4   # bf16 rows in, e4m3 rows + fp32 scales out
+
+
+def measure_kv_append(w, dev, reps=20):
+    """The cache write of the workload's new tokens (latent row and indexer key),
+    timed alone with CUDA events on the launching stream, L2 flushed before
+    every launch. Rows are drawn for up to 8,192 tokens and repeated."""
+    import torch
+    from mla_prefill_attention_gb300 import Seqs, mla_kv_append
+    from mla_prefill_attention_gb300 import inputs as I
+    ps = w.seqs()
+    T = ps.total_q
+    g = min(T, 8192)
+    lat = torch.from_numpy(I.gen_new_rows_bf16(w.seed, g, 576).view(np.int16)).to(dev).view(torch.bfloat16)
+    kid = torch.from_numpy(I.gen_new_rows_bf16(w.seed, g, 128, I.T_NEWKIDX).view(np.int16)).to(dev)
+    kid = kid.view(torch.bfloat16)
+    reps_rows = -(-T // g)
+    lat = lat.repeat(reps_rows, 1)[:T].contiguous()
+    kid = kid.repeat(reps_rows, 1)[:T].contiguous()
+    nb = ps.num_blocks
+    kv = torch.zeros((nb, 256, 576), dtype=torch.uint8, device=dev)
+    ks = torch.zeros((nb, 256), dtype=torch.float32, device=dev)
+    ki = torch.zeros((nb, 256, 128), dtype=torch.uint8, device=dev)
+    kis = torch.zeros((nb, 256), dtype=torch.float32, device=dev)
+    seqs = Seqs.from_paged(ps, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        mla_kv_append(seqs, lat, kv, ks, kid, ki, kis)
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        mla_kv_append(seqs, lat, kv, ks, kid, ki, kis)
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    pk, src = peaks()
+    gbs = T * KV_APPEND_BYTES_PER_TOKEN / (ms / 1000.0) / 1e9
+    return {"tokens": T, "ms": ms, "tokens_per_s": T / (ms / 1000.0),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(pk["hbm_gbs"]), "unit": "GB/s",
+                         "frac": gbs / float(pk["hbm_gbs"]), "traffic": None,
+                         "bytes_per_token": KV_APPEND_BYTES_PER_TOKEN,
+                         "peak_source": f"{src} hbm_gbs (copy, burst)",
+                         "kernel": "kv_append_kernel: one warp per token, bf16 rows -> e4m3 + fp32 scale, "
+                                   "L2 flushed before each launch"}}
+
+
+MERGE_BYTES_PER_ROW_PART = 512 * 2 + 4    # one part's bf16 row and its lse
+
+
+def measure_merge(w, dev, n_parts=2, reps=20):
+    """The log-sum-exp merge of n_parts partial results of the workload's shape
+    (all new tokens x heads rows of 512), timed alone with CUDA events, L2
+    flushed before every launch."""
+    import torch
+    from mla_prefill_attention_gb300 import mla_merge_attn
+    rows = w.seqs().total_q * w.heads
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    outs = [torch.randn((rows, 512), generator=g, device=dev).to(torch.bfloat16) for _ in range(n_parts)]
+    lses = [torch.rand((rows,), generator=g, device=dev) * 20.0 for _ in range(n_parts)]
+    out = torch.empty_like(outs[0])
+    lse = torch.empty_like(lses[0])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        mla_merge_attn(outs, lses, out=out, lse=lse)
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        mla_merge_attn(outs, lses, out=out, lse=lse)
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    pk, src = peaks()
+    nbytes = rows * MERGE_BYTES_PER_ROW_PART * (n_parts + 1)
+    gbs = nbytes / (ms / 1000.0) / 1e9
+    return {"rows": rows, "parts": n_parts, "ms": ms,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(pk["hbm_gbs"]), "unit": "GB/s",
+                         "frac": gbs / float(pk["hbm_gbs"]), "traffic": None,
+                         "bytes_per_row": MERGE_BYTES_PER_ROW_PART * (n_parts + 1),
+                         "peak_source": f"{src} hbm_gbs (copy, burst)",
+                         "kernel": "merge_kernel: one warp per 512-value row, fp32 weights, bf16 out; "
+                                   "L2 flushed before each launch"}}
+
+
 def config_of(w):
     c = {"workload": w.name, "batch": len(w.q_lens), "q_lens": w.q_lens, "prefix_lens": w.prefix_lens,
          "heads": w.heads, "d_qk": 576, "d_v": 512, "page": 256, "q_dtype": "bf16",
@@ -428,6 +520,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-kv-append", action="store_true", help="skip the separate cache-write measurement")
+    ap.add_argument("--no-merge", action="store_true", help="skip the separate partial-result merge measurement")
     args = ap.parse_args()
 
     from mla_prefill_attention_gb300 import inputs as I
@@ -555,6 +649,10 @@ def main():
             ms, h2d, d2h = r
             line["e2e"] = {"value": world * run.tokens / (ms / 1000.0), "unit": "tok/s", "h2d_bytes_per_step": h2d,
                            "d2h_bytes_per_step": d2h}
+    if rank == 0 and not args.no_kv_append:
+        line["kv_append"] = measure_kv_append(w, dev)
+    if rank == 0 and not args.no_merge:
+        line["lse_merge"] = measure_merge(w, dev)
     if rank == 0 and not args.no_cpu_baseline:
         n, dt, fl = run.oracle_rate(args.cpu_budget)
         val = run.tokens / (dt * run.flops / fl)

@@ -163,6 +163,53 @@ mla_status_t mla_prefill_dense_static(const mla_seqs_t *seqs, const void *q_bf16
                                       const uint8_t *kv_e4m3, const float *kv_scale, float sm_scale,
                                       void *out_bf16, float *lse, int32_t *dev_err, cudaStream_t stream);
 
+/* Cache write of the new tokens: the step before attention, which reads the
+ * rows this call stores ("More throughput from fewer GPUs", section System
+ * architecture: FP8 KV cache, one latent row per token; section KV hand-off
+ * and caching: 256-token chunks; GLM-5.3 Teil 2, footnote 3: indexer keys of
+ * 128 FP8 values plus a 4-byte scale). For new token t of sequence b, at
+ * position p = prefix_lens[b] + t - cu_seqlens_q[b] (page block_table[b][p/256],
+ * slot p%256):
+ *   kv_scale[p] = max(amax / 448, 2^-126), amax = max_d |latent[t,d]| (d < 576);
+ *                 1 if amax = 0
+ *   kv[p][d]    = the e4m3 code nearest to latent[t,d] * (1 / kv_scale[p]),
+ *                 ties to the even code, magnitudes above 448 stored as 448
+ * where the division, the reciprocal and the product are IEEE binary32
+ * operations (the floor keeps the reciprocal finite). With kidx_bf16 set, the
+ * 128-dim indexer key kidx[t] goes the same way into ki[p] / ki_scale[p];
+ * with it NULL, ki and ki_scale are not used. Layouts: latent bf16 [Tq, 576],
+ * kidx bf16 [Tq, 128], caches as in the data layout above. Nothing but the
+ * new tokens' rows is written; two new tokens must not map to one cache row.
+ * Inputs must be finite (a NaN or infinity makes that row unspecified). A page
+ * id outside [0, num_blocks) sets MLA_DEVERR_BAD_PAGE and that token writes
+ * nothing. latent, kidx, kv and ki 16-byte aligned; kv_scale, ki_scale 4-byte
+ * aligned. No workspace. */
+mla_status_t mla_kv_append(const mla_seqs_t *seqs, const void *latent_bf16, const void *kidx_bf16,
+                           uint8_t *kv_e4m3, float *kv_scale, uint8_t *ki_e4m3, float *ki_scale,
+                           int32_t *dev_err, cudaStream_t stream);
+
+/* Most partial results one mla_merge_attn call combines. */
+#define MLA_MERGE_MAX_PARTS 8
+
+/* Merge of partial attention results over disjoint key sets: the
+ * log-sum-exp combination by which attention split over shards of the cache
+ * is put back together (GLM-5.3 Teil 2, section "DCP: Sharding auch des
+ * KV-Caches": each GPU attends over its own shard and the partial results are
+ * combined through their log-sum-exp). Part i holds, per row (one (token,
+ * head) pair), the output o_i of attention over its keys and lse_i, as written
+ * by mla_prefill_dense / mla_prefill_sparse. For each row:
+ *   lse = ln sum_i exp(lse_i),   out = sum_i exp(lse_i - lse) * o_i
+ * which is attention over the union of the parts' keys. A part with lse_i =
+ * -inf (no keys) adds nothing; a row whose parts are all -inf gets out = 0,
+ * lse = -inf. Arithmetic in fp32, out rounded once to bf16.
+ * outs_bf16, lses: HOST arrays of n_parts DEVICE pointers; part i is bf16
+ * [rows, 512] (16-byte aligned) and f32 [rows] (4-byte aligned). out_bf16:
+ * bf16 [rows, 512], 16-byte aligned; it may be one of the parts (in place).
+ * lse_out: f32 [rows] or NULL. n_parts in [1, MLA_MERGE_MAX_PARTS]; a NaN or
+ * +inf lse gives an unspecified row. No workspace. */
+mla_status_t mla_merge_attn(int32_t n_parts, const void *const *outs_bf16, const float *const *lses, int64_t rows,
+                            void *out_bf16, float *lse_out, cudaStream_t stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char *mla_last_error(void);
 

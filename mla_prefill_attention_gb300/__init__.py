@@ -1,4 +1,5 @@
-"""GB300 (sm_103a) MLA prefill attention: dense, indexer top-k and sparse.
+"""GB300 (sm_103a) MLA prefill attention: cache write, dense, indexer top-k, sparse
+and the log-sum-exp merge of partial results.
 
 The compute path is the CUDA library ``libmla.so`` (C ABI in include/mla.h);
 ``binding`` marshals PyTorch tensors into it. Nothing here falls back to a
@@ -15,6 +16,8 @@ from .binding import (  # noqa: F401
     chunk_bounds,
     chunked_prefill_sparse,
     mla_indexer_topk,
+    mla_kv_append,
+    mla_merge_attn,
     mla_prefill_dense,
     mla_prefill_dense_static,
     mla_prefill_sparse,

@@ -20,7 +20,7 @@ MLA_DEVERR_BAD_PAGE, MLA_DEVERR_BAD_INDEX, MLA_DEVERR_TIMEOUT, MLA_DEVERR_INTERN
 MLA_OP_DENSE, MLA_OP_INDEXER, MLA_OP_SPARSE = 0, 1, 2
 
 EXPORTS = ("mla_workspace_size", "mla_prefill_dense", "mla_indexer_topk", "mla_prefill_sparse", "mla_last_error",
-           "mla_prefill_dense_static")
+           "mla_prefill_dense_static", "mla_kv_append", "mla_merge_attn")
 DENSE_STATIC_MAX_WORK_ITEMS = 65536
 
 
@@ -66,6 +66,10 @@ def load(path: str = LIB_PATH):
                                      vp, vp]
     L.mla_prefill_dense_static.restype = ctypes.c_int
     L.mla_prefill_dense_static.argtypes = [ctypes.POINTER(mla_seqs_t), vp, i32, vp, vp, f32, vp, vp, vp, vp]
+    L.mla_kv_append.restype = ctypes.c_int
+    L.mla_kv_append.argtypes = [ctypes.POINTER(mla_seqs_t), vp, vp, vp, vp, vp, vp, vp, vp]
+    L.mla_merge_attn.restype = ctypes.c_int
+    L.mla_merge_attn.argtypes = [i32, vp, vp, i64, vp, vp, vp]
     L.mla_last_error.restype = ctypes.c_char_p
     L.mla_last_error.argtypes = []
     _lib = L
@@ -182,6 +186,37 @@ def mla_prefill_sparse(seqs: Seqs, q: torch.Tensor, kv: torch.Tensor, kv_scale: 
     _check(load().mla_prefill_sparse(ctypes.byref(c), _ptr(q), H, _ptr(kv), _ptr(kv_scale), float(sm_scale),
                                      _ptr(idx), int(idx.shape[1]), _ptr(out), _ptr(lse), _ptr(ws), wsb,
                                      _ptr(dev_err), _stream()))
+    return out, lse
+
+
+def mla_kv_append(seqs: Seqs, latent: torch.Tensor, kv: torch.Tensor, kv_scale: torch.Tensor, kidx=None, ki=None,
+                  ki_scale=None, dev_err=None):
+    """Quantise the new tokens' rows into the paged caches (in place).
+    latent bf16 [Tq,576] -> kv uint8 [nb,256,576] + kv_scale f32 [nb,256];
+    kidx bf16 [Tq,128] (optional) -> ki uint8 [nb,256,128] + ki_scale f32 [nb,256]."""
+    c = seqs.c()
+    _check(load().mla_kv_append(ctypes.byref(c), _ptr(latent), _ptr(kidx), _ptr(kv), _ptr(kv_scale), _ptr(ki),
+                                _ptr(ki_scale), _ptr(dev_err), _stream()))
+
+
+MLA_MERGE_MAX_PARTS = 8
+
+
+def mla_merge_attn(outs, lses, out=None, lse=None, want_lse: bool = True):
+    """Log-sum-exp merge of partial results over disjoint key sets.
+    outs: list of bf16 [..., 512] tensors, lses: list of f32 tensors of the
+    matching leading shape. Returns (out, lse) (out may be passed as outs[0])."""
+    n = len(outs)
+    if n != len(lses):
+        raise ValueError("outs and lses differ in length")
+    rows = outs[0].numel() // 512
+    if out is None:
+        out = torch.empty_like(outs[0])
+    if lse is None and want_lse:
+        lse = torch.empty_like(lses[0])
+    po = (ctypes.c_void_p * n)(*[t.data_ptr() for t in outs])
+    pl = (ctypes.c_void_p * n)(*[t.data_ptr() for t in lses])
+    _check(load().mla_merge_attn(n, po, pl, rows, _ptr(out), _ptr(lse), _stream()))
     return out, lse
 
 

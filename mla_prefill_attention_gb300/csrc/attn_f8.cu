@@ -150,15 +150,6 @@ struct RowTile {
     int64_t tok;        // sparse: the token
 };
 
-__device__ __forceinline__ int find_seq(const int32_t *cu, int batch, int64_t t) {
-    int lo = 0, hi = batch - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-}
-
 // Dense: row tile `tile` of sequence b. Sparse: heads h0.. of token tok, whose
 // top-k indices give its keys.
 template <bool kSparse>

@@ -41,6 +41,17 @@ __device__ __forceinline__ void set_dev_err(int32_t *dev_err, int bit) {
     if (dev_err) atomicOr(dev_err, bit);
 }
 
+// Sequence of global new-token t: the last b with cu[b] <= t (cu non-decreasing,
+// so sequences without new tokens are passed over).
+__device__ __forceinline__ int find_seq(const int32_t *cu, int batch, int64_t t) {
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
 // Physical cache row of position s of the sequence whose block-table row is bt;
 // -1 (and an error bit) if the page id is outside [0, num_blocks).
 __device__ __forceinline__ int64_t cache_row(const int32_t *bt, int32_t max_blocks, int32_t num_blocks, int64_t s,

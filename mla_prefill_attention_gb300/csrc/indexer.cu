@@ -18,15 +18,6 @@
 namespace mla {
 namespace idx {
 
-__device__ __forceinline__ int find_seq(const int32_t *cu, int batch, int64_t t) {
-    int lo = 0, hi = batch - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-}
-
 // ---------------------------------------------------------------------------
 // exact top-k over one score row per token
 // ---------------------------------------------------------------------------

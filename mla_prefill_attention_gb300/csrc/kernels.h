@@ -63,4 +63,35 @@ cudaError_t launch_indexer_scores_tc(const IndexerArgs &a, const int4 *work, int
                                      const CUtensorMap &tmap_q, cudaStream_t st);
 cudaError_t launch_topk(const IndexerArgs &a, int64_t n_tokens, cudaStream_t st);
 
+struct AppendArgs {
+    const __nv_bfloat16 *latent; // [Tq, 576]
+    const __nv_bfloat16 *kidx;   // [Tq, 128] or null
+    uint8_t *kv;                 // [num_blocks, 256, 576] e4m3
+    float *kv_scale;             // [num_blocks, 256]
+    uint8_t *ki;                 // [num_blocks, 256, 128] e4m3 (unused without kidx)
+    float *ki_scale;             // [num_blocks, 256]
+    const int32_t *block_table;
+    int32_t max_blocks, num_blocks;
+    const int32_t *cu_seqlens;
+    const int32_t *prefix_lens;
+    int32_t batch;
+    int64_t n_tokens;
+    int32_t *dev_err;
+};
+
+// Cache write of the new tokens (per-token absmax/448 e4m3 rows), one warp per token.
+cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t st);
+
+constexpr int kMergeMaxParts = 8;
+struct MergeArgs {
+    const uint4 *outs[kMergeMaxParts];   // part i: bf16 [rows, 512]
+    const float *lses[kMergeMaxParts];   // part i: f32 [rows]
+    int32_t n_parts;
+    int64_t rows;
+    uint4 *out;                          // bf16 [rows, 512] (may be one of the parts)
+    float *lse;                          // f32 [rows] or null
+};
+// Log-sum-exp merge of partial attention results, one warp per row.
+cudaError_t launch_merge(const MergeArgs &a, cudaStream_t st);
+
 }  // namespace mla

@@ -14,6 +14,8 @@
 #include "../../include/mla.h"
 #include "kernels.h"
 
+static_assert(MLA_MERGE_MAX_PARTS == mla::kMergeMaxParts, "merge part limit");
+
 namespace {
 
 thread_local std::string g_err;
@@ -315,6 +317,73 @@ mla_status_t mla_prefill_sparse(const mla_seqs_t *seqs, const void *q_bf16, int3
     a.topk = topk;
     cudaError_t e = mla::launch_sparse_f8(a, tq, stream);
     if (e != cudaSuccess) return cuda_fail(e, "sparse launch");
+    return MLA_OK;
+}
+
+mla_status_t mla_kv_append(const mla_seqs_t *seqs, const void *latent_bf16, const void *kidx_bf16,
+                           uint8_t *kv_e4m3, float *kv_scale, uint8_t *ki_e4m3, float *ki_scale,
+                           int32_t *dev_err, cudaStream_t stream) {
+    g_err.clear();
+    mla_status_t st = check_seqs(seqs);
+    if (st != MLA_OK) return st;
+    if (!latent_bf16 || !kv_e4m3 || !kv_scale) return fail(MLA_ERR_INVALID_ARG, "latent, kv and kv_scale must be set");
+    if (!aligned(latent_bf16, 16) || !aligned(kv_e4m3, 16))
+        return fail(MLA_ERR_INVALID_ARG, "latent and kv must be 16-byte aligned");
+    if (!aligned(kv_scale, 4)) return fail(MLA_ERR_INVALID_ARG, "kv_scale must be 4-byte aligned");
+    if (kidx_bf16) {
+        if (!ki_e4m3 || !ki_scale) return fail(MLA_ERR_INVALID_ARG, "ki and ki_scale must be set with kidx");
+        if (!aligned(kidx_bf16, 16) || !aligned(ki_e4m3, 16))
+            return fail(MLA_ERR_INVALID_ARG, "kidx and ki must be 16-byte aligned");
+        if (!aligned(ki_scale, 4)) return fail(MLA_ERR_INVALID_ARG, "ki_scale must be 4-byte aligned");
+    }
+    const int64_t tq = seqs->cu_seqlens_q_host[seqs->batch];
+    if (tq == 0) return MLA_OK;
+    if (tq > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "too many new tokens");
+    mla::AppendArgs a{};
+    a.latent = static_cast<const __nv_bfloat16 *>(latent_bf16);
+    a.kidx = static_cast<const __nv_bfloat16 *>(kidx_bf16);
+    a.kv = kv_e4m3;
+    a.kv_scale = kv_scale;
+    a.ki = kidx_bf16 ? ki_e4m3 : nullptr;
+    a.ki_scale = kidx_bf16 ? ki_scale : nullptr;
+    a.block_table = seqs->block_table;
+    a.max_blocks = seqs->max_blocks_per_seq;
+    a.num_blocks = seqs->num_blocks;
+    a.cu_seqlens = seqs->cu_seqlens_q;
+    a.prefix_lens = seqs->prefix_lens;
+    a.batch = seqs->batch;
+    a.n_tokens = tq;
+    a.dev_err = dev_err;
+    const cudaError_t e = mla::launch_kv_append(a, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kv append launch");
+    return MLA_OK;
+}
+
+mla_status_t mla_merge_attn(int32_t n_parts, const void *const *outs_bf16, const float *const *lses, int64_t rows,
+                            void *out_bf16, float *lse_out, cudaStream_t stream) {
+    g_err.clear();
+    if (n_parts < 1 || n_parts > MLA_MERGE_MAX_PARTS)
+        return fail(MLA_ERR_UNSUPPORTED, "n_parts must be in [1, %d] (got %d)", MLA_MERGE_MAX_PARTS, n_parts);
+    if (!outs_bf16 || !lses || !out_bf16) return fail(MLA_ERR_INVALID_ARG, "outs, lses and out must be set");
+    if (rows < 0) return fail(MLA_ERR_INVALID_ARG, "rows must be >= 0");
+    if (!aligned(out_bf16, 16)) return fail(MLA_ERR_INVALID_ARG, "out must be 16-byte aligned");
+    if (lse_out && !aligned(lse_out, 4)) return fail(MLA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+    mla::MergeArgs a{};
+    for (int i = 0; i < n_parts; ++i) {
+        if (!outs_bf16[i] || !lses[i]) return fail(MLA_ERR_INVALID_ARG, "part %d: out and lse must be set", i);
+        if (!aligned(outs_bf16[i], 16) || !aligned(lses[i], 4))
+            return fail(MLA_ERR_INVALID_ARG, "part %d: out must be 16-byte and lse 4-byte aligned", i);
+        a.outs[i] = static_cast<const uint4 *>(outs_bf16[i]);
+        a.lses[i] = lses[i];
+    }
+    if (rows == 0) return MLA_OK;
+    if ((rows + 7) / 8 > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "too many rows");
+    a.n_parts = n_parts;
+    a.rows = rows;
+    a.out = static_cast<uint4 *>(out_bf16);
+    a.lse = lse_out;
+    const cudaError_t e = mla::launch_merge(a, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
     return MLA_OK;
 }
 

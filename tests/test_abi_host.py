@@ -112,3 +112,44 @@ def test_workspace_sizes(lib):
     assert lib.mla_workspace_size(B.MLA_OP_SPARSE, ctypes.byref(s.c), 64, 2048) == 0
     assert lib.mla_workspace_size(B.MLA_OP_DENSE, None, 64, 0) == 0
     assert lib.mla_workspace_size(B.MLA_OP_DENSE, ctypes.byref(s.c), 40, 0) == 0
+
+
+def test_kv_append_rejects_bad_arguments(lib):
+    s = HostSeqs([100], [300])
+
+    def app(lat=FAKE, kidx=None, kv=FAKE, kvs=FAKE, ki=None, kis=None, seqs=s):
+        return lib.mla_kv_append(ctypes.byref(seqs.c) if seqs is not None else None, lat, kidx, kv, kvs, ki, kis,
+                                 None, None)
+
+    assert app(seqs=None) == B.MLA_ERR_INVALID_ARG
+    assert app(lat=None) == B.MLA_ERR_INVALID_ARG
+    assert app(lat=FAKE_MIS) == B.MLA_ERR_INVALID_ARG
+    assert app(kv=FAKE_MIS) == B.MLA_ERR_INVALID_ARG
+    assert app(kvs=ctypes.c_void_p(0x100002)) == B.MLA_ERR_INVALID_ARG
+    assert app(kidx=FAKE) == B.MLA_ERR_INVALID_ARG             # key given without its cache
+    assert b"ki" in lib.mla_last_error()
+    assert app(kidx=FAKE_MIS, ki=FAKE, kis=FAKE) == B.MLA_ERR_INVALID_ARG
+    short = HostSeqs([300], [0], max_blocks=1)                   # needs 2 pages
+    assert app(seqs=short) == B.MLA_ERR_INVALID_ARG
+    assert app(seqs=HostSeqs([0, 0], [7, 0])) == B.MLA_OK      # nothing to write: no launch
+
+
+def test_merge_rejects_bad_arguments(lib):
+    def arr(*ps):
+        return (ctypes.c_void_p * len(ps))(*ps)
+
+    two = arr(0x100000, 0x200000)
+    lses = arr(0x300000, 0x400000)
+    ok = lib.mla_merge_attn(2, two, lses, 0, FAKE, None, None)
+    assert ok == B.MLA_OK                                       # no rows: nothing to launch
+    assert lib.mla_merge_attn(0, two, lses, 10, FAKE, None, None) == B.MLA_ERR_UNSUPPORTED
+    assert lib.mla_merge_attn(9, arr(*[0x100000] * 9), arr(*[0x300000] * 9), 10, FAKE, None,
+                              None) == B.MLA_ERR_UNSUPPORTED
+    assert lib.mla_merge_attn(2, None, lses, 10, FAKE, None, None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_merge_attn(2, two, lses, 10, None, None, None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_merge_attn(2, two, lses, -1, FAKE, None, None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_merge_attn(2, arr(0x100000, 0x200008), lses, 10, FAKE, None, None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_merge_attn(2, two, arr(0x300000, 0x400002), 10, FAKE, None, None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_merge_attn(2, arr(0x100000, 0), lses, 10, FAKE, None, None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_merge_attn(2, two, lses, 10, FAKE_MIS, None, None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_merge_attn(2, two, lses, 10, FAKE, ctypes.c_void_p(0x500002), None) == B.MLA_ERR_INVALID_ARG
