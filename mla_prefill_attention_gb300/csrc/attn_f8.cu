@@ -278,7 +278,7 @@ __device__ __noinline__ void load_q_split(const AttnArgs &a, const RowTile &rt, 
     const uint4 *qa = reinterpret_cast<const uint4 *>(a.q + (rt.grow0 + (oka ? ra : 0)) * kDqk + 8 * tc);
     const uint4 *qb = reinterpret_cast<const uint4 *>(a.q + (rt.grow0 + (okb ? rb : 0)) * kDqk + 8 * tc);
     float mxa = 0.f, mxb = 0.f;
-#pragma unroll 6
+#pragma unroll 9
     for (int g = 0; g < 18; ++g) {
         const uint4 va = oka ? __ldg(qa + 4 * g) : make_uint4(0, 0, 0, 0);
         const uint4 vb = okb ? __ldg(qb + 4 * g) : make_uint4(0, 0, 0, 0);
@@ -654,6 +654,11 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                 }
             }
             mma_commit_w(smem_u32(&sh.bar[B_FINAL]), lead);
+        } else if (kSparse && lane == 1 && n_rt > 1) {
+            // the second token's queries are split long after they are first needed
+            // in L2: fetch them now, so that split reads L2 instead of HBM
+            const RowTile rt1 = tile_of(1);
+            bulk_prefetch_l2(a.q + rt1.grow0 * kDqk, static_cast<uint32_t>(rt1.nvalid) * kDqk * 2);
         }
         __syncwarp();
     } else {

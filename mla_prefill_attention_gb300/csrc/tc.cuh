@@ -293,6 +293,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (16-B aligned, size % 16 == 0); no completion.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2-D tiled tensor copy global -> shared through the TMA engine, completing
 // `bytes` of the mbarrier's transaction count. x is the innermost coordinate
 // (its byte offset must be a multiple of 16); the tensor map lives in kernel
