@@ -191,7 +191,12 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+// The mbarrier receives one arrival once all of this thread's earlier cp.async copies
+// have landed (its expected count includes these arrivals); the thread does not wait.
+__device__ __forceinline__ void cp_async_arrive(uint32_t mbar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(mbar) : "memory");
+}
+__device__ __align__(16) uint8_t g_zero_row[128];   // the source of padding rows
 
 struct Walk {
     int n0, total;
@@ -396,7 +401,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
             if ((i >= B_S_FREE && i < B_S_FREE + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) || i == B_Q_FULL ||
                 i == B_O_FREE)
                 cnt = kSmWarps<kSparse>;
-            if (kSparse && i >= B_FULL && i < B_FULL + kStages<true>) cnt = 2;   // both warps of a gather pair
+            if (kSparse && i >= B_FULL && i < B_FULL + kStages<true>) cnt = 64;  // every lane of a gather pair
             if (i >= B_XCH && i < B_XCH + 4) cnt = 2;                          // the quadrant's two softmax warps
             mbar_init(smem_u32(&sh.bar[i]), cnt);
         }
@@ -512,7 +517,9 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
         // =================== row gathers (sparse): pair p takes tiles p, p+2, ... ===================
         // Key k's 576 bytes go by 16-byte cp.async into the swizzled slices, eight
         // lanes per row (one 128-byte slice row per instruction and row), four rows
-        // per warp instruction; a key that is padding (-1) or invalid is zeroed.
+        // per warp instruction; a key that is padding (-1) or invalid copies zeros.
+        // Copies complete asynchronously on the stage's barrier, so a pair's next
+        // tile is on its way before the previous one has landed.
         constexpr int BN = kBN<true>, ST = kStages<true>, kBoxes = BN / kGroupRows;
         constexpr int kSliceB = kSliceBytes<true>, kStageB = kStageBytes<true>;
         const int gk = lane >> 3, gc = lane & 7;
@@ -557,19 +564,17 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                 const int k = 4 * g + gk, kb = (4 * g) >> 5;     // kb: the same for the four rows
                 const int64_t r0 = kb == 0 ? krow[0] : (kb == 1 ? krow[1] : krow[2]);
                 const int64_t row = __shfl_sync(0xffffffffu, r0, k & 31);
-                const uint8_t *src = a.kv + (row >= 0 ? row : 0) * kDqk + 16 * gc;
+                const uint8_t *src = row >= 0 ? a.kv + row * kDqk + 16 * gc : g_zero_row + 16 * gc;
+                const int sstep = row >= 0 ? 128 : 0;
 #pragma unroll
                 for (int s = 0; s < kSlices; ++s) {
                     if (s == kSlices - 1 && gc >= 4) break;      // the RoPE slice holds 64 bytes
-                    const uint32_t off = s * kSliceB + swz(k, gc);
-                    if (row >= 0) cp_async16(sst + off, src + 128 * s);
-                    else *reinterpret_cast<uint4 *>(sbase + st * kStageB + off) = make_uint4(0, 0, 0, 0);
+                    cp_async16(sst + s * kSliceB + swz(k, gc), src + sstep * s);
                 }
             }
-            cp_async_wait_all();
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_FULL + st]));
+            // no wait: each lane's arrival lands on the stage's barrier when its copies
+            // have (the issuer fences them into the async proxy before its MMAs)
+            cp_async_arrive(smem_u32(&sh.bar[B_FULL + st]));
         }
     } else if (warp == kIssuerWarp<kSparse>) {
         // =================== MMA issuer (lane 0; the other lanes wait at the end) ===================
@@ -602,6 +607,7 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                 };
                 if (!wait(B_FULL + 0 * ST + st, ph)) return false;
                 fence_after_sync();
+                if (kSparse) fence_proxy_async();   // the gathers' cp.async writes, for the MMAs
                 slice(4, 0u);
                 if (kParts<kSparse> == 3) {
                     mma_commit_w(smem_u32(&sh.bar[B_EMPTY + 0 * ST + st]), lead);   // RoPE slice free

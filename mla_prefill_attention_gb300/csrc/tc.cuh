@@ -293,6 +293,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// Four rows (y0..y3, any order, out-of-range ones read as zero) of a 2-D tensor
+// whose map has a one-row box, starting at column x: 4 x box-width bytes to dst,
+// row i at dst + i * box width, swizzled as the map says, completing on mbar.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int x, int y0, int y1, int y2, int y3,
+                                            uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+        "%4, %5, %6}], [%7];\n" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(mbar)
+        : "memory");
+}
+
 // Bulk prefetch of global memory into L2 (16-B aligned, size % 16 == 0); no completion.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
