@@ -1,19 +1,21 @@
-// Dense MLA prefill attention with e4m3 tensor-core operands (tcgen05 kind::f8f6f4).
+// MLA prefill attention, dense and sparse, with e4m3 tensor-core operands
+// (tcgen05 kind::f8f6f4).
 //
-// The cache holds e4m3 codes, so the key/value operand needs no conversion: a
-// 96-key tile is copied by TMA straight from its pages into 128-byte-swizzled
-// shared memory, and both MMAs read the codes as they are. The other operand of
-// each product is split into two e4m3 terms whose sum carries bf16 precision:
+// The cache holds e4m3 codes, so the key/value operand needs no conversion: key
+// tiles go straight from the pages into 128-byte-swizzled shared memory (dense:
+// TMA boxes; sparse: rows gathered by index) and both MMAs read the codes as
+// they are. The other operand of each product is split into two e4m3 terms whose
+// sum carries bf16 precision:
 //
 //   Q/s_Q = Qh + Ql   (s_Q a power of two per row; for bf16 input the split is
 //                      exact while |Q/s_Q| >= 2^-2, and the largest element sits
 //                      in [128, 256))
 //   P     = Ph + Pl   (P rounded to f16 first; 8 significant bits in total)
 //
-//   S   = Qh K^T + Ql K^T          M=64 N=96, K=576 (A = Qh, Ql in TMEM)
+//   S   = Qh K^T + Ql K^T          M=64, N=BN keys, K=576 (A = Qh, Ql in TMEM)
 //   u   = S s_Q sigma sm_scale log2(e) + log2(sigma)
 //   P   = 2^(u - m + 6),  l += P / sigma     (m: reference max, log2 domain)
-//   O  += Ph V + Pl V              M=64 N=256 x 2 chunks of the 512 value dims
+//   O  += Ph V + Pl V              M=64, N=256 x 2 chunks of the 512 value dims
 //
 // and out = O / l, lse = ln2 (m - 6 + log2 l). The offset 6 keeps the largest
 // weights of a row in the normal e4m3 range (a P of 1 would leave most of the
@@ -27,24 +29,31 @@
 // TMEM (M=64 layout: row r in lane 32*(r/16) + r%16 + 16*h, h = lane half)
 //   h=0 cols   0..143 : Qh (576 codes, four per column)
 //   h=0 cols 144..287 : Ql
-//   h=0 cols 288..383 : S buffer 0,  cols 384..479 : S buffer 1
+//   h=0 cols 288..    : S (dense: one buffer of 128 columns; sparse: two of 96)
 //   h=1 cols   0..511 : O
 //
 // Shared memory
-//   3 stages x 5 slices x [96 keys][128 B], 128-byte swizzle (TMA box 128 B x 32
-//     keys; a page holds 8 boxes, so no box straddles a page). Slices 0-3 are
-//     the value dims (K-major for QK, MN-major for PV); slice 4 is the RoPE part
-//     (dims 512..575, the box's upper 64 bytes zero-filled by TMA)
-//   P: 2 buffers x {Ph, Pl} x [64 rows][96 keys], K-major without swizzle
-//     (16-byte x 8-row core matrices; 128 B apart along the keys, 768 B apart
-//     along the rows)
+//   dense: 2 stages x 5 slices x [128 keys][128 B]; sparse: 3 stages x 5 slices x
+//     [96 keys][128 B]; 128-byte swizzle. Slices 0-3 are the value dims (K-major
+//     for QK, MN-major for PV); slice 4 holds the 64 RoPE dims (upper 64 bytes
+//     unused). A dense stage is released in three parts as the tensor core is done
+//     with them (the RoPE slice after QK, value dims 0-255 and 256-511 after the
+//     two PV chunks); a sparse stage is released whole after PV.
+//   P: 2 buffers x {Ph, Pl} x [64 rows][BN keys], K-major without swizzle
+//     (16-byte x 8-row core matrices; 128 B apart along the keys, BN/16 * 128 B
+//     apart along the rows)
 //
-// Warps: 0-3 softmax (as in the f16 kernel: warp w owns TMEM quadrant w, thread
-// (tq, tc) rows 16w + tq and 16w + tq + 8 x 24 keys; they also split Q into
-// TMEM and run the epilogue), 4 TMA producer and key metadata, 5 MMA issue.
-// Keys past a row tile's causal limit are zeroed in shared memory (they may be
-// unwritten cache rows; a NaN code there would survive a zero weight).
-// Every wait is bounded; one that runs out sets MLA_DEVERR_TIMEOUT.
+// Warps
+//   dense (10): 0-7 softmax (two per TMEM lane quadrant, 64 keys of a tile each;
+//     they also split Q into TMEM and run the epilogue), 8 TMA producer and key
+//     metadata, 9 MMA issue.
+//   sparse (9): 0-3 softmax (96 keys each), two pairs of gather warps (4 and 6,
+//     7 and 8: cp.async rows by index, completing on the stage barrier), 5 MMA
+//     issue.
+// Keys past a row's causal limit, padding indices and invalid pages are zeroed in
+// shared memory (an unwritten cache row could hold a NaN code, which a zero
+// weight would not cancel). Every wait is bounded; one that runs out sets
+// MLA_DEVERR_TIMEOUT.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -70,7 +79,7 @@ template <bool S> constexpr int kStages = S ? 3 : 2;
 template <bool S> constexpr int kParts = S ? 1 : 3;
 template <bool S> constexpr int kSBufs = S ? 2 : 1;
 constexpr int kBNMax = 128;
-// Warps. dense: 10 = 8 softmax (two per TMEM lane quadrant, 48 of a tile's 96 keys
+// Warps. dense: 10 = 8 softmax (two per TMEM lane quadrant, 64 of a tile's 128 keys
 // each: the softmax of tile t then ends before QK(t+1) does), TMA producer (8),
 // issuer (9). sparse: 9 = 4 softmax (96 keys each; with eight, the register cap of
 // 13 warps costs more than the shorter softmax gains), issuer (5) and two pairs of
