@@ -241,7 +241,41 @@ class SparseRun:
         mla_prefill_sparse(self.seqs, d["q"], d["kv"], d["ks"], self.w.sm_scale, self.idx, out=self.out, lse=self.lse)
 
     def e2e(self, steps, warmup):
-        return None
+        """Both calls with every input in pinned host memory and the output, lse and
+        selected indices copied back, copies inside the timed region."""
+        import torch
+        from mla_prefill_attention_gb300 import mla_indexer_topk, mla_prefill_sparse
+        h = {k: torch.from_numpy(v).pin_memory() for k, v in self.host.items() if k != "q"}
+        h["q"] = torch.from_numpy(self.host["q"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        hout = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
+        hlse = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+        hidx = torch.empty(self.idx.shape, dtype=torch.int32).pin_memory()
+        d = self.d
+
+        def one():
+            for k in h:
+                d[k].copy_(h[k], non_blocking=True)
+            mla_indexer_topk(self.seqs, d["qi"], d["w"], 0, d["ki"], d["kis"], self.w.topk, idx_out=self.idx,
+                             workspace=self.ws)
+            mla_prefill_sparse(self.seqs, d["q"], d["kv"], d["ks"], self.w.sm_scale, self.idx, out=self.out,
+                               lse=self.lse)
+            hout.copy_(self.out, non_blocking=True)
+            hlse.copy_(self.lse, non_blocking=True)
+            hidx.copy_(self.idx, non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            one()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        h2d = sum(t.numel() * t.element_size() for t in h.values())
+        d2h = hout.numel() * 2 + hlse.numel() * 4 + hidx.numel() * 4
+        return ms, h2d, d2h
 
     def oracle_rate(self, budget_s, seed=0):
         from oracle import oracle as O

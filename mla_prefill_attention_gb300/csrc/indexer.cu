@@ -356,6 +356,10 @@ __device__ __noinline__ void topk_radix(const IndexerArgs &a, const float4 *row4
 // Block-wide bitonic sort of v[0..P) in shared memory (P a power of two).
 template <typename T, bool kDescending>
 __device__ __forceinline__ void bitonic_sort(T *v, int P) {
+    // Pair (lo, hi) of index i at stride s <= 32 lies inside elements 64w .. 64w+63
+    // of the warp w that owns i (i mod 512 in 32w .. 32w+31), so those stages only
+    // need the warp's own lanes in step; a block barrier follows each wider stage
+    // and the last stage of every size (the next size starts wide).
     for (int size = 2; size <= P; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             for (int i = threadIdx.x; i < P / 2; i += TK_NT) {
@@ -367,7 +371,8 @@ __device__ __forceinline__ void bitonic_sort(T *v, int P) {
                     v[hi] = x;
                 }
             }
-            __syncthreads();
+            if (stride > 32 || stride == 1) __syncthreads();
+            else __syncwarp();
         }
     }
 }
