@@ -413,6 +413,25 @@ RUNS = {"tiny512": DenseRun, "prefix12k": DenseRun, "dense32k": DenseRun, "ragge
         "sparse64k": SparseRun, "chunked200k": ChunkedRun}
 
 
+def max_over_ranks(ms, device=None):
+    """The slowest rank's time under torch.distributed (every rank calls it);
+    unchanged in a single process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, tokens_per_rank, steps, total_ms):
+    """Whole-job tokens per second: each of the world ranks runs its own replica
+    of the workload, tokens_per_rank new tokens per step, in total_ms (the
+    slowest rank's time)."""
+    return world * tokens_per_rank * steps / (total_ms / 1000.0)
+
+
 def time_steps(run, steps, warmup):
     import torch
     for _ in range(warmup):
@@ -618,13 +637,11 @@ def main():
     total_ms, per_ms = time_steps(run, args.steps, args.warmup)
     clk = clocks.stop()
     if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dev)
         dist.barrier()
 
     ms_per_step = total_ms / args.steps
-    value = world * run.tokens * args.steps / (total_ms / 1000.0)
+    value = job_throughput(world, run.tokens, args.steps, total_ms)
     kern_ms = statistics.mean(per_ms)
     tflops = run.flops / (kern_ms / 1000.0) / 1e12
     pk, src = peaks()
