@@ -413,6 +413,17 @@ RUNS = {"tiny512": DenseRun, "prefix12k": DenseRun, "dense32k": DenseRun, "ragge
         "sparse64k": SparseRun, "chunked200k": ChunkedRun}
 
 
+# DRAM bytes (read + written) per launch of the timed kernels, from one ncu capture
+# of dram__bytes_read.sum + dram__bytes_write.sum (one pass) on the bench's own
+# command line for that workload. A kernel change invalidates its entry: set it to
+# None until it is captured again.
+TRAFFIC = {
+    "dense32k": {"attention": 2454125824 + 2117622272},
+    "sparse64k": {"indexer_topk": 76688128 + 1955476736 + 2014642944 + 63335424,
+                  "sparse_attention": 815294976 + 530747136},
+}
+
+
 def max_over_ranks(ms, device=None):
     """The slowest rank's time under torch.distributed (every rank calls it);
     unchanged in a single process."""
@@ -650,7 +661,7 @@ def main():
         # Each algorithmic FLOP runs as two e4m3 tensor FLOPs (the two-term Q and P), at
         # twice the bf16 rate: the fraction is the same against either roof.
         roof = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
-                "traffic": None,
+                "traffic": TRAFFIC.get(w.name, {}).get("attention"),
                 "peak_source": f"{src} bf16 sustained; the kernel runs each algorithmic FLOP as two e4m3 tensor "
                                f"FLOPs at twice the bf16 rate, so this equals the e4m3 roof",
                 "kernel": "attn_f8_kernel: tcgen05 kind::f8f6f4, e4m3 cache tiles by TMA, two-term e4m3 Q and P, "
@@ -659,12 +670,14 @@ def main():
         idx_ms, att_ms = statistics.mean(run.split_ms[0]), statistics.mean(run.split_ms[1])
         idx_tf = run.indexer_flops / (idx_ms / 1000.0) / 1e12
         att_tf = run.sparse_flops / (att_ms / 1000.0) / 1e12
+        tr = TRAFFIC.get(w.name, {})
         roof = {"bound": "tensor", "achieved": idx_tf, "peak": 2 * peak, "unit": "TFLOP/s",
-                "frac": idx_tf / (2 * peak), "traffic": None,
+                "frac": idx_tf / (2 * peak), "traffic": tr.get("indexer_topk"),
                 "peak_source": f"e4m3 dense = 2 x {src} bf16 sustained (the nominal e4m3:bf16 ratio)",
                 "kernel": "mla_indexer_topk (indexer scores on tcgen05 e4m3 + exact top-k), the larger share",
                 "split_ms": {"indexer_topk": idx_ms, "sparse_attention": att_ms},
                 "sparse_attention": {"achieved": att_tf, "peak": peak, "frac": att_tf / peak,
+                                     "traffic": tr.get("sparse_attention"),
                                      "kernel": "attn_f8_kernel<sparse>: tcgen05 e4m3, gathered rows"}}
     else:   # chunked: the last step's per-call totals over all chunks
         run.collect_chunk_ms()
