@@ -419,7 +419,7 @@ RUNS = {"tiny512": DenseRun, "prefix12k": DenseRun, "dense32k": DenseRun, "ragge
 # None until it is captured again.
 TRAFFIC = {
     "dense32k": {"attention": 2454125824 + 2117622272},
-    "sparse64k": {"indexer_topk": 76688128 + 1955476736 + 2014642944 + 63335424,
+    "sparse64k": {"indexer_topk": 76787200 + 1955591168 + 2014747904 + 63284736,
                   "sparse_attention": 815294976 + 530747136},
 }
 

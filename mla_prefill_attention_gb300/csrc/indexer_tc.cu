@@ -5,11 +5,11 @@
 // earlier token to pick 2,048; footnote 3: an indexer key is 128 FP8 values
 // plus a 4-byte scale.)
 //
-// One CTA scores 4 query tokens (x 64 heads) against a chunk of keys, 128 keys
+// One CTA scores 3 query tokens (x 64 heads) against a chunk of keys, 128 keys
 // at a time:
 //
 //   D[key][64 j + h] = k_key . q_{t_j,h}    tcgen05.mma e4m3 x e4m3 -> f32,
-//                                           M = 128 keys, N = 256 = 4 tokens x 64
+//                                           M = 128 keys, N = 192 = 3 tokens x 64
 //                                           heads, K = 128 (4 steps of 32)
 //
 // so TMEM lane = key and each epilogue thread owns one key: the head sum
@@ -20,15 +20,18 @@
 //
 // Keys arrive by TMA: a 128-key tile starts at a multiple of 128 and so lies in
 // one 256-token page, i.e. 128 contiguous rows of the paged key cache, copied
-// with the 128-byte swizzle the MMA's K-major operand layout expects. The 4
-// tokens' queries (256 rows) are one more TMA copy.
+// with the 128-byte swizzle the MMA's K-major operand layout expects. The 3
+// tokens' queries (192 rows) are one more TMA copy.
 //
-// Warps: 0-15 epilogue (warp w reads TMEM lane quadrant w%4 = keys 32(w%4)..+31
-// of token w/4), 16 TMA producer, 17 MMA issue + TMEM owner. Key tiles go
-// through a 6-stage ring; the accumulator is double-buffered in TMEM (2 x 256
-// columns) so the MMA of tile i+1 overlaps the epilogue of tile i. The head
-// sum runs on paired f32 FMAs (fma.rn.f32x2: two IEEE fmas, so the same
-// result as scalar ones) with four independent accumulator pairs.
+// Warps: 0-11 epilogue (warp w reads TMEM lane quadrant w%4 = keys 32(w%4)..+31
+// of token w/4), 12 TMA producer, 13 MMA issue + TMEM owner. Key tiles go
+// through a 6-stage ring; the accumulator is double-buffered in TMEM (2 x 192
+// columns) so the MMA of tile i+1 overlaps the epilogue of tile i. Fourteen
+// warps leave each thread 128 registers, enough for its token's 64 head weights
+// (as 32 register pairs, loaded once), so the head sum reads no memory: per
+// tile a thread takes its key's 64 values in two halves of 32 and runs paired
+// f32 FMAs (fma.rn.f32x2: two IEEE fmas, so the same result as scalar ones)
+// with four independent accumulator pairs.
 // Every wait is bounded and reports MLA_DEVERR_TIMEOUT.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -42,13 +45,14 @@ namespace idxtc {
 
 using namespace tc;
 
-constexpr int TOK = kIdxTokensPerCta;   // 4 query tokens per CTA
+constexpr int TOK = kIdxTokensPerCta;   // 3 query tokens per CTA
 constexpr int KT = 128;                 // keys per tile
 constexpr int STAGES = 6;
-constexpr int kEpiWarps = 16;           // 4 tokens x 4 TMEM lane quadrants
+constexpr int kEpiWarps = 4 * TOK;      // tokens x 4 TMEM lane quadrants
+constexpr int kDCols = 256;             // TMEM columns per accumulator buffer (TOK x 64 used)
 constexpr int NT = 32 * (kEpiWarps + 2);
 constexpr int kProducerWarp = kEpiWarps, kIssuerWarp = kEpiWarps + 1;
-constexpr int kQBytes = TOK * kHidx * kDidx;       // 32 KB
+constexpr int kQBytes = TOK * kHidx * kDidx;       // 24 KB
 constexpr int kTileBytes = KT * kDidx;             // 16 KB
 constexpr int kDynSmem = 1024 + kQBytes + STAGES * kTileBytes;
 constexpr long long kWaitCycles = 200000000LL;
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(NT, 1)
                 const uint64_t dk = dk0 + static_cast<uint64_t>((s * kTileBytes) >> 4);
 #pragma unroll
                 for (int ks = 0; ks < kDidx / 32; ++ks)
-                    mma_e4m3_ss(tmem + 256u * db, dk + 2 * ks, dq + 2 * ks, id, ks > 0 ? 1u : 0u);
+                    mma_e4m3_ss(tmem + kDCols * db, dk + 2 * ks, dq + 2 * ks, id, ks > 0 ? 1u : 0u);
                 mma_commit(smem_u32(&sh.bar[B_K_EMPTY + s]));
                 mma_commit(smem_u32(&sh.bar[B_D_FULL + db]));
             }
@@ -171,10 +175,16 @@ __global__ void __launch_bounds__(NT, 1)
         const int quad = warp & 3, j = warp >> 2;                     // keys 32 quad.., token j
         const uint32_t lane_addr = static_cast<uint32_t>(32 * quad) << 16;
         const int kk = 32 * quad + lane;                              // key within the tile
-        // head weights by read-only global loads: the L1 path costs the tensor core's
-        // shared-memory operand reads nothing, which broadcast shared loads did (measured)
+        // the token's head weights, as pairs, for every tile of the chunk
         const float4 *wg = reinterpret_cast<const float4 *>(a.w + static_cast<int64_t>(q0 + i0 + min(j, ntok - 1)) *
                                                             a.w_stride);
+        uint64_t wp[kHidx / 2];
+#pragma unroll
+        for (int h4 = 0; h4 < kHidx / 4; ++h4) {
+            const float4 w4 = __ldg(wg + h4);
+            wp[2 * h4] = pack2(w4.x, w4.y);
+            wp[2 * h4 + 1] = pack2(w4.z, w4.w);
+        }
         float *out_row = a.scores + static_cast<int64_t>(q0 + i0 + j) * a.score_stride;
         const int pos_hi = min(k_hi, P + i0 + j + 1);                 // causal bound of token j (exclusive)
         // The key scales go through a register pipeline: the page of tile i+3 and
@@ -209,21 +219,23 @@ __global__ void __launch_bounds__(NT, 1)
             blk3 = page_blk(i + 4);
             if (!wait_bar(sh, a.dev_err, B_D_FULL + db, (i >> 1) & 1)) break;
             fence_after_sync();
-            uint32_t d0[32], d1[32];
-            tmem_ld32(tmem + lane_addr + 256u * db + 64u * j, d0);
-            tmem_ld32(tmem + lane_addr + 256u * db + 64u * j + 32, d1);
-            tmem_ld_wait();
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_D_EMPTY + db]));
             uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-            for (int h4 = 0; h4 < 8; ++h4) {
-                const float4 wa = __ldg(wg + h4), wb = __ldg(wg + 8 + h4);
-                ffma2(acc[0], pack2(wa.x, wa.y), pack2(relu_bits(d0[4 * h4 + 0]), relu_bits(d0[4 * h4 + 1])));
-                ffma2(acc[1], pack2(wa.z, wa.w), pack2(relu_bits(d0[4 * h4 + 2]), relu_bits(d0[4 * h4 + 3])));
-                ffma2(acc[2], pack2(wb.x, wb.y), pack2(relu_bits(d1[4 * h4 + 0]), relu_bits(d1[4 * h4 + 1])));
-                ffma2(acc[3], pack2(wb.z, wb.w), pack2(relu_bits(d1[4 * h4 + 2]), relu_bits(d1[4 * h4 + 3])));
+            for (int half = 0; half < 2; ++half) {     // heads 32*half .. +31
+                uint32_t d[32];
+                tmem_ld32(tmem + lane_addr + kDCols * db + 64u * j + 32u * half, d);
+                tmem_ld_wait();
+                if (half == 1) {   // both halves read: the buffer goes back to the MMA
+                    fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_D_EMPTY + db]));
+                }
+#pragma unroll
+                for (int h4 = 0; h4 < 8; ++h4) {
+                    const int w2 = 16 * half + 2 * h4;
+                    ffma2(acc[2 * (h4 & 1)], wp[w2], pack2(relu_bits(d[4 * h4 + 0]), relu_bits(d[4 * h4 + 1])));
+                    ffma2(acc[2 * (h4 & 1) + 1], wp[w2 + 1], pack2(relu_bits(d[4 * h4 + 2]), relu_bits(d[4 * h4 + 3])));
+                }
             }
             const float sc = (sum2(acc[0]) + sum2(acc[1])) + (sum2(acc[2]) + sum2(acc[3]));
             if (j < ntok && pos < pos_hi) out_row[pos] = ok_key ? sig * sc : -INFINITY;

@@ -54,10 +54,11 @@ bool encode_kv_tmap(CUtensorMap *map, const uint8_t *kv, int32_t num_blocks);
 cudaError_t launch_sparse_f8(const AttnArgs &a, int64_t n_tokens, cudaStream_t st);
 
 // Indexer score work item: x = sequence, y = first new token (in-sequence),
-// z = token count (<= 4), w = key chunk. tmap_k: the key cache as
+// z = token count (<= kIdxTokensPerCta), w = key chunk. tmap_k: the key cache as
 // [num_blocks * 256 rows][128 B]; tmap_q: the queries as [Tq * 64 rows][128 B];
-// both with 128-byte boxes rows wide, 128-byte swizzle (128- and 256-row boxes).
-constexpr int kIdxTokensPerCta = 4;
+// both with 128-byte-wide boxes and the 128-byte swizzle (boxes of 128 key rows and of
+// kIdxTokensPerCta * 64 query rows).
+constexpr int kIdxTokensPerCta = 3;
 constexpr int kIdxKeyChunk = 8192;
 cudaError_t launch_indexer_scores_tc(const IndexerArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_k,
                                      const CUtensorMap &tmap_q, cudaStream_t st);

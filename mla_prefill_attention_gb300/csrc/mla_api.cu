@@ -287,7 +287,7 @@ mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, co
     a.dev_err = dev_err;
     CUtensorMap tmap_k, tmap_q;
     if (!encode_rows128(&tmap_k, ki_e4m3, static_cast<uint64_t>(seqs->num_blocks) * 256, 128) ||
-        !encode_rows128(&tmap_q, qi_e4m3, static_cast<uint64_t>(tq) * 64, 256))
+        !encode_rows128(&tmap_q, qi_e4m3, static_cast<uint64_t>(tq) * 64, mla::kIdxTokensPerCta * 64))
         return fail(MLA_ERR_CUDA, "tensor map encoding for the indexer failed");
     if ((e = mla::launch_indexer_scores_tc(a, dwork, static_cast<int>(work.size()), tmap_k, tmap_q, stream)) !=
         cudaSuccess)
