@@ -14,8 +14,8 @@
 // (rounded to nearest even), so every code is fixed by the definition; the
 // floor at the smallest normal value keeps the reciprocal finite.
 //
-// Pure streaming work (2,120 bytes moved per token with the indexer key): one
-// warp per token, 16-byte loads, 8-byte code stores, the row maximum reduced
+// Pure streaming work (2,120 bytes moved per token with the indexer key): four
+// tokens per warp, 16-byte loads, 8-byte code stores, the row maximum reduced
 // on the bf16 magnitude bits (a token's two maxima packed in one word, so one
 // shuffle chain serves both).
 #include <cuda_runtime.h>
@@ -26,7 +26,8 @@
 namespace mla {
 namespace app {
 
-constexpr int kWarps = 8;   // tokens per CTA, one per warp
+constexpr int kWarps = 8;          // warps per CTA
+constexpr int kTokensPerWarp = 4;
 
 // Pairwise maxima of the magnitudes of eight bf16 values (sign bits cleared):
 // two 16-bit maxima in one word. bf16 magnitude order equals the order of
@@ -58,74 +59,68 @@ __device__ __forceinline__ float scale_of(uint32_t mag) {
     return amax > 0.f ? fmaxf(__fdiv_rn(amax, 448.f), 0x1p-126f) : 1.f;
 }
 
-// One token's rows as this lane holds them: the latent row is 72 chunks of 8
-// bf16 (lanes 0..31 take chunks lane and 32 + lane, lanes 0..7 also 64 +
-// lane); the indexer key's 16 chunks go to lanes 8..23, which hold one latent
-// chunk fewer.
-struct TokenRows {
-    uint4 v0, v1, v2, k0;
-    int64_t row;   // cache row, -1 if the token's page is invalid
-};
+// Four tokens per warp, eight lanes per token: lane 8u + i takes chunks i, i+8,
+// ..., i+80 of token u's 88 chunks of 8 values (72 latent, then 16 key), i.e.
+// nine latent chunks and two key chunks, so every lane has work and each load
+// instruction covers four 128-byte runs.
+constexpr int kLatChunks = kDqk / 8, kKeyChunks = kDidx / 8;   // 72, 16
+constexpr int kLatPerLane = kLatChunks / 8, kKeyPerLane = kKeyChunks / 8;   // 9, 2
 
-__device__ __forceinline__ TokenRows load_token(const AppendArgs &a, int64_t t, int lane, bool has_k) {
-    TokenRows r;
-    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    r.v2 = r.k0 = z;
-    const uint4 *lat = reinterpret_cast<const uint4 *>(a.latent) + t * (kDqk / 8);
-    r.v0 = __ldg(lat + lane);
-    r.v1 = __ldg(lat + 32 + lane);
-    if (lane < 8) r.v2 = __ldg(lat + 64 + lane);
-    if (has_k) r.k0 = __ldg(reinterpret_cast<const uint4 *>(a.kidx) + t * (kDidx / 8) + (lane - 8));
-    const int b = find_seq(a.cu_seqlens, a.batch, t);
-    const int64_t pos = __ldg(a.prefix_lens + b) + (t - __ldg(a.cu_seqlens + b));
-    r.row = cache_row(a.block_table + static_cast<int64_t>(b) * a.max_blocks, a.max_blocks, a.num_blocks, pos,
-                      lane == 0 ? a.dev_err : nullptr);
-    return r;
-}
-
-// Both rows' maxima over the warp: latent in the high half-word, key in the low.
-__device__ __forceinline__ uint32_t row_maxima(const TokenRows &r) {
-    uint32_t m = (fold16(__vmaxu2(__vmaxu2(mag8(r.v0), mag8(r.v1)), mag8(r.v2))) << 16) | fold16(mag8(r.k0));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = __vmaxu2(m, __shfl_xor_sync(0xffffffffu, m, off));
-    return m;
-}
-
-__device__ __forceinline__ void store_token(const AppendArgs &a, const TokenRows &r, int lane, bool has_k, float sl,
-                                            float il, float sk, float ik) {
-    if (r.row < 0) return;   // the same for every lane of the warp
-    uint2 *dst = reinterpret_cast<uint2 *>(a.kv + r.row * kDqk);
-    dst[lane] = quant8(r.v0, il);
-    dst[32 + lane] = quant8(r.v1, il);
-    if (lane < 8) dst[64 + lane] = quant8(r.v2, il);
-    if (lane == 0) a.kv_scale[r.row] = sl;
-    if (has_k) {
-        reinterpret_cast<uint2 *>(a.ki + r.row * kDidx)[lane - 8] = quant8(r.k0, ik);
-        if (lane == 8) a.ki_scale[r.row] = sk;
-    }
-}
-
-// One token per warp; the two rows' scales and reciprocals come out of one
-// pass of the division and reciprocal code (lane 0 computes the latent row's,
-// lane 1 the key's) and are broadcast by shuffles.
 __global__ void __launch_bounds__(kWarps * 32) kv_append_kernel(AppendArgs a) {
-    const int lane = threadIdx.x & 31;
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    if (t >= a.n_tokens) return;
-    const bool has_k = a.kidx != nullptr && lane >= 8 && lane < 8 + kDidx / 8;
-    const TokenRows r = load_token(a, t, lane, has_k);
-    const uint32_t m = row_maxima(r);
-    const float s = scale_of((lane & 1) ? (m & 0xffffu) : (m >> 16));
+    const int lane = threadIdx.x & 31, u = lane >> 3, i8 = lane & 7;
+    const int64_t t = (static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5)) * kTokensPerWarp + u;
+    const bool live = t < a.n_tokens;
+    const bool has_k = a.kidx != nullptr;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    uint4 lv[kLatPerLane], kv4[kKeyPerLane];
+    const uint4 *lat = reinterpret_cast<const uint4 *>(a.latent) + (live ? t : 0) * kLatChunks + i8;
+    const uint4 *key = has_k ? reinterpret_cast<const uint4 *>(a.kidx) + (live ? t : 0) * kKeyChunks + i8 : nullptr;
+#pragma unroll
+    for (int m = 0; m < kLatPerLane; ++m) lv[m] = live ? __ldg(lat + 8 * m) : z;
+#pragma unroll
+    for (int m = 0; m < kKeyPerLane; ++m) kv4[m] = live && has_k ? __ldg(key + 8 * m) : z;
+
+    int64_t row = -1;
+    if (live) {
+        const int b = find_seq(a.cu_seqlens, a.batch, t);
+        const int64_t pos = __ldg(a.prefix_lens + b) + (t - __ldg(a.cu_seqlens + b));
+        row = cache_row(a.block_table + static_cast<int64_t>(b) * a.max_blocks, a.max_blocks, a.num_blocks, pos,
+                        i8 == 0 ? a.dev_err : nullptr);
+    }
+    // both rows' maxima over the token's eight lanes: latent high half-word, key low
+    uint32_t ml = 0, mk = 0;
+#pragma unroll
+    for (int m = 0; m < kLatPerLane; ++m) ml = __vmaxu2(ml, mag8(lv[m]));
+#pragma unroll
+    for (int m = 0; m < kKeyPerLane; ++m) mk = __vmaxu2(mk, mag8(kv4[m]));
+    uint32_t mx = (fold16(ml) << 16) | fold16(mk);
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) mx = __vmaxu2(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    // one pass of the division and reciprocal code for the warp's eight rows: lane
+    // 8u takes token u's latent row, lane 8u + 1 its key
+    const float s = scale_of((i8 & 1) ? (mx & 0xffffu) : (mx >> 16));
     const float inv = __frcp_rn(s);
-    store_token(a, r, lane, has_k, __shfl_sync(0xffffffffu, s, 0), __shfl_sync(0xffffffffu, inv, 0),
-                __shfl_sync(0xffffffffu, s, 1), __shfl_sync(0xffffffffu, inv, 1));
+    const float sl = __shfl_sync(0xffffffffu, s, 8 * u), il = __shfl_sync(0xffffffffu, inv, 8 * u);
+    const float sk = __shfl_sync(0xffffffffu, s, 8 * u + 1), ik = __shfl_sync(0xffffffffu, inv, 8 * u + 1);
+    if (row < 0) return;   // the same for the token's eight lanes; the shuffles are done
+    uint2 *dl = reinterpret_cast<uint2 *>(a.kv + row * kDqk) + i8;
+#pragma unroll
+    for (int m = 0; m < kLatPerLane; ++m) dl[8 * m] = quant8(lv[m], il);
+    if (i8 == 0) a.kv_scale[row] = sl;
+    if (has_k) {
+        uint2 *dk = reinterpret_cast<uint2 *>(a.ki + row * kDidx) + i8;
+#pragma unroll
+        for (int m = 0; m < kKeyPerLane; ++m) dk[8 * m] = quant8(kv4[m], ik);
+        if (i8 == 0) a.ki_scale[row] = sk;
+    }
 }
 
 }  // namespace app
 
 cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t st) {
     if (a.n_tokens <= 0) return cudaSuccess;
-    const int64_t grid = (a.n_tokens + app::kWarps - 1) / app::kWarps;
+    const int64_t per_cta = app::kWarps * app::kTokensPerWarp;
+    const int64_t grid = (a.n_tokens + per_cta - 1) / per_cta;
     app::kv_append_kernel<<<static_cast<unsigned>(grid), app::kWarps * 32, 0, st>>>(a);
     return cudaGetLastError();
 }
