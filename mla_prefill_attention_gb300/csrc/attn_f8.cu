@@ -329,21 +329,31 @@ __device__ __noinline__ void load_q_split(const AttnArgs &a, const RowTile &rt, 
             tl[w] = e4m3x2_of(x0 - g01.x, x1 - g01.y) | (e4m3x2_of(x2 - g23.x, x3 - g23.y) << 16);
         }
     };
-    // this warp's column groups g_first .. g_first + g_count - 1 (all 18, or one half)
-#pragma unroll 1
-    for (int g0 = g_first; g0 < g_first + g_count; g0 += 8) {
-        uint32_t wh[32], wl[32];
+    // this warp's column groups g_first .. g_first + g_count - 1 (all 18, or one half), four
+    // at a time, the next four groups' loads in flight while the current ones are split
+    constexpr int kC = 4;
+    uint4 buf[2][2 * kC];
+    auto fetch = [&](int g0, uint4 (&b)[2 * kC]) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kC; ++i) {
             const int g = g0 + i;
-            uint4 va = make_uint4(0, 0, 0, 0), vb = make_uint4(0, 0, 0, 0);
-            if (g < g_first + g_count) {
-                if (oka) va = __ldg(qa + 4 * g);
-                if (okb) vb = __ldg(qb + 4 * g);
-            }
+            const bool in = g < g_first + g_count;
+            b[2 * i] = in && oka ? __ldg(qa + 4 * g) : make_uint4(0, 0, 0, 0);
+            b[2 * i + 1] = in && okb ? __ldg(qb + 4 * g) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    fetch(g_first, buf[0]);
+#pragma unroll
+    for (int c = 0; c < (18 + kC - 1) / kC; ++c) {
+        const int g0 = g_first + kC * c;
+        if (g0 >= g_first + g_count) break;
+        if (g0 + kC < g_first + g_count) fetch(g0 + kC, buf[(c + 1) & 1]);
+        uint32_t wh[4 * kC], wl[4 * kC];
+#pragma unroll
+        for (int i = 0; i < kC; ++i) {
             uint32_t ha[2], la[2], hb[2], lb[2];
-            split8(va, ia, ha, la);
-            split8(vb, ib, hb, lb);
+            split8(buf[c & 1][2 * i], ia, ha, la);
+            split8(buf[c & 1][2 * i + 1], ib, hb, lb);
             wh[4 * i + 0] = ha[0];
             wh[4 * i + 1] = ha[1];
             wh[4 * i + 2] = hb[0];
@@ -353,10 +363,10 @@ __device__ __noinline__ void load_q_split(const AttnArgs &a, const RowTile &rt, 
             wl[4 * i + 2] = lb[0];
             wl[4 * i + 3] = lb[1];
         }
-        const int left = g_first + g_count - g0;        // 8 or more, 2 (all 18) or 1 (a half)
-        if (left >= 8) {
-            tmem_st_16x256b_x8(tq_addr + kColQh + 8 * g0, wh);
-            tmem_st_16x256b_x8(tq_addr + kColQl + 8 * g0, wl);
+        const int left = g_first + g_count - g0;        // 4 or more, 2 (all 18) or 1 (a half)
+        if (left >= kC) {
+            tmem_st_16x256b_x4(tq_addr + kColQh + 8 * g0, wh);
+            tmem_st_16x256b_x4(tq_addr + kColQl + 8 * g0, wl);
         } else if (left == 2) {
             tmem_st_16x256b_x2(tq_addr + kColQh + 8 * g0, wh);
             tmem_st_16x256b_x2(tq_addr + kColQl + 8 * g0, wl);
