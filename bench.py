@@ -418,9 +418,9 @@ RUNS = {"tiny512": DenseRun, "prefix12k": DenseRun, "dense32k": DenseRun, "ragge
 # command line for that workload. A kernel change invalidates its entry: set it to
 # None until it is captured again.
 TRAFFIC = {
-    "dense32k": {"attention": None},
+    "dense32k": {"attention": 2453488384 + 2118204416},
     "sparse64k": {"indexer_topk": 76787200 + 1955591168 + 2014747904 + 63284736,
-                  "sparse_attention": None},
+                  "sparse_attention": 804065536 + 534941440},
 }
 
 
