@@ -419,7 +419,7 @@ RUNS = {"tiny512": DenseRun, "prefix12k": DenseRun, "dense32k": DenseRun, "ragge
 # None until it is captured again.
 TRAFFIC = {
     "dense32k": {"attention": 2453488384 + 2118204416},
-    "sparse64k": {"indexer_topk": 76787200 + 1955591168 + 2014747904 + 63284736,
+    "sparse64k": {"indexer_topk": None,
                   "sparse_attention": 804065536 + 534941440},
 }
 
@@ -515,7 +515,7 @@ def measure_kv_append(w, dev, reps=20):
                          "frac": gbs / float(pk["hbm_gbs"]), "traffic": None,
                          "bytes_per_token": KV_APPEND_BYTES_PER_TOKEN,
                          "peak_source": f"{src} hbm_gbs (copy, burst)",
-                         "kernel": "kv_append_kernel: one warp per token, bf16 rows -> e4m3 + fp32 scale, "
+                         "kernel": "kv_append_kernel: four tokens per warp, bf16 rows -> e4m3 + fp32 scale, "
                                    "L2 flushed before each launch"}}
 
 

@@ -384,21 +384,70 @@ __device__ __forceinline__ int pow2_at_least(int x) {
 }
 
 constexpr int TK_SAMPLE = 1024;
-constexpr int TK_PU = 4;    // float4 loads in flight per lane in the sampled passes
+constexpr int TK_CH = 16;   // consecutive scores per lane and step of a sampled pass (four float4)
+static_assert(TK_CH == 16 && TK_CH * 32 < 65536, "a warp step's counts are packed in 16 bits");
 
 __device__ __forceinline__ int bit_width(uint32_t x) { return x ? 32 - __clz(x) : 0; }
 
+// The float whose order key is t, for t != 0 (0 is the key of every NaN). The
+// key 0xFFFFFFFF maps to a NaN, which no score exceeds.
+__device__ __forceinline__ float ord_inv(uint32_t t) {
+    return __uint_as_float((t & 0x80000000u) ? (t & 0x7FFFFFFFu) : ~t);
+}
+
+// A lane's TK_CH consecutive scores from position TK_CH * c as four float4 loads
+// inside the row's float4 span (the row stride is a multiple of 4 floats); bit j
+// of vm marks position TK_CH * c + j < n.
+__device__ __forceinline__ void load_chunk(const float4 *row4, int c, bool live, int n4, int n, float4 (&v)[4],
+                                           uint32_t &vm) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int q = 4 * c + u;
+        v[u] = live && q < n4 ? row4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const int lim = live ? n - TK_CH * c : 0;
+    vm = lim >= TK_CH ? 0xFFFFu : (lim > 0 ? (1u << lim) - 1u : 0u);
+}
+
+// Bit j of wm: score j of the chunk lies above the bracket; of gm: at or above
+// its low end. Float compares with the ends' floats decide what the order keys
+// would: the keys keep the order of non-NaN floats and tie -0 with +0; a NaN
+// (key 0) is above no end and at or above the low end only when that end is
+// key 0 (lo_all).
+__device__ __forceinline__ void classify(const float4 (&v)[4], float f_hi, float f_lo, bool lo_all, uint32_t &wm,
+                                         uint32_t &gm) {
+    wm = 0;
+    gm = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (f[e] > f_hi) wm |= 1u << (4 * u + e);
+            if (lo_all || f[e] >= f_lo) gm |= 1u << (4 * u + e);
+        }
+    }
+}
+
+// A candidate (order key << 32 | position) as a digit key: its offset from the
+// bracket's low key in the top kb bits, so the digits cover only the bits in
+// which the candidates can differ.
+__device__ __forceinline__ uint64_t cand_key(uint64_t c, uint32_t t_lo, int kb) {
+    return kb ? static_cast<uint64_t>(static_cast<uint32_t>(c >> 32) - t_lo) << (64 - kb) : 0ull;
+}
+
 // Sampled path: the k-th largest score is bracketed from an evenly spaced sample
 // of 1,024 scores (ranks expected +- 4 standard deviations + 2); two passes over
-// the row follow, each warp over its own contiguous segment with no atomics and
-// no block barrier: one counts the keys above the bracket (winners) and inside
-// it (candidates), the other stores them in position order. The candidates'
-// keys are re-based to the bracket (score bits - low end, then the position's
-// significant bits), and the radix digits run over those few bits in shared
-// memory; candidates at or above the k-th key follow the winners, and the two
-// ascending runs are merged. Returns false, having written nothing, when the
-// bracket misses (too few or too many keys inside it); the caller then takes
-// the radix path. The order is key64's, so ties resolve the same way.
+// the row follow, each warp over its own contiguous segment and each lane over
+// 16 consecutive scores per step, with no atomics and no block barrier: one
+// counts the scores above the bracket (winners) and inside it (candidates), the
+// other stores the winners' positions and the candidates' (order key, position)
+// in position order. Radix digits over the bracket's significant key bits find
+// the k-th candidate score; the candidates above it and the first ones equal to
+// it (lowest positions first, as the key order wants) follow the winners, and
+// the two ascending runs are merged. Returns false, having written nothing, when
+// the bracket misses (too few or too many scores inside it); the caller then
+// takes the radix path.
 __device__ __noinline__ bool topk_sampled(const IndexerArgs &a, const float *row, const float4 *row4, int n,
                                           int32_t *out, uint64_t *cand, uint32_t *hist, int32_t *sel,
                                           uint32_t (*wcnt)[2], uint32_t *info, TkState &st, uint32_t *wsum) {
@@ -412,34 +461,28 @@ __device__ __noinline__ bool topk_sampled(const IndexerArgs &a, const float *row
     const float e = static_cast<float>(k) * TK_SAMPLE / static_cast<float>(n);
     const float mg = 4.f * sqrtf(e) + 2.f;
     const int rh = static_cast<int>(floorf(e - mg)), rl = static_cast<int>(ceilf(e + mg));
-    const uint32_t t_hi = rh >= 0 ? samp[rh] : 0xFFFFFFFFu;   // winners: ord > t_hi
-    const uint32_t t_lo = rl < TK_SAMPLE ? samp[rl] : 0u;      // candidates: t_lo <= ord <= t_hi
+    const uint32_t t_hi = rh >= 0 ? samp[rh] : 0xFFFFFFFFu;   // winners: key > t_hi
+    const uint32_t t_lo = rl < TK_SAMPLE ? samp[rl] : 0u;      // candidates: t_lo <= key <= t_hi
     __syncthreads();                                          // samp is reused as the histogram
+    if (t_hi == 0u) return false;                             // NaNs above the bracket: radix path
+    const float f_hi = ord_inv(t_hi), f_lo = t_lo ? ord_inv(t_lo) : 0.f;
+    const bool lo_all = t_lo == 0u;
     const int n4 = (n + 3) >> 2;
-    const int seg4 = (n4 + TK_NW - 1) / TK_NW;
-    const int q_lo = warp * seg4, q_hi = min(n4, q_lo + seg4);
+    const int nch = (n + TK_CH - 1) / TK_CH;
+    const int segc = (nch + TK_NW - 1) / TK_NW;
+    const int c_lo = warp * segc, c_hi = min(nch, c_lo + segc);
     // ---- pass 1: counts per warp segment ----
-    uint32_t cw = 0, cc = 0;
-    for (int q0 = q_lo; q0 < q_hi; q0 += 32 * TK_PU) {
-        float4 v[TK_PU];
-#pragma unroll
-        for (int u = 0; u < TK_PU; ++u) {
-            const int q = q0 + 32 * u + lane;
-            v[u] = q < q_hi ? row4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < TK_PU; ++u) {
-            const int q = q0 + 32 * u + lane;
-            const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int e4 = 0; e4 < 4; ++e4) {
-                const uint32_t o = ord_f32(f[e4]);
-                const bool in = q < q_hi && 4 * q + e4 < n;
-                cw += (in && o > t_hi) ? 1u : 0u;
-                cc += (in && o >= t_lo && o <= t_hi) ? 1u : 0u;
-            }
-        }
+    uint32_t cw = 0, cg = 0;
+    for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+        const int c = c0 + lane;
+        float4 v[4];
+        uint32_t vm, wm, gm;
+        load_chunk(row4, c, c < c_hi, n4, n, v, vm);
+        classify(v, f_hi, f_lo, lo_all, wm, gm);
+        cw += __popc(wm & vm);
+        cg += __popc(gm & vm);
     }
+    uint32_t cc = cg - cw;                                    // winners are at or above the low end too
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         cw += __shfl_xor_sync(0xffffffffu, cw, o);
@@ -466,58 +509,41 @@ __device__ __noinline__ bool topk_sampled(const IndexerArgs &a, const float *row
     __syncthreads();
     if (!info[2]) return false;
     const uint32_t n_win = info[0], nc = info[1];
-    // candidate key: (ord - t_lo) above the position's pb significant bits (complemented),
-    // shifted to the top of 64 bits so the standard digit sequence applies
-    const int pb = bit_width(static_cast<uint32_t>(n - 1));
-    const int kb = bit_width(t_hi - t_lo) + pb;               // <= 32 + 31
-    const uint32_t pmask = pb >= 32 ? 0xFFFFFFFFu : ((1u << pb) - 1u);
-    // ---- pass 2: winners' positions and candidates' keys, in position order ----
+    // ---- pass 2: winners' positions and candidates' (key, position), in position order ----
     uint32_t wo = wcnt[warp][0], co = wcnt[warp][1];
-    for (int q0 = q_lo; q0 < q_hi; q0 += 32 * TK_PU) {
-        float4 v[TK_PU];
+    for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+        const int c = c0 + lane;
+        float4 v[4];
+        uint32_t vm, wm, gm;
+        load_chunk(row4, c, c < c_hi, n4, n, v, vm);
+        classify(v, f_hi, f_lo, lo_all, wm, gm);
+        wm &= vm;
+        uint32_t cm = gm & ~wm & vm;
+        const uint32_t x = (static_cast<uint32_t>(__popc(cm)) << 16) | static_cast<uint32_t>(__popc(wm));
+        uint32_t incl = x;
 #pragma unroll
-        for (int u = 0; u < TK_PU; ++u) {
-            const int q = q0 + 32 * u + lane;
-            v[u] = q < q_hi ? row4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += y;
         }
-#pragma unroll
-        for (int u = 0; u < TK_PU; ++u) {
-            const int q = q0 + 32 * u + lane;
-            const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-            uint32_t wm = 0, cm = 0, o[4];
-#pragma unroll
-            for (int e4 = 0; e4 < 4; ++e4) {
-                o[e4] = ord_f32(f[e4]);
-                if (q < q_hi && 4 * q + e4 < n) {
-                    if (o[e4] > t_hi) wm |= 1u << e4;
-                    else if (o[e4] >= t_lo) cm |= 1u << e4;
-                }
-            }
-            const uint32_t x = (static_cast<uint32_t>(__popc(cm)) << 16) | static_cast<uint32_t>(__popc(wm));
-            uint32_t incl = x;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
-                if (lane >= d) incl += y;
-            }
-            const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31), ex = incl - x;
-            uint32_t pw = wo + (ex & 0xFFFFu), pc = co + (ex >> 16);
-#pragma unroll
-            for (int e4 = 0; e4 < 4; ++e4) {
-                const uint32_t s4 = static_cast<uint32_t>(4 * q + e4);
-                if (wm >> e4 & 1u) {
-                    sel[pw++] = static_cast<int32_t>(s4);
-                } else if (cm >> e4 & 1u) {
-                    const uint64_t key = (static_cast<uint64_t>(o[e4] - t_lo) << pb) | ((~s4) & pmask);
-                    cand[pc++] = key << (64 - kb);
-                }
-            }
-            wo += tot & 0xFFFFu;
-            co += tot >> 16;
+        const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31), ex = incl - x;
+        uint32_t pw = wo + (ex & 0xFFFFu), pc = co + (ex >> 16);
+        const int s0 = TK_CH * c;
+        while (wm) {
+            sel[pw++] = s0 + __ffs(wm) - 1;
+            wm &= wm - 1;
         }
+        while (cm) {     // rare: the score is read again (an L1 hit) rather than picked from registers
+            const int s = s0 + __ffs(cm) - 1;
+            cand[pc++] = (static_cast<uint64_t>(ord_f32(row[s])) << 32) | static_cast<uint32_t>(s);
+            cm &= cm - 1;
+        }
+        wo += tot & 0xFFFFu;
+        co += tot >> 16;
     }
-    // ---- the k-th key among the candidates (digits over the kb significant bits) ----
+    // ---- the k-th candidate score: digits over the kb bits in which candidates differ ----
     const uint32_t need = static_cast<uint32_t>(k) - n_win;
+    const int kb = bit_width(t_hi - t_lo);
     if (tid == 0) {
         st.prefix = 0;
         st.bits = 0;
@@ -525,49 +551,61 @@ __device__ __noinline__ bool topk_sampled(const IndexerArgs &a, const float *row
     }
     __syncthreads();
     if (need > 0) {
-        const int widths[6] = {12, 12, 8, 12, 12, 8};
+        const int widths[3] = {12, 12, 8};   // 32 bits cover any kb
         int di = 0;
-        while (di < 6 && st.bits < kb) {
+        while (di < 3 && st.bits < kb) {
             const int width = widths[di++], shift = 64 - st.bits - width;
             const uint64_t pf = st.prefix;
             const int bb = st.bits;
             for (int d = tid; d < (1 << width); d += TK_NT) hist[d] = 0;
             __syncthreads();
             for (uint32_t i = tid; i < nc; i += TK_NT) {
-                const uint64_t key = cand[i];
+                const uint64_t key = cand_key(cand[i], t_lo, kb);
                 hist_add(hist, prefix_match(key, pf, bb), static_cast<uint32_t>((key >> shift) & ((1u << width) - 1)));
             }
             __syncthreads();
             pick(hist, width, shift, st, wsum);
         }
-        if (st.bits < kb) {   // 64 bits cover any kb; unreachable
+        if (st.bits < kb) {   // every digit finds its bin; unreachable
             topk_fail(a, out);
             return true;
         }
-        // ---- candidates at or above the k-th key, in order, after the winners ----
+        // ---- candidates above the k-th score, and the first `take` equal to it, after the winners ----
         const uint64_t kth = st.prefix;
-        uint32_t base = n_win;
+        const uint32_t take = st.krem;
+        uint32_t base_a = 0, base_e = 0;
         for (uint32_t c0 = 0; c0 < nc; c0 += 4 * TK_NT) {
             const uint32_t i0 = c0 + 4 * tid;
-            uint32_t f = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (i0 + j < nc && cand[i0 + j] >= kth) f |= 1u << j;
-            uint32_t tot;
-            uint32_t o = base + block_excl_scan(static_cast<uint32_t>(__popc(f)), wsum, tot);
+            uint32_t fa = 0, fe = 0;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (f >> j & 1u) {
-                    if (o < static_cast<uint32_t>(k)) {
-                        const uint32_t lowbits = static_cast<uint32_t>(cand[i0 + j] >> (64 - kb)) & pmask;
-                        sel[o] = static_cast<int32_t>((~lowbits) & pmask);
-                    }
-                    ++o;
+                if (i0 + j < nc) {
+                    const uint64_t key = cand_key(cand[i0 + j], t_lo, kb);
+                    if (key > kth) fa |= 1u << j;
+                    else if (key == kth) fe |= 1u << j;
                 }
             }
-            base += tot;
+            uint32_t tot;
+            const uint32_t ex = block_excl_scan((static_cast<uint32_t>(__popc(fe)) << 16) |
+                                                    static_cast<uint32_t>(__popc(fa)), wsum, tot);
+            uint32_t ra = base_a + (ex & 0xFFFFu), re = base_e + (ex >> 16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (fa >> j & 1u) {
+                    const uint32_t o = n_win + ra + min(re, take);
+                    if (o < static_cast<uint32_t>(k)) sel[o] = static_cast<int32_t>(cand[i0 + j] & 0xFFFFFFFFu);
+                    ++ra;
+                } else if (fe >> j & 1u) {
+                    const uint32_t o = n_win + ra + re;
+                    if (re < take && o < static_cast<uint32_t>(k))
+                        sel[o] = static_cast<int32_t>(cand[i0 + j] & 0xFFFFFFFFu);
+                    ++re;
+                }
+            }
+            base_a += tot & 0xFFFFu;
+            base_e += tot >> 16;
         }
-        if (base != static_cast<uint32_t>(k)) {
+        if (base_a + take != need || base_e < take) {   // the digits guarantee both; report instead of guessing
             topk_fail(a, out);
             return true;
         }

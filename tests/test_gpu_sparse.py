@@ -83,6 +83,36 @@ def test_indexer_per_token_weights():
     assert np.array_equal(np.sort(ref, axis=1), got)
 
 
+def test_indexer_signed_scores_and_zero_ties():
+    """Per-token weights of both signs make over a quarter of the scores
+    negative; 40% of the key rows are zero, so every row holds a block of zero
+    scores, and with k near half the row the cut falls inside that block for
+    most rows: the lower positions must go first."""
+    import torch
+    pb = Problem([64, 40], [2000, 1900], 16, seed=34, with_indexer=True)
+    rng = np.random.default_rng(34)
+    T = pb.ps.total_q
+    wt = (rng.choice([-1.0, 1.0], (T, 64)) * 2.0 ** -rng.integers(0, 5, (T, 64))).astype(np.float32)
+    ki = pb.ki.reshape(-1, 128).copy()
+    ki[rng.random(ki.shape[0]) < 0.4] = 0                        # e4m3 code 0 is +0
+    pb.ki = ki.reshape(pb.ki.shape)
+    d = pb.device()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    from mla_prefill_attention_gb300 import mla_indexer_topk
+    idx = mla_indexer_topk(d["seqs"], d["qi"], torch.from_numpy(wt).cuda(), 64, d["ki"], d["kis"], 1000, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    toks = np.arange(T)
+    ref, sc = O.indexer_topk(pb.ps, pb.qi, wt, 64, toks, pb.ki, pb.kis, 1000, want_scores=True, ctx_cap=2100)
+    # the case is what it claims: for most rows the 1000th largest score is a zero
+    kth = np.array([np.sort(sc[t, :int(pb.ps.prefix_lens[0 if t < 64 else 1]) + (t if t < 64 else t - 64) + 1])[::-1][999]
+                    for t in toks])
+    assert np.mean(kth == 0.0) > 0.5 and np.any(sc[~np.isnan(sc)] < 0)
+    got = idx.cpu().numpy()
+    assert np.array_equal(np.sort(ref, axis=1), np.sort(got, axis=1))
+    assert np.all(np.diff(got, axis=1) > 0)
+
+
 def test_indexer_ties_go_to_lower_position():
     """Keys repeat three rows, so whole groups of scores tie at the cut."""
     import torch
