@@ -29,9 +29,10 @@
 // columns) so the MMA of tile i+1 overlaps the epilogue of tile i. Fourteen
 // warps leave each thread 128 registers, enough for its token's 64 head weights
 // (as 32 register pairs, loaded once), so the head sum reads no memory: per
-// tile a thread takes its key's 64 values in two halves of 32 and runs paired
-// f32 FMAs (fma.rn.f32x2: two IEEE fmas, so the same result as scalar ones)
-// with four independent accumulator pairs.
+// tile a thread takes its key's 64 values in four chunks of 16, the load of the
+// next chunk in flight while one is reduced, and runs paired f32 FMAs
+// (fma.rn.f32x2: two IEEE fmas, so the same result as scalar ones) with four
+// independent accumulator pairs.
 // Every wait is bounded and reports MLA_DEVERR_TIMEOUT.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -220,21 +221,27 @@ __global__ void __launch_bounds__(NT, 1)
             if (!wait_bar(sh, a.dev_err, B_D_FULL + db, (i >> 1) & 1)) break;
             fence_after_sync();
             uint64_t acc[4] = {0, 0, 0, 0};
+            // heads in four chunks of 16 columns, the load of chunk c+1 in flight
+            // while chunk c is reduced
+            const uint32_t col0 = tmem + lane_addr + kDCols * db + 64u * j;
+            uint32_t d[2][16];
+            tmem_ld16(col0, d[0]);
+            tmem_ld_wait();
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {     // heads 32*half .. +31
-                uint32_t d[32];
-                tmem_ld32(tmem + lane_addr + kDCols * db + 64u * j + 32u * half, d);
-                tmem_ld_wait();
-                if (half == 1) {   // both halves read: the buffer goes back to the MMA
+            for (int c = 0; c < 4; ++c) {              // heads 16c .. 16c+15
+                if (c < 3) tmem_ld16(col0 + 16u * (c + 1), d[(c + 1) & 1]);
+#pragma unroll
+                for (int h4 = 0; h4 < 4; ++h4) {
+                    const uint32_t *x = d[c & 1] + 4 * h4;
+                    const int w2 = 8 * c + 2 * h4;
+                    ffma2(acc[2 * (h4 & 1)], wp[w2], pack2(relu_bits(x[0]), relu_bits(x[1])));
+                    ffma2(acc[2 * (h4 & 1) + 1], wp[w2 + 1], pack2(relu_bits(x[2]), relu_bits(x[3])));
+                }
+                if (c < 3) tmem_ld_wait();
+                if (c == 2) {      // every column read: the buffer goes back to the MMA
                     fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_D_EMPTY + db]));
-                }
-#pragma unroll
-                for (int h4 = 0; h4 < 8; ++h4) {
-                    const int w2 = 16 * half + 2 * h4;
-                    ffma2(acc[2 * (h4 & 1)], wp[w2], pack2(relu_bits(d[4 * h4 + 0]), relu_bits(d[4 * h4 + 1])));
-                    ffma2(acc[2 * (h4 & 1) + 1], wp[w2 + 1], pack2(relu_bits(d[4 * h4 + 2]), relu_bits(d[4 * h4 + 3])));
                 }
             }
             const float sc = (sum2(acc[0]) + sum2(acc[1])) + (sum2(acc[2]) + sum2(acc[3]));
