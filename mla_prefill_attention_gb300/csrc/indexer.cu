@@ -174,8 +174,11 @@ __device__ __forceinline__ void pick_digit(const uint32_t *hist, int width, int 
 }
 
 __device__ __noinline__ void pick(const uint32_t *hist, int width, int shift, TkState &st, uint32_t *wsum) {
-    if (width == 12) pick_digit<4096 / TK_NT>(hist, width, shift, st, wsum);
-    else pick_digit<1>(hist, width, shift, st, wsum);
+    static_assert(TK_NT == 512, "bins per thread assume 512 threads");
+    if (width == 12) pick_digit<8>(hist, width, shift, st, wsum);
+    else if (width == 11) pick_digit<4>(hist, width, shift, st, wsum);
+    else if (width == 10) pick_digit<2>(hist, width, shift, st, wsum);
+    else pick_digit<1>(hist, width, shift, st, wsum);   // up to 512 bins, one per thread
 }
 
 __device__ __forceinline__ void topk_fail(const IndexerArgs &a, int32_t *out) {
@@ -377,12 +380,6 @@ __device__ __forceinline__ void bitonic_sort(T *v, int P) {
     }
 }
 
-__device__ __forceinline__ int pow2_at_least(int x) {
-    int p = 2;
-    while (p < x) p <<= 1;
-    return p;
-}
-
 constexpr int TK_SAMPLE = 1024;
 constexpr int TK_CH = 16;   // consecutive scores per lane and step of a sampled pass (four float4)
 static_assert(TK_CH == 16 && TK_CH * 32 < 65536, "a warp step's counts are packed in 16 bits");
@@ -551,7 +548,17 @@ __device__ __noinline__ bool topk_sampled(const IndexerArgs &a, const float *row
     }
     __syncthreads();
     if (need > 0) {
-        const int widths[3] = {12, 12, 8};   // 32 bits cover any kb
+        // kb bits in at most three digits of at most 12 bits (4,096 bins):
+        // one for kb <= 12, two near-equal ones for kb <= 24, else 12 + 12 + rest
+        int widths[3] = {kb, 0, 0};
+        if (kb > 24) {
+            widths[0] = 12;
+            widths[1] = 12;
+            widths[2] = kb - 24;
+        } else if (kb > 12) {
+            widths[0] = kb - kb / 2;
+            widths[1] = kb / 2;
+        }
         int di = 0;
         while (di < 3 && st.bits < kb) {
             const int width = widths[di++], shift = 64 - st.bits - width;
