@@ -5,8 +5,8 @@
 // earlier token to pick 2,048; footnote 3: an indexer key is 128 FP8 values
 // plus a 4-byte scale.)
 //
-// One CTA scores 3 query tokens (x 64 heads) against a chunk of keys, 128 keys
-// at a time:
+// One CTA scores 3 query tokens (x 64 heads) against a chunk of keys (2,048 to
+// 32,768, chosen by the host), 128 keys at a time:
 //
 //   D[key][64 j + h] = k_key . q_{t_j,h}    tcgen05.mma e4m3 x e4m3 -> f32,
 //                                           M = 128 keys, N = 192 = 3 tokens x 64
@@ -57,7 +57,7 @@ constexpr int kQBytes = TOK * kHidx * kDidx;       // 24 KB
 constexpr int kTileBytes = KT * kDidx;             // 16 KB
 constexpr int kDynSmem = 1024 + kQBytes + STAGES * kTileBytes;
 constexpr long long kWaitCycles = 200000000LL;
-static_assert(kIdxKeyChunk % KT == 0 && kPage % KT == 0, "key tiles must not straddle pages or chunks");
+static_assert(kIdxKeyChunkMin % KT == 0 && kPage % KT == 0, "key tiles must not straddle pages or chunks");
 
 enum Bar {
     B_Q_FULL = 0,
@@ -110,8 +110,8 @@ __global__ void __launch_bounds__(NT, 1)
     const int b = it.x, i0 = it.y, ntok = it.z;
     const int q0 = __ldg(a.cu_seqlens + b), P = __ldg(a.prefix_lens + b);
     const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.max_blocks;
-    const int k_lo = it.w * kIdxKeyChunk;
-    const int k_hi = min(k_lo + kIdxKeyChunk, P + i0 + ntok);       // exclusive
+    const int k_lo = it.w * a.key_chunk;
+    const int k_hi = min(k_lo + a.key_chunk, P + i0 + ntok);        // exclusive
     const int n_tiles = (k_hi - k_lo + KT - 1) / KT;
 
     if (tid == 0) {

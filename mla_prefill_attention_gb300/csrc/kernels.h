@@ -42,6 +42,7 @@ struct IndexerArgs {
     int32_t topk;
     int32_t *idx_out;            // [Tq, topk]
     int32_t *dev_err;
+    int32_t key_chunk;           // keys per indexer work item (a power of two, 2,048 .. 32,768)
 };
 
 // Dense attention on e4m3 operands (kind::f8f6f4). Work item: x = sequence,
@@ -54,12 +55,15 @@ bool encode_kv_tmap(CUtensorMap *map, const uint8_t *kv, int32_t num_blocks);
 cudaError_t launch_sparse_f8(const AttnArgs &a, int64_t n_tokens, cudaStream_t st);
 
 // Indexer score work item: x = sequence, y = first new token (in-sequence),
-// z = token count (<= kIdxTokensPerCta), w = key chunk. tmap_k: the key cache as
+// z = token count (<= kIdxTokensPerCta), w = key chunk (keys w * key_chunk ..
+// +key_chunk; the host takes the longest chunk, from kIdxKeyChunkMax down to
+// kIdxKeyChunkMin, that still gives every SM several items). tmap_k: the key cache as
 // [num_blocks * 256 rows][128 B]; tmap_q: the queries as [Tq * 64 rows][128 B];
 // both with 128-byte-wide boxes and the 128-byte swizzle (boxes of 128 key rows and of
 // kIdxTokensPerCta * 64 query rows).
 constexpr int kIdxTokensPerCta = 3;
-constexpr int kIdxKeyChunk = 8192;
+constexpr int kIdxKeyChunkMax = 32768;
+constexpr int kIdxKeyChunkMin = 2048;
 cudaError_t launch_indexer_scores_tc(const IndexerArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_k,
                                      const CUtensorMap &tmap_q, cudaStream_t st);
 cudaError_t launch_topk(const IndexerArgs &a, int64_t n_tokens, cudaStream_t st);

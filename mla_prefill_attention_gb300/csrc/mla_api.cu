@@ -105,18 +105,49 @@ int64_t max_context(const mla_seqs_t *s) {
     return m;
 }
 
-std::vector<int4> indexer_schedule(const mla_seqs_t *s) {
+// Work items of the indexer: (sequence, first token, token count, key chunk)
+// for every group of kIdxTokensPerCta tokens and every chunk of `chunk` keys
+// they can see.
+int64_t indexer_items(const mla_seqs_t *s, int chunk) {
+    int64_t n = 0;
+    for (int b = 0; b < s->batch; ++b) {
+        const int t = s->cu_seqlens_q_host[b + 1] - s->cu_seqlens_q_host[b];
+        const int P = s->prefix_lens_host[b];
+        for (int i0 = 0; i0 < t; i0 += mla::kIdxTokensPerCta) {
+            const int keys = P + i0 + std::min(mla::kIdxTokensPerCta, t - i0);
+            n += (keys + chunk - 1) / chunk;
+        }
+    }
+    return n;
+}
+
+std::vector<int4> indexer_schedule(const mla_seqs_t *s, int chunk) {
     std::vector<int4> items;
+    items.reserve(static_cast<size_t>(indexer_items(s, chunk)));
     for (int b = 0; b < s->batch; ++b) {
         const int t = s->cu_seqlens_q_host[b + 1] - s->cu_seqlens_q_host[b];
         const int P = s->prefix_lens_host[b];
         for (int i0 = 0; i0 < t; i0 += mla::kIdxTokensPerCta) {
             const int nt = std::min(mla::kIdxTokensPerCta, t - i0);
             const int keys = P + i0 + nt;
-            for (int c = 0; c * mla::kIdxKeyChunk < keys; ++c) items.push_back(make_int4(b, i0, nt, c));
+            for (int c = 0; c * chunk < keys; ++c) items.push_back(make_int4(b, i0, nt, c));
         }
     }
     return items;
+}
+
+// Longer key chunks spread each CTA's start (TMEM allocation, barriers, the
+// query load, the first tiles of the pipeline) over more tiles; shorter ones
+// give more CTAs. Take the longest chunk that still gives every SM at least
+// eight items (one CTA per SM), so the last wave stays a small share.
+int indexer_key_chunk(const mla_seqs_t *s) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        sms = 1;
+    int chunk = mla::kIdxKeyChunkMax;
+    while (chunk > mla::kIdxKeyChunkMin && indexer_items(s, chunk) < 8 * static_cast<int64_t>(sms)) chunk /= 2;
+    return chunk;
 }
 
 // fp32 score row per query token; rows start 16-byte aligned (the top-k reads them 4 at a time)
@@ -202,7 +233,9 @@ size_t mla_workspace_size(mla_op_t op, const mla_seqs_t *seqs, int32_t num_heads
             if (!heads_ok(num_heads)) return 0;
             return round_up(dense_schedule(seqs, num_heads).size() * sizeof(int4), kWsAlign);
         case MLA_OP_INDEXER:
-            return indexer_score_bytes(seqs) + round_up(indexer_schedule(seqs).size() * sizeof(int4), kWsAlign);
+            // room for the work list at the shortest key chunk, whatever chunk the call takes
+            return indexer_score_bytes(seqs) +
+                   round_up(static_cast<size_t>(indexer_items(seqs, mla::kIdxKeyChunkMin)) * sizeof(int4), kWsAlign);
         case MLA_OP_SPARSE:
             return 0;
     }
@@ -256,7 +289,8 @@ mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, co
     const int64_t tq = seqs->cu_seqlens_q_host[seqs->batch];
     if (tq == 0) return MLA_OK;
     if (tq * 64 > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "too many query tokens for the indexer (Tq * 64 > 2^31 - 1)");
-    const std::vector<int4> work = indexer_schedule(seqs);
+    const int key_chunk = indexer_key_chunk(seqs);
+    const std::vector<int4> work = indexer_schedule(seqs, key_chunk);
     const size_t sbytes = indexer_score_bytes(seqs);
     const size_t need = sbytes + round_up(work.size() * sizeof(int4), kWsAlign);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
@@ -285,6 +319,7 @@ mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, co
     a.topk = topk;
     a.idx_out = idx_out;
     a.dev_err = dev_err;
+    a.key_chunk = key_chunk;
     CUtensorMap tmap_k, tmap_q;
     if (!encode_rows128(&tmap_k, ki_e4m3, static_cast<uint64_t>(seqs->num_blocks) * 256, 128) ||
         !encode_rows128(&tmap_q, qi_e4m3, static_cast<uint64_t>(tq) * 64, mla::kIdxTokensPerCta * 64))
