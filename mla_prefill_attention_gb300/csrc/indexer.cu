@@ -426,6 +426,60 @@ __device__ __forceinline__ void classify(const float4 (&v)[4], float f_hi, float
     }
 }
 
+// One step of a warp's pass over the row: lane chunk c classified into winner
+// and candidate masks, and the warp scan of their counts (winners in the low 16
+// bits, candidates in the high 16): ex counts the lower lanes, tot the warp.
+__device__ __forceinline__ void pass_step(const float4 *row4, int c, bool live, int n4, int n, float f_hi, float f_lo,
+                                          bool lo_all, uint32_t &wm, uint32_t &cm, uint32_t &ex, uint32_t &tot) {
+    float4 v[4];
+    uint32_t vm, gm;
+    load_chunk(row4, c, live, n4, n, v, vm);
+    classify(v, f_hi, f_lo, lo_all, wm, gm);
+    wm &= vm;
+    cm = gm & ~wm & vm;
+    const uint32_t x = (static_cast<uint32_t>(__popc(cm)) << 16) | static_cast<uint32_t>(__popc(wm));
+    const int lane = threadIdx.x & 31;
+    uint32_t incl = x;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+    }
+    tot = __shfl_sync(0xffffffffu, incl, 31);
+    ex = incl - x;
+}
+
+// A lane's winners (positions) from slot pw and candidates ((order key,
+// position); the score is read again, an L1 hit, rather than picked from
+// registers) from slot pc, in position order; slots at or past wcap / ccap are
+// not written.
+__device__ __forceinline__ void put_hits(const float *row, int s0, uint32_t wm, uint32_t cm, uint32_t pw, uint32_t pc,
+                                         uint32_t wcap, uint32_t ccap, int32_t *wdst, uint64_t *cdst) {
+    while (wm) {
+        if (pw < wcap) wdst[pw] = s0 + __ffs(wm) - 1;
+        ++pw;
+        wm &= wm - 1;
+    }
+    while (cm) {
+        if (pc < ccap) {
+            const int s = s0 + __ffs(cm) - 1;
+            cdst[pc] = (static_cast<uint64_t>(ord_f32(row[s])) << 32) | static_cast<uint32_t>(s);
+        }
+        ++pc;
+        cm &= cm - 1;
+    }
+}
+
+// The warp whose run of final slots holds slot d: the last w with first slot
+// <= d (a warp with an empty run shares its first slot with the next warp).
+__device__ __forceinline__ int run_owner(const uint32_t (*first)[2], int which, uint32_t d) {
+    int w = 0;
+#pragma unroll
+    for (int step = TK_NW / 2; step > 0; step >>= 1)
+        if (w + step < TK_NW && first[w + step][which] <= d) w += step;
+    return w;
+}
+
 // A candidate (order key << 32 | position) as a digit key: its offset from the
 // bracket's low key in the top kb bits, so the digits cover only the bits in
 // which the candidates can differ.
@@ -434,12 +488,13 @@ __device__ __forceinline__ uint64_t cand_key(uint64_t c, uint32_t t_lo, int kb) 
 }
 
 // Sampled path: the k-th largest score is bracketed from an evenly spaced sample
-// of 1,024 scores (ranks expected +- 4 standard deviations + 2); two passes over
-// the row follow, each warp over its own contiguous segment and each lane over
-// 16 consecutive scores per step, with no atomics and no block barrier: one
-// counts the scores above the bracket (winners) and inside it (candidates), the
-// other stores the winners' positions and the candidates' (order key, position)
-// in position order. Radix digits over the bracket's significant key bits find
+// of 1,024 scores (ranks expected +- 4 standard deviations + 2); one pass over
+// the row follows, each warp over its own contiguous segment and each lane over
+// 16 consecutive scores per step, with no atomics and no block barrier: the
+// winners (above the bracket) and candidates (inside it) go, as positions and
+// as (order key, position), in position order into slots of the warp's own and
+// are then compacted; a second, ordered pass runs only when a warp has more
+// than its slots hold. Radix digits over the bracket's significant key bits find
 // the k-th candidate score; the candidates above it and the first ones equal to
 // it (lowest positions first, as the key order wants) follow the winners, and
 // the two ascending runs are merged. Returns false, having written nothing, when
@@ -468,33 +523,31 @@ __device__ __noinline__ bool topk_sampled(const IndexerArgs &a, const float *row
     const int nch = (n + TK_CH - 1) / TK_CH;
     const int segc = (nch + TK_NW - 1) / TK_NW;
     const int c_lo = warp * segc, c_hi = min(nch, c_lo + segc);
-    // ---- pass 1: counts per warp segment ----
-    uint32_t cw = 0, cg = 0;
+    // ---- one pass: each warp puts its winners' positions and its candidates'
+    // (key, position) in position order into slots of its own; the counts run on
+    // past the slots, so an overflow is seen ----
+    constexpr uint32_t kWinSlots = TK_SEL / TK_NW, kCandSlots = TK_CAP / TK_NW;
+    uint32_t wn = 0, cn = 0;
     for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
         const int c = c0 + lane;
-        float4 v[4];
-        uint32_t vm, wm, gm;
-        load_chunk(row4, c, c < c_hi, n4, n, v, vm);
-        classify(v, f_hi, f_lo, lo_all, wm, gm);
-        cw += __popc(wm & vm);
-        cg += __popc(gm & vm);
-    }
-    uint32_t cc = cg - cw;                                    // winners are at or above the low end too
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        cw += __shfl_xor_sync(0xffffffffu, cw, o);
-        cc += __shfl_xor_sync(0xffffffffu, cc, o);
+        uint32_t wm, cm, ex, tot;
+        pass_step(row4, c, c < c_hi, n4, n, f_hi, f_lo, lo_all, wm, cm, ex, tot);
+        put_hits(row, TK_CH * c, wm, cm, wn + (ex & 0xFFFFu), cn + (ex >> 16), kWinSlots, kCandSlots,
+                 sel + warp * kWinSlots, cand + warp * kCandSlots);
+        wn += tot & 0xFFFFu;
+        cn += tot >> 16;
     }
     if (lane == 0) {
-        wcnt[warp][0] = cw;
-        wcnt[warp][1] = cc;
+        wcnt[warp][0] = wn;
+        wcnt[warp][1] = cn;
     }
     __syncthreads();
     if (tid == 0) {
-        uint32_t tw = 0, tc = 0;
+        uint32_t tw = 0, tc = 0, fits = 1;
         for (int w = 0; w < TK_NW; ++w) {
             const uint32_t x = wcnt[w][0], y = wcnt[w][1];
-            wcnt[w][0] = tw;
+            if (x > kWinSlots || y > kCandSlots) fits = 0;
+            wcnt[w][0] = tw;                                  // from here on: the warp's first final slot
             wcnt[w][1] = tc;
             tw += x;
             tc += y;
@@ -502,41 +555,46 @@ __device__ __noinline__ bool topk_sampled(const IndexerArgs &a, const float *row
         info[0] = tw;
         info[1] = tc;
         info[2] = (tw <= static_cast<uint32_t>(k) && static_cast<uint32_t>(k) <= tw + tc && tc <= TK_CAP) ? 1u : 0u;
+        info[3] = fits;
     }
     __syncthreads();
     if (!info[2]) return false;
     const uint32_t n_win = info[0], nc = info[1];
-    // ---- pass 2: winners' positions and candidates' (key, position), in position order ----
-    uint32_t wo = wcnt[warp][0], co = wcnt[warp][1];
-    for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-        const int c = c0 + lane;
-        float4 v[4];
-        uint32_t vm, wm, gm;
-        load_chunk(row4, c, c < c_hi, n4, n, v, vm);
-        classify(v, f_hi, f_lo, lo_all, wm, gm);
-        wm &= vm;
-        uint32_t cm = gm & ~wm & vm;
-        const uint32_t x = (static_cast<uint32_t>(__popc(cm)) << 16) | static_cast<uint32_t>(__popc(wm));
-        uint32_t incl = x;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d) incl += y;
+    if (info[3]) {
+        // ---- compaction: final slot d takes entry d - first(w) of the warp w whose
+        // run holds d. Every entry moves down (a warp's first final slot is at most
+        // its own first slot), so in rounds of TK_NT final slots a round's stores
+        // land below every later round's sources; one barrier inside a round
+        // separates its loads from its stores ----
+        const uint32_t rounds = (max(n_win, nc) + TK_NT - 1) / TK_NT;
+        for (uint32_t r = 0; r < rounds; ++r) {
+            const uint32_t d = r * TK_NT + tid;
+            int32_t wv = 0;
+            uint64_t cv = 0;
+            if (d < n_win) {
+                const int w = run_owner(wcnt, 0, d);
+                wv = sel[w * kWinSlots + (d - wcnt[w][0])];
+            }
+            if (d < nc) {
+                const int w = run_owner(wcnt, 1, d);
+                cv = cand[w * kCandSlots + (d - wcnt[w][1])];
+            }
+            __syncthreads();
+            if (d < n_win) sel[d] = wv;
+            if (d < nc) cand[d] = cv;
         }
-        const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31), ex = incl - x;
-        uint32_t pw = wo + (ex & 0xFFFFu), pc = co + (ex >> 16);
-        const int s0 = TK_CH * c;
-        while (wm) {
-            sel[pw++] = s0 + __ffs(wm) - 1;
-            wm &= wm - 1;
+    } else {
+        // ---- a warp's slots overflowed: a second pass writes every entry straight
+        // to its final slot ----
+        uint32_t wo = wcnt[warp][0], co = wcnt[warp][1];
+        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+            const int c = c0 + lane;
+            uint32_t wm, cm, ex, tot;
+            pass_step(row4, c, c < c_hi, n4, n, f_hi, f_lo, lo_all, wm, cm, ex, tot);
+            put_hits(row, TK_CH * c, wm, cm, wo + (ex & 0xFFFFu), co + (ex >> 16), TK_SEL, TK_CAP, sel, cand);
+            wo += tot & 0xFFFFu;
+            co += tot >> 16;
         }
-        while (cm) {     // rare: the score is read again (an L1 hit) rather than picked from registers
-            const int s = s0 + __ffs(cm) - 1;
-            cand[pc++] = (static_cast<uint64_t>(ord_f32(row[s])) << 32) | static_cast<uint32_t>(s);
-            cm &= cm - 1;
-        }
-        wo += tot & 0xFFFFu;
-        co += tot >> 16;
     }
     // ---- the k-th candidate score: digits over the kb bits in which candidates differ ----
     const uint32_t need = static_cast<uint32_t>(k) - n_win;

@@ -113,6 +113,36 @@ def test_indexer_signed_scores_and_zero_ties():
     assert np.all(np.diff(got, axis=1) > 0)
 
 
+def test_indexer_clustered_winners():
+    """The largest scores all sit in the first 1,500 positions (their key scales
+    are 2^10 times the others, exact), so the first warp's stretch of the row
+    holds far more selected positions than an even spread would put there: the
+    sets must still match the oracle. The premise is checked on the oracle's
+    scores with the sampled bracket (1,024 evenly spaced scores, ranks k*1024/n
+    -+ (4 sqrt(.) + 2)): the first sixteenth of the row holds more than 128 of
+    the scores above the bracket."""
+    pb = Problem([16], [30000], 16, seed=35, with_indexer=True)
+    bt = pb.ps.block_table[0]
+    kis = pb.kis.copy()
+    for s in range(1500):
+        kis[bt[s // 256], s % 256] *= 1024.0
+    pb.kis = kis
+    d = pb.device()
+    k = 1000
+    idx = run_indexer(pb, d, k)
+    toks = np.arange(16)
+    ref, sc = O.indexer_topk(pb.ps, pb.qi, pb.w, 0, toks, pb.ki, pb.kis, k, want_scores=True, ctx_cap=30016)
+    n = 30001
+    row = sc[0, :n]
+    samp = np.sort(row[(np.arange(1024) * n) // 1024])[::-1]
+    e = k * 1024 / n
+    t_hi = samp[int(np.floor(e - (4 * np.sqrt(e) + 2)))]
+    assert np.count_nonzero(row[: n // 16] > t_hi) > 128
+    got = idx.cpu().numpy()
+    assert np.array_equal(np.sort(ref, axis=1), np.sort(got, axis=1))
+    assert np.all(np.diff(got, axis=1) > 0)
+
+
 def test_indexer_ties_go_to_lower_position():
     """Keys repeat three rows, so whole groups of scores tie at the cut."""
     import torch
