@@ -481,10 +481,10 @@ __device__ __forceinline__ int run_owner(const uint32_t (*first)[2], int which, 
 }
 
 // A candidate (order key << 32 | position) as a digit key: its offset from the
-// bracket's low key in the top kb bits, so the digits cover only the bits in
-// which the candidates can differ.
-__device__ __forceinline__ uint64_t cand_key(uint64_t c, uint32_t t_lo, int kb) {
-    return kb ? static_cast<uint64_t>(static_cast<uint32_t>(c >> 32) - t_lo) << (64 - kb) : 0ull;
+// bracket's low key in the top kb bits (kb <= 32), so the digits cover only the
+// bits in which the candidates can differ.
+__device__ __forceinline__ uint32_t cand_key(uint64_t c, uint32_t t_lo, int kb) {
+    return kb ? (static_cast<uint32_t>(c >> 32) - t_lo) << (32 - kb) : 0u;
 }
 
 // Sampled path: the k-th largest score is bracketed from an evenly spaced sample
@@ -618,25 +618,24 @@ __device__ __noinline__ bool topk_sampled(const IndexerArgs &a, const float *row
             widths[1] = kb / 2;
         }
         int di = 0;
-        while (di < 3 && st.bits < kb) {
-            const int width = widths[di++], shift = 64 - st.bits - width;
-            const uint64_t pf = st.prefix;
-            const int bb = st.bits;
+        while (di < 3 && st.bits < kb) {     // 32-bit keys: the state's prefix holds them in its top half
+            const int width = widths[di++], bb = st.bits, shift = 32 - bb - width;
+            const uint32_t pf = static_cast<uint32_t>(st.prefix >> 32);
             for (int d = tid; d < (1 << width); d += TK_NT) hist[d] = 0;
             __syncthreads();
             for (uint32_t i = tid; i < nc; i += TK_NT) {
-                const uint64_t key = cand_key(cand[i], t_lo, kb);
-                hist_add(hist, prefix_match(key, pf, bb), static_cast<uint32_t>((key >> shift) & ((1u << width) - 1)));
+                const uint32_t key = cand_key(cand[i], t_lo, kb);
+                hist_add(hist, bb == 0 || (key >> (32 - bb)) == (pf >> (32 - bb)), (key >> shift) & ((1u << width) - 1));
             }
             __syncthreads();
-            pick(hist, width, shift, st, wsum);
+            pick(hist, width, shift + 32, st, wsum);
         }
         if (st.bits < kb) {   // every digit finds its bin; unreachable
             topk_fail(a, out);
             return true;
         }
         // ---- candidates above the k-th score, and the first `take` equal to it, after the winners ----
-        const uint64_t kth = st.prefix;
+        const uint32_t kth = static_cast<uint32_t>(st.prefix >> 32);
         const uint32_t take = st.krem;
         uint32_t base_a = 0, base_e = 0;
         for (uint32_t c0 = 0; c0 < nc; c0 += 4 * TK_NT) {
@@ -645,7 +644,7 @@ __device__ __noinline__ bool topk_sampled(const IndexerArgs &a, const float *row
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 if (i0 + j < nc) {
-                    const uint64_t key = cand_key(cand[i0 + j], t_lo, kb);
+                    const uint32_t key = cand_key(cand[i0 + j], t_lo, kb);
                     if (key > kth) fa |= 1u << j;
                     else if (key == kth) fe |= 1u << j;
                 }
