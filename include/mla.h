@@ -71,7 +71,8 @@ typedef enum {
 typedef enum {
     MLA_OP_DENSE = 0,
     MLA_OP_INDEXER = 1,
-    MLA_OP_SPARSE = 2
+    MLA_OP_SPARSE = 2,
+    MLA_OP_DENSE_HOST = 3   /* mla_prefill_dense_host, any chunk count */
 } mla_op_t;
 
 /* Ragged batch of sequences over one paged cache (256-token pages). */
@@ -162,6 +163,42 @@ mla_status_t mla_prefill_sparse(const mla_seqs_t *seqs, const void *q_bf16, int3
 mla_status_t mla_prefill_dense_static(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads,
                                       const uint8_t *kv_e4m3, const float *kv_scale, float sm_scale,
                                       void *out_bf16, float *lse, int32_t *dev_err, cudaStream_t stream);
+
+/* Most pieces mla_prefill_dense_host cuts the new tokens into. */
+#define MLA_DENSE_HOST_MAX_CHUNKS 64
+
+/* Dense prefill from host memory to host memory, with the copies overlapped
+ * with the attention. This entry point has no counterpart on the source pages:
+ * it serves callers whose queries and cache sit in host memory. It computes
+ * exactly what mla_prefill_dense computes (the same tiles with the same
+ * arithmetic, so the results are identical) and leaves the results in host
+ * memory:
+ *   1. the cache (kv_host, kv_scale_host: num_blocks * 256 rows) is copied to
+ *      kv_e4m3 / kv_scale;
+ *   2. the new tokens are cut into n_chunks near-equal pieces of consecutive
+ *      tokens (moved to tile boundaries: 64 rows of token x head), and each
+ *      piece's query rows are copied from q_host to q_bf16 (same [Tq, H, 576]
+ *      layout), its attention runs as soon as its rows have arrived, and its
+ *      out and lse rows are copied back to out_host / lse_host ([Tq, H, 512]
+ *      bf16, [Tq, H] f32) as soon as it has finished.
+ * Copies to the device, attention and copies back run on three sets of
+ * streams of the call's own, so piece c+1's queries travel while piece c is
+ * computed and piece c-1's output travels back. The call is ordered on
+ * `stream`: it starts after the work queued there and that stream waits for
+ * its last copy back; the host buffers may be read after synchronising with
+ * `stream`. Host buffers should be page-locked (cudaHostAlloc or registered),
+ * or the copies do not overlap. q_bf16, kv_e4m3, kv_scale, out_bf16 and lse
+ * are device buffers the caller owns, with mla_prefill_dense's layout and
+ * alignment; lse may be NULL only with lse_host NULL. n_chunks in [1,
+ * MLA_DENSE_HOST_MAX_CHUNKS]. workspace: mla_workspace_size(MLA_OP_DENSE_HOST,
+ * ...) bytes, 16-byte aligned. Errors: the checks of mla_prefill_dense, plus
+ * MLA_ERR_INVALID_ARG for a NULL host pointer or n_chunks out of range. */
+mla_status_t mla_prefill_dense_host(const mla_seqs_t *seqs, const void *q_host, int32_t num_heads,
+                                    const uint8_t *kv_host, const float *kv_scale_host, float sm_scale,
+                                    void *out_host, float *lse_host, void *q_bf16, uint8_t *kv_e4m3,
+                                    float *kv_scale, void *out_bf16, float *lse, int32_t n_chunks,
+                                    void *workspace, size_t workspace_bytes, int32_t *dev_err,
+                                    cudaStream_t stream);
 
 /* Cache write of the new tokens: the step before attention, which reads the
  * rows this call stores ("More throughput from fewer GPUs", section System

@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     MLA_DEVERR_BAD_INDEX,
     MLA_DEVERR_BAD_PAGE,
     MLA_OP_DENSE,
+    MLA_OP_DENSE_HOST,
     MLA_OP_INDEXER,
     MLA_OP_SPARSE,
     MlaError,
@@ -19,6 +20,7 @@ from .binding import (  # noqa: F401
     mla_kv_append,
     mla_merge_attn,
     mla_prefill_dense,
+    mla_prefill_dense_host,
     mla_prefill_dense_static,
     mla_prefill_sparse,
     mla_workspace_size,

@@ -17,11 +17,12 @@ LIB_PATH = os.path.join(_HERE, "libmla.so")
 
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_WORKSPACE = range(5)
 MLA_DEVERR_BAD_PAGE, MLA_DEVERR_BAD_INDEX, MLA_DEVERR_TIMEOUT, MLA_DEVERR_INTERNAL = 1, 2, 4, 8
-MLA_OP_DENSE, MLA_OP_INDEXER, MLA_OP_SPARSE = 0, 1, 2
+MLA_OP_DENSE, MLA_OP_INDEXER, MLA_OP_SPARSE, MLA_OP_DENSE_HOST = 0, 1, 2, 3
 
 EXPORTS = ("mla_workspace_size", "mla_prefill_dense", "mla_indexer_topk", "mla_prefill_sparse", "mla_last_error",
-           "mla_prefill_dense_static", "mla_kv_append", "mla_merge_attn")
+           "mla_prefill_dense_static", "mla_kv_append", "mla_merge_attn", "mla_prefill_dense_host")
 DENSE_STATIC_MAX_WORK_ITEMS = 65536
+DENSE_HOST_MAX_CHUNKS = 64
 
 
 class MlaError(RuntimeError):
@@ -66,6 +67,9 @@ def load(path: str = LIB_PATH):
                                      vp, vp]
     L.mla_prefill_dense_static.restype = ctypes.c_int
     L.mla_prefill_dense_static.argtypes = [ctypes.POINTER(mla_seqs_t), vp, i32, vp, vp, f32, vp, vp, vp, vp]
+    L.mla_prefill_dense_host.restype = ctypes.c_int
+    L.mla_prefill_dense_host.argtypes = [ctypes.POINTER(mla_seqs_t), vp, i32, vp, vp, f32, vp, vp, vp, vp, vp, vp, vp,
+                                         i32, vp, sz, vp, vp]
     L.mla_kv_append.restype = ctypes.c_int
     L.mla_kv_append.argtypes = [ctypes.POINTER(mla_seqs_t), vp, vp, vp, vp, vp, vp, vp, vp]
     L.mla_merge_attn.restype = ctypes.c_int
@@ -157,6 +161,25 @@ def mla_prefill_dense_static(seqs: Seqs, q: torch.Tensor, kv: torch.Tensor, kv_s
     _check(load().mla_prefill_dense_static(ctypes.byref(c), _ptr(q), H, _ptr(kv), _ptr(kv_scale), float(sm_scale),
                                            _ptr(out), _ptr(lse), _ptr(dev_err), _stream()))
     return out, lse
+
+
+def mla_prefill_dense_host(seqs: Seqs, q_host: torch.Tensor, kv_host: torch.Tensor, kv_scale_host: torch.Tensor,
+                           sm_scale: float, q: torch.Tensor, kv: torch.Tensor, kv_scale: torch.Tensor,
+                           out_host: torch.Tensor, out: torch.Tensor, lse_host=None, lse=None, n_chunks: int = 8,
+                           workspace=None, dev_err=None):
+    """Dense prefill from host tensors to host tensors (pinned for overlap): the
+    cache and, piece by piece, the query rows are copied into the device buffers
+    q / kv / kv_scale, each piece's attention runs as its rows arrive and its
+    out (and lse) rows are copied back into out_host (lse_host) as it finishes.
+    Same results as mla_prefill_dense. Ordered on the current stream."""
+    H = q.shape[1]
+    ws, wsb = _workspace(MLA_OP_DENSE_HOST, seqs, H, 0, workspace)
+    c = seqs.c()
+    _check(load().mla_prefill_dense_host(ctypes.byref(c), _ptr(q_host), H, _ptr(kv_host), _ptr(kv_scale_host),
+                                         float(sm_scale), _ptr(out_host), _ptr(lse_host), _ptr(q), _ptr(kv),
+                                         _ptr(kv_scale), _ptr(out), _ptr(lse), int(n_chunks), _ptr(ws), wsb,
+                                         _ptr(dev_err), _stream()))
+    return out_host, lse_host
 
 
 def mla_indexer_topk(seqs: Seqs, qi: torch.Tensor, w: torch.Tensor, w_token_stride: int, ki: torch.Tensor,

@@ -68,24 +68,29 @@ bool heads_ok(int32_t h) { return h == 16 || h == 32 || h == 64 || h == 128; }
 
 // Paired row tiles: tile i with tile n-1-i of the same sequence (the V-shaped
 // chunk pairing of the PCP scheme, applied at tile granularity), items sorted
-// by decreasing work so the costliest go first.
-std::vector<int4> dense_schedule(const mla_seqs_t *s, int32_t H) {
+// by decreasing work so the costliest go first. Only the tiles of the new
+// tokens [t0, t1) (global indices, on tile boundaries of their sequences) are
+// scheduled; within each sequence's share of that range the first tile pairs
+// with the last.
+std::vector<int4> dense_schedule_range(const mla_seqs_t *s, int32_t H, int64_t t0, int64_t t1) {
     struct Item {
         int4 v;
         int64_t cost;
     };
     std::vector<Item> items;
     for (int b = 0; b < s->batch; ++b) {
-        const int64_t t = s->cu_seqlens_q_host[b + 1] - s->cu_seqlens_q_host[b];
+        const int64_t c0 = s->cu_seqlens_q_host[b], c1 = s->cu_seqlens_q_host[b + 1];
+        const int64_t l0 = std::max(t0, c0) - c0, l1 = std::min(t1, c1) - c0;
+        if (l1 <= l0) continue;
         const int64_t P = s->prefix_lens_host[b];
-        const int64_t rows = t * H;
-        const int64_t n = (rows + kBM - 1) / kBM;
+        const int64_t rows = (c1 - c0) * H;
+        const int64_t i_lo = l0 * H / kBM, i_hi = (l1 * H + kBM - 1) / kBM;
         auto tile_keys = [&](int64_t i) {
             const int64_t last_row = std::min(rows, (i + 1) * kBM) - 1;
             return P + last_row / H + 1;
         };
-        for (int64_t i = 0; i < (n + 1) / 2; ++i) {
-            const int64_t j = n - 1 - i;
+        for (int64_t m = 0; m < (i_hi - i_lo + 1) / 2; ++m) {
+            const int64_t i = i_lo + m, j = i_hi - 1 - m;
             Item it;
             it.v = make_int4(b, static_cast<int>(i), j != i ? static_cast<int>(j) : -1, 0);
             it.cost = tile_keys(i) + (j != i ? tile_keys(j) : 0);
@@ -96,6 +101,41 @@ std::vector<int4> dense_schedule(const mla_seqs_t *s, int32_t H) {
     std::vector<int4> out(items.size());
     for (size_t i = 0; i < items.size(); ++i) out[i] = items[i].v;
     return out;
+}
+
+std::vector<int4> dense_schedule(const mla_seqs_t *s, int32_t H) {
+    return dense_schedule_range(s, H, 0, s->cu_seqlens_q_host[s->batch]);
+}
+
+// Token boundaries of n_chunks near-equal pieces of the new tokens, each moved
+// down to a tile boundary of the sequence it falls in (a tile is 64 rows of
+// token x head, i.e. 64/H tokens for H <= 64); pieces may come out empty.
+std::vector<int64_t> dense_chunk_bounds(const mla_seqs_t *s, int32_t H, int32_t n_chunks) {
+    const int64_t tq = s->cu_seqlens_q_host[s->batch];
+    const int64_t g = H < kBM ? kBM / H : 1;     // tokens per tile
+    std::vector<int64_t> bnd(static_cast<size_t>(n_chunks) + 1);
+    bnd[0] = 0;
+    bnd[n_chunks] = tq;
+    int b = 0;
+    for (int c = 1; c < n_chunks; ++c) {
+        const int64_t t = tq * c / n_chunks;
+        while (b + 1 < s->batch && s->cu_seqlens_q_host[b + 1] <= t) ++b;
+        const int64_t c0 = s->cu_seqlens_q_host[b];
+        bnd[c] = std::max(bnd[c - 1], c0 + (t - c0) / g * g);
+    }
+    return bnd;
+}
+
+// Upper bound of the items of all pieces: a piece's share of a sequence adds at
+// most half a pair to the plain schedule, and the shares number at most
+// batch + n_chunks.
+size_t dense_host_items_bound(const mla_seqs_t *s, int32_t H) {
+    size_t tiles = 0;
+    for (int b = 0; b < s->batch; ++b) {
+        const int64_t rows = static_cast<int64_t>(s->cu_seqlens_q_host[b + 1] - s->cu_seqlens_q_host[b]) * H;
+        tiles += static_cast<size_t>((rows + kBM - 1) / kBM);
+    }
+    return tiles / 2 + static_cast<size_t>(s->batch) + MLA_DENSE_HOST_MAX_CHUNKS + 1;
 }
 
 int64_t max_context(const mla_seqs_t *s) {
@@ -238,6 +278,9 @@ size_t mla_workspace_size(mla_op_t op, const mla_seqs_t *seqs, int32_t num_heads
                    round_up(static_cast<size_t>(indexer_items(seqs, mla::kIdxKeyChunkMin)) * sizeof(int4), kWsAlign);
         case MLA_OP_SPARSE:
             return 0;
+        case MLA_OP_DENSE_HOST:
+            if (!heads_ok(num_heads)) return 0;
+            return round_up(dense_host_items_bound(seqs, num_heads) * sizeof(int4), kWsAlign);
     }
     return 0;
 }
@@ -267,6 +310,119 @@ mla_status_t mla_prefill_dense(const mla_seqs_t *seqs, const void *q_bf16, int32
         return fail(MLA_ERR_CUDA, "tensor map encoding for the latent cache failed");
     e = mla::launch_dense_f8(a, static_cast<const int4 *>(workspace), static_cast<int>(work.size()), tmap_kv, stream);
     if (e != cudaSuccess) return cuda_fail(e, "dense launch");
+    return MLA_OK;
+}
+
+namespace {
+// Streams and events of one host-to-host call; destroyed when the call returns
+// (CUDA releases them once the work queued on them has finished).
+struct HostPipe {
+    cudaStream_t s_in = nullptr, s_out = nullptr, s_c[2] = {nullptr, nullptr};
+    std::vector<cudaEvent_t> ev;
+    ~HostPipe() {
+        for (cudaEvent_t e : ev) cudaEventDestroy(e);
+        for (cudaStream_t x : {s_in, s_out, s_c[0], s_c[1]})
+            if (x) cudaStreamDestroy(x);
+    }
+    cudaError_t event(cudaEvent_t *e) {
+        cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
+        if (r == cudaSuccess) ev.push_back(*e);
+        return r;
+    }
+};
+}  // namespace
+
+mla_status_t mla_prefill_dense_host(const mla_seqs_t *seqs, const void *q_host, int32_t num_heads,
+                                    const uint8_t *kv_host, const float *kv_scale_host, float sm_scale,
+                                    void *out_host, float *lse_host, void *q_bf16, uint8_t *kv_e4m3, float *kv_scale,
+                                    void *out_bf16, float *lse, int32_t n_chunks, void *workspace,
+                                    size_t workspace_bytes, int32_t *dev_err, cudaStream_t stream) {
+    g_err.clear();
+    mla_status_t st = check_seqs(seqs);
+    if (st != MLA_OK) return st;
+    if (!heads_ok(num_heads)) return fail(MLA_ERR_UNSUPPORTED, "num_heads must be 16, 32, 64 or 128 (got %d)", num_heads);
+    if ((st = check_attn_ptrs(q_bf16, kv_e4m3, kv_scale, out_bf16, lse, sm_scale)) != MLA_OK) return st;
+    if (!q_host || !kv_host || !kv_scale_host || !out_host)
+        return fail(MLA_ERR_INVALID_ARG, "q_host, kv_host, kv_scale_host and out_host must be set");
+    if (lse_host && !lse) return fail(MLA_ERR_INVALID_ARG, "lse_host needs the device lse buffer");
+    if (n_chunks < 1 || n_chunks > MLA_DENSE_HOST_MAX_CHUNKS)
+        return fail(MLA_ERR_INVALID_ARG, "n_chunks must be in [1, %d] (got %d)", MLA_DENSE_HOST_MAX_CHUNKS, n_chunks);
+    const int64_t tq = seqs->cu_seqlens_q_host[seqs->batch];
+    if (tq == 0) return MLA_OK;
+    const std::vector<int64_t> bnd = dense_chunk_bounds(seqs, num_heads, n_chunks);
+    std::vector<int4> work;
+    std::vector<size_t> off(static_cast<size_t>(n_chunks) + 1, 0);
+    for (int c = 0; c < n_chunks; ++c) {
+        const std::vector<int4> w = dense_schedule_range(seqs, num_heads, bnd[c], bnd[c + 1]);
+        work.insert(work.end(), w.begin(), w.end());
+        off[c + 1] = work.size();
+    }
+    const size_t need = round_up(work.size() * sizeof(int4), kWsAlign);
+    if (work.size() > dense_host_items_bound(seqs, num_heads))   // the bound the workspace size promises
+        return fail(MLA_ERR_INVALID_ARG, "internal: %zu work items above the workspace bound", work.size());
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16))
+        return fail(MLA_ERR_WORKSPACE, "dense from host needs %zu workspace bytes (16-byte aligned), got %zu", need,
+                    workspace ? workspace_bytes : 0);
+    const mla::AttnArgs a = attn_args(seqs, q_bf16, num_heads, kv_e4m3, kv_scale, sm_scale, out_bf16, lse, dev_err);
+    CUtensorMap tmap_kv;
+    if (!mla::encode_kv_tmap(&tmap_kv, kv_e4m3, seqs->num_blocks))
+        return fail(MLA_ERR_CUDA, "tensor map encoding for the latent cache failed");
+
+    HostPipe p;
+    cudaError_t e;
+    cudaEvent_t ev_entry, ev_end;
+#define MLA_TRY(x, what)                       \
+    if ((e = (x)) != cudaSuccess) return cuda_fail(e, what)
+    MLA_TRY(cudaStreamCreateWithFlags(&p.s_in, cudaStreamNonBlocking), "stream");
+    MLA_TRY(cudaStreamCreateWithFlags(&p.s_out, cudaStreamNonBlocking), "stream");
+    MLA_TRY(cudaStreamCreateWithFlags(&p.s_c[0], cudaStreamNonBlocking), "stream");
+    MLA_TRY(cudaStreamCreateWithFlags(&p.s_c[1], cudaStreamNonBlocking), "stream");
+    MLA_TRY(p.event(&ev_entry), "event");
+    MLA_TRY(p.event(&ev_end), "event");
+    // everything queued on `stream` before this call comes first
+    MLA_TRY(cudaEventRecord(ev_entry, stream), "event record");
+    for (cudaStream_t x : {p.s_in, p.s_out, p.s_c[0], p.s_c[1]}) MLA_TRY(cudaStreamWaitEvent(x, ev_entry, 0), "wait");
+    // the cache and the work lists first, then the queries piece by piece
+    const size_t rows_kv = static_cast<size_t>(seqs->num_blocks) * 256;
+    MLA_TRY(cudaMemcpyAsync(kv_e4m3, kv_host, rows_kv * 576, cudaMemcpyHostToDevice, p.s_in), "cache copy");
+    MLA_TRY(cudaMemcpyAsync(kv_scale, kv_scale_host, rows_kv * sizeof(float), cudaMemcpyHostToDevice, p.s_in),
+            "cache scale copy");
+    MLA_TRY(cudaMemcpyAsync(workspace, work.data(), work.size() * sizeof(int4), cudaMemcpyHostToDevice, p.s_in),
+            "schedule upload");
+    const size_t q_row = static_cast<size_t>(num_heads) * 576 * 2, o_row = static_cast<size_t>(num_heads) * 512 * 2,
+                 l_row = static_cast<size_t>(num_heads) * sizeof(float);
+    const int4 *dwork = static_cast<const int4 *>(workspace);
+    for (int c = 0; c < n_chunks; ++c) {
+        if (bnd[c + 1] == bnd[c]) continue;
+        const size_t t0 = static_cast<size_t>(bnd[c]), nt = static_cast<size_t>(bnd[c + 1] - bnd[c]);
+        cudaEvent_t ev_in, ev_done;
+        MLA_TRY(p.event(&ev_in), "event");
+        MLA_TRY(p.event(&ev_done), "event");
+        MLA_TRY(cudaMemcpyAsync(static_cast<char *>(q_bf16) + t0 * q_row, static_cast<const char *>(q_host) + t0 * q_row,
+                                nt * q_row, cudaMemcpyHostToDevice, p.s_in),
+                "query copy");
+        MLA_TRY(cudaEventRecord(ev_in, p.s_in), "event record");
+        // pieces share no data, so consecutive ones go to two streams and the
+        // start of one overlaps the last CTAs of the other
+        cudaStream_t cs = p.s_c[c & 1];
+        MLA_TRY(cudaStreamWaitEvent(cs, ev_in, 0), "wait");
+        const int n_items = static_cast<int>(off[c + 1] - off[c]);
+        if (n_items > 0) MLA_TRY(mla::launch_dense_f8(a, dwork + off[c], n_items, tmap_kv, cs), "dense launch");
+        MLA_TRY(cudaEventRecord(ev_done, cs), "event record");
+        MLA_TRY(cudaStreamWaitEvent(p.s_out, ev_done, 0), "wait");
+        MLA_TRY(cudaMemcpyAsync(static_cast<char *>(out_host) + t0 * o_row, static_cast<const char *>(out_bf16) + t0 * o_row,
+                                nt * o_row, cudaMemcpyDeviceToHost, p.s_out),
+                "output copy");
+        if (lse_host)
+            MLA_TRY(cudaMemcpyAsync(reinterpret_cast<char *>(lse_host) + t0 * l_row,
+                                    reinterpret_cast<const char *>(lse) + t0 * l_row, nt * l_row,
+                                    cudaMemcpyDeviceToHost, p.s_out),
+                    "lse copy");
+    }
+    // the caller's stream resumes after the last copy back
+    MLA_TRY(cudaEventRecord(ev_end, p.s_out), "event record");
+    MLA_TRY(cudaStreamWaitEvent(stream, ev_end, 0), "wait");
+#undef MLA_TRY
     return MLA_OK;
 }
 

@@ -93,6 +93,31 @@ def test_rejects_bad_arguments(lib):
                                   0, None, None) == B.MLA_ERR_INVALID_ARG
 
 
+def dense_host(lib, s, H=64, qh=FAKE, kvh=FAKE, ksh=FAKE, oh=FAKE, lh=None, lse=None, chunks=4, ws=None, wsb=0):
+    return lib.mla_prefill_dense_host(ctypes.byref(s.c), qh, H, kvh, ksh, 0.07, oh, lh, FAKE, FAKE, FAKE, FAKE, lse,
+                                      chunks, ws, wsb, None, None)
+
+
+def test_dense_host_rejects_bad_arguments(lib):
+    s = HostSeqs([100], [0])
+    for kw in ({"qh": None}, {"kvh": None}, {"ksh": None}, {"oh": None}, {"lh": FAKE}):
+        assert dense_host(lib, s, **kw) == B.MLA_ERR_INVALID_ARG, kw
+    for c in (0, B.DENSE_HOST_MAX_CHUNKS + 1):
+        assert dense_host(lib, s, chunks=c) == B.MLA_ERR_INVALID_ARG
+        assert b"n_chunks" in lib.mla_last_error()
+    assert dense_host(lib, s, H=48) == B.MLA_ERR_UNSUPPORTED
+    assert dense_host(lib, s) == B.MLA_ERR_WORKSPACE
+    assert dense_host(lib, s, ws=FAKE, wsb=16) == B.MLA_ERR_WORKSPACE
+    assert dense_host(lib, HostSeqs([0, 0], [5, 0])) == B.MLA_OK          # nothing to do, nothing touched
+    # room for every piece's work list: the plain list plus at most one half-pair per
+    # (piece, sequence) share
+    for q_lens, H in (([100], 64), ([700, 33, 300], 16), ([5000], 128)):
+        hs = HostSeqs(q_lens, [0] * len(q_lens))
+        tiles = sum(-(-t * H // 64) for t in q_lens)
+        ws = lib.mla_workspace_size(B.MLA_OP_DENSE_HOST, ctypes.byref(hs.c), H, 0)
+        assert ws % 256 == 0 and ws >= (tiles // 2 + len(q_lens) + B.DENSE_HOST_MAX_CHUNKS) * 16
+
+
 def test_empty_batch_is_a_noop(lib):
     s = HostSeqs([0, 0], [5, 0])
     assert dense(lib, s) == B.MLA_OK

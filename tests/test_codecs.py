@@ -91,3 +91,24 @@ def test_generator_rows_are_independent_streams():
     # per-token scale is absmax/448 of the drawn row, so the largest code is +-448
     vals = np.array([O.e4m3_value(int(x)) for x in c[0]])
     assert np.max(np.abs(vals)) == 448.0
+
+
+def test_parity_rounding_allowance():
+    """The attention check measures error beyond the bf16 rounding of the output:
+    the exact result rounded to bf16 scores zero there (while its raw error is
+    not zero), and a planted error of 3e-2 of a row's RMS still fails."""
+    torch = pytest.importorskip("torch")
+    from tests.parity import TOL_MAX, bf16_half_spacing, rel_errors
+    rng = np.random.default_rng(5)
+    ora = rng.standard_normal((200, 512)) * np.exp2(rng.uniform(-6, 6, (200, 1)))
+    ora[:, 7] *= 6.0                                         # entries far above their row's RMS
+    rounded = torch.from_numpy(ora).to(torch.bfloat16).double().numpy()
+    assert np.all(np.abs(rounded - ora) <= bf16_half_spacing(ora))
+    raw_mx, _, _ = rel_errors(rounded, ora)
+    mx, mean, _ = rel_errors(rounded, ora, beyond_rounding=True)
+    assert raw_mx > 0.01 and mx == 0.0 and mean == 0.0
+    bad = rounded.copy()
+    rms = np.sqrt(np.mean(ora[3] ** 2))
+    bad[3, 100] += 3e-2 * rms
+    mx, _, _ = rel_errors(bad, ora, beyond_rounding=True)
+    assert mx > TOL_MAX

@@ -143,3 +143,37 @@ def test_bad_page_sets_device_flag():
     torch.cuda.synchronize()
     assert int(err.item()) & MLA_DEVERR_BAD_PAGE
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("q_lens,prefix,H,chunks", [
+    ([700, 33, 300], [100, 0, 2000], 64, 5),   # pieces cross sequence boundaries
+    ([257], [40], 16, 3),                      # four tokens per tile: pieces move to tile boundaries
+    ([129, 64], [0, 300], 128, 64),            # two tiles per token, the most pieces
+    ([0, 50], [10, 0], 64, 8),                 # an empty sequence
+    ([3], [0], 32, 8),                         # fewer tiles than pieces: some pieces empty
+])
+def test_dense_from_host_matches_device_call(q_lens, prefix, H, chunks):
+    """The host-to-host call (copies overlapped with attention, piece by piece)
+    returns exactly what the device call returns, and both match the oracle."""
+    import torch
+    from mla_prefill_attention_gb300 import mla_prefill_dense_host
+    pb = Problem(q_lens, prefix, H, seed=400 + H + chunks, shuffle=True, sm_scale=0.09)
+    d = pb.device()
+    out_d, lse_d = run_dense(pb, d)
+    T = pb.ps.total_q
+    qh = torch.from_numpy(pb.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    kvh, ksh = torch.from_numpy(pb.kv).pin_memory(), torch.from_numpy(pb.ks).pin_memory()
+    oh = torch.full((T, H, 512), float("nan"), dtype=torch.bfloat16).pin_memory()
+    lh = torch.full((T, H), float("nan"), dtype=torch.float32).pin_memory()
+    q2, kv2, ks2 = torch.zeros_like(d["q"]), torch.zeros_like(d["kv"]), torch.zeros_like(d["ks"])
+    o2, l2 = torch.zeros_like(out_d), torch.zeros_like(lse_d)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla_prefill_dense_host(d["seqs"], qh, kvh, ksh, pb.sm_scale, q2, kv2, ks2, oh, o2, lse_host=lh, lse=l2,
+                           n_chunks=chunks, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(oh.view(torch.int16), out_d.cpu().view(torch.int16))
+    assert torch.equal(lh, lse_d.cpu())
+    toks = np.arange(T)
+    ora, ora_lse = O.mla_dense(pb.ps, pb.q, toks, pb.kv, pb.ks, pb.sm_scale)
+    check_attention(bf16_to_np(oh), ora, lh.numpy(), ora_lse, f"from host {q_lens}/H{H}/{chunks}")
