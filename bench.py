@@ -100,6 +100,7 @@ class ClockSampler:
 # Pieces the host-to-host dense call cuts the new tokens into (copies of one
 # piece overlap the attention of the others).
 E2E_PIECES = 16
+SPARSE_E2E_PIECES = 8
 
 def host_dense(w):
     from mla_prefill_attention_gb300 import inputs as I
@@ -246,28 +247,29 @@ class SparseRun:
             self.mid.append(e)
         mla_prefill_sparse(self.seqs, d["q"], d["kv"], d["ks"], self.w.sm_scale, self.idx, out=self.out, lse=self.lse)
 
+    e2e_pieces = SPARSE_E2E_PIECES
+
     def e2e(self, steps, warmup):
-        """Both calls with every input in pinned host memory and the output, lse and
-        selected indices copied back, copies inside the timed region."""
+        """The host-to-host sparse step (mla_prefill_sparse_host): every input in
+        pinned host memory, the weights and caches copied in, then qi and q in
+        SPARSE_E2E_PIECES pieces, each piece's indexer, top-k and sparse attention
+        as its rows arrive, and its output, lse and selected indices copied back,
+        the copies overlapped with the kernels of other pieces; all of it inside
+        the timed region."""
         import torch
-        from mla_prefill_attention_gb300 import mla_indexer_topk, mla_prefill_sparse
+        from mla_prefill_attention_gb300 import mla_prefill_sparse_host
         h = {k: torch.from_numpy(v).pin_memory() for k, v in self.host.items() if k != "q"}
         h["q"] = torch.from_numpy(self.host["q"].view(np.int16)).view(torch.bfloat16).pin_memory()
         hout = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
         hlse = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
         hidx = torch.empty(self.idx.shape, dtype=torch.int32).pin_memory()
         d = self.d
+        host_out = {"out": hout, "lse": hlse, "idx": hidx}
+        dev_out = {"out": self.out, "lse": self.lse, "idx": self.idx}
 
         def one():
-            for k in h:
-                d[k].copy_(h[k], non_blocking=True)
-            mla_indexer_topk(self.seqs, d["qi"], d["w"], 0, d["ki"], d["kis"], self.w.topk, idx_out=self.idx,
-                             workspace=self.ws)
-            mla_prefill_sparse(self.seqs, d["q"], d["kv"], d["ks"], self.w.sm_scale, self.idx, out=self.out,
-                               lse=self.lse)
-            hout.copy_(self.out, non_blocking=True)
-            hlse.copy_(self.lse, non_blocking=True)
-            hidx.copy_(self.idx, non_blocking=True)
+            mla_prefill_sparse_host(self.seqs, h, d, host_out, dev_out, self.w.sm_scale, w_token_stride=0,
+                                    topk=self.w.topk, n_chunks=SPARSE_E2E_PIECES, workspace=self.ws)
 
         for _ in range(warmup):
             one()

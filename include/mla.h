@@ -200,6 +200,50 @@ mla_status_t mla_prefill_dense_host(const mla_seqs_t *seqs, const void *q_host, 
                                     void *workspace, size_t workspace_bytes, int32_t *dev_err,
                                     cudaStream_t stream);
 
+/* The tensors of one sparse step, once in host memory and once on the device
+ * (mla_prefill_sparse_host). Layouts as in mla_indexer_topk and
+ * mla_prefill_sparse; w holds one 64-value row (w_token_stride 0) or a row per
+ * token at w + t * w_token_stride. */
+typedef struct {
+    void *q_bf16;       /* [Tq, H, 576] bf16 */
+    uint8_t *qi_e4m3;   /* [Tq, 64, 128] */
+    float *w;           /* indexer head weights */
+    uint8_t *kv_e4m3;   /* [num_blocks, 256, 576] */
+    float *kv_scale;    /* [num_blocks, 256] */
+    uint8_t *ki_e4m3;   /* [num_blocks, 256, 128] */
+    float *ki_scale;    /* [num_blocks, 256] */
+} mla_sparse_inputs_t;
+
+typedef struct {
+    void *out_bf16;     /* [Tq, H, 512] bf16 */
+    float *lse;         /* [Tq, H], or NULL */
+    int32_t *idx;       /* [Tq, topk] selected positions */
+} mla_sparse_outputs_t;
+
+/* The sparse step (mla_indexer_topk, then mla_prefill_sparse over the
+ * selected rows) from host memory to host memory, with the copies overlapped
+ * with the kernels. This entry point has no counterpart on the source pages:
+ * it serves callers whose inputs sit in host memory. It computes exactly what
+ * the two device calls compute (identical indices and outputs):
+ *   1. w, the latent cache and the indexer keys are copied to the device
+ *      buffers of `dev_in`;
+ *   2. the new tokens are cut into n_chunks near-equal pieces of consecutive
+ *      tokens (moved to the indexer's 3-token group boundaries); each piece's
+ *      qi and q rows are copied in, its indexer scores, top-k and sparse
+ *      attention run as soon as they have arrived, and its out, lse and idx
+ *      rows are copied back to `host_out` as soon as it has finished.
+ * Streams, ordering and page-locking as in mla_prefill_dense_host. Every
+ * pointer of host_in, dev_in, host_out and dev_out must be set, except the
+ * lse pair: NULL in both or set in both. topk in [1, 2048]; n_chunks in [1,
+ * MLA_DENSE_HOST_MAX_CHUNKS]. workspace: mla_workspace_size(MLA_OP_INDEXER,
+ * ...) bytes, 256-byte aligned. Errors: the checks of the two device calls,
+ * plus MLA_ERR_INVALID_ARG for a NULL pointer or n_chunks out of range. */
+mla_status_t mla_prefill_sparse_host(const mla_seqs_t *seqs, int32_t num_heads, float sm_scale,
+                                     int64_t w_token_stride, int32_t topk, const mla_sparse_inputs_t *host_in,
+                                     const mla_sparse_inputs_t *dev_in, const mla_sparse_outputs_t *host_out,
+                                     const mla_sparse_outputs_t *dev_out, int32_t n_chunks, void *workspace,
+                                     size_t workspace_bytes, int32_t *dev_err, cudaStream_t stream);
+
 /* Cache write of the new tokens: the step before attention, which reads the
  * rows this call stores ("More throughput from fewer GPUs", section System
  * architecture: FP8 KV cache, one latent row per token; section KV hand-off

@@ -23,5 +23,6 @@ from .binding import (  # noqa: F401
     mla_prefill_dense_host,
     mla_prefill_dense_static,
     mla_prefill_sparse,
+    mla_prefill_sparse_host,
     mla_workspace_size,
 )

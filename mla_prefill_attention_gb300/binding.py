@@ -20,7 +20,8 @@ MLA_DEVERR_BAD_PAGE, MLA_DEVERR_BAD_INDEX, MLA_DEVERR_TIMEOUT, MLA_DEVERR_INTERN
 MLA_OP_DENSE, MLA_OP_INDEXER, MLA_OP_SPARSE, MLA_OP_DENSE_HOST = 0, 1, 2, 3
 
 EXPORTS = ("mla_workspace_size", "mla_prefill_dense", "mla_indexer_topk", "mla_prefill_sparse", "mla_last_error",
-           "mla_prefill_dense_static", "mla_kv_append", "mla_merge_attn", "mla_prefill_dense_host")
+           "mla_prefill_dense_static", "mla_kv_append", "mla_merge_attn", "mla_prefill_dense_host",
+           "mla_prefill_sparse_host")
 DENSE_STATIC_MAX_WORK_ITEMS = 65536
 DENSE_HOST_MAX_CHUNKS = 64
 
@@ -42,6 +43,16 @@ class mla_seqs_t(ctypes.Structure):
         ("max_blocks_per_seq", ctypes.c_int32),
         ("num_blocks", ctypes.c_int32),
     ]
+
+
+class mla_sparse_inputs_t(ctypes.Structure):
+    _fields_ = [("q_bf16", ctypes.c_void_p), ("qi_e4m3", ctypes.c_void_p), ("w", ctypes.c_void_p),
+                ("kv_e4m3", ctypes.c_void_p), ("kv_scale", ctypes.c_void_p), ("ki_e4m3", ctypes.c_void_p),
+                ("ki_scale", ctypes.c_void_p)]
+
+
+class mla_sparse_outputs_t(ctypes.Structure):
+    _fields_ = [("out_bf16", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("idx", ctypes.c_void_p)]
 
 
 _lib = None
@@ -70,6 +81,11 @@ def load(path: str = LIB_PATH):
     L.mla_prefill_dense_host.restype = ctypes.c_int
     L.mla_prefill_dense_host.argtypes = [ctypes.POINTER(mla_seqs_t), vp, i32, vp, vp, f32, vp, vp, vp, vp, vp, vp, vp,
                                          i32, vp, sz, vp, vp]
+    L.mla_prefill_sparse_host.restype = ctypes.c_int
+    L.mla_prefill_sparse_host.argtypes = [ctypes.POINTER(mla_seqs_t), i32, f32, i64, i32,
+                                          ctypes.POINTER(mla_sparse_inputs_t), ctypes.POINTER(mla_sparse_inputs_t),
+                                          ctypes.POINTER(mla_sparse_outputs_t), ctypes.POINTER(mla_sparse_outputs_t),
+                                          i32, vp, sz, vp, vp]
     L.mla_kv_append.restype = ctypes.c_int
     L.mla_kv_append.argtypes = [ctypes.POINTER(mla_seqs_t), vp, vp, vp, vp, vp, vp, vp, vp]
     L.mla_merge_attn.restype = ctypes.c_int
@@ -180,6 +196,36 @@ def mla_prefill_dense_host(seqs: Seqs, q_host: torch.Tensor, kv_host: torch.Tens
                                          _ptr(kv_scale), _ptr(out), _ptr(lse), int(n_chunks), _ptr(ws), wsb,
                                          _ptr(dev_err), _stream()))
     return out_host, lse_host
+
+
+SPARSE_INPUTS = ("q", "qi", "w", "kv", "ks", "ki", "kis")   # field order of mla_sparse_inputs_t
+
+
+def _inputs(t: dict) -> mla_sparse_inputs_t:
+    return mla_sparse_inputs_t(*[None if t.get(k) is None else t[k].data_ptr() for k in SPARSE_INPUTS])
+
+
+def _outputs(t: dict) -> mla_sparse_outputs_t:
+    return mla_sparse_outputs_t(*[None if t.get(k) is None else t[k].data_ptr() for k in ("out", "lse", "idx")])
+
+
+def mla_prefill_sparse_host(seqs: Seqs, host_in: dict, dev_in: dict, host_out: dict, dev_out: dict, sm_scale: float,
+                            w_token_stride: int = 0, topk: int = 2048, n_chunks: int = 8, workspace=None,
+                            dev_err=None):
+    """The sparse step (indexer top-k, then sparse attention) from host tensors
+    to host tensors (pinned for overlap). host_in / dev_in: dicts with keys q,
+    qi, w, kv, ks, ki, kis (the tensors of mla_indexer_topk and
+    mla_prefill_sparse, once in host and once in device memory); host_out /
+    dev_out: out, idx and optionally lse. Same results as the two device calls.
+    Ordered on the current stream."""
+    H = dev_in["q"].shape[1]
+    ws, wsb = _workspace(MLA_OP_INDEXER, seqs, H, topk, workspace)
+    c = seqs.c()
+    hi, di, ho, do = _inputs(host_in), _inputs(dev_in), _outputs(host_out), _outputs(dev_out)
+    _check(load().mla_prefill_sparse_host(ctypes.byref(c), H, float(sm_scale), int(w_token_stride), int(topk),
+                                          ctypes.byref(hi), ctypes.byref(di), ctypes.byref(ho), ctypes.byref(do),
+                                          int(n_chunks), _ptr(ws), wsb, _ptr(dev_err), _stream()))
+    return host_out
 
 
 def mla_indexer_topk(seqs: Seqs, qi: torch.Tensor, w: torch.Tensor, w_token_stride: int, ki: torch.Tensor,

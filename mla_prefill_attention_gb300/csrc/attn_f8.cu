@@ -397,9 +397,8 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
     int64_t toks[2] = {-1, -1};
     int n_rt;
     if (kSparse) {
-        const int64_t tq = __ldg(a.cu_seqlens + a.batch);
-        toks[0] = 2 * static_cast<int64_t>(blockIdx.x);
-        toks[1] = toks[0] + 1 < tq ? toks[0] + 1 : -1;
+        toks[0] = a.tok_begin + 2 * static_cast<int64_t>(blockIdx.x);
+        toks[1] = toks[0] + 1 < a.tok_end ? toks[0] + 1 : -1;
         h0 = blockIdx.y * BM;
         n_rt = toks[1] >= 0 ? 2 : 1;
     } else {
@@ -969,7 +968,8 @@ cudaError_t launch_dense_f8(const AttnArgs &a, const int4 *work, int n_work, con
     return cudaGetLastError();
 }
 
-cudaError_t launch_sparse_f8(const AttnArgs &a, int64_t n_tokens, cudaStream_t st) {
+cudaError_t launch_sparse_f8(const AttnArgs &a, cudaStream_t st) {
+    const int64_t n_tokens = a.tok_end - a.tok_begin;
     cudaError_t e = cudaFuncSetAttribute(f8attn::attn_f8_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          f8attn::kDynSmem<true>);
     if (e != cudaSuccess) return e;

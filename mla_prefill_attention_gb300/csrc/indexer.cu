@@ -701,7 +701,7 @@ __global__ void __launch_bounds__(TK_NT, 2) topk_kernel(const IndexerArgs a) {
     __shared__ uint32_t wcnt[TK_NW][2];
     __shared__ uint32_t info[4];
 
-    const int64_t t = blockIdx.x;
+    const int64_t t = a.tok0 + blockIdx.x;
     const int b = find_seq(a.cu_seqlens, a.batch, t);
     const int n = __ldg(a.prefix_lens + b) + static_cast<int>(t - __ldg(a.cu_seqlens + b)) + 1;
     int32_t *out = a.idx_out + t * a.topk;

@@ -24,6 +24,7 @@ struct AttnArgs {
     const int32_t *idx;          // sparse: [Tq, topk]
     int32_t topk;
     int32_t *dev_err;
+    int64_t tok_begin, tok_end;  // sparse: the new tokens this launch attends for (global indices)
 };
 
 struct IndexerArgs {
@@ -43,6 +44,7 @@ struct IndexerArgs {
     int32_t *idx_out;            // [Tq, topk]
     int32_t *dev_err;
     int32_t key_chunk;           // keys per indexer work item (a power of two, 2,048 .. 32,768)
+    int64_t tok0;                // top-k: first token of the launch (CTA i selects for token tok0 + i)
 };
 
 // Dense attention on e4m3 operands (kind::f8f6f4). Work item: x = sequence,
@@ -51,8 +53,8 @@ struct IndexerArgs {
 cudaError_t launch_dense_f8(const AttnArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_kv, cudaStream_t st);
 bool encode_kv_tmap(CUtensorMap *map, const uint8_t *kv, int32_t num_blocks);
 // Sparse attention on e4m3 operands: rows gathered by index (cp.async), two
-// tokens x 64 heads per CTA.
-cudaError_t launch_sparse_f8(const AttnArgs &a, int64_t n_tokens, cudaStream_t st);
+// tokens x 64 heads per CTA, for the tokens [a.tok_begin, a.tok_end).
+cudaError_t launch_sparse_f8(const AttnArgs &a, cudaStream_t st);
 
 // Indexer score work item: x = sequence, y = first new token (in-sequence),
 // z = token count (<= kIdxTokensPerCta), w = key chunk (keys w * key_chunk ..

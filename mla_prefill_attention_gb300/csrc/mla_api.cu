@@ -146,33 +146,37 @@ int64_t max_context(const mla_seqs_t *s) {
 }
 
 // Work items of the indexer: (sequence, first token, token count, key chunk)
-// for every group of kIdxTokensPerCta tokens and every chunk of `chunk` keys
-// they can see.
-int64_t indexer_items(const mla_seqs_t *s, int chunk) {
-    int64_t n = 0;
+// for every group of kIdxTokensPerCta tokens whose first token lies in
+// [t0, t1) (global indices; groups start every kIdxTokensPerCta tokens from
+// the start of their sequence) and every chunk of `chunk` keys it can see.
+template <typename F>
+void indexer_groups(const mla_seqs_t *s, int64_t t0, int64_t t1, F &&f) {
     for (int b = 0; b < s->batch; ++b) {
+        const int64_t c0 = s->cu_seqlens_q_host[b];
         const int t = s->cu_seqlens_q_host[b + 1] - s->cu_seqlens_q_host[b];
         const int P = s->prefix_lens_host[b];
         for (int i0 = 0; i0 < t; i0 += mla::kIdxTokensPerCta) {
-            const int keys = P + i0 + std::min(mla::kIdxTokensPerCta, t - i0);
-            n += (keys + chunk - 1) / chunk;
+            if (c0 + i0 < t0 || c0 + i0 >= t1) continue;
+            const int nt = std::min(mla::kIdxTokensPerCta, t - i0);
+            f(b, i0, nt, P + i0 + nt);
         }
     }
+}
+
+int64_t indexer_items(const mla_seqs_t *s, int chunk, int64_t t0, int64_t t1) {
+    int64_t n = 0;
+    indexer_groups(s, t0, t1, [&](int, int, int, int keys) { n += (keys + chunk - 1) / chunk; });
     return n;
 }
 
-std::vector<int4> indexer_schedule(const mla_seqs_t *s, int chunk) {
+int64_t indexer_items(const mla_seqs_t *s, int chunk) { return indexer_items(s, chunk, 0, s->cu_seqlens_q_host[s->batch]); }
+
+std::vector<int4> indexer_schedule(const mla_seqs_t *s, int chunk, int64_t t0, int64_t t1) {
     std::vector<int4> items;
-    items.reserve(static_cast<size_t>(indexer_items(s, chunk)));
-    for (int b = 0; b < s->batch; ++b) {
-        const int t = s->cu_seqlens_q_host[b + 1] - s->cu_seqlens_q_host[b];
-        const int P = s->prefix_lens_host[b];
-        for (int i0 = 0; i0 < t; i0 += mla::kIdxTokensPerCta) {
-            const int nt = std::min(mla::kIdxTokensPerCta, t - i0);
-            const int keys = P + i0 + nt;
-            for (int c = 0; c * chunk < keys; ++c) items.push_back(make_int4(b, i0, nt, c));
-        }
-    }
+    items.reserve(static_cast<size_t>(indexer_items(s, chunk, t0, t1)));
+    indexer_groups(s, t0, t1, [&](int b, int i0, int nt, int keys) {
+        for (int c = 0; c * chunk < keys; ++c) items.push_back(make_int4(b, i0, nt, c));
+    });
     return items;
 }
 
@@ -180,13 +184,14 @@ std::vector<int4> indexer_schedule(const mla_seqs_t *s, int chunk) {
 // query load, the first tiles of the pipeline) over more tiles; shorter ones
 // give more CTAs. Take the longest chunk that still gives every SM at least
 // eight items (one CTA per SM), so the last wave stays a small share.
-int indexer_key_chunk(const mla_seqs_t *s) {
+int indexer_key_chunk(const mla_seqs_t *s, int64_t t0, int64_t t1) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
         sms = 1;
     int chunk = mla::kIdxKeyChunkMax;
-    while (chunk > mla::kIdxKeyChunkMin && indexer_items(s, chunk) < 8 * static_cast<int64_t>(sms)) chunk /= 2;
+    while (chunk > mla::kIdxKeyChunkMin && indexer_items(s, chunk, t0, t1) < 8 * static_cast<int64_t>(sms))
+        chunk /= 2;
     return chunk;
 }
 
@@ -426,12 +431,9 @@ mla_status_t mla_prefill_dense_host(const mla_seqs_t *seqs, const void *q_host, 
     return MLA_OK;
 }
 
-mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, const float *w, int64_t w_token_stride,
-                              const uint8_t *ki_e4m3, const float *ki_scale, int32_t topk, int32_t *idx_out,
-                              void *workspace, size_t workspace_bytes, int32_t *dev_err, cudaStream_t stream) {
-    g_err.clear();
-    mla_status_t st = check_seqs(seqs);
-    if (st != MLA_OK) return st;
+namespace {
+mla_status_t check_indexer_args(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, const float *w, int64_t w_token_stride,
+                                const uint8_t *ki_e4m3, const float *ki_scale, int32_t topk, const int32_t *idx_out) {
     if (!qi_e4m3 || !w || !ki_e4m3 || !ki_scale || !idx_out)
         return fail(MLA_ERR_INVALID_ARG, "qi, w, ki, ki_scale and idx_out must be set");
     if (!aligned(qi_e4m3, 16) || !aligned(ki_e4m3, 16))
@@ -442,22 +444,14 @@ mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, co
     if (w_token_stride < 0 || w_token_stride % 4 != 0)
         return fail(MLA_ERR_INVALID_ARG, "w_token_stride must be a non-negative multiple of 4");
     if (topk < 1 || topk > 2048) return fail(MLA_ERR_UNSUPPORTED, "topk must be in [1, 2048] (got %d)", topk);
-    const int64_t tq = seqs->cu_seqlens_q_host[seqs->batch];
-    if (tq == 0) return MLA_OK;
-    if (tq * 64 > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "too many query tokens for the indexer (Tq * 64 > 2^31 - 1)");
-    const int key_chunk = indexer_key_chunk(seqs);
-    const std::vector<int4> work = indexer_schedule(seqs, key_chunk);
-    const size_t sbytes = indexer_score_bytes(seqs);
-    const size_t need = sbytes + round_up(work.size() * sizeof(int4), kWsAlign);
-    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
-        return fail(MLA_ERR_WORKSPACE, "indexer needs %zu workspace bytes (256-byte aligned), got %zu", need,
-                    workspace ? workspace_bytes : 0);
-    int4 *dwork = reinterpret_cast<int4 *>(static_cast<char *>(workspace) + sbytes);
-    cudaError_t e = cudaSuccess;
-    if (!work.empty()) {
-        e = cudaMemcpyAsync(dwork, work.data(), work.size() * sizeof(int4), cudaMemcpyHostToDevice, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "schedule upload");
-    }
+    if (static_cast<int64_t>(seqs->cu_seqlens_q_host[seqs->batch]) * 64 > INT32_MAX)
+        return fail(MLA_ERR_UNSUPPORTED, "too many query tokens for the indexer (Tq * 64 > 2^31 - 1)");
+    return MLA_OK;
+}
+
+mla::IndexerArgs indexer_args(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, const float *w, int64_t w_token_stride,
+                              const uint8_t *ki_e4m3, const float *ki_scale, int32_t topk, int32_t *idx_out,
+                              void *workspace, int32_t *dev_err) {
     mla::IndexerArgs a{};
     a.qi = qi_e4m3;
     a.w = w;
@@ -475,6 +469,35 @@ mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, co
     a.topk = topk;
     a.idx_out = idx_out;
     a.dev_err = dev_err;
+    return a;
+}
+}  // namespace
+
+mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, const float *w, int64_t w_token_stride,
+                              const uint8_t *ki_e4m3, const float *ki_scale, int32_t topk, int32_t *idx_out,
+                              void *workspace, size_t workspace_bytes, int32_t *dev_err, cudaStream_t stream) {
+    g_err.clear();
+    mla_status_t st = check_seqs(seqs);
+    if (st != MLA_OK) return st;
+    if ((st = check_indexer_args(seqs, qi_e4m3, w, w_token_stride, ki_e4m3, ki_scale, topk, idx_out)) != MLA_OK)
+        return st;
+    const int64_t tq = seqs->cu_seqlens_q_host[seqs->batch];
+    if (tq == 0) return MLA_OK;
+    const int key_chunk = indexer_key_chunk(seqs, 0, tq);
+    const std::vector<int4> work = indexer_schedule(seqs, key_chunk, 0, tq);
+    const size_t sbytes = indexer_score_bytes(seqs);
+    const size_t need = sbytes + round_up(work.size() * sizeof(int4), kWsAlign);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+        return fail(MLA_ERR_WORKSPACE, "indexer needs %zu workspace bytes (256-byte aligned), got %zu", need,
+                    workspace ? workspace_bytes : 0);
+    int4 *dwork = reinterpret_cast<int4 *>(static_cast<char *>(workspace) + sbytes);
+    cudaError_t e = cudaSuccess;
+    if (!work.empty()) {
+        e = cudaMemcpyAsync(dwork, work.data(), work.size() * sizeof(int4), cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "schedule upload");
+    }
+    mla::IndexerArgs a = indexer_args(seqs, qi_e4m3, w, w_token_stride, ki_e4m3, ki_scale, topk, idx_out, workspace,
+                                      dev_err);
     a.key_chunk = key_chunk;
     CUtensorMap tmap_k, tmap_q;
     if (!encode_rows128(&tmap_k, ki_e4m3, static_cast<uint64_t>(seqs->num_blocks) * 256, 128) ||
@@ -506,8 +529,150 @@ mla_status_t mla_prefill_sparse(const mla_seqs_t *seqs, const void *q_bf16, int3
     mla::AttnArgs a = attn_args(seqs, q_bf16, num_heads, kv_e4m3, kv_scale, sm_scale, out_bf16, lse, dev_err);
     a.idx = idx;
     a.topk = topk;
-    cudaError_t e = mla::launch_sparse_f8(a, tq, stream);
+    a.tok_begin = 0;
+    a.tok_end = tq;
+    cudaError_t e = mla::launch_sparse_f8(a, stream);
     if (e != cudaSuccess) return cuda_fail(e, "sparse launch");
+    return MLA_OK;
+}
+
+mla_status_t mla_prefill_sparse_host(const mla_seqs_t *seqs, int32_t num_heads, float sm_scale,
+                                     int64_t w_token_stride, int32_t topk, const mla_sparse_inputs_t *host_in,
+                                     const mla_sparse_inputs_t *dev_in, const mla_sparse_outputs_t *host_out,
+                                     const mla_sparse_outputs_t *dev_out, int32_t n_chunks, void *workspace,
+                                     size_t workspace_bytes, int32_t *dev_err, cudaStream_t stream) {
+    g_err.clear();
+    mla_status_t st = check_seqs(seqs);
+    if (st != MLA_OK) return st;
+    if (!host_in || !dev_in || !host_out || !dev_out)
+        return fail(MLA_ERR_INVALID_ARG, "host_in, dev_in, host_out and dev_out must be set");
+    const mla_sparse_inputs_t &hi = *host_in, &di = *dev_in;
+    const mla_sparse_outputs_t &ho = *host_out, &dO = *dev_out;
+    if (!hi.q_bf16 || !hi.qi_e4m3 || !hi.w || !hi.kv_e4m3 || !hi.kv_scale || !hi.ki_e4m3 || !hi.ki_scale ||
+        !ho.out_bf16 || !ho.idx)
+        return fail(MLA_ERR_INVALID_ARG, "every host pointer but lse must be set");
+    if (!ho.lse != !dO.lse) return fail(MLA_ERR_INVALID_ARG, "lse must be set on both sides or on neither");
+    if (!heads_ok(num_heads)) return fail(MLA_ERR_UNSUPPORTED, "num_heads must be 16, 32, 64 or 128 (got %d)", num_heads);
+    if ((st = check_indexer_args(seqs, di.qi_e4m3, di.w, w_token_stride, di.ki_e4m3, di.ki_scale, topk, dO.idx)) !=
+        MLA_OK)
+        return st;
+    if ((st = check_attn_ptrs(di.q_bf16, di.kv_e4m3, di.kv_scale, dO.out_bf16, dO.lse, sm_scale)) != MLA_OK) return st;
+    if (n_chunks < 1 || n_chunks > MLA_DENSE_HOST_MAX_CHUNKS)
+        return fail(MLA_ERR_INVALID_ARG, "n_chunks must be in [1, %d] (got %d)", MLA_DENSE_HOST_MAX_CHUNKS, n_chunks);
+    const int64_t tq = seqs->cu_seqlens_q_host[seqs->batch];
+    if (tq == 0) return MLA_OK;
+    // pieces on indexer group boundaries, each with its key chunk and work list
+    std::vector<int64_t> bnd(static_cast<size_t>(n_chunks) + 1);
+    bnd[0] = 0;
+    bnd[n_chunks] = tq;
+    for (int c = 1, b = 0; c < n_chunks; ++c) {
+        const int64_t t = tq * c / n_chunks;
+        while (b + 1 < seqs->batch && seqs->cu_seqlens_q_host[b + 1] <= t) ++b;
+        const int64_t c0 = seqs->cu_seqlens_q_host[b];
+        bnd[c] = std::max(bnd[c - 1], c0 + (t - c0) / mla::kIdxTokensPerCta * mla::kIdxTokensPerCta);
+    }
+    std::vector<int4> work;
+    std::vector<size_t> off(static_cast<size_t>(n_chunks) + 1, 0);
+    std::vector<int> chunk(static_cast<size_t>(n_chunks), mla::kIdxKeyChunkMax);
+    for (int c = 0; c < n_chunks; ++c) {
+        if (bnd[c + 1] > bnd[c]) {
+            chunk[c] = indexer_key_chunk(seqs, bnd[c], bnd[c + 1]);
+            const std::vector<int4> w = indexer_schedule(seqs, chunk[c], bnd[c], bnd[c + 1]);
+            work.insert(work.end(), w.begin(), w.end());
+        }
+        off[c + 1] = work.size();
+    }
+    const size_t sbytes = indexer_score_bytes(seqs);
+    const size_t need = sbytes + round_up(work.size() * sizeof(int4), kWsAlign);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+        return fail(MLA_ERR_WORKSPACE, "sparse from host needs %zu workspace bytes (256-byte aligned), got %zu", need,
+                    workspace ? workspace_bytes : 0);
+    int4 *dwork = reinterpret_cast<int4 *>(static_cast<char *>(workspace) + sbytes);
+    mla::IndexerArgs ia = indexer_args(seqs, di.qi_e4m3, di.w, w_token_stride, di.ki_e4m3, di.ki_scale, topk, dO.idx,
+                                       workspace, dev_err);
+    mla::AttnArgs aa = attn_args(seqs, di.q_bf16, num_heads, di.kv_e4m3, di.kv_scale, sm_scale, dO.out_bf16, dO.lse,
+                                 dev_err);
+    aa.idx = dO.idx;
+    aa.topk = topk;
+    CUtensorMap tmap_k, tmap_q;
+    if (!encode_rows128(&tmap_k, di.ki_e4m3, static_cast<uint64_t>(seqs->num_blocks) * 256, 128) ||
+        !encode_rows128(&tmap_q, di.qi_e4m3, static_cast<uint64_t>(tq) * 64, mla::kIdxTokensPerCta * 64))
+        return fail(MLA_ERR_CUDA, "tensor map encoding for the indexer failed");
+
+    HostPipe p;
+    cudaError_t e;
+    cudaEvent_t ev_entry, ev_end;
+#define MLA_TRY(x, what)                       \
+    if ((e = (x)) != cudaSuccess) return cuda_fail(e, what)
+    MLA_TRY(cudaStreamCreateWithFlags(&p.s_in, cudaStreamNonBlocking), "stream");
+    MLA_TRY(cudaStreamCreateWithFlags(&p.s_out, cudaStreamNonBlocking), "stream");
+    MLA_TRY(cudaStreamCreateWithFlags(&p.s_c[0], cudaStreamNonBlocking), "stream");
+    MLA_TRY(cudaStreamCreateWithFlags(&p.s_c[1], cudaStreamNonBlocking), "stream");
+    MLA_TRY(p.event(&ev_entry), "event");
+    MLA_TRY(p.event(&ev_end), "event");
+    MLA_TRY(cudaEventRecord(ev_entry, stream), "event record");
+    for (cudaStream_t x : {p.s_in, p.s_out, p.s_c[0], p.s_c[1]}) MLA_TRY(cudaStreamWaitEvent(x, ev_entry, 0), "wait");
+    // weights, caches and work lists first, then qi and q piece by piece
+    const size_t rows_kv = static_cast<size_t>(seqs->num_blocks) * 256;
+    const size_t w_floats = w_token_stride ? static_cast<size_t>(tq - 1) * static_cast<size_t>(w_token_stride) + 64 : 64;
+    MLA_TRY(cudaMemcpyAsync(di.w, hi.w, w_floats * sizeof(float), cudaMemcpyHostToDevice, p.s_in), "weight copy");
+    MLA_TRY(cudaMemcpyAsync(di.ki_e4m3, hi.ki_e4m3, rows_kv * 128, cudaMemcpyHostToDevice, p.s_in), "key copy");
+    MLA_TRY(cudaMemcpyAsync(di.ki_scale, hi.ki_scale, rows_kv * sizeof(float), cudaMemcpyHostToDevice, p.s_in),
+            "key scale copy");
+    MLA_TRY(cudaMemcpyAsync(di.kv_e4m3, hi.kv_e4m3, rows_kv * 576, cudaMemcpyHostToDevice, p.s_in), "cache copy");
+    MLA_TRY(cudaMemcpyAsync(di.kv_scale, hi.kv_scale, rows_kv * sizeof(float), cudaMemcpyHostToDevice, p.s_in),
+            "cache scale copy");
+    if (!work.empty())
+        MLA_TRY(cudaMemcpyAsync(dwork, work.data(), work.size() * sizeof(int4), cudaMemcpyHostToDevice, p.s_in),
+                "schedule upload");
+    const size_t q_row = static_cast<size_t>(num_heads) * 576 * 2, qi_row = 64 * 128,
+                 o_row = static_cast<size_t>(num_heads) * 512 * 2, l_row = static_cast<size_t>(num_heads) * sizeof(float),
+                 i_row = static_cast<size_t>(topk) * sizeof(int32_t);
+    auto at = [](const void *base, size_t bytes) { return static_cast<char *>(const_cast<void *>(base)) + bytes; };
+    for (int c = 0; c < n_chunks; ++c) {
+        if (bnd[c + 1] == bnd[c]) continue;
+        const size_t t0 = static_cast<size_t>(bnd[c]), nt = static_cast<size_t>(bnd[c + 1] - bnd[c]);
+        cudaEvent_t ev_in, ev_done;
+        MLA_TRY(p.event(&ev_in), "event");
+        MLA_TRY(p.event(&ev_done), "event");
+        MLA_TRY(cudaMemcpyAsync(at(di.qi_e4m3, t0 * qi_row), at(hi.qi_e4m3, t0 * qi_row), nt * qi_row,
+                                cudaMemcpyHostToDevice, p.s_in),
+                "indexer query copy");
+        MLA_TRY(cudaMemcpyAsync(at(di.q_bf16, t0 * q_row), at(hi.q_bf16, t0 * q_row), nt * q_row,
+                                cudaMemcpyHostToDevice, p.s_in),
+                "query copy");
+        MLA_TRY(cudaEventRecord(ev_in, p.s_in), "event record");
+        // pieces share no data (each writes its own score, index and output
+        // rows), so consecutive ones go to two streams
+        cudaStream_t cs = p.s_c[c & 1];
+        MLA_TRY(cudaStreamWaitEvent(cs, ev_in, 0), "wait");
+        mla::IndexerArgs a = ia;
+        a.key_chunk = chunk[c];
+        a.tok0 = bnd[c];
+        const int n_items = static_cast<int>(off[c + 1] - off[c]);
+        if (n_items > 0)
+            MLA_TRY(mla::launch_indexer_scores_tc(a, dwork + off[c], n_items, tmap_k, tmap_q, cs), "indexer score launch");
+        MLA_TRY(mla::launch_topk(a, static_cast<int64_t>(nt), cs), "top-k launch");
+        mla::AttnArgs sa = aa;
+        sa.tok_begin = bnd[c];
+        sa.tok_end = bnd[c + 1];
+        MLA_TRY(mla::launch_sparse_f8(sa, cs), "sparse launch");
+        MLA_TRY(cudaEventRecord(ev_done, cs), "event record");
+        MLA_TRY(cudaStreamWaitEvent(p.s_out, ev_done, 0), "wait");
+        MLA_TRY(cudaMemcpyAsync(at(ho.out_bf16, t0 * o_row), at(dO.out_bf16, t0 * o_row), nt * o_row,
+                                cudaMemcpyDeviceToHost, p.s_out),
+                "output copy");
+        if (ho.lse)
+            MLA_TRY(cudaMemcpyAsync(at(ho.lse, t0 * l_row), at(dO.lse, t0 * l_row), nt * l_row, cudaMemcpyDeviceToHost,
+                                    p.s_out),
+                    "lse copy");
+        MLA_TRY(cudaMemcpyAsync(at(ho.idx, t0 * i_row), at(dO.idx, t0 * i_row), nt * i_row, cudaMemcpyDeviceToHost,
+                                p.s_out),
+                "index copy");
+    }
+    MLA_TRY(cudaEventRecord(ev_end, p.s_out), "event record");
+    MLA_TRY(cudaStreamWaitEvent(stream, ev_end, 0), "wait");
+#undef MLA_TRY
     return MLA_OK;
 }
 

@@ -118,6 +118,38 @@ def test_dense_host_rejects_bad_arguments(lib):
         assert ws % 256 == 0 and ws >= (tiles // 2 + len(q_lens) + B.DENSE_HOST_MAX_CHUNKS) * 16
 
 
+def sparse_host(lib, s, hi=None, di=None, ho=None, do=None, topk=2048, chunks=4, ws=None, wsb=0, H=64):
+    full_in = B.mla_sparse_inputs_t(*([0x100000] * 7))
+    full_out = B.mla_sparse_outputs_t(0x100000, None, 0x100000)
+    hi, di = hi or full_in, di or full_in
+    ho, do = ho or full_out, do or full_out
+    return lib.mla_prefill_sparse_host(ctypes.byref(s.c), H, 0.07, 0, topk, ctypes.byref(hi), ctypes.byref(di),
+                                       ctypes.byref(ho), ctypes.byref(do), chunks, ws, wsb, None, None)
+
+
+def test_sparse_host_rejects_bad_arguments(lib):
+    s = HostSeqs([100], [0])
+    assert lib.mla_prefill_sparse_host(ctypes.byref(s.c), 64, 0.07, 0, 2048, None, None, None, None, 4, None, 0,
+                                       None, None) == B.MLA_ERR_INVALID_ARG
+    for i in range(7):                                      # each host input left out in turn
+        fields = [0x100000] * 7
+        fields[i] = None
+        assert sparse_host(lib, s, hi=B.mla_sparse_inputs_t(*fields)) == B.MLA_ERR_INVALID_ARG, i
+    for i in range(7):                                      # and each device input
+        fields = [0x100000] * 7
+        fields[i] = None
+        assert sparse_host(lib, s, di=B.mla_sparse_inputs_t(*fields)) == B.MLA_ERR_INVALID_ARG, i
+    assert sparse_host(lib, s, ho=B.mla_sparse_outputs_t(None, None, 0x100000)) == B.MLA_ERR_INVALID_ARG
+    assert sparse_host(lib, s, ho=B.mla_sparse_outputs_t(0x100000, 0x100000, 0x100000)) == B.MLA_ERR_INVALID_ARG
+    assert b"lse" in lib.mla_last_error()                   # lse on one side only
+    for c in (0, B.DENSE_HOST_MAX_CHUNKS + 1):
+        assert sparse_host(lib, s, chunks=c) == B.MLA_ERR_INVALID_ARG
+    assert sparse_host(lib, s, topk=0) == B.MLA_ERR_UNSUPPORTED
+    assert sparse_host(lib, s, H=48) == B.MLA_ERR_UNSUPPORTED
+    assert sparse_host(lib, s) == B.MLA_ERR_WORKSPACE
+    assert sparse_host(lib, HostSeqs([0, 0], [5, 0])) == B.MLA_OK
+
+
 def test_empty_batch_is_a_noop(lib):
     s = HostSeqs([0, 0], [5, 0])
     assert dense(lib, s) == B.MLA_OK

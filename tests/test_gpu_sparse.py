@@ -258,3 +258,50 @@ def test_chunked200k_selected_chunks():
             td = toks[:4]
             ora_d, ora_dl = O.mla_dense(sub, q[td], td, kv, ks, w.sm_scale)
             check_attention(bf16_to_np(outd[td]), ora_d, lsed[td].cpu().numpy(), ora_dl, "last chunk dense")
+
+
+@pytest.mark.parametrize("q_lens,prefix,H,chunks,per_token_w", [
+    ([50, 30], [700, 100], 64, 5, False),     # pieces cross a sequence boundary
+    ([64, 40], [3000, 200], 128, 3, True),    # one weight row per token, 128 heads
+    ([7], [300], 16, 64, False),              # more pieces than 3-token groups: some pieces empty
+])
+def test_sparse_from_host_matches_device_calls(q_lens, prefix, H, chunks, per_token_w):
+    """The host-to-host sparse step (copies overlapped with the indexer, top-k
+    and sparse attention of other pieces) returns exactly what the two device
+    calls return, and both match the oracle."""
+    import torch
+    from mla_prefill_attention_gb300 import mla_indexer_topk, mla_prefill_sparse, mla_prefill_sparse_host
+    pb = Problem(q_lens, prefix, H, seed=500 + H + chunks, with_indexer=True, sm_scale=0.08)
+    T, topk = pb.ps.total_q, 256
+    w = pb.w
+    if per_token_w:
+        rng = np.random.default_rng(7)
+        w = (2.0 ** -rng.integers(0, 5, (T, 64))).astype(np.float32)
+    stride = 64 if per_token_w else 0
+    d = pb.device()
+    dw = torch.from_numpy(w).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx_d = mla_indexer_topk(d["seqs"], d["qi"], dw, stride, d["ki"], d["kis"], topk, dev_err=err)
+    out_d, lse_d = mla_prefill_sparse(d["seqs"], d["q"], d["kv"], d["ks"], pb.sm_scale, idx_d, dev_err=err)
+    torch.cuda.synchronize()
+    host_in = {"q": torch.from_numpy(pb.q.view(np.int16)).view(torch.bfloat16), "qi": torch.from_numpy(pb.qi),
+               "w": torch.from_numpy(w), "kv": torch.from_numpy(pb.kv), "ks": torch.from_numpy(pb.ks),
+               "ki": torch.from_numpy(pb.ki), "kis": torch.from_numpy(pb.kis)}
+    host_in = {k: v.pin_memory() for k, v in host_in.items()}
+    dev_in = {k: torch.zeros_like(v, device="cuda") for k, v in host_in.items()}
+    host_out = {"out": torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory(),
+                "lse": torch.empty((T, H), dtype=torch.float32).pin_memory(),
+                "idx": torch.empty((T, topk), dtype=torch.int32).pin_memory()}
+    dev_out = {k: torch.zeros_like(v, device="cuda") for k, v in host_out.items()}
+    mla_prefill_sparse_host(d["seqs"], host_in, dev_in, host_out, dev_out, pb.sm_scale, w_token_stride=stride,
+                            topk=topk, n_chunks=chunks, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(host_out["idx"], idx_d.cpu())
+    assert torch.equal(host_out["out"].view(torch.int16), out_d.cpu().view(torch.int16))
+    assert torch.equal(host_out["lse"], lse_d.cpu())
+    toks = np.arange(T)
+    ref = O.indexer_topk(pb.ps, pb.qi, w, stride, toks, pb.ki, pb.kis, topk)
+    assert np.array_equal(np.sort(ref, axis=1), np.sort(host_out["idx"].numpy(), axis=1))
+    ora, ora_lse = O.mla_sparse(pb.ps, pb.q, toks, pb.kv, pb.ks, pb.sm_scale, host_out["idx"].numpy())
+    check_attention(bf16_to_np(host_out["out"]), ora, host_out["lse"].numpy(), ora_lse, f"sparse from host {q_lens}")
