@@ -143,6 +143,33 @@ def test_indexer_clustered_winners():
     assert np.all(np.diff(got, axis=1) > 0)
 
 
+def test_indexer_radix_fallback():
+    """The key scales at the 1,024 evenly spaced sample positions of the row are
+    2^-10 times the others (exact), so the sample sees only tiny scores and the
+    bracket it gives holds far more than k scores above it: the top-k must take
+    its exact radix path and still match the oracle. The premise is checked on
+    the oracle's scores with the sampled bracket's rule."""
+    pb = Problem([1], [30000], 16, seed=36, with_indexer=True)
+    n, k = 30001, 1000
+    bt = pb.ps.block_table[0]
+    kis = pb.kis.copy()
+    samp_pos = (np.arange(1024) * n) // 1024
+    for s in samp_pos:
+        kis[bt[s // 256], s % 256] *= 2.0 ** -10
+    pb.kis = kis
+    d = pb.device()
+    idx = run_indexer(pb, d, k)
+    ref, sc = O.indexer_topk(pb.ps, pb.qi, pb.w, 0, np.arange(1), pb.ki, pb.kis, k, want_scores=True, ctx_cap=n)
+    row = sc[0, :n]
+    samp = np.sort(row[samp_pos])[::-1]
+    e = k * 1024 / n
+    t_hi = samp[int(np.floor(e - (4 * np.sqrt(e) + 2)))]
+    assert np.count_nonzero(row > t_hi) > k                  # the bracket misses
+    got = idx.cpu().numpy()
+    assert np.array_equal(np.sort(ref, axis=1), np.sort(got, axis=1))
+    assert np.all(np.diff(got[0]) > 0)
+
+
 def test_indexer_ties_go_to_lower_position():
     """Keys repeat three rows, so whole groups of scores tie at the cut."""
     import torch
