@@ -427,7 +427,7 @@ RUNS = {"tiny512": DenseRun, "prefix12k": DenseRun, "dense32k": DenseRun, "ragge
 # None until it is captured again.
 TRAFFIC = {
     "dense32k": {"attention": 2453488384 + 2118204416},
-    "sparse64k": {"indexer_topk": 76614912 + 1955293952 + 2014218496 + 63028224,
+    "sparse64k": {"indexer_topk": 76614912 + 1955293952 + 2015314176 + 66477312,
                   "sparse_attention": 807216896 + 533257472},
 }
 

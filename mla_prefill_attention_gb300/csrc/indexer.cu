@@ -14,6 +14,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace mla {
 namespace idx {
@@ -711,6 +712,13 @@ __global__ void __launch_bounds__(TK_NT, 2) topk_kernel(const IndexerArgs a) {
     }
     const float *row = a.scores + t * a.score_stride;
     const float4 *row4 = reinterpret_cast<const float4 *>(row);
+    if (threadIdx.x == 0) {
+        // the whole row into L2 while the sample is read and sorted, so the pass
+        // over it reads L2 (rows start 16-byte aligned; whole float4s)
+        const uint32_t bytes = static_cast<uint32_t>((n + 3) >> 2) * 16u;
+        for (uint32_t off = 0; off < bytes; off += 65536u)
+            tc::bulk_prefetch_l2(reinterpret_cast<const char *>(row) + off, min(65536u, bytes - off));
+    }
     if (!topk_sampled(a, row, row4, n, out, cand, hist, sel, wcnt, info, st, wsum)) {
         __syncthreads();
         topk_radix(a, row4, n, out, cand, hist, sel, st, wsum);
