@@ -207,7 +207,7 @@ class DenseRun:
 
 class SparseRun:
     """One step = mla_indexer_topk + mla_prefill_sparse over every new token."""
-    launches_per_step = 3
+    launches_per_step = 2
 
     def __init__(self, w, dev):
         import torch
@@ -231,6 +231,7 @@ class SparseRun:
         self.tokens = T
         self.indexer_flops = F.indexer_flops(w.q_lens, w.prefix_lens)
         self.sparse_flops = F.sparse_flops(w.q_lens, w.prefix_lens, H, w.topk)
+        self.sparse_gathered_bytes = F.sparse_gathered_bytes(w.q_lens, w.prefix_lens, w.topk)
         self.flops = self.sparse_flops + self.indexer_flops
         self.min_bytes = None
         self.mid = []          # events between the two calls, one per step, when recording
@@ -303,14 +304,15 @@ class SparseRun:
 
 
 class ChunkedRun:
-    """One step = the whole chunked prefill of a long prompt: for every chunk,
+    """One step = the whole chunked prefill of a long prompt through the
+    library's chunk driver (chunked_prefill_sparse): for every chunk,
     mla_indexer_topk + mla_prefill_sparse after the cached prefix of the earlier
     chunks. Every chunk's queries are resident in HBM before timing. Also times
     the dense path on the final chunk (reported beside the step)."""
 
     def __init__(self, w, dev):
         import torch
-        from mla_prefill_attention_gb300 import MLA_OP_DENSE, MLA_OP_INDEXER, Seqs, chunk_bounds, inputs as I
+        from mla_prefill_attention_gb300 import MLA_OP_DENSE, MLA_OP_INDEXER, chunk_bounds, chunk_seqs, inputs as I
         from mla_prefill_attention_gb300 import mla_workspace_size
         from mla_prefill_attention_gb300 import flops as F
         self.w, self.dev = w, dev
@@ -322,20 +324,15 @@ class ChunkedRun:
         self.host = dict(kv=kv, ks=ks, ki=ki, kis=kis, w=wh)
         self.d = {k: torch.from_numpy(v).to(dev) for k, v in self.host.items()}
         self.bounds = chunk_bounds(N, w.chunk)
-        self.chunks = []
-        max_c = max(e - s for s, e in self.bounds)
-        ws = 0
-        for s, e in self.bounds:
-            sub = I.PagedSeqs(np.array([0, e - s], np.int32), np.array([s], np.int32), self.ps.block_table,
-                              self.ps.num_blocks)
-            seqs = Seqs.from_paged(sub, device=dev)
+        self.seqs = chunk_seqs(self.ps.block_table, self.ps.num_blocks, N, w.chunk, device=dev)
+        self.q, self.qi = {}, {}
+        for c, (s, e) in enumerate(self.bounds):
             q = I.gen_q_bf16(w.seed, N, w.heads, token_rows=np.arange(s, e))
-            qi = I.gen_indexer_q(w.seed, N, token_rows=np.arange(s, e))
-            self.chunks.append(dict(seqs=seqs, sub=sub, q=torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).to(dev),
-                                    qi=torch.from_numpy(qi).to(dev)))
-            ws = max(ws, mla_workspace_size(MLA_OP_INDEXER, seqs, 64, w.topk))
-        last = self.chunks[-1]["seqs"]
-        ws = max(ws, mla_workspace_size(MLA_OP_DENSE, last, w.heads))
+            self.q[s] = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).to(dev)
+            self.qi[s] = torch.from_numpy(I.gen_indexer_q(w.seed, N, token_rows=np.arange(s, e))).to(dev)
+        max_c = max(e - s for s, e in self.bounds)
+        ws = max(mla_workspace_size(MLA_OP_INDEXER, sq, 64, w.topk) for sq in self.seqs)
+        ws = max(ws, mla_workspace_size(MLA_OP_DENSE, self.seqs[-1], w.heads), 16)
         H = w.heads
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
         self.out = torch.empty((max_c, H, 512), dtype=torch.bfloat16, device=dev)
@@ -344,26 +341,29 @@ class ChunkedRun:
         self.tokens = N
         self.indexer_flops = F.indexer_flops(w.q_lens, w.prefix_lens)
         self.sparse_flops = F.sparse_flops(w.q_lens, w.prefix_lens, H, w.topk)
+        self.sparse_gathered_bytes = F.sparse_gathered_bytes(w.q_lens, w.prefix_lens, w.topk)
         self.flops = self.sparse_flops + self.indexer_flops
-        self.launches_per_step = 3 * len(self.bounds)
+        self.launches_per_step = 2 * len(self.bounds)
         self.chunk_ms = [0.0] * len(self.bounds)
         self.ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in self.bounds]
         self.min_bytes = None
 
-    def _chunk(self, c):
-        from mla_prefill_attention_gb300 import mla_indexer_topk, mla_prefill_sparse
-        ch, d, n = self.chunks[c], self.d, self.bounds[c][1] - self.bounds[c][0]
-        mla_indexer_topk(ch["seqs"], ch["qi"], d["w"], 0, d["ki"], d["kis"], self.w.topk, idx_out=self.idx[:n],
-                         workspace=self.ws)
-        self.ev[c][1].record()
-        mla_prefill_sparse(ch["seqs"], ch["q"], d["kv"], d["ks"], self.w.sm_scale, self.idx[:n], out=self.out[:n],
-                           lse=self.lse[:n])
-
     def step(self):
-        for c in range(len(self.bounds)):
+        from mla_prefill_attention_gb300 import chunked_prefill_sparse
+        d = self.d
+        nxt = {"c": None}
+
+        def before(c):
+            if c > 0:
+                self.ev[c - 1][2].record()
             self.ev[c][0].record()
-            self._chunk(c)
-            self.ev[c][2].record()
+
+        chunked_prefill_sparse(self.ps.block_table, self.ps.num_blocks, self.tokens, self.w.chunk,
+                               lambda s, e: self.q[s], d["kv"], d["ks"], lambda s, e: self.qi[s], d["w"], 0,
+                               d["ki"], d["kis"], self.w.sm_scale, topk=self.w.topk, on_chunk=lambda *a: None,
+                               out=self.out, lse=self.lse, idx=self.idx, workspace=self.ws, seqs_list=self.seqs,
+                               before_chunk=before, after_indexer=lambda c: self.ev[c][1].record())
+        self.ev[-1][2].record()
 
     def collect_chunk_ms(self):
         """Per-chunk times of the last step, and the two calls' totals over all chunks."""
@@ -374,10 +374,10 @@ class ChunkedRun:
         """The dense path on the final chunk (same inputs), median of reps calls."""
         import torch
         from mla_prefill_attention_gb300 import mla_prefill_dense
-        ch, d = self.chunks[-1], self.d
-        n = self.bounds[-1][1] - self.bounds[-1][0]
-        call = lambda: mla_prefill_dense(ch["seqs"], ch["q"], d["kv"], d["ks"], self.w.sm_scale, out=self.out[:n],
-                                         lse=self.lse[:n], workspace=self.ws)
+        d = self.d
+        s, e = self.bounds[-1]
+        call = lambda: mla_prefill_dense(self.seqs[-1], self.q[s], d["kv"], d["ks"], self.w.sm_scale,
+                                         out=self.out[:e - s], lse=self.lse[:e - s], workspace=self.ws)
         call()
         times = []
         for _ in range(reps):
@@ -404,7 +404,8 @@ class ChunkedRun:
             c = int(rng.integers(0, len(self.bounds)))
             s, e = self.bounds[c]
             t = int(rng.integers(0, e - s))
-            sub = self.chunks[c]["sub"]
+            sub = I.PagedSeqs(np.array([0, e - s], np.int32), np.array([s], np.int32), self.ps.block_table,
+                              self.ps.num_blocks)
             q = I.gen_q_bf16(w.seed, w.q_lens[0], w.heads, token_rows=np.array([s + t]))
             qi = I.gen_indexer_q(w.seed, w.q_lens[0], token_rows=np.array([s + t]))
             t0 = time.perf_counter()
@@ -427,7 +428,7 @@ RUNS = {"tiny512": DenseRun, "prefix12k": DenseRun, "dense32k": DenseRun, "ragge
 # None until it is captured again.
 TRAFFIC = {
     "dense32k": {"attention": 2453488384 + 2118204416},
-    "sparse64k": {"indexer_topk": 76614912 + 1955293952 + 2015314176 + 66477312,
+    "sparse64k": {"indexer_topk": None,
                   "sparse_attention": 807216896 + 533257472},
 }
 
@@ -582,6 +583,112 @@ def config_of(w):
     return c
 
 
+def e4m3_peak():
+    """Dense e4m3 tensor peak: the measured sustained bf16 figure times the
+    nominal e4m3:bf16 ratio of 2 (no e4m3 GEMM is measured)."""
+    pk, src = peaks()
+    bf16 = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
+    return 2.0 * bf16, f"e4m3 dense = 2 x {src} bf16 sustained ({bf16:.1f} TFLOP/s; the nominal e4m3:bf16 ratio)"
+
+
+def sparse_attention_roof(run, att_ms):
+    """Sparse attention against both bounds: the e4m3 tensor roof (its MMAs
+    are e4m3) and min(tensor, HBM x AI) with every selected row counted as read
+    from HBM (the pessimistic gathered-bytes bound; unique cache rows fit L2)."""
+    pk, src = peaks()
+    peak, psrc = e4m3_peak()
+    tf = run.sparse_flops / (att_ms / 1000.0) / 1e12
+    hbm = float(pk["hbm_gbs"])
+    ai = run.sparse_flops / run.sparse_gathered_bytes
+    roof_ai = min(peak, hbm * ai / 1000.0)
+    return {"ms": att_ms, "achieved": tf, "unit": "TFLOP/s", "tensor_peak": peak, "frac_tensor": tf / peak,
+            "ai_flop_per_byte": ai, "hbm_gbs": hbm, "hbm_x_ai_roof": roof_ai, "frac_hbm_x_ai": tf / roof_ai,
+            "gathered_bytes": run.sparse_gathered_bytes, "traffic": TRAFFIC.get(run.w.name, {}).get("sparse_attention"),
+            "peak_source": f"{psrc}; {src} hbm_gbs (copy)",
+            "kernel": "attn_f8_kernel<sparse>: tcgen05 e4m3, rows gathered by index"}
+
+
+def roofline_of(run, per_ms):
+    """(attention TFLOP/s, roofline object of the dominant kernel) of a timed run."""
+    peak, psrc = e4m3_peak()
+    kern_ms = statistics.mean(per_ms)
+    tflops = run.flops / (kern_ms / 1000.0) / 1e12
+    if isinstance(run, DenseRun):
+        roof = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                "traffic": TRAFFIC.get(run.w.name, {}).get("attention"),
+                "algorithmic_tflop": run.flops / 1e12, "peak_source": psrc,
+                "note": "algorithmic FLOPs (2,176 per visible query-key-head triple) over the e4m3 roof; the kernel "
+                        "issues two e4m3 MMAs per algorithmic product (two-term Q and P)",
+                "kernel": "attn_f8_kernel: tcgen05 kind::f8f6f4, e4m3 cache tiles by TMA, two-term e4m3 Q and P, "
+                          "64 rows x 128 keys"}
+        return tflops, roof
+    if isinstance(run, SparseRun):
+        idx_ms, att_ms = statistics.mean(run.split_ms[0]), statistics.mean(run.split_ms[1])
+        traffic = TRAFFIC.get(run.w.name, {}).get("indexer_topk")
+        kernel = "indexer_topk_kernel: tcgen05 e4m3 scores, streaming exact top-k in shared memory"
+    else:
+        run.collect_chunk_ms()
+        idx_ms, att_ms = run.split_total
+        traffic = None
+        kernel = "indexer_topk_kernel over all chunks: tcgen05 e4m3 scores, streaming exact top-k"
+    idx_tf = run.indexer_flops / (idx_ms / 1000.0) / 1e12
+    roof = {"bound": "tensor", "achieved": idx_tf, "peak": peak, "unit": "TFLOP/s", "frac": idx_tf / peak,
+            "traffic": traffic, "peak_source": psrc, "kernel": kernel + ", the larger share of the step",
+            "split_ms": {"indexer_topk": idx_ms, "sparse_attention": att_ms},
+            "sparse_attention": sparse_attention_roof(run, att_ms)}
+    return tflops, roof
+
+
+def measure_workload(name, dev, steps, warmup):
+    """One workload timed on its own (W warm-up steps, then K), for the extra
+    objects of the default line: per-step time, throughput and rooflines."""
+    import torch
+    from mla_prefill_attention_gb300 import inputs as I
+    w = I.WORKLOADS[name]
+    run = RUNS[name](w, dev)
+    total_ms, per_ms = time_steps(run, steps, warmup)
+    tflops, roof = roofline_of(run, per_ms)
+    obj = {"workload": name, "steps": steps, "warmup": warmup, "ms_per_step": total_ms / steps,
+           "value": run.tokens * steps / (total_ms / 1000.0), "unit": "tok/s", "attention_tflops": tflops,
+           "roofline": roof, "config": config_of(w)}
+    if isinstance(run, ChunkedRun):
+        obj["chunks"] = {"count": len(run.bounds), "chunk_tokens": w.chunk,
+                         "ms_per_chunk_last_step": [round(x, 3) for x in run.chunk_ms],
+                         "total_ms_last_step": round(sum(run.chunk_ms), 3),
+                         "dense_last_chunk_ms": run.dense_last_chunk_ms(),
+                         "sparse_last_chunk_ms": round(run.chunk_ms[-1], 3)}
+    del run
+    torch.cuda.empty_cache()
+    return obj
+
+
+def cpu_info():
+    """CPU model and the cores this process may run on (for the CPU baseline)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model", "hardware")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:
+        try:
+            model = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            model = next((l.split(":", 1)[1].strip() for l in model.splitlines() if l.startswith("Model name")), None)
+        except (OSError, subprocess.SubprocessError):
+            model = None
+    try:
+        affinity = len(os.sched_getaffinity(0))
+    except AttributeError:
+        affinity = os.cpu_count() or 1
+    return {"cpu_model": model, "affinity_cores": affinity}
+
+
+EXTRA_WORKLOADS = ("prefix12k", "ragged4", "sparse64k", "chunked200k")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -594,6 +701,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kv-append", action="store_true", help="skip the separate cache-write measurement")
     ap.add_argument("--no-merge", action="store_true", help="skip the separate partial-result merge measurement")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads' objects")
     args = ap.parse_args()
 
     from mla_prefill_attention_gb300 import inputs as I
@@ -601,7 +709,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    cinfo = cpu_info()
+    cores = int(os.environ.get("OMP_NUM_THREADS", cinfo["affinity_cores"]))
 
     if args.impl == "reference":
         # the reference arm is the fp64 CPU oracle, on rank 0 only
@@ -620,19 +729,24 @@ def main():
         from mla_prefill_attention_gb300 import flops as F
         total_flops = F.dense_flops(w.q_lens, w.prefix_lens, w.heads)
         budget = max(2.0, 120.0 / max(1, args.steps + args.warmup))
-        rates = []
+        rates, sampled = [], 0
         for i in range(args.warmup + args.steps):
             n, dt, fl = run.oracle_rate(budget, seed=i)
             if i >= args.warmup:
-                rates.append(w_tokens := run.ps.total_q / (dt * total_flops / fl))
+                rates.append(run.ps.total_q / (dt * total_flops / fl))
+                sampled += n
         val = statistics.median(rates)
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tok/s", "n_gpus": 1,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * run.ps.total_q / val,
+                "extrapolated": True, "sampled_tokens_per_step": sampled // max(1, args.steps),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": config_of(w),
                 "cpu_baseline": {"value": val, "unit": "tok/s", "cores": cores, "kind": "oracle",
-                                 "sample": f"{n} random query tokens x {w.heads} heads per step, extrapolated by "
-                                           f"algorithmic FLOPs to all {run.ps.total_q} tokens"},
+                                 "extrapolated": True, "sampled_tokens_per_step": sampled // max(1, args.steps),
+                                 **cinfo,
+                                 "sample": f"random query tokens x {w.heads} heads per step (about "
+                                           f"{sampled // max(1, args.steps)}), timed, extrapolated by algorithmic "
+                                           f"FLOPs to all {run.ps.total_q} tokens"},
                 "e2e": {"value": val, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -661,45 +775,7 @@ def main():
 
     ms_per_step = total_ms / args.steps
     value = job_throughput(world, run.tokens, args.steps, total_ms)
-    kern_ms = statistics.mean(per_ms)
-    tflops = run.flops / (kern_ms / 1000.0) / 1e12
-    pk, src = peaks()
-    peak = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
-    if isinstance(run, DenseRun):
-        # Each algorithmic FLOP runs as two e4m3 tensor FLOPs (the two-term Q and P), at
-        # twice the bf16 rate: the fraction is the same against either roof.
-        roof = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
-                "traffic": TRAFFIC.get(w.name, {}).get("attention"),
-                "peak_source": f"{src} bf16 sustained; the kernel runs each algorithmic FLOP as two e4m3 tensor "
-                               f"FLOPs at twice the bf16 rate, so this equals the e4m3 roof",
-                "kernel": "attn_f8_kernel: tcgen05 kind::f8f6f4, e4m3 cache tiles by TMA, two-term e4m3 Q and P, "
-                          "64 rows x 128 keys"}
-    elif getattr(run, "split_ms", None):
-        idx_ms, att_ms = statistics.mean(run.split_ms[0]), statistics.mean(run.split_ms[1])
-        idx_tf = run.indexer_flops / (idx_ms / 1000.0) / 1e12
-        att_tf = run.sparse_flops / (att_ms / 1000.0) / 1e12
-        tr = TRAFFIC.get(w.name, {})
-        roof = {"bound": "tensor", "achieved": idx_tf, "peak": 2 * peak, "unit": "TFLOP/s",
-                "frac": idx_tf / (2 * peak), "traffic": tr.get("indexer_topk"),
-                "peak_source": f"e4m3 dense = 2 x {src} bf16 sustained (the nominal e4m3:bf16 ratio)",
-                "kernel": "mla_indexer_topk (indexer scores on tcgen05 e4m3 + exact top-k), the larger share",
-                "split_ms": {"indexer_topk": idx_ms, "sparse_attention": att_ms},
-                "sparse_attention": {"achieved": att_tf, "peak": peak, "frac": att_tf / peak,
-                                     "traffic": tr.get("sparse_attention"),
-                                     "kernel": "attn_f8_kernel<sparse>: tcgen05 e4m3, gathered rows"}}
-    else:   # chunked: the last step's per-call totals over all chunks
-        run.collect_chunk_ms()
-        idx_ms, att_ms = run.split_total
-        idx_tf = run.indexer_flops / (idx_ms / 1000.0) / 1e12
-        att_tf = run.sparse_flops / (att_ms / 1000.0) / 1e12
-        roof = {"bound": "tensor", "achieved": idx_tf, "peak": 2 * peak, "unit": "TFLOP/s",
-                "frac": idx_tf / (2 * peak), "traffic": None,
-                "peak_source": f"e4m3 dense = 2 x {src} bf16 sustained (the nominal e4m3:bf16 ratio)",
-                "kernel": "mla_indexer_topk over all chunks (indexer scores on tcgen05 e4m3 + exact top-k), the "
-                          "larger share",
-                "split_ms": {"indexer_topk": idx_ms, "sparse_attention": att_ms},
-                "sparse_attention": {"achieved": att_tf, "peak": peak, "frac": att_tf / peak,
-                                     "kernel": "attn_f8_kernel<sparse>: tcgen05 e4m3, gathered rows"}}
+    tflops, roof = roofline_of(run, per_ms)
     line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
@@ -710,9 +786,9 @@ def main():
     if clk:
         line["clocks"] = clk
     if isinstance(run, ChunkedRun):
-        run.collect_chunk_ms()
         line["chunks"] = {"count": len(run.bounds), "chunk_tokens": run.w.chunk,
                           "ms_per_chunk_last_step": [round(x, 3) for x in run.chunk_ms],
+                          "total_ms_last_step": round(sum(run.chunk_ms), 3),
                           "dense_last_chunk_ms": run.dense_last_chunk_ms(),
                           "sparse_last_chunk_ms": round(run.chunk_ms[-1], 3)}
     if rank == 0 and not args.no_e2e:
@@ -731,8 +807,20 @@ def main():
         n, dt, fl = run.oracle_rate(args.cpu_budget)
         val = run.tokens / (dt * run.flops / fl)
         line["cpu_baseline"] = {"value": val, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                                "extrapolated": True, "sampled_tokens": n, **cinfo,
                                 "sample": f"{n} random query tokens x all heads of the {w.name} workload "
                                           f"({dt:.1f} s), extrapolated by algorithmic FLOPs"}
+    del run
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_extras:
+        # the other workloads, each timed on its own outside the headline's timed region
+        extras = {}
+        for name in EXTRA_WORKLOADS:
+            if name == w.name:
+                continue
+            k = 2 if name == "chunked200k" else min(args.steps, 5)
+            extras[name] = measure_workload(name, dev, k, max(3, min(args.warmup, 3)))
+        line["workloads"] = extras
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:

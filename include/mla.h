@@ -24,7 +24,7 @@
  *   indexer keys   ki      e4m3  [num_blocks, 256, 128]
  *   indexer scale  ki_scale f32  [num_blocks, 256]
  *   top-k indices  idx     int32 [Tq, topk]  positions within the sequence,
- *                                            ascending, -1 padding at the end
+ *                                            distinct, -1 padding at the end
  * Position s of sequence b lives at page block_table[b*max_blocks_per_seq +
  * s/256], slot s%256. New token i of sequence b is at position prefix_lens[b]
  * + i and attends to positions 0..prefix_lens[b]+i (itself included); its
@@ -67,6 +67,10 @@ typedef enum {
 #define MLA_DEVERR_BAD_INDEX 2  /* sparse index outside [-1, position of the query] */
 #define MLA_DEVERR_TIMEOUT 4    /* a bounded wait inside a kernel gave up; that CTA's rows are not written */
 #define MLA_DEVERR_INTERNAL 8   /* a kernel invariant failed (a library bug); the row is -1 filled */
+#define MLA_DEVERR_SEQ_MISMATCH 16  /* the device cu_seqlens_q disagrees with its host mirror: no row at or
+                                       past the host's count is read or written; a unit of work (a pair of
+                                       row tiles, a group of indexer tokens) that either side does not
+                                       count in full is skipped whole, leaving its rows unwritten */
 
 typedef enum {
     MLA_OP_DENSE = 0,
@@ -114,13 +118,19 @@ mla_status_t mla_prefill_dense(const mla_seqs_t *seqs, const void *q_bf16, int32
  * and a 4-byte scale per key). For new token t at position p:
  *   score(t,s) = ki_scale_s * sum_{h<64} w[t,h] * max(0, sum_{d<128} dec(qi[t,h,d]) * dec(ki_s[d]))
  * for s = 0..p; idx[t,:] = the min(topk, p+1) positions with the largest
- * scores, ties going to the lower position, written in ascending position
- * order and padded with -1. Scores are accumulated in fp32 (exact when q and
- * k hold small integers). w_token_stride 0 shares one 64-value row among all
- * tokens; otherwise it is a multiple of 4. topk in [1, 2048]. qi, ki, w
- * 16-byte aligned. workspace:
- * mla_workspace_size(MLA_OP_INDEXER, ...) bytes (fp32 scores of every
- * visible (token, position) pair plus scheduling data). */
+ * scores, ties going to the lower position. A row with p+1 <= topk holds
+ * 0..p and then -1; a longer row holds its topk distinct positions in an
+ * order that is fixed for given inputs (not necessarily ascending). Scores
+ * are accumulated in fp32 (exact when q and k hold small integers).
+ * w_token_stride 0 shares one 64-value row among all
+ * tokens; otherwise it is a multiple of 4. topk in [1, 2048]. qi, ki, w and
+ * ki_scale 16-byte aligned. The scores never leave the GPU's on-chip memory:
+ * one CTA streams every key a group of three tokens can see and keeps each
+ * token's candidates in shared memory (a threshold set from a sample of the
+ * keys decides which enter; a group the fast path cannot finish exactly is
+ * redone by an exact streaming pass). workspace: mla_workspace_size(
+ * MLA_OP_INDEXER, ...) bytes: a 16-byte work item and a 4-byte flag per group
+ * of three tokens, whatever the context length. */
 mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, const float *w,
                               int64_t w_token_stride, const uint8_t *ki_e4m3, const float *ki_scale,
                               int32_t topk, int32_t *idx_out, void *workspace, size_t workspace_bytes,
@@ -158,8 +168,13 @@ mla_status_t mla_prefill_sparse(const mla_seqs_t *seqs, const void *q_bf16, int3
  * calls whose work overlaps on the GPU (different streams, no ordering
  * between them) race and may return wrong results; calls on one stream are
  * ordered and safe. Nothing in the array needs to start at zero: each call
- * writes every entry it reads. A batch needing more than
- * MLA_DENSE_STATIC_MAX_WORK_ITEMS items returns MLA_ERR_UNSUPPORTED. */
+ * writes every entry it reads. The array's address is looked up once per
+ * device and kept for the life of the process: after cudaDeviceReset() on a
+ * device, do not call this entry point on that device again. A batch needing
+ * more than MLA_DENSE_STATIC_MAX_WORK_ITEMS items returns
+ * MLA_ERR_UNSUPPORTED. The work list is built on the GPU from the device
+ * cu_seqlens_q; if it disagrees with the host mirror, MLA_DEVERR_SEQ_MISMATCH
+ * is set and only rows both count are computed. */
 mla_status_t mla_prefill_dense_static(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads,
                                       const uint8_t *kv_e4m3, const float *kv_scale, float sm_scale,
                                       void *out_bf16, float *lse, int32_t *dev_err, cudaStream_t stream);

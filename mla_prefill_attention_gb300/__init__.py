@@ -8,6 +8,7 @@ CPU or PyTorch implementation.
 from .binding import (  # noqa: F401
     MLA_DEVERR_BAD_INDEX,
     MLA_DEVERR_BAD_PAGE,
+    MLA_DEVERR_SEQ_MISMATCH,
     MLA_OP_DENSE,
     MLA_OP_DENSE_HOST,
     MLA_OP_INDEXER,
@@ -15,6 +16,7 @@ from .binding import (  # noqa: F401
     MlaError,
     Seqs,
     chunk_bounds,
+    chunk_seqs,
     chunked_prefill_sparse,
     mla_indexer_topk,
     mla_kv_append,

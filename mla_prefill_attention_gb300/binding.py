@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libmla.so")
 
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_WORKSPACE = range(5)
 MLA_DEVERR_BAD_PAGE, MLA_DEVERR_BAD_INDEX, MLA_DEVERR_TIMEOUT, MLA_DEVERR_INTERNAL = 1, 2, 4, 8
+MLA_DEVERR_SEQ_MISMATCH = 16
 MLA_OP_DENSE, MLA_OP_INDEXER, MLA_OP_SPARSE, MLA_OP_DENSE_HOST = 0, 1, 2, 3
 
 EXPORTS = ("mla_workspace_size", "mla_prefill_dense", "mla_indexer_topk", "mla_prefill_sparse", "mla_last_error",
@@ -231,7 +232,7 @@ def mla_prefill_sparse_host(seqs: Seqs, host_in: dict, dev_in: dict, host_out: d
 def mla_indexer_topk(seqs: Seqs, qi: torch.Tensor, w: torch.Tensor, w_token_stride: int, ki: torch.Tensor,
                      ki_scale: torch.Tensor, topk: int = 2048, idx_out=None, workspace=None, dev_err=None):
     """Indexer scores + exact top-k. qi uint8 [Tq,64,128]; w f32; ki uint8 [nb,256,128].
-    Returns idx int32 [Tq, topk] (ascending positions, -1 padded)."""
+    Returns idx int32 [Tq, topk] (distinct positions in a fixed order, -1 padded)."""
     if idx_out is None:
         idx_out = torch.empty((qi.shape[0], topk), dtype=torch.int32, device=qi.device)
     ws, wsb = _workspace(MLA_OP_INDEXER, seqs, 64, topk, workspace)
@@ -294,23 +295,48 @@ def chunk_bounds(total: int, chunk: int):
     return [(s, min(s + chunk, total)) for s in range(0, total, chunk)]
 
 
+def chunk_seqs(block_table, num_blocks: int, total: int, chunk: int, device="cuda"):
+    """One Seqs per prefill chunk of a prompt of `total` tokens: chunk c holds
+    the new tokens [c*chunk, min((c+1)*chunk, total)) after a cached prefix of
+    c*chunk tokens, over the prompt's block-table row."""
+    return [Seqs([0, e - s], [s], block_table, num_blocks, device=device) for s, e in chunk_bounds(total, chunk)]
+
+
 def chunked_prefill_sparse(block_table, num_blocks: int, total: int, chunk: int, q_chunk_fn, kv, kv_scale, qi_chunk_fn,
                            w, w_token_stride: int, ki, ki_scale, sm_scale: float, topk: int = 2048,
-                           on_chunk=None, dev_err=None):
+                           on_chunk=None, dev_err=None, out=None, lse=None, idx=None, workspace=None,
+                           seqs_list=None, before_chunk=None, after_indexer=None):
     """Chunked prefill of one prompt of `total` tokens (GLM-5.3-Flash page,
     section on snapshots: prompts are read in fixed-size chunks). Chunk c covers
     new tokens [c*chunk, min((c+1)*chunk, total)) after a cached prefix of
     c*chunk tokens; each runs the indexer + top-k and then sparse MLA over the
     selected rows. q_chunk_fn(start, end) / qi_chunk_fn(start, end) return the
     chunk's device query tensors. on_chunk(c, start, end, out, lse, idx) sees
-    every chunk's result (the caller keeps what it needs)."""
+    every chunk's result (the caller keeps what it needs); without it the
+    results are returned as a list.
+
+    out, lse, idx: optional device buffers of at least `chunk` rows, reused by
+    every chunk (then on_chunk must take what it keeps before returning);
+    workspace: an optional buffer of mla_workspace_size(MLA_OP_INDEXER, ...)
+    bytes for the largest chunk; seqs_list: the chunks' Seqs (chunk_seqs),
+    built here if absent. before_chunk(c) / after_indexer(c) are called before
+    chunk c's first call and between its two calls (e.g. to record events)."""
     results = []
+    seqs_list = seqs_list or chunk_seqs(block_table, num_blocks, total, chunk, device=kv.device)
     for c, (s, e) in enumerate(chunk_bounds(total, chunk)):
-        seqs = Seqs([0, e - s], [s], block_table, num_blocks, device=kv.device)
-        idx = mla_indexer_topk(seqs, qi_chunk_fn(s, e), w, w_token_stride, ki, ki_scale, topk, dev_err=dev_err)
-        out, lse = mla_prefill_sparse(seqs, q_chunk_fn(s, e), kv, kv_scale, sm_scale, idx, dev_err=dev_err)
+        n = e - s
+        seqs = seqs_list[c]
+        if before_chunk is not None:
+            before_chunk(c)
+        ix = mla_indexer_topk(seqs, qi_chunk_fn(s, e), w, w_token_stride, ki, ki_scale, topk,
+                              idx_out=None if idx is None else idx[:n], workspace=workspace, dev_err=dev_err)
+        if after_indexer is not None:
+            after_indexer(c)
+        o, l = mla_prefill_sparse(seqs, q_chunk_fn(s, e), kv, kv_scale, sm_scale, ix,
+                                  out=None if out is None else out[:n], lse=None if lse is None else lse[:n],
+                                  dev_err=dev_err)
         if on_chunk is not None:
-            on_chunk(c, s, e, out, lse, idx)
+            on_chunk(c, s, e, o, l, ix)
         else:
-            results.append((out, lse, idx))
+            results.append((o, l, ix))
     return results

@@ -185,6 +185,23 @@ __device__ __forceinline__ RowTile make_tile(const AttnArgs &a, int b, int tile,
     return rt;
 }
 
+// A dense work item is backed when each of its row tiles lies wholly inside both
+// the device's and the host's count of rows. An item that is not (an empty filler
+// item, or a device cu_seqlens that disagrees with its host mirror) is skipped
+// whole, before any barrier or TMEM is set up, so no row at or past the host's
+// count is ever touched. Out of line: the check runs once per CTA and must not
+// share registers with the kernel's loops.
+__device__ __noinline__ bool dense_item_backed(const AttnArgs &a, int b, int tile0, int tile1) {
+    auto ok = [&](int tile) {
+        if (tile < 0) return false;
+        const int64_t q0 = __ldg(a.cu_seqlens + b), qn = __ldg(a.cu_seqlens + b + 1) - q0;
+        const int64_t rows = qn * a.H, r_lo = static_cast<int64_t>(tile) * BM;
+        const int64_t nvalid = min(static_cast<int64_t>(BM), rows - r_lo);
+        return nvalid > 0 && q0 * a.H + r_lo + nvalid <= a.total_q * a.H;
+    };
+    return ok(tile0) && (tile1 < 0 || ok(tile1));
+}
+
 // Last key position row `row` may see (dense), the token's position (sparse); -1: no row.
 template <bool kSparse>
 __device__ __forceinline__ int row_limit(const AttnArgs &a, const RowTile &rt, int row) {
@@ -409,6 +426,11 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
         n_rt = tiles[1] >= 0 ? 2 : 1;
     }
     auto tile_of = [&](int r) { return make_tile<kSparse>(a, b, tiles[r], toks[r], h0); };
+    if (!kSparse && !dense_item_backed(a, b, tiles[0], tiles[1])) {
+        // (filler items are reported by the kernel that wrote them)
+        if (tid == 0 && tiles[0] >= 0) set_dev_err(a.dev_err, MLA_DEVERR_SEQ_MISMATCH);
+        return;
+    }
     Walk walk;
     walk.n0 = tile_of(0).n_ktiles;
     walk.total = walk.n0 + (n_rt > 1 ? tile_of(1).n_ktiles : 0);
@@ -450,6 +472,11 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
         const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.max_blocks;
         uint32_t fix_phase = 0;
         bool ok = true;
+        // parity of the last phase armed on each full barrier (and the fix barrier),
+        // -1 if none: before the CTA exits, each of those phases is waited for, so no
+        // TMA write lands in shared memory after a CTA that gave up has left
+        int armed[3][ST] = {{-1, -1}, {-1, -1}, {-1, -1}};
+        int fix_armed = -1;
         auto wait_empty = [&](int part, int t) -> bool {
             return t < ST || wait(B_EMPTY + part * ST + t % ST, ((t / ST) - 1) & 1);
         };
@@ -487,12 +514,14 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh.bar[B_META + (t & 3)]));
             };
+            const int ph = (t / ST) & 1;
             if (nval == BN) {
                 if (!(ok = wait_empty(0, t))) break;
                 if (lane == 0) {
                     mbar_expect_tx(smem_u32(&sh.bar[B_FULL + 0 * ST + st]), kSliceBytes<false>);
                     load(4, 0);
                 }
+                armed[0][st] = ph;
                 meta();
                 if (!(ok = wait_empty(1, t))) break;
                 if (lane == 0) {
@@ -500,12 +529,14 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                     load(0, 1);
                     load(1, 1);
                 }
+                armed[1][st] = ph;
                 if (!(ok = wait_empty(2, t))) break;
                 if (lane == 0) {
                     mbar_expect_tx(smem_u32(&sh.bar[B_FULL + 2 * ST + st]), 2 * kSliceBytes<false>);
                     load(2, 2);
                     load(3, 2);
                 }
+                armed[2][st] = ph;
             } else {
                 if (!(ok = wait_empty(0, t) && wait_empty(1, t) && wait_empty(2, t))) break;
                 meta();
@@ -516,8 +547,10 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                             tma_load_2d(sdst + s * kSliceBytes<false>, &tmap_kv, 128 * s, static_cast<int>(brow),
                                         smem_u32(&sh.bar[B_FIX]));
                     }
+                    fix_armed = static_cast<int>(fix_phase);
                     if (!(ok = wait(B_FIX, fix_phase))) break;
                     fix_phase ^= 1;
+                    fix_armed = -1;
                 }
                 // rows nval..BN-1 of every slice (a row is 128 contiguous bytes)
                 for (int s = 0; s < kSlices; ++s) {
@@ -529,8 +562,20 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
                 __syncwarp();
                 if (lane == 0)
                     for (int part = 0; part < 3; ++part) mbar_arrive(smem_u32(&sh.bar[B_FULL + part * ST + st]));
+                for (int part = 0; part < 3; ++part) armed[part][st] = ph;
             }
         }
+        // drain: every phase armed above has completed once its copies have landed
+        if (lane == 0) {
+            bool drained = fix_armed < 0 || mbar_wait_cycles(smem_u32(&sh.bar[B_FIX]), fix_armed, kWaitCycles);
+            for (int part = 0; part < 3; ++part)
+                for (int s2 = 0; s2 < ST; ++s2)
+                    if (armed[part][s2] >= 0)
+                        drained = mbar_wait_cycles(smem_u32(&sh.bar[B_FULL + part * ST + s2]), armed[part][s2],
+                                                   kWaitCycles) && drained;
+            if (!drained) set_dev_err(a.dev_err, MLA_DEVERR_TIMEOUT);
+        }
+        __syncwarp();
     } else if (kSparse && warp >= kSmWarps<kSparse> && warp != kIssuerWarp<kSparse>) {
         // =================== row gathers (sparse): pair p takes tiles p, p+2, ... ===================
         // Key k's 576 bytes go by 16-byte cp.async into the swizzled slices, eight
@@ -594,6 +639,8 @@ __global__ void __launch_bounds__(kThreads<kSparse>, 1)
             // have (the issuer fences them into the async proxy before its MMAs)
             cp_async_arrive(smem_u32(&sh.bar[B_FULL + st]));
         }
+        // before the CTA can exit (also after a wait that gave up): this lane's copies have landed
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
     } else if (warp == kIssuerWarp<kSparse>) {
         // =================== MMA issuer (lane 0; the other lanes wait at the end) ===================
         // One thread issues: the same instruction stream issued warp-wide with a

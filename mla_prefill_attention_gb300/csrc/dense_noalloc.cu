@@ -52,10 +52,13 @@ cudaError_t static_work_ptr(int4 **out) {
 // counts gives each sequence its first item, then each thread writes the items
 // of its own sequence: (b, tile i, tile n-1-i or -1). Exactly n_items entries
 // are written (the count the host derived from its mirror of cu_seqlens):
-// items past the device count become empty (-1, -1), so no entry left over
-// from an earlier call is ever read.
+// items past the device count become empty (tile -1, which the attention
+// kernel skips), so no entry left over from an earlier call is ever read. If
+// the device count differs from n_items (the device cu_seqlens disagrees with
+// its host mirror) MLA_DEVERR_SEQ_MISMATCH is set; items past n_items are
+// dropped.
 __global__ void build_pairs_kernel(const int32_t *__restrict__ cu, int32_t batch, int32_t H, int4 *work,
-                                   int32_t n_items) {
+                                   int32_t n_items, int32_t *dev_err) {
     __shared__ int32_t scan[1024];
     __shared__ int32_t base;
     if (threadIdx.x == 0) base = 0;
@@ -86,6 +89,7 @@ __global__ void build_pairs_kernel(const int32_t *__restrict__ cu, int32_t batch
         __syncthreads();
     }
     for (int32_t i = base + threadIdx.x; i < n_items; i += blockDim.x) work[i] = make_int4(0, -1, -1, 0);
+    if (threadIdx.x == 0 && base != n_items && dev_err) atomicOr(dev_err, MLA_DEVERR_SEQ_MISMATCH);
 }
 
 }  // namespace
@@ -120,7 +124,7 @@ extern "C" mla_status_t mla_prefill_dense_static(const mla_seqs_t *seqs, const v
     cudaError_t e = static_work_ptr(&work);
     if (e != cudaSuccess) return mla::report(MLA_ERR_CUDA, cudaGetErrorString(e));
     build_pairs_kernel<<<1, 1024, 0, stream>>>(seqs->cu_seqlens_q, seqs->batch, num_heads, work,
-                                               static_cast<int32_t>(items));
+                                               static_cast<int32_t>(items), dev_err);
     if ((e = cudaGetLastError()) != cudaSuccess) return mla::report(MLA_ERR_CUDA, cudaGetErrorString(e));
     const mla::AttnArgs a =
         mla::make_attn_args(seqs, q_bf16, num_heads, kv_e4m3, kv_scale, sm_scale, out_bf16, lse, dev_err);

@@ -25,7 +25,18 @@ struct AttnArgs {
     int32_t topk;
     int32_t *dev_err;
     int64_t tok_begin, tok_end;  // sparse: the new tokens this launch attends for (global indices)
+    int64_t total_q;             // new tokens by the host mirror of cu_seqlens: no row at or past total_q * H
+                                 // is read or written whatever the device copy says
 };
+
+// Dense attention on e4m3 operands (kind::f8f6f4). Work item: x = sequence,
+// y = 64-row tile, z = paired row tile or -1. tmap_kv: the latent cache as
+// [num_blocks * 256 rows][576 B], 128 x 128 boxes, 128-byte swizzle (encode_kv_tmap).
+cudaError_t launch_dense_f8(const AttnArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_kv, cudaStream_t st);
+bool encode_kv_tmap(CUtensorMap *map, const uint8_t *kv, int32_t num_blocks);
+// Sparse attention on e4m3 operands: rows gathered by index (cp.async), two
+// tokens x 64 heads per CTA, for the tokens [a.tok_begin, a.tok_end).
+cudaError_t launch_sparse_f8(const AttnArgs &a, cudaStream_t st);
 
 struct IndexerArgs {
     const uint8_t *qi;           // [Tq, 64, 128] e4m3
@@ -38,37 +49,26 @@ struct IndexerArgs {
     const int32_t *cu_seqlens;
     const int32_t *prefix_lens;
     int32_t batch;
-    float *scores;               // workspace [Tq, score_stride]
-    int64_t score_stride;
     int32_t topk;
     int32_t *idx_out;            // [Tq, topk]
     int32_t *dev_err;
-    int32_t key_chunk;           // keys per indexer work item (a power of two, 2,048 .. 32,768)
-    int64_t tok0;                // top-k: first token of the launch (CTA i selects for token tok0 + i)
+    int64_t total_q;             // new tokens by the host mirror of cu_seqlens
+    int32_t *fail;               // one flag per work item: the fast path left the group to the exact path
 };
 
-// Dense attention on e4m3 operands (kind::f8f6f4). Work item: x = sequence,
-// y = 64-row tile, z = paired row tile or -1. tmap_kv: the latent cache as
-// [num_blocks * 256 rows][576 B], 128 x 128 boxes, 128-byte swizzle (encode_kv_tmap).
-cudaError_t launch_dense_f8(const AttnArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_kv, cudaStream_t st);
-bool encode_kv_tmap(CUtensorMap *map, const uint8_t *kv, int32_t num_blocks);
-// Sparse attention on e4m3 operands: rows gathered by index (cp.async), two
-// tokens x 64 heads per CTA, for the tokens [a.tok_begin, a.tok_end).
-cudaError_t launch_sparse_f8(const AttnArgs &a, cudaStream_t st);
-
-// Indexer score work item: x = sequence, y = first new token (in-sequence),
-// z = token count (<= kIdxTokensPerCta), w = key chunk (keys w * key_chunk ..
-// +key_chunk; the host takes the longest chunk, from kIdxKeyChunkMax down to
-// kIdxKeyChunkMin, that still gives every SM several items). tmap_k: the key cache as
-// [num_blocks * 256 rows][128 B]; tmap_q: the queries as [Tq * 64 rows][128 B];
-// both with 128-byte-wide boxes and the 128-byte swizzle (boxes of 128 key rows and of
-// kIdxTokensPerCta * 64 query rows).
+// Indexer scores and streaming exact top-k in one kernel. Work item: x =
+// sequence, y = first new token (in-sequence), z = token count (<=
+// kIdxTokensPerCta); the CTA streams every key those tokens see. tmap_k: the
+// key cache as [num_blocks * 256 rows][128 B]; tmap_q: the queries as [Tq * 64
+// rows][128 B]; both with 128-byte-wide boxes and the 128-byte swizzle (boxes of
+// 128 key rows and of kIdxTokensPerCta * 64 query rows). Each token keeps up to
+// kIdxCandidates candidates in shared memory. Two launches: the fast path
+// (sampled threshold) for every item, then the exact streaming path for the
+// items it flagged in a.fail (one int32 per item, written by the first launch).
 constexpr int kIdxTokensPerCta = 3;
-constexpr int kIdxKeyChunkMax = 32768;
-constexpr int kIdxKeyChunkMin = 2048;
-cudaError_t launch_indexer_scores_tc(const IndexerArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_k,
-                                     const CUtensorMap &tmap_q, cudaStream_t st);
-cudaError_t launch_topk(const IndexerArgs &a, int64_t n_tokens, cudaStream_t st);
+constexpr int kIdxCandidates = 5120;
+cudaError_t launch_indexer_topk(const IndexerArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_k,
+                                const CUtensorMap &tmap_q, cudaStream_t st);
 
 struct AppendArgs {
     const __nv_bfloat16 *latent; // [Tq, 576]

@@ -145,12 +145,17 @@ int64_t max_context(const mla_seqs_t *s) {
     return m;
 }
 
-// Work items of the indexer: (sequence, first token, token count, key chunk)
-// for every group of kIdxTokensPerCta tokens whose first token lies in
-// [t0, t1) (global indices; groups start every kIdxTokensPerCta tokens from
-// the start of their sequence) and every chunk of `chunk` keys it can see.
-template <typename F>
-void indexer_groups(const mla_seqs_t *s, int64_t t0, int64_t t1, F &&f) {
+// Work items of the indexer: (sequence, first token, token count, 0) for every
+// group of kIdxTokensPerCta tokens whose first token lies in [t0, t1) (global
+// indices; groups start every kIdxTokensPerCta tokens from the start of their
+// sequence). A CTA streams every key its group can see, so the items are sorted
+// by that count, longest first (LPT), to keep the last wave short.
+std::vector<int4> indexer_schedule(const mla_seqs_t *s, int64_t t0, int64_t t1) {
+    struct Item {
+        int4 v;
+        int64_t keys;
+    };
+    std::vector<Item> items;
     for (int b = 0; b < s->batch; ++b) {
         const int64_t c0 = s->cu_seqlens_q_host[b];
         const int t = s->cu_seqlens_q_host[b + 1] - s->cu_seqlens_q_host[b];
@@ -158,49 +163,28 @@ void indexer_groups(const mla_seqs_t *s, int64_t t0, int64_t t1, F &&f) {
         for (int i0 = 0; i0 < t; i0 += mla::kIdxTokensPerCta) {
             if (c0 + i0 < t0 || c0 + i0 >= t1) continue;
             const int nt = std::min(mla::kIdxTokensPerCta, t - i0);
-            f(b, i0, nt, P + i0 + nt);
+            items.push_back({make_int4(b, i0, nt, 0), static_cast<int64_t>(P) + i0 + nt});
         }
     }
+    std::stable_sort(items.begin(), items.end(), [](const Item &x, const Item &y) { return x.keys > y.keys; });
+    std::vector<int4> out(items.size());
+    for (size_t i = 0; i < items.size(); ++i) out[i] = items[i].v;
+    return out;
 }
 
-int64_t indexer_items(const mla_seqs_t *s, int chunk, int64_t t0, int64_t t1) {
-    int64_t n = 0;
-    indexer_groups(s, t0, t1, [&](int, int, int, int keys) { n += (keys + chunk - 1) / chunk; });
+// Indexer workspace: the work list (16 bytes per item), then one int32 flag per
+// item (the fast path marks the items it leaves to the exact path).
+size_t indexer_ws_bytes(size_t n_items) {
+    return round_up(n_items * sizeof(int4), kWsAlign) + round_up(n_items * sizeof(int32_t), kWsAlign);
+}
+
+size_t indexer_groups(const mla_seqs_t *s) {
+    size_t n = 0;
+    for (int b = 0; b < s->batch; ++b) {
+        const int t = s->cu_seqlens_q_host[b + 1] - s->cu_seqlens_q_host[b];
+        n += static_cast<size_t>((t + mla::kIdxTokensPerCta - 1) / mla::kIdxTokensPerCta);
+    }
     return n;
-}
-
-int64_t indexer_items(const mla_seqs_t *s, int chunk) { return indexer_items(s, chunk, 0, s->cu_seqlens_q_host[s->batch]); }
-
-std::vector<int4> indexer_schedule(const mla_seqs_t *s, int chunk, int64_t t0, int64_t t1) {
-    std::vector<int4> items;
-    items.reserve(static_cast<size_t>(indexer_items(s, chunk, t0, t1)));
-    indexer_groups(s, t0, t1, [&](int b, int i0, int nt, int keys) {
-        for (int c = 0; c * chunk < keys; ++c) items.push_back(make_int4(b, i0, nt, c));
-    });
-    return items;
-}
-
-// Longer key chunks spread each CTA's start (TMEM allocation, barriers, the
-// query load, the first tiles of the pipeline) over more tiles; shorter ones
-// give more CTAs. Take the longest chunk that still gives every SM at least
-// eight items (one CTA per SM), so the last wave stays a small share.
-int indexer_key_chunk(const mla_seqs_t *s, int64_t t0, int64_t t1) {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-        sms = 1;
-    int chunk = mla::kIdxKeyChunkMax;
-    while (chunk > mla::kIdxKeyChunkMin && indexer_items(s, chunk, t0, t1) < 8 * static_cast<int64_t>(sms))
-        chunk /= 2;
-    return chunk;
-}
-
-// fp32 score row per query token; rows start 16-byte aligned (the top-k reads them 4 at a time)
-int64_t score_stride(const mla_seqs_t *s) { return (max_context(s) + 3) / 4 * 4; }
-
-size_t indexer_score_bytes(const mla_seqs_t *s) {
-    const int64_t tq = s->cu_seqlens_q_host[s->batch];
-    return round_up(static_cast<size_t>(tq) * static_cast<size_t>(score_stride(s)) * sizeof(float), kWsAlign);
 }
 
 // 2-D tensor map over a row-major u8 matrix [rows][width] for TMA copies of
@@ -250,6 +234,7 @@ mla::AttnArgs attn_args(const mla_seqs_t *s, const void *q, int32_t H, const uin
     a.H = H;
     a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
     a.dev_err = dev_err;
+    a.total_q = s->cu_seqlens_q_host[s->batch];
     return a;
 }
 
@@ -278,9 +263,8 @@ size_t mla_workspace_size(mla_op_t op, const mla_seqs_t *seqs, int32_t num_heads
             if (!heads_ok(num_heads)) return 0;
             return round_up(dense_schedule(seqs, num_heads).size() * sizeof(int4), kWsAlign);
         case MLA_OP_INDEXER:
-            // room for the work list at the shortest key chunk, whatever chunk the call takes
-            return indexer_score_bytes(seqs) +
-                   round_up(static_cast<size_t>(indexer_items(seqs, mla::kIdxKeyChunkMin)) * sizeof(int4), kWsAlign);
+            // the work list and a flag per item: the scores stay on chip
+            return indexer_ws_bytes(indexer_groups(seqs));
         case MLA_OP_SPARSE:
             return 0;
         case MLA_OP_DENSE_HOST:
@@ -438,9 +422,9 @@ mla_status_t check_indexer_args(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, 
         return fail(MLA_ERR_INVALID_ARG, "qi, w, ki, ki_scale and idx_out must be set");
     if (!aligned(qi_e4m3, 16) || !aligned(ki_e4m3, 16))
         return fail(MLA_ERR_INVALID_ARG, "qi and ki must be 16-byte aligned");
-    if (!aligned(w, 16)) return fail(MLA_ERR_INVALID_ARG, "w must be 16-byte aligned");
-    if (!aligned(ki_scale, 4) || !aligned(idx_out, 4))
-        return fail(MLA_ERR_INVALID_ARG, "ki_scale and idx_out must be 4-byte aligned");
+    if (!aligned(w, 16) || !aligned(ki_scale, 16))
+        return fail(MLA_ERR_INVALID_ARG, "w and ki_scale must be 16-byte aligned");
+    if (!aligned(idx_out, 4)) return fail(MLA_ERR_INVALID_ARG, "idx_out must be 4-byte aligned");
     if (w_token_stride < 0 || w_token_stride % 4 != 0)
         return fail(MLA_ERR_INVALID_ARG, "w_token_stride must be a non-negative multiple of 4");
     if (topk < 1 || topk > 2048) return fail(MLA_ERR_UNSUPPORTED, "topk must be in [1, 2048] (got %d)", topk);
@@ -451,7 +435,7 @@ mla_status_t check_indexer_args(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, 
 
 mla::IndexerArgs indexer_args(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, const float *w, int64_t w_token_stride,
                               const uint8_t *ki_e4m3, const float *ki_scale, int32_t topk, int32_t *idx_out,
-                              void *workspace, int32_t *dev_err) {
+                              int32_t *dev_err) {
     mla::IndexerArgs a{};
     a.qi = qi_e4m3;
     a.w = w;
@@ -464,11 +448,10 @@ mla::IndexerArgs indexer_args(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, co
     a.cu_seqlens = seqs->cu_seqlens_q;
     a.prefix_lens = seqs->prefix_lens;
     a.batch = seqs->batch;
-    a.scores = static_cast<float *>(workspace);
-    a.score_stride = score_stride(seqs);
     a.topk = topk;
     a.idx_out = idx_out;
     a.dev_err = dev_err;
+    a.total_q = seqs->cu_seqlens_q_host[seqs->batch];
     return a;
 }
 }  // namespace
@@ -483,30 +466,23 @@ mla_status_t mla_indexer_topk(const mla_seqs_t *seqs, const uint8_t *qi_e4m3, co
         return st;
     const int64_t tq = seqs->cu_seqlens_q_host[seqs->batch];
     if (tq == 0) return MLA_OK;
-    const int key_chunk = indexer_key_chunk(seqs, 0, tq);
-    const std::vector<int4> work = indexer_schedule(seqs, key_chunk, 0, tq);
-    const size_t sbytes = indexer_score_bytes(seqs);
-    const size_t need = sbytes + round_up(work.size() * sizeof(int4), kWsAlign);
-    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
-        return fail(MLA_ERR_WORKSPACE, "indexer needs %zu workspace bytes (256-byte aligned), got %zu", need,
+    const std::vector<int4> work = indexer_schedule(seqs, 0, tq);
+    const size_t need = indexer_ws_bytes(work.size());
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16))
+        return fail(MLA_ERR_WORKSPACE, "indexer needs %zu workspace bytes (16-byte aligned), got %zu", need,
                     workspace ? workspace_bytes : 0);
-    int4 *dwork = reinterpret_cast<int4 *>(static_cast<char *>(workspace) + sbytes);
-    cudaError_t e = cudaSuccess;
-    if (!work.empty()) {
-        e = cudaMemcpyAsync(dwork, work.data(), work.size() * sizeof(int4), cudaMemcpyHostToDevice, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "schedule upload");
-    }
-    mla::IndexerArgs a = indexer_args(seqs, qi_e4m3, w, w_token_stride, ki_e4m3, ki_scale, topk, idx_out, workspace,
-                                      dev_err);
-    a.key_chunk = key_chunk;
+    if (work.size() > static_cast<size_t>(INT32_MAX)) return fail(MLA_ERR_UNSUPPORTED, "too many query tokens");
+    int4 *dwork = static_cast<int4 *>(workspace);
+    cudaError_t e = cudaMemcpyAsync(dwork, work.data(), work.size() * sizeof(int4), cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "schedule upload");
+    mla::IndexerArgs a = indexer_args(seqs, qi_e4m3, w, w_token_stride, ki_e4m3, ki_scale, topk, idx_out, dev_err);
+    a.fail = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + round_up(work.size() * sizeof(int4), kWsAlign));
     CUtensorMap tmap_k, tmap_q;
     if (!encode_rows128(&tmap_k, ki_e4m3, static_cast<uint64_t>(seqs->num_blocks) * 256, 128) ||
         !encode_rows128(&tmap_q, qi_e4m3, static_cast<uint64_t>(tq) * 64, mla::kIdxTokensPerCta * 64))
         return fail(MLA_ERR_CUDA, "tensor map encoding for the indexer failed");
-    if ((e = mla::launch_indexer_scores_tc(a, dwork, static_cast<int>(work.size()), tmap_k, tmap_q, stream)) !=
-        cudaSuccess)
-        return cuda_fail(e, "indexer score launch");
-    if ((e = mla::launch_topk(a, tq, stream)) != cudaSuccess) return cuda_fail(e, "top-k launch");
+    if ((e = mla::launch_indexer_topk(a, dwork, static_cast<int>(work.size()), tmap_k, tmap_q, stream)) != cudaSuccess)
+        return cuda_fail(e, "indexer launch");
     return MLA_OK;
 }
 
@@ -573,23 +549,22 @@ mla_status_t mla_prefill_sparse_host(const mla_seqs_t *seqs, int32_t num_heads, 
     }
     std::vector<int4> work;
     std::vector<size_t> off(static_cast<size_t>(n_chunks) + 1, 0);
-    std::vector<int> chunk(static_cast<size_t>(n_chunks), mla::kIdxKeyChunkMax);
     for (int c = 0; c < n_chunks; ++c) {
         if (bnd[c + 1] > bnd[c]) {
-            chunk[c] = indexer_key_chunk(seqs, bnd[c], bnd[c + 1]);
-            const std::vector<int4> w = indexer_schedule(seqs, chunk[c], bnd[c], bnd[c + 1]);
+            const std::vector<int4> w = indexer_schedule(seqs, bnd[c], bnd[c + 1]);
             work.insert(work.end(), w.begin(), w.end());
         }
         off[c + 1] = work.size();
     }
-    const size_t sbytes = indexer_score_bytes(seqs);
-    const size_t need = sbytes + round_up(work.size() * sizeof(int4), kWsAlign);
-    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
-        return fail(MLA_ERR_WORKSPACE, "sparse from host needs %zu workspace bytes (256-byte aligned), got %zu", need,
+    const size_t need = indexer_ws_bytes(work.size());
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16))
+        return fail(MLA_ERR_WORKSPACE, "sparse from host needs %zu workspace bytes (16-byte aligned), got %zu", need,
                     workspace ? workspace_bytes : 0);
-    int4 *dwork = reinterpret_cast<int4 *>(static_cast<char *>(workspace) + sbytes);
+    int4 *dwork = static_cast<int4 *>(workspace);
+    int32_t *dfail = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) +
+                                                 round_up(work.size() * sizeof(int4), kWsAlign));
     mla::IndexerArgs ia = indexer_args(seqs, di.qi_e4m3, di.w, w_token_stride, di.ki_e4m3, di.ki_scale, topk, dO.idx,
-                                       workspace, dev_err);
+                                       dev_err);
     mla::AttnArgs aa = attn_args(seqs, di.q_bf16, num_heads, di.kv_e4m3, di.kv_scale, sm_scale, dO.out_bf16, dO.lse,
                                  dev_err);
     aa.idx = dO.idx;
@@ -642,17 +617,15 @@ mla_status_t mla_prefill_sparse_host(const mla_seqs_t *seqs, int32_t num_heads, 
                                 cudaMemcpyHostToDevice, p.s_in),
                 "query copy");
         MLA_TRY(cudaEventRecord(ev_in, p.s_in), "event record");
-        // pieces share no data (each writes its own score, index and output
-        // rows), so consecutive ones go to two streams
+        // pieces share no data (each writes its own index and output rows), so
+        // consecutive ones go to two streams
         cudaStream_t cs = p.s_c[c & 1];
         MLA_TRY(cudaStreamWaitEvent(cs, ev_in, 0), "wait");
-        mla::IndexerArgs a = ia;
-        a.key_chunk = chunk[c];
-        a.tok0 = bnd[c];
         const int n_items = static_cast<int>(off[c + 1] - off[c]);
+        mla::IndexerArgs pa = ia;
+        pa.fail = dfail + off[c];
         if (n_items > 0)
-            MLA_TRY(mla::launch_indexer_scores_tc(a, dwork + off[c], n_items, tmap_k, tmap_q, cs), "indexer score launch");
-        MLA_TRY(mla::launch_topk(a, static_cast<int64_t>(nt), cs), "top-k launch");
+            MLA_TRY(mla::launch_indexer_topk(pa, dwork + off[c], n_items, tmap_k, tmap_q, cs), "indexer launch");
         mla::AttnArgs sa = aa;
         sa.tok_begin = bnd[c];
         sa.tok_end = bnd[c + 1];

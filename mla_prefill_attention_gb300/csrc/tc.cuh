@@ -208,6 +208,15 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// 1-D bulk copy global -> shared through the TMA engine (both addresses 16-byte
+// aligned, bytes a multiple of 16), completing `bytes` of the mbarrier's
+// transaction count.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
+
 // 2-D tiled tensor copy global -> shared through the TMA engine, completing
 // `bytes` of the mbarrier's transaction count. x is the innermost coordinate
 // (its byte offset must be a multiple of 16); the tensor map lives in kernel

@@ -61,3 +61,13 @@ def dense_min_bytes(total_q: int, heads: int, cache_tokens: int) -> int:
     """Compulsory HBM bytes of one dense call: bf16 Q and O, the e4m3 cache
     rows with their fp32 scales, fp32 LSE."""
     return total_q * heads * (2 * D_QK + 2 * D_V + 4) + cache_tokens * (D_QK + 4)
+
+
+def sparse_gathered_bytes(q_lens, prefix_lens, topk: int, heads: int = 64, row_bytes: int = D_QK + 4) -> int:
+    """Bytes sparse MLA moves when every selected row is read from HBM (no
+    reuse across queries): per (query, selected key) pair the 580-byte row and
+    its 4-byte index, and per query its bf16 query and output rows (the
+    arithmetic intensity of "GLM-5.3-Optimierungen, Teil 2", footnote 1, in
+    this library's 580-byte row format: ~214 FLOP/B at 64 heads)."""
+    tq = sum(int(t) for t in q_lens)
+    return sparse_pairs(q_lens, prefix_lens, topk) * (row_bytes + 4) + tq * heads * 2 * (D_QK + D_V)

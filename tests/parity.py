@@ -3,15 +3,24 @@ seeded generators, upload, sampling of rows, and the tolerance check."""
 from __future__ import annotations
 
 import math
+import os
 
 import numpy as np
 
 from mla_prefill_attention_gb300 import inputs as I
 
-# attention tolerance, relative to the rms of the oracle output over the checked rows
+# attention tolerance, relative to the rms of each oracle output row
 TOL_MAX = 2e-2
 TOL_MEAN = 2e-3
 TOL_LSE_ABS = 1e-3
+# How far the raw error may sit above the floor that rounding the exact result
+# to bf16 already gives on the same rows, as a fraction of the bounds above.
+FLOOR_MARGIN = 0.5
+
+# Uniform rows per sequence or chunk in the sampled checks of the large
+# workloads (first and last 64 rows and every chunk boundary +-2 come on top).
+UNIFORM_ROWS = int(os.environ.get("MLA_TEST_UNIFORM_ROWS", "1024"))
+EDGE_ROWS = 64
 
 
 def rel_errors(gpu: np.ndarray, ora: np.ndarray, beyond_rounding: bool = False):
@@ -25,17 +34,17 @@ def rel_errors(gpu: np.ndarray, ora: np.ndarray, beyond_rounding: bool = False):
     moves it by up to 2^-8 of itself); early causal rows, which average only a
     few cache rows, reach 12x on the tiny workload.
 
-    beyond_rounding: the error of each element is first reduced by the most
-    that rounding to bf16 can move it (half the bf16 spacing at the oracle's or
-    the GPU's value, whichever is larger), so an exact result delivered in bf16
-    scores zero and what remains is the computation's own error."""
+    beyond_rounding: the error of each element is first reduced by half the
+    bf16 spacing at the oracle's value, the most that rounding the exact
+    result to bf16 can move it, so an exact result delivered in bf16 scores
+    zero and what remains is the computation's own error."""
     o = ora.astype(np.float64).reshape(-1, ora.shape[-1])
     g = gpu.astype(np.float64).reshape(-1, ora.shape[-1])
     rms_row = np.sqrt(np.mean(o ** 2, axis=1, keepdims=True))
     rms_row[rms_row == 0] = 1.0
     d = np.abs(g - o)
     if beyond_rounding:
-        d = np.maximum(d - np.maximum(bf16_half_spacing(o), bf16_half_spacing(g)), 0.0)
+        d = np.maximum(d - bf16_half_spacing(o), 0.0)
     r = d / rms_row
     return float(r.max()), float(r.mean()), math.sqrt(float(np.mean(o ** 2)))
 
@@ -49,14 +58,38 @@ def bf16_half_spacing(x):
     return np.where(a > 0, np.exp2(e - 8), 0.0)
 
 
-def check_attention(gpu_out, ora_out, gpu_lse=None, ora_lse=None, what=""):
-    """Output within the bounds beyond the bf16 rounding of the output (see
-    rel_errors); the raw errors, rounding included, are in the message."""
+def round_bf16(x):
+    """x rounded to the nearest bf16 value (8 significant bits, ties to even),
+    as float64; the bf16 exponent range is not modelled (attention outputs lie
+    far inside it)."""
+    m, e = np.frexp(np.asarray(x, dtype=np.float64))
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def attention_errors(gpu_out, ora_out):
+    """(own max, own mean, raw max, raw mean, floor max, floor mean, rms): the
+    error beyond the bf16 rounding of the output, the raw error, and the raw
+    error of the oracle's own result rounded to bf16 (the floor no bf16 output
+    can go below), all relative to each row's RMS."""
     mx, mean, rms = rel_errors(gpu_out, ora_out, beyond_rounding=True)
     raw_mx, raw_mean, _ = rel_errors(gpu_out, ora_out)
+    fl_mx, fl_mean, _ = rel_errors(round_bf16(ora_out), ora_out)
+    return mx, mean, raw_mx, raw_mean, fl_mx, fl_mean, rms
+
+
+def check_attention(gpu_out, ora_out, gpu_lse=None, ora_lse=None, what=""):
+    """Two bounds, both relative to each output row's RMS:
+    * the error beyond the bf16 rounding of the exact result (rel_errors with
+      beyond_rounding) is at most TOL_MAX (max) and TOL_MEAN (mean);
+    * the raw error is at most the floor that rounding the oracle's exact
+      result to bf16 gives on the same rows, plus FLOOR_MARGIN of those bounds.
+    LSE within TOL_LSE_ABS absolute."""
     assert np.all(np.isfinite(gpu_out)), f"{what}: non-finite output"
-    assert mx <= TOL_MAX and mean <= TOL_MEAN, (f"{what}: beyond bf16 rounding max {mx:.3e} mean {mean:.3e}; "
-                                                f"raw max {raw_mx:.3e} mean {raw_mean:.3e} (rms {rms:.3e})")
+    mx, mean, raw_mx, raw_mean, fl_mx, fl_mean, rms = attention_errors(gpu_out, ora_out)
+    msg = (f"{what}: beyond bf16 rounding max {mx:.3e} mean {mean:.3e}; raw max {raw_mx:.3e} mean {raw_mean:.3e}; "
+           f"bf16 floor max {fl_mx:.3e} mean {fl_mean:.3e} (rms {rms:.3e})")
+    assert mx <= TOL_MAX and mean <= TOL_MEAN, msg
+    assert raw_mx <= fl_mx + FLOOR_MARGIN * TOL_MAX and raw_mean <= fl_mean + FLOOR_MARGIN * TOL_MEAN, msg
     if gpu_lse is not None:
         dl = float(np.max(np.abs(gpu_lse.astype(np.float64) - ora_lse)))
         assert dl <= TOL_LSE_ABS, f"{what}: lse max abs err {dl:.3e}"
@@ -95,13 +128,172 @@ class Problem:
         return d
 
 
-def sample_tokens(total: int, n_uniform: int, seed: int, edge: int = 8, boundaries=()):
-    """First/last `edge` tokens, tokens at +-1 of each boundary, n_uniform random."""
+def sample_tokens(total: int, n_uniform: int, seed: int, edge: int = 8, boundaries=(), reach: int = 1):
+    """First/last `edge` tokens, tokens within +-reach of each boundary, n_uniform random."""
     rng = np.random.default_rng(seed)
     s = set(range(min(edge, total))) | set(range(max(0, total - edge), total))
     for b in boundaries:
-        for d in (-1, 0, 1):
+        for d in range(-reach, reach + 1):
             if 0 <= b + d < total:
                 s.add(b + d)
     s |= set(rng.integers(0, total, n_uniform).tolist()) if total > 0 else set()
     return np.array(sorted(s), dtype=np.int64)
+
+
+def sample_rows(cu_seqlens, seed: int, n_uniform: int = None, edge: int = EDGE_ROWS, chunks: int = 16,
+                extra_boundaries=()):
+    """The stratified sample of the large workloads' checks, per sequence: its
+    first and last `edge` tokens, the tokens within +-2 of each boundary of its
+    `chunks` equal chunks (and of extra_boundaries, global indices), and
+    n_uniform (UNIFORM_ROWS by default) uniform draws. Returns sorted global
+    token indices."""
+    n_uniform = UNIFORM_ROWS if n_uniform is None else n_uniform
+    cu = [int(x) for x in cu_seqlens]
+    out = set()
+    for b in range(len(cu) - 1):
+        c0, n = cu[b], cu[b + 1] - cu[b]
+        if n == 0:
+            continue
+        bounds = [n * k // chunks for k in range(1, chunks)]
+        bounds += [x - c0 for x in extra_boundaries if c0 <= x < c0 + n]
+        local = sample_tokens(n, n_uniform, seed + 7919 * b, edge=edge, boundaries=bounds, reach=2)
+        out |= set((local + c0).tolist())
+    return np.array(sorted(out), dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
+# full-size checks on the GPU in plain PyTorch (an independent calculation,
+# used where the fp64 oracle cannot cover every row in reasonable time)
+# ---------------------------------------------------------------------------
+def check_attention_torch(gpu_out, ref_out, gpu_lse=None, ref_lse=None, what=""):
+    """check_attention on the GPU against an fp32 reference (torch tensors
+    [..., 512]); the reference's own error (~1e-6 of a row) is far below the
+    bounds. Returns (own max, own mean, raw max, raw mean)."""
+    import torch
+    g, r = gpu_out.float().reshape(-1, gpu_out.shape[-1]), ref_out.float().reshape(-1, ref_out.shape[-1])
+    assert bool(torch.isfinite(g).all()), f"{what}: non-finite output"
+    rms = r.pow(2).mean(dim=1, keepdim=True).sqrt()
+    rms = torch.where(rms > 0, rms, torch.ones_like(rms))
+    _, e = torch.frexp(r)
+    hs = torch.where(r != 0, torch.ldexp(torch.ones_like(r), (e - 9).float()), torch.zeros_like(r))
+    d = (g - r).abs()
+    own = (d - hs).clamp_min(0) / rms
+    raw = d / rms
+    fl = (r.to(torch.bfloat16).float() - r).abs() / rms
+    vals = [float(x) for x in (own.max(), own.mean(), raw.max(), raw.mean(), fl.max(), fl.mean())]
+    msg = (f"{what}: beyond bf16 rounding max {vals[0]:.3e} mean {vals[1]:.3e}; raw max {vals[2]:.3e} "
+           f"mean {vals[3]:.3e}; bf16 floor max {vals[4]:.3e} mean {vals[5]:.3e}")
+    assert vals[0] <= TOL_MAX and vals[1] <= TOL_MEAN, msg
+    assert vals[2] <= vals[4] + FLOOR_MARGIN * TOL_MAX and vals[3] <= vals[5] + FLOOR_MARGIN * TOL_MEAN, msg
+    if gpu_lse is not None:
+        dl = float((gpu_lse.double() - ref_lse.double()).abs().max())
+        assert dl <= TOL_LSE_ABS, f"{what}: lse max abs err {dl:.3e}"
+    return vals[:4]
+
+
+def _cache_rows(ps, b, positions):
+    """Physical cache rows of positions (int64 tensor) of sequence b."""
+    import torch
+    bt = torch.as_tensor(ps.block_table[b], device=positions.device, dtype=torch.int64)
+    return bt[positions // 256] * 256 + positions % 256
+
+
+def sparse_reference_torch(ps, q, kv, ks, sm_scale, idx, block=64):
+    """Sparse MLA in plain PyTorch fp32 (TF32 off) for every new token:
+    gathered rows K_s = ks_s * dec(kv_s), V_s = K_s[:512], softmax over the
+    token's index list (-1 skipped). Returns (out f32 [Tq,H,512], lse [Tq,H])."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        T, H = q.shape[0], q.shape[1]
+        out = torch.empty((T, H, 512), dtype=torch.float32, device=q.device)
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+        kvf = kv.view(-1, 576)
+        ksf = ks.view(-1)
+        cu = [int(x) for x in ps.cu_seqlens_q]
+        for b in range(ps.batch):
+            for t0 in range(cu[b], cu[b + 1], block):
+                t1 = min(t0 + block, cu[b + 1])
+                ix = idx[t0:t1].long()
+                ok = ix >= 0
+                rows = _cache_rows(ps, b, ix.clamp_min(0))
+                K = kvf[rows].view(torch.float8_e4m3fn).float() * ksf[rows][..., None]   # [n, k, 576]
+                lg = torch.einsum("thd,tsd->ths", q[t0:t1].float(), K) * sm_scale
+                lg = lg.masked_fill(~ok[:, None, :], float("-inf"))
+                l = torch.logsumexp(lg, dim=-1)
+                p = torch.exp(lg - torch.where(torch.isfinite(l), l, torch.zeros_like(l))[..., None])
+                out[t0:t1] = torch.einsum("ths,tsd->thd", p, K[..., :512])
+                lse[t0:t1] = l
+        return out, lse
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+def check_topk_torch(ps, qi, w, w_stride, ki, kis, topk, idx, block=16, tokens=None):
+    """Every row of an indexer top-k result against scores computed in plain
+    PyTorch fp32 on the GPU. With integer e4m3 inputs and power-of-two weights
+    and key scales every product and partial sum is an exact fp32 value, so
+    these scores equal the fp64 definition under any summation order. The
+    expected set of a row is every position scoring above the k-th largest
+    score plus the lowest positions scoring equal to it (ties go to the lower
+    position); rows of p+1 <= topk keep 0..p. Also checks the row layout:
+    distinct positions, -1 padding only at the end. tokens: (t0, t1) global range
+    to check (default all)."""
+    import torch
+    f8 = torch.float8_e4m3fn
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        kif, kisf = ki.view(-1, 128), kis.view(-1)
+        cu = [int(x) for x in ps.cu_seqlens_q]
+        lo, hi = tokens if tokens is not None else (0, cu[-1])
+        for b in range(ps.batch):
+            P = int(ps.prefix_lens[b])
+            c0, c1 = max(cu[b], lo), min(cu[b + 1], hi)
+            if c1 <= c0:
+                continue
+            ctx = P + (c1 - cu[b])
+            rows = _cache_rows(ps, b, torch.arange(ctx, device=qi.device))
+            K = kif[rows].view(f8).float()            # [ctx, 128]
+            sig = kisf[rows]
+            for t0 in range(c0, c1, block):
+                t1 = min(t0 + block, c1)
+                n = t1 - t0
+                pos = P + (t0 - cu[b]) + torch.arange(n, device=qi.device)
+                m = int(pos[-1]) + 1
+                Q = qi[t0:t1].view(f8).float()         # [n, 64, 128]
+                if w_stride == 0:
+                    W = w.view(-1)[:64][None, :].expand(n, 64)
+                else:
+                    W = w.view(-1)[(torch.arange(t0, t1, device=qi.device)[:, None] * w_stride +
+                                   torch.arange(64, device=qi.device)[None, :])]
+                D = torch.matmul(Q.reshape(n * 64, 128), K[:m].t()).view(n, 64, m)
+                sc = (D.clamp_min(0) * W[:, :, None]).sum(dim=1) * sig[None, :m]
+                valid = torch.arange(m, device=qi.device)[None, :] <= pos[:, None]
+                exp = torch.zeros((n, m), dtype=torch.bool, device=qi.device)
+                short = pos + 1 <= topk
+                exp[short] = valid[short]
+                long_rows = ~short
+                if bool(long_rows.any()):
+                    s = torch.where(valid, sc, torch.full_like(sc, float("-inf")))[long_rows]
+                    kth = torch.topk(s, topk, dim=1).values[:, -1:]
+                    v = valid[long_rows]
+                    gt, eq = (s > kth) & v, (s == kth) & v
+                    need = topk - gt.sum(dim=1, keepdim=True)
+                    exp[long_rows] = gt | (eq & (eq.cumsum(dim=1) <= need))
+                g = idx[t0:t1].long()
+                okg = g >= 0
+                assert bool((g >= -1).all()), f"tokens {t0}..{t1}: index below -1"
+                cnt = okg.sum(dim=1)
+                assert bool((cnt == torch.clamp(pos + 1, max=topk)).all()), f"tokens {t0}..{t1}: wrong counts"
+                assert bool((okg[:, :-1] | ~okg[:, 1:]).all()), f"tokens {t0}..{t1}: -1 before a position"
+                gs = torch.sort(torch.where(okg, g, torch.full_like(g, 1 << 40)), dim=1).values
+                assert bool((gs[:, 1:] != gs[:, :-1])[okg[:, 1:]].all()), f"tokens {t0}..{t1}: repeated position"
+                # padding and any out-of-range entry land in a spare last column
+                got = torch.zeros((n, m + 1), dtype=torch.bool, device=qi.device)
+                got.scatter_(1, torch.where(okg & (g < m), g, torch.full_like(g, m)), torch.ones_like(okg))
+                bad = (got[:, :m] != exp).any(dim=1) | (got[:, m] & (okg & (g >= m)).any(dim=1))
+                assert not bool(bad.any()), f"token {t0 + int(bad.nonzero()[0])}: selection differs"
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev

@@ -164,8 +164,14 @@ def test_workspace_sizes(lib):
     dense_ws = lib.mla_workspace_size(B.MLA_OP_DENSE, ctypes.byref(s.c), 64, 0)
     tiles = 4096 * 64 // 64
     assert dense_ws == -(-((tiles + 1) // 2 * 16) // 256) * 256
+    # the indexer keeps its scores on chip: only its work list (one 16-byte item
+    # per group of three tokens) and a 4-byte flag per item need device memory,
+    # whatever the context length
     idx_ws = lib.mla_workspace_size(B.MLA_OP_INDEXER, ctypes.byref(s.c), 64, 2048)
-    assert idx_ws >= 4096 * 16384 * 4
+    items = -(-4096 // 3)
+    assert idx_ws == -(-(items * 16) // 256) * 256 + -(-(items * 4) // 256) * 256
+    long_ctx = HostSeqs([4096], [196608])
+    assert lib.mla_workspace_size(B.MLA_OP_INDEXER, ctypes.byref(long_ctx.c), 64, 2048) == idx_ws
     assert lib.mla_workspace_size(B.MLA_OP_SPARSE, ctypes.byref(s.c), 64, 2048) == 0
     assert lib.mla_workspace_size(B.MLA_OP_DENSE, None, 64, 0) == 0
     assert lib.mla_workspace_size(B.MLA_OP_DENSE, ctypes.byref(s.c), 40, 0) == 0

@@ -4,7 +4,7 @@ import pytest
 
 from oracle import oracle as O
 from mla_prefill_attention_gb300 import inputs as I
-from tests.parity import Problem, bf16_to_np, check_attention, sample_tokens
+from tests.parity import UNIFORM_ROWS, Problem, bf16_to_np, check_attention, rel_errors, sample_rows, sample_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -73,23 +73,73 @@ def test_unwritten_cache_slots_are_ignored():
     check_rows(pb, out, lse, np.arange(pb.ps.total_q), "NaN-filled unwritten slots")
 
 
+def dense_via_sparse_slices(pb, d, out_dense, lse_dense, what, block=4096):
+    """Every row of a dense call against an independent path over the same
+    keys: for each token, sparse attention over each 2,048-position slice of
+    its visible keys (positions as index lists), the slices' partial results
+    merged by their log-sum-exp. Runs on the GPU over all rows, so a fault
+    confined to some CTAs of the dense grid (a wrong work item, tile or stage)
+    shows even where the sampled oracle rows miss it. Each side rounds to bf16
+    on its own (the slices, their merge and the dense output), so the bounds
+    are four times the oracle bounds; a wrong tile errs by the whole row."""
+    import torch
+    from mla_prefill_attention_gb300 import Seqs, mla_merge_attn, mla_prefill_sparse
+    ps, K = pb.ps, 2048
+    worst = (0.0, 0.0, 0.0)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for b in range(ps.batch):
+        c0, n, P = int(ps.cu_seqlens_q[b]), ps.seq_len(b) - int(ps.prefix_lens[b]), int(ps.prefix_lens[b])
+        for t0 in range(0, n, block):
+            nb = min(block, n - t0)
+            seqs = Seqs([0, nb], [P + t0], ps.block_table[b:b + 1], ps.num_blocks)
+            q = d["q"][c0 + t0:c0 + t0 + nb]
+            pos = torch.arange(P + t0, P + t0 + nb, device="cuda", dtype=torch.int32)[:, None]
+            outs, lses = [], []
+            for j in range((P + t0 + nb - 1) // K + 1):
+                idx = torch.arange(j * K, (j + 1) * K, device="cuda", dtype=torch.int32)[None, :].expand(nb, K)
+                idx = torch.where(idx <= pos, idx, torch.full_like(idx, -1)).contiguous()
+                o, l = mla_prefill_sparse(seqs, q, d["kv"], d["ks"], pb.sm_scale, idx, dev_err=err)
+                outs.append(o)
+                lses.append(l)
+            while len(outs) > 1:      # groups of up to 8 parts: at most two merge levels here
+                g = [(outs[i:i + 8], lses[i:i + 8]) for i in range(0, len(outs), 8)]
+                outs, lses = map(list, zip(*[mla_merge_attn(o, l) if len(o) > 1 else (o[0], l[0]) for o, l in g]))
+            torch.cuda.synchronize()
+            assert int(err.item()) == 0
+            ref_o = out_dense[c0 + t0:c0 + t0 + nb].float()
+            rms = ref_o.pow(2).mean(dim=-1, keepdim=True).sqrt()
+            rel = (outs[0].float() - ref_o).abs() / torch.where(rms > 0, rms, torch.ones_like(rms))
+            mx, mean = float(rel.max()), float(rel.mean())
+            dl = float((lses[0] - lse_dense[c0 + t0:c0 + t0 + nb]).abs().max())
+            worst = (max(worst[0], mx), max(worst[1], mean), max(worst[2], dl))
+    assert worst[0] <= 4 * 2e-2 and worst[1] <= 4 * 2e-3 and worst[2] <= 4e-3, f"{what}: slices vs dense {worst}"
+    return worst
+
+
 def test_prefix12k_sampled():
     w = I.WORKLOADS["prefix12k"]
     pb = Problem(w.q_lens, w.prefix_lens, w.heads, w.seed, w.shuffle, w.sm_scale)
-    out, lse = run_dense(pb)
-    toks = sample_tokens(pb.ps.total_q, 24, seed=1, boundaries=range(0, 4096, 256))
+    d = pb.device()
+    out, lse = run_dense(pb, d)
+    toks = sample_rows(pb.ps.cu_seqlens_q, seed=1, extra_boundaries=range(0, 4096, 256))
     check_rows(pb, out, lse, toks, "prefix12k")
+    dense_via_sparse_slices(pb, d, out, lse, "prefix12k")
 
 
 @pytest.mark.parametrize("name", ["dense32k", "ragged4"])
 def test_32k_sampled(name):
+    """Sampled rows against the oracle: per sequence the first and last 64, the
+    16 chunk boundaries +-2 and uniform draws (1,024 for the single 32k prompt,
+    256 per prompt of the ragged batch); then every row against the sparse
+    slice path."""
     w = I.WORKLOADS[name]
     pb = Problem(w.q_lens, w.prefix_lens, w.heads, w.seed, w.shuffle, w.sm_scale)
-    out, lse = run_dense(pb)
-    cu = pb.ps.cu_seqlens_q
-    bounds = list(cu) + [int(cu[-1]) * k // 16 for k in range(16)]
-    toks = sample_tokens(pb.ps.total_q, 16, seed=2, edge=4, boundaries=bounds)
+    d = pb.device()
+    out, lse = run_dense(pb, d)
+    n_uni = None if len(w.q_lens) == 1 else max(1, UNIFORM_ROWS // 4)
+    toks = sample_rows(pb.ps.cu_seqlens_q, seed=2, n_uniform=n_uni)
     check_rows(pb, out, lse, toks, name)
+    dense_via_sparse_slices(pb, d, out, lse, name)
 
 
 def test_page_shuffle_is_bit_identical():
@@ -177,3 +227,25 @@ def test_dense_from_host_matches_device_call(q_lens, prefix, H, chunks):
     toks = np.arange(T)
     ora, ora_lse = O.mla_dense(pb.ps, pb.q, toks, pb.kv, pb.ks, pb.sm_scale)
     check_attention(bf16_to_np(oh), ora, lh.numpy(), ora_lse, f"from host {q_lens}/H{H}/{chunks}")
+
+
+def test_device_counts_fewer_tokens_than_host():
+    """The device cu_seqlens counts 50 new tokens, its host mirror 100. The host
+    pairs row tile i with tile 99-i, and every such pair holds a tile the device
+    does not back, so every work item is skipped whole and reported
+    (MLA_DEVERR_SEQ_MISMATCH): nothing in or around the output buffer (guard
+    rows on both sides) is written."""
+    import torch
+    from mla_prefill_attention_gb300 import MLA_DEVERR_SEQ_MISMATCH, mla_prefill_dense
+    pb = Problem([100], [40], 64, seed=78, sm_scale=0.09)
+    d = pb.device()
+    seqs = d["seqs"]
+    seqs.cu = torch.tensor([0, 50], dtype=torch.int32, device="cuda")
+    full = torch.full((102, 64, 512), 12345, dtype=torch.int16, device="cuda")
+    lse_full = torch.full((102, 64), 7.0, dtype=torch.float32, device="cuda")
+    out, lse = full[1:101].view(torch.bfloat16), lse_full[1:101]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla_prefill_dense(seqs, d["q"], d["kv"], d["ks"], pb.sm_scale, out=out, lse=lse, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == MLA_DEVERR_SEQ_MISMATCH
+    assert bool((full == 12345).all()) and bool((lse_full == 7.0).all())

@@ -5,7 +5,8 @@ import pytest
 
 from oracle import oracle as O
 from mla_prefill_attention_gb300 import inputs as I
-from tests.parity import TOL_MAX, TOL_MEAN, Problem, bf16_to_np, check_attention, rel_errors, sample_tokens
+from tests.parity import (TOL_MAX, TOL_MEAN, UNIFORM_ROWS, Problem, bf16_to_np, check_attention, check_attention_torch,
+                          check_topk_torch, rel_errors, sample_rows, sample_tokens, sparse_reference_torch)
 
 pytestmark = pytest.mark.gpu
 
@@ -52,17 +53,20 @@ def check_idx(pb, idx, toks, topk):
     ([300, 7, 129], [0, 2000, 513], 64),   # ragged batch with prefixes
     ([64], [3000], 2048),                  # all rows longer than topk
     ([20], [2030], 2048),                  # rows cross t+1 = topk
+    ([7], [20000], 16),                    # a small k over a long context
+    ([2, 1], [5000, 2047], 2048),          # a group of one token; a sequence with one short row
 ])
 def test_indexer_small_exact(q_lens, prefix, topk):
     pb = Problem(q_lens, prefix, 16, seed=200 + topk, with_indexer=True)
     d = pb.device()
     idx = run_indexer(pb, d, topk)
     check_idx(pb, idx, np.arange(pb.ps.total_q), topk)
-    # positions are ascending, -1 padding only at the end
+    # distinct positions, -1 padding only at the end; a second call gives the same rows
     a = idx.cpu().numpy()
     for r in a:
         v = r[r >= 0]
-        assert np.all(np.diff(v) > 0) and np.all(r[len(v):] == -1)
+        assert len(np.unique(v)) == len(v) and np.all(r[len(v):] == -1)
+    assert np.array_equal(a, run_indexer(pb, d, topk).cpu().numpy())
 
 
 def test_indexer_per_token_weights():
@@ -110,17 +114,15 @@ def test_indexer_signed_scores_and_zero_ties():
     assert np.mean(kth == 0.0) > 0.5 and np.any(sc[~np.isnan(sc)] < 0)
     got = idx.cpu().numpy()
     assert np.array_equal(np.sort(ref, axis=1), np.sort(got, axis=1))
-    assert np.all(np.diff(got, axis=1) > 0)
+    assert all(len(np.unique(r)) == len(r) for r in got)
 
 
 def test_indexer_clustered_winners():
     """The largest scores all sit in the first 1,500 positions (their key scales
-    are 2^10 times the others, exact), so the first warp's stretch of the row
-    holds far more selected positions than an even spread would put there: the
-    sets must still match the oracle. The premise is checked on the oracle's
-    scores with the sampled bracket (1,024 evenly spaced scores, ranks k*1024/n
-    -+ (4 sqrt(.) + 2)): the first sixteenth of the row holds more than 128 of
-    the scores above the bracket."""
+    are 2^10 times the others, exact): after the first compaction the running
+    threshold lies above every later score, so the rest of the stream adds
+    nothing. The premise is checked on the oracle: every selected position is
+    below 1,500."""
     pb = Problem([16], [30000], 16, seed=35, with_indexer=True)
     bt = pb.ps.block_table[0]
     kis = pb.kis.copy()
@@ -131,43 +133,102 @@ def test_indexer_clustered_winners():
     k = 1000
     idx = run_indexer(pb, d, k)
     toks = np.arange(16)
-    ref, sc = O.indexer_topk(pb.ps, pb.qi, pb.w, 0, toks, pb.ki, pb.kis, k, want_scores=True, ctx_cap=30016)
-    n = 30001
-    row = sc[0, :n]
-    samp = np.sort(row[(np.arange(1024) * n) // 1024])[::-1]
-    e = k * 1024 / n
-    t_hi = samp[int(np.floor(e - (4 * np.sqrt(e) + 2)))]
-    assert np.count_nonzero(row[: n // 16] > t_hi) > 128
+    ref = O.indexer_topk(pb.ps, pb.qi, pb.w, 0, toks, pb.ki, pb.kis, k)
+    assert np.all(ref < 1500)
     got = idx.cpu().numpy()
     assert np.array_equal(np.sort(ref, axis=1), np.sort(got, axis=1))
-    assert np.all(np.diff(got, axis=1) > 0)
+    assert all(len(np.unique(r)) == len(r) for r in got)
 
 
-def test_indexer_radix_fallback():
-    """The key scales at the 1,024 evenly spaced sample positions of the row are
-    2^-10 times the others (exact), so the sample sees only tiny scores and the
-    bracket it gives holds far more than k scores above it: the top-k must take
-    its exact radix path and still match the oracle. The premise is checked on
-    the oracle's scores with the sampled bracket's rule."""
-    pb = Problem([1], [30000], 16, seed=36, with_indexer=True)
-    n, k = 30001, 1000
+def test_indexer_rising_scores():
+    """Key scales double every 512 positions (exact powers of two), so nearly
+    every key scores above the running threshold when it arrives: the buffer
+    refills and is compacted every few thousand keys, the worst case for the
+    streaming selection. The premise is checked on the oracle: most selected
+    positions lie in the last 2k."""
+    pb = Problem([4], [30000], 16, seed=36, with_indexer=True)
+    n, k = 30004, 1000
     bt = pb.ps.block_table[0]
     kis = pb.kis.copy()
-    samp_pos = (np.arange(1024) * n) // 1024
-    for s in samp_pos:
-        kis[bt[s // 256], s % 256] *= 2.0 ** -10
+    for s in range(n):
+        kis[bt[s // 256], s % 256] = 2.0 ** (s // 512)
     pb.kis = kis
     d = pb.device()
     idx = run_indexer(pb, d, k)
-    ref, sc = O.indexer_topk(pb.ps, pb.qi, pb.w, 0, np.arange(1), pb.ki, pb.kis, k, want_scores=True, ctx_cap=n)
-    row = sc[0, :n]
-    samp = np.sort(row[samp_pos])[::-1]
-    e = k * 1024 / n
-    t_hi = samp[int(np.floor(e - (4 * np.sqrt(e) + 2)))]
-    assert np.count_nonzero(row > t_hi) > k                  # the bracket misses
+    toks = np.arange(4)
+    ref = O.indexer_topk(pb.ps, pb.qi, pb.w, 0, toks, pb.ki, pb.kis, k)
+    assert np.mean(ref >= 30000 - 2 * k) > 0.9
     got = idx.cpu().numpy()
     assert np.array_equal(np.sort(ref, axis=1), np.sort(got, axis=1))
-    assert np.all(np.diff(got[0]) > 0)
+    assert all(len(np.unique(r)) == len(r) for r in got)
+
+
+def test_indexer_all_scores_equal():
+    """Every key row is the same, so every score of a token is equal: each
+    compaction must fall back to the exact k-th key and keep the lowest
+    positions, and the result is positions 0..k-1."""
+    pb = Problem([6], [20000], 16, seed=37, with_indexer=True)
+    pb.ki[:] = pb.ki.reshape(-1, 128)[0]
+    d = pb.device()
+    k = 2048
+    idx = run_indexer(pb, d, k)
+    got = idx.cpu().numpy()
+    assert np.array_equal(got, np.tile(np.arange(k, dtype=np.int32), (6, 1)))
+    check_idx(pb, idx, np.arange(6), k)
+
+
+def sample_tile_ids(n_keys):
+    """The key tiles (of 128) the indexer's fast path scores first for a group
+    whose keys are 0 .. n_keys-1: one every n_tiles // S tiles, S from 8 to 32
+    (none when every key fits a token's 5,120-entry buffer)."""
+    n_tiles = -(-n_keys // 128)
+    if n_tiles * 128 <= 5120:
+        return []
+    S = min(32, max(8, n_tiles // 32))
+    g = n_tiles // S
+    return [i * g + g // 2 for i in range(S)]
+
+
+def test_indexer_fallback_when_the_sample_misleads():
+    """The keys of the sampled tiles score 2^10 times higher than the rest
+    (their key scales, exact powers of two), so the threshold the sample gives
+    lies above every other key and fewer than k keys reach the buffer: the
+    group must be redone on the exact streaming path and still match the
+    oracle."""
+    pb = Problem([1], [30000], 16, seed=38, with_indexer=True)
+    n, k = 30001, 1000
+    bt = pb.ps.block_table[0]
+    kis = pb.kis.copy()
+    for tile in sample_tile_ids(n):
+        for s in range(tile * 128, min(n, tile * 128 + 128)):
+            kis[bt[s // 256], s % 256] *= 1024.0
+    pb.kis = kis
+    d = pb.device()
+    idx = run_indexer(pb, d, k)
+    check_idx(pb, idx, np.arange(1), k)
+    assert len(np.unique(idx.cpu().numpy()[0])) == k
+
+
+def test_indexer_fallback_when_a_warp_overflows():
+    """The keys in the first 32 slots of every 128-key tile (one TMEM lane
+    quadrant, so one epilogue warp) score 2^10 times higher than the rest, so
+    far more than a warp's quarter of the candidate buffer clears the sampled
+    threshold in that one warp: the group must be redone on the exact path."""
+    pb = Problem([2], [30000], 16, seed=39, with_indexer=True)
+    n, k = 30002, 1500
+    bt = pb.ps.block_table[0]
+    kis = pb.kis.copy()
+    for s in range(n):
+        if s % 128 < 32:
+            kis[bt[s // 256], s % 256] *= 1024.0
+    pb.kis = kis
+    d = pb.device()
+    idx = run_indexer(pb, d, k)
+    ref = O.indexer_topk(pb.ps, pb.qi, pb.w, 0, np.arange(2), pb.ki, pb.kis, k)
+    assert np.all(ref % 128 < 32)
+    got = idx.cpu().numpy()
+    assert np.array_equal(np.sort(ref, axis=1), np.sort(got, axis=1))
+    assert all(len(np.unique(r)) == len(r) for r in got)
 
 
 def test_indexer_ties_go_to_lower_position():
@@ -237,54 +298,93 @@ def test_sparse_padding_and_bad_index():
 
 
 def test_sparse64k_sampled():
+    """8,192 query tokens after 57,344 cached ones. Sampled rows against the
+    fp64 oracle (first and last 64, the 16 chunk boundaries +-2, 1,024 uniform):
+    index sets bit-exact and attention within the bounds. Then every row: the
+    selection against exact fp32 scores and the attention against an fp32
+    reference over the selected rows, both in plain PyTorch on the GPU."""
     w = I.WORKLOADS["sparse64k"]
     pb = Problem(w.q_lens, w.prefix_lens, w.heads, w.seed, w.shuffle, w.sm_scale, with_indexer=True)
     d = pb.device()
     idx = run_indexer(pb, d, w.topk)
-    toks = sample_tokens(pb.ps.total_q, 16, seed=3, edge=4)
+    toks = sample_rows(pb.ps.cu_seqlens_q, seed=3)
     check_idx(pb, idx, toks, w.topk)
     out, lse = run_sparse(pb, d, idx)
     ora, ora_lse = O.mla_sparse(pb.ps, pb.q[toks], toks, pb.kv, pb.ks, pb.sm_scale, idx[toks].cpu().numpy())
     check_attention(bf16_to_np(out[toks]), ora, lse[toks].cpu().numpy(), ora_lse, "sparse64k")
+    check_topk_torch(pb.ps, d["qi"], d["w"], 0, d["ki"], d["kis"], w.topk, idx)
+    ref, ref_lse = sparse_reference_torch(pb.ps, d["q"], d["kv"], d["ks"], pb.sm_scale, idx)
+    check_attention_torch(out, ref, lse, ref_lse, "sparse64k, every row")
 
 
-def test_chunked200k_selected_chunks():
-    """The 200,000-token prompt in 6,144-token chunks: indexer + sparse on
-    chunks 0, 1, 16 and the ragged last one (32), each against the oracle on
-    sampled rows; dense on the last chunk against its own oracle."""
+def test_chunked200k_driver():
+    """The 200,000-token prompt through the library's chunk driver
+    (chunked_prefill_sparse: 33 chunks of 6,144 tokens, each attending to every
+    earlier token through the indexer, top-k and sparse attention). Every
+    chunk: all rows' selections against exact fp32 scores (plain PyTorch on the
+    GPU), and sampled rows (first and last 4, 16 uniform) against the fp64
+    oracle, index sets bit-exact and attention within the bounds. The last
+    chunk also runs the dense path, 64+ rows against its own oracle."""
     import torch
-    from mla_prefill_attention_gb300 import Seqs, chunk_bounds, mla_indexer_topk, mla_prefill_dense, mla_prefill_sparse
+    from mla_prefill_attention_gb300 import Seqs, chunk_bounds, chunked_prefill_sparse, mla_prefill_dense
     w = I.WORKLOADS["chunked200k"]
+    N = w.q_lens[0]
     ps = w.seqs()
     kv, ks = I.gen_latent_cache(w.seed, ps)
     ki, kis = I.gen_indexer_keys(w.seed, ps)
     wh = I.gen_indexer_w(w.seed)
     dkv, dks = torch.from_numpy(kv).cuda(), torch.from_numpy(ks).cuda()
     dki, dkis, dw = torch.from_numpy(ki).cuda(), torch.from_numpy(kis).cuda(), torch.from_numpy(wh).cuda()
-    bounds = chunk_bounds(200000, w.chunk)
+    bounds = chunk_bounds(N, w.chunk)
     assert len(bounds) == 33 and bounds[-1] == (196608, 200000)
-    for c in (0, 1, 16, 32):
-        s, e = bounds[c]
+    n_uni = max(4, UNIFORM_ROWS // 64)
+    picks = [sample_tokens(e - s, n_uni, seed=c, edge=4) for c, (s, e) in enumerate(bounds)]
+    got = {}
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev_q = {}
+
+    def q_fn(s, e):
+        q = torch.from_numpy(I.gen_q_bf16(w.seed, N, w.heads, token_rows=np.arange(s, e)).view(np.int16))
+        dev_q["q"] = q.view(torch.bfloat16).cuda()
+        return dev_q["q"]
+
+    def qi_fn(s, e):
+        dev_q["qi"] = torch.from_numpy(I.gen_indexer_q(w.seed, N, token_rows=np.arange(s, e))).cuda()
+        return dev_q["qi"]
+
+    def on_chunk(c, s, e, out, lse, idx):
         sub = I.PagedSeqs(np.array([0, e - s], np.int32), np.array([s], np.int32), ps.block_table, ps.num_blocks)
-        seqs = Seqs.from_paged(sub)
-        q = I.gen_q_bf16(w.seed, 200000, w.heads, token_rows=np.arange(s, e))
-        qi = I.gen_indexer_q(w.seed, 200000, token_rows=np.arange(s, e))
-        dq = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).cuda()
-        dqi = torch.from_numpy(qi).cuda()
-        idx = mla_indexer_topk(seqs, dqi, dw, 0, dki, dkis, w.topk)
-        out, lse = mla_prefill_sparse(seqs, dq, dkv, dks, w.sm_scale, idx)
-        torch.cuda.synchronize()
-        toks = sample_tokens(e - s, 6, seed=c, edge=2)
-        ref = O.indexer_topk(sub, qi[toks], wh, 0, toks, ki, kis, w.topk)
-        assert np.array_equal(np.sort(idx[toks].cpu().numpy(), 1), np.sort(ref, 1)), f"chunk {c}"
-        ora, ora_lse = O.mla_sparse(sub, q[toks], toks, kv, ks, w.sm_scale, ref)
-        check_attention(bf16_to_np(out[toks]), ora, lse[toks].cpu().numpy(), ora_lse, f"chunk {c}")
-        if c == 32:
-            outd, lsed = mla_prefill_dense(seqs, dq, dkv, dks, w.sm_scale)
-            torch.cuda.synchronize()
-            td = toks[:4]
-            ora_d, ora_dl = O.mla_dense(sub, q[td], td, kv, ks, w.sm_scale)
-            check_attention(bf16_to_np(outd[td]), ora_d, lsed[td].cpu().numpy(), ora_dl, "last chunk dense")
+        check_topk_torch(sub, dev_q["qi"], dw, 0, dki, dkis, w.topk, idx)
+        t = torch.from_numpy(picks[c]).cuda()
+        got[c] = (bf16_to_np(out[t]), lse[t].cpu().numpy(), idx[t].cpu().numpy())
+        if c == len(bounds) - 1:
+            seqs = Seqs.from_paged(sub)
+            outd, lsed = mla_prefill_dense(seqs, dev_q["q"], dkv, dks, w.sm_scale, dev_err=err)
+            td = sample_tokens(e - s, 48, seed=99, edge=8)
+            got["dense"] = (td, bf16_to_np(outd[torch.from_numpy(td).cuda()]),
+                            lsed[torch.from_numpy(td).cuda()].cpu().numpy())
+
+    chunked_prefill_sparse(ps.block_table, ps.num_blocks, N, w.chunk, q_fn, dkv, dks, qi_fn, dw, 0, dki, dkis,
+                           w.sm_scale, topk=w.topk, on_chunk=on_chunk, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for c, (s, e) in enumerate(bounds):
+        toks = picks[c]
+        sub = I.PagedSeqs(np.array([0, e - s], np.int32), np.array([s], np.int32), ps.block_table, ps.num_blocks)
+        qi = I.gen_indexer_q(w.seed, N, token_rows=toks + s)
+        ref = O.indexer_topk(sub, qi, wh, 0, toks, ki, kis, w.topk)
+        out, lse, idx = got[c]
+        assert np.array_equal(np.sort(idx, 1), np.sort(ref, 1)), f"chunk {c}"
+        q = I.gen_q_bf16(w.seed, N, w.heads, token_rows=toks + s)
+        ora, ora_lse = O.mla_sparse(sub, q, toks, kv, ks, w.sm_scale, ref)
+        check_attention(out, ora, lse, ora_lse, f"chunk {c}")
+    s, e = bounds[-1]
+    td, outd, lsed = got["dense"]
+    assert len(td) >= 64
+    sub = I.PagedSeqs(np.array([0, e - s], np.int32), np.array([s], np.int32), ps.block_table, ps.num_blocks)
+    q = I.gen_q_bf16(w.seed, N, w.heads, token_rows=td + s)
+    ora_d, ora_dl = O.mla_dense(sub, q, td, kv, ks, w.sm_scale)
+    check_attention(outd, ora_d, lsed, ora_dl, "last chunk dense")
 
 
 @pytest.mark.parametrize("q_lens,prefix,H,chunks,per_token_w", [
