@@ -225,6 +225,56 @@ def gen_latent_cache(seed: int, seqs: PagedSeqs, tensor: int = T_KV):
     return codes, scales
 
 
+# ----------------------------------------------------------------------------
+# the 656-byte row format
+# ----------------------------------------------------------------------------
+# Reading of "GLM-5.3-Optimierungen, Teil 2", footnote 1 ("656 FP8-KV im
+# fp8_ds_mla-Format"): 656 bytes per token hold the 512 latent dims as e4m3 codes
+# with one fp32 scale per 128 dims (absmax/448, 1 for an all-zero group) and the
+# 64 RoPE dims as bf16: bytes 0..511 codes, 512..527 the four scales
+# (little-endian), 528..655 the RoPE values (little-endian).
+DS_ROW = 656
+DS_GROUPS = 4
+
+
+def pack_ds_rows(x: np.ndarray) -> np.ndarray:
+    """Latent rows [n, 576] (float64) -> 656-byte rows [n, 656] (uint8)."""
+    x = np.asarray(x, dtype=np.float64)
+    n = x.shape[0]
+    lat = x[:, :D_V].reshape(n, DS_GROUPS, D_V // DS_GROUPS)
+    amax = np.max(np.abs(lat), axis=2)
+    scale = np.where(amax > 0, amax / 448.0, 1.0).astype(np.float32)
+    codes = e4m3_bits(lat / scale.astype(np.float64)[:, :, None]).reshape(n, D_V)
+    rope = bf16_bits(x[:, D_V:])
+    out = np.empty((n, DS_ROW), dtype=np.uint8)
+    out[:, :D_V] = codes
+    out[:, D_V:D_V + 16] = np.ascontiguousarray(scale.astype("<f4")).view(np.uint8).reshape(n, 16)
+    out[:, D_V + 16:] = np.ascontiguousarray(rope.astype("<u2")).view(np.uint8).reshape(n, 128)
+    return out
+
+
+def ds_rows(seed: int, b: int, positions, tensor: int = T_KV) -> np.ndarray:
+    """656-byte rows of tokens at `positions` of sequence b (the same N(0,1) draws
+    as latent_rows)."""
+    s = np.asarray(positions, dtype=np.int64)
+    return pack_ds_rows(normal_rows(seed, tensor, (np.int64(b) << 32) | s, D_QK))
+
+
+def gen_latent_cache_ds(seed: int, seqs: PagedSeqs, tensor: int = T_KV) -> np.ndarray:
+    """Paged cache of 656-byte rows [num_blocks, 256, 656]; unused slots hold zero
+    codes, scales 1 and zero RoPE values."""
+    nb = seqs.num_blocks
+    empty = pack_ds_rows(np.zeros((1, D_QK)))[0]
+    cache = np.tile(empty, (nb, PAGE, 1))
+    for b in range(seqs.batch):
+        s = np.arange(seqs.seq_len(b), dtype=np.int64)
+        pg = seqs.block_table[b, s // PAGE]
+        for c0 in range(0, s.shape[0], 65536):
+            sl = s[c0:c0 + 65536]
+            cache[pg[c0:c0 + 65536], sl % PAGE] = ds_rows(seed, b, sl, tensor)
+    return cache
+
+
 def _int_e4m3(seed, tensor, rows, n, lo, hi):
     r = _rows(rows)
     out = np.empty((r.shape[0], n), dtype=np.uint8)

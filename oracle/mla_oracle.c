@@ -24,7 +24,9 @@
  *    V_s = first 512 dims of K_s. The head's W_UV is applied outside.
  *  - Causal with a cached prefix: new token i of a sequence with prefix P sits
  *    at position p = P + i and attends to positions 0..p (itself included).
- *  - FP8 is OCP e4m3fn; one fp32 scale per cached token.
+ *  - FP8 is OCP e4m3fn; one fp32 scale per cached token. The 656-byte row of
+ *    GLM-5.3 Teil 2, footnote 1, is read as 512 e4m3 latent codes, one fp32
+ *    scale per 128 latent dims and 64 bf16 RoPE values.
  *  - Indexer: score(t,s) = sigmaI_s * sum_h w_{t,h} * max(0, q_{t,h} . k_s),
  *    s <= p; the selected set is the first min(topk, p+1) positions in the
  *    order (score descending, position ascending).
@@ -105,25 +107,55 @@ static int64_t cache_row(const int32_t *bt, int32_t max_blocks, int32_t num_bloc
     return (int64_t)page * ORA_PAGE + s % ORA_PAGE;
 }
 
+/* Cache row formats. ORA_FMT_580: 576 e4m3 codes in kv (row r at r*576) and one
+ * fp32 scale per row in kv_scale: K[d] = sigma_r * dec(c[d]). ORA_FMT_656 (the
+ * 656-byte row of GLM-5.3 Teil 2, footnote 1, read as 512 e4m3 latent codes,
+ * four fp32 scales, one per 128 dims, then 64 bf16 RoPE values, little-endian):
+ * K[d] = sigma_{r,d/128} * dec(c[d]) for d < 512, K[512+i] = bf16 value i. */
+#define ORA_FMT_580 0
+#define ORA_FMT_656 1
+#define ORA_ROW656 656
+
+static float f32_le(const uint8_t *p) {
+    uint32_t u = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* The 576 key values of cache row r. */
+static void decode_row(int fmt, const uint8_t *kv, const float *kv_scale, int64_t r, double *k) {
+    if (fmt == ORA_FMT_580) {
+        const uint8_t *c = kv + r * ORA_DQK;
+        double sigma = (double)kv_scale[r];
+        for (int d = 0; d < ORA_DQK; ++d) k[d] = sigma * e4m3_table[c[d]];
+    } else {
+        const uint8_t *row = kv + r * ORA_ROW656;
+        for (int d = 0; d < ORA_DV; ++d) k[d] = (double)f32_le(row + ORA_DV + 4 * (d / 128)) * e4m3_table[row[d]];
+        for (int i = 0; i < ORA_DQK - ORA_DV; ++i)
+            k[ORA_DV + i] = ora_bf16((uint16_t)(row[ORA_DV + 16 + 2 * i] | (row[ORA_DV + 17 + 2 * i] << 8)));
+    }
+}
+
 /* Softmax attention of one query row over a list of key positions.
- * logit_s = sm_scale * sum_d q[d] * K_s[d],   K_s[d] = sigma_s * dec(c_s[d]);
+ * logit_s = sm_scale * sum_d q[d] * K_s[d] (K_s from the row's format);
  * m = max logit; w_s = exp(logit_s - m); out = sum w_s V_s / sum w_s with
  * V_s = K_s[0..511]; lse = m + ln(sum w_s). Keys with pos < 0 are skipped.
  * Returns 0, or -1 if a position is unmapped. With no keys: out = 0, lse = -inf. */
-static int attend_row(const double *q, const int64_t *pos, int64_t n, int b,
+static int attend_row(int fmt, const double *q, const int64_t *pos, int64_t n, int b,
                       const int32_t *bt, int32_t max_blocks, int32_t num_blocks,
                       const uint8_t *kv, const float *kv_scale, double sm_scale,
                       double *out, double *lse, double *logit) {
     int64_t valid = 0;
     double m = -INFINITY;
+    double k[ORA_DQK];
     for (int64_t j = 0; j < n; ++j) {
         if (pos[j] < 0) continue;
         int64_t r = cache_row(bt, max_blocks, num_blocks, b, pos[j]);
         if (r < 0) return -1;
-        const uint8_t *c = kv + r * ORA_DQK;
-        double sigma = (double)kv_scale[r];
+        decode_row(fmt, kv, kv_scale, r, k);
         double dot = 0.0;
-        for (int d = 0; d < ORA_DQK; ++d) dot += q[d] * (sigma * e4m3_table[c[d]]);
+        for (int d = 0; d < ORA_DQK; ++d) dot += q[d] * k[d];
         logit[j] = sm_scale * dot;
         if (logit[j] > m) m = logit[j];
         ++valid;
@@ -137,11 +169,10 @@ static int attend_row(const double *q, const int64_t *pos, int64_t n, int b,
     for (int64_t j = 0; j < n; ++j) {
         if (pos[j] < 0) continue;
         int64_t r = cache_row(bt, max_blocks, num_blocks, b, pos[j]);
-        const uint8_t *c = kv + r * ORA_DQK;
-        double sigma = (double)kv_scale[r];
+        decode_row(fmt, kv, kv_scale, r, k);
         double w = exp(logit[j] - m);
         l += w;
-        for (int d = 0; d < ORA_DV; ++d) out[d] += w * (sigma * e4m3_table[c[d]]);
+        for (int d = 0; d < ORA_DV; ++d) out[d] += w * k[d];
     }
     for (int d = 0; d < ORA_DV; ++d) out[d] /= l;
     *lse = m + log(l);
@@ -152,11 +183,11 @@ static int attend_row(const double *q, const int64_t *pos, int64_t n, int b,
  * q: fp64 [n_sel, H, 576] (the selected tokens' query rows); tokens: global
  * new-token indices into cu_seqlens_q. out: [n_sel, H, 512]; lse: [n_sel, H].
  * Returns 0, or a negative count of failed rows. */
-int ora_mla_dense(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *prefix_lens,
-                  const int32_t *block_table, int32_t max_blocks, int32_t num_blocks,
-                  const double *q, const int64_t *tokens, int64_t n_sel, int32_t H,
-                  const uint8_t *kv, const float *kv_scale, double sm_scale,
-                  double *out, double *lse) {
+int ora_mla_dense_fmt(int fmt, int32_t batch, const int32_t *cu_seqlens_q, const int32_t *prefix_lens,
+                      const int32_t *block_table, int32_t max_blocks, int32_t num_blocks,
+                      const double *q, const int64_t *tokens, int64_t n_sel, int32_t H,
+                      const uint8_t *kv, const float *kv_scale, double sm_scale,
+                      double *out, double *lse) {
     ora_init();
     int64_t fails = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(+ : fails)
@@ -172,7 +203,7 @@ int ora_mla_dense(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *pre
         int64_t *pos = (int64_t *)malloc((size_t)n * sizeof(int64_t));
         double *logit = (double *)malloc((size_t)n * sizeof(double));
         for (int64_t s = 0; s < n; ++s) pos[s] = s;
-        if (attend_row(q + rh * ORA_DQK, pos, n, b, block_table, max_blocks, num_blocks, kv, kv_scale,
+        if (attend_row(fmt, q + rh * ORA_DQK, pos, n, b, block_table, max_blocks, num_blocks, kv, kv_scale,
                        sm_scale, out + rh * ORA_DV, lse + rh, logit) != 0)
             ++fails;
         free(pos);
@@ -184,11 +215,11 @@ int ora_mla_dense(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *pre
 /* Sparse MLA: as dense, but query token sel attends only to the positions
  * idx[sel*topk .. +topk] (entries < 0 are padding). The causal limit is not
  * re-applied: the index list is the whole key set. */
-int ora_mla_sparse(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *prefix_lens,
-                   const int32_t *block_table, int32_t max_blocks, int32_t num_blocks,
-                   const double *q, const int64_t *tokens, int64_t n_sel, int32_t H,
-                   const uint8_t *kv, const float *kv_scale, double sm_scale,
-                   const int32_t *idx, int32_t topk, double *out, double *lse) {
+int ora_mla_sparse_fmt(int fmt, int32_t batch, const int32_t *cu_seqlens_q, const int32_t *prefix_lens,
+                       const int32_t *block_table, int32_t max_blocks, int32_t num_blocks,
+                       const double *q, const int64_t *tokens, int64_t n_sel, int32_t H,
+                       const uint8_t *kv, const float *kv_scale, double sm_scale,
+                       const int32_t *idx, int32_t topk, double *out, double *lse) {
     ora_init();
     (void)prefix_lens;
     int64_t fails = 0;
@@ -203,13 +234,31 @@ int ora_mla_sparse(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *pr
         int64_t *pos = (int64_t *)malloc((size_t)topk * sizeof(int64_t));
         double *logit = (double *)malloc((size_t)topk * sizeof(double));
         for (int64_t j = 0; j < topk; ++j) pos[j] = idx[sel * topk + j];
-        if (attend_row(q + rh * ORA_DQK, pos, topk, b, block_table, max_blocks, num_blocks, kv, kv_scale,
+        if (attend_row(fmt, q + rh * ORA_DQK, pos, topk, b, block_table, max_blocks, num_blocks, kv, kv_scale,
                        sm_scale, out + rh * ORA_DV, lse + rh, logit) != 0)
             ++fails;
         free(pos);
         free(logit);
     }
     return fails ? (int)-fails : 0;
+}
+
+/* The 580-byte-row entry points (codes + per-token scale). */
+int ora_mla_dense(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *prefix_lens,
+                  const int32_t *block_table, int32_t max_blocks, int32_t num_blocks,
+                  const double *q, const int64_t *tokens, int64_t n_sel, int32_t H,
+                  const uint8_t *kv, const float *kv_scale, double sm_scale,
+                  double *out, double *lse) {
+    return ora_mla_dense_fmt(ORA_FMT_580, batch, cu_seqlens_q, prefix_lens, block_table, max_blocks, num_blocks, q,
+                             tokens, n_sel, H, kv, kv_scale, sm_scale, out, lse);
+}
+int ora_mla_sparse(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *prefix_lens,
+                   const int32_t *block_table, int32_t max_blocks, int32_t num_blocks,
+                   const double *q, const int64_t *tokens, int64_t n_sel, int32_t H,
+                   const uint8_t *kv, const float *kv_scale, double sm_scale,
+                   const int32_t *idx, int32_t topk, double *out, double *lse) {
+    return ora_mla_sparse_fmt(ORA_FMT_580, batch, cu_seqlens_q, prefix_lens, block_table, max_blocks, num_blocks, q,
+                              tokens, n_sel, H, kv, kv_scale, sm_scale, idx, topk, out, lse);
 }
 
 typedef struct {

@@ -43,6 +43,10 @@ def lib():
         L.ora_mla_dense.argtypes = seq + [vp, vp, i64, i32, vp, vp, dbl, vp, vp]
         L.ora_mla_sparse.restype = ctypes.c_int
         L.ora_mla_sparse.argtypes = seq + [vp, vp, i64, i32, vp, vp, dbl, vp, i32, vp, vp]
+        L.ora_mla_dense_fmt.restype = ctypes.c_int
+        L.ora_mla_dense_fmt.argtypes = [ctypes.c_int] + seq + [vp, vp, i64, i32, vp, vp, dbl, vp, vp]
+        L.ora_mla_sparse_fmt.restype = ctypes.c_int
+        L.ora_mla_sparse_fmt.argtypes = [ctypes.c_int] + seq + [vp, vp, i64, i32, vp, vp, dbl, vp, i32, vp, vp]
         L.ora_indexer_topk.restype = ctypes.c_int
         L.ora_indexer_topk.argtypes = seq + [vp, vp, i64, vp, i64, vp, vp, i32, vp, vp, i64]
         L.ora_e4m3_nearest.restype = ctypes.c_uint8
@@ -125,6 +129,56 @@ def mla_sparse(seqs, q, tokens, kv, kv_scale, sm_scale, idx):
         raise ValueError(f"oracle sparse: {-rc} rows failed")
     return out, lse
 
+
+
+FMT_656 = 1
+
+
+def mla_dense_ds(seqs, q, tokens, kv_ds, sm_scale):
+    """fp64 dense causal MLA over a cache of 656-byte rows [num_blocks, 256, 656]
+    (512 e4m3 latent codes, four fp32 scales, 64 bf16 RoPE values per token).
+    q: bf16 bits [n, H, 576] (uint16) or fp64; returns (out [n,H,512], lse [n,H])."""
+    q = np.asarray(q)
+    qd = bf16_to_f64(q) if q.dtype == np.uint16 else _c(q, np.float64)
+    n, H = qd.shape[0], qd.shape[1]
+    tok = _c(tokens, np.int64)
+    if tok.shape != (n,) or qd.shape[2] != 576:
+        raise ValueError("q must be [len(tokens), H, 576]")
+    kvc = _c(kv_ds, np.uint8)
+    if kvc.shape[-1] != 656:
+        raise ValueError("kv_ds must hold 656-byte rows")
+    keep, sa = _seq_args(seqs)
+    out = np.zeros((n, H, 512), dtype=np.float64)
+    lse = np.zeros((n, H), dtype=np.float64)
+    dummy = np.ones(1, dtype=np.float32)
+    rc = lib().ora_mla_dense_fmt(FMT_656, *sa, _p(qd), _p(tok), n, H, _p(kvc), _p(dummy), float(sm_scale), _p(out),
+                                 _p(lse))
+    if rc != 0:
+        raise ValueError(f"oracle dense: {-rc} rows failed (token out of range or unmapped page)")
+    return out, lse
+
+
+def mla_sparse_ds(seqs, q, tokens, kv_ds, sm_scale, idx):
+    """fp64 sparse MLA over idx [n, topk] (-1 = padding) on 656-byte rows."""
+    q = np.asarray(q)
+    qd = bf16_to_f64(q) if q.dtype == np.uint16 else _c(q, np.float64)
+    n, H = qd.shape[0], qd.shape[1]
+    ix = _c(idx, np.int32)
+    tok = _c(tokens, np.int64)
+    if tok.shape != (n,) or ix.shape[0] != n or qd.shape[2] != 576:
+        raise ValueError("q must be [len(tokens), H, 576] and idx [len(tokens), topk]")
+    kvc = _c(kv_ds, np.uint8)
+    if kvc.shape[-1] != 656:
+        raise ValueError("kv_ds must hold 656-byte rows")
+    keep, sa = _seq_args(seqs)
+    out = np.zeros((n, H, 512), dtype=np.float64)
+    lse = np.zeros((n, H), dtype=np.float64)
+    dummy = np.ones(1, dtype=np.float32)
+    rc = lib().ora_mla_sparse_fmt(FMT_656, *sa, _p(qd), _p(tok), n, H, _p(kvc), _p(dummy), float(sm_scale), _p(ix),
+                                  ix.shape[1], _p(out), _p(lse))
+    if rc != 0:
+        raise ValueError(f"oracle sparse: {-rc} rows failed")
+    return out, lse
 
 def indexer_topk(seqs, qi, w, w_stride, tokens, ki, ki_scale, topk, want_scores=False, ctx_cap=0):
     """Exact top-k selection per selected token; returns idx [n, topk] ascending,
