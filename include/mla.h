@@ -148,6 +148,33 @@ mla_status_t mla_prefill_sparse(const mla_seqs_t *seqs, const void *q_bf16, int3
                                 void *workspace, size_t workspace_bytes, int32_t *dev_err,
                                 cudaStream_t stream);
 
+/* Bytes of one row of the alternative cache layout: the 656-byte row of
+ * GLM-5.3 Teil 2, footnote 1 (656 FP8 KV bytes per token, FlashMLA's
+ * fp8_ds_mla format), read as 512 e4m3 latent codes (bytes 0..511), one fp32
+ * scale per 128 latent dims (bytes 512..527, little-endian; dim d of the latent
+ * is scales[d/128] * dec(code[d])) and the 64 RoPE dims as bf16 (bytes
+ * 528..655). Pages hold 256 rows, as for the 580-byte layout. */
+#define MLA_DS_ROW_BYTES 656
+
+/* Dense causal MLA prefill on a cache of 656-byte rows kv_ds [num_blocks, 256,
+ * 656]: what mla_prefill_dense computes, with K_s[d] = scales_s[d/128] *
+ * dec(code_s[d]) for d < 512 and K_s[512+i] = the bf16 RoPE value i, V_s =
+ * K_s[0:512]. The rows are dequantised to f16 in shared memory (relative to a
+ * row's largest group scale, so the scale ratios and the RoPE values are
+ * rounded once to 11 significant bits) and multiplied on the tensor cores in
+ * f16 with fp32 accumulation. Arguments, workspace (mla_workspace_size(
+ * MLA_OP_DENSE, ...)) and errors as mla_prefill_dense; kv_ds 16-byte aligned. */
+mla_status_t mla_prefill_dense_ds(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads,
+                                  const uint8_t *kv_ds, float sm_scale, void *out_bf16, float *lse,
+                                  void *workspace, size_t workspace_bytes, int32_t *dev_err, cudaStream_t stream);
+
+/* Sparse MLA over selected rows of a cache of 656-byte rows: what
+ * mla_prefill_sparse computes, with the rows read as in mla_prefill_dense_ds.
+ * No workspace. */
+mla_status_t mla_prefill_sparse_ds(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads,
+                                   const uint8_t *kv_ds, float sm_scale, const int32_t *idx, int32_t topk,
+                                   void *out_bf16, float *lse, int32_t *dev_err, cudaStream_t stream);
+
 /* Largest work list mla_prefill_dense_static can hold: 65,536 items of 16
  * bytes (1 MiB of device memory, reserved on every GPU that loads the library
  * for the life of the process). One item covers two 64-row query tiles, so

@@ -22,9 +22,11 @@ from .binding import (  # noqa: F401
     mla_kv_append,
     mla_merge_attn,
     mla_prefill_dense,
+    mla_prefill_dense_ds,
     mla_prefill_dense_host,
     mla_prefill_dense_static,
     mla_prefill_sparse,
+    mla_prefill_sparse_ds,
     mla_prefill_sparse_host,
     mla_workspace_size,
 )

@@ -22,7 +22,7 @@ MLA_OP_DENSE, MLA_OP_INDEXER, MLA_OP_SPARSE, MLA_OP_DENSE_HOST = 0, 1, 2, 3
 
 EXPORTS = ("mla_workspace_size", "mla_prefill_dense", "mla_indexer_topk", "mla_prefill_sparse", "mla_last_error",
            "mla_prefill_dense_static", "mla_kv_append", "mla_merge_attn", "mla_prefill_dense_host",
-           "mla_prefill_sparse_host")
+           "mla_prefill_sparse_host", "mla_prefill_dense_ds", "mla_prefill_sparse_ds")
 DENSE_STATIC_MAX_WORK_ITEMS = 65536
 DENSE_HOST_MAX_CHUNKS = 64
 
@@ -87,6 +87,10 @@ def load(path: str = LIB_PATH):
                                           ctypes.POINTER(mla_sparse_inputs_t), ctypes.POINTER(mla_sparse_inputs_t),
                                           ctypes.POINTER(mla_sparse_outputs_t), ctypes.POINTER(mla_sparse_outputs_t),
                                           i32, vp, sz, vp, vp]
+    L.mla_prefill_dense_ds.restype = ctypes.c_int
+    L.mla_prefill_dense_ds.argtypes = [ctypes.POINTER(mla_seqs_t), vp, i32, vp, f32, vp, vp, vp, sz, vp, vp]
+    L.mla_prefill_sparse_ds.restype = ctypes.c_int
+    L.mla_prefill_sparse_ds.argtypes = [ctypes.POINTER(mla_seqs_t), vp, i32, vp, f32, vp, i32, vp, vp, vp, vp]
     L.mla_kv_append.restype = ctypes.c_int
     L.mla_kv_append.argtypes = [ctypes.POINTER(mla_seqs_t), vp, vp, vp, vp, vp, vp, vp, vp]
     L.mla_merge_attn.restype = ctypes.c_int
@@ -256,6 +260,36 @@ def mla_prefill_sparse(seqs: Seqs, q: torch.Tensor, kv: torch.Tensor, kv_scale: 
     _check(load().mla_prefill_sparse(ctypes.byref(c), _ptr(q), H, _ptr(kv), _ptr(kv_scale), float(sm_scale),
                                      _ptr(idx), int(idx.shape[1]), _ptr(out), _ptr(lse), _ptr(ws), wsb,
                                      _ptr(dev_err), _stream()))
+    return out, lse
+
+
+def mla_prefill_dense_ds(seqs: Seqs, q: torch.Tensor, kv_ds: torch.Tensor, sm_scale: float, out=None, lse=None,
+                         want_lse: bool = True, workspace=None, dev_err=None):
+    """Dense causal MLA prefill on a cache of 656-byte rows kv_ds uint8 [nb,256,656]
+    (512 e4m3 codes, four fp32 group scales, 64 bf16 RoPE values). Returns (out, lse)."""
+    H = q.shape[1]
+    if out is None:
+        out = torch.empty((q.shape[0], H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((q.shape[0], H), dtype=torch.float32, device=q.device)
+    ws, wsb = _workspace(MLA_OP_DENSE, seqs, H, 0, workspace)
+    c = seqs.c()
+    _check(load().mla_prefill_dense_ds(ctypes.byref(c), _ptr(q), H, _ptr(kv_ds), float(sm_scale), _ptr(out),
+                                       _ptr(lse), _ptr(ws), wsb, _ptr(dev_err), _stream()))
+    return out, lse
+
+
+def mla_prefill_sparse_ds(seqs: Seqs, q: torch.Tensor, kv_ds: torch.Tensor, sm_scale: float, idx: torch.Tensor,
+                          out=None, lse=None, want_lse: bool = True, dev_err=None):
+    """Sparse MLA over idx [Tq, topk] (-1 skipped) on a cache of 656-byte rows. Returns (out, lse)."""
+    H = q.shape[1]
+    if out is None:
+        out = torch.empty((q.shape[0], H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((q.shape[0], H), dtype=torch.float32, device=q.device)
+    c = seqs.c()
+    _check(load().mla_prefill_sparse_ds(ctypes.byref(c), _ptr(q), H, _ptr(kv_ds), float(sm_scale), _ptr(idx),
+                                        int(idx.shape[1]), _ptr(out), _ptr(lse), _ptr(dev_err), _stream()))
     return out, lse
 
 

@@ -38,6 +38,12 @@ bool encode_kv_tmap(CUtensorMap *map, const uint8_t *kv, int32_t num_blocks);
 // tokens x 64 heads per CTA, for the tokens [a.tok_begin, a.tok_end).
 cudaError_t launch_sparse_f8(const AttnArgs &a, cudaStream_t st);
 
+// The same two on a cache of 656-byte rows (512 e4m3 latent codes, four fp32
+// group scales, 64 bf16 RoPE values; a.kv_scale unused): rows dequantised to f16
+// in shared memory, tcgen05 kind::f16, 64 query rows x 80 keys per tile.
+cudaError_t launch_dense_ds(const AttnArgs &a, const int4 *work, int n_work, cudaStream_t st);
+cudaError_t launch_sparse_ds(const AttnArgs &a, cudaStream_t st);
+
 struct IndexerArgs {
     const uint8_t *qi;           // [Tq, 64, 128] e4m3
     const float *w;              // row t at w + t * w_stride

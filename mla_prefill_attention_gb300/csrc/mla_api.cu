@@ -649,6 +649,55 @@ mla_status_t mla_prefill_sparse_host(const mla_seqs_t *seqs, int32_t num_heads, 
     return MLA_OK;
 }
 
+mla_status_t mla_prefill_dense_ds(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads, const uint8_t *kv_ds,
+                                  float sm_scale, void *out_bf16, float *lse, void *workspace, size_t workspace_bytes,
+                                  int32_t *dev_err, cudaStream_t stream) {
+    g_err.clear();
+    mla_status_t st = check_seqs(seqs);
+    if (st != MLA_OK) return st;
+    if (!heads_ok(num_heads)) return fail(MLA_ERR_UNSUPPORTED, "num_heads must be 16, 32, 64 or 128 (got %d)", num_heads);
+    // the row format carries its own scales: any 4-byte-aligned stand-in passes the scale check
+    if ((st = check_attn_ptrs(q_bf16, kv_ds, reinterpret_cast<const float *>(kv_ds), out_bf16, lse, sm_scale)) != MLA_OK)
+        return st;
+    const std::vector<int4> work = dense_schedule(seqs, num_heads);
+    const size_t need = round_up(work.size() * sizeof(int4), kWsAlign);
+    if (work.empty()) return MLA_OK;
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16))
+        return fail(MLA_ERR_WORKSPACE, "dense needs %zu workspace bytes (16-byte aligned), got %zu", need,
+                    workspace ? workspace_bytes : 0);
+    if (static_cast<int64_t>(work.size()) > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "too many tiles");
+    cudaError_t e = cudaMemcpyAsync(workspace, work.data(), work.size() * sizeof(int4), cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "schedule upload");
+    mla::AttnArgs a = attn_args(seqs, q_bf16, num_heads, kv_ds, nullptr, sm_scale, out_bf16, lse, dev_err);
+    e = mla::launch_dense_ds(a, static_cast<const int4 *>(workspace), static_cast<int>(work.size()), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "dense launch");
+    return MLA_OK;
+}
+
+mla_status_t mla_prefill_sparse_ds(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads, const uint8_t *kv_ds,
+                                   float sm_scale, const int32_t *idx, int32_t topk, void *out_bf16, float *lse,
+                                   int32_t *dev_err, cudaStream_t stream) {
+    g_err.clear();
+    mla_status_t st = check_seqs(seqs);
+    if (st != MLA_OK) return st;
+    if (!heads_ok(num_heads)) return fail(MLA_ERR_UNSUPPORTED, "num_heads must be 16, 32, 64 or 128 (got %d)", num_heads);
+    if ((st = check_attn_ptrs(q_bf16, kv_ds, reinterpret_cast<const float *>(kv_ds), out_bf16, lse, sm_scale)) != MLA_OK)
+        return st;
+    if (!idx || !aligned(idx, 4)) return fail(MLA_ERR_INVALID_ARG, "idx must be set and 4-byte aligned");
+    if (topk < 1 || topk > 2048) return fail(MLA_ERR_UNSUPPORTED, "topk must be in [1, 2048] (got %d)", topk);
+    const int64_t tq = seqs->cu_seqlens_q_host[seqs->batch];
+    if (tq == 0) return MLA_OK;
+    if (tq > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "too many query tokens");
+    mla::AttnArgs a = attn_args(seqs, q_bf16, num_heads, kv_ds, nullptr, sm_scale, out_bf16, lse, dev_err);
+    a.idx = idx;
+    a.topk = topk;
+    a.tok_begin = 0;
+    a.tok_end = tq;
+    const cudaError_t e = mla::launch_sparse_ds(a, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "sparse launch");
+    return MLA_OK;
+}
+
 mla_status_t mla_kv_append(const mla_seqs_t *seqs, const void *latent_bf16, const void *kidx_bf16,
                            uint8_t *kv_e4m3, float *kv_scale, uint8_t *ki_e4m3, float *ki_scale,
                            int32_t *dev_err, cudaStream_t stream) {
