@@ -662,6 +662,58 @@ def measure_workload(name, dev, steps, warmup):
     return obj
 
 
+def measure_ds_layout(name, dev, steps, warmup):
+    """The workload on the 656-byte cache rows (mla_prefill_dense_ds /
+    mla_prefill_sparse_ds, the sparse step's indices from mla_indexer_topk
+    outside the timed calls): per-call time of the attention alone and its
+    roofline against the bf16 tensor peak (these kernels run kind::f16)."""
+    import torch
+    from mla_prefill_attention_gb300 import (MLA_OP_DENSE, Seqs, inputs as I, mla_indexer_topk, mla_prefill_dense_ds,
+                                             mla_prefill_sparse_ds, mla_workspace_size)
+    from mla_prefill_attention_gb300 import flops as F
+    w = I.WORKLOADS[name]
+    ps = w.seqs()
+    seqs = Seqs.from_paged(ps, device=dev)
+    q = torch.from_numpy(I.gen_q_bf16(w.seed, ps.total_q, w.heads).view(np.int16)).view(torch.bfloat16).to(dev)
+    kv = torch.from_numpy(I.gen_latent_cache_ds(w.seed, ps)).to(dev)
+    out = torch.empty((ps.total_q, w.heads, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((ps.total_q, w.heads), dtype=torch.float32, device=dev)
+    if w.sparse:
+        qi, wh, ki, kis = [torch.from_numpy(x).to(dev) for x in I.gen_indexer_inputs(w.seed, ps)]
+        idx = mla_indexer_topk(seqs, qi, wh, 0, ki, kis, w.topk)
+        flops = F.sparse_flops(w.q_lens, w.prefix_lens, w.heads, w.topk)
+        call = lambda: mla_prefill_sparse_ds(seqs, q, kv, w.sm_scale, idx, out=out, lse=lse)
+    else:
+        ws = torch.empty(max(16, mla_workspace_size(MLA_OP_DENSE, seqs, w.heads)), dtype=torch.uint8, device=dev)
+        flops = F.dense_flops(w.q_lens, w.prefix_lens, w.heads)
+        call = lambda: mla_prefill_dense_ds(seqs, q, kv, w.sm_scale, out=out, lse=lse, workspace=ws)
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    pk, src = peaks()
+    bf16 = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
+    tf = flops / (ms / 1000.0) / 1e12
+    obj = {"workload": name, "layout": "656-byte rows (512 e4m3 + 4 fp32 group scales + 64 bf16 RoPE)",
+           "steps": steps, "warmup": warmup, "ms_per_call": ms, "value": ps.total_q / (ms / 1000.0),
+           "unit": "tok/s", "attention_tflops": tf,
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16, "unit": "TFLOP/s", "frac": tf / bf16,
+                        "peak_source": f"{src} bf16 sustained (kind::f16 MMAs)",
+                        "kernel": "attn_ds kernel: rows dequantised to f16 in shared memory, tcgen05 kind::f16, "
+                                  "64 rows x 80 keys"}}
+    del q, kv, out, lse
+    torch.cuda.empty_cache()
+    return obj
+
+
 def cpu_info():
     """CPU model and the cores this process may run on (for the CPU baseline)."""
     model = None
@@ -820,6 +872,8 @@ def main():
                 continue
             k = 2 if name == "chunked200k" else min(args.steps, 5)
             extras[name] = measure_workload(name, dev, k, max(3, min(args.warmup, 3)))
+        for name in ("dense32k", "sparse64k"):
+            extras[name + "_656B"] = measure_ds_layout(name, dev, min(args.steps, 5), 3)
         line["workloads"] = extras
     if world > 1:
         dist.destroy_process_group()

@@ -89,6 +89,7 @@ def check_attention(gpu_out, ora_out, gpu_lse=None, ora_lse=None, what="", lse_e
     mx, mean, raw_mx, raw_mean, fl_mx, fl_mean, rms = attention_errors(gpu_out, ora_out)
     msg = (f"{what}: beyond bf16 rounding max {mx:.3e} mean {mean:.3e}; raw max {raw_mx:.3e} mean {raw_mean:.3e}; "
            f"bf16 floor max {fl_mx:.3e} mean {fl_mean:.3e} (rms {rms:.3e})")
+    print(msg)
     assert mx <= TOL_MAX and mean <= TOL_MEAN, msg
     assert raw_mx <= fl_mx + FLOOR_MARGIN * TOL_MAX and raw_mean <= fl_mean + FLOOR_MARGIN * TOL_MEAN, msg
     if gpu_lse is not None:
