@@ -48,6 +48,9 @@ H_IDX = 64          # indexer heads
 
 # tensor ids of the counter-based streams
 T_Q, T_KV, T_QIDX, T_KIDX, T_WIDX, T_PERM, T_MISC, T_NEWKV, T_NEWKIDX, T_GAIN = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
+T_QMHA, T_WUKV = 11, 12
+D_HEAD_QK = 192     # non-absorbed form: 128 no-RoPE + 64 RoPE dims per head
+D_HEAD_V = 128
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "inputs_gen.c")
@@ -189,14 +192,30 @@ def make_seqs(q_lens, prefix_lens, seed: int, shuffle: bool, extra_blocks: int =
     return PagedSeqs(cu, np.asarray(prefix_lens, dtype=np.int32), bt, total)
 
 
-def gen_q_bf16(seed: int, total_q: int, heads: int, token_rows=None, dim: int = D_QK) -> np.ndarray:
+def gen_q_bf16(seed: int, total_q: int, heads: int, token_rows=None, dim: int = D_QK, tensor: int = T_Q) -> np.ndarray:
     """bf16 bits [n, heads, dim] of N(0,1) queries; row stream = token*heads + head.
     token_rows selects global query tokens (default: all total_q)."""
     toks = np.arange(total_q, dtype=np.int64) if token_rows is None else np.asarray(token_rows, np.int64)
     rows = _rows((toks[:, None] * heads + np.arange(heads, dtype=np.int64)[None, :]).reshape(-1))
     out = np.empty((toks.shape[0], heads, dim), dtype=np.uint16)
-    _gen().gen_normal_bf16(seed, T_Q, _p(rows), rows.shape[0], dim, _p(out))
+    _gen().gen_normal_bf16(seed, tensor, _p(rows), rows.shape[0], dim, _p(out))
     return out
+
+
+def gen_q_mha(seed: int, total_q: int, heads: int, token_rows=None) -> np.ndarray:
+    """bf16 bits [n, heads, 192] of N(0,1) per-head queries of the non-absorbed
+    form (128 no-RoPE dims, then 64 RoPE dims)."""
+    return gen_q_bf16(seed, total_q, heads, token_rows, dim=D_HEAD_QK, tensor=T_QMHA)
+
+
+def gen_w_ukv(seed: int, heads: int) -> np.ndarray:
+    """bf16 bits [heads, 256, 512] of the key/value up-projection (random-init:
+    no trained weights): N(0,1) * 2^-4 rounded to bf16, so a no-RoPE key or a
+    value dim of an N(0,1) latent row has a standard deviation near sqrt(512)/16.
+    Rows 0..127 of head h are W_UK_h, rows 128..255 W_UV_h; row stream h*256 + i."""
+    rows = np.arange(heads * 256, dtype=np.int64)
+    x = normal_rows(seed, T_WUKV, rows, D_V) * 2.0 ** -4
+    return bf16_bits(x).reshape(heads, 256, D_V)
 
 
 def latent_rows(seed: int, b: int, positions, tensor: int = T_KV):
@@ -364,6 +383,9 @@ WORKLOADS = {
     # sparse top-2048 at 64k context: 8,192 new tokens after a 57,344-token prefix
     "sparse64k": Workload("sparse64k", 3, 64, [8192], [57344], True, sparse=True,
                           notes="indexer 64x128 + top-2048 + sparse MLA, 8,192 queries at the end of 65,536"),
+    # a batch of short prompts (each within the top-k of 2,048), the non-absorbed (MHA) path's workload
+    "mha_short": Workload("mha_short", 5, 64, [2048, 1536, 1024, 1024, 768, 512, 300, 77], [0] * 8, True,
+                          notes="8 prompts of 77-2,048 tokens (7,289 in all), 64 heads, non-absorbed MHA path"),
     # chunked prefill of a 200,000-token prompt in 6,144-token chunks
     "chunked200k": Workload("chunked200k", 4, 64, [200000], [0], True, sparse=True, chunk=6144,
                             notes="200,000-token prompt in 6,144-token chunks (32 full + 3,392)"),

@@ -32,6 +32,11 @@
  *    order (score descending, position ascending).
  *  - Merge of partial results (DCP section of GLM-5.3 Teil 2): out and lse of
  *    attention over a union of disjoint key sets from each set's out and lse.
+ *  - Non-absorbed (MHA) form for short prompts (GLM-5.3 Teil 2, section
+ *    Ausprobieren: without the sparse_mla_force_mqa flag, prefill batches whose
+ *    prompts fit within the top-k of 2,048 tokens take the dense MHA path): per
+ *    head the latent row is up-projected into a 128-dim no-RoPE key and a
+ *    128-dim value; the key gets the 64 shared RoPE dims appended (192 dims).
  *  - Cache write (the step before attention): per token and row, scale =
  *    absmax / 448 (1 for a zero row, at least 2^-126 otherwise), codes =
  *    nearest e4m3 of x times the reciprocal of the scale, ties to even,
@@ -452,4 +457,115 @@ void ora_merge(int32_t n_parts, const double *outs, const double *lses, int64_t 
         }
         lse[r] = m + log(total);
     }
+}
+
+/* Non-absorbed (MHA) dense causal prefill for n_sel selected new tokens.
+ *
+ * Per head h, with c_s = K_s[0..511] and r_s = K_s[512..575] the latent and RoPE
+ * parts of the decoded cache row of position s (580-byte rows):
+ *   k_{s,h} = [ W_UK_h c_s ; r_s ]        192 dims
+ *   v_{s,h} = W_UV_h c_s                  128 dims
+ * where w_ukv is [H][256][512]: rows 0..127 of head h are W_UK_h and rows
+ * 128..255 are W_UV_h (k_{s,h}[i] = sum_d W_UK_h[i][d] c_s[d]). Query row
+ * q_{t,h} (192 dims: 128 no-RoPE, then 64 RoPE, RoPE already applied) attends
+ * causally to s = 0..p:
+ *   logit_s = sm_scale * q_{t,h} . k_{s,h}
+ *   out[t,h] = sum_s exp(logit_s - m) v_{s,h} / sum_s exp(logit_s - m)   (128 dims)
+ *   lse[t,h] = m + ln sum_s exp(logit_s - m),   m = max_s logit_s
+ * The up-projection of every key a sequence's selected tokens see is computed
+ * first (one plain matrix product per key and head), then the attention.
+ * q: fp64 [n_sel][H][192]; w_ukv: fp64 [H][256][512]; out: [n_sel][H][128];
+ * lse: [n_sel][H]. Returns 0, or a negative count of failed rows (token out of
+ * range or a needed key on an unmapped page). */
+int ora_mla_mha(int32_t batch, const int32_t *cu_seqlens_q, const int32_t *prefix_lens,
+                const int32_t *block_table, int32_t max_blocks, int32_t num_blocks,
+                const double *q, const int64_t *tokens, int64_t n_sel, int32_t H,
+                const uint8_t *kv, const float *kv_scale, const double *w_ukv, double sm_scale,
+                double *out, double *lse) {
+    ora_init();
+    int64_t fails = 0;
+    int *seq_of = (int *)malloc((size_t)(n_sel > 0 ? n_sel : 1) * sizeof(int));
+    int64_t *pos_of = (int64_t *)malloc((size_t)(n_sel > 0 ? n_sel : 1) * sizeof(int64_t));
+    for (int64_t sel = 0; sel < n_sel; ++sel) {
+        int64_t i;
+        seq_of[sel] = locate(batch, cu_seqlens_q, tokens[sel], &i);
+        pos_of[sel] = seq_of[sel] >= 0 ? (int64_t)prefix_lens[seq_of[sel]] + i : -1;
+        if (seq_of[sel] < 0) ++fails;
+    }
+    for (int b = 0; b < batch; ++b) {
+        int64_t need = -1;                     /* the largest position a selected token of b sees */
+        for (int64_t sel = 0; sel < n_sel; ++sel)
+            if (seq_of[sel] == b && pos_of[sel] > need) need = pos_of[sel];
+        if (need < 0) continue;
+        const int64_t n_keys = need + 1;
+        double *kh = (double *)malloc((size_t)(n_keys * H * 192) * sizeof(double));
+        double *vh = (double *)malloc((size_t)(n_keys * H * 128) * sizeof(double));
+        int unmapped = 0;
+        /* step 1: the up-projection of keys 0..need, every head */
+#pragma omp parallel for schedule(dynamic, 4) reduction(| : unmapped)
+        for (int64_t s = 0; s < n_keys; ++s) {
+            const int64_t r = cache_row(block_table, max_blocks, num_blocks, b, s);
+            if (r < 0) {
+                unmapped = 1;
+                continue;
+            }
+            double k[ORA_DQK];
+            decode_row(ORA_FMT_580, kv, kv_scale, r, k);
+            for (int h = 0; h < H; ++h) {
+                const double *wk = w_ukv + (int64_t)h * 256 * ORA_DV;      /* W_UK_h: rows 0..127 */
+                const double *wv = wk + 128 * ORA_DV;                      /* W_UV_h: rows 128..255 */
+                double *kout = kh + (s * H + h) * 192;
+                double *vout = vh + (s * H + h) * 128;
+                for (int i = 0; i < 128; ++i) {
+                    double acc = 0.0;
+                    for (int d = 0; d < ORA_DV; ++d) acc += wk[(int64_t)i * ORA_DV + d] * k[d];
+                    kout[i] = acc;
+                }
+                for (int j = 0; j < 64; ++j) kout[128 + j] = k[ORA_DV + j];
+                for (int i = 0; i < 128; ++i) {
+                    double acc = 0.0;
+                    for (int d = 0; d < ORA_DV; ++d) acc += wv[(int64_t)i * ORA_DV + d] * k[d];
+                    vout[i] = acc;
+                }
+            }
+        }
+        /* step 2: causal softmax attention of each selected token and head */
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : fails)
+        for (int64_t rh = 0; rh < n_sel * H; ++rh) {
+            const int64_t sel = rh / H, h = rh % H;
+            if (seq_of[sel] != b) continue;
+            if (unmapped) {
+                ++fails;
+                continue;
+            }
+            const int64_t p = pos_of[sel];
+            const double *qr = q + rh * 192;
+            double *logit = (double *)malloc((size_t)(p + 1) * sizeof(double));
+            double m = -INFINITY;
+            for (int64_t s = 0; s <= p; ++s) {
+                const double *kr = kh + (s * H + h) * 192;
+                double dot = 0.0;
+                for (int e = 0; e < 192; ++e) dot += qr[e] * kr[e];
+                logit[s] = sm_scale * dot;
+                if (logit[s] > m) m = logit[s];
+            }
+            double *o = out + rh * 128;
+            for (int i = 0; i < 128; ++i) o[i] = 0.0;
+            double l = 0.0;
+            for (int64_t s = 0; s <= p; ++s) {
+                const double wgt = exp(logit[s] - m);
+                const double *vr = vh + (s * H + h) * 128;
+                l += wgt;
+                for (int i = 0; i < 128; ++i) o[i] += wgt * vr[i];
+            }
+            for (int i = 0; i < 128; ++i) o[i] /= l;
+            lse[rh] = m + log(l);
+            free(logit);
+        }
+        free(kh);
+        free(vh);
+    }
+    free(seq_of);
+    free(pos_of);
+    return fails ? (int)-fails : 0;
 }

@@ -47,6 +47,8 @@ def lib():
         L.ora_mla_dense_fmt.argtypes = [ctypes.c_int] + seq + [vp, vp, i64, i32, vp, vp, dbl, vp, vp]
         L.ora_mla_sparse_fmt.restype = ctypes.c_int
         L.ora_mla_sparse_fmt.argtypes = [ctypes.c_int] + seq + [vp, vp, i64, i32, vp, vp, dbl, vp, i32, vp, vp]
+        L.ora_mla_mha.restype = ctypes.c_int
+        L.ora_mla_mha.argtypes = seq + [vp, vp, i64, i32, vp, vp, vp, dbl, vp, vp]
         L.ora_indexer_topk.restype = ctypes.c_int
         L.ora_indexer_topk.argtypes = seq + [vp, vp, i64, vp, i64, vp, vp, i32, vp, vp, i64]
         L.ora_e4m3_nearest.restype = ctypes.c_uint8
@@ -179,6 +181,32 @@ def mla_sparse_ds(seqs, q, tokens, kv_ds, sm_scale, idx):
     if rc != 0:
         raise ValueError(f"oracle sparse: {-rc} rows failed")
     return out, lse
+
+def mla_mha(seqs, q, tokens, kv, kv_scale, w_ukv, sm_scale):
+    """fp64 non-absorbed (MHA) dense causal prefill for the selected tokens:
+    per head, keys [W_UK_h c_s ; r_s] (192 dims) and values W_UV_h c_s (128
+    dims) from the 580-byte cache rows. q: bf16 bits [n, H, 192] (uint16) or
+    fp64; w_ukv: bf16 bits or fp64 [H, 256, 512] (rows 0..127 of head h W_UK_h,
+    rows 128..255 W_UV_h). Returns (out [n, H, 128], lse [n, H])."""
+    q = np.asarray(q)
+    qd = bf16_to_f64(q) if q.dtype == np.uint16 else _c(q, np.float64)
+    w = np.asarray(w_ukv)
+    wd = bf16_to_f64(w) if w.dtype == np.uint16 else _c(w, np.float64)
+    n, H = qd.shape[0], qd.shape[1]
+    tok = _c(tokens, np.int64)
+    if tok.shape != (n,) or qd.shape[2] != 192:
+        raise ValueError("q must be [len(tokens), H, 192]")
+    if wd.shape != (H, 256, 512):
+        raise ValueError("w_ukv must be [H, 256, 512]")
+    kvc, kvs = _c(kv, np.uint8), _c(kv_scale, np.float32)
+    keep, sa = _seq_args(seqs)
+    out = np.zeros((n, H, 128), dtype=np.float64)
+    lse = np.zeros((n, H), dtype=np.float64)
+    rc = lib().ora_mla_mha(*sa, _p(qd), _p(tok), n, H, _p(kvc), _p(kvs), _p(wd), float(sm_scale), _p(out), _p(lse))
+    if rc != 0:
+        raise ValueError(f"oracle mha: {-rc} rows failed (token out of range or unmapped page)")
+    return out, lse
+
 
 def indexer_topk(seqs, qi, w, w_stride, tokens, ki, ki_scale, topk, want_scores=False, ctx_cap=0):
     """Exact top-k selection per selected token; returns idx [n, topk] ascending,
