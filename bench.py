@@ -428,7 +428,7 @@ RUNS = {"tiny512": DenseRun, "prefix12k": DenseRun, "dense32k": DenseRun, "ragge
 # None until it is captured again.
 TRAFFIC = {
     "dense32k": {"attention": 2453488384 + 2118204416},
-    "sparse64k": {"indexer_topk": None,
+    "sparse64k": {"indexer_topk": 76523008 + 26764032,      # the fast-path launch (profiles/indexer_topk_sparse64k.md)
                   "sparse_attention": 807216896 + 533257472},
 }
 

@@ -76,7 +76,8 @@ typedef enum {
     MLA_OP_DENSE = 0,
     MLA_OP_INDEXER = 1,
     MLA_OP_SPARSE = 2,
-    MLA_OP_DENSE_HOST = 3   /* mla_prefill_dense_host, any chunk count */
+    MLA_OP_DENSE_HOST = 3,  /* mla_prefill_dense_host, any chunk count */
+    MLA_OP_MHA = 4          /* mla_prefill_mha */
 } mla_op_t;
 
 /* Ragged batch of sequences over one paged cache (256-token pages). */
@@ -174,6 +175,29 @@ mla_status_t mla_prefill_dense_ds(const mla_seqs_t *seqs, const void *q_bf16, in
 mla_status_t mla_prefill_sparse_ds(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads,
                                    const uint8_t *kv_ds, float sm_scale, const int32_t *idx, int32_t topk,
                                    void *out_bf16, float *lse, int32_t *dev_err, cudaStream_t stream);
+
+/* Non-absorbed (MHA) dense causal prefill, the path GLM-5.3 Teil 2 (section
+ * Ausprobieren) describes for prefill batches whose prompts fit within the
+ * top-k of 2,048 tokens when sparse_mla_force_mqa is off. Per head h, with c_s
+ * = kv_scale_s * dec(kv_s[0:512]) and r_s = kv_scale_s * dec(kv_s[512:576]):
+ *   k[s,h] = [ W_UK_h c_s ; r_s ]  (192 dims),   v[s,h] = W_UV_h c_s  (128 dims)
+ *   out[t,h,:] = sum_s softmax_s(sm_scale * q[t,h,:] . k[s,h]) v[s,h],  s = 0..p
+ *   lse[t,h]   = ln sum_s exp(sm_scale * q[t,h,:] . k[s,h])
+ * q_bf16: [Tq, H, 192] (128 no-RoPE dims, then 64 RoPE dims with RoPE applied);
+ * w_ukv_bf16: [H, 256, 512], rows 0..127 of head h are W_UK_h and rows
+ * 128..255 W_UV_h (k[s,h][i] = sum_d W_UK_h[i][d] c_s[d]); out_bf16: [Tq, H,
+ * 128]; lse: [Tq, H] or NULL. The keys and values of every sequence's whole
+ * context are first up-projected into the workspace as bf16 (k and v rows of
+ * 256 bytes per head, 128 bytes of RoPE dims per row; each context padded to
+ * 128 rows), then attended. Any prompt length works; the workspace grows with
+ * the context times the heads, which is why the path suits short prompts.
+ * num_heads in {16, 32, 64, 128}; q, w_ukv, out and kv 16-byte aligned.
+ * workspace: mla_workspace_size(MLA_OP_MHA, ...) bytes, 256-byte aligned.
+ * Errors as mla_prefill_dense. */
+mla_status_t mla_prefill_mha(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads, const void *w_ukv_bf16,
+                             const uint8_t *kv_e4m3, const float *kv_scale, float sm_scale, void *out_bf16,
+                             float *lse, void *workspace, size_t workspace_bytes, int32_t *dev_err,
+                             cudaStream_t stream);
 
 /* Largest work list mla_prefill_dense_static can hold: 65,536 items of 16
  * bytes (1 MiB of device memory, reserved on every GPU that loads the library

@@ -18,11 +18,11 @@ LIB_PATH = os.path.join(_HERE, "libmla.so")
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_WORKSPACE = range(5)
 MLA_DEVERR_BAD_PAGE, MLA_DEVERR_BAD_INDEX, MLA_DEVERR_TIMEOUT, MLA_DEVERR_INTERNAL = 1, 2, 4, 8
 MLA_DEVERR_SEQ_MISMATCH = 16
-MLA_OP_DENSE, MLA_OP_INDEXER, MLA_OP_SPARSE, MLA_OP_DENSE_HOST = 0, 1, 2, 3
+MLA_OP_DENSE, MLA_OP_INDEXER, MLA_OP_SPARSE, MLA_OP_DENSE_HOST, MLA_OP_MHA = 0, 1, 2, 3, 4
 
 EXPORTS = ("mla_workspace_size", "mla_prefill_dense", "mla_indexer_topk", "mla_prefill_sparse", "mla_last_error",
            "mla_prefill_dense_static", "mla_kv_append", "mla_merge_attn", "mla_prefill_dense_host",
-           "mla_prefill_sparse_host", "mla_prefill_dense_ds", "mla_prefill_sparse_ds")
+           "mla_prefill_sparse_host", "mla_prefill_dense_ds", "mla_prefill_sparse_ds", "mla_prefill_mha")
 DENSE_STATIC_MAX_WORK_ITEMS = 65536
 DENSE_HOST_MAX_CHUNKS = 64
 
@@ -91,6 +91,8 @@ def load(path: str = LIB_PATH):
     L.mla_prefill_dense_ds.argtypes = [ctypes.POINTER(mla_seqs_t), vp, i32, vp, f32, vp, vp, vp, sz, vp, vp]
     L.mla_prefill_sparse_ds.restype = ctypes.c_int
     L.mla_prefill_sparse_ds.argtypes = [ctypes.POINTER(mla_seqs_t), vp, i32, vp, f32, vp, i32, vp, vp, vp, vp]
+    L.mla_prefill_mha.restype = ctypes.c_int
+    L.mla_prefill_mha.argtypes = [ctypes.POINTER(mla_seqs_t), vp, i32, vp, vp, vp, f32, vp, vp, vp, sz, vp, vp]
     L.mla_kv_append.restype = ctypes.c_int
     L.mla_kv_append.argtypes = [ctypes.POINTER(mla_seqs_t), vp, vp, vp, vp, vp, vp, vp, vp]
     L.mla_merge_attn.restype = ctypes.c_int
@@ -164,6 +166,24 @@ def mla_prefill_dense(seqs: Seqs, q: torch.Tensor, kv: torch.Tensor, kv_scale: t
     c = seqs.c()
     _check(load().mla_prefill_dense(ctypes.byref(c), _ptr(q), H, _ptr(kv), _ptr(kv_scale), float(sm_scale),
                                     _ptr(out), _ptr(lse), _ptr(ws), wsb, _ptr(dev_err), _stream()))
+    return out, lse
+
+
+def mla_prefill_mha(seqs: Seqs, q: torch.Tensor, w_ukv: torch.Tensor, kv: torch.Tensor, kv_scale: torch.Tensor,
+                    sm_scale: float, out=None, lse=None, want_lse: bool = True, workspace=None, dev_err=None):
+    """Non-absorbed (MHA) dense causal prefill. q bf16 [Tq,H,192] (128 no-RoPE dims,
+    then 64 RoPE dims); w_ukv bf16 [H,256,512] (rows 0..127 of head h W_UK_h, rows
+    128..255 W_UV_h); kv uint8 [nb,256,576]; kv_scale f32 [nb,256].
+    Returns (out bf16 [Tq,H,128], lse f32 [Tq,H] or None)."""
+    H = q.shape[1]
+    if out is None:
+        out = torch.empty((q.shape[0], H, 128), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((q.shape[0], H), dtype=torch.float32, device=q.device)
+    ws, wsb = _workspace(MLA_OP_MHA, seqs, H, 0, workspace)
+    c = seqs.c()
+    _check(load().mla_prefill_mha(ctypes.byref(c), _ptr(q), H, _ptr(w_ukv), _ptr(kv), _ptr(kv_scale),
+                                  float(sm_scale), _ptr(out), _ptr(lse), _ptr(ws), wsb, _ptr(dev_err), _stream()))
     return out, lse
 
 

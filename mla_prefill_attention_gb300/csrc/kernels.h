@@ -44,6 +44,41 @@ cudaError_t launch_sparse_f8(const AttnArgs &a, cudaStream_t st);
 cudaError_t launch_dense_ds(const AttnArgs &a, const int4 *work, int n_work, cudaStream_t st);
 cudaError_t launch_sparse_ds(const AttnArgs &a, cudaStream_t st);
 
+// Non-absorbed (MHA) path: per-head keys [W_UK c ; r] (192 dims) and values
+// W_UV c (128 dims), up-projected from the 580-byte cache rows into a workspace,
+// then causal attention per head.
+constexpr int kDr = 64;        // RoPE dims
+constexpr int kDvh = 128;      // no-RoPE key dims and value dims per head
+struct MhaArgs {
+    const __nv_bfloat16 *q;      // [Tq, H, 192]
+    const uint8_t *kv;           // [num_blocks, 256, 576] e4m3
+    const float *kv_scale;       // [num_blocks, 256]
+    const int32_t *block_table;  // [batch, max_blocks]
+    int32_t max_blocks, num_blocks;
+    __nv_bfloat16 *kn;           // [H, R, 128] up-projected no-RoPE keys
+    __nv_bfloat16 *v;            // [H, R, 128] up-projected values
+    __nv_bfloat16 *kr;           // [R, 64] RoPE dims of the keys
+    int64_t R;                   // key rows: each sequence's context padded to 128
+    __nv_bfloat16 *out;          // [Tq, H, 128]
+    float *lse;                  // [Tq, H] or null
+    int32_t H;
+    int32_t up_heads;            // heads per up-projection CTA (divides H)
+    float sm_scale_log2;
+    int32_t *dev_err;
+};
+// Up-projection: work item = {sequence, first position (a multiple of 128),
+// key-row base of those rows, context length}; tmap_w: w_ukv as [H*256 rows][512]
+// bf16, 64 x 256 boxes, 128-byte swizzle.
+cudaError_t launch_mha_up(const MhaArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_w, cudaStream_t st);
+// Attention: work item = two int4, {sequence, first new token in it, that
+// token's global index, valid rows <= 128} and {prefix, key-row base, key tiles
+// of 64, 0}; one CTA per item and head. tmap_q: q as [Tq][H][192] bf16, boxes
+// of 64 dims x 1 head x 128 tokens; tmap_kn / tmap_v: [H*R rows][128], 64 x 64
+// boxes; tmap_kr: [R][64], 64 x 64 boxes; all with the 128-byte swizzle.
+cudaError_t launch_mha_attn(const MhaArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_q,
+                            const CUtensorMap &tmap_kn, const CUtensorMap &tmap_kr, const CUtensorMap &tmap_v,
+                            cudaStream_t st);
+
 struct IndexerArgs {
     const uint8_t *qi;           // [Tq, 64, 128] e4m3
     const float *w;              // row t at w + t * w_stride

@@ -1,0 +1,531 @@
+// Non-absorbed (MHA) MLA prefill for short prompts (tcgen05 kind::f16, bf16).
+//
+// GLM-5.3-Optimierungen Teil 2, section Ausprobieren: without the
+// sparse_mla_force_mqa flag, prefill batches whose prompts fit within the
+// top-k of 2,048 tokens take the dense MHA path. Per head h, with c_s the 512
+// latent values and r_s the 64 RoPE values of cached token s (580-byte row:
+// sigma_s * dec(codes)):
+//
+//   k_{s,h} = [ W_UK_h c_s ; r_s ]   (192 dims)      v_{s,h} = W_UV_h c_s   (128 dims)
+//   out[t,h] = sum_s softmax_s(sm_scale q_{t,h} . k_{s,h}) v_{s,h},   s <= p(t)
+//
+// Two kernels.
+//
+// 1. Up-projection, one CTA per 128 cached rows of a sequence and a group of
+//    heads: 256 threads decode the rows' e4m3 codes into bf16 (exact: an e4m3
+//    value has 4 significant bits) in shared memory, in the 128-byte-swizzled
+//    K-major layout (8 slices of 64 latent dims); the tensor core multiplies
+//    them by each head's [256 x 512] slice of w_ukv (TMA, 64-dim boxes through
+//    a 3-stage ring): D[row][n] = sum_d dec(c)[row][d] W[h][n][d], M = 128
+//    rows, N = 256 (k then v), K = 512, into one of two TMEM accumulators;
+//    four epilogue warps (thread = row) scale by sigma_row and write bf16 k and
+//    v rows head-major, [H][R][128]. The first head group also writes the
+//    RoPE dims, bf16(sigma * dec(c)), as [R][64]. Rows past the context are
+//    written as zeros (each sequence's rows are padded to 128).
+//
+// 2. Attention, one CTA per 128 new tokens of a sequence and one head:
+//      S  = Q K^T        M = 128 tokens, N = 64 keys, K = 192 (3 x 64-dim
+//                        slices: two no-RoPE, one RoPE); S in one of two TMEM
+//                        buffers so QK(t+1) runs during the softmax of tile t
+//      P  = 2^(S*sm_scale*log2e - m)   in registers (a thread per query row),
+//                        rounded to bf16 into shared memory
+//      O += P V          M = 128, N = 128 value dims, K = 64 keys (O in TMEM)
+//    m is the row's running reference maximum; O and l are rescaled only when
+//    a tile raises it by more than 8 (log2 units), so P stays below 2^8. l
+//    sums the fp32 P. At the end out = O / l and lse = ln2 (m + log2 l).
+//    Warps 0-3 softmax and epilogue (warp w owns TMEM lanes 32w..32w+31 =
+//    query rows), 4 TMA producer, 5 MMA issuer (one thread).
+//
+// Every wait is bounded; one that runs out sets MLA_DEVERR_TIMEOUT and the
+// CTA stops; before it exits, the producer waits for its copies and the issuer
+// for its MMAs.
+#include <cuda.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace mla {
+namespace mha {
+
+using namespace tc;
+
+constexpr long long kWaitCycles = 200000000LL;
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, int32_t *dev_err) {
+    if (mbar_wait_cycles(smem_u32(bar), parity, kWaitCycles)) return true;
+    set_dev_err(dev_err, MLA_DEVERR_TIMEOUT);
+    return false;
+}
+
+// Two e4m3 codes (low byte first) as two bf16 values (exact).
+__device__ __forceinline__ uint32_t bf16x2_of_e4m3x2(uint16_t two) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+    return pack_bf162(f.x, f.y);
+}
+
+// ===========================================================================
+// 1. up-projection
+// ===========================================================================
+constexpr int UP_ROWS = 128;
+constexpr int UP_NT = 320;                       // warps 0-7 decode; then 0-3 epilogue, 8 producer, 9 issuer
+constexpr int UP_WST = 3;                        // weight ring stages
+constexpr int kUpSlice = UP_ROWS * 128;          // one 64-dim slice of the decoded rows: 16 KB
+constexpr int kUpA = 8 * kUpSlice;               // 128 KB
+constexpr int kUpW = 256 * 128;                  // one 64-dim slice of one head's 256 weight rows: 32 KB
+constexpr int kUpOffW = kUpA;
+constexpr int kUpOffSig = kUpOffW + UP_WST * kUpW;
+constexpr int kUpSmem = 1024 + kUpOffSig + UP_ROWS * 4;
+static_assert(kUpSmem <= 232448 - 256, "shared memory");
+
+enum UpBar { U_W_FULL = 0, U_W_EMPTY = U_W_FULL + UP_WST, U_D_FULL = U_W_EMPTY + UP_WST, U_D_FREE = U_D_FULL + 2,
+             U_FINAL = U_D_FREE + 2, U_NBAR };
+
+__global__ void __launch_bounds__(UP_NT, 1)
+    up_kernel(const MhaArgs a, const int4 *__restrict__ work, const __grid_constant__ CUtensorMap tmap_w) {
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    __shared__ uint64_t bar[U_NBAR];
+    __shared__ uint32_t tmem_slot;
+    const uint32_t raw = smem_u32(dsm);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint8_t *sbase = dsm + pad;
+    const uint32_t sbase_a = raw + pad;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const int n_hg = a.H / a.up_heads;
+    const int4 it = work[blockIdx.x / n_hg];
+    const int hg = blockIdx.x % n_hg;
+    const int b = it.x, pos0 = it.y, ctx = it.w;
+    const int64_t row0 = it.z;
+    const int h0 = hg * a.up_heads, nh = a.up_heads;
+    float *sig = reinterpret_cast<float *>(sbase + kUpOffSig);
+
+    if (tid == 0) {
+        for (int i = 0; i < U_NBAR; ++i) mbar_init(smem_u32(&bar[i]), (i >= U_D_FREE && i < U_D_FREE + 2) ? 4u : 1u);
+        mbar_fence_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(&tmem_slot), 512);
+        tmem_relinquish();
+    }
+    if (warp == 8 && lane == 0) tma_prefetch_desc(&tmap_w);
+
+    // ----- decode: thread (row r, half) takes latent dims 256*half .. +255 -----
+    if (warp < 8) {
+        const int r = tid >> 1, half = tid & 1;
+        const int pos = pos0 + r;
+        int64_t cr = -1;
+        if (pos < ctx) cr = cache_row(a.block_table + static_cast<int64_t>(b) * a.max_blocks, a.max_blocks,
+                                      a.num_blocks, pos, a.dev_err);
+        const float s = cr >= 0 ? __ldg(a.kv_scale + cr) : 0.f;
+        if (half == 0) sig[r] = s;
+        const uint8_t *src = a.kv + (cr >= 0 ? cr : 0) * kDqk;
+#pragma unroll 4
+        for (int c = 0; c < 16; ++c) {
+            const int d0 = 256 * half + 16 * c;
+            uint4 raw16 = make_uint4(0u, 0u, 0u, 0u);
+            if (cr >= 0) raw16 = __ldg(reinterpret_cast<const uint4 *>(src + d0));
+            const uint32_t wv[4] = {raw16.x, raw16.y, raw16.z, raw16.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                o[2 * k] = bf16x2_of_e4m3x2(static_cast<uint16_t>(wv[k] & 0xFFFFu));
+                o[2 * k + 1] = bf16x2_of_e4m3x2(static_cast<uint16_t>(wv[k] >> 16));
+            }
+            const int ch = (d0 & 63) >> 3;
+            uint8_t *rowp = sbase + (d0 >> 6) * kUpSlice + r * 128;
+            *reinterpret_cast<uint4 *>(rowp + ((ch ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(rowp + (((ch + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        if (hg == 0) {      // the shared RoPE dims: 32 per thread
+            uint4 rr[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+            if (cr >= 0) {
+                rr[0] = __ldg(reinterpret_cast<const uint4 *>(src + kDv + 32 * half));
+                rr[1] = __ldg(reinterpret_cast<const uint4 *>(src + kDv + 32 * half + 16));
+            }
+            uint32_t o[16];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const uint32_t wv[4] = {rr[q].x, rr[q].y, rr[q].z, rr[q].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const uint16_t two = static_cast<uint16_t>(wv[k] >> (16 * e));
+                        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+                        o[8 * q + 2 * k + e] = pack_bf162(s * f.x, s * f.y);
+                    }
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(a.kr + (row0 + r) * kDr + 32 * half);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        }
+        fence_proxy_async();
+    }
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 8) {
+        // =================== TMA producer: each head's weight slices ===================
+        if (lane == 0) {
+            int n = 0;
+            bool ok = true;
+            for (int hh = 0; hh < nh && ok; ++hh)
+                for (int s = 0; s < 8 && ok; ++s, ++n) {
+                    const int st = n % UP_WST;
+                    if (n >= UP_WST && !(ok = wait_bar(&bar[U_W_EMPTY + st], ((n / UP_WST) - 1) & 1, a.dev_err))) break;
+                    mbar_expect_tx(smem_u32(&bar[U_W_FULL + st]), kUpW);
+                    tma_load_2d(sbase_a + kUpOffW + st * kUpW, &tmap_w, 64 * s, (h0 + hh) * 256,
+                                smem_u32(&bar[U_W_FULL + st]));
+                }
+            // drain: the last load of every stage has landed before the CTA exits
+            for (int j = (n > UP_WST ? n - UP_WST : 0); j < n; ++j)
+                if (!mbar_wait_cycles(smem_u32(&bar[U_W_FULL + j % UP_WST]), (j / UP_WST) & 1, kWaitCycles))
+                    set_dev_err(a.dev_err, MLA_DEVERR_TIMEOUT);
+        }
+    } else if (warp == 9) {
+        // =================== MMA issuer ===================
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(128, 256, true, true, false, false);
+            const uint64_t da0 = sdesc(sbase_a, 16, 1024, kSw128);
+            const uint64_t dw0 = sdesc(sbase_a + kUpOffW, 16, 1024, kSw128);
+            int n = 0;
+            bool ok = true;
+            for (int hh = 0; hh < nh && ok; ++hh) {
+                const int db = hh & 1;
+                if (hh >= 2 && !(ok = wait_bar(&bar[U_D_FREE + db], ((hh >> 1) - 1) & 1, a.dev_err))) break;
+                fence_after_sync();
+                const uint32_t d = tmem + 256u * db;
+                for (int s = 0; s < 8; ++s, ++n) {
+                    const int st = n % UP_WST;
+                    if (!(ok = wait_bar(&bar[U_W_FULL + st], (n / UP_WST) & 1, a.dev_err))) break;
+                    fence_after_sync();
+                    const uint64_t da = da0 + static_cast<uint64_t>((s * kUpSlice) >> 4);
+                    const uint64_t dw = dw0 + static_cast<uint64_t>((st * kUpW) >> 4);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16_ss_w(d, da + 2 * ks, dw + 2 * ks, idesc, (s | ks) ? 1u : 0u, 1u);
+                    mma_commit(smem_u32(&bar[U_W_EMPTY + st]));
+                }
+                if (ok) mma_commit(smem_u32(&bar[U_D_FULL + db]));
+            }
+            mma_commit(smem_u32(&bar[U_FINAL]));
+        }
+    } else if (warp < 4) {
+        // =================== epilogue: thread = row ===================
+        const int r = 32 * warp + lane;
+        const float s = sig[r];
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * warp) << 16;
+        for (int hh = 0; hh < nh; ++hh) {
+            const int db = hh & 1, h = h0 + hh;
+            const bool got = wait_bar(&bar[U_D_FULL + db], (hh >> 1) & 1, a.dev_err);
+            if (!__all_sync(0xffffffffu, got)) break;
+            fence_after_sync();
+            const int64_t krow = (static_cast<int64_t>(h) * a.R + row0 + r) * kDvh;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_addr + 256u * db + 32u * c, v);
+                tmem_ld_wait();
+                uint32_t o[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    o[k] = pack_bf162(s * __uint_as_float(v[2 * k]), s * __uint_as_float(v[2 * k + 1]));
+                __nv_bfloat16 *base = (c < 4 ? a.kn : a.v) + krow + 32 * (c & 3);
+                uint4 *dst = reinterpret_cast<uint4 *>(base);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) dst[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+            }
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar[U_D_FREE + db]));
+        }
+    }
+
+    __syncthreads();
+    if (warp == 9) {
+        if (!mbar_wait_cycles(smem_u32(&bar[U_FINAL]), 0, kWaitCycles)) set_dev_err(a.dev_err, MLA_DEVERR_TIMEOUT);
+        fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ===========================================================================
+// 2. attention
+// ===========================================================================
+constexpr int AT_BM = 128;                    // query tokens per CTA
+constexpr int AT_BN = 64;                     // keys per tile
+constexpr int AT_ST = 3;                      // K/V ring stages
+constexpr int AT_NT = 192;
+constexpr int kQSlice = AT_BM * 128;          // 128 tokens x 64 dims bf16: 16 KB
+constexpr int kKSlice = AT_BN * 128;          // 64 keys x 64 dims bf16: 8 KB
+constexpr int kStage = 5 * kKSlice;           // no-RoPE 0, no-RoPE 1, RoPE, V 0, V 1
+constexpr int kOffKV = 3 * kQSlice;
+constexpr int kOffP = kOffKV + AT_ST * kStage;
+constexpr int kPBuf = AT_BM * AT_BN * 2;      // 16 KB
+constexpr int kAtSmem = 1024 + kOffP + 2 * kPBuf;
+constexpr float kRescale = 8.f;               // log2 units
+static_assert(kAtSmem <= 232448 - 256, "shared memory");
+
+enum AtBar { A_Q_FULL = 0, A_KV_FULL, A_KV_EMPTY = A_KV_FULL + AT_ST, A_S_FULL = A_KV_EMPTY + AT_ST,
+             A_S_FREE = A_S_FULL + 2, A_P_FULL = A_S_FREE + 2, A_PV_DONE = A_P_FULL + 2, A_FINAL = A_PV_DONE + 2,
+             A_NBAR };
+
+__global__ void __launch_bounds__(AT_NT, 1)
+    attn_kernel(const MhaArgs a, const int4 *__restrict__ work, const __grid_constant__ CUtensorMap tmap_q,
+                const __grid_constant__ CUtensorMap tmap_kn, const __grid_constant__ CUtensorMap tmap_kr,
+                const __grid_constant__ CUtensorMap tmap_v) {
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    __shared__ uint64_t bar[A_NBAR];
+    __shared__ uint32_t tmem_slot;
+    const uint32_t raw = smem_u32(dsm);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint8_t *sbase = dsm + pad;
+    const uint32_t sbase_a = raw + pad;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // work item: {b, first new token in the sequence, its global index, valid rows},
+    //            {prefix, key-row base, key tiles, -}
+    const int item = blockIdx.x / a.H, h = blockIdx.x % a.H;
+    const int4 w0 = work[2 * item], w1 = work[2 * item + 1];
+    const int i0 = w0.y, n_valid = w0.w, P = w1.x, n_tiles = w1.z;
+    const int64_t t0 = w0.z, kb = w1.y;
+
+    if (tid == 0) {
+        for (int i = 0; i < A_NBAR; ++i) {
+            uint32_t cnt = 1;
+            if ((i >= A_S_FREE && i < A_S_FREE + 2) || (i >= A_P_FULL && i < A_P_FULL + 2)) cnt = 4;
+            mbar_init(smem_u32(&bar[i]), cnt);
+        }
+        mbar_fence_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(&tmem_slot), 256);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_kn);
+        tma_prefetch_desc(&tmap_kr);
+        tma_prefetch_desc(&tmap_v);
+    }
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 4) {
+        // =================== TMA producer ===================
+        if (lane == 0) {
+            mbar_expect_tx(smem_u32(&bar[A_Q_FULL]), 3 * kQSlice);
+            for (int s = 0; s < 3; ++s)
+                tma_load_3d(sbase_a + s * kQSlice, &tmap_q, 64 * s, h, static_cast<int>(t0), smem_u32(&bar[A_Q_FULL]));
+            const int krow0 = static_cast<int>(static_cast<int64_t>(h) * a.R + kb);
+            int t = 0;
+            for (; t < n_tiles; ++t) {
+                const int st = t % AT_ST;
+                if (t >= AT_ST && !wait_bar(&bar[A_KV_EMPTY + st], ((t / AT_ST) - 1) & 1, a.dev_err)) break;
+                const uint32_t sb = sbase_a + kOffKV + st * kStage, fb = smem_u32(&bar[A_KV_FULL + st]);
+                mbar_expect_tx(fb, kStage);
+                tma_load_2d(sb, &tmap_kn, 0, krow0 + AT_BN * t, fb);
+                tma_load_2d(sb + kKSlice, &tmap_kn, 64, krow0 + AT_BN * t, fb);
+                tma_load_2d(sb + 2 * kKSlice, &tmap_kr, 0, static_cast<int>(kb) + AT_BN * t, fb);
+                tma_load_2d(sb + 3 * kKSlice, &tmap_v, 0, krow0 + AT_BN * t, fb);
+                tma_load_2d(sb + 4 * kKSlice, &tmap_v, 64, krow0 + AT_BN * t, fb);
+            }
+            // drain: the query tile and the last load of every stage have landed
+            if (!mbar_wait_cycles(smem_u32(&bar[A_Q_FULL]), 0, kWaitCycles)) set_dev_err(a.dev_err, MLA_DEVERR_TIMEOUT);
+            for (int j = (t > AT_ST ? t - AT_ST : 0); j < t; ++j)
+                if (!mbar_wait_cycles(smem_u32(&bar[A_KV_FULL + j % AT_ST]), (j / AT_ST) & 1, kWaitCycles))
+                    set_dev_err(a.dev_err, MLA_DEVERR_TIMEOUT);
+        }
+    } else if (warp == 5) {
+        // =================== MMA issuer: QK(t+1) before PV(t) ===================
+        if (lane == 0) {
+            const uint32_t id_qk = idesc_f16(AT_BM, AT_BN, true, true, false, false);
+            const uint32_t id_pv = idesc_f16(AT_BM, 128, true, true, false, true);
+            const uint64_t dq0 = sdesc(sbase_a, 16, 1024, kSw128);
+            const uint64_t dk0 = sdesc(sbase_a + kOffKV, 16, 1024, kSw128);
+            const uint64_t dv0 = sdesc(sbase_a + kOffKV + 3 * kKSlice, kKSlice, 1024, kSw128);
+            const uint64_t dp0 = sdesc(sbase_a + kOffP, 128, 1024, kSwNone);
+            auto qk = [&](int t) -> bool {
+                const int st = t % AT_ST, sb = t & 1;
+                if (!wait_bar(&bar[A_KV_FULL + st], (t / AT_ST) & 1, a.dev_err)) return false;
+                if (t >= 2 && !wait_bar(&bar[A_S_FREE + sb], ((t >> 1) - 1) & 1, a.dev_err)) return false;
+                fence_after_sync();
+                const uint32_t d = tmem + static_cast<uint32_t>(AT_BN * sb);
+#pragma unroll
+                for (int s = 0; s < 3; ++s) {
+                    const uint64_t da = dq0 + static_cast<uint64_t>((s * kQSlice) >> 4);
+                    const uint64_t db = dk0 + static_cast<uint64_t>((st * kStage + s * kKSlice) >> 4);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) mma_f16_ss_w(d, da + 2 * ks, db + 2 * ks, id_qk, (s | ks) ? 1u : 0u, 1u);
+                }
+                mma_commit(smem_u32(&bar[A_S_FULL + sb]));
+                return true;
+            };
+            auto pv = [&](int t) -> bool {
+                const int st = t % AT_ST, pb = t & 1;
+                if (!wait_bar(&bar[A_P_FULL + pb], (t >> 1) & 1, a.dev_err)) return false;
+                fence_after_sync();
+                const uint64_t da = dp0 + static_cast<uint64_t>((pb * kPBuf) >> 4);
+                const uint64_t dv = dv0 + static_cast<uint64_t>((st * kStage) >> 4);
+#pragma unroll
+                for (int ks = 0; ks < AT_BN / 16; ++ks)
+                    mma_f16_ss_w(tmem + 128u, da + 16 * ks, dv + 128 * ks, id_pv, (t | ks) ? 1u : 0u, 1u);
+                mma_commit(smem_u32(&bar[A_KV_EMPTY + st]));
+                mma_commit(smem_u32(&bar[A_PV_DONE + pb]));
+                return true;
+            };
+            bool ok = n_tiles > 0 && wait_bar(&bar[A_Q_FULL], 0, a.dev_err);
+            if (ok) ok = qk(0);
+            for (int t = 0; t < n_tiles && ok; ++t) {
+                if (t + 1 < n_tiles && !(ok = qk(t + 1))) break;
+                ok = pv(t);
+            }
+            mma_commit(smem_u32(&bar[A_FINAL]));
+        }
+    } else {
+        // =================== softmax + epilogue: thread = query row ===================
+        const int r = 32 * warp + lane;
+        const int64_t pos = static_cast<int64_t>(P) + i0 + r;      // the row's position in its sequence
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * warp) << 16;
+        const float scale = a.sm_scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        uint8_t *prow = sbase + kOffP + (r >> 3) * 1024 + (r & 7) * 16;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int sb = t & 1;
+            ok = __all_sync(0xffffffffu, wait_bar(&bar[A_S_FULL + sb], (t >> 1) & 1, a.dev_err));
+            if (!ok) break;
+            fence_after_sync();
+            uint32_t sv[64];
+            tmem_ld32(tmem + lane_addr + static_cast<uint32_t>(AT_BN * sb), *reinterpret_cast<uint32_t(*)[32]>(sv));
+            tmem_ld32(tmem + lane_addr + static_cast<uint32_t>(AT_BN * sb + 32),
+                      *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+            tmem_ld_wait();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar[A_S_FREE + sb]));
+            // logits in log2 units; keys past the row's position are masked
+            const int64_t k0 = static_cast<int64_t>(AT_BN) * t;
+            float u[64];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                u[j] = (k0 + j <= pos) ? __uint_as_float(sv[j]) * scale : -INFINITY;
+                mx = fmaxf(mx, u[j]);
+            }
+            if (t == 0) {
+                m = mx;
+            } else {
+                const bool need = mx > m + kRescale;
+                if (__any_sync(0xffffffffu, need)) {
+                    // O is rescaled in TMEM once PV(t-1) has finished with it
+                    ok = __all_sync(0xffffffffu, wait_bar(&bar[A_PV_DONE + ((t - 1) & 1)], ((t - 1) >> 1) & 1, a.dev_err));
+                    if (!ok) break;
+                    fence_after_sync();
+                    const float f = need ? fast_exp2(m - mx) : 1.f;
+                    if (need) {
+                        l *= f;
+                        m = mx;
+                    }
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tmem + lane_addr + 128u + 32u * c, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+                        tmem_st32(tmem + lane_addr + 128u + 32u * c, o);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            // P = 2^(u - m): fp32 into l, bf16 into the P buffer of this tile
+            uint32_t pw[32];
+            float ls = 0.f;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const float p0 = fast_exp2(u[2 * k] - m), p1 = fast_exp2(u[2 * k + 1] - m);
+                ls += p0 + p1;
+                pw[k] = pack_bf162(p0, p1);
+            }
+            l += ls;
+            if (t >= 2) {       // PV(t-2) has read the buffer
+                ok = __all_sync(0xffffffffu, wait_bar(&bar[A_PV_DONE + sb], ((t >> 1) - 1) & 1, a.dev_err));
+                if (!ok) break;
+            }
+            uint8_t *pdst = prow + sb * kPBuf;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4 *>(pdst + c * 128) = make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+            fence_proxy_async();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar[A_P_FULL + sb]));
+        }
+        // ----- epilogue -----
+        if (ok && n_tiles > 0) {
+            const int tl = n_tiles - 1;
+            ok = __all_sync(0xffffffffu, wait_bar(&bar[A_PV_DONE + (tl & 1)], (tl >> 1) & 1, a.dev_err));
+        }
+        if (ok && n_tiles > 0) {
+            fence_after_sync();
+            const float inv = 1.f / l;
+            const bool live = r < n_valid;
+            __nv_bfloat16 *orow = a.out + ((t0 + r) * a.H + h) * kDvh;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_addr + 128u + 32u * c, o);
+                tmem_ld_wait();
+                if (live) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        w[k] = pack_bf162(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                }
+            }
+            if (live && a.lse) a.lse[(t0 + r) * a.H + h] = (m + log2f(l)) * kLn2;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 5) {
+        if (!mbar_wait_cycles(smem_u32(&bar[A_FINAL]), 0, kWaitCycles)) set_dev_err(a.dev_err, MLA_DEVERR_TIMEOUT);
+        fence_after_sync();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+}  // namespace mha
+
+cudaError_t launch_mha_up(const MhaArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_w, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(mha::up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mha::kUpSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t n_cta = static_cast<int64_t>(n_work) * (a.H / a.up_heads);
+    if (n_cta > 0) mha::up_kernel<<<static_cast<unsigned>(n_cta), mha::UP_NT, mha::kUpSmem, st>>>(a, work, tmap_w);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mha_attn(const MhaArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_q,
+                            const CUtensorMap &tmap_kn, const CUtensorMap &tmap_kr, const CUtensorMap &tmap_v,
+                            cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(mha::attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mha::kAtSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t n_cta = static_cast<int64_t>(n_work) * a.H;
+    if (n_cta > 0)
+        mha::attn_kernel<<<static_cast<unsigned>(n_cta), mha::AT_NT, mha::kAtSmem, st>>>(a, work, tmap_q, tmap_kn,
+                                                                                      tmap_kr, tmap_v);
+    return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -191,20 +191,38 @@ size_t indexer_groups(const mla_seqs_t *s) {
 // box_rows x 128-byte boxes with the 128-byte swizzle (bytes past the row end
 // read as zero). The encoder is fetched from the driver once; no link against
 // the driver library is needed.
-bool encode_u8_rows(CUtensorMap *map, const void *base, uint64_t width, uint64_t rows, uint32_t box_rows) {
-    using Encode = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-    static Encode encode = nullptr;
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiled tiled_encoder() {
+    static EncodeTiled encode = nullptr;
     if (!encode) {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q{};
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
                 cudaSuccess ||
             q != cudaDriverEntryPointSuccess || !fn)
-            return false;
-        encode = reinterpret_cast<Encode>(fn);
+            return nullptr;
+        encode = reinterpret_cast<EncodeTiled>(fn);
     }
+    return encode;
+}
+
+// Tensor map over a bf16 tensor of rank 2 or 3 (dims innermost first, byte
+// strides of the outer dims), 128-byte swizzle, zero fill past the edges.
+bool encode_bf16(CUtensorMap *map, const void *base, cuuint32_t rank, const cuuint64_t *dims,
+                 const cuuint64_t *strides, const cuuint32_t *box) {
+    const EncodeTiled encode = tiled_encoder();
+    if (!encode) return false;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_u8_rows(CUtensorMap *map, const void *base, uint64_t width, uint64_t rows, uint32_t box_rows) {
+    const EncodeTiled encode = tiled_encoder();
+    if (!encode) return false;
     const cuuint64_t dims[2] = {width, rows};
     const cuuint64_t strides[1] = {width};
     const cuuint32_t box[2] = {128, box_rows};
@@ -215,6 +233,51 @@ bool encode_u8_rows(CUtensorMap *map, const void *base, uint64_t width, uint64_t
 }
 bool encode_rows128(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
     return encode_u8_rows(map, base, 128, rows, box_rows);
+}
+
+// The non-absorbed path's plan: key rows (each sequence with new tokens gets
+// its context padded to 128 rows), the up-projection items (one per 128 rows)
+// and the attention items (one per 128 new tokens, two int4 each, longest
+// first), and the workspace layout.
+struct MhaPlan {
+    std::vector<int4> up, at;
+    int64_t R = 0;
+    size_t off_at = 0, off_up = 0, off_kn = 0, off_v = 0, off_kr = 0, bytes = 0;
+};
+MhaPlan mha_plan(const mla_seqs_t *s, int32_t H) {
+    MhaPlan p;
+    struct At {
+        int4 a, b;
+    };
+    std::vector<At> at;
+    for (int b = 0; b < s->batch; ++b) {
+        const int64_t c0 = s->cu_seqlens_q_host[b], q = s->cu_seqlens_q_host[b + 1] - c0;
+        if (q <= 0) continue;
+        const int64_t P = s->prefix_lens_host[b], ctx = P + q;
+        const int64_t kb = p.R;
+        for (int64_t y = 0; y < ctx; y += 128)
+            p.up.push_back(make_int4(b, static_cast<int>(y), static_cast<int>(kb + y), static_cast<int>(ctx)));
+        for (int64_t i0 = 0; i0 < q; i0 += 128) {
+            const int64_t nv = std::min<int64_t>(128, q - i0);
+            const int64_t n_tiles = (P + i0 + nv + 63) / 64;
+            at.push_back({make_int4(b, static_cast<int>(i0), static_cast<int>(c0 + i0), static_cast<int>(nv)),
+                          make_int4(static_cast<int>(P), static_cast<int>(kb), static_cast<int>(n_tiles), 0)});
+        }
+        p.R += (ctx + 127) / 128 * 128;
+    }
+    std::stable_sort(at.begin(), at.end(), [](const At &x, const At &y) { return x.b.z > y.b.z; });
+    for (const At &x : at) {
+        p.at.push_back(x.a);
+        p.at.push_back(x.b);
+    }
+    p.off_at = 0;
+    p.off_up = round_up(p.at.size() * sizeof(int4), kWsAlign);
+    p.off_kn = p.off_up + round_up(p.up.size() * sizeof(int4), kWsAlign);
+    const size_t kv_bytes = round_up(static_cast<size_t>(H) * static_cast<size_t>(p.R) * 256, kWsAlign);
+    p.off_v = p.off_kn + kv_bytes;
+    p.off_kr = p.off_v + kv_bytes;
+    p.bytes = p.off_kr + round_up(static_cast<size_t>(p.R) * 128, kWsAlign);
+    return p;
 }
 
 mla::AttnArgs attn_args(const mla_seqs_t *s, const void *q, int32_t H, const uint8_t *kv, const float *kv_scale,
@@ -270,6 +333,9 @@ size_t mla_workspace_size(mla_op_t op, const mla_seqs_t *seqs, int32_t num_heads
         case MLA_OP_DENSE_HOST:
             if (!heads_ok(num_heads)) return 0;
             return round_up(dense_host_items_bound(seqs, num_heads) * sizeof(int4), kWsAlign);
+        case MLA_OP_MHA:
+            if (!heads_ok(num_heads)) return 0;
+            return mha_plan(seqs, num_heads).bytes;
     }
     return 0;
 }
@@ -671,6 +737,71 @@ mla_status_t mla_prefill_dense_ds(const mla_seqs_t *seqs, const void *q_bf16, in
     mla::AttnArgs a = attn_args(seqs, q_bf16, num_heads, kv_ds, nullptr, sm_scale, out_bf16, lse, dev_err);
     e = mla::launch_dense_ds(a, static_cast<const int4 *>(workspace), static_cast<int>(work.size()), stream);
     if (e != cudaSuccess) return cuda_fail(e, "dense launch");
+    return MLA_OK;
+}
+
+mla_status_t mla_prefill_mha(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads, const void *w_ukv_bf16,
+                             const uint8_t *kv_e4m3, const float *kv_scale, float sm_scale, void *out_bf16,
+                             float *lse, void *workspace, size_t workspace_bytes, int32_t *dev_err,
+                             cudaStream_t stream) {
+    g_err.clear();
+    mla_status_t st = check_seqs(seqs);
+    if (st != MLA_OK) return st;
+    if (!heads_ok(num_heads)) return fail(MLA_ERR_UNSUPPORTED, "num_heads must be 16, 32, 64 or 128 (got %d)", num_heads);
+    if ((st = check_attn_ptrs(q_bf16, kv_e4m3, kv_scale, out_bf16, lse, sm_scale)) != MLA_OK) return st;
+    if (!w_ukv_bf16 || !aligned(w_ukv_bf16, 16)) return fail(MLA_ERR_INVALID_ARG, "w_ukv must be set and 16-byte aligned");
+    const MhaPlan p = mha_plan(seqs, num_heads);
+    if (p.at.empty()) return MLA_OK;
+    if (!workspace || workspace_bytes < p.bytes || !aligned(workspace, kWsAlign))
+        return fail(MLA_ERR_WORKSPACE, "mha needs %zu workspace bytes (256-byte aligned), got %zu", p.bytes,
+                    workspace ? workspace_bytes : 0);
+    const int64_t tq = seqs->cu_seqlens_q_host[seqs->batch];
+    if (static_cast<int64_t>(num_heads) * p.R > INT32_MAX || tq > INT32_MAX ||
+        static_cast<int64_t>(p.at.size() / 2) * num_heads > INT32_MAX)
+        return fail(MLA_ERR_UNSUPPORTED, "batch too large for the non-absorbed path");
+    char *ws = static_cast<char *>(workspace);
+    std::vector<int4> lists(p.off_kn / sizeof(int4), make_int4(0, 0, 0, 0));
+    std::copy(p.at.begin(), p.at.end(), lists.begin() + p.off_at / sizeof(int4));
+    std::copy(p.up.begin(), p.up.end(), lists.begin() + p.off_up / sizeof(int4));
+    cudaError_t e = cudaMemcpyAsync(ws, lists.data(), p.off_kn, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "schedule upload");
+
+    mla::MhaArgs a{};
+    a.q = static_cast<const __nv_bfloat16 *>(q_bf16);
+    a.kv = kv_e4m3;
+    a.kv_scale = kv_scale;
+    a.block_table = seqs->block_table;
+    a.max_blocks = seqs->max_blocks_per_seq;
+    a.num_blocks = seqs->num_blocks;
+    a.kn = reinterpret_cast<__nv_bfloat16 *>(ws + p.off_kn);
+    a.v = reinterpret_cast<__nv_bfloat16 *>(ws + p.off_v);
+    a.kr = reinterpret_cast<__nv_bfloat16 *>(ws + p.off_kr);
+    a.R = p.R;
+    a.out = static_cast<__nv_bfloat16 *>(out_bf16);
+    a.lse = lse;
+    a.H = num_heads;
+    a.up_heads = std::min(num_heads, 8);
+    a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+    a.dev_err = dev_err;
+
+    const cuuint64_t H = static_cast<cuuint64_t>(num_heads), R = static_cast<cuuint64_t>(p.R);
+    CUtensorMap tw, tq_map, tkn, tkr, tv;
+    const cuuint64_t w_dims[2] = {512, H * 256}, w_str[1] = {1024};
+    const cuuint32_t w_box[2] = {64, 256};
+    const cuuint64_t q_dims[3] = {192, H, static_cast<cuuint64_t>(tq)}, q_str[2] = {384, H * 384};
+    const cuuint32_t q_box[3] = {64, 1, 128};
+    const cuuint64_t kv_dims[2] = {128, H * R}, kv_str[1] = {256};
+    const cuuint64_t kr_dims[2] = {64, R}, kr_str[1] = {128};
+    const cuuint32_t k_box[2] = {64, 64};
+    if (!encode_bf16(&tw, w_ukv_bf16, 2, w_dims, w_str, w_box) || !encode_bf16(&tq_map, q_bf16, 3, q_dims, q_str, q_box) ||
+        !encode_bf16(&tkn, a.kn, 2, kv_dims, kv_str, k_box) || !encode_bf16(&tv, a.v, 2, kv_dims, kv_str, k_box) ||
+        !encode_bf16(&tkr, a.kr, 2, kr_dims, kr_str, k_box))
+        return fail(MLA_ERR_CUDA, "tensor map encoding failed");
+    e = mla::launch_mha_up(a, reinterpret_cast<const int4 *>(ws + p.off_up), static_cast<int>(p.up.size()), tw, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "mha up-projection launch");
+    e = mla::launch_mha_attn(a, reinterpret_cast<const int4 *>(ws + p.off_at), static_cast<int>(p.at.size() / 2), tq_map,
+                             tkn, tkr, tv, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "mha attention launch");
     return MLA_OK;
 }
 

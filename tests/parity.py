@@ -194,7 +194,7 @@ def sample_rows(cu_seqlens, seed: int, n_uniform: int = None, edge: int = EDGE_R
 # full-size checks on the GPU in plain PyTorch (an independent calculation,
 # used where the fp64 oracle cannot cover every row in reasonable time)
 # ---------------------------------------------------------------------------
-def check_attention_torch(gpu_out, ref_out, gpu_lse=None, ref_lse=None, what=""):
+def check_attention_torch(gpu_out, ref_out, gpu_lse=None, ref_lse=None, what="", lse_extra=None):
     """check_attention on the GPU against an fp32 reference (torch tensors
     [..., 512]); the reference's own error (~1e-6 of a row) is far below the
     bounds. Returns (own max, own mean, raw max, raw mean)."""
@@ -214,9 +214,11 @@ def check_attention_torch(gpu_out, ref_out, gpu_lse=None, ref_lse=None, what="")
            f"mean {vals[3]:.3e}; bf16 floor max {vals[4]:.3e} mean {vals[5]:.3e}")
     assert vals[0] <= TOL_MAX and vals[1] <= TOL_MEAN, msg
     assert vals[2] <= vals[4] + FLOOR_MARGIN * TOL_MAX and vals[3] <= vals[5] + FLOOR_MARGIN * TOL_MEAN, msg
+    print(msg)
     if gpu_lse is not None:
-        dl = float((gpu_lse.double() - ref_lse.double()).abs().max())
-        assert dl <= TOL_LSE_ABS, f"{what}: lse max abs err {dl:.3e}"
+        dl = (gpu_lse.double() - ref_lse.double()).abs()
+        tol = TOL_LSE_ABS + (0.0 if lse_extra is None else lse_extra.double())
+        assert bool((dl <= tol).all()), f"{what}: lse max abs err {float(dl.max()):.3e}"
     return vals[:4]
 
 
@@ -363,5 +365,63 @@ def sparse_reference_ds_torch(ps, q, kv_ds, sm_scale, idx, block=64):
                 out[t0:t1] = torch.einsum("ths,tsd->thd", p, K[..., :512])
                 lse[t0:t1] = l
         return out, lse
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+# ---------------------------------------------------------------------------
+# the non-absorbed (MHA) path
+# ---------------------------------------------------------------------------
+BF16_UNIT_ROUNDOFF = 2.0 ** -9
+
+
+def mha_reference_torch(ps, q, w, kv, ks, sm_scale, toks=None, q_block=256):
+    """The non-absorbed path in plain PyTorch, fp32 (TF32 off), on the GPU, for
+    every new token (or the global tokens `toks`): c_s = ks_s * dec(kv_s),
+    k = [W_UK c ; r], v = W_UV c per head, causal softmax. Also returns the
+    per-row bound on the move of the log-sum-exp when the kernel rounds each
+    key to bf16: u * sm_scale * max_s sum_d |q_d| |k_s[d]| (u = 2^-9).
+    q: bf16 [Tq, H, 192]; w: bf16 [H, 256, 512]. Returns (out [n, H, 128], lse
+    [n, H], lse_bound [n, H]) in token order."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        H = q.shape[1]
+        wf = w.float()
+        kvf, ksf = kv.view(-1, 576), ks.view(-1)
+        cu = [int(x) for x in ps.cu_seqlens_q]
+        want = torch.arange(cu[-1], device=q.device) if toks is None else torch.as_tensor(toks, device=q.device)
+        out = torch.zeros((want.numel(), H, 128), dtype=torch.float32, device=q.device)
+        lse = torch.zeros((want.numel(), H), dtype=torch.float32, device=q.device)
+        bnd = torch.zeros((want.numel(), H), dtype=torch.float64, device=q.device)
+        for b in range(ps.batch):
+            sel = ((want >= cu[b]) & (want < cu[b + 1])).nonzero().flatten()
+            if sel.numel() == 0:
+                continue
+            P = int(ps.prefix_lens[b])
+            tq = want[sel]
+            ctx = P + int(tq.max()) - cu[b] + 1
+            rows = _cache_rows(ps, b, torch.arange(ctx, device=q.device))
+            C = kvf[rows].view(torch.float8_e4m3fn).float() * ksf[rows][:, None]          # [ctx, 576]
+            Kn = torch.einsum("sd,hid->hsi", C[:, :512], wf[:, :128, :])                  # [H, ctx, 128]
+            V = torch.einsum("sd,hid->hsi", C[:, :512], wf[:, 128:, :])
+            K = torch.cat([Kn, C[None, :, 512:].expand(H, ctx, 64)], dim=2)              # [H, ctx, 192]
+            for j0 in range(0, sel.numel(), q_block):
+                js = sel[j0:j0 + q_block]
+                t = want[js]
+                pos = P + (t - cu[b])
+                qb = q[t].float().permute(1, 0, 2)                                      # [H, n, 192]
+                lg = torch.einsum("hnd,hsd->hns", qb, K) * sm_scale
+                mask = torch.arange(ctx, device=q.device)[None, :] > pos[:, None]       # [n, ctx]
+                lg = lg.masked_fill(mask[None], float("-inf"))
+                l = torch.logsumexp(lg, dim=-1)                                         # [H, n]
+                p = torch.exp(lg - l[..., None])
+                out[js] = torch.einsum("hns,hsi->nhi", p, V)
+                lse[js] = l.t()
+                mag = torch.einsum("hnd,hsd->hns", qb.abs().double(), K.abs().double())
+                mag = mag.masked_fill(mask[None], 0.0)
+                bnd[js] = (BF16_UNIT_ROUNDOFF * sm_scale * mag.amax(dim=-1)).t()
+        return out, lse, bnd
     finally:
         torch.backends.cuda.matmul.allow_tf32 = prev

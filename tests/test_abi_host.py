@@ -216,3 +216,31 @@ def test_merge_rejects_bad_arguments(lib):
     assert lib.mla_merge_attn(2, arr(0x100000, 0), lses, 10, FAKE, None, None) == B.MLA_ERR_INVALID_ARG
     assert lib.mla_merge_attn(2, two, lses, 10, FAKE_MIS, None, None) == B.MLA_ERR_INVALID_ARG
     assert lib.mla_merge_attn(2, two, lses, 10, FAKE, ctypes.c_void_p(0x500002), None) == B.MLA_ERR_INVALID_ARG
+
+
+def test_mha_rejects_bad_arguments_and_sizes_its_workspace(lib):
+    s = HostSeqs([300, 77], [0, 40])
+
+    def mha(seqs=s, H=64, q=FAKE, w=FAKE, out=FAKE, ws=None, wsb=0, scale=0.07):
+        return lib.mla_prefill_mha(ctypes.byref(seqs.c) if seqs is not None else None, q, H, w, FAKE, FAKE, scale,
+                                   out, None, ws, wsb, None, None)
+
+    assert mha(seqs=None) == B.MLA_ERR_INVALID_ARG
+    assert mha(H=48) == B.MLA_ERR_UNSUPPORTED
+    assert mha(q=FAKE_MIS) == B.MLA_ERR_INVALID_ARG
+    assert mha(w=None) == B.MLA_ERR_INVALID_ARG
+    assert mha(w=FAKE_MIS) == B.MLA_ERR_INVALID_ARG
+    assert mha(scale=float("inf")) == B.MLA_ERR_INVALID_ARG
+    assert mha() == B.MLA_ERR_WORKSPACE
+    # work lists (two 16-byte items per 128 new tokens, one per 128 context rows),
+    # then k and v (256 bytes per row and head) and the RoPE dims (128 bytes per row)
+    H = 64
+    rows = 384 + 128                      # contexts 300 and 117, each padded to 128
+    at = (3 + 1) * 2 * 16
+    up = (3 + 1) * 16
+    rnd = lambda x: -(-x // 256) * 256
+    want = rnd(at) + rnd(up) + 2 * rnd(H * rows * 256) + rnd(rows * 128)
+    assert lib.mla_workspace_size(B.MLA_OP_MHA, ctypes.byref(s.c), H, 0) == want
+    assert mha(ws=FAKE, wsb=want - 1) == B.MLA_ERR_WORKSPACE
+    assert mha(ws=ctypes.c_void_p(0x100010), wsb=want) == B.MLA_ERR_WORKSPACE      # not 256-byte aligned
+    assert mha(seqs=HostSeqs([0, 0], [5, 0])) == B.MLA_OK                         # no new tokens: no launch
