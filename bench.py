@@ -714,6 +714,67 @@ def measure_ds_layout(name, dev, steps, warmup):
     return obj
 
 
+def measure_mha(name, dev, steps, warmup):
+    """The non-absorbed (MHA) path on a batch of short prompts (mla_prefill_mha:
+    up-projection of every context row's keys and values, then causal attention
+    per head), beside the absorbed dense path on the same prompts. FLOPs of the
+    MHA path: 2 * 512 * 256 * heads per context row (up-projection) plus
+    2 * (192 + 128) per visible (query, key, head) triple (attention)."""
+    import torch
+    from mla_prefill_attention_gb300 import (MLA_OP_DENSE, MLA_OP_MHA, Seqs, inputs as I, mla_prefill_dense,
+                                             mla_prefill_mha, mla_workspace_size)
+    from mla_prefill_attention_gb300 import flops as F
+    w = I.WORKLOADS[name]
+    ps = w.seqs()
+    seqs = Seqs.from_paged(ps, device=dev)
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    q = bf(I.gen_q_mha(w.seed, ps.total_q, w.heads))
+    wu = bf(I.gen_w_ukv(w.seed, w.heads))
+    kv, ks = [torch.from_numpy(x).to(dev) for x in I.gen_latent_cache(w.seed, ps)]
+    out = torch.empty((ps.total_q, w.heads, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((ps.total_q, w.heads), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(256, mla_workspace_size(MLA_OP_MHA, seqs, w.heads)), dtype=torch.uint8, device=dev)
+    qa = bf(I.gen_q_bf16(w.seed, ps.total_q, w.heads))
+    outa = torch.empty((ps.total_q, w.heads, 512), dtype=torch.bfloat16, device=dev)
+    lsea = torch.empty((ps.total_q, w.heads), dtype=torch.float32, device=dev)
+    wsa = torch.empty(max(16, mla_workspace_size(MLA_OP_DENSE, seqs, w.heads)), dtype=torch.uint8, device=dev)
+
+    def timed(call):
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        ev = []
+        for _ in range(steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            call()
+            b.record()
+            ev.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    ms = timed(lambda: mla_prefill_mha(seqs, q, wu, kv, ks, w.sm_scale, out=out, lse=lse, workspace=ws))
+    ms_abs = timed(lambda: mla_prefill_dense(seqs, qa, kv, ks, w.sm_scale, out=outa, lse=lsea, workspace=wsa))
+    pairs = sum((p + n) * (p + n + 1) // 2 - p * (p + 1) // 2 for n, p in zip(w.q_lens, w.prefix_lens))
+    ctx_rows = sum(n + p for n, p in zip(w.q_lens, w.prefix_lens))
+    flops = 2.0 * 512 * 256 * w.heads * ctx_rows + 2.0 * (192 + 128) * w.heads * pairs
+    pk, src = peaks()
+    bf16 = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
+    tf = flops / (ms / 1000.0) / 1e12
+    abs_tf = F.dense_flops(w.q_lens, w.prefix_lens, w.heads) / (ms_abs / 1000.0) / 1e12
+    obj = {"workload": name, "q_lens": w.q_lens, "heads": w.heads, "steps": steps, "warmup": warmup,
+           "ms_per_call": ms, "value": ps.total_q / (ms / 1000.0), "unit": "tok/s", "tflops": tf,
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16, "unit": "TFLOP/s", "frac": tf / bf16,
+                        "peak_source": f"{src} bf16 sustained (kind::f16 MMAs)",
+                        "kernel": "mha up_kernel (M=128 rows x N=256, K=512) + attn_kernel (M=128 tokens, 64-key "
+                                  "tiles, d_qk 192, d_v 128), bf16 tcgen05"},
+           "absorbed_dense_same_prompts": {"ms_per_call": ms_abs, "value": ps.total_q / (ms_abs / 1000.0),
+                                           "attention_tflops": abs_tf}}
+    del q, wu, kv, ks, out, lse, ws, qa, outa, lsea, wsa
+    torch.cuda.empty_cache()
+    return obj
+
+
 def cpu_info():
     """CPU model and the cores this process may run on (for the CPU baseline)."""
     model = None
@@ -874,6 +935,7 @@ def main():
             extras[name] = measure_workload(name, dev, k, max(3, min(args.warmup, 3)))
         for name in ("dense32k", "sparse64k"):
             extras[name + "_656B"] = measure_ds_layout(name, dev, min(args.steps, 5), 3)
+        extras["mha_short"] = measure_mha("mha_short", dev, min(args.steps, 10), 3)
         line["workloads"] = extras
     if world > 1:
         dist.destroy_process_group()

@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -55,9 +56,9 @@ struct MhaArgs {
     const float *kv_scale;       // [num_blocks, 256]
     const int32_t *block_table;  // [batch, max_blocks]
     int32_t max_blocks, num_blocks;
-    __nv_bfloat16 *kn;           // [H, R, 128] up-projected no-RoPE keys
-    __nv_bfloat16 *v;            // [H, R, 128] up-projected values
-    __nv_bfloat16 *kr;           // [R, 64] RoPE dims of the keys
+    __half *kn;                  // [H, R, 128] up-projected no-RoPE keys (f16)
+    __half *v;                   // [H, R, 128] up-projected values (f16)
+    __half *kr;                  // [R, 64] RoPE dims of the keys (f16)
     int64_t R;                   // key rows: each sequence's context padded to 128
     __nv_bfloat16 *out;          // [Tq, H, 128]
     float *lse;                  // [Tq, H] or null
@@ -73,8 +74,8 @@ cudaError_t launch_mha_up(const MhaArgs &a, const int4 *work, int n_work, const 
 // Attention: work item = two int4, {sequence, first new token in it, that
 // token's global index, valid rows <= 128} and {prefix, key-row base, key tiles
 // of 64, 0}; one CTA per item and head. tmap_q: q as [Tq][H][192] bf16, boxes
-// of 64 dims x 1 head x 128 tokens; tmap_kn / tmap_v: [H*R rows][128], 64 x 64
-// boxes; tmap_kr: [R][64], 64 x 64 boxes; all with the 128-byte swizzle.
+// of 64 dims x 1 head x 128 tokens; tmap_kn / tmap_v: f16 [H*R rows][128], 64 x
+// 64 boxes; tmap_kr: f16 [R][64], 64 x 64 boxes; all with the 128-byte swizzle.
 cudaError_t launch_mha_attn(const MhaArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_q,
                             const CUtensorMap &tmap_kn, const CUtensorMap &tmap_kr, const CUtensorMap &tmap_v,
                             cudaStream_t st);

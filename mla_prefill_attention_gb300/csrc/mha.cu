@@ -1,4 +1,4 @@
-// Non-absorbed (MHA) MLA prefill for short prompts (tcgen05 kind::f16, bf16).
+// Non-absorbed (MHA) MLA prefill for short prompts (tcgen05 kind::f16).
 //
 // GLM-5.3-Optimierungen Teil 2, section Ausprobieren: without the
 // sparse_mla_force_mqa flag, prefill batches whose prompts fit within the
@@ -18,17 +18,22 @@
 //    them by each head's [256 x 512] slice of w_ukv (TMA, 64-dim boxes through
 //    a 3-stage ring): D[row][n] = sum_d dec(c)[row][d] W[h][n][d], M = 128
 //    rows, N = 256 (k then v), K = 512, into one of two TMEM accumulators;
-//    four epilogue warps (thread = row) scale by sigma_row and write bf16 k and
+//    four epilogue warps (thread = row) scale by sigma_row and write f16 k and
 //    v rows head-major, [H][R][128]. The first head group also writes the
-//    RoPE dims, bf16(sigma * dec(c)), as [R][64]. Rows past the context are
-//    written as zeros (each sequence's rows are padded to 128).
+//    RoPE dims, f16(sigma * dec(c)), as [R][64]. Rows past the context are
+//    written as zeros (each sequence's rows are padded to 128). f16 keeps 11
+//    significant bits of each up-projected value (bf16 would keep 8: its
+//    rounding of the keys alone moved logits by ~1e-3 and outputs by up to
+//    2.5e-2 of a row's RMS); the values must stay inside the f16 range.
 //
-// 2. Attention, one CTA per 128 new tokens of a sequence and one head:
+// 2. Attention, one CTA per 128 new tokens of a sequence and one head; the
+//    bf16 query tile is converted to f16 in shared memory once (values below
+//    2^-14 lose bits, so a query must lie inside the f16 range):
 //      S  = Q K^T        M = 128 tokens, N = 64 keys, K = 192 (3 x 64-dim
 //                        slices: two no-RoPE, one RoPE); S in one of two TMEM
 //                        buffers so QK(t+1) runs during the softmax of tile t
 //      P  = 2^(S*sm_scale*log2e - m)   in registers (a thread per query row),
-//                        rounded to bf16 into shared memory
+//                        rounded to f16 into shared memory
 //      O += P V          M = 128, N = 128 value dims, K = 64 keys (O in TMEM)
 //    m is the row's running reference maximum; O and l are rescaled only when
 //    a tile raises it by more than 8 (log2 units), so P stays below 2^8. l
@@ -157,7 +162,7 @@ __global__ void __launch_bounds__(UP_NT, 1)
                         const uint16_t two = static_cast<uint16_t>(wv[k] >> (16 * e));
                         const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
                         const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
-                        o[8 * q + 2 * k + e] = pack_bf162(s * f.x, s * f.y);
+                        o[8 * q + 2 * k + e] = pack_half2(s * f.x, s * f.y);
                     }
             }
             uint4 *dst = reinterpret_cast<uint4 *>(a.kr + (row0 + r) * kDr + 32 * half);
@@ -235,8 +240,8 @@ __global__ void __launch_bounds__(UP_NT, 1)
                 uint32_t o[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k)
-                    o[k] = pack_bf162(s * __uint_as_float(v[2 * k]), s * __uint_as_float(v[2 * k + 1]));
-                __nv_bfloat16 *base = (c < 4 ? a.kn : a.v) + krow + 32 * (c & 3);
+                    o[k] = pack_half2(s * __uint_as_float(v[2 * k]), s * __uint_as_float(v[2 * k + 1]));
+                __half *base = (c < 4 ? a.kn : a.v) + krow + 32 * (c & 3);
                 uint4 *dst = reinterpret_cast<uint4 *>(base);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) dst[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
@@ -272,7 +277,7 @@ constexpr int kAtSmem = 1024 + kOffP + 2 * kPBuf;
 constexpr float kRescale = 8.f;               // log2 units
 static_assert(kAtSmem <= 232448 - 256, "shared memory");
 
-enum AtBar { A_Q_FULL = 0, A_KV_FULL, A_KV_EMPTY = A_KV_FULL + AT_ST, A_S_FULL = A_KV_EMPTY + AT_ST,
+enum AtBar { A_Q_FULL = 0, A_Q_F16, A_KV_FULL, A_KV_EMPTY = A_KV_FULL + AT_ST, A_S_FULL = A_KV_EMPTY + AT_ST,
              A_S_FREE = A_S_FULL + 2, A_P_FULL = A_S_FREE + 2, A_PV_DONE = A_P_FULL + 2, A_FINAL = A_PV_DONE + 2,
              A_NBAR };
 
@@ -299,7 +304,7 @@ __global__ void __launch_bounds__(AT_NT, 1)
     if (tid == 0) {
         for (int i = 0; i < A_NBAR; ++i) {
             uint32_t cnt = 1;
-            if ((i >= A_S_FREE && i < A_S_FREE + 2) || (i >= A_P_FULL && i < A_P_FULL + 2)) cnt = 4;
+            if ((i >= A_S_FREE && i < A_S_FREE + 2) || (i >= A_P_FULL && i < A_P_FULL + 2) || i == A_Q_F16) cnt = 4;
             mbar_init(smem_u32(&bar[i]), cnt);
         }
         mbar_fence_init();
@@ -346,8 +351,8 @@ __global__ void __launch_bounds__(AT_NT, 1)
     } else if (warp == 5) {
         // =================== MMA issuer: QK(t+1) before PV(t) ===================
         if (lane == 0) {
-            const uint32_t id_qk = idesc_f16(AT_BM, AT_BN, true, true, false, false);
-            const uint32_t id_pv = idesc_f16(AT_BM, 128, true, true, false, true);
+            const uint32_t id_qk = idesc_f16(AT_BM, AT_BN, false, false, false, false);
+            const uint32_t id_pv = idesc_f16(AT_BM, 128, false, false, false, true);
             const uint64_t dq0 = sdesc(sbase_a, 16, 1024, kSw128);
             const uint64_t dk0 = sdesc(sbase_a + kOffKV, 16, 1024, kSw128);
             const uint64_t dv0 = sdesc(sbase_a + kOffKV + 3 * kKSlice, kKSlice, 1024, kSw128);
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(AT_NT, 1)
                 mma_commit(smem_u32(&bar[A_PV_DONE + pb]));
                 return true;
             };
-            bool ok = n_tiles > 0 && wait_bar(&bar[A_Q_FULL], 0, a.dev_err);
+            bool ok = n_tiles > 0 && wait_bar(&bar[A_Q_F16], 0, a.dev_err);
             if (ok) ok = qk(0);
             for (int t = 0; t < n_tiles && ok; ++t) {
                 if (t + 1 < n_tiles && !(ok = qk(t + 1))) break;
@@ -398,7 +403,30 @@ __global__ void __launch_bounds__(AT_NT, 1)
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         uint8_t *prow = sbase + kOffP + (r >> 3) * 1024 + (r & 7) * 16;
-        for (int t = 0; t < n_tiles; ++t) {
+        // the query row to f16, in place (the swizzle moves whole 16-byte chunks, so
+        // each thread's row stays its own 3 x 128 bytes)
+        ok = n_tiles > 0 && __all_sync(0xffffffffu, wait_bar(&bar[A_Q_FULL], 0, a.dev_err));
+        if (ok) {
+#pragma unroll
+            for (int s = 0; s < 3; ++s) {
+                uint4 *row = reinterpret_cast<uint4 *>(sbase + s * kQSlice + r * 128);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 x = row[c];
+                    uint32_t *wv = reinterpret_cast<uint32_t *>(&x);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wv[k]));
+                        wv[k] = pack_half2(f.x, f.y);
+                    }
+                    row[c] = x;
+                }
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar[A_Q_F16]));
+        }
+        for (int t = 0; t < n_tiles && ok; ++t) {
             const int sb = t & 1;
             ok = __all_sync(0xffffffffu, wait_bar(&bar[A_S_FULL + sb], (t >> 1) & 1, a.dev_err));
             if (!ok) break;
@@ -446,14 +474,14 @@ __global__ void __launch_bounds__(AT_NT, 1)
                     tmem_st_wait();
                 }
             }
-            // P = 2^(u - m): fp32 into l, bf16 into the P buffer of this tile
+            // P = 2^(u - m): fp32 into l, f16 into the P buffer of this tile
             uint32_t pw[32];
             float ls = 0.f;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
                 const float p0 = fast_exp2(u[2 * k] - m), p1 = fast_exp2(u[2 * k + 1] - m);
                 ls += p0 + p1;
-                pw[k] = pack_bf162(p0, p1);
+                pw[k] = pack_half2(p0, p1);
             }
             l += ls;
             if (t >= 2) {       // PV(t-2) has read the buffer

@@ -208,14 +208,14 @@ EncodeTiled tiled_encoder() {
     return encode;
 }
 
-// Tensor map over a bf16 tensor of rank 2 or 3 (dims innermost first, byte
-// strides of the outer dims), 128-byte swizzle, zero fill past the edges.
-bool encode_bf16(CUtensorMap *map, const void *base, cuuint32_t rank, const cuuint64_t *dims,
-                 const cuuint64_t *strides, const cuuint32_t *box) {
+// Tensor map over a 16-bit (bf16 or f16) tensor of rank 2 or 3 (dims innermost
+// first, byte strides of the outer dims), 128-byte swizzle, zero fill past the edges.
+bool encode_16bit(CUtensorMap *map, CUtensorMapDataType type, const void *base, cuuint32_t rank,
+                  const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box) {
     const EncodeTiled encode = tiled_encoder();
     if (!encode) return false;
     const cuuint32_t estr[3] = {1, 1, 1};
-    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides, box, estr,
+    return encode(map, type, rank, const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -773,9 +773,9 @@ mla_status_t mla_prefill_mha(const mla_seqs_t *seqs, const void *q_bf16, int32_t
     a.block_table = seqs->block_table;
     a.max_blocks = seqs->max_blocks_per_seq;
     a.num_blocks = seqs->num_blocks;
-    a.kn = reinterpret_cast<__nv_bfloat16 *>(ws + p.off_kn);
-    a.v = reinterpret_cast<__nv_bfloat16 *>(ws + p.off_v);
-    a.kr = reinterpret_cast<__nv_bfloat16 *>(ws + p.off_kr);
+    a.kn = reinterpret_cast<__half *>(ws + p.off_kn);
+    a.v = reinterpret_cast<__half *>(ws + p.off_v);
+    a.kr = reinterpret_cast<__half *>(ws + p.off_kr);
     a.R = p.R;
     a.out = static_cast<__nv_bfloat16 *>(out_bf16);
     a.lse = lse;
@@ -793,9 +793,12 @@ mla_status_t mla_prefill_mha(const mla_seqs_t *seqs, const void *q_bf16, int32_t
     const cuuint64_t kv_dims[2] = {128, H * R}, kv_str[1] = {256};
     const cuuint64_t kr_dims[2] = {64, R}, kr_str[1] = {128};
     const cuuint32_t k_box[2] = {64, 64};
-    if (!encode_bf16(&tw, w_ukv_bf16, 2, w_dims, w_str, w_box) || !encode_bf16(&tq_map, q_bf16, 3, q_dims, q_str, q_box) ||
-        !encode_bf16(&tkn, a.kn, 2, kv_dims, kv_str, k_box) || !encode_bf16(&tv, a.v, 2, kv_dims, kv_str, k_box) ||
-        !encode_bf16(&tkr, a.kr, 2, kr_dims, kr_str, k_box))
+    const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (!encode_16bit(&tw, BF, w_ukv_bf16, 2, w_dims, w_str, w_box) ||
+        !encode_16bit(&tq_map, BF, q_bf16, 3, q_dims, q_str, q_box) ||
+        !encode_16bit(&tkn, F16, a.kn, 2, kv_dims, kv_str, k_box) ||
+        !encode_16bit(&tv, F16, a.v, 2, kv_dims, kv_str, k_box) ||
+        !encode_16bit(&tkr, F16, a.kr, 2, kr_dims, kr_str, k_box))
         return fail(MLA_ERR_CUDA, "tensor map encoding failed");
     e = mla::launch_mha_up(a, reinterpret_cast<const int4 *>(ws + p.off_up), static_cast<int>(p.up.size()), tw, stream);
     if (e != cudaSuccess) return cuda_fail(e, "mha up-projection launch");

@@ -372,15 +372,12 @@ def sparse_reference_ds_torch(ps, q, kv_ds, sm_scale, idx, block=64):
 # ---------------------------------------------------------------------------
 # the non-absorbed (MHA) path
 # ---------------------------------------------------------------------------
-BF16_UNIT_ROUNDOFF = 2.0 ** -9
-
-
 def mha_reference_torch(ps, q, w, kv, ks, sm_scale, toks=None, q_block=256):
     """The non-absorbed path in plain PyTorch, fp32 (TF32 off), on the GPU, for
     every new token (or the global tokens `toks`): c_s = ks_s * dec(kv_s),
     k = [W_UK c ; r], v = W_UV c per head, causal softmax. Also returns the
     per-row bound on the move of the log-sum-exp when the kernel rounds each
-    key to bf16: u * sm_scale * max_s sum_d |q_d| |k_s[d]| (u = 2^-9).
+    key to f16: u * sm_scale * max_s sum_d |q_d| |k_s[d]| (u = 2^-11).
     q: bf16 [Tq, H, 192]; w: bf16 [H, 256, 512]. Returns (out [n, H, 128], lse
     [n, H], lse_bound [n, H]) in token order."""
     import torch
@@ -421,7 +418,7 @@ def mha_reference_torch(ps, q, w, kv, ks, sm_scale, toks=None, q_block=256):
                 lse[js] = l.t()
                 mag = torch.einsum("hnd,hsd->hns", qb.abs().double(), K.abs().double())
                 mag = mag.masked_fill(mask[None], 0.0)
-                bnd[js] = (BF16_UNIT_ROUNDOFF * sm_scale * mag.amax(dim=-1)).t()
+                bnd[js] = (F16_UNIT_ROUNDOFF * sm_scale * mag.amax(dim=-1)).t()
         return out, lse, bnd
     finally:
         torch.backends.cuda.matmul.allow_tf32 = prev
