@@ -668,7 +668,7 @@ def measure_ds_layout(name, dev, steps, warmup):
     outside the timed calls): per-call time of the attention alone and its
     roofline against the bf16 tensor peak (these kernels run kind::f16)."""
     import torch
-    from mla_prefill_attention_gb300 import (MLA_OP_DENSE, Seqs, inputs as I, mla_indexer_topk, mla_prefill_dense_ds,
+    from mla_prefill_attention_gb300 import (MLA_OP_DENSE_DS, Seqs, inputs as I, mla_indexer_topk, mla_prefill_dense_ds,
                                              mla_prefill_sparse_ds, mla_workspace_size)
     from mla_prefill_attention_gb300 import flops as F
     w = I.WORKLOADS[name]
@@ -684,7 +684,7 @@ def measure_ds_layout(name, dev, steps, warmup):
         flops = F.sparse_flops(w.q_lens, w.prefix_lens, w.heads, w.topk)
         call = lambda: mla_prefill_sparse_ds(seqs, q, kv, w.sm_scale, idx, out=out, lse=lse)
     else:
-        ws = torch.empty(max(16, mla_workspace_size(MLA_OP_DENSE, seqs, w.heads)), dtype=torch.uint8, device=dev)
+        ws = torch.empty(max(256, mla_workspace_size(MLA_OP_DENSE_DS, seqs, w.heads)), dtype=torch.uint8, device=dev)
         flops = F.dense_flops(w.q_lens, w.prefix_lens, w.heads)
         call = lambda: mla_prefill_dense_ds(seqs, q, kv, w.sm_scale, out=out, lse=lse, workspace=ws)
     for _ in range(warmup):
@@ -707,8 +707,8 @@ def measure_ds_layout(name, dev, steps, warmup):
            "unit": "tok/s", "attention_tflops": tf,
            "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16, "unit": "TFLOP/s", "frac": tf / bf16,
                         "peak_source": f"{src} bf16 sustained (kind::f16 MMAs)",
-                        "kernel": "attn_ds kernel: rows dequantised to f16 in shared memory, tcgen05 kind::f16, "
-                                  "64 rows x 80 keys"}}
+                        "kernel": "attn_ds kernel: dense rows converted once to f16 and loaded by TMA, sparse rows "
+                                  "gathered and converted in shared memory; tcgen05 kind::f16, 64 rows x 80 keys"}}
     del q, kv, out, lse
     torch.cuda.empty_cache()
     return obj

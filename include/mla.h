@@ -77,7 +77,8 @@ typedef enum {
     MLA_OP_INDEXER = 1,
     MLA_OP_SPARSE = 2,
     MLA_OP_DENSE_HOST = 3,  /* mla_prefill_dense_host, any chunk count */
-    MLA_OP_MHA = 4          /* mla_prefill_mha */
+    MLA_OP_MHA = 4,         /* mla_prefill_mha */
+    MLA_OP_DENSE_DS = 5     /* mla_prefill_dense_ds */
 } mla_op_t;
 
 /* Ragged batch of sequences over one paged cache (256-token pages). */
@@ -160,11 +161,14 @@ mla_status_t mla_prefill_sparse(const mla_seqs_t *seqs, const void *q_bf16, int3
 /* Dense causal MLA prefill on a cache of 656-byte rows kv_ds [num_blocks, 256,
  * 656]: what mla_prefill_dense computes, with K_s[d] = scales_s[d/128] *
  * dec(code_s[d]) for d < 512 and K_s[512+i] = the bf16 RoPE value i, V_s =
- * K_s[0:512]. The rows are dequantised to f16 in shared memory (relative to a
- * row's largest group scale, so the scale ratios and the RoPE values are
- * rounded once to 11 significant bits) and multiplied on the tensor cores in
- * f16 with fp32 accumulation. Arguments, workspace (mla_workspace_size(
- * MLA_OP_DENSE, ...)) and errors as mla_prefill_dense; kv_ds 16-byte aligned. */
+ * K_s[0:512]. Every key row the new tokens see is first dequantised once into
+ * an f16 row in the workspace (relative to the row's largest group scale, so
+ * the scale ratios and the RoPE values are rounded once to 11 significant
+ * bits), and the attention kernel multiplies those rows on the tensor cores in
+ * f16 with fp32 accumulation. workspace: mla_workspace_size(MLA_OP_DENSE_DS,
+ * ...) bytes, 256-byte aligned: the work list plus about 1,164 bytes per key
+ * row of every sequence's context (its f16 row and metadata). Arguments and
+ * errors otherwise as mla_prefill_dense; kv_ds 16-byte aligned. */
 mla_status_t mla_prefill_dense_ds(const mla_seqs_t *seqs, const void *q_bf16, int32_t num_heads,
                                   const uint8_t *kv_ds, float sm_scale, void *out_bf16, float *lse,
                                   void *workspace, size_t workspace_bytes, int32_t *dev_err, cudaStream_t stream);

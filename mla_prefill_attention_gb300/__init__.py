@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     MLA_DEVERR_BAD_PAGE,
     MLA_DEVERR_SEQ_MISMATCH,
     MLA_OP_DENSE,
+    MLA_OP_DENSE_DS,
     MLA_OP_DENSE_HOST,
     MLA_OP_INDEXER,
     MLA_OP_MHA,

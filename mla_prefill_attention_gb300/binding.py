@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libmla.so")
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_WORKSPACE = range(5)
 MLA_DEVERR_BAD_PAGE, MLA_DEVERR_BAD_INDEX, MLA_DEVERR_TIMEOUT, MLA_DEVERR_INTERNAL = 1, 2, 4, 8
 MLA_DEVERR_SEQ_MISMATCH = 16
-MLA_OP_DENSE, MLA_OP_INDEXER, MLA_OP_SPARSE, MLA_OP_DENSE_HOST, MLA_OP_MHA = 0, 1, 2, 3, 4
+MLA_OP_DENSE, MLA_OP_INDEXER, MLA_OP_SPARSE, MLA_OP_DENSE_HOST, MLA_OP_MHA, MLA_OP_DENSE_DS = 0, 1, 2, 3, 4, 5
 
 EXPORTS = ("mla_workspace_size", "mla_prefill_dense", "mla_indexer_topk", "mla_prefill_sparse", "mla_last_error",
            "mla_prefill_dense_static", "mla_kv_append", "mla_merge_attn", "mla_prefill_dense_host",
@@ -292,7 +292,7 @@ def mla_prefill_dense_ds(seqs: Seqs, q: torch.Tensor, kv_ds: torch.Tensor, sm_sc
         out = torch.empty((q.shape[0], H, 512), dtype=torch.bfloat16, device=q.device)
     if lse is None and want_lse:
         lse = torch.empty((q.shape[0], H), dtype=torch.float32, device=q.device)
-    ws, wsb = _workspace(MLA_OP_DENSE, seqs, H, 0, workspace)
+    ws, wsb = _workspace(MLA_OP_DENSE_DS, seqs, H, 0, workspace)
     c = seqs.c()
     _check(load().mla_prefill_dense_ds(ctypes.byref(c), _ptr(q), H, _ptr(kv_ds), float(sm_scale), _ptr(out),
                                        _ptr(lse), _ptr(ws), wsb, _ptr(dev_err), _stream()))

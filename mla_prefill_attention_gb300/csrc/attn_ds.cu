@@ -51,6 +51,15 @@
 // bytes and group scales of the next tile are fetched into registers while the
 // current one is converted), 7 MMA issue, 10-11 idle.
 //
+// Dense calls convert first: a conversion kernel writes every key row, once,
+// as the f16 K' row above into a workspace in sequence order (each sequence's
+// rows padded to whole 80-key tiles) together with each tile's key metadata;
+// the attention kernel then loads its slices by TMA (one producer thread, 10 KB
+// boxes straight into the ring) instead of converting each row in every CTA that
+// reads it (loads in registers were the bound: tensor pipe 45% busy, stalled on
+// their latency). Sparse calls gather rows by index and convert them in the
+// loader warps as described above.
+//
 // Tensor-core order: QK(t+1) is issued before PV(t), so the softmax of tile t
 // overlaps QK(t+1), and the ring lets the loaders fill tile t+2 while tiles t
 // and t+1 are in use. Every wait is bounded; a wait that runs out sets
@@ -115,6 +124,8 @@ struct __align__(16) KeyMeta {
     float4 sl[BN / 2];                   // 2^8 sigma of both keys, log2 sigma of both (-inf = masked)
     float2 isig[BN / 2];                 // 1/sigma of both
 };
+
+static_assert(sizeof(KeyMeta) == kDsMetaBytes && BN == kDsTileKeys, "converted key metadata layout");
 
 struct Shared {
     KeyMeta meta[4];                     // per key tile, ring of 4
@@ -364,8 +375,9 @@ __device__ __forceinline__ void load_q_tmem(const AttnArgs &a, const RowTile &rt
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <bool kSparse>
-__global__ void __launch_bounds__(NT, 1) attn_kernel(const AttnArgs a, const int4 *__restrict__ work) {
+template <bool kSparse, bool kConv>
+__global__ void __launch_bounds__(NT, 1) attn_kernel(const AttnArgs a, const int4 *__restrict__ work,
+                                                    const __grid_constant__ CUtensorMap tmap_k) {
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ Shared sh;
     const uint32_t raw = smem_u32(dsm);
@@ -408,7 +420,8 @@ __global__ void __launch_bounds__(NT, 1) attn_kernel(const AttnArgs a, const int
     if (tid == 0) {
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
-            if (i < B_FREE_PAIR || (i >= B_META && i < B_META + 4)) cnt = kLoaders;     // FULL_ROPE, FULL_PAIR, META
+            if (i < B_FREE_PAIR || (i >= B_META && i < B_META + 4))
+                cnt = kConv ? 1 : kLoaders;                                               // FULL_ROPE, FULL_PAIR, META
             if ((i >= B_S_FREE && i < B_S_FREE + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) || i == B_Q_FULL ||
                 i == B_O_FREE)
                 cnt = 4;                                                                  // softmax warps
@@ -427,7 +440,58 @@ __global__ void __launch_bounds__(NT, 1) attn_kernel(const AttnArgs a, const int
     const uint32_t tmem = sh.tmem_base;
     const Wait wait{&sh, a.dev_err};
 
-    if (is_loader(warp)) {
+    if (kConv && warp == 4) {
+        // =================== TMA producer (converted rows) ===================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_k);
+            const int64_t cb = __ldg(a.conv_base + b);            // converted row of the sequence's key 0
+            int armed_rope[2] = {-1, -1}, armed_meta[4] = {-1, -1, -1, -1}, armed_pair[kPairs];
+#pragma unroll
+            for (int p = 0; p < kPairs; ++p) armed_pair[p] = -1;
+            bool ok = true;
+            for (int t = 0; t < walk.total && ok; ++t) {
+                const int rb = t & 1, j = walk.j(t);
+                const int krow = static_cast<int>(cb + static_cast<int64_t>(j) * BN);
+                // RoPE slot rb: free once QK of tile t-2 is complete
+                if (t >= 2 && !(ok = wait(B_S_FULL + rb, ((t >> 1) - 1) & 1))) break;
+                const uint32_t fr = smem_u32(&sh.bar[B_FULL_ROPE + rb]);
+                mbar_expect_tx(fr, kSlot);
+                tma_load_2d(sbase_a + kOffRope + rb * kSlot, &tmap_k, kDv, krow, fr);
+                armed_rope[rb] = (t >> 1) & 1;
+                // nope pairs; pair c of tile t uses slot pair (4t + c) mod 9
+                for (int c = 0; c < 4; ++c) {
+                    const int qn = 4 * t + c, p = qn % kPairs;
+                    if (qn >= kPairs && !(ok = wait(B_FREE_PAIR + p, ((qn / kPairs) - 1) & 1))) break;
+                    if (c == 0) {   // the tile's metadata (its ring slot was last read by the softmax of tile t-4)
+                        const uint32_t fm = smem_u32(&sh.bar[B_META + (t & 3)]);
+                        mbar_expect_tx(fm, static_cast<uint32_t>(sizeof(KeyMeta)));
+                        bulk_load(smem_u32(&sh.meta[t & 3]),
+                                  a.kmeta + (cb / BN + j) * static_cast<int64_t>(sizeof(KeyMeta)),
+                                  static_cast<uint32_t>(sizeof(KeyMeta)), fm);
+                        armed_meta[t & 3] = (t >> 2) & 1;
+                    }
+                    const uint32_t fp = smem_u32(&sh.bar[B_FULL_PAIR + p]);
+                    mbar_expect_tx(fp, 2 * kSlot);
+                    tma_load_2d(sbase_a + (2 * p) * kSlot, &tmap_k, 128 * c, krow, fp);
+                    tma_load_2d(sbase_a + (2 * p + 1) * kSlot, &tmap_k, 128 * c + 64, krow, fp);
+                    armed_pair[p] = (qn / kPairs) & 1;
+                }
+            }
+            // drain: the last copy into every slot has landed
+            bool drained = true;
+            for (int i = 0; i < 2; ++i)
+                if (armed_rope[i] >= 0)
+                    drained = mbar_wait_cycles(smem_u32(&sh.bar[B_FULL_ROPE + i]), armed_rope[i], kWaitCycles) && drained;
+            for (int i = 0; i < 4; ++i)
+                if (armed_meta[i] >= 0)
+                    drained = mbar_wait_cycles(smem_u32(&sh.bar[B_META + i]), armed_meta[i], kWaitCycles) && drained;
+            for (int i = 0; i < kPairs; ++i)
+                if (armed_pair[i] >= 0)
+                    drained = mbar_wait_cycles(smem_u32(&sh.bar[B_FULL_PAIR + i]), armed_pair[i], kWaitCycles) && drained;
+            if (!drained) set_dev_err(a.dev_err, MLA_DEVERR_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (!kConv && is_loader(warp)) {
         // =================== loaders ===================
         // Loader warp w covers keys 16w..16w+15 of a tile as two groups of 8;
         // lane l holds 16-byte chunk l%4 of one 64-dim slice row of key
@@ -821,23 +885,90 @@ __global__ void __launch_bounds__(NT, 1) attn_kernel(const AttnArgs a, const int
     }
 }
 
+// ---------------------------------------------------------------------------
+// conversion of the dense keys: one thread per (converted row, 16-dim chunk);
+// chunks 0..31 hold the latent codes, 32..35 the RoPE dims; chunk 0 also writes
+// the row's entry of its tile's key metadata. The arithmetic is the loaders'
+// (store_codes, store_rope, write_meta), so the f16 rows are the same bits.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) convert_kernel(const AttnArgs a, int64_t n_rows) {
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t row = gid / 36;
+    const int ch = static_cast<int>(gid % 36);
+    if (row >= n_rows) return;
+    int lo = 0, hi = a.batch - 1;          // the sequence: the last b with conv_base[b] <= row
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(a.conv_base + mid) <= row) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int64_t pos = row - __ldg(a.conv_base + b);
+    int64_t crow = -1;
+    if (pos < __ldg(a.conv_ctx + b))
+        crow = cache_row(a.block_table + static_cast<int64_t>(b) * a.max_blocks, a.max_blocks, a.num_blocks, pos,
+                         a.dev_err);
+    const GroupRatios gr = group_ratios(row_scales(a, crow));
+    uint32_t h[8];
+    if (ch < 32) {
+        const uint4 r = crow >= 0 ? __ldg(reinterpret_cast<const uint4 *>(a.kv + crow * kRow) + ch)
+                                  : make_uint4(0, 0, 0, 0);
+        h[0] = f16x2_of_e4m3x2(__byte_perm(r.x, 0u, 0x4140u));
+        h[1] = f16x2_of_e4m3x2(__byte_perm(r.x, 0u, 0x4342u));
+        h[2] = f16x2_of_e4m3x2(__byte_perm(r.y, 0u, 0x4140u));
+        h[3] = f16x2_of_e4m3x2(__byte_perm(r.y, 0u, 0x4342u));
+        h[4] = f16x2_of_e4m3x2(__byte_perm(r.z, 0u, 0x4140u));
+        h[5] = f16x2_of_e4m3x2(__byte_perm(r.z, 0u, 0x4342u));
+        h[6] = f16x2_of_e4m3x2(__byte_perm(r.w, 0u, 0x4140u));
+        h[7] = f16x2_of_e4m3x2(__byte_perm(r.w, 0u, 0x4342u));
+        const uint32_t ratio = gr.h[ch >> 3];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) h[u] = hmul2_bits(h[u], ratio);
+    } else {
+        const int i = ch - 32;
+        uint4 r[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if (crow >= 0) {
+            r[0] = __ldg(reinterpret_cast<const uint4 *>(a.kv + crow * kRow + kOffRopeBytes + 32 * i));
+            r[1] = __ldg(reinterpret_cast<const uint4 *>(a.kv + crow * kRow + kOffRopeBytes + 32 * i) + 1);
+        }
+        const float scale = (1.f / kCodeScale) / gr.sig;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const __nv_bfloat162 *bb = reinterpret_cast<const __nv_bfloat162 *>(&r[u]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(bb[e]);
+                h[4 * u + e] = pack_half2(f.x * scale, f.y * scale);
+            }
+        }
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(a.kconv + row * kDqk) + 2 * ch;
+    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    if (ch == 0) write_meta(reinterpret_cast<KeyMeta *>(a.kmeta)[row / BN], static_cast<int>(row % BN), crow, gr.sig);
+}
+
 }  // namespace dsattn
 
-cudaError_t launch_dense_ds(const AttnArgs &a, const int4 *work, int n_work, cudaStream_t st) {
-    cudaError_t e =
-        cudaFuncSetAttribute(dsattn::attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dsattn::kDynSmem);
+cudaError_t launch_dense_ds(const AttnArgs &a, const int4 *work, int n_work, int64_t n_conv_rows,
+                            const CUtensorMap &tmap_conv, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(dsattn::attn_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         dsattn::kDynSmem);
     if (e != cudaSuccess) return e;
-    if (n_work > 0) dsattn::attn_kernel<false><<<n_work, dsattn::NT, dsattn::kDynSmem, st>>>(a, work);
+    if (n_work <= 0) return cudaSuccess;
+    const int64_t threads = n_conv_rows * 36;
+    dsattn::convert_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(a, n_conv_rows);
+    dsattn::attn_kernel<false, true><<<n_work, dsattn::NT, dsattn::kDynSmem, st>>>(a, work, tmap_conv);
     return cudaGetLastError();
 }
 
 cudaError_t launch_sparse_ds(const AttnArgs &a, cudaStream_t st) {
     const int64_t n_tokens = a.tok_end - a.tok_begin;
     cudaError_t e =
-        cudaFuncSetAttribute(dsattn::attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dsattn::kDynSmem);
+        cudaFuncSetAttribute(dsattn::attn_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dsattn::kDynSmem);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(n_tokens), (a.H + dsattn::BM - 1) / dsattn::BM);
-    if (n_tokens > 0) dsattn::attn_kernel<true><<<grid, dsattn::NT, dsattn::kDynSmem, st>>>(a, nullptr);
+    CUtensorMap unused{};
+    if (n_tokens > 0) dsattn::attn_kernel<true, false><<<grid, dsattn::NT, dsattn::kDynSmem, st>>>(a, nullptr, unused);
     return cudaGetLastError();
 }
 

@@ -28,6 +28,12 @@ struct AttnArgs {
     int64_t tok_begin, tok_end;  // sparse: the new tokens this launch attends for (global indices)
     int64_t total_q;             // new tokens by the host mirror of cu_seqlens: no row at or past total_q * H
                                  // is read or written whatever the device copy says
+    // dense calls on 656-byte rows: the converted keys (f16 [rows][576], each
+    // sequence's rows from conv_base[b], padded to 80-key tiles) and their tile metadata
+    __half *kconv;
+    uint8_t *kmeta;
+    const int32_t *conv_base;    // [batch], converted row of each sequence's key 0
+    const int32_t *conv_ctx;     // [batch], keys each sequence has (prefix + new)
 };
 
 // Dense attention on e4m3 operands (kind::f8f6f4). Work item: x = sequence,
@@ -40,9 +46,15 @@ bool encode_kv_tmap(CUtensorMap *map, const uint8_t *kv, int32_t num_blocks);
 cudaError_t launch_sparse_f8(const AttnArgs &a, cudaStream_t st);
 
 // The same two on a cache of 656-byte rows (512 e4m3 latent codes, four fp32
-// group scales, 64 bf16 RoPE values; a.kv_scale unused): rows dequantised to f16
-// in shared memory, tcgen05 kind::f16, 64 query rows x 80 keys per tile.
-cudaError_t launch_dense_ds(const AttnArgs &a, const int4 *work, int n_work, cudaStream_t st);
+// group scales, 64 bf16 RoPE values; a.kv_scale unused): tcgen05 kind::f16, 64
+// query rows x 80 keys per tile. Dense: the rows are first converted to f16
+// (a.kconv, a.kmeta; n_conv_rows rows) and loaded by TMA through tmap_conv
+// ([rows][576] f16, 64 x 80 boxes, 128-byte swizzle); sparse: gathered and
+// converted in shared memory.
+constexpr int kDsTileKeys = 80;
+constexpr int kDsMetaBytes = 960;     // one key tile's metadata
+cudaError_t launch_dense_ds(const AttnArgs &a, const int4 *work, int n_work, int64_t n_conv_rows,
+                            const CUtensorMap &tmap_conv, cudaStream_t st);
 cudaError_t launch_sparse_ds(const AttnArgs &a, cudaStream_t st);
 
 // Non-absorbed (MHA) path: per-head keys [W_UK c ; r] (192 dims) and values

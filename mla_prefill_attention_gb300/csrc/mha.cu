@@ -26,7 +26,9 @@
 //    rounding of the keys alone moved logits by ~1e-3 and outputs by up to
 //    2.5e-2 of a row's RMS); the values must stay inside the f16 range.
 //
-// 2. Attention, one CTA per 128 new tokens of a sequence and one head; the
+// 2. Attention, one CTA per 128 new tokens of a sequence and one head (the
+//    grid head-major: every tile of head 0 in longest-first order, then head 1,
+//    ...; a head's keys and values, 0.5 KB a row, stay in L2 while its tiles run); the
 //    bf16 query tile is converted to f16 in shared memory once (values below
 //    2^-14 lose bits, so a query must lie inside the f16 range):
 //      S  = Q K^T        M = 128 tokens, N = 64 keys, K = 192 (3 x 64-dim
@@ -263,6 +265,43 @@ __global__ void __launch_bounds__(UP_NT, 1)
 // ===========================================================================
 // 2. attention
 // ===========================================================================
+// paired f32 arithmetic (two IEEE operations per instruction) and a three-input max
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t pk2u(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 upk2(uint64_t v) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+    return f;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 constexpr int AT_BM = 128;                    // query tokens per CTA
 constexpr int AT_BN = 64;                     // keys per tile
 constexpr int AT_ST = 3;                      // K/V ring stages
@@ -295,8 +334,10 @@ __global__ void __launch_bounds__(AT_NT, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // work item: {b, first new token in the sequence, its global index, valid rows},
-    //            {prefix, key-row base, key tiles, -}
-    const int item = blockIdx.x / a.H, h = blockIdx.x % a.H;
+    //            {prefix, key-row base, key tiles, -}; the grid runs head-major, so
+    //            the CTAs in flight share one head's keys and values in L2
+    const int n_items = static_cast<int>(gridDim.x) / a.H;
+    const int item = blockIdx.x % n_items, h = blockIdx.x / n_items;
     const int4 w0 = work[2 * item], w1 = work[2 * item + 1];
     const int i0 = w0.y, n_valid = w0.w, P = w1.x, n_tiles = w1.z;
     const int64_t t0 = w0.z, kb = w1.y;
@@ -399,7 +440,7 @@ __global__ void __launch_bounds__(AT_NT, 1)
         const int r = 32 * warp + lane;
         const int64_t pos = static_cast<int64_t>(P) + i0 + r;      // the row's position in its sequence
         const uint32_t lane_addr = static_cast<uint32_t>(32 * warp) << 16;
-        const float scale = a.sm_scale_log2;
+        const uint64_t scale2 = pk2(a.sm_scale_log2, a.sm_scale_log2);
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         uint8_t *prow = sbase + kOffP + (r >> 3) * 1024 + (r & 7) * 16;
@@ -439,14 +480,26 @@ __global__ void __launch_bounds__(AT_NT, 1)
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bar[A_S_FREE + sb]));
-            // logits in log2 units; keys past the row's position are masked
+            // logits in log2 units, two per paired multiply; keys past the row's position
+            // are masked (only tiles that reach past it need the compare)
             const int64_t k0 = static_cast<int64_t>(AT_BN) * t;
-            float u[64];
+            uint64_t u2[32];
             float mx = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                u[j] = (k0 + j <= pos) ? __uint_as_float(sv[j]) * scale : -INFINITY;
-                mx = fmaxf(mx, u[j]);
+            for (int k = 0; k < 32; ++k) u2[k] = mul2(pk2u(sv[2 * k], sv[2 * k + 1]), scale2);
+            if (k0 + AT_BN - 1 > pos) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    float2 f = upk2(u2[k]);
+                    if (k0 + 2 * k > pos) f.x = -INFINITY;
+                    if (k0 + 2 * k + 1 > pos) f.y = -INFINITY;
+                    u2[k] = pk2(f.x, f.y);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const float2 f = upk2(u2[k]);
+                mx = max3(mx, f.x, f.y);
             }
             if (t == 0) {
                 m = mx;
@@ -476,14 +529,20 @@ __global__ void __launch_bounds__(AT_NT, 1)
             }
             // P = 2^(u - m): fp32 into l, f16 into the P buffer of this tile
             uint32_t pw[32];
-            float ls = 0.f;
+            uint64_t ls2 = 0;
+            const uint64_t m2 = pk2(m, m);
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-                const float p0 = fast_exp2(u[2 * k] - m), p1 = fast_exp2(u[2 * k + 1] - m);
-                ls += p0 + p1;
+                const float2 d = upk2(sub2(u2[k], m2));
+                const float p0 = fast_exp2(d.x), p1 = fast_exp2(d.y);
+                const uint64_t pp = pk2(p0, p1);
+                ls2 = k == 0 ? pp : add2(ls2, pp);
                 pw[k] = pack_half2(p0, p1);
             }
-            l += ls;
+            {
+                const float2 f = upk2(ls2);
+                l += f.x + f.y;
+            }
             if (t >= 2) {       // PV(t-2) has read the buffer
                 ok = __all_sync(0xffffffffu, wait_bar(&bar[A_PV_DONE + sb], ((t >> 1) - 1) & 1, a.dev_err));
                 if (!ok) break;

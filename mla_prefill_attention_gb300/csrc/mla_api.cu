@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstring>
 #include <string>
 #include <vector>
 
@@ -136,13 +137,6 @@ size_t dense_host_items_bound(const mla_seqs_t *s, int32_t H) {
         tiles += static_cast<size_t>((rows + kBM - 1) / kBM);
     }
     return tiles / 2 + static_cast<size_t>(s->batch) + MLA_DENSE_HOST_MAX_CHUNKS + 1;
-}
-
-int64_t max_context(const mla_seqs_t *s) {
-    int64_t m = 0;
-    for (int b = 0; b < s->batch; ++b)
-        m = std::max<int64_t>(m, s->prefix_lens_host[b] + s->cu_seqlens_q_host[b + 1] - s->cu_seqlens_q_host[b]);
-    return m;
 }
 
 // Work items of the indexer: (sequence, first token, token count, 0) for every
@@ -280,6 +274,35 @@ MhaPlan mha_plan(const mla_seqs_t *s, int32_t H) {
     return p;
 }
 
+// Dense calls on 656-byte rows: each sequence with new tokens gets its keys
+// converted to f16 rows from conv_base[b] (its context padded to whole 80-key
+// tiles). Workspace: work list | conv_base, conv_ctx | f16 rows | tile metadata.
+struct DsPlan {
+    std::vector<int4> work;
+    std::vector<int32_t> base, ctx;
+    int64_t rows = 0;
+    size_t off_ints = 0, off_rows = 0, off_meta = 0, bytes = 0;
+};
+DsPlan ds_plan(const mla_seqs_t *s, int32_t H) {
+    DsPlan p;
+    p.work = dense_schedule(s, H);
+    p.base.assign(static_cast<size_t>(s->batch), 0);
+    p.ctx.assign(static_cast<size_t>(s->batch), 0);
+    for (int b = 0; b < s->batch; ++b) {
+        const int64_t q = s->cu_seqlens_q_host[b + 1] - s->cu_seqlens_q_host[b];
+        p.base[b] = static_cast<int32_t>(p.rows);
+        if (q <= 0) continue;
+        const int64_t ctx = s->prefix_lens_host[b] + q;
+        p.ctx[b] = static_cast<int32_t>(ctx);
+        p.rows += (ctx + mla::kDsTileKeys - 1) / mla::kDsTileKeys * mla::kDsTileKeys;
+    }
+    p.off_ints = round_up(p.work.size() * sizeof(int4), kWsAlign);
+    p.off_rows = p.off_ints + round_up(2 * static_cast<size_t>(s->batch) * sizeof(int32_t), kWsAlign);
+    p.off_meta = p.off_rows + round_up(static_cast<size_t>(p.rows) * 576 * 2, kWsAlign);
+    p.bytes = p.off_meta + round_up(static_cast<size_t>(p.rows / mla::kDsTileKeys) * mla::kDsMetaBytes, kWsAlign);
+    return p;
+}
+
 mla::AttnArgs attn_args(const mla_seqs_t *s, const void *q, int32_t H, const uint8_t *kv, const float *kv_scale,
                         float sm_scale, void *out, float *lse, int32_t *dev_err) {
     mla::AttnArgs a{};
@@ -336,6 +359,9 @@ size_t mla_workspace_size(mla_op_t op, const mla_seqs_t *seqs, int32_t num_heads
         case MLA_OP_MHA:
             if (!heads_ok(num_heads)) return 0;
             return mha_plan(seqs, num_heads).bytes;
+        case MLA_OP_DENSE_DS:
+            if (!heads_ok(num_heads)) return 0;
+            return ds_plan(seqs, num_heads).bytes;
     }
     return 0;
 }
@@ -725,17 +751,32 @@ mla_status_t mla_prefill_dense_ds(const mla_seqs_t *seqs, const void *q_bf16, in
     // the row format carries its own scales: any 4-byte-aligned stand-in passes the scale check
     if ((st = check_attn_ptrs(q_bf16, kv_ds, reinterpret_cast<const float *>(kv_ds), out_bf16, lse, sm_scale)) != MLA_OK)
         return st;
-    const std::vector<int4> work = dense_schedule(seqs, num_heads);
-    const size_t need = round_up(work.size() * sizeof(int4), kWsAlign);
-    if (work.empty()) return MLA_OK;
-    if (!workspace || workspace_bytes < need || !aligned(workspace, 16))
-        return fail(MLA_ERR_WORKSPACE, "dense needs %zu workspace bytes (16-byte aligned), got %zu", need,
-                    workspace ? workspace_bytes : 0);
-    if (static_cast<int64_t>(work.size()) > INT32_MAX) return fail(MLA_ERR_UNSUPPORTED, "too many tiles");
-    cudaError_t e = cudaMemcpyAsync(workspace, work.data(), work.size() * sizeof(int4), cudaMemcpyHostToDevice, stream);
+    const DsPlan p = ds_plan(seqs, num_heads);
+    if (p.work.empty()) return MLA_OK;
+    if (!workspace || workspace_bytes < p.bytes || !aligned(workspace, kWsAlign))
+        return fail(MLA_ERR_WORKSPACE, "dense (656-byte rows) needs %zu workspace bytes (256-byte aligned), got %zu",
+                    p.bytes, workspace ? workspace_bytes : 0);
+    if (static_cast<int64_t>(p.work.size()) > INT32_MAX || p.rows > INT32_MAX / 36)
+        return fail(MLA_ERR_UNSUPPORTED, "too many tiles");
+    char *ws = static_cast<char *>(workspace);
+    std::vector<char> head(p.off_rows, 0);
+    std::memcpy(head.data(), p.work.data(), p.work.size() * sizeof(int4));
+    std::memcpy(head.data() + p.off_ints, p.base.data(), p.base.size() * sizeof(int32_t));
+    std::memcpy(head.data() + p.off_ints + p.base.size() * sizeof(int32_t), p.ctx.data(), p.ctx.size() * sizeof(int32_t));
+    cudaError_t e = cudaMemcpyAsync(ws, head.data(), head.size(), cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e, "schedule upload");
     mla::AttnArgs a = attn_args(seqs, q_bf16, num_heads, kv_ds, nullptr, sm_scale, out_bf16, lse, dev_err);
-    e = mla::launch_dense_ds(a, static_cast<const int4 *>(workspace), static_cast<int>(work.size()), stream);
+    a.conv_base = reinterpret_cast<const int32_t *>(ws + p.off_ints);
+    a.conv_ctx = a.conv_base + seqs->batch;
+    a.kconv = reinterpret_cast<__half *>(ws + p.off_rows);
+    a.kmeta = reinterpret_cast<uint8_t *>(ws + p.off_meta);
+    CUtensorMap tmap;
+    const cuuint64_t dims[2] = {576, static_cast<cuuint64_t>(p.rows)}, strides[1] = {1152};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(mla::kDsTileKeys)};
+    if (!encode_16bit(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.kconv, 2, dims, strides, box))
+        return fail(MLA_ERR_CUDA, "tensor map encoding failed");
+    e = mla::launch_dense_ds(a, reinterpret_cast<const int4 *>(ws), static_cast<int>(p.work.size()), p.rows, tmap,
+                             stream);
     if (e != cudaSuccess) return cuda_fail(e, "dense launch");
     return MLA_OK;
 }
@@ -780,7 +821,23 @@ mla_status_t mla_prefill_mha(const mla_seqs_t *seqs, const void *q_bf16, int32_t
     a.out = static_cast<__nv_bfloat16 *>(out_bf16);
     a.lse = lse;
     a.H = num_heads;
-    a.up_heads = std::min(num_heads, 8);
+    // heads per up-projection CTA: the fewest waves of CTAs times the work of one,
+    // counting the decode of a CTA's 128 rows as two heads' worth
+    {
+        int sms = 148;
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int64_t n_up = static_cast<int64_t>(p.up.size());
+        int64_t best = -1;
+        for (int g = 8; g <= num_heads; g *= 2) {
+            const int64_t ctas = n_up * (num_heads / g), waves = (ctas + sms - 1) / sms;
+            const int64_t cost = waves * (g + 2);
+            if (best < 0 || cost < best) {
+                best = cost;
+                a.up_heads = g;
+            }
+        }
+    }
     a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
     a.dev_err = dev_err;
 
