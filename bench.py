@@ -639,9 +639,10 @@ def roofline_of(run, per_ms):
     return tflops, roof
 
 
-def measure_workload(name, dev, steps, warmup):
+def measure_workload(name, dev, steps, warmup, e2e=False):
     """One workload timed on its own (W warm-up steps, then K), for the extra
-    objects of the default line: per-step time, throughput and rooflines."""
+    objects of the default line: per-step time, throughput and rooflines; with
+    e2e, also the same step host to host (the run's e2e method)."""
     import torch
     from mla_prefill_attention_gb300 import inputs as I
     w = I.WORKLOADS[name]
@@ -651,6 +652,13 @@ def measure_workload(name, dev, steps, warmup):
     obj = {"workload": name, "steps": steps, "warmup": warmup, "ms_per_step": total_ms / steps,
            "value": run.tokens * steps / (total_ms / 1000.0), "unit": "tok/s", "attention_tflops": tflops,
            "roofline": roof, "config": config_of(w)}
+    if e2e:
+        r = run.e2e(steps, warmup)
+        if r is not None:
+            ms, h2d, d2h = r
+            obj["e2e"] = {"value": run.tokens / (ms / 1000.0), "unit": "tok/s", "ms_per_step": ms,
+                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                          "pieces": getattr(run, "e2e_pieces", None)}
     if isinstance(run, ChunkedRun):
         obj["chunks"] = {"count": len(run.bounds), "chunk_tokens": w.chunk,
                          "ms_per_chunk_last_step": [round(x, 3) for x in run.chunk_ms],
@@ -932,7 +940,8 @@ def main():
             if name == w.name:
                 continue
             k = 2 if name == "chunked200k" else min(args.steps, 5)
-            extras[name] = measure_workload(name, dev, k, max(3, min(args.warmup, 3)))
+            extras[name] = measure_workload(name, dev, k, max(3, min(args.warmup, 3)),
+                                            e2e=(name == "sparse64k" and not args.no_e2e))
         for name in ("dense32k", "sparse64k"):
             extras[name + "_656B"] = measure_ds_layout(name, dev, min(args.steps, 5), 3)
         extras["mha_short"] = measure_mha("mha_short", dev, min(args.steps, 10), 3)
