@@ -244,3 +244,24 @@ def test_mha_rejects_bad_arguments_and_sizes_its_workspace(lib):
     assert mha(ws=FAKE, wsb=want - 1) == B.MLA_ERR_WORKSPACE
     assert mha(ws=ctypes.c_void_p(0x100010), wsb=want) == B.MLA_ERR_WORKSPACE      # not 256-byte aligned
     assert mha(seqs=HostSeqs([0, 0], [5, 0])) == B.MLA_OK                         # no new tokens: no launch
+
+
+def test_dense_ds_workspace_holds_the_converted_rows(lib):
+    """Dense calls on 656-byte rows convert every context row once: the workspace
+    holds the work list, the per-sequence bases and lengths, 1,152 bytes of f16
+    per row (contexts padded to 80-key tiles) and 960 bytes of metadata per tile."""
+    s = HostSeqs([100, 0, 37], [500, 9, 0])
+    H = 64
+    rnd = lambda x: -(-x // 256) * 256
+    tiles = [(100 * H + 63) // 64, (37 * H + 63) // 64]
+    items = sum((t + 1) // 2 for t in tiles)
+    rows = 640 + 80                        # contexts 600 and 37 padded to 80; the empty sequence adds none
+    want = rnd(items * 16) + rnd(2 * 3 * 4) + rnd(rows * 1152) + rnd(rows // 80 * 960)
+    assert lib.mla_workspace_size(B.MLA_OP_DENSE_DS, ctypes.byref(s.c), H, 0) == want
+
+    def dds(ws=None, wsb=0):
+        return lib.mla_prefill_dense_ds(ctypes.byref(s.c), FAKE, H, FAKE, 0.07, FAKE, None, ws, wsb, None, None)
+
+    assert dds() == B.MLA_ERR_WORKSPACE
+    assert dds(FAKE, want - 1) == B.MLA_ERR_WORKSPACE
+    assert dds(ctypes.c_void_p(0x100010), want) == B.MLA_ERR_WORKSPACE        # not 256-byte aligned
