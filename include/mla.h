@@ -191,9 +191,10 @@ mla_status_t mla_prefill_sparse_ds(const mla_seqs_t *seqs, const void *q_bf16, i
  * w_ukv_bf16: [H, 256, 512], rows 0..127 of head h are W_UK_h and rows
  * 128..255 W_UV_h (k[s,h][i] = sum_d W_UK_h[i][d] c_s[d]); out_bf16: [Tq, H,
  * 128]; lse: [Tq, H] or NULL. The keys and values of every sequence's whole
- * context are first up-projected into the workspace as bf16 (k and v rows of
+ * context are first up-projected into the workspace as f16 (k and v rows of
  * 256 bytes per head, 128 bytes of RoPE dims per row; each context padded to
- * 128 rows), then attended. Any prompt length works; the workspace grows with
+ * 128 rows), then attended with the queries converted to f16 and P in f16 (so
+ * every value must lie inside the f16 range). Any prompt length works; the workspace grows with
  * the context times the heads, which is why the path suits short prompts.
  * num_heads in {16, 32, 64, 128}; q, w_ukv, out and kv 16-byte aligned.
  * workspace: mla_workspace_size(MLA_OP_MHA, ...) bytes, 256-byte aligned.
