@@ -427,9 +427,9 @@ RUNS = {"tiny512": DenseRun, "prefix12k": DenseRun, "dense32k": DenseRun, "ragge
 # command line for that workload. A kernel change invalidates its entry: set it to
 # None until it is captured again.
 TRAFFIC = {
-    "dense32k": {"attention": 2453488384 + 2118204416},
-    "sparse64k": {"indexer_topk": 76523008 + 26764032,      # the fast-path launch (profiles/indexer_topk_sparse64k.md)
-                  "sparse_attention": 807216896 + 533257472},
+    "dense32k": {"attention": 2455451904 + 2118966016},
+    "sparse64k": {"indexer_topk": 75921408 + 25915904,        # the fast-path launch
+                  "sparse_attention": 805456128 + 531233536},
 }
 
 
