@@ -99,7 +99,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # Pieces the host-to-host dense call cuts the new tokens into (copies of one
 # piece overlap the attention of the others).
-E2E_PIECES = 16
+E2E_PIECES = 32
 SPARSE_E2E_PIECES = 8
 
 def host_dense(w):
