@@ -153,3 +153,38 @@ def test_sparse64k_ds_sampled_and_every_row():
                     lse_extra=ds_lse_bound(pb.ps, d["q"], d["kv"], pb.sm_scale, toks, idx))
     ref, ref_lse = sparse_reference_ds_torch(pb.ps, d["q"], d["kv"], pb.sm_scale, idx)
     check_attention_torch(out, ref, None, None, "sparse64k ds, every row")
+
+
+def test_dense_ds_page_shuffle_and_repeat_are_bit_identical():
+    """The converted rows are laid out by position, so where the pages sit in the
+    cache cannot change a bit of the result; nor can a second call."""
+    import torch
+    a = DsProblem([150, 300], [20, 0], 32, seed=631)
+    ps_b = I.make_seqs([150, 300], [20, 0], 631, shuffle=True, extra_blocks=9)
+    assert not np.array_equal(a.ps.block_table, ps_b.block_table)
+    kv_b = I.gen_latent_cache_ds(631, ps_b)
+    from mla_prefill_attention_gb300 import Seqs
+    da = a.device()
+    db = dict(da, seqs=Seqs.from_paged(ps_b), kv=torch.from_numpy(kv_b).cuda())
+    oa, la = run_dense(a, da)
+    ob, lb = run_dense(a, db)
+    oa2, la2 = run_dense(a, da)
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
+    assert torch.equal(oa, oa2) and torch.equal(la, la2)
+
+
+def test_dense_ds_bad_page_sets_device_flag():
+    """A block-table entry outside [0, num_blocks) is reported by the conversion
+    (its rows become zero keys) and the kernels do not fault."""
+    import torch
+    from mla_prefill_attention_gb300 import MLA_DEVERR_BAD_PAGE, Seqs, mla_prefill_dense_ds
+    pb = DsProblem([40], [300], 16, seed=632)
+    bt = pb.ps.block_table.copy()
+    bt[0, 0] = pb.ps.num_blocks + 5
+    d = pb.device()
+    seqs = Seqs(pb.ps.cu_seqlens_q, pb.ps.prefix_lens, bt, pb.ps.num_blocks)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, _ = mla_prefill_dense_ds(seqs, d["q"], d["kv"], pb.sm_scale, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & MLA_DEVERR_BAD_PAGE
+    assert bool(torch.isfinite(out.float()).all())

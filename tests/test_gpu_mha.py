@@ -117,3 +117,16 @@ def test_mha_bad_page_sets_device_flag():
     out, lse = run_mha(pb, d, err=err)
     assert int(err.item()) & MLA_DEVERR_BAD_PAGE
     assert bool(torch.isfinite(out.float()).all())
+
+
+def test_mha_long_prompt_with_prefix_sampled_and_every_row():
+    """The path takes any length: 4,200 new tokens after a 1,000-token prefix
+    (contexts past the top-k, tiles of up to 81 key tiles), 64 heads; sampled
+    rows against the fp64 oracle, every row against the fp32 reference."""
+    pb = MhaProblem([4200], [1000], 64, seed=45)
+    d = pb.device()
+    out, lse = run_mha(pb, d)
+    toks = sample_rows(pb.ps.cu_seqlens_q, seed=6, n_uniform=48, edge=8, chunks=8)
+    check_vs_oracle(pb, d, out, lse, toks, "mha 4200 after 1000 sampled")
+    ref, ref_lse, bnd = mha_reference_torch(pb.ps, d["q"], d["w"], d["kv"], d["ks"], pb.sm_scale)
+    check_attention_torch(out, ref, lse, ref_lse, "mha 4200 after 1000, every row", lse_extra=bnd)
