@@ -81,7 +81,7 @@ struct MhaArgs {
 };
 // Up-projection: work item = {sequence, first position (a multiple of 128),
 // key-row base of those rows, context length}; tmap_w: w_ukv as [H*256 rows][512]
-// bf16, 64 x 256 boxes, 128-byte swizzle.
+// bf16, 64 x 128 boxes (a half head's rows), 128-byte swizzle.
 cudaError_t launch_mha_up(const MhaArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_w, cudaStream_t st);
 // Attention: work item = two int4, {sequence, first new token in it, that
 // token's global index, valid rows <= 128} and {prefix, key-row base, key tiles

@@ -13,11 +13,11 @@
 //
 // 1. Up-projection, one CTA per 128 cached rows of a sequence and a group of
 //    heads: 256 threads decode the rows' e4m3 codes into bf16 (exact: an e4m3
-//    value has 4 significant bits) in shared memory, in the 128-byte-swizzled
-//    K-major layout (8 slices of 64 latent dims); the tensor core multiplies
-//    them by each head's [256 x 512] slice of w_ukv (TMA, 64-dim boxes through
-//    a 3-stage ring): D[row][n] = sum_d dec(c)[row][d] W[h][n][d], M = 128
-//    rows, N = 256 (k then v), K = 512, into one of two TMEM accumulators;
+//    value has 4 significant bits) straight into TMEM, the MMA's A operand; the
+//    tensor core multiplies them by each half head's [128 x 512] slice of w_ukv
+//    (TMA, 64-dim boxes through a 12-stage ring): D[row][n] = sum_d
+//    dec(c)[row][d] W[h][n][d], M = 128 rows, N = 128 (the k rows, then the v
+//    rows), K = 512, into one of two TMEM accumulators;
 //    four epilogue warps (thread = row) scale by sigma_row and write f16 k and
 //    v rows head-major, [H][R][128]. The first head group also writes the
 //    RoPE dims, f16(sigma * dec(c)), as [R][64]. Rows past the context are
@@ -79,18 +79,21 @@ __device__ __forceinline__ uint32_t bf16x2_of_e4m3x2(uint16_t two) {
 // ===========================================================================
 constexpr int UP_ROWS = 128;
 constexpr int UP_NT = 320;                       // warps 0-7 decode; then 0-3 epilogue, 8 producer, 9 issuer
-constexpr int UP_WST = 3;                        // weight ring stages
-constexpr int kUpSlice = UP_ROWS * 128;          // one 64-dim slice of the decoded rows: 16 KB
-constexpr int kUpA = 8 * kUpSlice;               // 128 KB
-constexpr int kUpW = 256 * 128;                  // one 64-dim slice of one head's 256 weight rows: 32 KB
-constexpr int kUpOffW = kUpA;
-constexpr int kUpOffSig = kUpOffW + UP_WST * kUpW;
+constexpr int UP_WST = 12;                       // weight ring stages
+constexpr int kUpW = 128 * 128;                  // one 64-dim slice of 128 weight rows (a head's k or v part): 16 KB
+constexpr int kUpOffSig = UP_WST * kUpW;
 constexpr int kUpSmem = 1024 + kUpOffSig + UP_ROWS * 4;
+constexpr uint32_t kUpColA = 0, kUpColD = 256;   // TMEM: decoded rows (512 bf16 = 256 columns), two 128-column D
 static_assert(kUpSmem <= 232448 - 256, "shared memory");
 
 enum UpBar { U_W_FULL = 0, U_W_EMPTY = U_W_FULL + UP_WST, U_D_FULL = U_W_EMPTY + UP_WST, U_D_FREE = U_D_FULL + 2,
              U_FINAL = U_D_FREE + 2, U_NBAR };
 
+// The decoded rows stay in TMEM as the A operand (lane = row, column c = latent
+// dims 2c, 2c+1), so shared memory holds only the weight ring: twelve 16 KB
+// slices in flight keep the tensor core fed across the round trip from L2. One
+// unit of work is half a head (its 128 k rows or its 128 v rows): M = 128 rows,
+// N = 128, K = 512, into one of two 128-column accumulators.
 __global__ void __launch_bounds__(UP_NT, 1)
     up_kernel(const MhaArgs a, const int4 *__restrict__ work, const __grid_constant__ CUtensorMap tmap_w) {
     extern __shared__ __align__(1024) uint8_t dsm[];
@@ -107,7 +110,7 @@ __global__ void __launch_bounds__(UP_NT, 1)
     const int hg = blockIdx.x % n_hg;
     const int b = it.x, pos0 = it.y, ctx = it.w;
     const int64_t row0 = it.z;
-    const int h0 = hg * a.up_heads, nh = a.up_heads;
+    const int h0 = hg * a.up_heads, n_units = 2 * a.up_heads;
     float *sig = reinterpret_cast<float *>(sbase + kUpOffSig);
 
     if (tid == 0) {
@@ -119,10 +122,15 @@ __global__ void __launch_bounds__(UP_NT, 1)
         tmem_relinquish();
     }
     if (warp == 8 && lane == 0) tma_prefetch_desc(&tmap_w);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_slot;
 
-    // ----- decode: thread (row r, half) takes latent dims 256*half .. +255 -----
+    // ----- decode into TMEM: warp w holds rows 32(w&3)..+31 (its lane quadrant)
+    // and latent dims 256(w>>2)..+255 (TMEM columns 128(w>>2)..+127) -----
     if (warp < 8) {
-        const int r = tid >> 1, half = tid & 1;
+        const int q = warp & 3, half = warp >> 2, r = 32 * q + lane;
         const int pos = pos0 + r;
         int64_t cr = -1;
         if (pos < ctx) cr = cache_row(a.block_table + static_cast<int64_t>(b) * a.max_blocks, a.max_blocks,
@@ -130,22 +138,23 @@ __global__ void __launch_bounds__(UP_NT, 1)
         const float s = cr >= 0 ? __ldg(a.kv_scale + cr) : 0.f;
         if (half == 0) sig[r] = s;
         const uint8_t *src = a.kv + (cr >= 0 ? cr : 0) * kDqk;
-#pragma unroll 4
-        for (int c = 0; c < 16; ++c) {
-            const int d0 = 256 * half + 16 * c;
-            uint4 raw16 = make_uint4(0u, 0u, 0u, 0u);
-            if (cr >= 0) raw16 = __ldg(reinterpret_cast<const uint4 *>(src + d0));
-            const uint32_t wv[4] = {raw16.x, raw16.y, raw16.z, raw16.w};
-            uint32_t o[8];
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + kUpColA + 128u * half;
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {                  // 64 latent dims = 32 TMEM columns per group
+            uint32_t o[32];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                o[2 * k] = bf16x2_of_e4m3x2(static_cast<uint16_t>(wv[k] & 0xFFFFu));
-                o[2 * k + 1] = bf16x2_of_e4m3x2(static_cast<uint16_t>(wv[k] >> 16));
+            for (int c = 0; c < 4; ++c) {
+                const int d0 = 256 * half + 64 * g + 16 * c;
+                uint4 raw16 = make_uint4(0u, 0u, 0u, 0u);
+                if (cr >= 0) raw16 = __ldg(reinterpret_cast<const uint4 *>(src + d0));
+                const uint32_t wv[4] = {raw16.x, raw16.y, raw16.z, raw16.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    o[8 * c + 2 * k] = bf16x2_of_e4m3x2(static_cast<uint16_t>(wv[k] & 0xFFFFu));
+                    o[8 * c + 2 * k + 1] = bf16x2_of_e4m3x2(static_cast<uint16_t>(wv[k] >> 16));
+                }
             }
-            const int ch = (d0 & 63) >> 3;
-            uint8_t *rowp = sbase + (d0 >> 6) * kUpSlice + r * 128;
-            *reinterpret_cast<uint4 *>(rowp + ((ch ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4 *>(rowp + (((ch + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            tmem_st32(taddr + 32u * g, o);
         }
         if (hg == 0) {      // the shared RoPE dims: 32 per thread
             uint4 rr[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
@@ -155,8 +164,8 @@ __global__ void __launch_bounds__(UP_NT, 1)
             }
             uint32_t o[16];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const uint32_t wv[4] = {rr[q].x, rr[q].y, rr[q].z, rr[q].w};
+            for (int qq = 0; qq < 2; ++qq) {
+                const uint32_t wv[4] = {rr[qq].x, rr[qq].y, rr[qq].z, rr[qq].w};
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
 #pragma unroll
@@ -164,30 +173,30 @@ __global__ void __launch_bounds__(UP_NT, 1)
                         const uint16_t two = static_cast<uint16_t>(wv[k] >> (16 * e));
                         const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
                         const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
-                        o[8 * q + 2 * k + e] = pack_half2(s * f.x, s * f.y);
+                        o[8 * qq + 2 * k + e] = pack_half2(s * f.x, s * f.y);
                     }
             }
             uint4 *dst = reinterpret_cast<uint4 *>(a.kr + (row0 + r) * kDr + 32 * half);
 #pragma unroll
             for (int k = 0; k < 4; ++k) dst[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
         }
-        fence_proxy_async();
+        tmem_st_wait();
     }
+    fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    const uint32_t tmem = tmem_slot;
 
     if (warp == 8) {
-        // =================== TMA producer: each head's weight slices ===================
+        // =================== TMA producer: each half head's weight slices ===================
         if (lane == 0) {
             int n = 0;
             bool ok = true;
-            for (int hh = 0; hh < nh && ok; ++hh)
+            for (int u = 0; u < n_units && ok; ++u)
                 for (int s = 0; s < 8 && ok; ++s, ++n) {
                     const int st = n % UP_WST;
                     if (n >= UP_WST && !(ok = wait_bar(&bar[U_W_EMPTY + st], ((n / UP_WST) - 1) & 1, a.dev_err))) break;
                     mbar_expect_tx(smem_u32(&bar[U_W_FULL + st]), kUpW);
-                    tma_load_2d(sbase_a + kUpOffW + st * kUpW, &tmap_w, 64 * s, (h0 + hh) * 256,
+                    tma_load_2d(sbase_a + st * kUpW, &tmap_w, 64 * s, (h0 + (u >> 1)) * 256 + 128 * (u & 1),
                                 smem_u32(&bar[U_W_FULL + st]));
                 }
             // drain: the last load of every stage has landed before the CTA exits
@@ -198,25 +207,23 @@ __global__ void __launch_bounds__(UP_NT, 1)
     } else if (warp == 9) {
         // =================== MMA issuer ===================
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16(128, 256, true, true, false, false);
-            const uint64_t da0 = sdesc(sbase_a, 16, 1024, kSw128);
-            const uint64_t dw0 = sdesc(sbase_a + kUpOffW, 16, 1024, kSw128);
+            const uint32_t idesc = idesc_f16(128, 128, true, true, false, false);
+            const uint64_t dw0 = sdesc(sbase_a, 16, 1024, kSw128);
             int n = 0;
             bool ok = true;
-            for (int hh = 0; hh < nh && ok; ++hh) {
-                const int db = hh & 1;
-                if (hh >= 2 && !(ok = wait_bar(&bar[U_D_FREE + db], ((hh >> 1) - 1) & 1, a.dev_err))) break;
+            for (int u = 0; u < n_units && ok; ++u) {
+                const int db = u & 1;
+                if (u >= 2 && !(ok = wait_bar(&bar[U_D_FREE + db], ((u >> 1) - 1) & 1, a.dev_err))) break;
                 fence_after_sync();
-                const uint32_t d = tmem + 256u * db;
+                const uint32_t d = tmem + kUpColD + 128u * db;
                 for (int s = 0; s < 8; ++s, ++n) {
                     const int st = n % UP_WST;
                     if (!(ok = wait_bar(&bar[U_W_FULL + st], (n / UP_WST) & 1, a.dev_err))) break;
                     fence_after_sync();
-                    const uint64_t da = da0 + static_cast<uint64_t>((s * kUpSlice) >> 4);
                     const uint64_t dw = dw0 + static_cast<uint64_t>((st * kUpW) >> 4);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_f16_ss_w(d, da + 2 * ks, dw + 2 * ks, idesc, (s | ks) ? 1u : 0u, 1u);
+                        mma_f16_ts_w(d, tmem + kUpColA + 32u * s + 8u * ks, dw + 2 * ks, idesc, (s | ks) ? 1u : 0u, 1u);
                     mma_commit(smem_u32(&bar[U_W_EMPTY + st]));
                 }
                 if (ok) mma_commit(smem_u32(&bar[U_D_FULL + db]));
@@ -228,23 +235,22 @@ __global__ void __launch_bounds__(UP_NT, 1)
         const int r = 32 * warp + lane;
         const float s = sig[r];
         const uint32_t lane_addr = static_cast<uint32_t>(32 * warp) << 16;
-        for (int hh = 0; hh < nh; ++hh) {
-            const int db = hh & 1, h = h0 + hh;
-            const bool got = wait_bar(&bar[U_D_FULL + db], (hh >> 1) & 1, a.dev_err);
+        for (int u = 0; u < n_units; ++u) {
+            const int db = u & 1, h = h0 + (u >> 1);
+            const bool got = wait_bar(&bar[U_D_FULL + db], (u >> 1) & 1, a.dev_err);
             if (!__all_sync(0xffffffffu, got)) break;
             fence_after_sync();
-            const int64_t krow = (static_cast<int64_t>(h) * a.R + row0 + r) * kDvh;
+            __half *base = ((u & 1) ? a.v : a.kn) + (static_cast<int64_t>(h) * a.R + row0 + r) * kDvh;
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
-                tmem_ld32(tmem + lane_addr + 256u * db + 32u * c, v);
+                tmem_ld32(tmem + lane_addr + kUpColD + 128u * db + 32u * c, v);
                 tmem_ld_wait();
                 uint32_t o[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k)
                     o[k] = pack_half2(s * __uint_as_float(v[2 * k]), s * __uint_as_float(v[2 * k + 1]));
-                __half *base = (c < 4 ? a.kn : a.v) + krow + 32 * (c & 3);
-                uint4 *dst = reinterpret_cast<uint4 *>(base);
+                uint4 *dst = reinterpret_cast<uint4 *>(base + 32 * c);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) dst[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
             }

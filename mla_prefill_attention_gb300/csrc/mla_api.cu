@@ -844,7 +844,7 @@ mla_status_t mla_prefill_mha(const mla_seqs_t *seqs, const void *q_bf16, int32_t
     const cuuint64_t H = static_cast<cuuint64_t>(num_heads), R = static_cast<cuuint64_t>(p.R);
     CUtensorMap tw, tq_map, tkn, tkr, tv;
     const cuuint64_t w_dims[2] = {512, H * 256}, w_str[1] = {1024};
-    const cuuint32_t w_box[2] = {64, 256};
+    const cuuint32_t w_box[2] = {64, 128};
     const cuuint64_t q_dims[3] = {192, H, static_cast<cuuint64_t>(tq)}, q_str[2] = {384, H * 384};
     const cuuint32_t q_box[3] = {64, 1, 128};
     const cuuint64_t kv_dims[2] = {128, H * R}, kv_str[1] = {256};
