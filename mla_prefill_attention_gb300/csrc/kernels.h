@@ -78,6 +78,7 @@ struct MhaArgs {
     int32_t up_heads;            // heads per up-projection CTA (divides H)
     float sm_scale_log2;
     int32_t *dev_err;
+    int64_t total_q;             // new tokens (rows of q) by the host mirror of cu_seqlens
 };
 // Up-projection: work item = {sequence, first position (a multiple of 128),
 // key-row base of those rows, context length}; tmap_w: w_ukv as [H*256 rows][512]
@@ -85,12 +86,11 @@ struct MhaArgs {
 cudaError_t launch_mha_up(const MhaArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_w, cudaStream_t st);
 // Attention: work item = two int4, {sequence, first new token in it, that
 // token's global index, valid rows <= 128} and {prefix, key-row base, key tiles
-// of 64, 0}; one CTA per item and head. tmap_q: q as [Tq][H][192] bf16, boxes
-// of 64 dims x 1 head x 128 tokens; tmap_kn / tmap_v: f16 [H*R rows][128], 64 x
-// 64 boxes; tmap_kr: f16 [R][64], 64 x 64 boxes; all with the 128-byte swizzle.
-cudaError_t launch_mha_attn(const MhaArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_q,
-                            const CUtensorMap &tmap_kn, const CUtensorMap &tmap_kr, const CUtensorMap &tmap_v,
-                            cudaStream_t st);
+// of 64, 0}; one CTA per item and head (q is read row by row into TMEM).
+// tmap_kn / tmap_v: f16 [H*R rows][128], 64 x 64 boxes; tmap_kr: f16 [R][64],
+// 64 x 64 boxes; all with the 128-byte swizzle.
+cudaError_t launch_mha_attn(const MhaArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_kn,
+                            const CUtensorMap &tmap_kr, const CUtensorMap &tmap_v, cudaStream_t st);
 
 struct IndexerArgs {
     const uint8_t *qi;           // [Tq, 64, 128] e4m3

@@ -28,11 +28,13 @@
 //
 // 2. Attention, one CTA per 128 new tokens of a sequence and one head (the
 //    grid head-major: every tile of head 0 in longest-first order, then head 1,
-//    ...; a head's keys and values, 0.5 KB a row, stay in L2 while its tiles run); the
-//    bf16 query tile is converted to f16 in shared memory once (values below
-//    2^-14 lose bits, so a query must lie inside the f16 range):
-//      S  = Q K^T        M = 128 tokens, N = 64 keys, K = 192 (3 x 64-dim
-//                        slices: two no-RoPE, one RoPE); S in one of two TMEM
+//    ...; a head's keys and values, 0.5 KB a row, stay in L2 while its tiles run).
+//    Each softmax thread reads its bf16 query row, converts it to f16 (values
+//    below 2^-14 lose bits, so a query must lie inside the f16 range) and stores
+//    it into TMEM, where the QK MMAs take their A operand; shared memory then
+//    holds four K/V stages:
+//      S  = Q K^T        M = 128 tokens, N = 64 keys, K = 192 (Q from TMEM; K in
+//                        3 x 64-dim slices: two no-RoPE, one RoPE); S in one of two TMEM
 //                        buffers so QK(t+1) runs during the softmax of tile t
 //      P  = 2^(S*sm_scale*log2e - m)   in registers (a thread per query row),
 //                        rounded to f16 into shared memory
@@ -310,25 +312,25 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 
 constexpr int AT_BM = 128;                    // query tokens per CTA
 constexpr int AT_BN = 64;                     // keys per tile
-constexpr int AT_ST = 3;                      // K/V ring stages
+constexpr int AT_ST = 4;                      // K/V ring stages
 constexpr int AT_NT = 192;
-constexpr int kQSlice = AT_BM * 128;          // 128 tokens x 64 dims bf16: 16 KB
 constexpr int kKSlice = AT_BN * 128;          // 64 keys x 64 dims bf16: 8 KB
 constexpr int kStage = 5 * kKSlice;           // no-RoPE 0, no-RoPE 1, RoPE, V 0, V 1
-constexpr int kOffKV = 3 * kQSlice;
+constexpr int kOffKV = 0;                     // the query tile lives in TMEM
 constexpr int kOffP = kOffKV + AT_ST * kStage;
 constexpr int kPBuf = AT_BM * AT_BN * 2;      // 16 KB
 constexpr int kAtSmem = 1024 + kOffP + 2 * kPBuf;
 constexpr float kRescale = 8.f;               // log2 units
+constexpr uint32_t kColQ = 256;               // TMEM: S buffers 0..127, O 128..255, Q 256..351
+constexpr uint32_t kAtTmemCols = 512;         // allocated and released as one (a power of two >= 352)
 static_assert(kAtSmem <= 232448 - 256, "shared memory");
 
-enum AtBar { A_Q_FULL = 0, A_Q_F16, A_KV_FULL, A_KV_EMPTY = A_KV_FULL + AT_ST, A_S_FULL = A_KV_EMPTY + AT_ST,
+enum AtBar { A_Q_F16 = 0, A_KV_FULL, A_KV_EMPTY = A_KV_FULL + AT_ST, A_S_FULL = A_KV_EMPTY + AT_ST,
              A_S_FREE = A_S_FULL + 2, A_P_FULL = A_S_FREE + 2, A_PV_DONE = A_P_FULL + 2, A_FINAL = A_PV_DONE + 2,
              A_NBAR };
 
 __global__ void __launch_bounds__(AT_NT, 1)
-    attn_kernel(const MhaArgs a, const int4 *__restrict__ work, const __grid_constant__ CUtensorMap tmap_q,
-                const __grid_constant__ CUtensorMap tmap_kn, const __grid_constant__ CUtensorMap tmap_kr,
+    attn_kernel(const MhaArgs a, const int4 *__restrict__ work, const __grid_constant__ CUtensorMap tmap_kn, const __grid_constant__ CUtensorMap tmap_kr,
                 const __grid_constant__ CUtensorMap tmap_v) {
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ uint64_t bar[A_NBAR];
@@ -357,11 +359,10 @@ __global__ void __launch_bounds__(AT_NT, 1)
         mbar_fence_init();
     }
     if (warp == 5) {
-        tmem_alloc(smem_u32(&tmem_slot), 256);
+        tmem_alloc(smem_u32(&tmem_slot), kAtTmemCols);
         tmem_relinquish();
     }
     if (warp == 4 && lane == 0) {
-        tma_prefetch_desc(&tmap_q);
         tma_prefetch_desc(&tmap_kn);
         tma_prefetch_desc(&tmap_kr);
         tma_prefetch_desc(&tmap_v);
@@ -373,9 +374,6 @@ __global__ void __launch_bounds__(AT_NT, 1)
     if (warp == 4) {
         // =================== TMA producer ===================
         if (lane == 0) {
-            mbar_expect_tx(smem_u32(&bar[A_Q_FULL]), 3 * kQSlice);
-            for (int s = 0; s < 3; ++s)
-                tma_load_3d(sbase_a + s * kQSlice, &tmap_q, 64 * s, h, static_cast<int>(t0), smem_u32(&bar[A_Q_FULL]));
             const int krow0 = static_cast<int>(static_cast<int64_t>(h) * a.R + kb);
             int t = 0;
             for (; t < n_tiles; ++t) {
@@ -389,8 +387,7 @@ __global__ void __launch_bounds__(AT_NT, 1)
                 tma_load_2d(sb + 3 * kKSlice, &tmap_v, 0, krow0 + AT_BN * t, fb);
                 tma_load_2d(sb + 4 * kKSlice, &tmap_v, 64, krow0 + AT_BN * t, fb);
             }
-            // drain: the query tile and the last load of every stage have landed
-            if (!mbar_wait_cycles(smem_u32(&bar[A_Q_FULL]), 0, kWaitCycles)) set_dev_err(a.dev_err, MLA_DEVERR_TIMEOUT);
+            // drain: the last load of every stage has landed
             for (int j = (t > AT_ST ? t - AT_ST : 0); j < t; ++j)
                 if (!mbar_wait_cycles(smem_u32(&bar[A_KV_FULL + j % AT_ST]), (j / AT_ST) & 1, kWaitCycles))
                     set_dev_err(a.dev_err, MLA_DEVERR_TIMEOUT);
@@ -400,7 +397,6 @@ __global__ void __launch_bounds__(AT_NT, 1)
         if (lane == 0) {
             const uint32_t id_qk = idesc_f16(AT_BM, AT_BN, false, false, false, false);
             const uint32_t id_pv = idesc_f16(AT_BM, 128, false, false, false, true);
-            const uint64_t dq0 = sdesc(sbase_a, 16, 1024, kSw128);
             const uint64_t dk0 = sdesc(sbase_a + kOffKV, 16, 1024, kSw128);
             const uint64_t dv0 = sdesc(sbase_a + kOffKV + 3 * kKSlice, kKSlice, 1024, kSw128);
             const uint64_t dp0 = sdesc(sbase_a + kOffP, 128, 1024, kSwNone);
@@ -412,10 +408,10 @@ __global__ void __launch_bounds__(AT_NT, 1)
                 const uint32_t d = tmem + static_cast<uint32_t>(AT_BN * sb);
 #pragma unroll
                 for (int s = 0; s < 3; ++s) {
-                    const uint64_t da = dq0 + static_cast<uint64_t>((s * kQSlice) >> 4);
                     const uint64_t db = dk0 + static_cast<uint64_t>((st * kStage + s * kKSlice) >> 4);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) mma_f16_ss_w(d, da + 2 * ks, db + 2 * ks, id_qk, (s | ks) ? 1u : 0u, 1u);
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16_ts_w(d, tmem + kColQ + 32u * s + 8u * ks, db + 2 * ks, id_qk, (s | ks) ? 1u : 0u, 1u);
                 }
                 mma_commit(smem_u32(&bar[A_S_FULL + sb]));
                 return true;
@@ -450,26 +446,29 @@ __global__ void __launch_bounds__(AT_NT, 1)
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         uint8_t *prow = sbase + kOffP + (r >> 3) * 1024 + (r & 7) * 16;
-        // the query row to f16, in place (the swizzle moves whole 16-byte chunks, so
-        // each thread's row stays its own 3 x 128 bytes)
-        ok = n_tiles > 0 && __all_sync(0xffffffffu, wait_bar(&bar[A_Q_FULL], 0, a.dev_err));
+        // the query row, converted to f16, into TMEM (lane = row, column c = dims
+        // 2c, 2c+1): the QK MMAs read it from there
+        ok = n_tiles > 0;
         if (ok) {
-#pragma unroll
-            for (int s = 0; s < 3; ++s) {
-                uint4 *row = reinterpret_cast<uint4 *>(sbase + s * kQSlice + r * 128);
+            const bool have = t0 + r < a.total_q;
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((have ? t0 + r : 0) * a.H + h) * 192);
+#pragma unroll 1
+            for (int g = 0; g < 3; ++g) {                 // 64 dims = 32 TMEM columns per group
+                uint32_t o[32];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    uint4 x = row[c];
-                    uint32_t *wv = reinterpret_cast<uint32_t *>(&x);
+                    const uint4 x = have ? __ldg(src + 8 * g + c) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wv[k]));
-                        wv[k] = pack_half2(f.x, f.y);
+                        o[4 * c + k] = pack_half2(f.x, f.y);
                     }
-                    row[c] = x;
                 }
+                tmem_st32(tmem + lane_addr + kColQ + 32u * g, o);
             }
-            fence_proxy_async();
+            tmem_st_wait();
+            fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bar[A_Q_F16]));
         }
@@ -595,7 +594,7 @@ __global__ void __launch_bounds__(AT_NT, 1)
     if (warp == 5) {
         if (!mbar_wait_cycles(smem_u32(&bar[A_FINAL]), 0, kWaitCycles)) set_dev_err(a.dev_err, MLA_DEVERR_TIMEOUT);
         fence_after_sync();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, kAtTmemCols);
     }
 }
 
@@ -609,14 +608,13 @@ cudaError_t launch_mha_up(const MhaArgs &a, const int4 *work, int n_work, const 
     return cudaGetLastError();
 }
 
-cudaError_t launch_mha_attn(const MhaArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_q,
-                            const CUtensorMap &tmap_kn, const CUtensorMap &tmap_kr, const CUtensorMap &tmap_v,
+cudaError_t launch_mha_attn(const MhaArgs &a, const int4 *work, int n_work, const CUtensorMap &tmap_kn, const CUtensorMap &tmap_kr, const CUtensorMap &tmap_v,
                             cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(mha::attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mha::kAtSmem);
     if (e != cudaSuccess) return e;
     const int64_t n_cta = static_cast<int64_t>(n_work) * a.H;
     if (n_cta > 0)
-        mha::attn_kernel<<<static_cast<unsigned>(n_cta), mha::AT_NT, mha::kAtSmem, st>>>(a, work, tmap_q, tmap_kn,
+        mha::attn_kernel<<<static_cast<unsigned>(n_cta), mha::AT_NT, mha::kAtSmem, st>>>(a, work, tmap_kn,
                                                                                       tmap_kr, tmap_v);
     return cudaGetLastError();
 }

@@ -840,27 +840,25 @@ mla_status_t mla_prefill_mha(const mla_seqs_t *seqs, const void *q_bf16, int32_t
     }
     a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
     a.dev_err = dev_err;
+    a.total_q = tq;
 
     const cuuint64_t H = static_cast<cuuint64_t>(num_heads), R = static_cast<cuuint64_t>(p.R);
-    CUtensorMap tw, tq_map, tkn, tkr, tv;
+    CUtensorMap tw, tkn, tkr, tv;
     const cuuint64_t w_dims[2] = {512, H * 256}, w_str[1] = {1024};
     const cuuint32_t w_box[2] = {64, 128};
-    const cuuint64_t q_dims[3] = {192, H, static_cast<cuuint64_t>(tq)}, q_str[2] = {384, H * 384};
-    const cuuint32_t q_box[3] = {64, 1, 128};
     const cuuint64_t kv_dims[2] = {128, H * R}, kv_str[1] = {256};
     const cuuint64_t kr_dims[2] = {64, R}, kr_str[1] = {128};
     const cuuint32_t k_box[2] = {64, 64};
     const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (!encode_16bit(&tw, BF, w_ukv_bf16, 2, w_dims, w_str, w_box) ||
-        !encode_16bit(&tq_map, BF, q_bf16, 3, q_dims, q_str, q_box) ||
         !encode_16bit(&tkn, F16, a.kn, 2, kv_dims, kv_str, k_box) ||
         !encode_16bit(&tv, F16, a.v, 2, kv_dims, kv_str, k_box) ||
         !encode_16bit(&tkr, F16, a.kr, 2, kr_dims, kr_str, k_box))
         return fail(MLA_ERR_CUDA, "tensor map encoding failed");
     e = mla::launch_mha_up(a, reinterpret_cast<const int4 *>(ws + p.off_up), static_cast<int>(p.up.size()), tw, stream);
     if (e != cudaSuccess) return cuda_fail(e, "mha up-projection launch");
-    e = mla::launch_mha_attn(a, reinterpret_cast<const int4 *>(ws + p.off_at), static_cast<int>(p.at.size() / 2), tq_map,
-                             tkn, tkr, tv, stream);
+    e = mla::launch_mha_attn(a, reinterpret_cast<const int4 *>(ws + p.off_at), static_cast<int>(p.at.size() / 2), tkn,
+                             tkr, tv, stream);
     if (e != cudaSuccess) return cuda_fail(e, "mha attention launch");
     return MLA_OK;
 }
