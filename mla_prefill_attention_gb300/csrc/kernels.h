@@ -79,6 +79,8 @@ struct MhaArgs {
     float sm_scale_log2;
     int32_t *dev_err;
     int64_t total_q;             // new tokens (rows of q) by the host mirror of cu_seqlens
+    int32_t ahead;               // attention: CTA blockIdx.x + ahead is the one expected to follow
+                                 // on the same SM (the SM count; set by the launcher)
 };
 // Up-projection: work item = {sequence, first position (a multiple of 128),
 // key-row base of those rows, context length}; tmap_w: w_ukv as [H*256 rows][512]

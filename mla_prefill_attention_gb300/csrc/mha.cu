@@ -447,17 +447,32 @@ __global__ void __launch_bounds__(AT_NT, 1)
         bool ok = true;
         uint8_t *prow = sbase + kOffP + (r >> 3) * 1024 + (r & 7) * 16;
         // the query row, converted to f16, into TMEM (lane = row, column c = dims
-        // 2c, 2c+1): the QK MMAs read it from there
+        // 2c, 2c+1): the QK MMAs read it from there. All 24 loads of the row go out
+        // at once (one memory round trip); then each thread asks L2 for its row of the
+        // CTA expected to follow on this SM, so that one finds its queries in L2.
         ok = n_tiles > 0;
         if (ok) {
             const bool have = t0 + r < a.total_q;
             const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((have ? t0 + r : 0) * a.H + h) * 192);
-#pragma unroll 1
+            uint4 xq[24];
+#pragma unroll
+            for (int c = 0; c < 24; ++c) xq[c] = have ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+            const int64_t nxt = static_cast<int64_t>(blockIdx.x) + a.ahead;
+            if (a.ahead > 0 && nxt < gridDim.x) {
+                const int item_n = static_cast<int>(nxt % n_items), h_n = static_cast<int>(nxt / n_items);
+                const int4 wn = work[2 * item_n];
+                if (r < wn.w && static_cast<int64_t>(wn.z) + r < a.total_q) {
+                    const char *row = reinterpret_cast<const char *>(a.q + ((wn.z + r) * static_cast<int64_t>(a.H) + h_n) * 192);
+#pragma unroll
+                    for (int k = 0; k < 3; ++k) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(row + 128 * k));
+                }
+            }
+#pragma unroll
             for (int g = 0; g < 3; ++g) {                 // 64 dims = 32 TMEM columns per group
                 uint32_t o[32];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const uint4 x = have ? __ldg(src + 8 * g + c) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 x = xq[8 * g + c];
                     const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -571,11 +586,13 @@ __global__ void __launch_bounds__(AT_NT, 1)
             const float inv = 1.f / l;
             const bool live = r < n_valid;
             __nv_bfloat16 *orow = a.out + ((t0 + r) * a.H + h) * kDvh;
-#pragma unroll 1
+            uint32_t ob[4][32];   // the row's 128 columns of O in one round trip
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + 128u + 32u * c, ob[c]);
+            tmem_ld_wait();
+#pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_addr + 128u + 32u * c, o);
-                tmem_ld_wait();
+                const uint32_t *o = ob[c];
                 if (live) {
                     uint32_t w[16];
 #pragma unroll
@@ -612,9 +629,16 @@ cudaError_t launch_mha_attn(const MhaArgs &a, const int4 *work, int n_work, cons
                             cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(mha::attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mha::kAtSmem);
     if (e != cudaSuccess) return e;
+    // one CTA per SM at a time (all of TMEM): the CTA that follows on an SM is about
+    // an SM count further on in the grid
+    int dev = 0, n_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    MhaArgs b = a;
+    b.ahead = n_sm;
     const int64_t n_cta = static_cast<int64_t>(n_work) * a.H;
     if (n_cta > 0)
-        mha::attn_kernel<<<static_cast<unsigned>(n_cta), mha::AT_NT, mha::kAtSmem, st>>>(a, work, tmap_kn,
+        mha::attn_kernel<<<static_cast<unsigned>(n_cta), mha::AT_NT, mha::kAtSmem, st>>>(b, work, tmap_kn,
                                                                                       tmap_kr, tmap_v);
     return cudaGetLastError();
 }
